@@ -1,0 +1,408 @@
+/*
+ * lrkv_oracle.c -- plain fp64 CPU oracle for attention over an LRKV-compressed
+ * KV cache.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg load this library.  It shares no code, header, table or
+ * helper with the CUDA library; the two only ever see the same input bits.
+ *
+ * What it computes (source: "Low-Rank Key Value Attention", O'Neill, Clancy,
+ * Matskevichus, Reid, arXiv:2601.11471v3, as presented in the slide deck
+ * "Low-Rank Key Value Attention: shared projections, specialized heads"):
+ *
+ *   Eqs. (2)-(3), frame "LRKV constrains differences between heads":
+ *       W_h^{K,V} = W_shared^{K,V} + U_h^{K,V} (B_h^{K,V})^T,
+ *       W_shared in R^{d x d_h}, U_h in R^{d x r}, B_h in R^{d_h x r}.
+ *   Eqs. (4)-(5), frame "Cache shared features and compact per-head latents":
+ *       K_s = X W_shared^K, V_s = X W_shared^V (L x d_h),
+ *       R_h^K = X U_h^K,   R_h^V = X U_h^V   (L x r),
+ *       implied full features K_h = K_s + R_h^K (B_h^K)^T, V_h likewise.
+ *   Frame "Compute logits without expanding historical keys":
+ *       a_h = softmax(q_h K_h^T / sqrt(d_h) + causal mask).
+ *   Frame "Aggregate values before the residual up-projection", Eq. (7):
+ *       o_h = a_h V_h  (= a_h V_s + (a_h R_h^V)(B_h^V)^T).
+ *
+ * The oracle deliberately takes the EXPANDED road: it forms W_h (or K_h, V_h)
+ * explicitly and runs textbook softmax attention.  The factored road of
+ * Eqs. (6)-(7) is what the GPU takes; the slides state the two are equal for
+ * the linear model (frame "Training learns the base and residuals together",
+ * block "Two different notions of equivalence").
+ *
+ * Readings where the pages leave a step open:
+ *   - no position encoding and no normalisation inside attention;
+ *   - decode: the query attends to all seq_len cached tokens (it is the newest
+ *     position and is already in the cache); prefill: query at absolute
+ *     position p attends to keys j <= p;
+ *   - softmax scale 1/sqrt(d_h) unless the caller passes another;
+ *   - cache values are produced by an fp64 sum, rounded to fp32 (nearest) and
+ *     then to bf16 (nearest, ties to even).
+ *
+ * Everything is fp64; bf16 inputs are widened exactly.  Parallelism is plain
+ * OpenMP over independent (sequence, head) pairs or token rows; no blocking,
+ * fusion or reordering of any sum.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef LRKV_ORACLE_MUTANT
+#define LRKV_ORACLE_MUTANT 0 /* planted-mistake builds used by the pin tests */
+#endif
+
+/* ---------------------------------------------------------------- scalars */
+
+static double bf(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* fp32 -> bf16, round to nearest with ties to even on the 16 dropped bits. */
+static uint16_t f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40u); /* quiet NaN */
+    uint32_t keep_lsb = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7fffu + keep_lsb) >> 16);
+}
+
+/* fp64 value -> fp32 (round to nearest) -> bf16 (round to nearest even). */
+uint16_t oracle_round_to_cache(double v) { return f32_to_bf16((float)v); }
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------- softmax */
+
+/* Textbook softmax: p_t = exp(l_t - max) / sum_u exp(l_u - max). */
+void oracle_softmax(int n, const double* logits, double* p) {
+    if (n <= 0) return;
+    double m = logits[0];
+    for (int t = 1; t < n; ++t) if (logits[t] > m) m = logits[t];
+    double s = 0.0;
+    for (int t = 0; t < n; ++t) { p[t] = exp(logits[t] - m); s += p[t]; }
+    for (int t = 0; t < n; ++t) p[t] /= s;
+}
+
+/* Single-head attention over explicit keys and values:
+ *   out = softmax(q K^T * scale) V,  K, V: [L][d_h] row-major. */
+void oracle_attend(int L, int d_h, const double* q, const double* K, const double* V,
+                   double scale, double* out) {
+    for (int i = 0; i < d_h; ++i) out[i] = 0.0;
+    if (L <= 0) return;
+    double* logits = (double*)malloc(sizeof(double) * (size_t)L);
+    double* p = (double*)malloc(sizeof(double) * (size_t)L);
+    for (int t = 0; t < L; ++t) {
+        double acc = 0.0;
+        for (int i = 0; i < d_h; ++i) acc += q[i] * K[(size_t)t * d_h + i];
+        logits[t] = acc * scale;
+    }
+    oracle_softmax(L, logits, p);
+    for (int t = 0; t < L; ++t)
+        for (int i = 0; i < d_h; ++i) out[i] += p[t] * V[(size_t)t * d_h + i];
+    free(logits);
+    free(p);
+}
+
+static double default_scale(double scale, int d_h) {
+#if LRKV_ORACLE_MUTANT == 3
+    return scale != 0.0 ? scale : 1.0 / (double)d_h; /* planted: wrong scale */
+#else
+    return scale != 0.0 ? scale : 1.0 / sqrt((double)d_h);
+#endif
+}
+
+/* Element (i, j) of B_h (d_h x r, row-major [H][d_h][r]). */
+static double b_elem(const uint16_t* Bm, int h, int d_h, int r, int i, int j) {
+#if LRKV_ORACLE_MUTANT == 6
+    /* planted: factor read as if stored transposed ([r][d_h]) */
+    return bf(Bm[(size_t)h * d_h * r + (size_t)j * d_h + i]);
+#else
+    return bf(Bm[((size_t)h * d_h + i) * r + j]);
+#endif
+}
+
+/* ---------------------------------------------------------------- Eqs. (4)-(5) */
+
+/* Cache contents for n token rows of X [n][d]:
+ *   sK = X W_shared^K, sV = X W_shared^V       -> [n][d_h]
+ *   zK[:,h,:] = X U_h^K, zV[:,h,:] = X U_h^V    -> [n][H][r]
+ * Weights: Ws* [d][d_h]; U* [H][d][r].  Each element is an fp64 sum over d,
+ * rounded to fp32 and then to bf16 (the reference rounding of the cache). */
+void oracle_append(int n, int d, int d_h, int H, int r, const uint16_t* X,
+                   const uint16_t* WsK, const uint16_t* WsV, const uint16_t* UK, const uint16_t* UV,
+                   uint16_t* sK, uint16_t* sV, uint16_t* zK, uint16_t* zV) {
+    #pragma omp parallel for schedule(dynamic)
+    for (int t = 0; t < n; ++t) {
+        const uint16_t* x = X + (size_t)t * d;
+        for (int i = 0; i < d_h; ++i) {
+            double ak = 0.0, av = 0.0;
+            for (int k = 0; k < d; ++k) {
+                ak += bf(x[k]) * bf(WsK[(size_t)k * d_h + i]);
+                av += bf(x[k]) * bf(WsV[(size_t)k * d_h + i]);
+            }
+            sK[(size_t)t * d_h + i] = oracle_round_to_cache(ak);
+            sV[(size_t)t * d_h + i] = oracle_round_to_cache(av);
+        }
+        for (int h = 0; h < H; ++h)
+            for (int j = 0; j < r; ++j) {
+                double ak = 0.0, av = 0.0;
+                for (int k = 0; k < d; ++k) {
+                    ak += bf(x[k]) * bf(UK[((size_t)h * d + k) * r + j]);
+                    av += bf(x[k]) * bf(UV[((size_t)h * d + k) * r + j]);
+                }
+                zK[((size_t)t * H + h) * r + j] = oracle_round_to_cache(ak);
+                zV[((size_t)t * H + h) * r + j] = oracle_round_to_cache(av);
+            }
+    }
+}
+
+/* ---------------------------------------------------------------- Eqs. (2)-(3) */
+
+/* W_h = W_shared + U_h B_h^T, explicitly, as a d x d_h fp64 matrix. */
+static void form_w_h(int d, int d_h, int r, int h, const uint16_t* Ws, const uint16_t* U,
+                     const uint16_t* Bm, double* W) {
+    for (int k = 0; k < d; ++k)
+        for (int i = 0; i < d_h; ++i) {
+            double w = bf(Ws[(size_t)k * d_h + i]);
+#if LRKV_ORACLE_MUTANT == 5
+            w = 0.0; /* planted: shared projection dropped */
+#endif
+            for (int j = 0; j < r; ++j) {
+#if LRKV_ORACLE_MUTANT != 1
+                w += bf(U[((size_t)h * d + k) * r + j]) * b_elem(Bm, h, d_h, r, i, j);
+#endif
+            }
+            W[(size_t)k * d_h + i] = w;
+        }
+}
+
+/* Rows [0, L) of X_b W (X_b: [L][d]) into F [L][d_h]. */
+static void project(int L, int d, int d_h, const uint16_t* Xb, const double* W, double* F) {
+    for (int t = 0; t < L; ++t)
+        for (int i = 0; i < d_h; ++i) {
+            double acc = 0.0;
+            for (int k = 0; k < d; ++k) acc += bf(Xb[(size_t)t * d + k]) * W[(size_t)k * d_h + i];
+            F[(size_t)t * d_h + i] = acc;
+        }
+}
+
+/* Implied full features from the cache of one token slot:
+ *   K_h[t] = s^K_t + B_h^K z^K_{h,t}   (row t of K_s + R_h^K (B_h^K)^T). */
+static void expand_from_cache(int d_h, int H, int r, int h, int64_t slot, const uint16_t* s_pool,
+                              const uint16_t* z_pool, const uint16_t* Bm, double* row) {
+    for (int i = 0; i < d_h; ++i) {
+        double v = bf(s_pool[slot * d_h + i]);
+#if LRKV_ORACLE_MUTANT == 5
+        v = 0.0;
+#endif
+        for (int j = 0; j < r; ++j) {
+#if LRKV_ORACLE_MUTANT != 1
+            v += b_elem(Bm, h, d_h, r, i, j) * bf(z_pool[(slot * H + h) * r + j]);
+#endif
+        }
+        row[i] = v;
+    }
+}
+
+/* ---------------------------------------------------------------- decode */
+
+/* E1 (expanded from weights).  For each sequence b with ctx_len[b] context
+ * rows X[b][0:ctx_len[b]][d] (row stride Lmax*d per sequence) and each head h:
+ * form W_h^K and W_h^V, K_h = X W_h^K, V_h = X W_h^V, then
+ * out[b][h] = softmax(q[b][h] K_h^T * scale) V_h.
+ * want: optional [B][H] mask of the pairs to compute (NULL = all).
+ * Returns 0, or -1 for a bad argument. */
+int oracle_decode_expanded(int B, int H, int d_h, int r, int d, int Lmax, const int32_t* ctx_len,
+                           const uint16_t* X, const uint16_t* WsK, const uint16_t* WsV,
+                           const uint16_t* UK, const uint16_t* UV, const uint16_t* BK,
+                           const uint16_t* BV, const uint16_t* q, double scale,
+                           const uint8_t* want, double* out) {
+    for (int b = 0; b < B; ++b)
+        if (ctx_len[b] < 0 || ctx_len[b] > Lmax) return -1;
+    scale = default_scale(scale, d_h);
+    int bad = 0;
+    #pragma omp parallel for schedule(dynamic)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        if (want && !want[bh]) continue;
+        int L = ctx_len[b];
+        double* WK = (double*)malloc(sizeof(double) * (size_t)d * d_h);
+        double* WV = (double*)malloc(sizeof(double) * (size_t)d * d_h);
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
+        double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
+        double qd[512];
+        if (!WK || !WV || !K || !V || d_h > 512) {
+            #pragma omp atomic write
+            bad = 1;
+        } else {
+            form_w_h(d, d_h, r, h, WsK, UK, BK, WK);
+            form_w_h(d, d_h, r, h, WsV, UV, BV, WV);
+            const uint16_t* Xb = X + (size_t)b * Lmax * d;
+            project(L, d, d_h, Xb, WK, K);
+            project(L, d, d_h, Xb, WV, V);
+            for (int i = 0; i < d_h; ++i) qd[i] = bf(q[((size_t)b * H + h) * d_h + i]);
+            oracle_attend(L, d_h, qd, K, V, scale, out + ((size_t)b * H + h) * d_h);
+        }
+        free(WK); free(WV); free(K); free(V);
+    }
+    return bad ? -1 : 0;
+}
+
+/* E2 (expanded from the paged cache).  Pools: s*[num_blocks*bs][d_h],
+ * z*[num_blocks*bs][H][r]; token t of sequence b lives in slot
+ * block_table[b][t / bs] * bs + t % bs.  For each (b, h): materialise
+ * K_h, V_h for t < seq_lens[b] and run textbook attention.
+ * Returns 0, or -1 when a block id or length is out of range. */
+int oracle_decode_cache(int B, int H, int d_h, int r, int bs, int num_blocks,
+                        const uint16_t* sK, const uint16_t* sV, const uint16_t* zK, const uint16_t* zV,
+                        const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                        const uint16_t* BK, const uint16_t* BV, const uint16_t* q, double scale,
+                        const uint8_t* want, double* out) {
+    for (int b = 0; b < B; ++b) {
+        if (seq_lens[b] < 0 || seq_lens[b] > max_pages * bs) return -1;
+        for (int p = 0; p < (seq_lens[b] + bs - 1) / bs; ++p) {
+            int32_t blk = block_table[(size_t)b * max_pages + p];
+            if (blk < 0 || blk >= num_blocks) return -1;
+        }
+    }
+    scale = default_scale(scale, d_h);
+    int bad = 0;
+    #pragma omp parallel for schedule(dynamic)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        if (want && !want[bh]) continue;
+        int L = seq_lens[b];
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
+        double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
+        double qd[512];
+        if (!K || !V || d_h > 512) {
+            #pragma omp atomic write
+            bad = 1;
+        } else {
+            for (int t = 0; t < L; ++t) {
+                int64_t slot = (int64_t)block_table[(size_t)b * max_pages + t / bs] * bs + t % bs;
+#if LRKV_ORACLE_MUTANT == 2
+                expand_from_cache(d_h, H, r, h, slot, sK, zK, BK, K + (size_t)t * d_h);
+                expand_from_cache(d_h, H, r, h, slot, sV, zV, BK, V + (size_t)t * d_h); /* planted */
+#else
+                expand_from_cache(d_h, H, r, h, slot, sK, zK, BK, K + (size_t)t * d_h);
+                expand_from_cache(d_h, H, r, h, slot, sV, zV, BV, V + (size_t)t * d_h);
+#endif
+            }
+            for (int i = 0; i < d_h; ++i) qd[i] = bf(q[((size_t)b * H + h) * d_h + i]);
+            oracle_attend(L, d_h, qd, K, V, scale, out + ((size_t)b * H + h) * d_h);
+        }
+        free(K); free(V);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ---------------------------------------------------------------- prefill */
+
+/* Causal limit: query at absolute position pos sees keys j <= pos. */
+static int visible(int pos) {
+#if LRKV_ORACLE_MUTANT == 4
+    return pos; /* planted: diagonal excluded */
+#else
+    return pos + 1;
+#endif
+}
+
+/* E1 causal prefill.  Queries q[b][i][h][d_h] for i < Tq sit at absolute
+ * positions q_start[b] + i; context rows X[b][0:q_start[b]+Tq][d] (stride
+ * Lmax*d).  out[b][i][h] = softmax over keys j <= q_start[b]+i. */
+int oracle_prefill_expanded(int B, int Tq, int H, int d_h, int r, int d, int Lmax,
+                            const int32_t* q_start, const uint16_t* X, const uint16_t* WsK,
+                            const uint16_t* WsV, const uint16_t* UK, const uint16_t* UV,
+                            const uint16_t* BK, const uint16_t* BV, const uint16_t* q,
+                            double scale, const uint8_t* want, double* out) {
+    for (int b = 0; b < B; ++b)
+        if (q_start[b] < 0 || q_start[b] + Tq > Lmax) return -1;
+    scale = default_scale(scale, d_h);
+    int bad = 0;
+    #pragma omp parallel for schedule(dynamic)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        if (want && !want[bh]) continue;
+        int L = q_start[b] + Tq;
+        double* WK = (double*)malloc(sizeof(double) * (size_t)d * d_h);
+        double* WV = (double*)malloc(sizeof(double) * (size_t)d * d_h);
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
+        double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
+        double qd[512];
+        if (!WK || !WV || !K || !V || d_h > 512) {
+            #pragma omp atomic write
+            bad = 1;
+        } else {
+            form_w_h(d, d_h, r, h, WsK, UK, BK, WK);
+            form_w_h(d, d_h, r, h, WsV, UV, BV, WV);
+            const uint16_t* Xb = X + (size_t)b * Lmax * d;
+            project(L, d, d_h, Xb, WK, K);
+            project(L, d, d_h, Xb, WV, V);
+            for (int i = 0; i < Tq; ++i) {
+                const uint16_t* qi = q + (((size_t)b * Tq + i) * H + h) * d_h;
+                for (int c = 0; c < d_h; ++c) qd[c] = bf(qi[c]);
+                oracle_attend(visible(q_start[b] + i), d_h, qd, K, V, scale,
+                              out + (((size_t)b * Tq + i) * H + h) * d_h);
+            }
+        }
+        free(WK); free(WV); free(K); free(V);
+    }
+    return bad ? -1 : 0;
+}
+
+/* E2 causal prefill from the paged cache (layout as oracle_decode_cache). */
+int oracle_prefill_cache(int B, int Tq, int H, int d_h, int r, int bs, int num_blocks,
+                         const uint16_t* sK, const uint16_t* sV, const uint16_t* zK,
+                         const uint16_t* zV, const int32_t* block_table, int max_pages,
+                         const int32_t* q_start, const uint16_t* BK, const uint16_t* BV,
+                         const uint16_t* q, double scale, const uint8_t* want, double* out) {
+    for (int b = 0; b < B; ++b) {
+        int L = q_start[b] + Tq;
+        if (q_start[b] < 0 || L > max_pages * bs) return -1;
+        for (int p = 0; p < (L + bs - 1) / bs; ++p) {
+            int32_t blk = block_table[(size_t)b * max_pages + p];
+            if (blk < 0 || blk >= num_blocks) return -1;
+        }
+    }
+    scale = default_scale(scale, d_h);
+    int bad = 0;
+    #pragma omp parallel for schedule(dynamic)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        if (want && !want[bh]) continue;
+        int L = q_start[b] + Tq;
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
+        double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
+        double qd[512];
+        if (!K || !V || d_h > 512) {
+            #pragma omp atomic write
+            bad = 1;
+        } else {
+            for (int t = 0; t < L; ++t) {
+                int64_t slot = (int64_t)block_table[(size_t)b * max_pages + t / bs] * bs + t % bs;
+                expand_from_cache(d_h, H, r, h, slot, sK, zK, BK, K + (size_t)t * d_h);
+                expand_from_cache(d_h, H, r, h, slot, sV, zV, BV, V + (size_t)t * d_h);
+            }
+            for (int i = 0; i < Tq; ++i) {
+                const uint16_t* qi = q + (((size_t)b * Tq + i) * H + h) * d_h;
+                for (int c = 0; c < d_h; ++c) qd[c] = bf(qi[c]);
+                oracle_attend(visible(q_start[b] + i), d_h, qd, K, V, scale,
+                              out + (((size_t)b * Tq + i) * H + h) * d_h);
+            }
+        }
+        free(K); free(V);
+    }
+    return bad ? -1 : 0;
+}
