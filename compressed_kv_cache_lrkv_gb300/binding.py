@@ -1,0 +1,179 @@
+"""Thin ctypes binding of liblrkv.so (include/lrkv.h): argument marshalling only.
+
+Every function here forwards to the C entry point of the same name; tensors
+are torch CUDA tensors whose data pointers are passed through.  Nothing is
+computed in Python, and there is no fallback: if the library cannot be loaded
+(or a call returns an error) an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+LRKV_OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "workspace too small", 4: "CUDA error",
+                5: "device bounds", 6: "timeout"}
+DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+
+EXPORTED = ["lrkv_abi_version", "lrkv_status_string", "lrkv_last_error", "lrkv_cache_block_bytes", "lrkv_append",
+            "lrkv_decode_workspace_bytes", "lrkv_decode", "lrkv_prefill_workspace_bytes", "lrkv_prefill"]
+
+
+class LrkvError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {detail}")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int32), ("d_h", ctypes.c_int32), ("r", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("softmax_scale", ctypes.c_float)]
+
+
+class Cache(ctypes.Structure):
+    _fields_ = [("sK", ctypes.c_void_p), ("sV", ctypes.c_void_p), ("zK", ctypes.c_void_p), ("zV", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (building first if needed) liblrkv.so and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        path = _build.build()
+    lib = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    P = ctypes.POINTER
+    lib.lrkv_abi_version.restype = ctypes.c_int
+    lib.lrkv_status_string.restype = ctypes.c_char_p
+    lib.lrkv_status_string.argtypes = [ctypes.c_int]
+    lib.lrkv_last_error.restype = ctypes.c_char_p
+    lib.lrkv_cache_block_bytes.restype = sz
+    lib.lrkv_cache_block_bytes.argtypes = [P(Dims)]
+    lib.lrkv_append.restype = ctypes.c_int
+    lib.lrkv_append.argtypes = [P(Dims), vp, vp, i32, vp, P(Cache), vp, vp]
+    lib.lrkv_decode_workspace_bytes.restype = sz
+    lib.lrkv_decode_workspace_bytes.argtypes = [P(Dims), i32]
+    lib.lrkv_decode.restype = ctypes.c_int
+    lib.lrkv_decode.argtypes = [P(Dims), vp, vp, vp, P(Cache), vp, i32, vp, i32, vp, vp, sz, vp, vp]
+    lib.lrkv_prefill_workspace_bytes.restype = sz
+    lib.lrkv_prefill_workspace_bytes.argtypes = [P(Dims), i32, i32]
+    lib.lrkv_prefill.restype = ctypes.c_int
+    lib.lrkv_prefill.argtypes = [P(Dims), vp, vp, vp, P(Cache), vp, i32, vp, i32, i32, vp, vp, sz, vp, vp]
+    _lib = lib
+    return lib
+
+
+def make_dims(H: int, d_h: int, r: int, d: int, block_size: int = 64, softmax_scale: float = 0.0) -> Dims:
+    return Dims(H, d_h, r, d, block_size, softmax_scale)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != LRKV_OK:
+        raise LrkvError(rc, where, load().lrkv_last_error().decode())
+
+
+class PagedCache:
+    """One layer's four cache pools (device tensors, bf16 bit patterns as int16/bfloat16)."""
+
+    def __init__(self, sK, sV, zK, zV):
+        self.sK, self.sV, self.zK, self.zV = sK, sV, zK, zV
+        self.num_blocks = int(sK.shape[0])
+
+    @classmethod
+    def empty(cls, num_blocks: int, H: int, d_h: int, r: int, block_size: int = 64, device="cuda"):
+        mk = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=device)
+        return cls(mk(num_blocks, block_size, d_h), mk(num_blocks, block_size, d_h),
+                   mk(num_blocks, block_size, H, r), mk(num_blocks, block_size, H, r))
+
+    def struct(self) -> Cache:
+        return Cache(_ptr(self.sK), _ptr(self.sV), _ptr(self.zK), _ptr(self.zV), self.num_blocks)
+
+    def tensors(self):
+        return self.sK, self.sV, self.zK, self.zV
+
+
+def abi_version() -> int:
+    return int(load().lrkv_abi_version())
+
+
+def cache_block_bytes(dims: Dims) -> int:
+    return int(load().lrkv_cache_block_bytes(ctypes.byref(dims)))
+
+
+def decode_workspace_bytes(dims: Dims, batch: int) -> int:
+    return int(load().lrkv_decode_workspace_bytes(ctypes.byref(dims), batch))
+
+
+def prefill_workspace_bytes(dims: Dims, batch: int, Tq: int) -> int:
+    return int(load().lrkv_prefill_workspace_bytes(ctypes.byref(dims), batch, Tq))
+
+
+def lrkv_append(dims: Dims, X, W_catT, slot_mapping, cache: PagedCache, status=None, stream=None):
+    """Eqs. (4)-(5): write rows of X [n, d] into the cache at slot_mapping [n]."""
+    n = int(X.shape[0])
+    c = cache.struct()
+    rc = load().lrkv_append(ctypes.byref(dims), _ptr(X), _ptr(W_catT), n, _ptr(slot_mapping), ctypes.byref(c),
+                            _ptr(status), _stream(stream))
+    _check(rc, "lrkv_append")
+
+
+def lrkv_decode(dims: Dims, q, BK, BV, cache: PagedCache, block_table, seq_lens, out, workspace, status=None,
+                stream=None):
+    """Factored decode (Eqs. (6)-(7)): q [B, H, d_h] -> out [B, H, d_h]."""
+    B = int(q.shape[0])
+    c = cache.struct()
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().lrkv_decode(ctypes.byref(dims), _ptr(q), _ptr(BK), _ptr(BV), ctypes.byref(c), _ptr(block_table),
+                            int(block_table.shape[1]), _ptr(seq_lens), B, _ptr(out), _ptr(workspace), ws_bytes,
+                            _ptr(status), _stream(stream))
+    _check(rc, "lrkv_decode")
+
+
+def lrkv_prefill(dims: Dims, q, BK, BV, cache: PagedCache, block_table, q_start, out, workspace=None, status=None,
+                 stream=None):
+    """Causal chunked prefill: q [B, Tq, H, d_h] at positions q_start[b] + i -> out [B, Tq, H, d_h]."""
+    B, Tq = int(q.shape[0]), int(q.shape[1])
+    c = cache.struct()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().lrkv_prefill(ctypes.byref(dims), _ptr(q), _ptr(BK), _ptr(BV), ctypes.byref(c), _ptr(block_table),
+                             int(block_table.shape[1]), _ptr(q_start), B, Tq, _ptr(out), _ptr(workspace), ws_bytes,
+                             _ptr(status), _stream(stream))
+    _check(rc, "lrkv_prefill")
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A 256-byte aligned device byte buffer (torch's allocator aligns to 512 B)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def pack_wcat_t(WsK, WsV, UK, UV) -> torch.Tensor:
+    """W_cat^T [N, d] from W_shared^{K,V} [d, d_h] and U^{K,V} [H, d, r] (column order of lrkv_append)."""
+    H, d, r = UK.shape
+    return torch.cat([WsK.t(), WsV.t(), UK.permute(0, 2, 1).reshape(H * r, d),
+                      UV.permute(0, 2, 1).reshape(H * r, d)], dim=0).contiguous()

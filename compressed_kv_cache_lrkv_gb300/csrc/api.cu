@@ -1,0 +1,282 @@
+// api.cu -- the extern "C" entry points of include/lrkv.h: argument validation,
+// TMA descriptor encoding, workspace carving and kernel launches on the
+// caller's stream.  No allocation, no state kept between calls.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "lrkv_internal.cuh"
+
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+lrkv_status fail(lrkv_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+lrkv_status ok() {
+    g_last_error[0] = '\0';
+    return LRKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+lrkv_status check_dims(const lrkv_dims* dm) {
+    if (!dm) return fail(LRKV_ERR_INVALID_ARG, "dims is NULL");
+    if (dm->block_size != 64) return fail(LRKV_ERR_UNSUPPORTED, "block_size %d (only 64 is supported)", dm->block_size);
+    if (dm->d_h != 64 && dm->d_h != 128) return fail(LRKV_ERR_UNSUPPORTED, "d_h %d (supported: 64, 128)", dm->d_h);
+    if (!(dm->r == 8 || dm->r == 16 || dm->r == 32))
+        return fail(LRKV_ERR_UNSUPPORTED, "r %d (supported: 8, 16, 32)", dm->r);
+    if (dm->r > dm->d_h) return fail(LRKV_ERR_UNSUPPORTED, "r %d > d_h %d", dm->r, dm->d_h);
+    if (dm->H < 1 || dm->H > 128) return fail(LRKV_ERR_UNSUPPORTED, "H %d (supported: 1..128)", dm->H);
+    if (dm->d < 8 || dm->d % 8 != 0) return fail(LRKV_ERR_UNSUPPORTED, "d %d (must be a positive multiple of 8)", dm->d);
+    if (!(dm->softmax_scale >= 0.f) || std::isinf(dm->softmax_scale))
+        return fail(LRKV_ERR_INVALID_ARG, "softmax_scale %g", (double)dm->softmax_scale);
+    return LRKV_OK;
+}
+
+lrkv_status check_cache(const lrkv_cache* c) {
+    if (!c) return fail(LRKV_ERR_INVALID_ARG, "cache is NULL");
+    if (!c->sK || !c->sV || !c->zK || !c->zV) return fail(LRKV_ERR_INVALID_ARG, "cache pool pointer is NULL");
+    if (!aligned16(c->sK) || !aligned16(c->sV) || !aligned16(c->zK) || !aligned16(c->zV))
+        return fail(LRKV_ERR_INVALID_ARG, "cache pool pointer not 16-byte aligned");
+    if (c->num_blocks < 1 || c->num_blocks > (1 << 24))
+        return fail(LRKV_ERR_INVALID_ARG, "num_blocks %d outside [1, 2^24]", c->num_blocks);
+    return LRKV_OK;
+}
+
+#define LRKV_REQUIRE_PTR(p)                                                               \
+    do {                                                                                  \
+        if (!(p)) return fail(LRKV_ERR_INVALID_ARG, "%s is NULL", #p);                    \
+        if (!aligned16(p)) return fail(LRKV_ERR_INVALID_ARG, "%s not 16-byte aligned", #p); \
+    } while (0)
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+lrkv_status device_info(DeviceInfo* di) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&di->sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&di->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return fail(LRKV_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+    return LRKV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix with a [box_rows][box_cols] box.
+lrkv_status make_tmap(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                      uint32_t box_rows, CUtensorMapSwizzle swz, const char* what) {
+    auto enc = encode_fn();
+    if (!enc) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+    return LRKV_OK;
+}
+
+lrkv_status cuda_status(cudaError_t e, const char* what) {
+    if (e != cudaSuccess) return fail(LRKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int lrkv_abi_version(void) { return LRKV_ABI_VERSION; }
+
+const char* lrkv_status_string(lrkv_status s) {
+    switch (s) {
+        case LRKV_OK: return "ok";
+        case LRKV_ERR_INVALID_ARG: return "invalid argument";
+        case LRKV_ERR_UNSUPPORTED: return "unsupported shape";
+        case LRKV_ERR_WORKSPACE: return "workspace too small";
+        case LRKV_ERR_CUDA: return "CUDA error";
+        case LRKV_ERR_DEVICE_BOUNDS: return "device-side index out of range";
+        case LRKV_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+const char* lrkv_last_error(void) { return g_last_error; }
+
+size_t lrkv_cache_block_bytes(const lrkv_dims* dims) {
+    if (check_dims(dims) != LRKV_OK) return 0;
+    return (size_t)dims->block_size * 2 * 2 * (size_t)(dims->d_h + dims->H * dims->r);
+}
+
+lrkv_status lrkv_append(const lrkv_dims* dims, const void* X, const void* W_catT, int32_t n_tok,
+                        const int32_t* slot_mapping, const lrkv_cache* cache, uint32_t* status_dev, void* stream) {
+    lrkv_status s = check_dims(dims);
+    if (s != LRKV_OK) return s;
+    if ((s = check_cache(cache)) != LRKV_OK) return s;
+    if (n_tok < 0) return fail(LRKV_ERR_INVALID_ARG, "n_tok %d < 0", n_tok);
+    if (n_tok == 0) return ok();
+    LRKV_REQUIRE_PTR(X);
+    LRKV_REQUIRE_PTR(W_catT);
+    if (!slot_mapping) return fail(LRKV_ERR_INVALID_ARG, "slot_mapping is NULL");
+    lrkv::AppendArgs a{};
+    a.X = static_cast<const uint16_t*>(X);
+    a.W = static_cast<const uint16_t*>(W_catT);
+    a.slots = slot_mapping;
+    a.sK = static_cast<uint16_t*>(cache->sK);
+    a.sV = static_cast<uint16_t*>(cache->sV);
+    a.zK = static_cast<uint16_t*>(cache->zK);
+    a.zV = static_cast<uint16_t*>(cache->zV);
+    a.status = status_dev;
+    a.n = n_tok;
+    a.d = dims->d;
+    a.N = 2 * (dims->d_h + dims->H * dims->r);
+    a.d_h = dims->d_h;
+    a.HR = dims->H * dims->r;
+    a.nslots = (long long)cache->num_blocks * dims->block_size;
+    if (n_tok >= lrkv::kAppendTcMinRows) {
+        CUtensorMap tX, tW;
+        const int bn = lrkv::append_tc_block_n(a.N);
+        if ((s = make_tmap(&tX, X, dims->d, n_tok, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "X")) != LRKV_OK) return s;
+        if ((s = make_tmap(&tW, W_catT, dims->d, a.N, 64, bn, CU_TENSOR_MAP_SWIZZLE_128B, "W_catT")) != LRKV_OK)
+            return s;
+        return cuda_status(lrkv::launch_append_tc(tX, tW, a, static_cast<cudaStream_t>(stream)),
+                           "lrkv_append launch");
+    }
+    return cuda_status(lrkv::launch_append(a, static_cast<cudaStream_t>(stream)), "lrkv_append launch");
+}
+
+size_t lrkv_decode_workspace_bytes(const lrkv_dims* dims, int32_t batch) {
+    if (check_dims(dims) != LRKV_OK || batch < 0) return 0;
+    DeviceInfo di;
+    if (device_info(&di) != LRKV_OK) return 0;
+    return lrkv::decode_workspace_bytes(dims->H, dims->d_h, dims->r, batch, di.sms, di.smem_optin);
+}
+
+lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, const void* BV, const lrkv_cache* cache,
+                        const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                        int32_t batch, void* out, void* workspace, size_t workspace_bytes, uint32_t* status_dev,
+                        void* stream) {
+    lrkv_status s = check_dims(dims);
+    if (s != LRKV_OK) return s;
+    if ((s = check_cache(cache)) != LRKV_OK) return s;
+    if (batch < 0) return fail(LRKV_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (batch == 0) return ok();
+    if (max_blocks_per_seq < 1 || (long long)max_blocks_per_seq * dims->block_size > (1LL << 30))
+        return fail(LRKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", max_blocks_per_seq);
+    LRKV_REQUIRE_PTR(q);
+    LRKV_REQUIRE_PTR(BK);
+    LRKV_REQUIRE_PTR(BV);
+    LRKV_REQUIRE_PTR(out);
+    if (!block_table || !seq_lens) return fail(LRKV_ERR_INVALID_ARG, "block_table or seq_lens is NULL");
+    DeviceInfo di;
+    if ((s = device_info(&di)) != LRKV_OK) return s;
+    const size_t need = lrkv::decode_workspace_bytes(dims->H, dims->d_h, dims->r, batch, di.sms, di.smem_optin);
+    if (!workspace || ((uintptr_t)workspace & 255u))
+        return fail(LRKV_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+    if (workspace_bytes < need)
+        return fail(LRKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+
+    CUtensorMap tK, tV;
+    const uint64_t rows = (uint64_t)cache->num_blocks * dims->block_size;
+    if ((s = make_tmap(&tK, cache->sK, dims->d_h, rows, 64, 8, CU_TENSOR_MAP_SWIZZLE_128B, "sK")) != LRKV_OK) return s;
+    if ((s = make_tmap(&tV, cache->sV, dims->d_h, rows, 64, 8, CU_TENSOR_MAP_SWIZZLE_128B, "sV")) != LRKV_OK) return s;
+
+    lrkv::DecodeArgs a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.BK = static_cast<const uint16_t*>(BK);
+    a.BV = static_cast<const uint16_t*>(BV);
+    a.zK = static_cast<const uint16_t*>(cache->zK);
+    a.zV = static_cast<const uint16_t*>(cache->zV);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.status = status_dev;
+    a.out = static_cast<uint16_t*>(out);
+    a.B = batch;
+    a.H = dims->H;
+    a.max_pages = max_blocks_per_seq;
+    a.num_blocks = cache->num_blocks;
+    const float scale = dims->softmax_scale > 0.f ? dims->softmax_scale : 1.0f / std::sqrt((float)dims->d_h);
+    a.scale_log2 = scale * 1.4426950408889634f;
+    lrkv::decode_carve_workspace(&a, workspace, dims->H, dims->d_h, dims->r, batch, di.sms, di.smem_optin);
+    return cuda_status(lrkv::launch_decode(tK, tV, a, dims->d_h, dims->r, di.sms, di.smem_optin,
+                                           static_cast<cudaStream_t>(stream)),
+                       "lrkv_decode launch");
+}
+
+size_t lrkv_prefill_workspace_bytes(const lrkv_dims* dims, int32_t batch, int32_t Tq) {
+    (void)batch;
+    (void)Tq;
+    if (check_dims(dims) != LRKV_OK) return 0;
+    return 0;
+}
+
+lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, const void* BV, const lrkv_cache* cache,
+                         const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* q_start, int32_t batch,
+                         int32_t Tq, void* out, void* workspace, size_t workspace_bytes, uint32_t* status_dev,
+                         void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    lrkv_status s = check_dims(dims);
+    if (s != LRKV_OK) return s;
+    if ((s = check_cache(cache)) != LRKV_OK) return s;
+    if (batch < 0 || Tq < 0) return fail(LRKV_ERR_INVALID_ARG, "batch %d / Tq %d < 0", batch, Tq);
+    if (batch == 0 || Tq == 0) return ok();
+    if (max_blocks_per_seq < 1 || (long long)max_blocks_per_seq * dims->block_size > (1LL << 30))
+        return fail(LRKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", max_blocks_per_seq);
+    LRKV_REQUIRE_PTR(q);
+    LRKV_REQUIRE_PTR(BK);
+    LRKV_REQUIRE_PTR(BV);
+    LRKV_REQUIRE_PTR(out);
+    if (!block_table || !q_start) return fail(LRKV_ERR_INVALID_ARG, "block_table or q_start is NULL");
+    lrkv::PrefillArgs a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.BK = static_cast<const uint16_t*>(BK);
+    a.BV = static_cast<const uint16_t*>(BV);
+    a.sK = static_cast<const uint16_t*>(cache->sK);
+    a.sV = static_cast<const uint16_t*>(cache->sV);
+    a.zK = static_cast<const uint16_t*>(cache->zK);
+    a.zV = static_cast<const uint16_t*>(cache->zV);
+    a.block_table = block_table;
+    a.q_start = q_start;
+    a.status = status_dev;
+    a.out = static_cast<uint16_t*>(out);
+    a.B = batch;
+    a.Tq = Tq;
+    a.H = dims->H;
+    a.max_pages = max_blocks_per_seq;
+    a.num_blocks = cache->num_blocks;
+    const float scale = dims->softmax_scale > 0.f ? dims->softmax_scale : 1.0f / std::sqrt((float)dims->d_h);
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return cuda_status(lrkv::launch_prefill(a, dims->d_h, dims->r, static_cast<cudaStream_t>(stream)),
+                       "lrkv_prefill launch");
+}
+
+}  // extern "C"

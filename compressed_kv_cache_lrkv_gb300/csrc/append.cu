@@ -1,0 +1,122 @@
+// append.cu -- Eqs. (4)-(5) of "Low-Rank Key Value Attention": write the
+// compressed cache rows of new tokens.
+//
+//   Y = X W_cat,  W_cat = [W_shared^K | W_shared^V | U_1^K..U_H^K | U_1^V..U_H^V]
+//   s^K_t = Y[t, 0:d_h], s^V_t = Y[t, d_h:2d_h], z^K_{h,t} = Y[t, 2d_h + h r : 2d_h + (h+1) r], z^V likewise.
+//
+// This file holds the bandwidth-bound variant used when few rows are appended
+// (a decode step appends one row per sequence): each warp owns four output
+// columns and reads their weight rows (W_cat^T, contiguous along d) exactly
+// once with 16-byte loads, for up to NT token rows at a time.  fp32 accumulation
+// in a fixed order, round-to-nearest-even to bf16, scatter to the row's slot.
+#include "kernels.h"
+#include "lrkv_internal.cuh"
+
+namespace lrkv {
+
+
+// Store one finished fp32 value of output column `col` for token slot `slot`.
+__device__ __forceinline__ void store_cache_value(const AppendArgs& a, long long slot, int col, float v) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    const uint16_t bits = *reinterpret_cast<const uint16_t*>(&b);
+    if (col < a.d_h)
+        a.sK[slot * a.d_h + col] = bits;
+    else if (col < 2 * a.d_h)
+        a.sV[slot * a.d_h + col - a.d_h] = bits;
+    else if (col < 2 * a.d_h + a.HR)
+        a.zK[slot * a.HR + col - 2 * a.d_h] = bits;
+    else
+        a.zV[slot * a.HR + col - 2 * a.d_h - a.HR] = bits;
+}
+
+// Slot of row t, or -1 to skip it (negative entry: padding; too large: status bit).
+__device__ __forceinline__ long long checked_slot(const AppendArgs& a, int t) {
+    const long long s = a.slots[t];
+    if (s < 0) return -1;
+    if (s >= a.nslots) {
+        set_status(a.status, LRKV_DEV_BAD_SLOT);
+        return -1;
+    }
+    return s;
+}
+
+__device__ __forceinline__ float dot8(const uint4& w, const uint4& x) {
+    float acc = bf16lo(w.x) * bf16lo(x.x);
+    acc = fmaf(bf16hi(w.x), bf16hi(x.x), acc);
+    acc = fmaf(bf16lo(w.y), bf16lo(x.y), acc);
+    acc = fmaf(bf16hi(w.y), bf16hi(x.y), acc);
+    acc = fmaf(bf16lo(w.z), bf16lo(x.z), acc);
+    acc = fmaf(bf16hi(w.z), bf16hi(x.z), acc);
+    acc = fmaf(bf16lo(w.w), bf16lo(x.w), acc);
+    acc = fmaf(bf16hi(w.w), bf16hi(x.w), acc);
+    return acc;
+}
+
+constexpr int kRowCols = 4;   // output columns per warp
+constexpr int kRowWarps = 8;  // warps per CTA
+
+template <int NT>
+__global__ void __launch_bounds__(256) append_rowwise_kernel(const AppendArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c0 = (blockIdx.x * kRowWarps + warp) * kRowCols;
+    const int t0 = blockIdx.y * NT;
+    if (c0 >= a.N) return;
+    float acc[kRowCols][NT];
+#pragma unroll
+    for (int c = 0; c < kRowCols; ++c)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[c][t] = 0.f;
+
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int k = lane * 8; k < a.d; k += 256) {
+        uint4 w[kRowCols];
+#pragma unroll
+        for (int c = 0; c < kRowCols; ++c)
+            w[c] = (c0 + c < a.N) ? __ldg(reinterpret_cast<const uint4*>(a.W + (size_t)(c0 + c) * a.d + k)) : zero;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t0 + t < a.n) {
+                const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + t) * a.d + k));
+#pragma unroll
+                for (int c = 0; c < kRowCols; ++c) acc[c][t] += dot8(w[c], x);
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < kRowCols; ++c)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float v = acc[c][t];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            acc[c][t] = v;
+        }
+#pragma unroll
+    for (int c = 0; c < kRowCols; ++c)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (lane == ((t * kRowCols + c) & 31) && t0 + t < a.n && c0 + c < a.N) {
+                const long long slot = checked_slot(a, t0 + t);
+                if (slot >= 0) store_cache_value(a, slot, c0 + c, acc[c][t]);
+            }
+        }
+}
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
+    const int cols_per_cta = kRowCols * kRowWarps;
+    const int gx = (a.N + cols_per_cta - 1) / cols_per_cta;
+#define LRKV_ROW(NTV)                                                                    \
+    {                                                                                    \
+        dim3 grid(gx, (a.n + NTV - 1) / NTV);                                            \
+        append_rowwise_kernel<NTV><<<grid, 256, 0, stream>>>(a);                         \
+        return cudaGetLastError();                                                       \
+    }
+    if (a.n <= 1) LRKV_ROW(1)
+    if (a.n <= 2) LRKV_ROW(2)
+    if (a.n <= 4) LRKV_ROW(4)
+    if (a.n <= 8) LRKV_ROW(8)
+    LRKV_ROW(16)
+#undef LRKV_ROW
+}
+
+}  // namespace lrkv

@@ -1,0 +1,558 @@
+// decode.cu -- factored LRKV decode (Eqs. (6)-(7) of "Low-Rank Key Value Attention").
+//
+// Per sequence b and head h, with q~_h = q_h B_h^K (frame "Compute logits without
+// expanding historical keys", step 1):
+//     score_t = (q_h . s^K_t + q~_h . z^K_{h,t}) * scale
+//     out_h   = sum_t p_t s^V_t + B_h^V (sum_t p_t z^V_{h,t})       (Eq. (7))
+// Per-head K_h / V_h are never formed.
+//
+// Kernel 1 (split): a persistent grid of one CTA per SM.  The cached tokens of
+// all sequences are cut into 8-token granules and divided evenly into at most
+// one contiguous range ("split") per CTA.  A producer warp streams each
+// granule's s^K, s^V (TMA tensor loads, 128-byte swizzle) and z^K, z^V (bulk
+// copies) into a ring of shared-memory stages; each stage is read from HBM
+// once, for all H heads.  Consumer warps own 16 heads each; NG groups of
+// ceil(H/16) warps take stages round-robin, each keeping its own online
+// softmax state and writing one partial (m, l, acc_s[d_h], acc_z[r]) per head.
+//   - q . s^K and p . s^V run on the tensor cores (mma.sync m16n8k16 / m16n8k8,
+//     heads on M, tokens on N / K) -- s is shared by all heads of the CTA;
+//   - q~ . z^K and p . z^V run on CUDA cores in fp32 (each z element is used
+//     once; no reuse for a tensor core to exploit).
+// Kernel 2 (combine): log-sum-exp merge of the partials of each (b, h), then the
+// residual up-projection B_h^V acc_z and the bf16 store.
+#include "kernels.h"
+#include "lrkv_internal.cuh"
+
+namespace lrkv {
+
+
+constexpr int kGran = 8;  // tokens per pipeline stage (granule)
+constexpr int kScratchFloats = 16 * 8 + 16 * 8 + 16;  // per consumer warp: z-scores, p, alpha
+
+struct Split {
+    int b, g0, g1;
+};
+
+// Granules of sequence b, or 0 when its length is outside [1, cap].
+__device__ __forceinline__ int seq_granules(const int32_t* seq_lens, int b, int cap) {
+    const int L = seq_lens[b];
+    return (L >= 1 && L <= cap) ? (L + kGran - 1) / kGran : 0;
+}
+
+// Even division of all granules into at most max(G, B) splits: chunk is chosen
+// so that sum_b ceil(gr_b / chunk) <= G whenever G > B; sequence b is then cut
+// into ns_b = ceil(gr_b / chunk) near-equal pieces.
+__device__ __forceinline__ int partition_chunk(const int32_t* seq_lens, int B, int cap, int G, int* nsplits) {
+    long long total = 0;
+    for (int b = 0; b < B; ++b) total += seq_granules(seq_lens, b, cap);
+    const int denom = G > B ? G - B : 1;
+    const int chunk = (int)max(1LL, (total + denom - 1) / denom);
+    int ns = 0;
+    for (int b = 0; b < B; ++b) ns += (seq_granules(seq_lens, b, cap) + chunk - 1) / chunk;
+    *nsplits = ns;
+    return chunk;
+}
+
+__device__ __forceinline__ Split split_info(const int32_t* seq_lens, int B, int cap, int chunk, int s) {
+    int base = 0;
+    for (int b = 0; b < B; ++b) {
+        const int gr = seq_granules(seq_lens, b, cap);
+        const int ns = (gr + chunk - 1) / chunk;
+        if (s < base + ns) {
+            const int i = s - base;
+            return Split{b, (int)((long long)i * gr / ns), (int)((long long)(i + 1) * gr / ns)};
+        }
+        base += ns;
+    }
+    return Split{0, 0, 0};
+}
+
+// First split index and split count of sequence b.
+__device__ __forceinline__ void seq_splits(const int32_t* seq_lens, int B, int cap, int chunk, int b, int* first,
+                                           int* count) {
+    int base = 0;
+    for (int bb = 0; bb < b; ++bb) base += (seq_granules(seq_lens, bb, cap) + chunk - 1) / chunk;
+    *first = base;
+    *count = (seq_granules(seq_lens, b, cap) + chunk - 1) / chunk;
+}
+
+// Bounded wait until a slot's stage tag equals `want` (sets LRKV_DEV_TIMEOUT on expiry).
+__device__ __forceinline__ bool wait_tag(volatile int* tag, int want, uint32_t* status) {
+    if (*tag == want) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (*tag != want) {
+        __nanosleep(32);
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            set_status(status, LRKV_DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Issue the loads of one 8-token granule (stage) into ring slot `slot`:
+// s^K, s^V by TMA tensor copies (128-byte swizzle), z^K, z^V by bulk copies.
+// An out-of-range block id is reported and the stage is marked empty.
+template <int D_H, int R>
+__device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUtensorMap* tm_sV, const DecodeArgs& a,
+                                            uint32_t st, uint32_t bar, int* meta_slot, int b, int gi,
+                                            uint64_t pol) {
+    const int blk = a.block_table[(size_t)b * a.max_pages + (gi >> 3)];
+    if (blk < 0 || blk >= a.num_blocks) {
+        set_status(a.status, LRKV_DEV_BAD_BLOCK);
+        *meta_slot = 0;
+        mbar_arrive(bar);
+        return;
+    }
+    *meta_slot = 1;
+    mbar_arrive_expect_tx(bar, 32u * D_H + 32u * a.H * R);
+    const int row = blk * kBlockSize + ((gi & 7) << 3);
+#pragma unroll
+    for (int i = 0; i < D_H / 64; ++i) {
+        tma_load_2d_hint(st + i * 1024, tm_sK, i * 64, row, bar, pol);
+        tma_load_2d_hint(st + 16 * D_H + i * 1024, tm_sV, i * 64, row, bar, pol);
+    }
+    const size_t zoff = (size_t)row * a.H * R;
+    bulk_load_hint(st + 32 * D_H, a.zK + zoff, 16u * a.H * R, bar, pol);
+    bulk_load_hint(st + 32 * D_H + 16 * a.H * R, a.zV + zoff, 16u * a.H * R, bar, pol);
+}
+
+// At most 8 warps per CTA (one per head tile and group), so each thread may
+// hold up to 255 registers.  There is no dedicated producer warp: thread 0
+// fills the ring at the start of each split, and afterwards the last warp to
+// release a stage refills that slot with the stage nslot positions ahead.
+template <int D_H, int R>
+__global__ void __launch_bounds__(256, 1)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_sK, const __grid_constant__ CUtensorMap tm_sV,
+                        const DecodeArgs a) {
+    static_assert(D_H == 64 || D_H == 128, "d_h");
+    static_assert(R % 8 == 0 && R <= 32, "r");
+    constexpr int NC = R / 8;                                   // 16-byte chunks per z row
+    constexpr int RP128 = (2 * R >= 128) ? 1 : 128 / (2 * R);   // z rows per 128-byte bank line
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t smem_s = smem_u32(smem);
+
+    const int H = a.H;
+    const int HT = (H + 15) >> 4;
+    const int NCW = HT * a.ng;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nslot = a.nslot;
+    const int stage_bytes = a.stage_bytes;
+
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + nslot * stage_bytes);
+    int* meta = reinterpret_cast<int*>(full + nslot);            // 1: stage holds data, 0: skipped
+    int* rel = meta + nslot;                                     // warps done with the slot's current stage
+    int* nissued = rel + nslot;                                  // stages ever issued into the slot
+    volatile int* tag = nissued + nslot;                         // CTA-wide index of the stage last issued
+    float* qt_s = reinterpret_cast<float*>(meta + ((4 * nslot + 3) & ~3));
+    float* scratch = qt_s + H * R;
+    volatile int* abort_flag = reinterpret_cast<int*>(scratch + NCW * kScratchFloats);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nslot; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            rel[s] = 0;
+            nissued[s] = 0;
+            tag[s] = -1;
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int cap = a.max_pages * kBlockSize;
+    int nsplits;
+    const int chunk = partition_chunk(a.seq_lens, a.B, cap, gridDim.x, &nsplits);
+    const uint64_t pol = policy_evict_first();
+
+    const int grp = warp / HT, ht = warp % HT;
+    const int h0 = ht * 16;
+    const int g = lane >> 2, tq = lane & 3;
+    const int hz = lane & 15, half = lane >> 4;
+    const int hzh = h0 + hz;
+    const bool hz_ok = hzh < H;
+    const int rot = (hz / RP128) % NC;
+    float* SZ = scratch + warp * kScratchFloats;
+    float* SP = SZ + 128;
+    float* SA = SP + 128;
+    const int nct = NCW * 32;
+    const int hA = h0 + g, hB = h0 + g + 8;
+
+    int kbase = 0;  // stages consumed by this CTA before the current split (ring position and phase)
+    for (int s = blockIdx.x; s < nsplits; s += gridDim.x) {
+        const Split sp = split_info(a.seq_lens, a.B, cap, chunk, s);
+        const int b = sp.b;
+        const int L = a.seq_lens[b];
+        const int nst = sp.g1 - sp.g0;
+
+        // Once every warp is here, all stages of the previous split have been
+        // released and no copy is in flight: fill the ring for this split.
+        named_bar(1, nct);
+        if (threadIdx.x == 0 && !*abort_flag) {
+            for (int k = 0; k < min(nslot, nst); ++k) {
+                const int slot = (kbase + k) % nslot;
+                tag[slot] = kbase + k;
+                issue_stage<D_H, R>(&tm_sK, &tm_sV, a, smem_s + slot * stage_bytes, smem_u32(&full[slot]),
+                                    &meta[slot], b, sp.g0 + k, pol);
+                ++nissued[slot];
+            }
+        }
+
+        // q~ = q B^K for every head of sequence b (fp32, shared memory).
+        for (int idx = threadIdx.x; idx < H * R; idx += nct) {
+            const int h = idx / R, j = idx - (idx / R) * R;
+            const uint16_t* qh = a.q + ((size_t)b * H + h) * D_H;
+            const uint16_t* bk = a.BK + (size_t)h * D_H * R + j;
+            float acc = 0.f;
+#pragma unroll 8
+            for (int dd = 0; dd < D_H; ++dd)
+                acc = fmaf(__uint_as_float((uint32_t)qh[dd] << 16), __uint_as_float((uint32_t)bk[dd * R] << 16), acc);
+            qt_s[idx] = acc;
+        }
+        named_bar(1, nct);
+
+        // This lane's q~ row, chunk-rotated so that z rows are read conflict-free.
+        float qt[R];
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                qt[cc * 8 + e] = hz_ok ? qt_s[hzh * R + ((cc + rot) % NC) * 8 + e] : 0.f;
+
+        // Query A fragments (heads on M): rows hA, hB; k = head dimension.
+        uint32_t qa[D_H / 16][4];
+        {
+            const uint32_t* qA = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * H + hA) * D_H);
+            const uint32_t* qB = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * H + hB) * D_H);
+#pragma unroll
+            for (int kk = 0; kk < D_H / 16; ++kk) {
+                qa[kk][0] = hA < H ? qA[kk * 8 + tq] : 0u;
+                qa[kk][1] = hB < H ? qB[kk * 8 + tq] : 0u;
+                qa[kk][2] = hA < H ? qA[kk * 8 + 4 + tq] : 0u;
+                qa[kk][3] = hB < H ? qB[kk * 8 + 4 + tq] : 0u;
+            }
+        }
+        named_bar(1, nct);  // every lane has its q~ before the next split rewrites it
+
+        float o[D_H / 8][4];
+#pragma unroll
+        for (int n = 0; n < D_H / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        float accz[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) accz[i] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+        // After an expired wait every consumer keeps walking its loops (so all of
+        // them still meet at the named barriers) but skips the work.
+        for (int j = grp; sp.g0 + j < sp.g1; j += a.ng) {
+            const int kk = kbase + j;
+            const int slot = kk % nslot;
+            if (*abort_flag) continue;
+            // Groups run at different speeds, so the slot may still hold a stage one or
+            // more ring rounds older than kk; its barrier parity alone cannot tell them
+            // apart.  Wait until stage kk has been issued into the slot, then for its data.
+            if (!wait_tag(tag + slot, kk, a.status) ||
+                !mbar_wait(smem_u32(&full[slot]), (kk / nslot) & 1, a.status)) {
+                *abort_flag = 1;
+                continue;
+            }
+            const int t0 = (sp.g0 + j) * kGran;
+            const int nvalid = meta[slot] ? min(kGran, L - t0) : 0;
+            const uint32_t st = smem_s + slot * stage_bytes;
+            const uint32_t sK_s = st, sV_s = st + 16 * D_H;
+            const uint8_t* zK_p = smem + slot * stage_bytes + 32 * D_H;
+            const uint8_t* zV_p = zK_p + 16 * H * R;
+
+            // --- shared logits q . s^K (tensor cores): 16 heads x 8 tokens
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk2 = 0; kk2 < D_H / 16; kk2 += 2) {
+                const int chunk16 = kk2 * 2 + (lane >> 3);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(sw128(sK_s + (chunk16 >> 3) * 1024, lane & 7, chunk16 & 7), b0, b1, b2, b3);
+                mma_16816(c, qa[kk2], b0, b1);
+                mma_16816(c, qa[kk2 + 1], b2, b3);
+            }
+
+            // --- residual logits q~ . z^K (CUDA cores): lane = (head hz, tokens half*4 .. +3)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = half * 4 + i;
+                float acc = 0.f;
+                if (hz_ok && t < nvalid) {
+                    const uint4* row = reinterpret_cast<const uint4*>(zK_p + ((size_t)t * H + hzh) * R * 2);
+#pragma unroll
+                    for (int cc = 0; cc < NC; ++cc) {
+                        const uint4 v = row[(cc + rot) % NC];
+                        acc = fmaf(qt[cc * 8 + 0], bf16lo(v.x), acc);
+                        acc = fmaf(qt[cc * 8 + 1], bf16hi(v.x), acc);
+                        acc = fmaf(qt[cc * 8 + 2], bf16lo(v.y), acc);
+                        acc = fmaf(qt[cc * 8 + 3], bf16hi(v.y), acc);
+                        acc = fmaf(qt[cc * 8 + 4], bf16lo(v.z), acc);
+                        acc = fmaf(qt[cc * 8 + 5], bf16hi(v.z), acc);
+                        acc = fmaf(qt[cc * 8 + 6], bf16lo(v.w), acc);
+                        acc = fmaf(qt[cc * 8 + 7], bf16hi(v.w), acc);
+                    }
+                }
+                SZ[hz * 8 + t] = acc;
+            }
+            __syncwarp();
+
+            // --- scores, mask, online softmax (rows hA: c0,c1; hB: c2,c3; tokens 2tq, 2tq+1)
+            const int ta = 2 * tq, tb = 2 * tq + 1;
+            float s0 = (ta < nvalid) ? (c[0] + SZ[g * 8 + ta]) * a.scale_log2 : -INFINITY;
+            float s1 = (tb < nvalid) ? (c[1] + SZ[g * 8 + tb]) * a.scale_log2 : -INFINITY;
+            float s2 = (ta < nvalid) ? (c[2] + SZ[(g + 8) * 8 + ta]) * a.scale_log2 : -INFINITY;
+            float s3 = (tb < nvalid) ? (c[3] + SZ[(g + 8) * 8 + tb]) * a.scale_log2 : -INFINITY;
+            float mx0 = fmaxf(s0, s1), mx1 = fmaxf(s2, s3);
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
+            const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
+            const float p0 = (mn0 == -INFINITY) ? 0.f : exp2f(s0 - mn0);
+            const float p1 = (mn0 == -INFINITY) ? 0.f : exp2f(s1 - mn0);
+            const float p2 = (mn1 == -INFINITY) ? 0.f : exp2f(s2 - mn1);
+            const float p3 = (mn1 == -INFINITY) ? 0.f : exp2f(s3 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            l0 = l0 * al0 + p0 + p1;
+            l1 = l1 * al1 + p2 + p3;
+#pragma unroll
+            for (int n = 0; n < D_H / 8; ++n) {
+                o[n][0] *= al0;
+                o[n][1] *= al0;
+                o[n][2] *= al1;
+                o[n][3] *= al1;
+            }
+            SP[g * 8 + ta] = p0;
+            SP[g * 8 + tb] = p1;
+            SP[(g + 8) * 8 + ta] = p2;
+            SP[(g + 8) * 8 + tb] = p3;
+            if (tq == 0) {
+                SA[g] = al0;
+                SA[g + 8] = al1;
+            }
+            __syncwarp();
+
+            // --- residual values p . z^V (CUDA cores)
+            {
+                const float al = SA[hz];
+#pragma unroll
+                for (int i = 0; i < R; ++i) accz[i] *= al;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = half * 4 + i;
+                    if (hz_ok && t < nvalid) {
+                        const float p = SP[hz * 8 + t];
+                        const uint4* row = reinterpret_cast<const uint4*>(zV_p + ((size_t)t * H + hzh) * R * 2);
+#pragma unroll
+                        for (int cc = 0; cc < NC; ++cc) {
+                            const uint4 v = row[(cc + rot) % NC];
+                            accz[cc * 8 + 0] = fmaf(p, bf16lo(v.x), accz[cc * 8 + 0]);
+                            accz[cc * 8 + 1] = fmaf(p, bf16hi(v.x), accz[cc * 8 + 1]);
+                            accz[cc * 8 + 2] = fmaf(p, bf16lo(v.y), accz[cc * 8 + 2]);
+                            accz[cc * 8 + 3] = fmaf(p, bf16hi(v.y), accz[cc * 8 + 3]);
+                            accz[cc * 8 + 4] = fmaf(p, bf16lo(v.z), accz[cc * 8 + 4]);
+                            accz[cc * 8 + 5] = fmaf(p, bf16hi(v.z), accz[cc * 8 + 5]);
+                            accz[cc * 8 + 6] = fmaf(p, bf16lo(v.w), accz[cc * 8 + 6]);
+                            accz[cc * 8 + 7] = fmaf(p, bf16hi(v.w), accz[cc * 8 + 7]);
+                        }
+                    }
+                }
+            }
+
+            // --- shared values p . s^V (tensor cores): P (16 heads x 8 tokens) . s^V (8 tokens x D_H)
+            {
+                const uint32_t pa0 = pack_bf16x2(p0, p1), pa1 = pack_bf16x2(p2, p3);
+                const uint32_t mlo = (ta < nvalid) ? 0x0000ffffu : 0u;
+                const uint32_t mhi = (tb < nvalid) ? 0xffff0000u : 0u;
+                const uint32_t msk = mlo | mhi;  // zero s^V of masked tokens (0 * NaN guard)
+#pragma unroll
+                for (int q4 = 0; q4 < D_H / 32; ++q4) {
+                    const int chunk16 = q4 * 4 + (lane >> 3);
+                    uint32_t v0, v1, v2, v3;
+                    ldmatrix_x4_trans(sw128(sV_s + (chunk16 >> 3) * 1024, lane & 7, chunk16 & 7), v0, v1, v2, v3);
+                    mma_1688(o[q4 * 4 + 0], pa0, pa1, v0 & msk);
+                    mma_1688(o[q4 * 4 + 1], pa0, pa1, v1 & msk);
+                    mma_1688(o[q4 * 4 + 2], pa0, pa1, v2 & msk);
+                    mma_1688(o[q4 * 4 + 3], pa0, pa1, v3 & msk);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                // Release; the last of the HT warps reading this stage refills the slot
+                // with the stage nslot positions ahead in this split.
+                __threadfence_block();
+                if (atomicAdd(&rel[slot], 1) == HT - 1) {
+                    rel[slot] = 0;
+                    __threadfence_block();
+                    const int jn = j + nslot;
+                    if (jn < sp.g1 - sp.g0 && !*abort_flag) {
+                        tag[slot] = kk + nslot;
+                        issue_stage<D_H, R>(&tm_sK, &tm_sV, a, st, smem_u32(&full[slot]), &meta[slot], b,
+                                            sp.g0 + jn, pol);
+                        ++nissued[slot];
+                    }
+                }
+            }
+        }
+        kbase += sp.g1 - sp.g0;
+
+        // --- write this group's partial for split s
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        const size_t P = (size_t)s * a.ng + grp;
+        const int W = D_H + R;
+        if (tq == 0) {
+            if (hA < H) *reinterpret_cast<float2*>(a.part_ml + (P * H + hA) * 2) = make_float2(m0, l0);
+            if (hB < H) *reinterpret_cast<float2*>(a.part_ml + (P * H + hB) * 2) = make_float2(m1, l1);
+        }
+#pragma unroll
+        for (int n = 0; n < D_H / 8; ++n) {
+            const int dcol = n * 8 + 2 * tq;
+            if (hA < H) *reinterpret_cast<float2*>(a.part_acc + (P * H + hA) * W + dcol) = make_float2(o[n][0], o[n][1]);
+            if (hB < H) *reinterpret_cast<float2*>(a.part_acc + (P * H + hB) * W + dcol) = make_float2(o[n][2], o[n][3]);
+        }
+#pragma unroll
+        for (int i = 0; i < R; ++i) accz[i] += __shfl_xor_sync(0xffffffffu, accz[i], 16);
+        if (half == 0 && hz_ok) {
+            float* dst = a.part_acc + (P * H + hzh) * W + D_H;
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) {
+                float4* d4 = reinterpret_cast<float4*>(dst + ((cc + rot) % NC) * 8);
+                d4[0] = make_float4(accz[cc * 8 + 0], accz[cc * 8 + 1], accz[cc * 8 + 2], accz[cc * 8 + 3]);
+                d4[1] = make_float4(accz[cc * 8 + 4], accz[cc * 8 + 5], accz[cc * 8 + 6], accz[cc * 8 + 7]);
+            }
+        }
+    }
+    // After an expired wait, make sure no copy is still landing in shared memory
+    // before the CTA exits: wait (bounded) for the last phase issued into each slot.
+    named_bar(1, nct);
+    if (threadIdx.x == 0 && *abort_flag)
+        for (int sl = 0; sl < nslot; ++sl)
+            if (nissued[sl] > 0) mbar_wait(smem_u32(&full[sl]), (nissued[sl] - 1) & 1, a.status);
+}
+
+// Log-sum-exp merge of a sequence's partials, residual up-projection, bf16 store.
+// grid (H, B), block D_H threads.
+template <int D_H, int R>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a, int G) {
+    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    const int H = a.H;
+    const int cap = a.max_pages * kBlockSize;
+    __shared__ float zs[R];
+    uint16_t* dst = a.out + ((size_t)b * H + h) * D_H;
+    const int L = a.seq_lens[b];
+    if (L < 1 || L > cap) {
+        if (tid == 0 && h == 0) set_status(a.status, LRKV_DEV_BAD_SEQLEN);
+        dst[tid] = 0;
+        return;
+    }
+    int nsplits;
+    const int chunk = partition_chunk(a.seq_lens, a.B, cap, G, &nsplits);
+    int first, count;
+    seq_splits(a.seq_lens, a.B, cap, chunk, b, &first, &count);
+    const size_t p0 = (size_t)first * a.ng;
+    const int np = count * a.ng;
+    const int W = D_H + R;
+
+    float M = -INFINITY;
+    for (int p = 0; p < np; ++p) M = fmaxf(M, a.part_ml[((p0 + p) * H + h) * 2]);
+    float lsum = 0.f, acc0 = 0.f, acc1 = 0.f;
+    for (int p = 0; p < np; ++p) {
+        const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + ((p0 + p) * H + h) * 2);
+        const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+        lsum = fmaf(w, ml.y, lsum);
+        const float* pa = a.part_acc + ((p0 + p) * H + h) * W;
+        acc0 = fmaf(w, pa[tid], acc0);
+        if (tid < R) acc1 = fmaf(w, pa[D_H + tid], acc1);
+    }
+    if (tid < R) zs[tid] = acc1;
+    __syncthreads();
+    float v = acc0;
+    const uint16_t* bv = a.BV + ((size_t)h * D_H + tid) * R;
+#pragma unroll
+    for (int j = 0; j < R; ++j) v = fmaf(__uint_as_float((uint32_t)bv[j] << 16), zs[j], v);
+    v = lsum > 0.f ? v / lsum : 0.f;
+    __nv_bfloat16 o = __float2bfloat16_rn(v);
+    dst[tid] = *reinterpret_cast<uint16_t*>(&o);
+}
+
+// ------------------------------------------------------------------ host side
+struct DecodePlan {
+    int ng, nslot, stage_bytes, smem_bytes, threads;
+};
+
+static int decode_fixed_smem(int H, int R, int ncw, int nslot) {
+    return nslot * 8 + ((4 * nslot + 3) & ~3) * 4 + H * R * 4 + ncw * kScratchFloats * 4 + 16 + 1024;
+}
+
+DecodePlan decode_plan(int H, int D_H, int R, int smem_limit) {
+    DecodePlan p{};
+    const int HT = (H + 15) / 16;
+    p.stage_bytes = ((32 * D_H + 32 * H * R) + 1023) & ~1023;
+    int nslot = 16;
+    while (nslot > 2 && nslot * p.stage_bytes + decode_fixed_smem(H, R, 8, nslot) > smem_limit) --nslot;
+    p.nslot = nslot;
+    int ng = max(1, min(8 / HT, nslot - 2));
+    p.ng = ng;
+    p.threads = 32 * HT * ng;
+    p.smem_bytes = nslot * p.stage_bytes + decode_fixed_smem(H, R, HT * ng, nslot);
+    return p;
+}
+
+size_t decode_workspace_bytes(int H, int D_H, int R, int B, int G, int smem_limit) {
+    const DecodePlan p = decode_plan(H, D_H, R, smem_limit);
+    const size_t pmax = (size_t)max(G, B) * p.ng;
+    const size_t ml_bytes = (pmax * H * 2 * sizeof(float) + 255) & ~(size_t)255;
+    return ml_bytes + pmax * H * (D_H + R) * sizeof(float);
+}
+
+void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int B, int G, int smem_limit) {
+    const DecodePlan p = decode_plan(H, D_H, R, smem_limit);
+    const size_t pmax = (size_t)max(G, B) * p.ng;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    a->part_ml = reinterpret_cast<float*>(base);
+    const size_t ml_bytes = (pmax * H * 2 * sizeof(float) + 255) & ~(size_t)255;
+    a->part_acc = reinterpret_cast<float*>(base + ml_bytes);
+}
+
+template <int D_H, int R>
+static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, const DecodePlan& p,
+                                   int G, cudaStream_t stream) {
+    auto kern = decode_split_kernel<D_H, R>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<G, p.threads, p.smem_bytes, stream>>>(tK, tV, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_combine_kernel<D_H, R><<<dim3(a.H, a.B), D_H, 0, stream>>>(a, G);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int G,
+                          int smem_limit, cudaStream_t stream) {
+    const DecodePlan p = decode_plan(a.H, D_H, R, smem_limit);
+    a.ng = p.ng;
+    a.nslot = p.nslot;
+    a.stage_bytes = p.stage_bytes;
+#define LRKV_DEC(DH, RR) \
+    if (D_H == DH && R == RR) return launch_decode_t<DH, RR>(tK, tV, a, p, G, stream);
+    LRKV_DEC(64, 8) LRKV_DEC(64, 16) LRKV_DEC(64, 32) LRKV_DEC(128, 8) LRKV_DEC(128, 16) LRKV_DEC(128, 32)
+#undef LRKV_DEC
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace lrkv

@@ -1,0 +1,64 @@
+// kernels.h -- argument blocks and launchers shared between the C-ABI layer
+// (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lrkv {
+
+struct AppendArgs {
+    const uint16_t* X;      // [n][d]
+    const uint16_t* W;      // [N][d]
+    const int32_t* slots;   // [n]
+    uint16_t *sK, *sV, *zK, *zV;
+    uint32_t* status;
+    int n, d, N, d_h, HR;
+    long long nslots;       // num_blocks * block_size
+};
+
+struct DecodeArgs {
+    const uint16_t* q;     // [B][H][D_H]
+    const uint16_t* BK;    // [H][D_H][R]
+    const uint16_t* BV;    // [H][D_H][R]
+    const uint16_t* zK;    // [nb*64][H][R]
+    const uint16_t* zV;
+    const int32_t* block_table;  // [B][max_pages]
+    const int32_t* seq_lens;     // [B]
+    float* part_ml;   // [Pmax][H][2]  running max (log2 domain) and sum
+    float* part_acc;  // [Pmax][H][D_H + R]
+    uint32_t* status;
+    uint16_t* out;    // [B][H][D_H]
+    int B, H, max_pages, num_blocks;
+    int ng, nslot, stage_bytes;
+    float scale_log2;  // softmax scale * log2(e)
+};
+
+struct PrefillArgs {
+    const uint16_t *q, *BK, *BV;        // q [B][Tq][H][D_H]; B* [H][D_H][R]
+    const uint16_t *sK, *sV, *zK, *zV;  // cache pools
+    const int32_t* block_table;         // [B][max_pages]
+    const int32_t* q_start;             // [B]
+    uint32_t* status;
+    uint16_t* out;                      // [B][Tq][H][D_H]
+    int B, Tq, H, max_pages, num_blocks;
+    float scale_log2;
+};
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+// Tensor-core path (rows >= kAppendTcMinRows): X and W_cat^T tensor maps with a
+// {64, 128} and {64, append_tc_block_n(N)} box, 128-byte swizzle.
+constexpr int kAppendTcMinRows = 64;
+int append_tc_block_n(int N);
+cudaError_t launch_append_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const AppendArgs& a,
+                             cudaStream_t stream);
+
+size_t decode_workspace_bytes(int H, int D_H, int R, int B, int G, int smem_limit);
+void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int B, int G, int smem_limit);
+cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int G,
+                          int smem_limit, cudaStream_t stream);
+
+cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, cudaStream_t stream);
+
+}  // namespace lrkv

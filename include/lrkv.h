@@ -1,0 +1,165 @@
+/*
+ * lrkv.h -- C ABI of the GB300 (sm_103a) library for attention over an
+ * LRKV-compressed KV cache.
+ *
+ * The method ("Low-Rank Key Value Attention", O'Neill, Clancy, Matskevichus,
+ * Reid, arXiv:2601.11471v3; slide deck of the same title):
+ *   each head's key/value projection is W_h = W_shared + U_h B_h^T
+ *   (Eqs. (2)-(3), frame "LRKV constrains differences between heads"), so per
+ *   token and layer the cache holds a shared d_h-vector s plus one r-vector z_h
+ *   per head, for keys and for values: 2(d_h + H r) elements (frame "Can heads
+ *   share storage while keeping distinct K/V features?").  Decode never expands
+ *   per-head keys or values; it evaluates the factored forms of Eqs. (6)-(7).
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are bf16 (IEEE binary16 brain-float bit patterns, uint16 in
+ *     memory) unless stated, row-major, in DEVICE memory owned by the caller.
+ *     The library allocates nothing and keeps no state between calls.
+ *   - Every pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous: they validate on the host, enqueue kernels and return.
+ *   - Host-detectable errors are returned before anything is launched; the
+ *     calling thread can then read a one-line explanation from
+ *     lrkv_last_error().  A launch failure returns LRKV_ERR_CUDA.
+ *   - Errors only the device can see (an index read from device memory that is
+ *     out of range, a bounded wait that expired) are OR-ed into the optional
+ *     uint32 word `status_dev` (device memory, may be NULL) as LRKV_DEV_* bits;
+ *     the offending access is skipped, never trapped.  Read the word after
+ *     synchronising the stream.
+ *   - Cache pages: the pools are indexed by physical block id b in
+ *     [0, num_blocks); token slot = b * block_size + offset.
+ *        sK, sV : [num_blocks][block_size][d_h]
+ *        zK, zV : [num_blocks][block_size][H][r]
+ *     (s = shared features K_s, V_s of Eq. (4); z_h = per-head latents R_h^K,
+ *     R_h^V of Eq. (5).)  B_h^K, B_h^V are weights, not cache entries.
+ *
+ * Supported shapes (others return LRKV_ERR_UNSUPPORTED):
+ *   block_size == 64, d_h in {64, 128}, r in {8, 16, 32, 64} with r <= d_h,
+ *   1 <= H <= 128, d a positive multiple of 8 (of 64 for the tensor-core append).
+ */
+#ifndef LRKV_H
+#define LRKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LRKV_ABI_VERSION 1
+
+typedef enum lrkv_status {
+    LRKV_OK = 0,
+    LRKV_ERR_INVALID_ARG = 1,   /* NULL or misaligned pointer, negative size, inconsistent arguments */
+    LRKV_ERR_UNSUPPORTED = 2,   /* shape outside the supported set above */
+    LRKV_ERR_WORKSPACE = 3,     /* workspace smaller than the *_workspace_bytes() figure */
+    LRKV_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    LRKV_ERR_DEVICE_BOUNDS = 5, /* meaning of the LRKV_DEV_BAD_* bits, for lrkv_status_string */
+    LRKV_ERR_TIMEOUT = 6        /* meaning of the LRKV_DEV_TIMEOUT bit, for lrkv_status_string */
+} lrkv_status;
+
+/* Bits kernels OR into *status_dev. */
+#define LRKV_DEV_BAD_BLOCK 0x1u  /* a block_table entry needed by a call is outside [0, num_blocks) */
+#define LRKV_DEV_BAD_SEQLEN 0x2u /* seq_len / q_start + Tq outside [1, max_blocks_per_seq * block_size]; that
+                                    sequence's output rows are written as zeros */
+#define LRKV_DEV_BAD_SLOT 0x4u   /* slot_mapping entry >= num_blocks * block_size (row skipped) */
+#define LRKV_DEV_TIMEOUT 0x8u    /* a pipeline wait in a kernel gave up after its time limit (about 2 s) */
+
+/* Model dimensions (frame "LRKV constrains differences between heads"). */
+typedef struct lrkv_dims {
+    int32_t H;           /* query heads */
+    int32_t d_h;         /* head width */
+    int32_t r;           /* residual rank of U_h B_h^T */
+    int32_t d;           /* hidden size of the rows appended to the cache */
+    int32_t block_size;  /* tokens per cache page; must be 64 */
+    float softmax_scale; /* logit scale; 0 means 1/sqrt(d_h) (frame "Compute logits ...") */
+} lrkv_dims;
+
+/* One layer's paged cache (device pointers, caller-owned, layout above). */
+typedef struct lrkv_cache {
+    void* sK;
+    void* sV;
+    void* zK;
+    void* zV;
+    int32_t num_blocks;
+} lrkv_cache;
+
+/* ABI version of the loaded library (LRKV_ABI_VERSION it was built with). */
+int lrkv_abi_version(void);
+
+/* Static description of a status code. */
+const char* lrkv_status_string(lrkv_status s);
+
+/* Explanation of the last non-OK status returned on the calling thread ("" if none). */
+const char* lrkv_last_error(void);
+
+/* Bytes of one cache page across the four pools: block_size * 2 * 2(d_h + H r).
+ * Returns 0 for unsupported dims. */
+size_t lrkv_cache_block_bytes(const lrkv_dims* dims);
+
+/*
+ * lrkv_append -- Eqs. (4)-(5): project n_tok hidden rows into the cache.
+ *   Y = X W_cat, W_cat = [W_shared^K | W_shared^V | U_1^K .. U_H^K | U_1^V .. U_H^V]
+ *   (d x N, N = 2(d_h + H r)), accumulated in fp32 and rounded to bf16
+ *   (nearest, ties to even); row t is written to token slot slot_mapping[t]:
+ *   columns [0,d_h) -> sK, [d_h,2d_h) -> sV, the next H r -> zK (head-major),
+ *   the last H r -> zV.
+ *   X            [n_tok][d]
+ *   W_catT       [N][d]  (W_cat transposed: row c holds the weights of output column c)
+ *   slot_mapping [n_tok] int32 (device); a negative entry skips the row,
+ *                an entry >= num_blocks*block_size sets LRKV_DEV_BAD_SLOT and skips it.
+ *   n_tok == 0 is a no-op.  Small n_tok runs a bandwidth-bound kernel, large n_tok a
+ *   tcgen05 tensor-core GEMM; both give bit-identical results whenever every fp32
+ *   partial sum is exact.
+ */
+lrkv_status lrkv_append(const lrkv_dims* dims, const void* X, const void* W_catT, int32_t n_tok,
+                        const int32_t* slot_mapping, const lrkv_cache* cache, uint32_t* status_dev,
+                        void* stream);
+
+/* Workspace bytes lrkv_decode needs for `batch` sequences on the CURRENT device. */
+size_t lrkv_decode_workspace_bytes(const lrkv_dims* dims, int32_t batch);
+
+/*
+ * lrkv_decode -- one decode step per sequence, factored form (Eqs. (6)-(7)):
+ *   q~_h = q_h B_h^K;  score_t = (q_h . s^K_t + q~_h . z^K_{h,t}) * scale;
+ *   a_h = softmax_t(score);  out_h = a_h V_s + (a_h R_h^V) (B_h^V)^T.
+ *   The query attends to all seq_lens[b] cached tokens (positions 0..L-1; it is
+ *   the newest position and is already in the cache).  Split over the sequence
+ *   across the GPU's SMs, merged by log-sum-exp in a second kernel.
+ *   q           [batch][H][d_h]
+ *   BK, BV      [H][d_h][r]  (B_h^K, B_h^V)
+ *   block_table [batch][max_blocks_per_seq] int32 (device)
+ *   seq_lens    [batch] int32 (device)
+ *   out         [batch][H][d_h]
+ *   workspace   device scratch of >= lrkv_decode_workspace_bytes(dims, batch) bytes, 256-byte aligned.
+ */
+lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, const void* BV,
+                        const lrkv_cache* cache, const int32_t* block_table, int32_t max_blocks_per_seq,
+                        const int32_t* seq_lens, int32_t batch, void* out, void* workspace,
+                        size_t workspace_bytes, uint32_t* status_dev, void* stream);
+
+/* Workspace bytes lrkv_prefill needs (0 today; kept so callers size it). */
+size_t lrkv_prefill_workspace_bytes(const lrkv_dims* dims, int32_t batch, int32_t Tq);
+
+/*
+ * lrkv_prefill -- causal chunked prefill over the cache (Eqs. (6)-(7) with the
+ *   causal mask of the softmax frame): query i of sequence b sits at absolute
+ *   position p = q_start[b] + i and attends to cached tokens j <= p.  The chunk's
+ *   own rows must already be in the cache (lrkv_append first).
+ *   Logits use the concatenated width d_h + r: [q | q~] . [s^K | z^K_h]; the
+ *   scale stays 1/sqrt(d_h) (the dot product is the same one).
+ *   q        [batch][Tq][H][d_h]
+ *   q_start  [batch] int32 (device)
+ *   out      [batch][Tq][H][d_h]
+ */
+lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, const void* BV,
+                         const lrkv_cache* cache, const int32_t* block_table, int32_t max_blocks_per_seq,
+                         const int32_t* q_start, int32_t batch, int32_t Tq, void* out, void* workspace,
+                         size_t workspace_bytes, uint32_t* status_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LRKV_H */

@@ -1,0 +1,86 @@
+"""C-ABI surface (no GPU needed): the library builds, loads, exports every entry
+point include/lrkv.h declares, and rejects bad host arguments before launching."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from compressed_kv_cache_lrkv_gb300 import binding as b
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lrkv.h")
+
+
+def _declared():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(lrkv_[a-z_]+)\s*\(", txt)))
+
+
+def test_header_declares_expected_calls():
+    names = _declared()
+    for n in ("lrkv_append", "lrkv_decode", "lrkv_prefill", "lrkv_decode_workspace_bytes", "lrkv_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = b.load()
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) <= set(b.EXPORTED) | set(_declared())
+    assert b.abi_version() == 1
+
+
+def test_status_strings():
+    lib = b.load()
+    for code in range(7):
+        assert lib.lrkv_status_string(code)
+    assert lib.lrkv_status_string(99) == b"unknown status"
+
+
+def test_cache_block_bytes_matches_accounting():
+    from compressed_kv_cache_lrkv_gb300 import accounting as A
+    for H, d_h, r in [(8, 64, 8), (8, 64, 16), (128, 128, 16), (32, 128, 32), (32, 128, 16)]:
+        assert b.cache_block_bytes(b.make_dims(H, d_h, r, H * d_h)) == A.page_bytes(H, d_h, r)
+
+
+@pytest.mark.parametrize("H,d_h,r,d,bs,why", [
+    (8, 96, 8, 512, 64, "d_h"), (8, 64, 12, 512, 64, "r"), (8, 64, 128, 512, 64, "r > d_h"),
+    (0, 64, 8, 512, 64, "H"), (129, 64, 8, 512, 64, "H"), (8, 64, 8, 500, 64, "d"), (8, 64, 8, 512, 32, "block"),
+])
+def test_unsupported_dims_rejected(H, d_h, r, d, bs, why):
+    dims = b.make_dims(H, d_h, r, d, bs)
+    assert b.cache_block_bytes(dims) == 0, why
+    lib = b.load()
+    c = b.Cache(16, 16, 16, 16, 1)
+    rc = lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, ctypes.byref(c), None, None)
+    assert rc == 2, lib.lrkv_last_error()
+
+
+def test_null_and_misaligned_pointers_rejected():
+    lib = b.load()
+    dims = b.make_dims(8, 64, 8, 512)
+    c = b.Cache(16, 16, 16, 16, 1)
+    assert lib.lrkv_append(ctypes.byref(dims), None, 16, 1, 16, ctypes.byref(c), None, None) == 1
+    assert b"X is NULL" in lib.lrkv_last_error()
+    assert lib.lrkv_append(ctypes.byref(dims), 24, 16, 1, 16, ctypes.byref(c), None, None) == 1
+    assert b"aligned" in lib.lrkv_last_error()
+    bad = b.Cache(16, 0, 16, 16, 1)
+    assert lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, ctypes.byref(bad), None, None) == 1
+    bad = b.Cache(16, 16, 16, 16, 0)
+    assert lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, ctypes.byref(bad), None, None) == 1
+    assert lib.lrkv_append(ctypes.byref(dims), 16, 16, -1, 16, ctypes.byref(c), None, None) == 1
+    # zero rows / zero batch are no-ops that succeed without touching the device
+    assert lib.lrkv_append(ctypes.byref(dims), None, None, 0, None, ctypes.byref(c), None, None) == 0
+    assert lib.lrkv_decode(ctypes.byref(dims), 16, 16, 16, ctypes.byref(c), 16, 1, 16, 0, 16, 256, 0, None,
+                           None) == 0
+    assert lib.lrkv_decode(ctypes.byref(dims), 16, 16, 16, ctypes.byref(c), 16, 0, 16, 1, 16, 256, 0, None,
+                           None) == 1
+    assert lib.lrkv_prefill(ctypes.byref(dims), 16, 16, 16, ctypes.byref(c), 16, 1, 16, 1, -3, 16, None, 0, None,
+                            None) == 1
+
+
+def test_nan_scale_rejected():
+    lib = b.load()
+    dims = b.make_dims(8, 64, 8, 512, softmax_scale=float("nan"))
+    assert b.cache_block_bytes(dims) == 0

@@ -1,0 +1,115 @@
+"""lrkv_append on the GPU against the oracle's reference rounding (Eqs. (4)-(5))."""
+import numpy as np
+import pytest
+import torch
+
+import lrkv_synth as S
+import oracle
+from cases import Weights, empty_pools, f64, pack_wcat_t, weights
+from gpu_util import dev_bf16, dev_i32, host_bits
+
+pytestmark = pytest.mark.gpu
+
+from compressed_kv_cache_lrkv_gb300 import binding as b  # noqa: E402
+
+CANARY = 0x7E57
+
+
+def run_append(H, d_h, r, d, X, w, slots, num_blocks, status=None):
+    dims = b.make_dims(H, d_h, r, d)
+    cache = b.PagedCache(*(dev_bf16(p) for p in empty_pools(num_blocks, H, d_h, r, fill=CANARY)))
+    st = status if status is not None else torch.zeros(1, dtype=torch.int32, device="cuda")
+    b.lrkv_append(dims, dev_bf16(X), dev_bf16(pack_wcat_t(w)), dev_i32(slots), cache, status=st)
+    torch.cuda.synchronize()
+    return tuple(host_bits(t) for t in cache.tensors()), int(st.item())
+
+
+def oracle_pools(H, d_h, r, X, w, slots, num_blocks):
+    pools = empty_pools(num_blocks, H, d_h, r, fill=CANARY)
+    keep = np.asarray(slots) >= 0
+    rows = oracle.get().append(X[keep], w.WsK, w.WsV, w.UK, w.UV)
+    oracle.scatter_rows(pools, np.asarray(slots)[keep], rows)
+    return pools
+
+
+def int_weights(seed, d, d_h, H, r, lo=-8, hi=8):
+    g = lambda nm, sh: S.int_grid_bf16(seed, nm, sh, lo, hi)
+    return Weights(g("a", (d, d_h)), g("b", (d, d_h)), g("c", (H, d, r)), g("e", (H, d, r)),
+                   g("f", (H, d_h, r)), g("g", (H, d_h, r)))
+
+
+@pytest.mark.parametrize("n", [1, 3, 4, 9, 16, 33, 64, 200, 1000])
+@pytest.mark.parametrize("H,d_h,r,d", [(8, 64, 8, 512), (32, 128, 32, 1024), (5, 128, 16, 264)])
+def test_append_bit_exact_on_exact_inputs(n, H, d_h, r, d):
+    """Integer-grid inputs: every fp32 partial sum is exact, so any summation order
+    gives the same value and the cache must match the reference bit for bit."""
+    X = S.int_grid_bf16(n, "X", (n, d), -8, 8)
+    w = int_weights(n + H, d, d_h, H, r)
+    nb = (n + 63) // 64 + 2
+    slots = S.permutation(n, "slots", nb * 64)[:n].astype(np.int32)
+    got, st = run_append(H, d_h, r, d, X, w, slots, nb)
+    ref = oracle_pools(H, d_h, r, X, w, slots, nb)
+    assert st == 0
+    for g_, r_, nm in zip(got, ref, ("sK", "sV", "zK", "zV")):
+        np.testing.assert_array_equal(g_, r_, err_msg=nm)
+
+
+def _bf16_ulp(x):
+    x = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+@pytest.mark.parametrize("n,H,d_h,r,d", [(5, 8, 64, 16, 512), (64, 32, 128, 32, 4096), (300, 8, 64, 8, 512),
+                                         (1000, 32, 128, 16, 4096)])
+def test_append_gaussian_within_accumulation_bound(n, H, d_h, r, d):
+    """Gaussian inputs: fp32 accumulation in any order lies within the standard
+    summation bound K u sum_k |x_k w_k| (u = 2^-24) of the exact sum, and each side
+    then rounds once to bf16; so |gpu - ref| <= 1 ulp(ref) + 2 K u sum|x w|.
+    Most elements are bit-identical; the rest are counted."""
+    X = S.gaussian_bf16(n, "X", (n, d))
+    w = weights(n, d, d_h, H, r)
+    nb = (n + 63) // 64 + 1
+    slots = np.arange(n, dtype=np.int32)
+    got, st = run_append(H, d_h, r, d, X, w, slots, nb)
+    ref = oracle_pools(H, d_h, r, X, w, slots, nb)
+    ax = np.abs(f64(X))
+    mags = [ax @ np.abs(f64(w.WsK)), ax @ np.abs(f64(w.WsV)),
+            np.stack([ax @ np.abs(f64(w.UK[h])) for h in range(H)], 1),
+            np.stack([ax @ np.abs(f64(w.UV[h])) for h in range(H)], 1)]
+    for g_, r_, mag, nm in zip(got, ref, mags, ("sK", "sV", "zK", "zV")):
+        gv = f64(g_.reshape(-1, *g_.shape[2:])[:n])
+        rv = f64(r_.reshape(-1, *r_.shape[2:])[:n])
+        bound = _bf16_ulp(rv) + 2 * d * 2.0 ** -24 * mag
+        assert np.all(np.abs(gv - rv) <= bound), nm
+        assert (gv != rv).mean() < 2e-2, nm
+
+
+@pytest.mark.parametrize("n", [6, 100])
+def test_append_slot_rules(n):
+    """Negative slots are skipped silently, out-of-range slots set the status bit and
+    are skipped; every other slot keeps its previous contents (both the row-wise and
+    the tensor-core path)."""
+    H, d_h, r, d = 8, 64, 8, 512
+    nb = 3
+    X = S.gaussian_bf16(3, "X", (n, d))
+    w = weights(3, d, d_h, H, r)
+    slots = S.permutation(4, "slots", nb * 64)[:n].astype(np.int32)
+    slots[1] = -1
+    slots[3] = nb * 64 + 3
+    slots[n - 1] = -7
+    got, st = run_append(H, d_h, r, d, X, w, slots, nb)
+    assert st == b.DEV_BAD_SLOT
+    keep = (slots >= 0) & (slots < nb * 64)
+    ok = slots[keep]
+    rows = oracle.get().append(X[keep], w.WsK, w.WsV, w.UK, w.UV)
+    ax = np.abs(f64(X[keep]))
+    mags = [ax @ np.abs(f64(w.WsK)), ax @ np.abs(f64(w.WsV)),
+            np.stack([ax @ np.abs(f64(w.UK[h])) for h in range(H)], 1),
+            np.stack([ax @ np.abs(f64(w.UV[h])) for h in range(H)], 1)]
+    for g_, row, mag in zip(got, rows, mags):
+        flat = g_.reshape((-1,) + g_.shape[2:])
+        rv = f64(row)
+        assert np.all(np.abs(f64(flat[ok]) - rv) <= _bf16_ulp(rv) + 2 * d * 2.0 ** -24 * mag)
+        untouched = np.setdiff1d(np.arange(nb * 64), ok)
+        assert np.all(flat[untouched] == CANARY)
