@@ -112,6 +112,11 @@ lrkv_status cuda_status(cudaError_t e, const char* what) {
 
 }  // namespace
 
+namespace lrkv {
+// Lets entry points defined in other translation units report through lrkv_last_error().
+lrkv_status report_error(lrkv_status s, const char* msg) { return fail(s, "%s", msg); }
+}  // namespace lrkv
+
 extern "C" {
 
 int lrkv_abi_version(void) { return LRKV_ABI_VERSION; }

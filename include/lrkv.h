@@ -139,6 +139,32 @@ lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, co
                         const int32_t* seq_lens, int32_t batch, void* out, void* workspace,
                         size_t workspace_bytes, uint32_t* status_dev, void* stream);
 
+/*
+ * lrkv_decode_static_ws -- lrkv_decode without a caller workspace.  (The paper has
+ *   no counterpart; this is a deployment convenience.)
+ *   For callers that cannot allocate device memory: cudaMalloc/cudaFree can
+ *   synchronise the whole device and stall other streams, some host frameworks
+ *   own the GPU allocator and forbid foreign allocations, and some deployments fix
+ *   their device-memory budget at start-up.  The scratch lives in a fixed array of
+ *   LRKV_STATIC_WS_BYTES inside the library's device image, which every GPU that
+ *   loads the library keeps until the process exits; this call allocates nothing.
+ *   Arguments, layouts and results are those of lrkv_decode.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Returns LRKV_ERR_WORKSPACE (explained by lrkv_last_error()) when
+ *     lrkv_decode_workspace_bytes(dims, batch) exceeds LRKV_STATIC_WS_BYTES.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents (nothing needs clearing: each call writes all scratch it reads).
+ *     Calls whose kernels overlap on the GPU -- e.g. on two streams at once --
+ *     race on it; serialise them.
+ */
+#define LRKV_STATIC_WS_BYTES ((size_t)16 << 20)
+lrkv_status lrkv_decode_static_ws(const lrkv_dims* dims, const void* q, const void* BK, const void* BV,
+                                  const lrkv_cache* cache, const int32_t* block_table, int32_t max_blocks_per_seq,
+                                  const int32_t* seq_lens, int32_t batch, void* out, uint32_t* status_dev,
+                                  void* stream);
+
 /* Workspace bytes lrkv_prefill needs (0 today; kept so callers size it). */
 size_t lrkv_prefill_workspace_bytes(const lrkv_dims* dims, int32_t batch, int32_t Tq);
 
