@@ -6,28 +6,31 @@
 //     out_h   = sum_t p_t s^V_t + B_h^V (sum_t p_t z^V_{h,t})       (Eq. (7))
 // Per-head K_h / V_h are never formed.
 //
-// Kernel 1 (split): a persistent grid of one CTA per SM.  The cached tokens of
-// all sequences are cut into 8-token granules and divided evenly into at most
-// one contiguous range ("split") per CTA.  A producer warp streams each
-// granule's s^K, s^V (TMA tensor loads, 128-byte swizzle) and z^K, z^V (bulk
-// copies) into a ring of shared-memory stages; each stage is read from HBM
-// once, for all H heads.  Consumer warps own 16 heads each; NG groups of
-// ceil(H/16) warps take stages round-robin, each keeping its own online
-// softmax state and writing one partial (m, l, acc_s[d_h], acc_z[r]) per head.
-//   - q . s^K and p . s^V run on the tensor cores (mma.sync m16n8k16 / m16n8k8,
-//     heads on M, tokens on N / K) -- s is shared by all heads of the CTA;
-//   - q~ . z^K and p . z^V run on CUDA cores in fp32 (each z element is used
-//     once; no reuse for a tensor core to exploit).
-// Kernel 2 (combine): log-sum-exp merge of the partials of each (b, h), then the
-// residual up-projection B_h^V acc_z and the bf16 store.
+// Kernel 0 (absorb): q~ for every (sequence, head) into the workspace, fp32.
+// Kernel 1 (split): a persistent grid of one CTA per SM, launched with
+//   programmatic dependent launch so it starts streaming while kernel 0 runs.
+//   The cached tokens of all sequences are cut into 8-token granules and divided
+//   evenly into at most one contiguous range ("split") per CTA.  Each granule's
+//   s^K, s^V (TMA tensor loads, 128-byte swizzle) and z^K, z^V (bulk copies) go
+//   into a ring of shared-memory stages, read from HBM once for all H heads.
+//   Consumer warps own 16 heads each; NG groups of ceil(H/16) warps take stages
+//   round-robin with their own online-softmax state, merged inside the CTA at
+//   the end of the split into one partial (m, l, acc_s[d_h], acc_z[r]) per head.
+//     - q . s^K and p . s^V run on the tensor cores (mma.sync m16n8k16 / m16n8k8,
+//       heads on M, tokens on N / K) -- s is shared by all heads of the CTA;
+//     - q~ . z^K and p . z^V run on CUDA cores in fp32 (each z element is used
+//       once; nothing for a tensor core to reuse).
+// Kernel 2 (combine): log-sum-exp merge of each (b, h)'s partials, the residual
+//   up-projection B_h^V acc_z, the bf16 store (also a dependent launch).
 #include "kernels.h"
 #include "lrkv_internal.cuh"
 
 namespace lrkv {
 
-
-constexpr int kGran = 8;  // tokens per pipeline stage (granule)
+constexpr int kGran = 8;                              // tokens per pipeline stage (granule)
 constexpr int kScratchFloats = 16 * 8 + 16 * 8 + 16;  // per consumer warp: z-scores, p, alpha
+constexpr int kPageCache = 64;                        // page ids of a split kept in shared memory
+constexpr int kMaxCombine = 1024;                     // partials one sequence may have (>= SM count)
 
 struct Split {
     int b, g0, g1;
@@ -94,14 +97,44 @@ __device__ __forceinline__ void named_bar(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Issue the loads of one 8-token granule (stage) into ring slot `slot`:
+// Programmatic dependent launch: let the next kernel on the stream start, and
+// wait for the previous one's results (both no-ops without the launch attribute).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ------------------------------------------------------------------ kernel 0
+// q~[b][h][j] = sum_d q[b][h][d] B^K[h][d][j]; one block = 256 / R heads of one sequence.
+template <int D_H, int R>
+__global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) {
+    pdl_trigger();
+    constexpr int HPB = 256 / R;
+    const int b = blockIdx.y, h0 = blockIdx.x * HPB;
+    const int hl = threadIdx.x / R, j = threadIdx.x % R, h = h0 + hl;
+    __shared__ float qs[HPB][D_H];
+    for (int i = threadIdx.x; i < HPB * D_H; i += 256) {
+        const int hh = h0 + i / D_H;
+        qs[i / D_H][i % D_H] =
+            hh < a.H ? __uint_as_float((uint32_t)a.q[((size_t)b * a.H + hh) * D_H + i % D_H] << 16) : 0.f;
+    }
+    __syncthreads();
+    if (h >= a.H) return;
+    const uint16_t* bk = a.BK + (size_t)h * D_H * R + j;
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 16
+    for (int dd = 0; dd < D_H; dd += 2) {
+        acc0 = fmaf(qs[hl][dd], __uint_as_float((uint32_t)bk[dd * R] << 16), acc0);
+        acc1 = fmaf(qs[hl][dd + 1], __uint_as_float((uint32_t)bk[(dd + 1) * R] << 16), acc1);
+    }
+    a.qt[((size_t)b * a.H + h) * R + j] = acc0 + acc1;
+}
+
+// Issue the loads of one 8-token granule (stage) of block `blk` into a ring slot:
 // s^K, s^V by TMA tensor copies (128-byte swizzle), z^K, z^V by bulk copies.
 // An out-of-range block id is reported and the stage is marked empty.
 template <int D_H, int R>
 __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUtensorMap* tm_sV, const DecodeArgs& a,
-                                            uint32_t st, uint32_t bar, int* meta_slot, int b, int gi,
+                                            uint32_t st, uint32_t bar, int* meta_slot, int blk, int gi,
                                             uint64_t pol) {
-    const int blk = a.block_table[(size_t)b * a.max_pages + (gi >> 3)];
     if (blk < 0 || blk >= a.num_blocks) {
         set_status(a.status, LRKV_DEV_BAD_BLOCK);
         *meta_slot = 0;
@@ -121,6 +154,7 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUte
     bulk_load_hint(st + 32 * D_H + 16 * a.H * R, a.zV + zoff, 16u * a.H * R, bar, pol);
 }
 
+// ------------------------------------------------------------------ kernel 1
 // At most 8 warps per CTA (one per head tile and group), so each thread may
 // hold up to 255 registers.  There is no dedicated producer warp: thread 0
 // fills the ring at the start of each split, and afterwards the last warp to
@@ -133,6 +167,7 @@ __global__ void __launch_bounds__(256, 1)
     static_assert(R % 8 == 0 && R <= 32, "r");
     constexpr int NC = R / 8;                                   // 16-byte chunks per z row
     constexpr int RP128 = (2 * R >= 128) ? 1 : 128 / (2 * R);   // z rows per 128-byte bank line
+    constexpr int W = D_H + R;                                  // accumulator width per head
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -151,8 +186,8 @@ __global__ void __launch_bounds__(256, 1)
     int* rel = meta + nslot;                                     // warps done with the slot's current stage
     int* nissued = rel + nslot;                                  // stages ever issued into the slot
     volatile int* tag = nissued + nslot;                         // CTA-wide index of the stage last issued
-    float* qt_s = reinterpret_cast<float*>(meta + ((4 * nslot + 3) & ~3));
-    float* scratch = qt_s + H * R;
+    int* pages = meta + ((4 * nslot + 3) & ~3);                  // block ids of the current split's pages
+    float* scratch = reinterpret_cast<float*>(pages + kPageCache);
     volatile int* abort_flag = reinterpret_cast<int*>(scratch + NCW * kScratchFloats);
 
     if (threadIdx.x == 0) {
@@ -184,6 +219,7 @@ __global__ void __launch_bounds__(256, 1)
     float* SA = SP + 128;
     const int nct = NCW * 32;
     const int hA = h0 + g, hB = h0 + g + 8;
+    bool qt_ready = false;
 
     int kbase = 0;  // stages consumed by this CTA before the current split (ring position and phase)
     for (int s = blockIdx.x; s < nsplits; s += gridDim.x) {
@@ -191,40 +227,48 @@ __global__ void __launch_bounds__(256, 1)
         const int b = sp.b;
         const int L = a.seq_lens[b];
         const int nst = sp.g1 - sp.g0;
+        const int pg0 = sp.g0 >> 3;
+        const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
 
-        // Once every warp is here, all stages of the previous split have been
-        // released and no copy is in flight: fill the ring for this split.
+        // Once every warp is here the previous split is fully consumed and merged:
+        // no copy is in flight and the ring memory is free.
+        named_bar(1, nct);
+        for (int i = threadIdx.x; i < kPageCache && pg0 + i < a.max_pages; i += nct) pages[i] = bt_row[pg0 + i];
+        fence_proxy_async_smem();  // generic accesses of the ring (merge) before async-proxy refills
         named_bar(1, nct);
         if (threadIdx.x == 0 && !*abort_flag) {
             for (int k = 0; k < min(nslot, nst); ++k) {
                 const int slot = (kbase + k) % nslot;
+                const int pi = ((sp.g0 + k) >> 3) - pg0;
                 tag[slot] = kbase + k;
                 issue_stage<D_H, R>(&tm_sK, &tm_sV, a, smem_s + slot * stage_bytes, smem_u32(&full[slot]),
-                                    &meta[slot], b, sp.g0 + k, pol);
+                                    &meta[slot], pi < kPageCache ? pages[pi] : bt_row[pg0 + pi], sp.g0 + k, pol);
                 ++nissued[slot];
             }
         }
-
-        // q~ = q B^K for every head of sequence b (fp32, shared memory).
-        for (int idx = threadIdx.x; idx < H * R; idx += nct) {
-            const int h = idx / R, j = idx - (idx / R) * R;
-            const uint16_t* qh = a.q + ((size_t)b * H + h) * D_H;
-            const uint16_t* bk = a.BK + (size_t)h * D_H * R + j;
-            float acc = 0.f;
-#pragma unroll 8
-            for (int dd = 0; dd < D_H; ++dd)
-                acc = fmaf(__uint_as_float((uint32_t)qh[dd] << 16), __uint_as_float((uint32_t)bk[dd * R] << 16), acc);
-            qt_s[idx] = acc;
+        if (!qt_ready) {
+            pdl_wait();  // q~ written by the absorb kernel
+            qt_ready = true;
         }
-        named_bar(1, nct);
 
         // This lane's q~ row, chunk-rotated so that z rows are read conflict-free.
         float qt[R];
+        {
+            const float* qrow = a.qt + ((size_t)b * H + (hz_ok ? hzh : 0)) * R;
 #pragma unroll
-        for (int cc = 0; cc < NC; ++cc)
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                qt[cc * 8 + e] = hz_ok ? qt_s[hzh * R + ((cc + rot) % NC) * 8 + e] : 0.f;
+            for (int cc = 0; cc < NC; ++cc) {
+                const float4* src = reinterpret_cast<const float4*>(qrow + ((cc + rot) % NC) * 8);
+                const float4 x0 = src[0], x1 = src[1];
+                qt[cc * 8 + 0] = hz_ok ? x0.x : 0.f;
+                qt[cc * 8 + 1] = hz_ok ? x0.y : 0.f;
+                qt[cc * 8 + 2] = hz_ok ? x0.z : 0.f;
+                qt[cc * 8 + 3] = hz_ok ? x0.w : 0.f;
+                qt[cc * 8 + 4] = hz_ok ? x1.x : 0.f;
+                qt[cc * 8 + 5] = hz_ok ? x1.y : 0.f;
+                qt[cc * 8 + 6] = hz_ok ? x1.z : 0.f;
+                qt[cc * 8 + 7] = hz_ok ? x1.w : 0.f;
+            }
+        }
 
         // Query A fragments (heads on M): rows hA, hB; k = head dimension.
         uint32_t qa[D_H / 16][4];
@@ -239,7 +283,6 @@ __global__ void __launch_bounds__(256, 1)
                 qa[kk][3] = hB < H ? qB[kk * 8 + 4 + tq] : 0u;
             }
         }
-        named_bar(1, nct);  // every lane has its q~ before the next split rewrites it
 
         float o[D_H / 8][4];
 #pragma unroll
@@ -251,7 +294,7 @@ __global__ void __launch_bounds__(256, 1)
 
         // After an expired wait every consumer keeps walking its loops (so all of
         // them still meet at the named barriers) but skips the work.
-        for (int j = grp; sp.g0 + j < sp.g1; j += a.ng) {
+        for (int j = grp; j < nst; j += a.ng) {
             const int kk = kbase + j;
             const int slot = kk % nslot;
             if (*abort_flag) continue;
@@ -397,38 +440,45 @@ __global__ void __launch_bounds__(256, 1)
                     rel[slot] = 0;
                     __threadfence_block();
                     const int jn = j + nslot;
-                    if (jn < sp.g1 - sp.g0 && !*abort_flag) {
+                    if (jn < nst && !*abort_flag) {
+                        const int pi = ((sp.g0 + jn) >> 3) - pg0;
                         tag[slot] = kk + nslot;
-                        issue_stage<D_H, R>(&tm_sK, &tm_sV, a, st, smem_u32(&full[slot]), &meta[slot], b,
-                                            sp.g0 + jn, pol);
+                        issue_stage<D_H, R>(&tm_sK, &tm_sV, a, st, smem_u32(&full[slot]), &meta[slot],
+                                            pi < kPageCache ? pages[pi] : bt_row[pg0 + pi], sp.g0 + jn, pol);
                         ++nissued[slot];
                     }
                 }
             }
         }
-        kbase += sp.g1 - sp.g0;
+        kbase += nst;
 
-        // --- write this group's partial for split s
+        // --- this group's state: m, l (log2 domain), o (rows hA, hB), accz (row hzh)
         l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-        const size_t P = (size_t)s * a.ng + grp;
-        const int W = D_H + R;
+#pragma unroll
+        for (int i = 0; i < R; ++i) accz[i] += __shfl_xor_sync(0xffffffffu, accz[i], 16);
+
+        // Groups write their state into the idle ring (or straight to the workspace
+        // when there is one group), then all consumers merge it per head.
+        named_bar(1, nct);  // every stage of this split consumed: the ring is idle
+        const bool direct = (a.ng == 1);
+        float* gml = direct ? a.part_ml + (size_t)s * H * 2 : reinterpret_cast<float*>(smem) + (size_t)grp * H * 2;
+        float* gacc = direct ? a.part_acc + (size_t)s * H * W
+                             : reinterpret_cast<float*>(smem) + (size_t)a.ng * H * 2 + (size_t)grp * H * W;
         if (tq == 0) {
-            if (hA < H) *reinterpret_cast<float2*>(a.part_ml + (P * H + hA) * 2) = make_float2(m0, l0);
-            if (hB < H) *reinterpret_cast<float2*>(a.part_ml + (P * H + hB) * 2) = make_float2(m1, l1);
+            if (hA < H) *reinterpret_cast<float2*>(gml + hA * 2) = make_float2(m0, l0);
+            if (hB < H) *reinterpret_cast<float2*>(gml + hB * 2) = make_float2(m1, l1);
         }
 #pragma unroll
         for (int n = 0; n < D_H / 8; ++n) {
             const int dcol = n * 8 + 2 * tq;
-            if (hA < H) *reinterpret_cast<float2*>(a.part_acc + (P * H + hA) * W + dcol) = make_float2(o[n][0], o[n][1]);
-            if (hB < H) *reinterpret_cast<float2*>(a.part_acc + (P * H + hB) * W + dcol) = make_float2(o[n][2], o[n][3]);
+            if (hA < H) *reinterpret_cast<float2*>(gacc + (size_t)hA * W + dcol) = make_float2(o[n][0], o[n][1]);
+            if (hB < H) *reinterpret_cast<float2*>(gacc + (size_t)hB * W + dcol) = make_float2(o[n][2], o[n][3]);
         }
-#pragma unroll
-        for (int i = 0; i < R; ++i) accz[i] += __shfl_xor_sync(0xffffffffu, accz[i], 16);
         if (half == 0 && hz_ok) {
-            float* dst = a.part_acc + (P * H + hzh) * W + D_H;
+            float* dst = gacc + (size_t)hzh * W + D_H;
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) {
                 float4* d4 = reinterpret_cast<float4*>(dst + ((cc + rot) % NC) * 8);
@@ -436,7 +486,36 @@ __global__ void __launch_bounds__(256, 1)
                 d4[1] = make_float4(accz[cc * 8 + 4], accz[cc * 8 + 5], accz[cc * 8 + 6], accz[cc * 8 + 7]);
             }
         }
+        if (!direct) {
+            named_bar(1, nct);
+            const float* sml = reinterpret_cast<const float*>(smem);
+            const float* sacc = sml + (size_t)a.ng * H * 2;
+            float* pml = a.part_ml + (size_t)s * H * 2;
+            float* pacc = a.part_acc + (size_t)s * H * W;
+            for (int h = threadIdx.x; h < H; h += nct) {
+                float M = -INFINITY, Ls = 0.f;
+                for (int gg = 0; gg < a.ng; ++gg) M = fmaxf(M, sml[(gg * H + h) * 2]);
+                for (int gg = 0; gg < a.ng; ++gg) {
+                    const float mg = sml[(gg * H + h) * 2];
+                    Ls += (mg == -INFINITY) ? 0.f : exp2f(mg - M) * sml[(gg * H + h) * 2 + 1];
+                }
+                *reinterpret_cast<float2*>(pml + h * 2) = make_float2(M, Ls);
+            }
+            for (int idx = threadIdx.x; idx < H * W; idx += nct) {
+                const int h = idx / W;
+                float M = -INFINITY;
+                for (int gg = 0; gg < a.ng; ++gg) M = fmaxf(M, sml[(gg * H + h) * 2]);
+                float v = 0.f;
+                for (int gg = 0; gg < a.ng; ++gg) {
+                    const float mg = sml[(gg * H + h) * 2];
+                    if (mg != -INFINITY) v = fmaf(exp2f(mg - M), sacc[(size_t)gg * H * W + idx], v);
+                }
+                pacc[idx] = v;
+            }
+        }
     }
+    // The combine kernel may now be scheduled; it waits for this grid to finish.
+    pdl_trigger();
     // After an expired wait, make sure no copy is still landing in shared memory
     // before the CTA exits: wait (bounded) for the last phase issued into each slot.
     named_bar(1, nct);
@@ -445,49 +524,88 @@ __global__ void __launch_bounds__(256, 1)
             if (nissued[sl] > 0) mbar_wait(smem_u32(&full[sl]), (nissued[sl] - 1) & 1, a.status);
 }
 
+// ------------------------------------------------------------------ kernel 2
 // Log-sum-exp merge of a sequence's partials, residual up-projection, bf16 store.
-// grid (H, B), block D_H threads.
+// grid (H, B), 256 threads.
 template <int D_H, int R>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a, int G) {
+__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a, int G) {
+    constexpr int W = D_H + R;
+    constexpr int NSL = 256 / W;  // partial slices accumulated in parallel
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int H = a.H;
     const int cap = a.max_pages * kBlockSize;
-    __shared__ float zs[R];
+    __shared__ float wsh[kMaxCombine];
+    __shared__ float red[8];
+    __shared__ float cacc[NSL][W];
+    pdl_wait();
     uint16_t* dst = a.out + ((size_t)b * H + h) * D_H;
     const int L = a.seq_lens[b];
     if (L < 1 || L > cap) {
         if (tid == 0 && h == 0) set_status(a.status, LRKV_DEV_BAD_SEQLEN);
-        dst[tid] = 0;
+        if (tid < D_H) dst[tid] = 0;
         return;
     }
     int nsplits;
     const int chunk = partition_chunk(a.seq_lens, a.B, cap, G, &nsplits);
-    int first, count;
-    seq_splits(a.seq_lens, a.B, cap, chunk, b, &first, &count);
-    const size_t p0 = (size_t)first * a.ng;
-    const int np = count * a.ng;
-    const int W = D_H + R;
+    int first, np;
+    seq_splits(a.seq_lens, a.B, cap, chunk, b, &first, &np);
+    const float* pml = a.part_ml + ((size_t)first * H + h) * 2;
+    const float* pacc = a.part_acc + ((size_t)first * H + h) * W;
+    const size_t pstride_ml = (size_t)H * 2, pstride = (size_t)H * W;
 
-    float M = -INFINITY;
-    for (int p = 0; p < np; ++p) M = fmaxf(M, a.part_ml[((p0 + p) * H + h) * 2]);
-    float lsum = 0.f, acc0 = 0.f, acc1 = 0.f;
-    for (int p = 0; p < np; ++p) {
-        const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + ((p0 + p) * H + h) * 2);
-        const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-        lsum = fmaf(w, ml.y, lsum);
-        const float* pa = a.part_acc + ((p0 + p) * H + h) * W;
-        acc0 = fmaf(w, pa[tid], acc0);
-        if (tid < R) acc1 = fmaf(w, pa[D_H + tid], acc1);
-    }
-    if (tid < R) zs[tid] = acc1;
+    float mloc = -INFINITY;
+    for (int p = tid; p < np; p += 256) mloc = fmaxf(mloc, pml[p * pstride_ml]);
+    for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
+    if ((tid & 31) == 0) red[tid >> 5] = mloc;
     __syncthreads();
-    float v = acc0;
-    const uint16_t* bv = a.BV + ((size_t)h * D_H + tid) * R;
+    float M = red[0];
 #pragma unroll
-    for (int j = 0; j < R; ++j) v = fmaf(__uint_as_float((uint32_t)bv[j] << 16), zs[j], v);
-    v = lsum > 0.f ? v / lsum : 0.f;
-    __nv_bfloat16 o = __float2bfloat16_rn(v);
-    dst[tid] = *reinterpret_cast<uint16_t*>(&o);
+    for (int i = 1; i < 8; ++i) M = fmaxf(M, red[i]);
+    __syncthreads();
+    float lloc = 0.f;
+    for (int p = tid; p < np; p += 256) {
+        const float2 ml = *reinterpret_cast<const float2*>(pml + p * pstride_ml);
+        const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+        wsh[p] = w;
+        lloc = fmaf(w, ml.y, lloc);
+    }
+    for (int off = 16; off > 0; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
+    if ((tid & 31) == 0) red[tid >> 5] = lloc;
+    __syncthreads();
+    float lsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) lsum += red[i];
+
+    const int sl = tid / W, c = tid - (tid / W) * W;
+    if (sl < NSL) {
+        float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+        int p = sl;
+        for (; p + 3 * NSL < np; p += 4 * NSL) {
+            v0 = fmaf(wsh[p], pacc[p * pstride + c], v0);
+            v1 = fmaf(wsh[p + NSL], pacc[(p + NSL) * pstride + c], v1);
+            v2 = fmaf(wsh[p + 2 * NSL], pacc[(p + 2 * NSL) * pstride + c], v2);
+            v3 = fmaf(wsh[p + 3 * NSL], pacc[(p + 3 * NSL) * pstride + c], v3);
+        }
+        for (; p < np; p += NSL) v0 = fmaf(wsh[p], pacc[p * pstride + c], v0);
+        cacc[sl][c] = (v0 + v1) + (v2 + v3);
+    }
+    __syncthreads();
+    if (tid < D_H) {
+        float v = 0.f;
+#pragma unroll
+        for (int i = 0; i < NSL; ++i) v += cacc[i][tid];
+        const uint16_t* bv = a.BV + ((size_t)h * D_H + tid) * R;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            float z = 0.f;
+#pragma unroll
+            for (int i = 0; i < NSL; ++i) z += cacc[i][D_H + j];
+            v = fmaf(__uint_as_float((uint32_t)bv[j] << 16), z, v);
+        }
+        v = lsum > 0.f ? v / lsum : 0.f;
+        const __nv_bfloat16 ob = __float2bfloat16_rn(v);
+        dst[tid] = *reinterpret_cast<const uint16_t*>(&ob);
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -495,8 +613,8 @@ struct DecodePlan {
     int ng, nslot, stage_bytes, smem_bytes, threads;
 };
 
-static int decode_fixed_smem(int H, int R, int ncw, int nslot) {
-    return nslot * 8 + ((4 * nslot + 3) & ~3) * 4 + H * R * 4 + ncw * kScratchFloats * 4 + 16 + 1024;
+static int decode_fixed_smem(int ncw, int nslot) {
+    return nslot * 8 + ((4 * nslot + 3) & ~3) * 4 + kPageCache * 4 + ncw * kScratchFloats * 4 + 16 + 1024;
 }
 
 DecodePlan decode_plan(int H, int D_H, int R, int smem_limit) {
@@ -504,46 +622,71 @@ DecodePlan decode_plan(int H, int D_H, int R, int smem_limit) {
     const int HT = (H + 15) / 16;
     p.stage_bytes = ((32 * D_H + 32 * H * R) + 1023) & ~1023;
     int nslot = 16;
-    while (nslot > 2 && nslot * p.stage_bytes + decode_fixed_smem(H, R, 8, nslot) > smem_limit) --nslot;
+    while (nslot > 2 && nslot * p.stage_bytes + decode_fixed_smem(8, nslot) > smem_limit) --nslot;
     p.nslot = nslot;
     int ng = max(1, min(8 / HT, nslot - 2));
+    // the group merge reuses the ring: ng * H * (D_H + R + 2) floats must fit in it
+    while (ng > 1 && (size_t)ng * H * (D_H + R + 2) * 4 > (size_t)nslot * p.stage_bytes) --ng;
     p.ng = ng;
     p.threads = 32 * HT * ng;
-    p.smem_bytes = nslot * p.stage_bytes + decode_fixed_smem(H, R, HT * ng, nslot);
+    p.smem_bytes = nslot * p.stage_bytes + decode_fixed_smem(HT * ng, nslot);
     return p;
 }
 
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
 size_t decode_workspace_bytes(int H, int D_H, int R, int B, int G, int smem_limit) {
-    const DecodePlan p = decode_plan(H, D_H, R, smem_limit);
-    const size_t pmax = (size_t)max(G, B) * p.ng;
-    const size_t ml_bytes = (pmax * H * 2 * sizeof(float) + 255) & ~(size_t)255;
-    return ml_bytes + pmax * H * (D_H + R) * sizeof(float);
+    (void)smem_limit;
+    const size_t pmax = (size_t)max(G, B);
+    return align256(pmax * H * 2 * sizeof(float)) + align256(pmax * H * (D_H + R) * sizeof(float)) +
+           align256((size_t)B * H * R * sizeof(float));
 }
 
 void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int B, int G, int smem_limit) {
-    const DecodePlan p = decode_plan(H, D_H, R, smem_limit);
-    const size_t pmax = (size_t)max(G, B) * p.ng;
+    (void)smem_limit;
+    const size_t pmax = (size_t)max(G, B);
     uint8_t* base = static_cast<uint8_t*>(ws);
     a->part_ml = reinterpret_cast<float*>(base);
-    const size_t ml_bytes = (pmax * H * 2 * sizeof(float) + 255) & ~(size_t)255;
-    a->part_acc = reinterpret_cast<float*>(base + ml_bytes);
+    base += align256(pmax * H * 2 * sizeof(float));
+    a->part_acc = reinterpret_cast<float*>(base);
+    base += align256(pmax * H * (D_H + R) * sizeof(float));
+    a->qt = reinterpret_cast<float*>(base);
+}
+
+template <typename... Args>
+static cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 template <int D_H, int R>
 static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, const DecodePlan& p,
                                    int G, cudaStream_t stream) {
-    auto kern = decode_split_kernel<D_H, R>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+    constexpr int HPB = 256 / R;
+    decode_absorb_kernel<D_H, R><<<dim3((a.H + HPB - 1) / HPB, a.B), 256, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    kern<<<G, p.threads, p.smem_bytes, stream>>>(tK, tV, a);
-    e = cudaGetLastError();
+    auto split = decode_split_kernel<D_H, R>;
+    e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<D_H, R><<<dim3(a.H, a.B), D_H, 0, stream>>>(a, G);
-    return cudaGetLastError();
+    e = launch_pdl(split, dim3(G), dim3(p.threads), p.smem_bytes, stream, tK, tV, a);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, a.B), dim3(256), 0, stream, a, G);
 }
 
 cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int G,
                           int smem_limit, cudaStream_t stream) {
+    if (G > kMaxCombine) return cudaErrorInvalidConfiguration;
     const DecodePlan p = decode_plan(a.H, D_H, R, smem_limit);
     a.ng = p.ng;
     a.nslot = p.nslot;

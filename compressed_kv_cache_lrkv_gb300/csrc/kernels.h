@@ -28,6 +28,7 @@ struct DecodeArgs {
     const int32_t* seq_lens;     // [B]
     float* part_ml;   // [Pmax][H][2]  running max (log2 domain) and sum
     float* part_acc;  // [Pmax][H][D_H + R]
+    float* qt;        // [B][H][R]  q~ = q B^K, fp32
     uint32_t* status;
     uint16_t* out;    // [B][H][D_H]
     int B, H, max_pages, num_blocks;
