@@ -103,29 +103,32 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------------ kernel 0
-// q~[b][h][j] = sum_d q[b][h][d] B^K[h][d][j]; one block = 256 / R heads of one sequence.
+// q~[b][h][j] = sum_d q[b][h][d] B^K[h][d][j]; one block per (head, sequence):
+// 256 / R slices of the d range are summed in parallel, then reduced in
+// shared memory, so all of B_h^K (d_h x r) is in flight at once.
 template <int D_H, int R>
 __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) {
     pdl_trigger();
-    constexpr int HPB = 256 / R;
-    const int b = blockIdx.y, h0 = blockIdx.x * HPB;
-    const int hl = threadIdx.x / R, j = threadIdx.x % R, h = h0 + hl;
-    __shared__ float qs[HPB][D_H];
-    for (int i = threadIdx.x; i < HPB * D_H; i += 256) {
-        const int hh = h0 + i / D_H;
-        qs[i / D_H][i % D_H] =
-            hh < a.H ? __uint_as_float((uint32_t)a.q[((size_t)b * a.H + hh) * D_H + i % D_H] << 16) : 0.f;
-    }
+    constexpr int NS = 256 / R;           // d slices
+    constexpr int DS = D_H / NS;          // d values per slice (>= 2)
+    static_assert(DS >= 1 && D_H % NS == 0, "slices");
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int j = threadIdx.x % R, sl = threadIdx.x / R;
+    __shared__ float part[NS][R];
+    const uint16_t* qrow = a.q + ((size_t)b * a.H + h) * D_H + sl * DS;
+    const uint16_t* bk = a.BK + ((size_t)h * D_H + sl * DS) * R + j;
+    float acc = 0.f;
+#pragma unroll
+    for (int dd = 0; dd < DS; ++dd)
+        acc = fmaf(__uint_as_float((uint32_t)qrow[dd] << 16), __uint_as_float((uint32_t)bk[dd * R] << 16), acc);
+    part[sl][j] = acc;
     __syncthreads();
-    if (h >= a.H) return;
-    const uint16_t* bk = a.BK + (size_t)h * D_H * R + j;
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 16
-    for (int dd = 0; dd < D_H; dd += 2) {
-        acc0 = fmaf(qs[hl][dd], __uint_as_float((uint32_t)bk[dd * R] << 16), acc0);
-        acc1 = fmaf(qs[hl][dd + 1], __uint_as_float((uint32_t)bk[(dd + 1) * R] << 16), acc1);
+    if (threadIdx.x < R) {
+        float v = 0.f;
+#pragma unroll
+        for (int i = 0; i < NS; ++i) v += part[i][threadIdx.x];
+        a.qt[((size_t)b * a.H + h) * R + threadIdx.x] = v;
     }
-    a.qt[((size_t)b * a.H + h) * R + j] = acc0 + acc1;
 }
 
 // Issue the loads of one 8-token granule (stage) of block `blk` into a ring slot:
@@ -464,21 +467,25 @@ __global__ void __launch_bounds__(256, 1)
         // when there is one group), then all consumers merge it per head.
         named_bar(1, nct);  // every stage of this split consumed: the ring is idle
         const bool direct = (a.ng == 1);
-        float* gml = direct ? a.part_ml + (size_t)s * H * 2 : reinterpret_cast<float*>(smem) + (size_t)grp * H * 2;
-        float* gacc = direct ? a.part_acc + (size_t)s * H * W
+        // Workspace partials are laid out [head][split][...] so that the combine reads
+        // one head's partials contiguously; the shared-memory staging is [group][head].
+        const size_t hs_ml = direct ? (size_t)a.pmax * 2 : 2;     // stride between heads
+        const size_t hs_acc = direct ? (size_t)a.pmax * W : W;
+        float* gml = direct ? a.part_ml + (size_t)s * 2 : reinterpret_cast<float*>(smem) + (size_t)grp * H * 2;
+        float* gacc = direct ? a.part_acc + (size_t)s * W
                              : reinterpret_cast<float*>(smem) + (size_t)a.ng * H * 2 + (size_t)grp * H * W;
         if (tq == 0) {
-            if (hA < H) *reinterpret_cast<float2*>(gml + hA * 2) = make_float2(m0, l0);
-            if (hB < H) *reinterpret_cast<float2*>(gml + hB * 2) = make_float2(m1, l1);
+            if (hA < H) *reinterpret_cast<float2*>(gml + hA * hs_ml) = make_float2(m0, l0);
+            if (hB < H) *reinterpret_cast<float2*>(gml + hB * hs_ml) = make_float2(m1, l1);
         }
 #pragma unroll
         for (int n = 0; n < D_H / 8; ++n) {
             const int dcol = n * 8 + 2 * tq;
-            if (hA < H) *reinterpret_cast<float2*>(gacc + (size_t)hA * W + dcol) = make_float2(o[n][0], o[n][1]);
-            if (hB < H) *reinterpret_cast<float2*>(gacc + (size_t)hB * W + dcol) = make_float2(o[n][2], o[n][3]);
+            if (hA < H) *reinterpret_cast<float2*>(gacc + (size_t)hA * hs_acc + dcol) = make_float2(o[n][0], o[n][1]);
+            if (hB < H) *reinterpret_cast<float2*>(gacc + (size_t)hB * hs_acc + dcol) = make_float2(o[n][2], o[n][3]);
         }
         if (half == 0 && hz_ok) {
-            float* dst = gacc + (size_t)hzh * W + D_H;
+            float* dst = gacc + (size_t)hzh * hs_acc + D_H;
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) {
                 float4* d4 = reinterpret_cast<float4*>(dst + ((cc + rot) % NC) * 8);
@@ -490,8 +497,8 @@ __global__ void __launch_bounds__(256, 1)
             named_bar(1, nct);
             const float* sml = reinterpret_cast<const float*>(smem);
             const float* sacc = sml + (size_t)a.ng * H * 2;
-            float* pml = a.part_ml + (size_t)s * H * 2;
-            float* pacc = a.part_acc + (size_t)s * H * W;
+            float* pml = a.part_ml + (size_t)s * 2;
+            float* pacc = a.part_acc + (size_t)s * W;
             for (int h = threadIdx.x; h < H; h += nct) {
                 float M = -INFINITY, Ls = 0.f;
                 for (int gg = 0; gg < a.ng; ++gg) M = fmaxf(M, sml[(gg * H + h) * 2]);
@@ -499,10 +506,10 @@ __global__ void __launch_bounds__(256, 1)
                     const float mg = sml[(gg * H + h) * 2];
                     Ls += (mg == -INFINITY) ? 0.f : exp2f(mg - M) * sml[(gg * H + h) * 2 + 1];
                 }
-                *reinterpret_cast<float2*>(pml + h * 2) = make_float2(M, Ls);
+                *reinterpret_cast<float2*>(pml + (size_t)h * a.pmax * 2) = make_float2(M, Ls);
             }
             for (int idx = threadIdx.x; idx < H * W; idx += nct) {
-                const int h = idx / W;
+                const int h = idx / W, c = idx - (idx / W) * W;
                 float M = -INFINITY;
                 for (int gg = 0; gg < a.ng; ++gg) M = fmaxf(M, sml[(gg * H + h) * 2]);
                 float v = 0.f;
@@ -510,7 +517,7 @@ __global__ void __launch_bounds__(256, 1)
                     const float mg = sml[(gg * H + h) * 2];
                     if (mg != -INFINITY) v = fmaf(exp2f(mg - M), sacc[(size_t)gg * H * W + idx], v);
                 }
-                pacc[idx] = v;
+                pacc[(size_t)h * a.pmax * W + c] = v;
             }
         }
     }
@@ -526,17 +533,16 @@ __global__ void __launch_bounds__(256, 1)
 
 // ------------------------------------------------------------------ kernel 2
 // Log-sum-exp merge of a sequence's partials, residual up-projection, bf16 store.
-// grid (H, B), 256 threads.
+// grid (H, B), 256 threads; one head's partials are contiguous in the workspace.
 template <int D_H, int R>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a, int G) {
     constexpr int W = D_H + R;
-    constexpr int NSL = 256 / W;  // partial slices accumulated in parallel
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int H = a.H;
     const int cap = a.max_pages * kBlockSize;
     __shared__ float wsh[kMaxCombine];
     __shared__ float red[8];
-    __shared__ float cacc[NSL][W];
+    __shared__ float cacc[W];
     pdl_wait();
     uint16_t* dst = a.out + ((size_t)b * H + h) * D_H;
     const int L = a.seq_lens[b];
@@ -549,12 +555,11 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a,
     const int chunk = partition_chunk(a.seq_lens, a.B, cap, G, &nsplits);
     int first, np;
     seq_splits(a.seq_lens, a.B, cap, chunk, b, &first, &np);
-    const float* pml = a.part_ml + ((size_t)first * H + h) * 2;
-    const float* pacc = a.part_acc + ((size_t)first * H + h) * W;
-    const size_t pstride_ml = (size_t)H * 2, pstride = (size_t)H * W;
+    const float* pml = a.part_ml + ((size_t)h * a.pmax + first) * 2;
+    const float* pacc = a.part_acc + ((size_t)h * a.pmax + first) * W;
 
     float mloc = -INFINITY;
-    for (int p = tid; p < np; p += 256) mloc = fmaxf(mloc, pml[p * pstride_ml]);
+    for (int p = tid; p < np; p += 256) mloc = fmaxf(mloc, pml[2 * p]);
     for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
     if ((tid & 31) == 0) red[tid >> 5] = mloc;
     __syncthreads();
@@ -564,7 +569,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a,
     __syncthreads();
     float lloc = 0.f;
     for (int p = tid; p < np; p += 256) {
-        const float2 ml = *reinterpret_cast<const float2*>(pml + p * pstride_ml);
+        const float2 ml = *reinterpret_cast<const float2*>(pml + 2 * p);
         const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
         wsh[p] = w;
         lloc = fmaf(w, ml.y, lloc);
@@ -576,32 +581,22 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a,
 #pragma unroll
     for (int i = 0; i < 8; ++i) lsum += red[i];
 
-    const int sl = tid / W, c = tid - (tid / W) * W;
-    if (sl < NSL) {
-        float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
-        int p = sl;
-        for (; p + 3 * NSL < np; p += 4 * NSL) {
-            v0 = fmaf(wsh[p], pacc[p * pstride + c], v0);
-            v1 = fmaf(wsh[p + NSL], pacc[(p + NSL) * pstride + c], v1);
-            v2 = fmaf(wsh[p + 2 * NSL], pacc[(p + 2 * NSL) * pstride + c], v2);
-            v3 = fmaf(wsh[p + 3 * NSL], pacc[(p + 3 * NSL) * pstride + c], v3);
+    if (tid < W) {
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        int p = 0;
+        for (; p + 8 <= np; p += 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = fmaf(wsh[p + u], pacc[(size_t)(p + u) * W + tid], v[u]);
         }
-        for (; p < np; p += NSL) v0 = fmaf(wsh[p], pacc[p * pstride + c], v0);
-        cacc[sl][c] = (v0 + v1) + (v2 + v3);
+        for (; p < np; ++p) v[0] = fmaf(wsh[p], pacc[(size_t)p * W + tid], v[0]);
+        cacc[tid] = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
     }
     __syncthreads();
     if (tid < D_H) {
-        float v = 0.f;
-#pragma unroll
-        for (int i = 0; i < NSL; ++i) v += cacc[i][tid];
+        float v = cacc[tid];
         const uint16_t* bv = a.BV + ((size_t)h * D_H + tid) * R;
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
-            float z = 0.f;
-#pragma unroll
-            for (int i = 0; i < NSL; ++i) z += cacc[i][D_H + j];
-            v = fmaf(__uint_as_float((uint32_t)bv[j] << 16), z, v);
-        }
+        for (int j = 0; j < R; ++j) v = fmaf(__uint_as_float((uint32_t)bv[j] << 16), cacc[D_H + j], v);
         v = lsum > 0.f ? v / lsum : 0.f;
         const __nv_bfloat16 ob = __float2bfloat16_rn(v);
         dst[tid] = *reinterpret_cast<const uint16_t*>(&ob);
@@ -672,8 +667,7 @@ static cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size
 template <int D_H, int R>
 static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, const DecodePlan& p,
                                    int G, cudaStream_t stream) {
-    constexpr int HPB = 256 / R;
-    decode_absorb_kernel<D_H, R><<<dim3((a.H + HPB - 1) / HPB, a.B), 256, 0, stream>>>(a);
+    decode_absorb_kernel<D_H, R><<<dim3(a.H, a.B), 256, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto split = decode_split_kernel<D_H, R>;
@@ -691,6 +685,7 @@ cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeAr
     a.ng = p.ng;
     a.nslot = p.nslot;
     a.stage_bytes = p.stage_bytes;
+    a.pmax = max(G, a.B);
 #define LRKV_DEC(DH, RR) \
     if (D_H == DH && R == RR) return launch_decode_t<DH, RR>(tK, tV, a, p, G, stream);
     LRKV_DEC(64, 8) LRKV_DEC(64, 16) LRKV_DEC(64, 32) LRKV_DEC(128, 8) LRKV_DEC(128, 16) LRKV_DEC(128, 32)

@@ -26,13 +26,14 @@ struct DecodeArgs {
     const uint16_t* zV;
     const int32_t* block_table;  // [B][max_pages]
     const int32_t* seq_lens;     // [B]
-    float* part_ml;   // [Pmax][H][2]  running max (log2 domain) and sum
-    float* part_acc;  // [Pmax][H][D_H + R]
+    float* part_ml;   // [H][Pmax][2]  running max (log2 domain) and sum
+    float* part_acc;  // [H][Pmax][D_H + R]
     float* qt;        // [B][H][R]  q~ = q B^K, fp32
     uint32_t* status;
     uint16_t* out;    // [B][H][D_H]
     int B, H, max_pages, num_blocks;
     int ng, nslot, stage_bytes;
+    int pmax;          // partial slots per head in the workspace (max(G, B))
     float scale_log2;  // softmax scale * log2(e)
 };
 
