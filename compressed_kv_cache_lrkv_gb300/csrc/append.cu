@@ -52,74 +52,62 @@ __device__ __forceinline__ float dot8(const uint4& w, const uint4& x) {
     return acc;
 }
 
-// One CTA owns COLS consecutive output columns; its 8 warps split the K
-// (hidden) dimension -- lane l of warp w reads 16-byte chunks
-// k = (w * 32 + l) * 8 + i * 2048 -- so every weight byte is read once, with
-// up to COLS * ceil(d / 2048) independent 16-byte loads in flight per lane.
-// Partial sums are reduced with warp shuffles and then across warps in shared
-// memory, always in the same order.
-template <int NT, int COLS>
-__global__ void __launch_bounds__(256) append_rowwise_kernel(const AppendArgs a) {
+// One 128-thread CTA per output column c and block of NT token rows: lane i of
+// the CTA reads the 16-byte chunks i, i + 128, ... of weight row c (W_cat^T is
+// contiguous along d), so the whole weight matrix is in flight in about one
+// memory round trip (N CTAs, one wave); the NT hidden rows are small and
+// stay in L1/L2.  Partial sums are reduced with warp shuffles and then across
+// the four warps in shared memory, always in the same order.
+template <int NT>
+__global__ void __launch_bounds__(128) append_rowwise_kernel(const AppendArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c0 = blockIdx.x * COLS;
+    const int c = blockIdx.x;
     const int t0 = blockIdx.y * NT;
-    __shared__ float red[8][COLS * NT];
-    float acc[COLS][NT];
+    __shared__ float red[4][NT];
+    float acc[NT];
 #pragma unroll
-    for (int c = 0; c < COLS; ++c)
-#pragma unroll
-        for (int t = 0; t < NT; ++t) acc[c][t] = 0.f;
-
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-#pragma unroll 2
-    for (int k = (warp * 32 + lane) * 8; k < a.d; k += 256 * 8) {
-        uint4 w[COLS];
-#pragma unroll
-        for (int c = 0; c < COLS; ++c)
-            w[c] = (c0 + c < a.N) ? __ldg(reinterpret_cast<const uint4*>(a.W + (size_t)(c0 + c) * a.d + k)) : zero;
+    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+    const uint16_t* wrow = a.W + (size_t)c * a.d;
+    const int nchunk = a.d >> 3;
+#pragma unroll 4
+    for (int k8 = threadIdx.x; k8 < nchunk; k8 += 128) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(wrow) + k8);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             if (t0 + t < a.n) {
-                const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + t) * a.d + k));
-#pragma unroll
-                for (int c = 0; c < COLS; ++c) acc[c][t] += dot8(w[c], x);
+                const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + t) * a.d) + k8);
+                acc[t] += dot8(w, x);
             }
         }
     }
 #pragma unroll
-    for (int c = 0; c < COLS; ++c)
+    for (int t = 0; t < NT; ++t) {
+        float v = acc[t];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            float v = acc[c][t];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) red[warp][c * NT + t] = v;
-        }
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) red[warp][t] = v;
+    }
     __syncthreads();
-    for (int i = threadIdx.x; i < COLS * NT; i += 256) {
-        const int c = i / NT, t = i % NT;
-        if (c0 + c < a.N && t0 + t < a.n) {
-            float v = 0.f;
-#pragma unroll
-            for (int ww = 0; ww < 8; ++ww) v += red[ww][i];
-            const long long slot = checked_slot(a, t0 + t);
-            if (slot >= 0) store_cache_value(a, slot, c0 + c, v);
-        }
+    if (threadIdx.x < NT && t0 + threadIdx.x < a.n) {
+        const int t = threadIdx.x;
+        const float v = (red[0][t] + red[1][t]) + (red[2][t] + red[3][t]);
+        const long long slot = checked_slot(a, t0 + t);
+        if (slot >= 0) store_cache_value(a, slot, c, v);
     }
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
-#define LRKV_ROW(NTV, COLSV)                                                             \
+#define LRKV_ROW(NTV)                                                                    \
     {                                                                                    \
-        dim3 grid((a.N + COLSV - 1) / COLSV, (a.n + NTV - 1) / NTV);                     \
-        append_rowwise_kernel<NTV, COLSV><<<grid, 256, 0, stream>>>(a);                  \
+        dim3 grid(a.N, (a.n + NTV - 1) / NTV);                                           \
+        append_rowwise_kernel<NTV><<<grid, 128, 0, stream>>>(a);                         \
         return cudaGetLastError();                                                       \
     }
-    if (a.n <= 1) LRKV_ROW(1, 4)
-    if (a.n <= 2) LRKV_ROW(2, 4)
-    if (a.n <= 4) LRKV_ROW(4, 4)
-    if (a.n <= 8) LRKV_ROW(8, 4)
-    LRKV_ROW(16, 2)
+    if (a.n <= 1) LRKV_ROW(1)
+    if (a.n <= 2) LRKV_ROW(2)
+    if (a.n <= 4) LRKV_ROW(4)
+    if (a.n <= 8) LRKV_ROW(8)
+    LRKV_ROW(16)
 #undef LRKV_ROW
 }
 

@@ -30,36 +30,50 @@ namespace lrkv {
 constexpr int kGran = 8;                              // tokens per pipeline stage (granule)
 constexpr int kScratchFloats = 16 * 8 + 16 * 8 + 16;  // per consumer warp: z-scores, p, alpha
 constexpr int kPageCache = 64;                        // page ids of a split kept in shared memory
-constexpr int kMaxCombine = 1024;                     // partials one sequence may have (>= SM count)
 
 struct Split {
     int b, g0, g1;
 };
 
+constexpr int kSeqCache = 256;                        // sequence lengths kept in shared memory
+
+// Sequence lengths, read from a shared-memory copy for the first kSeqCache
+// sequences (the partition below walks them several times per CTA).
+struct SeqLens {
+    const int32_t* g;
+    const int* s;
+    __device__ __forceinline__ int operator[](int b) const { return b < kSeqCache ? s[b] : g[b]; }
+};
+
+// Cooperative copy of the first kSeqCache lengths (caller synchronises afterwards).
+__device__ __forceinline__ void stage_seq_lens(int* dst, const int32_t* src, int B, int tid, int nthreads) {
+    for (int b = tid; b < B && b < kSeqCache; b += nthreads) dst[b] = src[b];
+}
+
 // Granules of sequence b, or 0 when its length is outside [1, cap].
-__device__ __forceinline__ int seq_granules(const int32_t* seq_lens, int b, int cap) {
-    const int L = seq_lens[b];
+__device__ __forceinline__ int seq_granules(const SeqLens& sl, int b, int cap) {
+    const int L = sl[b];
     return (L >= 1 && L <= cap) ? (L + kGran - 1) / kGran : 0;
 }
 
 // Even division of all granules into at most max(G, B) splits: chunk is chosen
 // so that sum_b ceil(gr_b / chunk) <= G whenever G > B; sequence b is then cut
 // into ns_b = ceil(gr_b / chunk) near-equal pieces.
-__device__ __forceinline__ int partition_chunk(const int32_t* seq_lens, int B, int cap, int G, int* nsplits) {
+__device__ __forceinline__ int partition_chunk(const SeqLens& sl, int B, int cap, int G, int* nsplits) {
     long long total = 0;
-    for (int b = 0; b < B; ++b) total += seq_granules(seq_lens, b, cap);
+    for (int b = 0; b < B; ++b) total += seq_granules(sl, b, cap);
     const int denom = G > B ? G - B : 1;
     const int chunk = (int)max(1LL, (total + denom - 1) / denom);
     int ns = 0;
-    for (int b = 0; b < B; ++b) ns += (seq_granules(seq_lens, b, cap) + chunk - 1) / chunk;
+    for (int b = 0; b < B; ++b) ns += (seq_granules(sl, b, cap) + chunk - 1) / chunk;
     *nsplits = ns;
     return chunk;
 }
 
-__device__ __forceinline__ Split split_info(const int32_t* seq_lens, int B, int cap, int chunk, int s) {
+__device__ __forceinline__ Split split_info(const SeqLens& sl, int B, int cap, int chunk, int s) {
     int base = 0;
     for (int b = 0; b < B; ++b) {
-        const int gr = seq_granules(seq_lens, b, cap);
+        const int gr = seq_granules(sl, b, cap);
         const int ns = (gr + chunk - 1) / chunk;
         if (s < base + ns) {
             const int i = s - base;
@@ -71,12 +85,12 @@ __device__ __forceinline__ Split split_info(const int32_t* seq_lens, int B, int 
 }
 
 // First split index and split count of sequence b.
-__device__ __forceinline__ void seq_splits(const int32_t* seq_lens, int B, int cap, int chunk, int b, int* first,
+__device__ __forceinline__ void seq_splits(const SeqLens& sl, int B, int cap, int chunk, int b, int* first,
                                            int* count) {
     int base = 0;
-    for (int bb = 0; bb < b; ++bb) base += (seq_granules(seq_lens, bb, cap) + chunk - 1) / chunk;
+    for (int bb = 0; bb < b; ++bb) base += (seq_granules(sl, bb, cap) + chunk - 1) / chunk;
     *first = base;
-    *count = (seq_granules(seq_lens, b, cap) + chunk - 1) / chunk;
+    *count = (seq_granules(sl, b, cap) + chunk - 1) / chunk;
 }
 
 // Bounded wait until a slot's stage tag equals `want` (sets LRKV_DEV_TIMEOUT on expiry).
@@ -190,7 +204,8 @@ __global__ void __launch_bounds__(256, 1)
     int* nissued = rel + nslot;                                  // stages ever issued into the slot
     volatile int* tag = nissued + nslot;                         // CTA-wide index of the stage last issued
     int* pages = meta + ((4 * nslot + 3) & ~3);                  // block ids of the current split's pages
-    float* scratch = reinterpret_cast<float*>(pages + kPageCache);
+    int* slc = pages + kPageCache;                               // first kSeqCache sequence lengths
+    float* scratch = reinterpret_cast<float*>(slc + kSeqCache);
     volatile int* abort_flag = reinterpret_cast<int*>(scratch + NCW * kScratchFloats);
 
     if (threadIdx.x == 0) {
@@ -203,11 +218,13 @@ __global__ void __launch_bounds__(256, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
+    stage_seq_lens(slc, a.seq_lens, a.B, threadIdx.x, blockDim.x);
     __syncthreads();
 
+    const SeqLens seql{a.seq_lens, slc};
     const int cap = a.max_pages * kBlockSize;
     int nsplits;
-    const int chunk = partition_chunk(a.seq_lens, a.B, cap, gridDim.x, &nsplits);
+    const int chunk = partition_chunk(seql, a.B, cap, gridDim.x, &nsplits);
     const uint64_t pol = policy_evict_first();
 
     const int grp = warp / HT, ht = warp % HT;
@@ -226,9 +243,9 @@ __global__ void __launch_bounds__(256, 1)
 
     int kbase = 0;  // stages consumed by this CTA before the current split (ring position and phase)
     for (int s = blockIdx.x; s < nsplits; s += gridDim.x) {
-        const Split sp = split_info(a.seq_lens, a.B, cap, chunk, s);
+        const Split sp = split_info(seql, a.B, cap, chunk, s);
         const int b = sp.b;
-        const int L = a.seq_lens[b];
+        const int L = seql[b];
         const int nst = sp.g1 - sp.g0;
         const int pg0 = sp.g0 >> 3;
         const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
@@ -533,71 +550,110 @@ __global__ void __launch_bounds__(256, 1)
 
 // ------------------------------------------------------------------ kernel 2
 // Log-sum-exp merge of a sequence's partials, residual up-projection, bf16 store.
-// grid (H, B), 256 threads; one head's partials are contiguous in the workspace.
+// grid (H, B), 1024 threads = NSL partial slices x W columns.  Each slice merges
+// its own partials (all loads issued together), then the slices are merged in
+// shared memory; the B_h^V row of each output column is prefetched up front.
 template <int D_H, int R>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a, int G) {
+__global__ void __launch_bounds__(1024) decode_combine_kernel(const DecodeArgs a, int G) {
     constexpr int W = D_H + R;
+    constexpr int NSL = 1024 / W;     // slices
+    constexpr int PPS = 8;            // partials a slice loads per round
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int H = a.H;
     const int cap = a.max_pages * kBlockSize;
-    __shared__ float wsh[kMaxCombine];
-    __shared__ float red[8];
-    __shared__ float cacc[W];
+    __shared__ float sm_m[NSL], sm_l[NSL];
+    __shared__ float sm_acc[NSL][W];
+    __shared__ int slc[kSeqCache];
+    const int sl = tid / W, c = tid - (tid / W) * W;
+
+    // B_h^V row of output column c (prefetched while the partials are loaded)
+    uint4 bvr[R / 8];
+    if (tid < D_H) {
+        const uint4* bv = reinterpret_cast<const uint4*>(a.BV + ((size_t)h * D_H + tid) * R);
+#pragma unroll
+        for (int i = 0; i < R / 8; ++i) bvr[i] = __ldg(bv + i);
+    }
+    stage_seq_lens(slc, a.seq_lens, a.B, tid, 1024);
+    __syncthreads();
+    const SeqLens seql{a.seq_lens, slc};
     pdl_wait();
     uint16_t* dst = a.out + ((size_t)b * H + h) * D_H;
-    const int L = a.seq_lens[b];
+    const int L = seql[b];
     if (L < 1 || L > cap) {
         if (tid == 0 && h == 0) set_status(a.status, LRKV_DEV_BAD_SEQLEN);
         if (tid < D_H) dst[tid] = 0;
         return;
     }
     int nsplits;
-    const int chunk = partition_chunk(a.seq_lens, a.B, cap, G, &nsplits);
+    const int chunk = partition_chunk(seql, a.B, cap, G, &nsplits);
     int first, np;
-    seq_splits(a.seq_lens, a.B, cap, chunk, b, &first, &np);
+    seq_splits(seql, a.B, cap, chunk, b, &first, &np);
     const float* pml = a.part_ml + ((size_t)h * a.pmax + first) * 2;
     const float* pacc = a.part_acc + ((size_t)h * a.pmax + first) * W;
 
-    float mloc = -INFINITY;
-    for (int p = tid; p < np; p += 256) mloc = fmaxf(mloc, pml[2 * p]);
-    for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
-    if ((tid & 31) == 0) red[tid >> 5] = mloc;
-    __syncthreads();
-    float M = red[0];
+    if (sl < NSL) {
+        float m = -INFINITY, l = 0.f, v = 0.f;
+        for (int p0 = sl; p0 < np; p0 += NSL * PPS) {
+            float2 ml[PPS];
+            float x[PPS];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) M = fmaxf(M, red[i]);
-    __syncthreads();
-    float lloc = 0.f;
-    for (int p = tid; p < np; p += 256) {
-        const float2 ml = *reinterpret_cast<const float2*>(pml + 2 * p);
-        const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-        wsh[p] = w;
-        lloc = fmaf(w, ml.y, lloc);
-    }
-    for (int off = 16; off > 0; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
-    if ((tid & 31) == 0) red[tid >> 5] = lloc;
-    __syncthreads();
-    float lsum = 0.f;
+            for (int u = 0; u < PPS; ++u) {
+                const int p = p0 + u * NSL;
+                ml[u] = p < np ? *reinterpret_cast<const float2*>(pml + 2 * p) : make_float2(-INFINITY, 0.f);
+                x[u] = p < np ? pacc[(size_t)p * W + c] : 0.f;
+            }
+            float mn = m;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) lsum += red[i];
-
-    if (tid < W) {
-        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        int p = 0;
-        for (; p + 8 <= np; p += 8) {
+            for (int u = 0; u < PPS; ++u) mn = fmaxf(mn, ml[u].x);
+            if (mn != -INFINITY) {
+                const float sc = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+                l *= sc;
+                v *= sc;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = fmaf(wsh[p + u], pacc[(size_t)(p + u) * W + tid], v[u]);
+                for (int u = 0; u < PPS; ++u) {
+                    const float w = (ml[u].x == -INFINITY) ? 0.f : exp2f(ml[u].x - mn);
+                    l = fmaf(w, ml[u].y, l);
+                    v = fmaf(w, x[u], v);
+                }
+                m = mn;
+            }
         }
-        for (; p < np; ++p) v[0] = fmaf(wsh[p], pacc[(size_t)p * W + tid], v[0]);
-        cacc[tid] = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+        sm_acc[sl][c] = v;
+        if (c == 0) {
+            sm_m[sl] = m;
+            sm_l[sl] = l;
+        }
+    }
+    __syncthreads();
+    if (tid < W) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NSL; ++i) M = fmaxf(M, sm_m[i]);
+        float lsum = 0.f, v = 0.f;
+#pragma unroll
+        for (int i = 0; i < NSL; ++i) {
+            const float w = (sm_m[i] == -INFINITY) ? 0.f : exp2f(sm_m[i] - M);
+            lsum = fmaf(w, sm_l[i], lsum);
+            v = fmaf(w, sm_acc[i][tid], v);
+        }
+        // each thread reads only its own column, so slice 0's slot can take the result
+        sm_acc[0][tid] = lsum > 0.f ? v / lsum : 0.f;
     }
     __syncthreads();
     if (tid < D_H) {
-        float v = cacc[tid];
-        const uint16_t* bv = a.BV + ((size_t)h * D_H + tid) * R;
+        float v = sm_acc[0][tid];
 #pragma unroll
-        for (int j = 0; j < R; ++j) v = fmaf(__uint_as_float((uint32_t)bv[j] << 16), cacc[D_H + j], v);
-        v = lsum > 0.f ? v / lsum : 0.f;
+        for (int i = 0; i < R / 8; ++i) {
+            const uint4 q = bvr[i];
+            v = fmaf(bf16lo(q.x), sm_acc[0][D_H + i * 8 + 0], v);
+            v = fmaf(bf16hi(q.x), sm_acc[0][D_H + i * 8 + 1], v);
+            v = fmaf(bf16lo(q.y), sm_acc[0][D_H + i * 8 + 2], v);
+            v = fmaf(bf16hi(q.y), sm_acc[0][D_H + i * 8 + 3], v);
+            v = fmaf(bf16lo(q.z), sm_acc[0][D_H + i * 8 + 4], v);
+            v = fmaf(bf16hi(q.z), sm_acc[0][D_H + i * 8 + 5], v);
+            v = fmaf(bf16lo(q.w), sm_acc[0][D_H + i * 8 + 6], v);
+            v = fmaf(bf16hi(q.w), sm_acc[0][D_H + i * 8 + 7], v);
+        }
         const __nv_bfloat16 ob = __float2bfloat16_rn(v);
         dst[tid] = *reinterpret_cast<const uint16_t*>(&ob);
     }
@@ -609,7 +665,8 @@ struct DecodePlan {
 };
 
 static int decode_fixed_smem(int ncw, int nslot) {
-    return nslot * 8 + ((4 * nslot + 3) & ~3) * 4 + kPageCache * 4 + ncw * kScratchFloats * 4 + 16 + 1024;
+    return nslot * 8 + ((4 * nslot + 3) & ~3) * 4 + (kPageCache + kSeqCache) * 4 + ncw * kScratchFloats * 4 + 16 +
+           1024;
 }
 
 DecodePlan decode_plan(int H, int D_H, int R, int smem_limit) {
@@ -675,12 +732,11 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
     if (e != cudaSuccess) return e;
     e = launch_pdl(split, dim3(G), dim3(p.threads), p.smem_bytes, stream, tK, tV, a);
     if (e != cudaSuccess) return e;
-    return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, a.B), dim3(256), 0, stream, a, G);
+    return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, a.B), dim3(1024), 0, stream, a, G);
 }
 
 cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int G,
                           int smem_limit, cudaStream_t stream) {
-    if (G > kMaxCombine) return cudaErrorInvalidConfiguration;
     const DecodePlan p = decode_plan(a.H, D_H, R, smem_limit);
     a.ng = p.ng;
     a.nslot = p.nslot;
