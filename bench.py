@@ -1,18 +1,25 @@
 #!/usr/bin/env python
-"""Benchmark of the LRKV decode step on the long-context workload.
+"""Benchmark of the LRKV hot path on GB300.
 
-A step is one pass of the hot path for one batch: lrkv_append writes the newest
-token's compressed row (s^K, s^V, z^K, z^V) of each sequence into the paged
-cache, then lrkv_decode attends each sequence's query over its whole cache
-(q~ absorption, split-K scan with online softmax, log-sum-exp combine and the
-B^V up-projection).  Workload: d=4096, H=32, d_h=128, r=32, batch 4, cached
-lengths uniform on [16384, 32768] (seeded), 64-token pages in a permuted pool.
+Default workload ("longctx"): the long-context decode step.  A step is one
+pass of the hot path for one batch: lrkv_append writes the newest token's
+compressed row (s^K, s^V, z^K, z^V) of each sequence into the paged cache, then
+lrkv_decode attends each sequence's query over its whole cache (q~ absorption,
+split-K scan with online softmax, log-sum-exp combine, B^V up-projection).
+d=4096, H=32, d_h=128, r=32, batch 4, cached lengths uniform on [16384, 32768]
+(seeded), 64-token pages in a permuted pool.  value = algorithmic bytes of the
+step (cache rows read, B^K/B^V, q in, out, plus the append's weights, hidden
+rows and new cache rows) / device time of the step, in GB/s.
 
-Prints one JSON line.  value = algorithmic bytes of the step (cache rows read,
-B^K/B^V, q in, out, plus the append's weights, hidden rows and new cache rows)
-divided by the device time of the step.
+Other workloads (--workload): "dsv2" (H=128, d_h=128, r=16, d=16384, batch 8,
+8192 tokens), "backbone12" (12 layers of d=512, H=8, d_h=64, r=16, batch 16,
+2048 tokens), "small" (the single-layer parity case) -- decode steps as above;
+"prefill": causal chunked prefill plus cache append (d=4096, H=32, d_h=128,
+r=16, batch 2, 4096-token prompts in 512-token chunks), value in prompt
+tokens/s with the tensor roofline of the prefill kernel.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lrkv|reference]
+Prints one JSON line.
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lrkv|reference] [--workload NAME]
 """
 from __future__ import annotations
 
@@ -35,53 +42,40 @@ import numpy as np  # noqa: E402
 import lrkv_synth as S  # noqa: E402
 from compressed_kv_cache_lrkv_gb300 import accounting as A  # noqa: E402
 
-METRIC = "LRKV decode cache-read GB/s (% of GB300 HBM peak) and decode tokens/sec"
-WORKLOAD = "longctx"
-FALLBACK_HBM_GBS = 6800.0
+METRIC_DECODE = "LRKV decode cache-read GB/s (% of GB300 HBM peak) and decode tokens/sec"
+METRIC_PREFILL = "LRKV chunked prefill + append prompt tokens/sec (bf16 tensor TFLOP/s of the prefill kernel)"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
-
-
-def workload_dims():
-    wl = S.WORKLOADS[WORKLOAD]
-    seq_lens = S.uniform_int(wl.seed, "seq_lens", wl.B, wl.L_min, wl.L).astype(np.int32)
-    return wl, seq_lens
-
-
-def step_bytes(wl, seq_lens):
-    dec = A.decode_algorithmic_bytes(wl.H, wl.d_h, wl.r, seq_lens)
-    app = A.append_algorithmic_bytes(wl.B, wl.d, wl.H, wl.d_h, wl.r)
-    return dec, app
+CSRC = os.path.join(ROOT, "compressed_kv_cache_lrkv_gb300", "csrc")
 
 
 def measured_peaks():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
-        with open(p) as f:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             j = json.load(f)
-        return float(j["hbm_gbs"]), "measured"
+        return {k: float(j[k]) for k in FALLBACK}, "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return dict(FALLBACK), "fallback"
 
 
-def kernel_source_hash():
+def source_hash(names):
     h = hashlib.sha256()
-    for name in ("decode.cu", "lrkv_internal.cuh", "kernels.h"):
-        with open(os.path.join(ROOT, "compressed_kv_cache_lrkv_gb300", "csrc", name), "rb") as f:
+    for name in names:
+        with open(os.path.join(CSRC, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
-    on the current decode kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "decode_split_longctx.md")
+def recorded_traffic(profile_name, sources):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
     try:
-        txt = open(p).read()
+        txt = open(os.path.join(ROOT, "profiles", profile_name)).read()
     except OSError:
         return None
     mh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
     mt = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
-    if not mh or not mt or mh.group(1) != kernel_source_hash():
+    if not mh or not mt or mh.group(1) != source_hash(sources):
         return None
     return int(mt.group(1))
 
@@ -106,8 +100,7 @@ class ClockSampler:
         except OSError:
             self.proc = None
             return
-        self.t = threading.Thread(target=self._read, daemon=True)
-        self.t.start()
+        threading.Thread(target=self._read, daemon=True).start()
         t0 = time.time()
         while not self.lines and time.time() - t0 < 5:
             time.sleep(0.05)
@@ -128,8 +121,6 @@ class ClockSampler:
         rows = [l for (t, l) in self.lines if (t0 is None or t >= t0) and (t1 is None or t <= t1)]
         if not rows:
             rows = [l for (_, l) in self.lines]
-        if not rows:
-            return None
         sm, smax, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -148,142 +139,278 @@ class ClockSampler:
 
 
 def dist_setup():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return world, rank, local
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def cpu_baseline_sample(wl, seq_lens, budget_s: float):
-    """Time the fp64 oracle (E2 decode, all heads) on the workload's first sequence,
-    repeated until about budget_s seconds have passed; returns the baseline dict."""
-    import oracle
-
-    o = oracle.get()
-    tokens = int(seq_lens[0])
-    pt = S.page_table(wl.seed, [tokens], 64)
-    pools = tuple(S.gaussian_bf16(wl.seed, n, shp) for n, shp in
-                  [("bl_sK", (pt.num_blocks, 64, wl.d_h)), ("bl_sV", (pt.num_blocks, 64, wl.d_h)),
-                   ("bl_zK", (pt.num_blocks, 64, wl.H, wl.r)), ("bl_zV", (pt.num_blocks, 64, wl.H, wl.r))])
-    BK = S.gaussian_bf16(wl.seed, "bl_BK", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
-    BV = S.gaussian_bf16(wl.seed, "bl_BV", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
-    q = S.gaussian_bf16(wl.seed, "bl_q", (1, wl.H, wl.d_h))
-    reps = 0
-    t0 = time.perf_counter()
-    while True:
-        o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
-        reps += 1
-        dt = time.perf_counter() - t0
-        if dt >= budget_s:
-            break
-    nbytes = A.decode_algorithmic_bytes(wl.H, wl.d_h, wl.r, [tokens]) * reps
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
-            "sample": f"E2 decode of the workload's first sequence ({tokens} cached tokens, all {wl.H} heads), "
-                      f"{reps} repetitions in {dt:.1f} s; fp64, OpenMP over heads"}
+def workload_seq_lens(wl):
+    if wl.ragged:
+        return S.uniform_int(wl.seed, "seq_lens", wl.B, wl.L_min, wl.L).astype(np.int32)
+    return np.full(wl.B, wl.L, np.int32)
 
 
-def run_reference(args, world, rank):
-    """--impl reference: the fp64 oracle on the host cores, bounded sample per step."""
-    wl, seq_lens = workload_dims()
-    if rank != 0:
-        print(json.dumps({"impl": "reference", "rank": rank, "skipped": True}), file=sys.stderr)
-        return
-    import oracle
+# ----------------------------------------------------------------------------- decode
+class DecodeHarness:
+    """Per layer: lrkv_append of each sequence's newest row, then lrkv_decode."""
 
-    o = oracle.get()
-    total_steps = args.steps + args.warmup
-    per_step_budget = max(0.01, 90.0 / max(total_steps, 1))
-    # calibrate tokens per step
-    probe = 256
-    pt = S.page_table(wl.seed, [probe], 64)
+    profile = "decode_split_longctx.md"
+    sources = ("decode.cu", "lrkv_internal.cuh", "kernels.h")
 
-    def inputs(tokens):
+    def __init__(self, wl, rank):
+        import torch
+
+        from compressed_kv_cache_lrkv_gb300 import binding as b
+        self.torch, self.b, self.wl = torch, b, wl
+        B, H, d_h, r, d = wl.B, wl.H, wl.d_h, wl.r, wl.d
+        self.seq_lens = workload_seq_lens(wl)
+        self.pt = S.page_table(wl.seed, self.seq_lens, 64)
+        nb = self.pt.num_blocks
+        gen = torch.Generator(device="cuda").manual_seed(1234 + rank)
+        rn = lambda *s, scale=1.0: (torch.randn(*s, generator=gen, device="cuda") * scale).to(torch.bfloat16)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+        self.dims = b.make_dims(H, d_h, r, d)
+        self.layers = []
+        for _ in range(wl.layers):
+            self.layers.append(dict(
+                cache=b.PagedCache(rn(nb, 64, d_h), rn(nb, 64, d_h), rn(nb, 64, H, r), rn(nb, 64, H, r)),
+                q=rn(B, H, d_h), BK=rn(H, d_h, r, scale=r ** -0.5), BV=rn(H, d_h, r, scale=r ** -0.5),
+                wcat=rn(2 * (d_h + H * r), d, scale=d ** -0.5), x=rn(B, d),
+                out=torch.empty(B, H, d_h, dtype=torch.bfloat16, device="cuda")))
+        self.bt = i32(self.pt.block_table)
+        self.sl = i32(self.pt.seq_lens)
+        self.slots = i32([self.pt.slot(i, int(L) - 1) for i, L in enumerate(self.seq_lens)])
+        self.ws = b.alloc_workspace(b.decode_workspace_bytes(self.dims, B))
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.cache_bytes = wl.layers * sum(t.numel() * t.element_size() for t in self.layers[0]["cache"].tensors())
+        dec = A.decode_algorithmic_bytes(H, d_h, r, self.seq_lens, layers=wl.layers)
+        app = wl.layers * A.append_algorithmic_bytes(B, d, H, d_h, r)
+        self.kernel_units = dec          # algorithmic bytes of the timed kernel calls
+        self.step_units = dec + app      # algorithmic bytes of a step
+        self.launches_per_step = wl.layers * 4
+
+    def step(self, stream):
+        b = self.b
+        for L in self.layers:
+            b.lrkv_append(self.dims, L["x"], L["wcat"], self.slots, L["cache"], status=self.status, stream=stream)
+            b.lrkv_decode(self.dims, L["q"], L["BK"], L["BV"], L["cache"], self.bt, self.sl, L["out"], self.ws,
+                          status=self.status, stream=stream)
+
+    def kernel(self, stream):
+        for L in self.layers:
+            self.b.lrkv_decode(self.dims, L["q"], L["BK"], L["BV"], L["cache"], self.bt, self.sl, L["out"], self.ws,
+                               status=self.status, stream=stream)
+
+    def e2e_setup(self):
+        t = self.torch
+        self.h_in = [(L["x"].cpu().pin_memory(), L["x"]) for L in self.layers] + \
+                    [(L["q"].cpu().pin_memory(), L["q"]) for L in self.layers] + \
+                    [(self.slots.cpu().pin_memory(), self.slots), (self.sl.cpu().pin_memory(), self.sl)]
+        self.h_out = [(t.empty_like(L["out"], device="cpu").pin_memory(), L["out"]) for L in self.layers]
+        return (sum(h.numel() * h.element_size() for h, _ in self.h_in),
+                sum(h.numel() * h.element_size() for h, _ in self.h_out))
+
+    def e2e_step(self, stream):
+        for h, d in self.h_in:
+            d.copy_(h, non_blocking=True)
+        self.step(stream)
+        for h, d in self.h_out:
+            h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    def report(self, step_s, kernel_s, e2e_s, world, peaks):
+        wl = self.wl
+        value = self.step_units * world / step_s / 1e9
+        achieved = self.kernel_units / kernel_s / 1e9
+        return {
+            "metric": METRIC_DECODE, "value": value, "unit": "GB/s",
+            "tokens_per_s": wl.B * world / step_s, "pct_of_hbm_peak": 100.0 * value / peaks["hbm_gbs"],
+            "config": {"workload": f"{wl.key}: {wl.description}", "B": wl.B,
+                       "seq_lens": [int(x) for x in self.seq_lens], "layers": wl.layers, "H": wl.H, "d_h": wl.d_h,
+                       "r": wl.r, "d": wl.d, "block_size": 64, "pages_per_layer": int(self.pt.num_blocks),
+                       "cache_bytes": int(self.cache_bytes),
+                       "l2": (f"inputs larger than L2: cache {self.cache_bytes / 2**20:.0f} MiB vs L2 "
+                              f"{L2_BYTES / 2**20:.0f} MiB") if self.cache_bytes > L2_BYTES else
+                             "cache fits in L2 (parity-sized workload; not an HBM measurement)",
+                       "step": "per layer: lrkv_append (1 row per sequence) + lrkv_decode",
+                       "parallelism": f"replicas x{world} (independent batches)"},
+            "roofline": {"kernel": "lrkv_decode (absorb + split + combine kernels)", "bound": "hbm",
+                         "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic(self.profile, self.sources) if wl.key == "longctx" else None,
+                         "algorithmic_bytes_per_launch": self.kernel_units // wl.layers,
+                         "avg_launch_ms": kernel_s * 1e3 / wl.layers},
+            "e2e_unit_value": lambda s: self.step_units * world / s / 1e9, "e2e_unit": "GB/s",
+        }
+
+    def cpu_baseline(self, budget_s):
+        """fp64 oracle (E2 decode, all heads) on the first sequence, repeated ~budget_s."""
+        import oracle
+        wl = self.wl
+        o = oracle.get()
+        tokens = int(self.seq_lens[0])
         pt = S.page_table(wl.seed, [tokens], 64)
         pools = tuple(S.gaussian_bf16(wl.seed, n, shp) for n, shp in
-                      [("rf_sK", (pt.num_blocks, 64, wl.d_h)), ("rf_sV", (pt.num_blocks, 64, wl.d_h)),
-                       ("rf_zK", (pt.num_blocks, 64, wl.H, wl.r)), ("rf_zV", (pt.num_blocks, 64, wl.H, wl.r))])
-        BK = S.gaussian_bf16(wl.seed, "rf_BK", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
-        BV = S.gaussian_bf16(wl.seed, "rf_BV", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
-        q = S.gaussian_bf16(wl.seed, "rf_q", (1, wl.H, wl.d_h))
-        return pt, pools, BK, BV, q
-
-    pt, pools, BK, BV, q = inputs(probe)
-    t0 = time.perf_counter()
-    o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
-    rate = probe / max(time.perf_counter() - t0, 1e-6)
-    tokens = int(max(64, min(int(seq_lens[0]), rate * per_step_budget)) // 64 * 64) or 64
-    pt, pools, BK, BV, q = inputs(tokens)
-    for _ in range(args.warmup):
-        o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
-    dt = (time.perf_counter() - t0) / max(args.steps, 1)
-    nbytes = A.decode_algorithmic_bytes(wl.H, wl.d_h, wl.r, [tokens])
-    val = nbytes / dt / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": S.WORKLOADS[WORKLOAD].description, "B": 1, "tokens_per_step": tokens,
-                       "H": wl.H, "d_h": wl.d_h, "r": wl.r},
-            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
-                             "sample": f"E2 decode, one sequence, first {tokens} tokens, all heads, per step"},
-            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line))
+                      [("bl_sK", (pt.num_blocks, 64, wl.d_h)), ("bl_sV", (pt.num_blocks, 64, wl.d_h)),
+                       ("bl_zK", (pt.num_blocks, 64, wl.H, wl.r)), ("bl_zV", (pt.num_blocks, 64, wl.H, wl.r))])
+        BK = S.gaussian_bf16(wl.seed, "bl_BK", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
+        BV = S.gaussian_bf16(wl.seed, "bl_BV", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
+        q = S.gaussian_bf16(wl.seed, "bl_q", (1, wl.H, wl.d_h))
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget_s:
+                break
+        nbytes = A.decode_algorithmic_bytes(wl.H, wl.d_h, wl.r, [tokens]) * reps
+        return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
+                "sample": f"E2 decode of the workload's first sequence ({tokens} cached tokens, all {wl.H} heads, "
+                          f"one layer), {reps} repetitions in {dt:.1f} s; fp64, OpenMP over heads"}
 
 
+# ----------------------------------------------------------------------------- prefill
+class PrefillHarness:
+    """Per 512-token chunk: lrkv_append of both sequences' rows, then lrkv_prefill."""
+
+    profile = "prefill_chunked.md"
+    sources = ("prefill.cu", "lrkv_internal.cuh", "kernels.h")
+
+    def __init__(self, wl, rank):
+        import torch
+
+        from compressed_kv_cache_lrkv_gb300 import binding as b
+        self.torch, self.b, self.wl = torch, b, wl
+        B, H, d_h, r, d, T, C = wl.B, wl.H, wl.d_h, wl.r, wl.d, wl.L, wl.chunk
+        self.pt = S.page_table(wl.seed, [T] * B, 64)
+        nb = self.pt.num_blocks
+        gen = torch.Generator(device="cuda").manual_seed(4321 + rank)
+        rn = lambda *s, scale=1.0: (torch.randn(*s, generator=gen, device="cuda") * scale).to(torch.bfloat16)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+        self.dims = b.make_dims(H, d_h, r, d)
+        self.cache = b.PagedCache.empty(nb, H, d_h, r)
+        self.BK, self.BV = rn(H, d_h, r, scale=r ** -0.5), rn(H, d_h, r, scale=r ** -0.5)
+        self.wcat = rn(2 * (d_h + H * r), d, scale=d ** -0.5)
+        self.bt = i32(self.pt.block_table)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.chunks = []
+        for c0 in range(0, T, C):
+            self.chunks.append(dict(
+                x=rn(B * C, d),  # both sequences' rows of this chunk
+                slots=i32(np.concatenate([S.slots_for(self.pt, bb, c0, c0 + C) for bb in range(B)])),
+                q=rn(B, C, H, d_h), qs=i32([c0] * B),
+                out=torch.empty(B, C, H, d_h, dtype=torch.bfloat16, device="cuda")))
+        app = A.append_flops(B * T, d, H, d_h, r)
+        pre = sum(A.prefill_flops(B, C, H, d_h, r, q_start=c0) for c0 in range(0, T, C))
+        self.kernel_units = pre
+        self.step_units = app + pre
+        self.app_flops = app
+        self.launches_per_step = 2 * len(self.chunks)
+
+    def step(self, stream):
+        b = self.b
+        for ch in self.chunks:
+            b.lrkv_append(self.dims, ch["x"], self.wcat, ch["slots"], self.cache, status=self.status, stream=stream)
+            b.lrkv_prefill(self.dims, ch["q"], self.BK, self.BV, self.cache, self.bt, ch["qs"], ch["out"],
+                           status=self.status, stream=stream)
+
+    def kernel(self, stream):
+        for ch in self.chunks:
+            self.b.lrkv_prefill(self.dims, ch["q"], self.BK, self.BV, self.cache, self.bt, ch["qs"], ch["out"],
+                                status=self.status, stream=stream)
+
+    def e2e_setup(self):
+        t = self.torch
+        self.h_in = [(ch[k].cpu().pin_memory(), ch[k]) for ch in self.chunks for k in ("x", "q")]
+        self.h_out = [(t.empty_like(ch["out"], device="cpu").pin_memory(), ch["out"]) for ch in self.chunks]
+        return (sum(h.numel() * h.element_size() for h, _ in self.h_in),
+                sum(h.numel() * h.element_size() for h, _ in self.h_out))
+
+    def e2e_step(self, stream):
+        for h, d in self.h_in:
+            d.copy_(h, non_blocking=True)
+        self.step(stream)
+        for h, d in self.h_out:
+            h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    def report(self, step_s, kernel_s, e2e_s, world, peaks):
+        wl = self.wl
+        tokens = wl.B * wl.L * world
+        achieved = self.kernel_units / kernel_s / 1e12
+        return {
+            "metric": METRIC_PREFILL, "value": tokens / step_s, "unit": "tokens/s",
+            "step_tflops": self.step_units * world / step_s / 1e12,
+            "config": {"workload": f"{wl.key}: {wl.description}", "B": wl.B, "prompt": wl.L, "chunk": wl.chunk,
+                       "H": wl.H, "d_h": wl.d_h, "r": wl.r, "d": wl.d, "block_size": 64,
+                       "l2": "prompt activations (X, q, out: 192 MiB) larger than L2",
+                       "step": "per 512-token chunk: lrkv_append (1024 rows) + lrkv_prefill",
+                       "flops_per_step": self.step_units, "append_flops": self.app_flops,
+                       "prefill_flops": self.kernel_units,
+                       "parallelism": f"replicas x{world} (independent batches)"},
+            "roofline": {"kernel": "lrkv_prefill (8 chunk launches)", "bound": "tensor", "achieved": achieved,
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                         "traffic": None, "algorithmic_flops_per_launch": self.kernel_units / len(self.chunks),
+                         "avg_launch_ms": kernel_s * 1e3 / len(self.chunks)},
+            "e2e_unit_value": lambda s: tokens / s, "e2e_unit": "tokens/s",
+        }
+
+    def cpu_baseline(self, budget_s):
+        """fp64 oracle (E2 causal prefill, all heads) on the first chunk of one sequence."""
+        import oracle
+        wl = self.wl
+        o = oracle.get()
+        C = wl.chunk
+        pt = S.page_table(wl.seed, [C], 64)
+        pools = tuple(S.gaussian_bf16(wl.seed, n, shp) for n, shp in
+                      [("bl_sK", (pt.num_blocks, 64, wl.d_h)), ("bl_sV", (pt.num_blocks, 64, wl.d_h)),
+                       ("bl_zK", (pt.num_blocks, 64, wl.H, wl.r)), ("bl_zV", (pt.num_blocks, 64, wl.H, wl.r))])
+        BK = S.gaussian_bf16(wl.seed, "bl_BK", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
+        BV = S.gaussian_bf16(wl.seed, "bl_BV", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
+        q = S.gaussian_bf16(wl.seed, "bl_q", (1, C, wl.H, wl.d_h))
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            o.prefill_cache(pools, pt.block_table, [0], BK, BV, q)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget_s:
+                break
+        return {"value": C * reps / dt, "unit": "tokens/s", "cores": o.num_threads(), "kind": "oracle",
+                "sample": f"E2 causal prefill of one sequence's first {C}-token chunk (all {wl.H} heads), "
+                          f"{reps} repetitions in {dt:.1f} s; fp64, OpenMP over heads"}
+
+
+HARNESS = {"longctx": DecodeHarness, "dsv2": DecodeHarness, "backbone12": DecodeHarness, "small": DecodeHarness,
+           "prefill": PrefillHarness}
+
+
+# ----------------------------------------------------------------------------- arms
 def run_gpu(args, world, rank, local):
     import torch
-
-    from compressed_kv_cache_lrkv_gb300 import binding as b
 
     torch.cuda.set_device(local)
     dist = None
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    wl, seq_lens = workload_dims()
-    B, H, d_h, r, d = wl.B, wl.H, wl.d_h, wl.r, wl.d
-    pt = S.page_table(wl.seed, seq_lens, 64)
-    nb = pt.num_blocks
-    gen = torch.Generator(device="cuda").manual_seed(1234 + rank)
-    randn = lambda *s, scale=1.0: (torch.randn(*s, generator=gen, device="cuda") * scale).to(torch.bfloat16)
-    cache = b.PagedCache(randn(nb, 64, d_h), randn(nb, 64, d_h), randn(nb, 64, H, r), randn(nb, 64, H, r))
-    q = randn(B, H, d_h)
-    BK = randn(H, d_h, r, scale=r ** -0.5)
-    BV = randn(H, d_h, r, scale=r ** -0.5)
-    wcat = randn(2 * (d_h + H * r), d, scale=d ** -0.5)
-    x_new = randn(B, d)
-    dev_i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
-    bt = dev_i32(pt.block_table)
-    sl = dev_i32(pt.seq_lens)
-    slots = dev_i32([pt.slot(i, int(L) - 1) for i, L in enumerate(seq_lens)])
-    dims = b.make_dims(H, d_h, r, d)
-    out = torch.empty(B, H, d_h, dtype=torch.bfloat16, device="cuda")
-    ws = b.alloc_workspace(b.decode_workspace_bytes(dims, B))
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wl = S.WORKLOADS[args.workload]
+    hz = HARNESS[args.workload](wl, rank)
     stream = torch.cuda.current_stream()
-    cache_bytes = sum(t.numel() * t.element_size() for t in cache.tensors())
 
-    def step():
-        b.lrkv_append(dims, x_new, wcat, slots, cache, status=status, stream=stream)
-        b.lrkv_decode(dims, q, BK, BV, cache, bt, sl, out, ws, status=status, stream=stream)
-
-    # The timed step is a CUDA graph of the two public calls, so host launch overhead
-    # stays out of the device-timed region; a second graph holds lrkv_decode alone.
+    # Each timed step is one replay of a CUDA graph of the public calls, so host
+    # launch overhead stays out of the device-timed region; a second graph holds
+    # only the dominant call (lrkv_decode / lrkv_prefill) for the roofline.
     for _ in range(3):
-        step()
+        hz.step(stream)
     torch.cuda.synchronize()
-    g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    cap_stream = torch.cuda.Stream()
-    cap_stream.wait_stream(stream)
-    with torch.cuda.stream(cap_stream):
-        with torch.cuda.graph(g_step, stream=cap_stream):
-            b.lrkv_append(dims, x_new, wcat, slots, cache, status=status, stream=cap_stream)
-            b.lrkv_decode(dims, q, BK, BV, cache, bt, sl, out, ws, status=status, stream=cap_stream)
-        with torch.cuda.graph(g_dec, stream=cap_stream):
-            b.lrkv_decode(dims, q, BK, BV, cache, bt, sl, out, ws, status=status, stream=cap_stream)
-    stream.wait_stream(cap_stream)
+    g_step, g_ker = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g_step, stream=cap):
+            hz.step(cap)
+        with torch.cuda.graph(g_ker, stream=cap):
+            hz.kernel(cap)
+    stream.wait_stream(cap)
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
@@ -295,95 +422,111 @@ def run_gpu(args, world, rank, local):
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for k in range(args.steps):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
         g_step.replay()
-    end.record(stream)
+    e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    total_ms = start.elapsed_time(end)
-    # lrkv_decode alone (absorb + split + combine kernels), same workload, same stream
-    d0 = torch.cuda.Event(enable_timing=True)
-    d1 = torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    for k in range(args.steps):
-        g_dec.replay()
-    d1.record(stream)
+    step_s = e0.elapsed_time(e1) * 1e-3 / args.steps
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    for _ in range(args.steps):
+        g_ker.replay()
+    k1.record(stream)
     torch.cuda.synchronize()
-    dec_avg_ms = d0.elapsed_time(d1) / args.steps
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item()):#x}")
+    kernel_s = k0.elapsed_time(k1) * 1e-3 / args.steps
+    if int(hz.status.item()) != 0:
+        raise RuntimeError(f"device status {int(hz.status.item()):#x}")
 
-    # end to end through the public API with host buffers (pinned), copies in the timed region
-    x_h = x_new.cpu().pin_memory()
-    q_h = q.cpu().pin_memory()
-    slots_h = slots.cpu().pin_memory()
-    sl_h = sl.cpu().pin_memory()
-    out_h = torch.empty_like(out, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (x_h, q_h, slots_h, sl_h))
-    d2h = out_h.numel() * out_h.element_size()
-    e2e_steps = max(1, min(args.steps, 500))
+    # end to end through the public API with pinned host buffers, copies in the timed region
+    h2d, d2h = hz.e2e_setup()
+    e2e_steps = max(1, min(args.steps, 200))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        x_new.copy_(x_h, non_blocking=True)
-        q.copy_(q_h, non_blocking=True)
-        slots.copy_(slots_h, non_blocking=True)
-        sl.copy_(sl_h, non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
-        stream.synchronize()
+        hz.e2e_step(stream)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     sampler.stop()
 
-    step_ms = total_ms / args.steps
     if dist:
-        t = torch.tensor([step_ms, e2e_s], device="cuda", dtype=torch.float64)
+        t = torch.tensor([step_s, kernel_s, e2e_s], device="cuda", dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, e2e_s = float(t[0]), float(t[1])
+        step_s, kernel_s, e2e_s = (float(x) for x in t)
     if rank != 0:
         dist.destroy_process_group()
         return
-    dec_bytes, app_bytes = step_bytes(wl, seq_lens)
-    bytes_step = (dec_bytes + app_bytes) * world
-    value = bytes_step / (step_ms * 1e-3) / 1e9
-    peak, peak_kind = measured_peaks()
-    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic()
+    peaks, peak_kind = measured_peaks()
+    rep = hz.report(step_s, kernel_s, e2e_s, world, peaks)
+    e2e_fn, e2e_unit = rep.pop("e2e_unit_value"), rep.pop("e2e_unit")
+    rep["roofline"]["peak_kind"] = peak_kind
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline_sample(wl, seq_lens, budget_s=15.0)
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: {wl.description}", "B": B, "seq_lens": [int(x) for x in seq_lens],
-                   "H": H, "d_h": d_h, "r": r, "d": d, "block_size": 64, "pages": int(nb),
-                   "cache_bytes": int(cache_bytes),
-                   "l2": f"inputs larger than L2: cache {cache_bytes / 2**20:.0f} MiB vs L2 {L2_BYTES / 2**20:.0f} MiB",
-                   "step": "lrkv_append (1 row per sequence) + lrkv_decode",
-                   "parallelism": f"replicas x{world} (independent batches)"},
-        "tokens_per_s": B * world / (step_ms * 1e-3),
-        "pct_of_hbm_peak": 100.0 * value / peak,
-        "roofline": {"kernel": "lrkv_decode (absorb + split + combine kernels)", "bound": "hbm", "achieved": achieved,
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "algorithmic_bytes_per_launch": dec_bytes,
-                     "avg_launch_ms": dec_avg_ms},
-        "cpu_baseline": cpu,
-        "e2e": {"value": bytes_step / e2e_s / 1e9, "unit": "GB/s", "ms_per_step": e2e_s * 1e3,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": 4 * args.steps,
-        "timing": "each step is one replay of a CUDA graph holding lrkv_append + lrkv_decode",
-        "clocks": sampler.summary(t_wall0 - 0.3, t_wall1 + 0.3),
-    }
+        cpu = hz.cpu_baseline(budget_s=15.0)
+    line = {"metric": rep.pop("metric"), "value": rep.pop("value"), "unit": rep.pop("unit"), "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
+    line.update(rep)
+    line["cpu_baseline"] = cpu
+    line["e2e"] = {"value": e2e_fn(e2e_s), "unit": e2e_unit, "ms_per_step": e2e_s * 1e3,
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+    line["gpu_launches"] = hz.launches_per_step * args.steps
+    line["timing"] = "each step is one replay of a CUDA graph of the public calls; CUDA events on the stream"
+    line["clocks"] = sampler.summary(t_wall0 - 0.3, t_wall1 + 0.3)
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the fp64 oracle on the host cores; each step is a bounded sample
+    of the workload (E2 decode of a prefix of the first sequence, all heads)."""
+    if rank != 0:
+        return
+    import oracle
+
+    wl = S.WORKLOADS[args.workload if args.workload != "prefill" else "longctx"]
+    seq_lens = workload_seq_lens(wl)
+    o = oracle.get()
+    per_step_budget = max(0.01, 90.0 / max(args.steps + args.warmup, 1))
+
+    def inputs(tokens):
+        pt = S.page_table(wl.seed, [tokens], 64)
+        pools = tuple(S.gaussian_bf16(wl.seed, n, shp) for n, shp in
+                      [("rf_sK", (pt.num_blocks, 64, wl.d_h)), ("rf_sV", (pt.num_blocks, 64, wl.d_h)),
+                       ("rf_zK", (pt.num_blocks, 64, wl.H, wl.r)), ("rf_zV", (pt.num_blocks, 64, wl.H, wl.r))])
+        BK = S.gaussian_bf16(wl.seed, "rf_BK", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
+        BV = S.gaussian_bf16(wl.seed, "rf_BV", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
+        q = S.gaussian_bf16(wl.seed, "rf_q", (1, wl.H, wl.d_h))
+        return pt, pools, BK, BV, q
+
+    probe = 256
+    pt, pools, BK, BV, q = inputs(probe)
+    t0 = time.perf_counter()
+    o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
+    rate = probe / max(time.perf_counter() - t0, 1e-6)
+    tokens = max(64, int(min(int(seq_lens[0]), rate * per_step_budget)) // 64 * 64)
+    pt, pools, BK, BV, q = inputs(tokens)
+    for _ in range(args.warmup):
+        o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    val = A.decode_algorithmic_bytes(wl.H, wl.d_h, wl.r, [tokens]) / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC_DECODE, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.key}: {wl.description}", "sample_tokens_per_step": tokens, "H": wl.H,
+                   "d_h": wl.d_h, "r": wl.r},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
+                         "sample": f"E2 decode of the first {tokens} tokens of one sequence, all heads, per step"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
 
 def main():
@@ -392,6 +535,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="lrkv", choices=["lrkv", "reference"])
+    ap.add_argument("--workload", default="longctx", choices=sorted(HARNESS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     world, rank, local = dist_setup()
