@@ -143,6 +143,19 @@ def dist_setup():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(values, dist, device="cpu"):
+    """Element-wise max of per-rank timings (a barrier-free control-plane reduction)."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def replica_seed(rank: int, base: int) -> int:
+    """Each rank decodes its own batch (disjoint sequences): weak scaling, no collective."""
+    return base + 1000 * rank
+
+
 def workload_seq_lens(wl):
     if wl.ragged:
         return S.uniform_int(wl.seed, "seq_lens", wl.B, wl.L_min, wl.L).astype(np.int32)
@@ -165,7 +178,7 @@ class DecodeHarness:
         self.seq_lens = workload_seq_lens(wl)
         self.pt = S.page_table(wl.seed, self.seq_lens, 64)
         nb = self.pt.num_blocks
-        gen = torch.Generator(device="cuda").manual_seed(1234 + rank)
+        gen = torch.Generator(device="cuda").manual_seed(replica_seed(rank, 1234))
         rn = lambda *s, scale=1.0: (torch.randn(*s, generator=gen, device="cuda") * scale).to(torch.bfloat16)
         i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
         self.dims = b.make_dims(H, d_h, r, d)
@@ -283,7 +296,7 @@ class PrefillHarness:
         B, H, d_h, r, d, T, C = wl.B, wl.H, wl.d_h, wl.r, wl.d, wl.L, wl.chunk
         self.pt = S.page_table(wl.seed, [T] * B, 64)
         nb = self.pt.num_blocks
-        gen = torch.Generator(device="cuda").manual_seed(4321 + rank)
+        gen = torch.Generator(device="cuda").manual_seed(replica_seed(rank, 4321))
         rn = lambda *s, scale=1.0: (torch.randn(*s, generator=gen, device="cuda") * scale).to(torch.bfloat16)
         i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
         self.dims = b.make_dims(H, d_h, r, d)
@@ -454,9 +467,7 @@ def run_gpu(args, world, rank, local):
     sampler.stop()
 
     if dist:
-        t = torch.tensor([step_s, kernel_s, e2e_s], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_s, kernel_s, e2e_s = (float(x) for x in t)
+        step_s, kernel_s, e2e_s = max_over_ranks([step_s, kernel_s, e2e_s], dist, device="cuda")
     if rank != 0:
         dist.destroy_process_group()
         return
