@@ -63,4 +63,12 @@ cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeAr
 
 cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, cudaStream_t stream);
 
+// Tensor-core prefill (d_h = 128, r = 16).  Maps: q as [B*Tq][H*d_h] box {64,128}
+// and s^K, s^V pools [nb*64][d_h] box {64,64}, both 128-byte swizzle; z^K, z^V
+// pools [nb*64][H*r] box {16,64} and B^K as [H*d_h][r] box {16,128}, 32-byte swizzle.
+struct PrefillMaps {
+    CUtensorMap q, sK, sV, zK, zV, BK;
+};
+cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, cudaStream_t stream);
+
 }  // namespace lrkv

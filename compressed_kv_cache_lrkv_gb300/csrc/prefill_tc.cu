@@ -1,0 +1,390 @@
+// prefill_tc.cu -- causal chunked prefill on the 5th-generation tensor cores
+// ("Low-Rank Key Value Attention", Eqs. (6)-(7) with the causal mask of the
+// softmax frame), for d_h = 128, r = 16.
+//
+// One CTA = 128 queries of one (sequence, head); key tiles of 128 tokens (two
+// cache pages).  Per tile j:
+//   S_j  = [Q | Q~] . [s^K | z^K_h]^T     tcgen05.mma M=128 N=128, K = 128 + 16,
+//                                          fp32 in TMEM (two S buffers)
+//   P_j  = exp2(S_j * scale * log2 e - m) bf16, written to swizzled shared memory
+//   O_s += P_j . s^V (N = 128),  O_z += P_j . z^V_h (N = 16)   in TMEM
+// with Q~ = Q . B_h^K computed on the tensor cores in the prologue, and the
+// epilogue out = (O_s + B_h^V O_z) / l in fp32.  Warp roles: warp 0 TMA
+// producer, warp 1 MMA issuer (one thread) and TMEM owner, warps 2..5 softmax /
+// epilogue (one query row per thread, TMEM lane quarter = warp % 4).
+// The running max is only raised (and O rescaled in TMEM) when a row's max grows
+// by more than 2^8, so most tiles need no O round trip.  Key rows past the
+// context are zero-filled (TMA out-of-bounds fill, or cleared in shared memory)
+// so masked tokens cannot inject NaN through 0 * garbage.
+#include "kernels.h"
+#include "lrkv_internal.cuh"
+
+namespace lrkv {
+
+namespace {
+
+constexpr int kBM = 128, kBN = 128;
+constexpr uint32_t OFF_Q = 0;           // [128 q][128 d] K-major, 128B swizzle, two 64-column blocks
+constexpr uint32_t OFF_QT = 32768;      // [128 q][16] K-major, 32B swizzle
+constexpr uint32_t OFF_BK = 36864;      // [128 d][16] MN-major (B operand of Q~), 32B swizzle
+constexpr uint32_t OFF_BV = 40960;      // [128 d][16] plain, epilogue
+constexpr uint32_t OFF_P = 45056;       // [128 q][128 keys] K-major, 128B swizzle
+constexpr uint32_t OFF_KV = 77824;      // two stages
+constexpr uint32_t KV_STAGE = 73728;
+constexpr uint32_t KV_SK = 0, KV_SV = 32768, KV_ZK = 65536, KV_ZV = 69632;
+constexpr uint32_t OFF_BAR = OFF_KV + 2 * KV_STAGE;
+constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;
+constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_OS = 256, TM_OZ = 384, TM_QT = 448, TM_COLS = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+__device__ __forceinline__ uint64_t kdesc128(uint32_t a) { return sdesc(a, 16, 1024, 2); }
+__device__ __forceinline__ uint64_t kdesc32(uint32_t a) { return sdesc(a, 16, 256, 6); }
+__device__ __forceinline__ uint64_t mndesc128(uint32_t a) { return sdesc(a, 16384, 1024, 2); }
+__device__ __forceinline__ uint64_t mndesc32(uint32_t a) { return sdesc(a, 16, 256, 6); }
+
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, uint32_t* status) {
+    const bool ok = mbar_wait(bar, parity, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constant__ PrefillMaps m, const PrefillArgs a) {
+    constexpr int D_H = 128, R = 16;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t S0 = smem_u32(smem);
+
+    const int qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, b = blockIdx.z;  // heavy query tiles first
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Tq = a.Tq, H = a.H;
+    const int qs = a.q_start[b];
+    const int ctx = qs + Tq;
+    const int q0 = qt * kBM;
+    auto out_row = [&](int i) { return a.out + (((size_t)b * Tq + i) * H + h) * D_H; };
+    if (qs < 0 || ctx > a.max_pages * kBlockSize) {
+        if (threadIdx.x == 0 && qt == 0 && h == 0) set_status(a.status, LRKV_DEV_BAD_SEQLEN);
+        for (int idx = threadIdx.x; idx < kBM * D_H; idx += blockDim.x) {
+            const int i = q0 + idx / D_H;
+            if (i < Tq) out_row(i)[idx % D_H] = 0;
+        }
+        return;
+    }
+    const int last_row = min(q0 + kBM - 1, Tq - 1);
+    const int nt = (qs + last_row) / kBN + 1;  // key tiles this CTA needs
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* q_full = bars + 0;
+    uint64_t* qt_mma = bars + 1;
+    uint64_t* qt_ready = bars + 2;
+    uint64_t* kv_full = bars + 3;   // [2]
+    uint64_t* kv_empty = bars + 5;  // [2]
+    uint64_t* s_full = bars + 7;    // [2]
+    uint64_t* p_full = bars + 9;
+    uint64_t* o_done = bars + 10;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+    volatile int* abort_flag = reinterpret_cast<int*>(bars + 13);
+    auto B = [&](uint64_t* p) { return smem_u32(p); };
+
+    if (threadIdx.x == 0) {
+        mbar_init(B(q_full), 1);
+        mbar_init(B(qt_mma), 1);
+        mbar_init(B(qt_ready), 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(B(kv_full + i), 1);
+            mbar_init(B(kv_empty + i), 1);
+            mbar_init(B(s_full + i), 1);
+        }
+        mbar_init(B(p_full), 128);
+        mbar_init(B(o_done), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const int oob_row = a.num_blocks * kBlockSize;  // whole box out of bounds -> zero fill
+            mbar_arrive_expect_tx(B(q_full), 32768 + 4096);
+            tma_load_2d(S0 + OFF_Q, &m.q, h * D_H, b * Tq + q0, B(q_full));
+            tma_load_2d(S0 + OFF_Q + 16384, &m.q, h * D_H + 64, b * Tq + q0, B(q_full));
+            tma_load_2d(S0 + OFF_BK, &m.BK, 0, h * D_H, B(q_full));
+            int issued = 0;
+            for (int j = 0; j < nt; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !mbar_wait(B(kv_empty + st), ((j >> 1) - 1) & 1, a.status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                const uint32_t bar = B(kv_full + st);
+                const uint32_t base = S0 + OFF_KV + st * KV_STAGE;
+                mbar_arrive_expect_tx(bar, KV_STAGE);
+                for (int p = 0; p < 2; ++p) {
+                    const int page = 2 * j + p;
+                    int row = oob_row;
+                    if (page * kBlockSize < ctx) {
+                        const int blk = a.block_table[(size_t)b * a.max_pages + page];
+                        if (blk >= 0 && blk < a.num_blocks)
+                            row = blk * kBlockSize;
+                        else
+                            set_status(a.status, LRKV_DEV_BAD_BLOCK);
+                    }
+                    tma_load_2d(base + KV_SK + p * 8192, &m.sK, 0, row, bar);
+                    tma_load_2d(base + KV_SK + 16384 + p * 8192, &m.sK, 64, row, bar);
+                    tma_load_2d(base + KV_SV + p * 8192, &m.sV, 0, row, bar);
+                    tma_load_2d(base + KV_SV + 16384 + p * 8192, &m.sV, 64, row, bar);
+                    tma_load_2d(base + KV_ZK + p * 2048, &m.zK, h * R, row, bar);
+                    tma_load_2d(base + KV_ZV + p * 2048, &m.zV, h * R, row, bar);
+                }
+                issued = j + 1;
+            }
+            if (*abort_flag)
+                for (int k = max(0, issued - 2); k < issued; ++k)
+                    mbar_wait(B(kv_full + (k & 1)), (k >> 1) & 1, a.status);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_S = idesc_bf16_f32(128, 128);
+            constexpr uint32_t id_QT = idesc_bf16_f32(128, 16) | (1u << 16);
+            constexpr uint32_t id_PVs = idesc_bf16_f32(128, 128) | (1u << 16);
+            constexpr uint32_t id_PVz = idesc_bf16_f32(128, 16) | (1u << 16);
+            bool ok = mbar_wait(B(q_full), 0, a.status);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D_H / 16; ++kk)
+                    tc_mma_bf16(tmem + TM_QT, kdesc128(S0 + OFF_Q + (kk >> 2) * 16384 + (kk & 3) * 32),
+                                mndesc32(S0 + OFF_BK + kk * 512), id_QT, kk > 0);
+            }
+            tc_commit(B(qt_mma));
+            ok = ok && mbar_wait(B(qt_ready), 0, a.status);
+            auto issue_S = [&](int jj) -> bool {
+                const int st = jj & 1;
+                if (!mbar_wait(B(kv_full + st), (jj >> 1) & 1, a.status)) return false;
+                tc_fence_after();
+                const uint32_t base = S0 + OFF_KV + st * KV_STAGE;
+                const uint32_t d = tmem + (st ? TM_S1 : TM_S0);
+#pragma unroll
+                for (int kk = 0; kk < D_H / 16; ++kk)
+                    tc_mma_bf16(d, kdesc128(S0 + OFF_Q + (kk >> 2) * 16384 + (kk & 3) * 32),
+                                kdesc128(base + KV_SK + (kk >> 2) * 16384 + (kk & 3) * 32), id_S, kk > 0);
+                tc_mma_bf16(d, kdesc32(S0 + OFF_QT), kdesc32(base + KV_ZK), id_S, 1);
+                tc_commit(B(s_full + st));
+                return true;
+            };
+            if (ok) ok = issue_S(0);
+            if (ok && nt > 1) ok = issue_S(1);
+            for (int j = 0; j < nt && ok; ++j) {
+                if (*abort_flag || !mbar_wait(B(p_full), j & 1, a.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t base = S0 + OFF_KV + (j & 1) * KV_STAGE;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint64_t pd = kdesc128(S0 + OFF_P + (kk >> 2) * 16384 + (kk & 3) * 32);
+                    tc_mma_bf16(tmem + TM_OS, pd, mndesc128(base + KV_SV + kk * 2048), id_PVs, (j | kk) != 0);
+                    tc_mma_bf16(tmem + TM_OZ, pd, mndesc32(base + KV_ZV + kk * 512), id_PVz, (j | kk) != 0);
+                }
+                tc_commit(B(o_done));
+                tc_commit(B(kv_empty + (j & 1)));
+                if (j + 2 < nt) ok = issue_S(j + 2);
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax / epilogue
+        const int qq = warp & 3;
+        const int row = qq * 32 + lane;              // query row within the tile = TMEM lane
+        const uint32_t tl = (uint32_t)(qq * 32) << 16;
+        const int st_tid = threadIdx.x - 64;         // 0..127
+        // B_h^V into shared memory for the epilogue (plain layout [d][j]).
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(a.BV + (size_t)h * D_H * R);
+            uint4* dst = reinterpret_cast<uint4*>(smem + OFF_BV);
+            for (int i = st_tid; i < D_H * R / 8; i += 128) dst[i] = src[i];
+        }
+        // Q~ row from TMEM -> bf16 -> shared memory (K-major, 32-byte swizzle).
+        bool ok = wait_all(B(qt_mma), 0, a.status);
+        tc_fence_after();
+        {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(tmem + tl + TM_QT, v);
+            uint4 c0, c1;
+            c0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+            c0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+            c0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+            c0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+            c1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
+            c1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
+            c1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
+            c1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
+            const int sw = (row >> 2) & 1;
+            *reinterpret_cast<uint4*>(smem + OFF_QT + row * 32 + ((0 ^ sw) << 4)) = c0;
+            *reinterpret_cast<uint4*>(smem + OFF_QT + row * 32 + ((1 ^ sw) << 4)) = c1;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(B(qt_ready));
+        asm volatile("bar.sync 2, 128;" ::: "memory");  // B^V staged
+
+        const int qpos = qs + min(q0 + row, Tq - 1);
+        float mref = -INFINITY, l = 0.f;
+        for (int j = 0; j < nt; ++j) {
+            if (!ok || *abort_flag) {
+                ok = false;
+                break;
+            }
+            ok = wait_all(B(s_full + (j & 1)), (j >> 1) & 1, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            float s[kBN];
+            {
+                uint32_t v[32];
+                const uint32_t sb = tmem + tl + ((j & 1) ? TM_S1 : TM_S0);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld_32x32b_x32(sb + c * 32, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
+                }
+            }
+            const int k0 = j * kBN;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) {
+                s[c] = (k0 + c <= qpos) ? s[c] * a.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[c]);
+            }
+            const float mnew = fmaxf(mref, mx);
+            const bool raise = mnew > mref + kRescaleThreshold;  // also true the first time a row sees a key
+            const float muse = raise ? mnew : mref;
+            const float alpha = raise ? ((mref == -INFINITY) ? 0.f : exp2f(mref - mnew)) : 1.f;
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) {
+                s[c] = (muse == -INFINITY) ? 0.f : exp2f(s[c] - muse);
+                rs += s[c];
+            }
+            l = l * alpha + rs;
+            mref = muse;
+            // PV_{j-1} must be done: it reads the P buffer and accumulates into O.
+            if (j > 0) {
+                ok = wait_all(B(o_done), (j - 1) & 1, a.status);
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, raise)) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld_32x32b_x32(tmem + tl + TM_OS + c * 32, v);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        tmem_st_32x32b_x32(tmem + tl + TM_OS + c * 32, v);
+                    }
+                    tmem_ld_32x32b_x16(tmem + tl + TM_OZ, v);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    tmem_st_32x32b_x16(tmem + tl + TM_OZ, v);
+                    tmem_wait_st();
+                }
+            }
+            // Key rows past the context may hold any bits: clear them before P . V reads them.
+            const uint32_t kvb = OFF_KV + (j & 1) * KV_STAGE;
+            if (k0 + kBN > ctx) {
+                ok = wait_all(B(kv_full + (j & 1)), (j >> 1) & 1, a.status);
+                if (!ok) break;
+                if (k0 + row >= ctx) {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    uint4* r0 = reinterpret_cast<uint4*>(smem + kvb + KV_SV + row * 128);
+                    uint4* r1 = reinterpret_cast<uint4*>(smem + kvb + KV_SV + 16384 + row * 128);
+                    uint4* rz = reinterpret_cast<uint4*>(smem + kvb + KV_ZV + row * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        r0[i] = z;
+                        r1[i] = z;
+                    }
+                    rz[0] = z;
+                    rz[1] = z;
+                }
+            }
+            // P row -> bf16 -> shared memory (K-major, 128-byte swizzle, two 64-key blocks)
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float* pp = s + blk * 64 + c * 8;
+                    uint4 pk;
+                    pk.x = pack_bf16x2(pp[0], pp[1]);
+                    pk.y = pack_bf16x2(pp[2], pp[3]);
+                    pk.z = pack_bf16x2(pp[4], pp[5]);
+                    pk.w = pack_bf16x2(pp[6], pp[7]);
+                    *reinterpret_cast<uint4*>(smem + OFF_P + blk * 16384 + row * 128 + ((c ^ (row & 7)) << 4)) = pk;
+                }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(B(p_full));
+        }
+        // ---- epilogue: out = (O_s + B^V O_z) / l
+        if (ok) ok = wait_all(B(o_done), (nt - 1) & 1, a.status);
+        if (ok) {
+            tc_fence_after();
+            uint32_t vz[16];
+            tmem_ld_32x32b_x16(tmem + tl + TM_OZ, vz);
+            float oz[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) oz[e] = __uint_as_float(vz[e]);
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int qrow = q0 + row;
+            const uint16_t* bv = reinterpret_cast<const uint16_t*>(smem + OFF_BV);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem + tl + TM_OS + c * 32, v);
+                if (qrow < Tq) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float o0 = __uint_as_float(v[e]), o1 = __uint_as_float(v[e + 1]);
+                        const int d0 = c * 32 + e;
+#pragma unroll
+                        for (int jj = 0; jj < R; ++jj) {
+                            o0 = fmaf(__uint_as_float((uint32_t)bv[d0 * R + jj] << 16), oz[jj], o0);
+                            o1 = fmaf(__uint_as_float((uint32_t)bv[(d0 + 1) * R + jj] << 16), oz[jj], o1);
+                        }
+                        pk[e / 2] = pack_bf16x2(o0 * inv, o1 * inv);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(out_row(qrow) + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+        }
+        if (!ok) *abort_flag = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TM_COLS);
+    }
+}
+
+cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid((a.Tq + kBM - 1) / kBM, a.H, a.B);
+    prefill_tc_kernel<<<grid, 192, kSmemBytes, stream>>>(maps, a);
+    return cudaGetLastError();
+}
+
+}  // namespace lrkv
