@@ -247,36 +247,26 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
             ok = wait_all(B(s_full + (j & 1)), (j >> 1) & 1, a.status);
             if (!ok) break;
             tc_fence_after();
-            float s[kBN];
-            {
-                uint32_t v[32];
-                const uint32_t sb = tmem + tl + ((j & 1) ? TM_S1 : TM_S0);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld_32x32b_x32(sb + c * 32, v);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
-                }
-            }
+            // Pass 1: row max over 32-column chunks of S (unscaled: max is order-preserving
+            // under the positive scale).  Pass 2 re-reads S from TMEM.
+            const uint32_t sb = tmem + tl + ((j & 1) ? TM_S1 : TM_S0);
             const int k0 = j * kBN;
+            const bool diag = k0 + kBN - 1 > qpos;
             float mx = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32_nowait(sb + c * 32, v);
+                tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                s[c] = (k0 + c <= qpos) ? s[c] * a.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[c]);
+                for (int e = 0; e < 32; ++e)
+                    if (!diag || k0 + c * 32 + e <= qpos) mx = fmaxf(mx, __uint_as_float(v[e]));
             }
+            mx *= a.scale_log2;
             const float mnew = fmaxf(mref, mx);
             const bool raise = mnew > mref + kRescaleThreshold;  // also true the first time a row sees a key
             const float muse = raise ? mnew : mref;
-            const float alpha = raise ? ((mref == -INFINITY) ? 0.f : exp2f(mref - mnew)) : 1.f;
-            float rs = 0.f;
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                s[c] = (muse == -INFINITY) ? 0.f : exp2f(s[c] - muse);
-                rs += s[c];
-            }
-            l = l * alpha + rs;
-            mref = muse;
+            const float alpha = raise ? ((mref == -INFINITY) ? 0.f : ex2_approx(mref - mnew)) : 1.f;
             // PV_{j-1} must be done: it reads the P buffer and accumulates into O.
             if (j > 0) {
                 ok = wait_all(B(o_done), (j - 1) & 1, a.status);
@@ -284,7 +274,7 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, raise)) {
                     uint32_t v[32];
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         tmem_ld_32x32b_x32(tmem + tl + TM_OS + c * 32, v);
 #pragma unroll
@@ -317,19 +307,36 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                     rz[1] = z;
                 }
             }
-            // P row -> bf16 -> shared memory (K-major, 128-byte swizzle, two 64-key blocks)
+            // Pass 2: p = 2^(s * scale log2 e - m) (one FFMA + one EX2), row sum, and the
+            // bf16 P row into shared memory (K-major, 128-byte swizzle, two 64-key blocks).
+            float rs = 0.f;
+            const float nm = -muse;
+            const bool live = muse != -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32_nowait(sb + c * 32, v);
+                tmem_wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-            for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float* pp = s + blk * 64 + c * 8;
-                    uint4 pk;
-                    pk.x = pack_bf16x2(pp[0], pp[1]);
-                    pk.y = pack_bf16x2(pp[2], pp[3]);
-                    pk.z = pack_bf16x2(pp[4], pp[5]);
-                    pk.w = pack_bf16x2(pp[6], pp[7]);
-                    *reinterpret_cast<uint4*>(smem + OFF_P + blk * 16384 + row * 128 + ((c ^ (row & 7)) << 4)) = pk;
+                for (int e = 0; e < 32; e += 2) {
+                    float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), a.scale_log2, nm));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), a.scale_log2, nm));
+                    if (!live || (diag && k0 + c * 32 + e > qpos)) p0 = 0.f;
+                    if (!live || (diag && k0 + c * 32 + e + 1 > qpos)) p1 = 0.f;
+                    rs += p0 + p1;
+                    pk[e / 2] = pack_bf16x2(p0, p1);
                 }
+                const int blk = c >> 1;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int chunk = (c & 1) * 4 + i;
+                    *reinterpret_cast<uint4*>(smem + OFF_P + blk * 16384 + row * 128 + ((chunk ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+            l = l * alpha + rs;
+            mref = muse;
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(B(p_full));
