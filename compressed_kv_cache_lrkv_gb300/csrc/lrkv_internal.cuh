@@ -10,7 +10,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/lrkv.h"
+#include "lrkv.h"
 
 namespace lrkv {
 

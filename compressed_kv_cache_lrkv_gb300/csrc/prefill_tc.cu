@@ -78,13 +78,15 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
     uint64_t* q_full = bars + 0;
     uint64_t* qt_mma = bars + 1;
     uint64_t* qt_ready = bars + 2;
-    uint64_t* kv_full = bars + 3;   // [2]
-    uint64_t* kv_empty = bars + 5;  // [2]
+    uint64_t* k_full = bars + 3;    // [2] s^K, z^K of a key tile landed
+    uint64_t* k_empty = bars + 5;   // [2] S MMA done with them
     uint64_t* s_full = bars + 7;    // [2]
     uint64_t* p_full = bars + 9;
     uint64_t* o_done = bars + 10;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
-    volatile int* abort_flag = reinterpret_cast<int*>(bars + 13);
+    uint64_t* v_full = bars + 11;   // [2] s^V, z^V landed
+    uint64_t* v_empty = bars + 13;  // [2] P.V MMA done with them
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+    volatile int* abort_flag = reinterpret_cast<int*>(bars + 16);
     auto B = [&](uint64_t* p) { return smem_u32(p); };
 
     if (threadIdx.x == 0) {
@@ -92,8 +94,10 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
         mbar_init(B(qt_mma), 1);
         mbar_init(B(qt_ready), 128);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(B(kv_full + i), 1);
-            mbar_init(B(kv_empty + i), 1);
+            mbar_init(B(k_full + i), 1);
+            mbar_init(B(k_empty + i), 1);
+            mbar_init(B(v_full + i), 1);
+            mbar_init(B(v_empty + i), 1);
             mbar_init(B(s_full + i), 1);
         }
         mbar_init(B(p_full), 128);
@@ -115,39 +119,60 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
             tma_load_2d(S0 + OFF_Q, &m.q, h * D_H, b * Tq + q0, B(q_full));
             tma_load_2d(S0 + OFF_Q + 16384, &m.q, h * D_H + 64, b * Tq + q0, B(q_full));
             tma_load_2d(S0 + OFF_BK, &m.BK, 0, h * D_H, B(q_full));
-            int issued = 0;
+            // Key halves (s^K, z^K) are released as soon as S_j is computed and value halves
+            // (s^V, z^V) after P_j V_j, so tile j+2's keys are requested about a tile earlier
+            // than its values.  Issue order K_j, V_j keeps each wait ahead of its need.
+            int issued_k = 0, issued_v = 0;
+            auto page_row = [&](int page) {
+                int row = oob_row;
+                if (page * kBlockSize < ctx) {
+                    const int blk = a.block_table[(size_t)b * a.max_pages + page];
+                    if (blk >= 0 && blk < a.num_blocks)
+                        row = blk * kBlockSize;
+                    else
+                        set_status(a.status, LRKV_DEV_BAD_BLOCK);
+                }
+                return row;
+            };
             for (int j = 0; j < nt; ++j) {
                 const int st = j & 1;
-                if (j >= 2 && !mbar_wait(B(kv_empty + st), ((j >> 1) - 1) & 1, a.status)) {
+                const uint32_t base = S0 + OFF_KV + st * KV_STAGE;
+                const int row0 = page_row(2 * j), row1 = page_row(2 * j + 1);
+                if (j >= 2 && !mbar_wait(B(k_empty + st), ((j >> 1) - 1) & 1, a.status)) {
                     *abort_flag = 1;
                     break;
                 }
                 if (*abort_flag) break;
-                const uint32_t bar = B(kv_full + st);
-                const uint32_t base = S0 + OFF_KV + st * KV_STAGE;
-                mbar_arrive_expect_tx(bar, KV_STAGE);
+                uint32_t bar = B(k_full + st);
+                mbar_arrive_expect_tx(bar, KV_STAGE / 2);
                 for (int p = 0; p < 2; ++p) {
-                    const int page = 2 * j + p;
-                    int row = oob_row;
-                    if (page * kBlockSize < ctx) {
-                        const int blk = a.block_table[(size_t)b * a.max_pages + page];
-                        if (blk >= 0 && blk < a.num_blocks)
-                            row = blk * kBlockSize;
-                        else
-                            set_status(a.status, LRKV_DEV_BAD_BLOCK);
-                    }
+                    const int row = p ? row1 : row0;
                     tma_load_2d(base + KV_SK + p * 8192, &m.sK, 0, row, bar);
                     tma_load_2d(base + KV_SK + 16384 + p * 8192, &m.sK, 64, row, bar);
+                    tma_load_2d(base + KV_ZK + p * 2048, &m.zK, h * R, row, bar);
+                }
+                issued_k = j + 1;
+                if (j >= 2 && !mbar_wait(B(v_empty + st), ((j >> 1) - 1) & 1, a.status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                bar = B(v_full + st);
+                mbar_arrive_expect_tx(bar, KV_STAGE / 2);
+                for (int p = 0; p < 2; ++p) {
+                    const int row = p ? row1 : row0;
                     tma_load_2d(base + KV_SV + p * 8192, &m.sV, 0, row, bar);
                     tma_load_2d(base + KV_SV + 16384 + p * 8192, &m.sV, 64, row, bar);
-                    tma_load_2d(base + KV_ZK + p * 2048, &m.zK, h * R, row, bar);
                     tma_load_2d(base + KV_ZV + p * 2048, &m.zV, h * R, row, bar);
                 }
-                issued = j + 1;
+                issued_v = j + 1;
             }
-            if (*abort_flag)
-                for (int k = max(0, issued - 2); k < issued; ++k)
-                    mbar_wait(B(kv_full + (k & 1)), (k >> 1) & 1, a.status);
+            if (*abort_flag) {
+                for (int k = max(0, issued_k - 2); k < issued_k; ++k)
+                    mbar_wait(B(k_full + (k & 1)), (k >> 1) & 1, a.status);
+                for (int k = max(0, issued_v - 2); k < issued_v; ++k)
+                    mbar_wait(B(v_full + (k & 1)), (k >> 1) & 1, a.status);
+            }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -168,7 +193,7 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
             ok = ok && mbar_wait(B(qt_ready), 0, a.status);
             auto issue_S = [&](int jj) -> bool {
                 const int st = jj & 1;
-                if (!mbar_wait(B(kv_full + st), (jj >> 1) & 1, a.status)) return false;
+                if (!mbar_wait(B(k_full + st), (jj >> 1) & 1, a.status)) return false;
                 tc_fence_after();
                 const uint32_t base = S0 + OFF_KV + st * KV_STAGE;
                 const uint32_t d = tmem + (st ? TM_S1 : TM_S0);
@@ -178,12 +203,17 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                                 kdesc128(base + KV_SK + (kk >> 2) * 16384 + (kk & 3) * 32), id_S, kk > 0);
                 tc_mma_bf16(d, kdesc32(S0 + OFF_QT), kdesc32(base + KV_ZK), id_S, 1);
                 tc_commit(B(s_full + st));
+                tc_commit(B(k_empty + st));
                 return true;
             };
             if (ok) ok = issue_S(0);
             if (ok && nt > 1) ok = issue_S(1);
             for (int j = 0; j < nt && ok; ++j) {
                 if (*abort_flag || !mbar_wait(B(p_full), j & 1, a.status)) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait(B(v_full + (j & 1)), (j >> 1) & 1, a.status)) {
                     ok = false;
                     break;
                 }
@@ -196,7 +226,7 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                     tc_mma_bf16(tmem + TM_OZ, pd, mndesc32(base + KV_ZV + kk * 512), id_PVz, (j | kk) != 0);
                 }
                 tc_commit(B(o_done));
-                tc_commit(B(kv_empty + (j & 1)));
+                tc_commit(B(v_empty + (j & 1)));
                 if (j + 2 < nt) ok = issue_S(j + 2);
             }
             if (!ok) *abort_flag = 1;
@@ -247,21 +277,30 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
             ok = wait_all(B(s_full + (j & 1)), (j >> 1) & 1, a.status);
             if (!ok) break;
             tc_fence_after();
-            // Pass 1: row max over 32-column chunks of S (unscaled: max is order-preserving
-            // under the positive scale).  Pass 2 re-reads S from TMEM.
+            // The whole S row comes out of TMEM in four back-to-back loads and one wait
+            // (serial load -> wait round trips would dominate the tile), and stays in
+            // registers for both passes: the row max (unscaled -- order-preserving under
+            // the positive scale), then p = 2^(s * scale log2 e - m).
             const uint32_t sb = tmem + tl + ((j & 1) ? TM_S1 : TM_S0);
             const int k0 = j * kBN;
             const bool diag = k0 + kBN - 1 > qpos;
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32_nowait(sb + c * 32, v);
-                tmem_wait_ld();
+            uint32_t sv[kBN];
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if (!diag || k0 + c * 32 + e <= qpos) mx = fmaxf(mx, __uint_as_float(v[e]));
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32_nowait(sb + c * 32, sv + c * 32);
+            tmem_wait_ld();
+            // eight independent partial maxima (one serial chain of 128 would stall on latency)
+            float m8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+            if (!diag) {
+#pragma unroll
+                for (int e = 0; e < kBN; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sv[e]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < kBN; ++e)
+                    if (k0 + e <= qpos) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sv[e]));
             }
+            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             mx *= a.scale_log2;
             const float mnew = fmaxf(mref, mx);
             const bool raise = mnew > mref + kRescaleThreshold;  // also true the first time a row sees a key
@@ -291,7 +330,7 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
             // Key rows past the context may hold any bits: clear them before P . V reads them.
             const uint32_t kvb = OFF_KV + (j & 1) * KV_STAGE;
             if (k0 + kBN > ctx) {
-                ok = wait_all(B(kv_full + (j & 1)), (j >> 1) & 1, a.status);
+                ok = wait_all(B(v_full + (j & 1)), (j >> 1) & 1, a.status);
                 if (!ok) break;
                 if (k0 + row >= ctx) {
                     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -307,16 +346,14 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                     rz[1] = z;
                 }
             }
-            // Pass 2: p = 2^(s * scale log2 e - m) (one FFMA + one EX2), row sum, and the
-            // bf16 P row into shared memory (K-major, 128-byte swizzle, two 64-key blocks).
-            float rs = 0.f;
+            // p = 2^(s * scale log2 e - m) (one FFMA + one EX2), row sum, and the bf16 P row
+            // into shared memory (K-major, 128-byte swizzle, two 64-key blocks).
+            float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             const float nm = -muse;
             const bool live = muse != -INFINITY;
-#pragma unroll 1
+#pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32_nowait(sb + c * 32, v);
-                tmem_wait_ld();
+                const uint32_t* v = sv + c * 32;
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
@@ -324,7 +361,7 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                     float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), a.scale_log2, nm));
                     if (!live || (diag && k0 + c * 32 + e > qpos)) p0 = 0.f;
                     if (!live || (diag && k0 + c * 32 + e + 1 > qpos)) p1 = 0.f;
-                    rs += p0 + p1;
+                    r8[(e >> 1) & 7] += p0 + p1;
                     pk[e / 2] = pack_bf16x2(p0, p1);
                 }
                 const int blk = c >> 1;
@@ -335,6 +372,7 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                         make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
             }
+            const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
             l = l * alpha + rs;
             mref = muse;
             fence_proxy_async_smem();
