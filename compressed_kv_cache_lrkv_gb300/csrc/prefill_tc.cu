@@ -42,6 +42,13 @@ __device__ __forceinline__ uint64_t kdesc32(uint32_t a) { return sdesc(a, 16, 25
 __device__ __forceinline__ uint64_t mndesc128(uint32_t a) { return sdesc(a, 16384, 1024, 2); }
 __device__ __forceinline__ uint64_t mndesc32(uint32_t a) { return sdesc(a, 16, 256, 6); }
 
+// Three-input f32 maximum (sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, uint32_t* status) {
     const bool ok = mbar_wait(bar, parity, status);
     return __all_sync(0xffffffffu, ok);
@@ -288,19 +295,23 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32_nowait(sb + c * 32, sv + c * 32);
             tmem_wait_ld();
+            // Causal mask on diagonal tiles only: masked scores become -inf in the register
+            // row, so the max and the exponentials below run without per-element branches
+            // (2^-inf = 0).
+            if (diag) {
+                const int lim = qpos - k0;  // keys k0 + e with e <= lim are visible
+#pragma unroll
+                for (int e = 0; e < kBN; ++e) sv[e] = e <= lim ? sv[e] : 0xff800000u;
+            }
             // eight independent partial maxima (one serial chain of 128 would stall on latency)
             float m8[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
-            if (!diag) {
+            for (int i = 0; i < 8; ++i) m8[i] = fmaxf(__uint_as_float(sv[i]), __uint_as_float(sv[8 + i]));
 #pragma unroll
-                for (int e = 0; e < kBN; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sv[e]));
-            } else {
+            for (int e = 16; e < kBN; e += 16)
 #pragma unroll
-                for (int e = 0; e < kBN; ++e)
-                    if (k0 + e <= qpos) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sv[e]));
-            }
-            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], __uint_as_float(sv[e + i]), __uint_as_float(sv[e + 8 + i]));
+            float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
             mx *= a.scale_log2;
             const float mnew = fmaxf(mref, mx);
             const bool raise = mnew > mref + kRescaleThreshold;  // also true the first time a row sees a key
@@ -349,18 +360,16 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
             // p = 2^(s * scale log2 e - m) (one FFMA + one EX2), row sum, and the bf16 P row
             // into shared memory (K-major, 128-byte swizzle, two 64-key blocks).
             float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            const float nm = -muse;
-            const bool live = muse != -INFINITY;
+            // A row that has seen no visible key yet (muse = -inf) gets p = 0 everywhere.
+            const float nm = muse == -INFINITY ? -INFINITY : -muse;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint32_t* v = sv + c * 32;
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), a.scale_log2, nm));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), a.scale_log2, nm));
-                    if (!live || (diag && k0 + c * 32 + e > qpos)) p0 = 0.f;
-                    if (!live || (diag && k0 + c * 32 + e + 1 > qpos)) p1 = 0.f;
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), a.scale_log2, nm));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), a.scale_log2, nm));
                     r8[(e >> 1) & 7] += p0 + p1;
                     pk[e / 2] = pack_bf16x2(p0, p1);
                 }
