@@ -299,6 +299,26 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// One lane of a converged warp (the same lane every time for the same active set), for
+// issuing single-thread tcgen05 instructions while the whole warp keeps warp-uniform
+// operands (descriptors, TMEM addresses) in uniform registers.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t p = 0;
+    asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}" : "=r"(p));
+    return p != 0;
+}
+
+// D (TMEM, fp32) (+)= A . B with A read from tensor memory: lane i holds row i of A, each
+// 32-bit column two consecutive K elements (bf16), so a K=16 step spans 8 columns.
+__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 }  // namespace lrkv
 
 namespace lrkv {

@@ -6,16 +6,21 @@
 // cache pages).  Per tile j:
 //   S_j  = [Q | Q~] . [s^K | z^K_h]^T     tcgen05.mma M=128 N=128, K = 128 + 16,
 //                                          fp32 in TMEM (two S buffers)
-//   P_j  = exp2(S_j * scale * log2 e - m) bf16, written to swizzled shared memory
-//   O_s += P_j . s^V (N = 128),  O_z += P_j . z^V_h (N = 16)   in TMEM
+//   P_j  = exp2(S_j * scale * log2 e - m) bf16, written back into the first 64 TMEM
+//          columns of S_j's own buffer
+//   O_s += P_j . s^V (N = 128),  O_z += P_j . z^V_h (N = 16)   in TMEM, A operand P_j
+//          read from TMEM
 // with Q~ = Q . B_h^K computed on the tensor cores in the prologue, and the
-// epilogue out = (O_s + B_h^V O_z) / l in fp32.  Warp roles: warp 0 TMA
-// producer, warp 1 MMA issuer (one thread) and TMEM owner, warps 2..5 softmax /
+// epilogue out = (O_s + B_h^V O_z) / l in fp32.  Warp roles: warp 0 key-tile TMA
+// producer (3-stage ring), warp 6 value-tile TMA producer (2-stage ring), warp 1
+// score-MMA issuer and TMEM owner, warp 7 P.V-MMA issuer, warps 2..5 softmax /
 // epilogue (one query row per thread, TMEM lane quarter = warp % 4).
 // The running max is only raised (and O rescaled in TMEM) when a row's max grows
 // by more than 2^8, so most tiles need no O round trip.  Key rows past the
 // context are zero-filled (TMA out-of-bounds fill, or cleared in shared memory)
 // so masked tokens cannot inject NaN through 0 * garbage.
+#include <type_traits>
+
 #include "kernels.h"
 #include "lrkv_internal.cuh"
 
@@ -28,11 +33,13 @@ constexpr uint32_t OFF_Q = 0;           // [128 q][128 d] K-major, 128B swizzle,
 constexpr uint32_t OFF_QT = 32768;      // [128 q][16] K-major, 32B swizzle
 constexpr uint32_t OFF_BK = 36864;      // [128 d][16] MN-major (B operand of Q~), 32B swizzle
 constexpr uint32_t OFF_BV = 40960;      // [128 d][16] plain, epilogue
-constexpr uint32_t OFF_P = 45056;       // [128 q][128 keys] K-major, 128B swizzle
-constexpr uint32_t OFF_KV = 77824;      // two stages
-constexpr uint32_t KV_STAGE = 73728;
-constexpr uint32_t KV_SK = 0, KV_SV = 32768, KV_ZK = 65536, KV_ZV = 69632;
-constexpr uint32_t OFF_BAR = OFF_KV + 2 * KV_STAGE;
+// Key ring (3 stages: s^K [128 keys][128] K-major 128B swizzle, then z^K_h [128][16] 32B
+// swizzle) and value ring (2 stages: s^V, z^V_h, same layouts, read MN-major).
+constexpr int kKStages = 3, kVStages = 2;
+constexpr uint32_t STAGE_BYTES = 36864, STAGE_Z = 32768;
+constexpr uint32_t OFF_K = 45056;
+constexpr uint32_t OFF_V = OFF_K + kKStages * STAGE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + kVStages * STAGE_BYTES;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;
 constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_OS = 256, TM_OZ = 384, TM_QT = 448, TM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -56,7 +63,9 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, uint32_t
 
 }  // namespace
 
-__global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constant__ PrefillMaps m, const PrefillArgs a) {
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillMaps m, const PrefillArgs a) {
     constexpr int D_H = 128, R = 16;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -85,30 +94,38 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
     uint64_t* q_full = bars + 0;
     uint64_t* qt_mma = bars + 1;
     uint64_t* qt_ready = bars + 2;
-    uint64_t* k_full = bars + 3;    // [2] s^K, z^K of a key tile landed
-    uint64_t* k_empty = bars + 5;   // [2] S MMA done with them
-    uint64_t* s_full = bars + 7;    // [2]
-    uint64_t* p_full = bars + 9;
-    uint64_t* o_done = bars + 10;
-    uint64_t* v_full = bars + 11;   // [2] s^V, z^V landed
-    uint64_t* v_empty = bars + 13;  // [2] P.V MMA done with them
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
-    volatile int* abort_flag = reinterpret_cast<int*>(bars + 16);
+    uint64_t* s_full = bars + 3;    // [2]
+    uint64_t* p_full = bars + 5;
+    uint64_t* o_done = bars + 6;
+    uint64_t* mma_drain = bars + 7;  // all MMAs of the CTA complete
+    uint64_t* k_full = bars + 8;    // [3] s^K, z^K of a key tile landed
+    uint64_t* k_empty = bars + 11;  // [3] S MMA done with them
+    uint64_t* v_full = bars + 14;   // [2] s^V, z^V landed
+    uint64_t* v_empty = bars + 16;  // [2] P.V MMA done with them
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+    volatile int* abort_flag = reinterpret_cast<int*>(bars + 19);
+    uint64_t* s_free = bars + 20;    // [2] P_j . V_j done: S buffer j % 2 may take S_{j+2}
+    uint64_t* pv_drain = bars + 22;  // all P.V MMAs complete
     auto B = [&](uint64_t* p) { return smem_u32(p); };
 
     if (threadIdx.x == 0) {
         mbar_init(B(q_full), 1);
         mbar_init(B(qt_mma), 1);
         mbar_init(B(qt_ready), 128);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(B(k_full + i), 1);
             mbar_init(B(k_empty + i), 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
             mbar_init(B(v_full + i), 1);
             mbar_init(B(v_empty + i), 1);
-            mbar_init(B(s_full + i), 1);
         }
+        for (int i = 0; i < 2; ++i) mbar_init(B(s_full + i), 1);
         mbar_init(B(p_full), 128);
         mbar_init(B(o_done), 1);
+        mbar_init(B(mma_drain), 1);
+        mbar_init(B(pv_drain), 1);
+        for (int i = 0; i < 2; ++i) mbar_init(B(s_free + i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -118,125 +135,181 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            const int oob_row = a.num_blocks * kBlockSize;  // whole box out of bounds -> zero fill
+    if (warp == 0 || warp == 6) {
+        // ---------------------------------------------------------------- TMA producers
+        // Warp 0 streams key tiles (s^K, z^K_h) into the 3-stage key ring, warp 6 value
+        // tiles (s^V, z^V_h) into the 2-stage value ring; each waits only on its own ring.
+        // Physical rows of this sequence's pages sit in registers, 32 pages per batch (lane
+        // i holds page 32 * batch + i), the next batch fetched one batch ahead, so no
+        // dependent global load sits between two tiles' copies.
+        const bool keys = warp == 0;
+        const int oob_row = a.num_blocks * kBlockSize;  // whole box out of bounds -> zero fill
+        const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
+        auto fetch = [&](int batch) {
+            const int page = batch * 32 + lane;
+            int row = oob_row;
+            if (page < a.max_pages && page * kBlockSize < ctx) {
+                const int blk = bt[page];
+                if (blk >= 0 && blk < a.num_blocks)
+                    row = blk * kBlockSize;
+                else
+                    set_status(a.status, LRKV_DEV_BAD_BLOCK);
+            }
+            return row;
+        };
+        if (keys && lane == 0) {
             mbar_arrive_expect_tx(B(q_full), 32768 + 4096);
             tma_load_2d(S0 + OFF_Q, &m.q, h * D_H, b * Tq + q0, B(q_full));
             tma_load_2d(S0 + OFF_Q + 16384, &m.q, h * D_H + 64, b * Tq + q0, B(q_full));
             tma_load_2d(S0 + OFF_BK, &m.BK, 0, h * D_H, B(q_full));
-            // Key halves (s^K, z^K) are released as soon as S_j is computed and value halves
-            // (s^V, z^V) after P_j V_j, so tile j+2's keys are requested about a tile earlier
-            // than its values.  Issue order K_j, V_j keeps each wait ahead of its need.
-            int issued_k = 0, issued_v = 0;
-            auto page_row = [&](int page) {
-                int row = oob_row;
-                if (page * kBlockSize < ctx) {
-                    const int blk = a.block_table[(size_t)b * a.max_pages + page];
-                    if (blk >= 0 && blk < a.num_blocks)
-                        row = blk * kBlockSize;
-                    else
-                        set_status(a.status, LRKV_DEV_BAD_BLOCK);
-                }
-                return row;
-            };
-            for (int j = 0; j < nt; ++j) {
-                const int st = j & 1;
-                const uint32_t base = S0 + OFF_KV + st * KV_STAGE;
-                const int row0 = page_row(2 * j), row1 = page_row(2 * j + 1);
-                if (j >= 2 && !mbar_wait(B(k_empty + st), ((j >> 1) - 1) & 1, a.status)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                if (*abort_flag) break;
-                uint32_t bar = B(k_full + st);
-                mbar_arrive_expect_tx(bar, KV_STAGE / 2);
-                for (int p = 0; p < 2; ++p) {
-                    const int row = p ? row1 : row0;
-                    tma_load_2d(base + KV_SK + p * 8192, &m.sK, 0, row, bar);
-                    tma_load_2d(base + KV_SK + 16384 + p * 8192, &m.sK, 64, row, bar);
-                    tma_load_2d(base + KV_ZK + p * 2048, &m.zK, h * R, row, bar);
-                }
-                issued_k = j + 1;
-                if (j >= 2 && !mbar_wait(B(v_empty + st), ((j >> 1) - 1) & 1, a.status)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                if (*abort_flag) break;
-                bar = B(v_full + st);
-                mbar_arrive_expect_tx(bar, KV_STAGE / 2);
-                for (int p = 0; p < 2; ++p) {
-                    const int row = p ? row1 : row0;
-                    tma_load_2d(base + KV_SV + p * 8192, &m.sV, 0, row, bar);
-                    tma_load_2d(base + KV_SV + 16384 + p * 8192, &m.sV, 64, row, bar);
-                    tma_load_2d(base + KV_ZV + p * 2048, &m.zV, h * R, row, bar);
-                }
-                issued_v = j + 1;
+        }
+        const int depth = keys ? kKStages : kVStages;
+        uint64_t* full = keys ? k_full : v_full;
+        uint64_t* empty = keys ? k_empty : v_empty;
+        const CUtensorMap* ms = keys ? &m.sK : &m.sV;
+        const CUtensorMap* mz = keys ? &m.zK : &m.zV;
+        const uint32_t ring = S0 + (keys ? OFF_K : OFF_V);
+        int cur = fetch(0), nxt = fetch(1);
+        int issued = 0;
+        bool ok = true;
+        for (int j = 0; j < nt; ++j) {
+            if (j > 0 && (j & 15) == 0) {  // pages 2j, 2j+1 start a new batch of 32
+                cur = nxt;
+                nxt = fetch((j >> 4) + 1);
+            }
+            const int row0 = __shfl_sync(0xffffffffu, cur, (2 * j) & 31);
+            const int row1 = __shfl_sync(0xffffffffu, cur, (2 * j + 1) & 31);
+            const int st = j % depth;
+            if (j >= depth && !wait_all(B(empty + st), (j / depth - 1) & 1, a.status)) {
+                ok = false;
+                break;
             }
             if (*abort_flag) {
-                for (int k = max(0, issued_k - 2); k < issued_k; ++k)
-                    mbar_wait(B(k_full + (k & 1)), (k >> 1) & 1, a.status);
-                for (int k = max(0, issued_v - 2); k < issued_v; ++k)
-                    mbar_wait(B(v_full + (k & 1)), (k >> 1) & 1, a.status);
+                ok = false;
+                break;
             }
+            if (lane == 0) {
+                const uint32_t base = ring + st * STAGE_BYTES, bar = B(full + st);
+                mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                for (int p = 0; p < 2; ++p) {
+                    const int row = p ? row1 : row0;
+                    tma_load_2d(base + p * 8192, ms, 0, row, bar);
+                    tma_load_2d(base + 16384 + p * 8192, ms, 64, row, bar);
+                    tma_load_2d(base + STAGE_Z + p * 2048, mz, h * R, row, bar);
+                }
+            }
+            __syncwarp();
+            issued = j + 1;
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t id_S = idesc_bf16_f32(128, 128);
-            constexpr uint32_t id_QT = idesc_bf16_f32(128, 16) | (1u << 16);
-            constexpr uint32_t id_PVs = idesc_bf16_f32(128, 128) | (1u << 16);
-            constexpr uint32_t id_PVz = idesc_bf16_f32(128, 16) | (1u << 16);
-            bool ok = mbar_wait(B(q_full), 0, a.status);
+        if (!ok) {
+            *abort_flag = 1;
+            // let this ring's copies still in flight land before the CTA exits
+            for (int k = max(0, issued - depth); k < issued; ++k) wait_all(B(full + k % depth), (k / depth) & 1, a.status);
+        }
+    } else if (warp == 1 || warp == 7) {
+        // ---------------------------------------------------------------- MMA issuers
+        // tcgen05.mma issue blocks once the tensor pipe's queue is full, so one issuing
+        // thread that also waits on barriers leaves the pipe idle between its bursts.  Two
+        // warps issue instead: warp 1 the score MMAs (Q~ in the prologue, then S_j), warp 7
+        // the P.V MMAs.  Each runs converged and lets one elected lane issue its tcgen05
+        // instructions and commits.  Descriptors are built once and advanced by adding
+        // (byte offset >> 4) to their start-address field; the tile loops are unrolled over
+        // the ring stages (6 = lcm of the 3 key stages and 2 S buffers; 2 value stages) so
+        // every operand of every MMA is loop-invariant -- operands that change from tile
+        // to tile cost a register-to-uniform move per MMA and halve the issue rate.
+        constexpr uint32_t id_S = idesc_bf16_f32(128, 128);
+        constexpr uint32_t id_QT = idesc_bf16_f32(128, 16) | (1u << 16);
+        constexpr uint32_t id_PVs = idesc_bf16_f32(128, 128) | (1u << 16);
+        constexpr uint32_t id_PVz = idesc_bf16_f32(128, 16) | (1u << 16);
+        constexpr uint64_t kStage = STAGE_BYTES >> 4;
+        bool ok = true;
+        if (warp == 1) {
+            const uint64_t dQ = kdesc128(S0 + OFF_Q), dQT = kdesc32(S0 + OFF_QT), dBK = mndesc32(S0 + OFF_BK);
+            const uint64_t dSK = kdesc128(S0 + OFF_K), dZK = kdesc32(S0 + OFF_K + STAGE_Z);
+            // K-step kk of a K-major 128-byte-swizzled [rows][128] tile: 64-column block kk/4, 32 bytes in.
+            auto kstep = [](int kk) -> uint64_t { return (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
+            ok = wait_all(B(q_full), 0, a.status);
             if (ok) {
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D_H / 16; ++kk)
-                    tc_mma_bf16(tmem + TM_QT, kdesc128(S0 + OFF_Q + (kk >> 2) * 16384 + (kk & 3) * 32),
-                                mndesc32(S0 + OFF_BK + kk * 512), id_QT, kk > 0);
+                    if (elect_one_sync()) tc_mma_bf16(tmem + TM_QT, dQ + kstep(kk), dBK + (kk * 512 >> 4), id_QT, kk > 0);
             }
-            tc_commit(B(qt_mma));
-            ok = ok && mbar_wait(B(qt_ready), 0, a.status);
-            auto issue_S = [&](int jj) -> bool {
-                const int st = jj & 1;
-                if (!mbar_wait(B(k_full + st), (jj >> 1) & 1, a.status)) return false;
+            if (elect_one_sync()) tc_commit(B(qt_mma));
+            __syncwarp();
+            ok = ok && wait_all(B(qt_ready), 0, a.status);
+            auto s_tile = [&](int jj, auto U) -> bool {
+                constexpr int st = decltype(U)::value % kKStages, sb = decltype(U)::value & 1;
+                // S buffer sb still holds P_{jj-2} until P_{jj-2} . V_{jj-2} has completed
+                if (*abort_flag || !wait_all(B(k_full + st), (jj / kKStages) & 1, a.status) ||
+                    (jj >= 2 && !wait_all(B(s_free + sb), ((jj >> 1) - 1) & 1, a.status)))
+                    return false;
                 tc_fence_after();
-                const uint32_t base = S0 + OFF_KV + st * KV_STAGE;
-                const uint32_t d = tmem + (st ? TM_S1 : TM_S0);
+                constexpr uint64_t so = st * kStage;
+                const uint32_t d = tmem + (sb ? TM_S1 : TM_S0);
 #pragma unroll
                 for (int kk = 0; kk < D_H / 16; ++kk)
-                    tc_mma_bf16(d, kdesc128(S0 + OFF_Q + (kk >> 2) * 16384 + (kk & 3) * 32),
-                                kdesc128(base + KV_SK + (kk >> 2) * 16384 + (kk & 3) * 32), id_S, kk > 0);
-                tc_mma_bf16(d, kdesc32(S0 + OFF_QT), kdesc32(base + KV_ZK), id_S, 1);
-                tc_commit(B(s_full + st));
-                tc_commit(B(k_empty + st));
+                    if (elect_one_sync()) tc_mma_bf16(d, dQ + kstep(kk), dSK + so + kstep(kk), id_S, kk > 0);
+                if (elect_one_sync()) {
+                    tc_mma_bf16(d, dQT, dZK + so, id_S, 1);
+                    tc_commit(B(s_full + sb));
+                    tc_commit(B(k_empty + st));
+                }
+                __syncwarp();
                 return true;
             };
-            if (ok) ok = issue_S(0);
-            if (ok && nt > 1) ok = issue_S(1);
-            for (int j = 0; j < nt && ok; ++j) {
-                if (*abort_flag || !mbar_wait(B(p_full), j & 1, a.status)) {
-                    ok = false;
-                    break;
-                }
-                if (!mbar_wait(B(v_full + (j & 1)), (j >> 1) & 1, a.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t base = S0 + OFF_KV + (j & 1) * KV_STAGE;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t pd = kdesc128(S0 + OFF_P + (kk >> 2) * 16384 + (kk & 3) * 32);
-                    tc_mma_bf16(tmem + TM_OS, pd, mndesc128(base + KV_SV + kk * 2048), id_PVs, (j | kk) != 0);
-                    tc_mma_bf16(tmem + TM_OZ, pd, mndesc32(base + KV_ZV + kk * 512), id_PVz, (j | kk) != 0);
-                }
-                tc_commit(B(o_done));
-                tc_commit(B(v_empty + (j & 1)));
-                if (j + 2 < nt) ok = issue_S(j + 2);
+            using I0 = std::integral_constant<int, 0>;
+            using I1 = std::integral_constant<int, 1>;
+            using I2 = std::integral_constant<int, 2>;
+            using I3 = std::integral_constant<int, 3>;
+            using I4 = std::integral_constant<int, 4>;
+            using I5 = std::integral_constant<int, 5>;
+            for (int jj = 0; jj < nt && ok; jj += 6) {
+                ok = s_tile(jj, I0{});
+                if (ok && jj + 1 < nt) ok = s_tile(jj + 1, I1{});
+                if (ok && jj + 2 < nt) ok = s_tile(jj + 2, I2{});
+                if (ok && jj + 3 < nt) ok = s_tile(jj + 3, I3{});
+                if (ok && jj + 4 < nt) ok = s_tile(jj + 4, I4{});
+                if (ok && jj + 5 < nt) ok = s_tile(jj + 5, I5{});
             }
             if (!ok) *abort_flag = 1;
+            // Every MMA this warp issued has finished before the CTA tears TMEM down.
+            if (elect_one_sync()) tc_commit(B(mma_drain));
+            __syncwarp();
+            wait_all(B(mma_drain), 0, a.status);
+        } else {
+            const uint64_t dSV = mndesc128(S0 + OFF_V), dZV = mndesc32(S0 + OFF_V + STAGE_Z);
+            auto pv_tile = [&](int j, auto PAR) -> bool {
+                constexpr int vs = decltype(PAR)::value;  // value stage = S buffer = j % 2
+                if (*abort_flag || !wait_all(B(p_full), j & 1, a.status) ||
+                    !wait_all(B(v_full + vs), (j >> 1) & 1, a.status))
+                    return false;
+                tc_fence_after();
+                constexpr uint64_t so = vs * kStage;
+                const uint32_t pt = tmem + (vs ? TM_S1 : TM_S0);  // P_j over S_j's columns
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    if (elect_one_sync()) {
+                        tc_mma_bf16_ts(tmem + TM_OS, pt + kk * 8, dSV + so + (kk * 2048 >> 4), id_PVs, (j | kk) != 0);
+                        tc_mma_bf16_ts(tmem + TM_OZ, pt + kk * 8, dZV + so + (kk * 512 >> 4), id_PVz, (j | kk) != 0);
+                    }
+                }
+                if (elect_one_sync()) {
+                    tc_commit(B(o_done));
+                    tc_commit(B(v_empty + vs));
+                    tc_commit(B(s_free + vs));
+                }
+                __syncwarp();
+                return true;
+            };
+            for (int j = 0; j < nt && ok; j += 2) {
+                ok = pv_tile(j, std::integral_constant<int, 0>{});
+                if (ok && j + 1 < nt) ok = pv_tile(j + 1, std::integral_constant<int, 1>{});
+            }
+            if (!ok) *abort_flag = 1;
+            if (elect_one_sync()) tc_commit(B(pv_drain));
+            __syncwarp();
+            wait_all(B(pv_drain), 0, a.status);
         }
     } else {
         // ---------------------------------------------------------------- softmax / epilogue
@@ -317,7 +390,48 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
             const bool raise = mnew > mref + kRescaleThreshold;  // also true the first time a row sees a key
             const float muse = raise ? mnew : mref;
             const float alpha = raise ? ((mref == -INFINITY) ? 0.f : ex2_approx(mref - mnew)) : 1.f;
-            // PV_{j-1} must be done: it reads the P buffer and accumulates into O.
+            // Key rows past the context may hold any bits: clear them before P . V reads them.
+            const uint32_t kvb = OFF_V + (j % kVStages) * STAGE_BYTES;
+            if (k0 + kBN > ctx) {
+                ok = wait_all(B(v_full + (j & 1)), (j >> 1) & 1, a.status);
+                if (!ok) break;
+                if (k0 + row >= ctx) {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    uint4* r0 = reinterpret_cast<uint4*>(smem + kvb + row * 128);
+                    uint4* r1 = reinterpret_cast<uint4*>(smem + kvb + 16384 + row * 128);
+                    uint4* rz = reinterpret_cast<uint4*>(smem + kvb + STAGE_Z + row * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        r0[i] = z;
+                        r1[i] = z;
+                    }
+                    rz[0] = z;
+                    rz[1] = z;
+                }
+            }
+            // p = 2^(s * scale log2 e - m) (one FFMA + one EX2), row sum, and the bf16 P row
+            // back into TMEM over the first 64 columns of S_j (keys 2c, 2c+1 in column c),
+            // where P_j . V_j takes its A operand from.
+            float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            // A row that has seen no visible key yet (muse = -inf) gets p = 0 everywhere.
+            const float nm = muse == -INFINITY ? -INFINITY : -muse;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t* v = sv + c * 32;
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), a.scale_log2, nm));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), a.scale_log2, nm));
+                    r8[(e >> 1) & 7] += p0 + p1;
+                    pk[e / 2] = pack_bf16x2(p0, p1);
+                }
+                tmem_st_32x32b_x16(sb + c * 16, pk);
+            }
+            const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+            l = l * alpha + rs;
+            mref = muse;
+            // O may only be rescaled once P_{j-1} . V_{j-1} has finished accumulating into it.
             if (j > 0) {
                 ok = wait_all(B(o_done), (j - 1) & 1, a.status);
                 if (!ok) break;
@@ -338,53 +452,8 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                     tmem_wait_st();
                 }
             }
-            // Key rows past the context may hold any bits: clear them before P . V reads them.
-            const uint32_t kvb = OFF_KV + (j & 1) * KV_STAGE;
-            if (k0 + kBN > ctx) {
-                ok = wait_all(B(v_full + (j & 1)), (j >> 1) & 1, a.status);
-                if (!ok) break;
-                if (k0 + row >= ctx) {
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-                    uint4* r0 = reinterpret_cast<uint4*>(smem + kvb + KV_SV + row * 128);
-                    uint4* r1 = reinterpret_cast<uint4*>(smem + kvb + KV_SV + 16384 + row * 128);
-                    uint4* rz = reinterpret_cast<uint4*>(smem + kvb + KV_ZV + row * 32);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        r0[i] = z;
-                        r1[i] = z;
-                    }
-                    rz[0] = z;
-                    rz[1] = z;
-                }
-            }
-            // p = 2^(s * scale log2 e - m) (one FFMA + one EX2), row sum, and the bf16 P row
-            // into shared memory (K-major, 128-byte swizzle, two 64-key blocks).
-            float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            // A row that has seen no visible key yet (muse = -inf) gets p = 0 everywhere.
-            const float nm = muse == -INFINITY ? -INFINITY : -muse;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t* v = sv + c * 32;
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), a.scale_log2, nm));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), a.scale_log2, nm));
-                    r8[(e >> 1) & 7] += p0 + p1;
-                    pk[e / 2] = pack_bf16x2(p0, p1);
-                }
-                const int blk = c >> 1;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int chunk = (c & 1) * 4 + i;
-                    *reinterpret_cast<uint4*>(smem + OFF_P + blk * 16384 + row * 128 + ((chunk ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
-            }
-            const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
-            l = l * alpha + rs;
-            mref = muse;
-            fence_proxy_async_smem();
+            tmem_wait_st();
+            fence_proxy_async_smem();  // zeroed value rows (if any) before the tensor core reads them
             tc_fence_before();
             mbar_arrive(B(p_full));
         }
@@ -437,7 +506,7 @@ cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, cud
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((a.Tq + kBM - 1) / kBM, a.H, a.B);
-    prefill_tc_kernel<<<grid, 192, kSmemBytes, stream>>>(maps, a);
+    prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(maps, a);
     return cudaGetLastError();
 }
 
