@@ -96,7 +96,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     uint64_t* qt_ready = bars + 2;
     uint64_t* s_full = bars + 3;    // [2]
     uint64_t* p_full = bars + 5;
-    uint64_t* o_done = bars + 6;
+    // o_done[j % 2]: P_j . V_j complete.  Softmax waits on it only before rescaling O (rare),
+    // so it may skip phases; two barriers by tile parity keep that safe: o_done[j % 2] cannot
+    // complete its next phase (P_{j+2} . V_{j+2}) before softmax has passed tile j + 2.
+    uint64_t* o_done = bars + 23;   // [2]
     uint64_t* mma_drain = bars + 7;  // all MMAs of the CTA complete
     uint64_t* k_full = bars + 8;    // [3] s^K, z^K of a key tile landed
     uint64_t* k_empty = bars + 11;  // [3] S MMA done with them
@@ -107,6 +110,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     uint64_t* s_free = bars + 20;    // [2] P_j . V_j done: S buffer j % 2 may take S_{j+2}
     uint64_t* pv_drain = bars + 22;  // all P.V MMAs complete
     auto B = [&](uint64_t* p) { return smem_u32(p); };
+    // The abort flag is read warp-uniformly: a warp whose lanes saw different values would
+    // reach its later warp-wide votes and shuffles with only some of its lanes.
+    auto aborted = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0); };
 
     if (threadIdx.x == 0) {
         mbar_init(B(q_full), 1);
@@ -122,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
         for (int i = 0; i < 2; ++i) mbar_init(B(s_full + i), 1);
         mbar_init(B(p_full), 128);
-        mbar_init(B(o_done), 1);
+        for (int i = 0; i < 2; ++i) mbar_init(B(o_done + i), 1);
         mbar_init(B(mma_drain), 1);
         mbar_init(B(pv_drain), 1);
         for (int i = 0; i < 2; ++i) mbar_init(B(s_free + i), 1);
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 ok = false;
                 break;
             }
-            if (*abort_flag) {
+            if (aborted()) {
                 ok = false;
                 break;
             }
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             auto s_tile = [&](int jj, auto U) -> bool {
                 constexpr int st = decltype(U)::value % kKStages, sb = decltype(U)::value & 1;
                 // S buffer sb still holds P_{jj-2} until P_{jj-2} . V_{jj-2} has completed
-                if (*abort_flag || !wait_all(B(k_full + st), (jj / kKStages) & 1, a.status) ||
+                if (aborted() || !wait_all(B(k_full + st), (jj / kKStages) & 1, a.status) ||
                     (jj >= 2 && !wait_all(B(s_free + sb), ((jj >> 1) - 1) & 1, a.status)))
                     return false;
                 tc_fence_after();
@@ -281,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const uint64_t dSV = mndesc128(S0 + OFF_V), dZV = mndesc32(S0 + OFF_V + STAGE_Z);
             auto pv_tile = [&](int j, auto PAR) -> bool {
                 constexpr int vs = decltype(PAR)::value;  // value stage = S buffer = j % 2
-                if (*abort_flag || !wait_all(B(p_full), j & 1, a.status) ||
+                if (aborted() || !wait_all(B(p_full), j & 1, a.status) ||
                     !wait_all(B(v_full + vs), (j >> 1) & 1, a.status))
                     return false;
                 tc_fence_after();
@@ -295,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     }
                 }
                 if (elect_one_sync()) {
-                    tc_commit(B(o_done));
+                    tc_commit(B(o_done + vs));
                     tc_commit(B(v_empty + vs));
                     tc_commit(B(s_free + vs));
                 }
@@ -350,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int qpos = qs + min(q0 + row, Tq - 1);
         float mref = -INFINITY, l = 0.f;
         for (int j = 0; j < nt; ++j) {
-            if (!ok || *abort_flag) {
+            if (!ok || aborted()) {
                 ok = false;
                 break;
             }
@@ -431,26 +437,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
             l = l * alpha + rs;
             mref = muse;
-            // O may only be rescaled once P_{j-1} . V_{j-1} has finished accumulating into it.
-            if (j > 0) {
-                ok = wait_all(B(o_done), (j - 1) & 1, a.status);
+            // O may only be rescaled once P_{j-1} . V_{j-1} has finished accumulating into it;
+            // without a rescale, P_j . V_j simply queues behind it in the tensor pipe.
+            if (j > 0 && __any_sync(0xffffffffu, raise)) {
+                ok = wait_all(B(o_done + ((j - 1) & 1)), ((j - 1) >> 1) & 1, a.status);
                 if (!ok) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, raise)) {
-                    uint32_t v[32];
+                uint32_t v[32];
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        tmem_ld_32x32b_x32(tmem + tl + TM_OS + c * 32, v);
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld_32x32b_x32(tmem + tl + TM_OS + c * 32, v);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        tmem_st_32x32b_x32(tmem + tl + TM_OS + c * 32, v);
-                    }
-                    tmem_ld_32x32b_x16(tmem + tl + TM_OZ, v);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st_32x32b_x16(tmem + tl + TM_OZ, v);
-                    tmem_wait_st();
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    tmem_st_32x32b_x32(tmem + tl + TM_OS + c * 32, v);
                 }
+                tmem_ld_32x32b_x16(tmem + tl + TM_OZ, v);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                tmem_st_32x32b_x16(tmem + tl + TM_OZ, v);
             }
             tmem_wait_st();
             fence_proxy_async_smem();  // zeroed value rows (if any) before the tensor core reads them
@@ -458,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             mbar_arrive(B(p_full));
         }
         // ---- epilogue: out = (O_s + B^V O_z) / l
-        if (ok) ok = wait_all(B(o_done), (nt - 1) & 1, a.status);
+        if (ok) ok = wait_all(B(o_done + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, a.status);
         if (ok) {
             tc_fence_after();
             uint32_t vz[16];
