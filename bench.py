@@ -286,7 +286,7 @@ class PrefillHarness:
     """Per 512-token chunk: lrkv_append of both sequences' rows, then lrkv_prefill."""
 
     profile = "prefill_chunked.md"
-    sources = ("prefill.cu", "lrkv_internal.cuh", "kernels.h")
+    sources = ("prefill_tc.cu", "lrkv_internal.cuh", "kernels.h")
 
     def __init__(self, wl, rank):
         import torch
@@ -362,7 +362,8 @@ class PrefillHarness:
                        "parallelism": f"replicas x{world} (independent batches)"},
             "roofline": {"kernel": "lrkv_prefill (8 chunk launches)", "bound": "tensor", "achieved": achieved,
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                         "traffic": None, "algorithmic_flops_per_launch": self.kernel_units / len(self.chunks),
+                         "traffic": recorded_traffic(self.profile, self.sources),
+                         "algorithmic_flops_per_launch": self.kernel_units / len(self.chunks),
                          "avg_launch_ms": kernel_s * 1e3 / len(self.chunks)},
             "e2e_unit_value": lambda s: tokens / s, "e2e_unit": "tokens/s",
         }

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(192, 1)
         // epilogue: warps 2..5 -> TMEM lane quarters 2, 3, 0, 1
         const int q = warp & 3;
         bool ok = mbar_wait(smem_u32(accf), 0, a.status);
-        ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
+        ok = __all_sync(0xffffffffu, ok && !*abort_flag);  // warp-uniform: tcgen05.ld below is warp-collective
         tc_fence_after();
         if (ok) {
             const int row = m0 + q * 32 + lane;

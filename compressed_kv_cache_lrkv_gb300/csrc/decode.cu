@@ -317,12 +317,15 @@ __global__ void __launch_bounds__(256, 1)
         for (int j = grp; j < nst; j += a.ng) {
             const int kk = kbase + j;
             const int slot = kk % nslot;
-            if (*abort_flag) continue;
+            // Abort and wait outcomes are made warp-uniform: the stage's work below is
+            // warp-collective (ldmatrix, mma.sync, shuffles).
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) continue;
             // Groups run at different speeds, so the slot may still hold a stage one or
             // more ring rounds older than kk; its barrier parity alone cannot tell them
             // apart.  Wait until stage kk has been issued into the slot, then for its data.
-            if (!wait_tag(tag + slot, kk, a.status) ||
-                !mbar_wait(smem_u32(&full[slot]), (kk / nslot) & 1, a.status)) {
+            const bool ready = wait_tag(tag + slot, kk, a.status) &&
+                               mbar_wait(smem_u32(&full[slot]), (kk / nslot) & 1, a.status);
+            if (!__all_sync(0xffffffffu, ready)) {
                 *abort_flag = 1;
                 continue;
             }

@@ -308,6 +308,26 @@ __device__ __forceinline__ bool elect_one_sync() {
     return p != 0;
 }
 
+// D (TMEM, fp32) (+)= A . B, kind::tf32, A read from tensor memory (one 32-bit element per
+// column, so a K=8 step spans 8 columns), B from shared memory.
+__device__ __forceinline__ void tc_mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor for kind::tf32: fp32 accumulator, A and B tf32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+    return (1u << 4)                       // D format: f32
+           | (2u << 7)                     // A format: tf32
+           | (2u << 10)                    // B format: tf32
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
 // D (TMEM, fp32) (+)= A . B with A read from tensor memory: lane i holds row i of A, each
 // 32-bit column two consecutive K elements (bf16), so a K=16 step spans 8 columns.
 __device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,

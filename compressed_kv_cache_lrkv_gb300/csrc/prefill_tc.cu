@@ -10,8 +10,9 @@
 //          columns of S_j's own buffer
 //   O_s += P_j . s^V (N = 128),  O_z += P_j . z^V_h (N = 16)   in TMEM, A operand P_j
 //          read from TMEM
-// with Q~ = Q . B_h^K computed on the tensor cores in the prologue, and the
-// epilogue out = (O_s + B_h^V O_z) / l in fp32.  Warp roles: warp 0 key-tile TMA
+// with Q~ = Q . B_h^K computed on the tensor cores in the prologue.  After the last
+// tile O_s += O_z . (B_h^V)^T runs as two kind::tf32 MMAs (A = O_z straight from TMEM,
+// B = B_h^V widened to fp32 in shared memory), so the epilogue is out = O_s / l.  Warp roles: warp 0 key-tile TMA
 // producer (3-stage ring), warp 6 value-tile TMA producer (2-stage ring), warp 1
 // score-MMA issuer and TMEM owner, warp 7 P.V-MMA issuer, warps 2..5 softmax /
 // epilogue (one query row per thread, TMEM lane quarter = warp % 4).
@@ -32,7 +33,10 @@ constexpr int kBM = 128, kBN = 128;
 constexpr uint32_t OFF_Q = 0;           // [128 q][128 d] K-major, 128B swizzle, two 64-column blocks
 constexpr uint32_t OFF_QT = 32768;      // [128 q][16] K-major, 32B swizzle
 constexpr uint32_t OFF_BK = 36864;      // [128 d][16] MN-major (B operand of Q~), 32B swizzle
-constexpr uint32_t OFF_BV = 40960;      // [128 d][16] plain, epilogue
+// After the prologue the B^K area and the 4 KiB after it hold B_h^V as fp32 for the final tf32 MMA:
+// [128 d][16 j], K-major without swizzle -- 8 x 4-element core matrices, element (d, j)
+// at (d / 8) * 512 + (j / 4) * 128 + (d % 8) * 16 + (j % 4) * 4.
+constexpr uint32_t OFF_BVF = OFF_BK;
 // Key ring (3 stages: s^K [128 keys][128] K-major 128B swizzle, then z^K_h [128][16] 32B
 // swizzle) and value ring (2 stages: s^V, z^V_h, same layouts, read MN-major).
 constexpr int kKStages = 3, kVStages = 2;
@@ -100,6 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // so it may skip phases; two barriers by tile parity keep that safe: o_done[j % 2] cannot
     // complete its next phase (P_{j+2} . V_{j+2}) before softmax has passed tile j + 2.
     uint64_t* o_done = bars + 23;   // [2]
+    uint64_t* fin_done = bars + 25;  // O_s += O_z . B^V^T complete
     uint64_t* mma_drain = bars + 7;  // all MMAs of the CTA complete
     uint64_t* k_full = bars + 8;    // [3] s^K, z^K of a key tile landed
     uint64_t* k_empty = bars + 11;  // [3] S MMA done with them
@@ -129,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         for (int i = 0; i < 2; ++i) mbar_init(B(s_full + i), 1);
         mbar_init(B(p_full), 128);
         for (int i = 0; i < 2; ++i) mbar_init(B(o_done + i), 1);
+        mbar_init(B(fin_done), 1);
         mbar_init(B(mma_drain), 1);
         mbar_init(B(pv_drain), 1);
         for (int i = 0; i < 2; ++i) mbar_init(B(s_free + i), 1);
@@ -312,6 +318,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 ok = pv_tile(j, std::integral_constant<int, 0>{});
                 if (ok && j + 1 < nt) ok = pv_tile(j + 1, std::integral_constant<int, 1>{});
             }
+            // O_s += O_z . (B_h^V)^T.  O_z is read as an MMA operand, so its last
+            // accumulation must have completed first.
+            ok = ok && wait_all(B(o_done + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, a.status);
+            if (ok) {
+                constexpr uint32_t id_fin = idesc_tf32_f32(128, 128);
+                const uint64_t dBV = sdesc(S0 + OFF_BVF, 128, 512, 0);
+                tc_fence_after();
+                if (elect_one_sync()) {
+                    tc_mma_tf32_ts(tmem + TM_OS, tmem + TM_OZ, dBV, id_fin, 1);
+                    tc_mma_tf32_ts(tmem + TM_OS, tmem + TM_OZ + 8, dBV + (256 >> 4), id_fin, 1);
+                    tc_commit(B(fin_done));
+                }
+                __syncwarp();
+            }
             if (!ok) *abort_flag = 1;
             if (elect_one_sync()) tc_commit(B(pv_drain));
             __syncwarp();
@@ -323,15 +343,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int row = qq * 32 + lane;              // query row within the tile = TMEM lane
         const uint32_t tl = (uint32_t)(qq * 32) << 16;
         const int st_tid = threadIdx.x - 64;         // 0..127
-        // B_h^V into shared memory for the epilogue (plain layout [d][j]).
-        {
-            const uint4* src = reinterpret_cast<const uint4*>(a.BV + (size_t)h * D_H * R);
-            uint4* dst = reinterpret_cast<uint4*>(smem + OFF_BV);
-            for (int i = st_tid; i < D_H * R / 8; i += 128) dst[i] = src[i];
-        }
         // Q~ row from TMEM -> bf16 -> shared memory (K-major, 32-byte swizzle).
         bool ok = wait_all(B(qt_mma), 0, a.status);
         tc_fence_after();
+        // B^K has been consumed (qt_mma): B_h^V, widened to fp32, takes its place for the
+        // final tf32 MMA -- thread d writes row d (16 values, 4 core-matrix chunks).
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(a.BV + ((size_t)h * D_H + st_tid) * R);
+            const uint4 w0 = src[0], w1 = src[1];
+            const uint32_t wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            uint8_t* rowp = smem + OFF_BVF + (st_tid >> 3) * 512 + (st_tid & 7) * 16;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                *reinterpret_cast<float4*>(rowp + q4 * 128) =
+                    make_float4(bf16lo(wb[2 * q4]), bf16hi(wb[2 * q4]), bf16lo(wb[2 * q4 + 1]), bf16hi(wb[2 * q4 + 1]));
+        }
         {
             uint32_t v[16];
             tmem_ld_32x32b_x16(tmem + tl + TM_QT, v);
@@ -351,7 +377,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(B(qt_ready));
-        asm volatile("bar.sync 2, 128;" ::: "memory");  // B^V staged
 
         const int qpos = qs + min(q0 + row, Tq - 1);
         float mref = -INFINITY, l = 0.f;
@@ -461,18 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             tc_fence_before();
             mbar_arrive(B(p_full));
         }
-        // ---- epilogue: out = (O_s + B^V O_z) / l
-        if (ok) ok = wait_all(B(o_done + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, a.status);
+        // ---- epilogue: out = O_s / l (O_s already holds the B_h^V O_z term)
+        if (ok) ok = wait_all(B(fin_done), 0, a.status);
         if (ok) {
             tc_fence_after();
-            uint32_t vz[16];
-            tmem_ld_32x32b_x16(tmem + tl + TM_OZ, vz);
-            float oz[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) oz[e] = __uint_as_float(vz[e]);
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int qrow = q0 + row;
-            const uint16_t* bv = reinterpret_cast<const uint16_t*>(smem + OFF_BV);
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
@@ -480,16 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 if (qrow < Tq) {
                     uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float o0 = __uint_as_float(v[e]), o1 = __uint_as_float(v[e + 1]);
-                        const int d0 = c * 32 + e;
-#pragma unroll
-                        for (int jj = 0; jj < R; ++jj) {
-                            o0 = fmaf(__uint_as_float((uint32_t)bv[d0 * R + jj] << 16), oz[jj], o0);
-                            o1 = fmaf(__uint_as_float((uint32_t)bv[(d0 + 1) * R + jj] << 16), oz[jj], o1);
-                        }
-                        pk[e / 2] = pack_bf16x2(o0 * inv, o1 * inv);
-                    }
+                    for (int e = 0; e < 32; e += 2)
+                        pk[e / 2] = pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
                     uint4* dst = reinterpret_cast<uint4*>(out_row(qrow) + c * 32);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
