@@ -312,6 +312,9 @@ class PrefillHarness:
                 slots=i32(np.concatenate([S.slots_for(self.pt, bb, c0, c0 + C) for bb in range(B)])),
                 q=rn(B, C, H, d_h), qs=i32([c0] * B),
                 out=torch.empty(B, C, H, d_h, dtype=torch.bfloat16, device="cuda")))
+        self.side = torch.cuda.Stream()
+        self.fork, self.join = torch.cuda.Event(), torch.cuda.Event()
+        self.appended = [torch.cuda.Event() for _ in self.chunks]
         app = A.append_flops(B * T, d, H, d_h, r)
         pre = sum(A.prefill_flops(B, C, H, d_h, r, q_start=c0) for c0 in range(0, T, C))
         self.kernel_units = pre
@@ -320,11 +323,22 @@ class PrefillHarness:
         self.launches_per_step = 2 * len(self.chunks)
 
     def step(self, stream):
-        b = self.b
-        for ch in self.chunks:
-            b.lrkv_append(self.dims, ch["x"], self.wcat, ch["slots"], self.cache, status=self.status, stream=stream)
+        """Chunk c's prefill needs chunk c's rows in the cache; chunk c+1's append only writes
+        rows that prefill c never reads (its keys end with chunk c).  So the appends run in
+        order on a side stream, each prefill waits for its own chunk's append, and the side
+        stream's GEMMs fill the SMs the prefill's last wave of CTAs leaves idle."""
+        b, side = self.b, self.side
+        self.fork.record(stream)
+        side.wait_event(self.fork)
+        for ch, ev in zip(self.chunks, self.appended):
+            b.lrkv_append(self.dims, ch["x"], self.wcat, ch["slots"], self.cache, status=self.status, stream=side)
+            ev.record(side)
+        for ch, ev in zip(self.chunks, self.appended):
+            stream.wait_event(ev)
             b.lrkv_prefill(self.dims, ch["q"], self.BK, self.BV, self.cache, self.bt, ch["qs"], ch["out"],
                            status=self.status, stream=stream)
+        self.join.record(side)
+        stream.wait_event(self.join)
 
     def kernel(self, stream):
         for ch in self.chunks:
@@ -356,7 +370,8 @@ class PrefillHarness:
             "config": {"workload": f"{wl.key}: {wl.description}", "B": wl.B, "prompt": wl.L, "chunk": wl.chunk,
                        "H": wl.H, "d_h": wl.d_h, "r": wl.r, "d": wl.d, "block_size": 64,
                        "l2": "prompt activations (X, q, out: 192 MiB) larger than L2",
-                       "step": "per 512-token chunk: lrkv_append (1024 rows) + lrkv_prefill",
+                       "step": "per 512-token chunk: lrkv_append (1024 rows) + lrkv_prefill; the appends run on a "
+                               "side stream (chunk c+1's append overlaps chunk c's prefill)",
                        "flops_per_step": self.step_units, "append_flops": self.app_flops,
                        "prefill_flops": self.kernel_units,
                        "parallelism": f"replicas x{world} (independent batches)"},
