@@ -20,8 +20,8 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "work
 DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 EXPORTED = ["lrkv_abi_version", "lrkv_status_string", "lrkv_last_error", "lrkv_cache_block_bytes", "lrkv_append",
-            "lrkv_decode_workspace_bytes", "lrkv_decode", "lrkv_decode_static_ws", "lrkv_prefill_workspace_bytes",
-            "lrkv_prefill"]
+            "lrkv_decode_workspace_bytes", "lrkv_decode", "lrkv_decode_fused", "lrkv_decode_static_ws",
+            "lrkv_prefill_workspace_bytes", "lrkv_prefill"]
 STATIC_WS_BYTES = 16 << 20  # LRKV_STATIC_WS_BYTES
 
 
@@ -67,6 +67,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lrkv_decode_workspace_bytes.argtypes = [P(Dims), i32]
     lib.lrkv_decode.restype = ctypes.c_int
     lib.lrkv_decode.argtypes = [P(Dims), vp, vp, vp, P(Cache), vp, i32, vp, i32, vp, vp, sz, vp, vp]
+    lib.lrkv_decode_fused.restype = ctypes.c_int
+    lib.lrkv_decode_fused.argtypes = [P(Dims), vp, vp, P(Cache), vp, i32, vp, i32, vp, vp, sz, vp, vp]
     lib.lrkv_decode_static_ws.restype = ctypes.c_int
     lib.lrkv_decode_static_ws.argtypes = [P(Dims), vp, vp, vp, P(Cache), vp, i32, vp, i32, vp, vp, vp]
     lib.lrkv_prefill_workspace_bytes.restype = sz
@@ -157,6 +159,17 @@ def lrkv_decode(dims: Dims, q, BK, BV, cache: PagedCache, block_table, seq_lens,
                             int(block_table.shape[1]), _ptr(seq_lens), B, _ptr(out), _ptr(workspace), ws_bytes,
                             _ptr(status), _stream(stream))
     _check(rc, "lrkv_decode")
+
+
+def lrkv_decode_fused(dims: Dims, q, q_tilde, cache: PagedCache, block_table, seq_lens, out, workspace, status=None,
+                      stream=None):
+    """Decode with absorbed weights: q [B, H, d_h], q~ [B, H, r] -> out [B, H, d_h + r] = [o_s | o_z]."""
+    B = int(q.shape[0])
+    c = cache.struct()
+    rc = load().lrkv_decode_fused(ctypes.byref(dims), _ptr(q), _ptr(q_tilde), ctypes.byref(c), _ptr(block_table),
+                                  int(block_table.shape[1]), _ptr(seq_lens), B, _ptr(out), _ptr(workspace),
+                                  int(workspace.numel() * workspace.element_size()), _ptr(status), _stream(stream))
+    _check(rc, "lrkv_decode_fused")
 
 
 def lrkv_decode_static_ws(dims: Dims, q, BK, BV, cache: PagedCache, block_table, seq_lens, out, status=None,

@@ -185,10 +185,13 @@ size_t lrkv_decode_workspace_bytes(const lrkv_dims* dims, int32_t batch) {
     return lrkv::decode_workspace_bytes(dims->H, dims->d_h, dims->r, batch, di.sms, di.smem_optin);
 }
 
-lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, const void* BV, const lrkv_cache* cache,
-                        const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                        int32_t batch, void* out, void* workspace, size_t workspace_bytes, uint32_t* status_dev,
-                        void* stream) {
+// Shared body of lrkv_decode (q~ = q B^K computed here, output B^V-projected) and
+// lrkv_decode_fused (q~ given by the caller, output [o_s | o_z] / l).
+static lrkv_status decode_impl(const lrkv_dims* dims, const void* q, const void* q_tilde, const void* BK,
+                               const void* BV, const lrkv_cache* cache, const int32_t* block_table,
+                               int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch, void* out,
+                               void* workspace, size_t workspace_bytes, uint32_t* status_dev, void* stream) {
+    const bool fused = q_tilde != nullptr;
     lrkv_status s = check_dims(dims);
     if (s != LRKV_OK) return s;
     if ((s = check_cache(cache)) != LRKV_OK) return s;
@@ -197,8 +200,12 @@ lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, co
     if (max_blocks_per_seq < 1 || (long long)max_blocks_per_seq * dims->block_size > (1LL << 30))
         return fail(LRKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", max_blocks_per_seq);
     LRKV_REQUIRE_PTR(q);
-    LRKV_REQUIRE_PTR(BK);
-    LRKV_REQUIRE_PTR(BV);
+    if (fused) {
+        LRKV_REQUIRE_PTR(q_tilde);
+    } else {
+        LRKV_REQUIRE_PTR(BK);
+        LRKV_REQUIRE_PTR(BV);
+    }
     LRKV_REQUIRE_PTR(out);
     if (!block_table || !seq_lens) return fail(LRKV_ERR_INVALID_ARG, "block_table or seq_lens is NULL");
     DeviceInfo di;
@@ -218,6 +225,8 @@ lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, co
     a.q = static_cast<const uint16_t*>(q);
     a.BK = static_cast<const uint16_t*>(BK);
     a.BV = static_cast<const uint16_t*>(BV);
+    a.qt_in = static_cast<const uint16_t*>(q_tilde);
+    a.fused_out = fused ? 1 : 0;
     a.zK = static_cast<const uint16_t*>(cache->zK);
     a.zV = static_cast<const uint16_t*>(cache->zV);
     a.block_table = block_table;
@@ -233,7 +242,24 @@ lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, co
     lrkv::decode_carve_workspace(&a, workspace, dims->H, dims->d_h, dims->r, batch, di.sms, di.smem_optin);
     return cuda_status(lrkv::launch_decode(tK, tV, a, dims->d_h, dims->r, di.sms, di.smem_optin,
                                            static_cast<cudaStream_t>(stream)),
-                       "lrkv_decode launch");
+                       fused ? "lrkv_decode_fused launch" : "lrkv_decode launch");
+}
+
+lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, const void* BV, const lrkv_cache* cache,
+                        const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                        int32_t batch, void* out, void* workspace, size_t workspace_bytes, uint32_t* status_dev,
+                        void* stream) {
+    return decode_impl(dims, q, nullptr, BK, BV, cache, block_table, max_blocks_per_seq, seq_lens, batch, out,
+                       workspace, workspace_bytes, status_dev, stream);
+}
+
+lrkv_status lrkv_decode_fused(const lrkv_dims* dims, const void* q, const void* q_tilde, const lrkv_cache* cache,
+                              const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              int32_t batch, void* out, void* workspace, size_t workspace_bytes,
+                              uint32_t* status_dev, void* stream) {
+    if (!q_tilde) return fail(LRKV_ERR_INVALID_ARG, "q_tilde is NULL");
+    return decode_impl(dims, q, q_tilde, nullptr, nullptr, cache, block_table, max_blocks_per_seq, seq_lens, batch,
+                       out, workspace, workspace_bytes, status_dev, stream);
 }
 
 size_t lrkv_prefill_workspace_bytes(const lrkv_dims* dims, int32_t batch, int32_t Tq) {

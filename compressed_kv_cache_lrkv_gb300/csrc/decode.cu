@@ -271,9 +271,24 @@ __global__ void __launch_bounds__(256, 1)
             qt_ready = true;
         }
 
-        // This lane's q~ row, chunk-rotated so that z rows are read conflict-free.
+        // This lane's q~ row, chunk-rotated so that z rows are read conflict-free: from the
+        // absorb kernel's fp32 output, or as bf16 straight from the caller (absorbed weights).
         float qt[R];
-        {
+        if (a.qt_in) {
+            const uint4* qrow = reinterpret_cast<const uint4*>(a.qt_in + ((size_t)b * H + (hz_ok ? hzh : 0)) * R);
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) {
+                const uint4 x = qrow[(cc + rot) % NC];
+                qt[cc * 8 + 0] = hz_ok ? bf16lo(x.x) : 0.f;
+                qt[cc * 8 + 1] = hz_ok ? bf16hi(x.x) : 0.f;
+                qt[cc * 8 + 2] = hz_ok ? bf16lo(x.y) : 0.f;
+                qt[cc * 8 + 3] = hz_ok ? bf16hi(x.y) : 0.f;
+                qt[cc * 8 + 4] = hz_ok ? bf16lo(x.z) : 0.f;
+                qt[cc * 8 + 5] = hz_ok ? bf16hi(x.z) : 0.f;
+                qt[cc * 8 + 6] = hz_ok ? bf16lo(x.w) : 0.f;
+                qt[cc * 8 + 7] = hz_ok ? bf16hi(x.w) : 0.f;
+            }
+        } else {
             const float* qrow = a.qt + ((size_t)b * H + (hz_ok ? hzh : 0)) * R;
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) {
@@ -571,7 +586,7 @@ __global__ void __launch_bounds__(1024) decode_combine_kernel(const DecodeArgs a
 
     // B_h^V row of output column c (prefetched while the partials are loaded)
     uint4 bvr[R / 8];
-    if (tid < D_H) {
+    if (tid < D_H && !a.fused_out) {  // (no B^V in the fused form)
         const uint4* bv = reinterpret_cast<const uint4*>(a.BV + ((size_t)h * D_H + tid) * R);
 #pragma unroll
         for (int i = 0; i < R / 8; ++i) bvr[i] = __ldg(bv + i);
@@ -580,11 +595,12 @@ __global__ void __launch_bounds__(1024) decode_combine_kernel(const DecodeArgs a
     __syncthreads();
     const SeqLens seql{a.seq_lens, slc};
     pdl_wait();
-    uint16_t* dst = a.out + ((size_t)b * H + h) * D_H;
+    const int OW = a.fused_out ? W : D_H;  // output row width
+    uint16_t* dst = a.out + ((size_t)b * H + h) * OW;
     const int L = seql[b];
     if (L < 1 || L > cap) {
         if (tid == 0 && h == 0) set_status(a.status, LRKV_DEV_BAD_SEQLEN);
-        if (tid < D_H) dst[tid] = 0;
+        if (tid < OW) dst[tid] = 0;
         return;
     }
     int nsplits;
@@ -641,7 +657,12 @@ __global__ void __launch_bounds__(1024) decode_combine_kernel(const DecodeArgs a
         }
         // each thread reads only its own column, so slice 0's slot can take the result
         sm_acc[0][tid] = lsum > 0.f ? v / lsum : 0.f;
+        if (a.fused_out) {  // [o_s | o_z] / l: the B^V up-projection belongs to the caller's W^O
+            const __nv_bfloat16 ob = __float2bfloat16_rn(sm_acc[0][tid]);
+            dst[tid] = *reinterpret_cast<const uint16_t*>(&ob);
+        }
     }
+    if (a.fused_out) return;
     __syncthreads();
     if (tid < D_H) {
         float v = sm_acc[0][tid];
@@ -727,13 +748,21 @@ static cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size
 template <int D_H, int R>
 static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, const DecodePlan& p,
                                    int G, cudaStream_t stream) {
-    decode_absorb_kernel<D_H, R><<<dim3(a.H, a.B), 256, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     auto split = decode_split_kernel<D_H, R>;
-    e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+    cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(split, dim3(G), dim3(p.threads), p.smem_bytes, stream, tK, tV, a);
+    if (a.qt_in) {
+        // q~ comes from the caller: no absorb kernel, and the split is an ordinary launch --
+        // a dependent launch could start streaming the cache before the caller's previous
+        // kernel on this stream (an append of the newest rows) has finished.
+        split<<<G, p.threads, p.smem_bytes, stream>>>(tK, tV, a);
+        e = cudaGetLastError();
+    } else {
+        decode_absorb_kernel<D_H, R><<<dim3(a.H, a.B), 256, 0, stream>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(split, dim3(G), dim3(p.threads), p.smem_bytes, stream, tK, tV, a);
+    }
     if (e != cudaSuccess) return e;
     return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, a.B), dim3(1024), 0, stream, a, G);
 }

@@ -29,8 +29,10 @@ struct DecodeArgs {
     float* part_ml;   // [H][Pmax][2]  running max (log2 domain) and sum
     float* part_acc;  // [H][Pmax][D_H + R]
     float* qt;        // [B][H][R]  q~ = q B^K, fp32
+    const uint16_t* qt_in;  // [B][H][R] bf16 q~ supplied by the caller (absorbed query weights), or null
     uint32_t* status;
-    uint16_t* out;    // [B][H][D_H]
+    uint16_t* out;    // [B][H][D_H], or [B][H][D_H + R] = [o_s | o_z] / l when fused_out
+    int fused_out;    // 1: no B^V up-projection (absorbed into the output projection)
     int B, H, max_pages, num_blocks;
     int ng, nslot, stage_bytes;
     int pmax;          // partial slots per head in the workspace (max(G, B))

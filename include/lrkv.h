@@ -140,6 +140,28 @@ lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, co
                         size_t workspace_bytes, uint32_t* status_dev, void* stream);
 
 /*
+ * lrkv_decode_fused -- lrkv_decode with both absorptions moved into the caller's
+ *   weights (the associativity of frame "Compute logits without expanding
+ *   historical keys", step 1, and of Eq. (7), "reduce the latents to one r-vector,
+ *   then map"): the query arrives with q~_h = x (W_h^Q B_h^K) already projected,
+ *   and the output is returned before the residual up-projection, for an output
+ *   projection with B_h^V folded into W^O.  Per sequence b and head h:
+ *     score_t = ([q_h | q~_h] . [s^K_t | z^K_{h,t}]) * scale;  a_h = softmax_t(score)
+ *     out_h   = [ sum_t a_t s^V_t  |  sum_t a_t z^V_{h,t} ]        (width d_h + r)
+ *   i.e. single-head softmax attention over the concatenated features.
+ *   q           [batch][H][d_h]   bf16
+ *   q_tilde     [batch][H][r]     bf16, 16-byte aligned
+ *   out         [batch][H][d_h + r] bf16 (nearest, ties to even from fp32)
+ *   Everything else (cache, block_table, seq_lens, workspace, status, errors, the
+ *   stream) is as for lrkv_decode; no B^K or B^V is read.  Unlike lrkv_decode, the
+ *   call does not overlap the caller's previous kernel on the stream.
+ */
+lrkv_status lrkv_decode_fused(const lrkv_dims* dims, const void* q, const void* q_tilde, const lrkv_cache* cache,
+                              const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              int32_t batch, void* out, void* workspace, size_t workspace_bytes,
+                              uint32_t* status_dev, void* stream);
+
+/*
  * lrkv_decode_static_ws -- lrkv_decode without a caller workspace.  (The paper has
  *   no counterpart; this is a deployment convenience.)
  *   For callers that cannot allocate device memory: cudaMalloc/cudaFree can

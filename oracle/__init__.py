@@ -95,6 +95,9 @@ class Oracle:
         L.oracle_decode_cache.argtypes = ([_c_int] * 6 + [_u16p] * 4 + [_i32p, _c_int, _i32p] +
                                           [_u16p] * 3 + [_c_double, _u8p_or_null, _f64p])
         L.oracle_decode_cache.restype = _c_int
+        L.oracle_decode_fused.argtypes = ([_c_int] * 6 + [_u16p] * 4 + [_i32p, _c_int, _i32p] +
+                                          [_u16p, _u16p, _c_double, _u8p_or_null, _f64p])
+        L.oracle_decode_fused.restype = _c_int
         L.oracle_prefill_expanded.argtypes = ([_c_int] * 7 + [_i32p] + [_u16p] * 8 +
                                               [_c_double, _u8p_or_null, _f64p])
         L.oracle_prefill_expanded.restype = _c_int
@@ -169,6 +172,22 @@ class Oracle:
                                           float(scale), wp, out)
         if rc != 0:
             raise ValueError("oracle_decode_cache: bad block id or length")
+        return out
+
+    def decode_fused(self, cache, block_table, seq_lens, q, q_tilde, scale=0.0, want=None, bs=64):
+        """Decode with absorbed weights: q [B, H, d_h], q~ [B, H, r] -> [B, H, d_h + r] = [o_s | o_z]."""
+        sK, sV, zK, zV = (_u16(c) for c in cache)
+        B, H, d_h = q.shape
+        r = q_tilde.shape[2]
+        nb = sK.shape[0]
+        bt = _i32(block_table)
+        max_pages = bt.shape[1]
+        out = np.zeros((B, H, d_h + r), np.float64)
+        w, wp = _want_ptr(want, B, H)
+        rc = self.lib.oracle_decode_fused(B, H, d_h, r, bs, nb, sK, sV, zK, zV, bt, max_pages, _i32(seq_lens),
+                                          _u16(q), _u16(q_tilde), float(scale), wp, out)
+        if rc != 0:
+            raise ValueError("oracle_decode_fused: bad block id or length")
         return out
 
     # -- prefill ----------------------------------------------------------------

@@ -308,6 +308,64 @@ int oracle_decode_cache(int B, int H, int d_h, int r, int bs, int num_blocks,
     return bad ? -1 : 0;
 }
 
+/* Decode with absorbed weights (both absorptions folded into the caller's projections,
+ * frame "Compute logits without expanding historical keys" step 1 and Eq. (7)): the query
+ * arrives as [q_h | q~_h] (q~_h = x W_h^Q B_h^K) and the result is returned before the
+ * residual up-projection.  Written out plainly, that is single-head softmax attention over
+ * concatenated features, with the scale of the d_h-wide dot product:
+ *     keys [s^K_t | z^K_{h,t}],  values [s^V_t | z^V_{h,t}],  query [q_h | q~_h],
+ *     out_h = softmax_t(([q_h | q~_h] . [s^K_t | z^K_{h,t}]) * scale) [s^V_t | z^V_{h,t}]
+ * out: [B][H][d_h + r].  Returns 0, or -1 when a block id or length is out of range. */
+int oracle_decode_fused(int B, int H, int d_h, int r, int bs, int num_blocks,
+                        const uint16_t* sK, const uint16_t* sV, const uint16_t* zK, const uint16_t* zV,
+                        const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                        const uint16_t* q, const uint16_t* qt, double scale, const uint8_t* want, double* out) {
+    for (int b = 0; b < B; ++b) {
+        if (seq_lens[b] < 0 || seq_lens[b] > max_pages * bs) return -1;
+        for (int p = 0; p < (seq_lens[b] + bs - 1) / bs; ++p) {
+            int32_t blk = block_table[(size_t)b * max_pages + p];
+            if (blk < 0 || blk >= num_blocks) return -1;
+        }
+    }
+    scale = default_scale(scale, d_h);
+    const int w = d_h + r;
+    int bad = 0;
+    #pragma omp parallel for schedule(dynamic)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        if (want && !want[bh]) continue;
+        int L = seq_lens[b];
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * w);
+        double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * w);
+        double* qc = (double*)malloc(sizeof(double) * (size_t)w);
+        if (!K || !V || !qc) {
+            #pragma omp atomic write
+            bad = 1;
+        } else {
+            for (int t = 0; t < L; ++t) {
+                int64_t slot = (int64_t)block_table[(size_t)b * max_pages + t / bs] * bs + t % bs;
+                for (int i = 0; i < d_h; ++i) {
+                    K[(size_t)t * w + i] = bf(sK[slot * d_h + i]);
+                    V[(size_t)t * w + i] = bf(sV[slot * d_h + i]);
+                }
+                for (int j = 0; j < r; ++j) {
+                    K[(size_t)t * w + d_h + j] = bf(zK[(slot * H + h) * r + j]);
+#if LRKV_ORACLE_MUTANT == 7
+                    V[(size_t)t * w + d_h + j] = 0.0; /* planted: residual values dropped */
+#else
+                    V[(size_t)t * w + d_h + j] = bf(zV[(slot * H + h) * r + j]);
+#endif
+                }
+            }
+            for (int i = 0; i < d_h; ++i) qc[i] = bf(q[((size_t)b * H + h) * d_h + i]);
+            for (int j = 0; j < r; ++j) qc[d_h + j] = bf(qt[((size_t)b * H + h) * r + j]);
+            oracle_attend(L, w, qc, K, V, scale, out + ((size_t)b * H + h) * w);
+        }
+        free(K); free(V); free(qc);
+    }
+    return bad ? -1 : 0;
+}
+
 /* ---------------------------------------------------------------- prefill */
 
 /* Causal limit: query at absolute position pos sees keys j <= pos. */

@@ -274,10 +274,60 @@ def pin_prefill_causal_edges(o):
     np.testing.assert_allclose(out[:, -1], dec, rtol=1e-13, atol=1e-15)
 
 
+# ---------------------------------------------------------------------------- absorbed (fused) decode
+def _gather_rows(pools, pt, b, L):
+    """Token rows 0..L-1 of sequence b from the paged pools: sK, sV [L, d_h]; zK, zV [L, H, r] (fp64)."""
+    slots = np.asarray(S.slots_for(pt, b, 0, L), np.int64)
+    return tuple(f64(p.reshape((-1,) + p.shape[2:])[slots]) for p in pools)
+
+
+def pin_fused_is_concatenated_attention(o):
+    """With both absorptions in the caller's weights, decode is single-head attention over
+    the concatenated features [q | q~] . [s^K | z^K_h] with values [s^V | z^V_h] and the
+    scale of the d_h-wide dot product: torch SDPA on exactly those tensors."""
+    B, H, d_h, r = 2, 3, 16, 8
+    lens = [150, 77]
+    pt = S.page_table(21, lens, 64, spare_blocks=2)
+    pools = random_pools(21, pt.num_blocks, H, d_h, r)
+    q = S.gaussian_bf16(21, "q", (B, H, d_h))
+    qt = S.gaussian_bf16(21, "qt", (B, H, r))
+    got = o.decode_fused(pools, pt.block_table, lens, q, qt)
+    for b in range(B):
+        sK, sV, zK, zV = _gather_rows(pools, pt, b, lens[b])
+        for h in range(H):
+            Kc = np.concatenate([sK, zK[:, h]], axis=1)[None]
+            Vc = np.concatenate([sV, zV[:, h]], axis=1)[None]
+            qc = np.concatenate([f64(q[b, h]), f64(qt[b, h])])[None, None]
+            ref = _sdpa(qc, Kc, Vc, 1.0 / np.sqrt(d_h))[0, 0]
+            np.testing.assert_allclose(got[b, h], ref, rtol=1e-12, atol=1e-14)
+
+
+def pin_fused_matches_factored_decode(o):
+    """On integer q and B^K, q~ = q B^K is exact in bf16, so the absorbed decode must agree
+    with the expanded decode: o_s + B^V o_z = softmax(q K_h^T * scale) V_h.  Pins where q~
+    enters the logits and that B^V is applied to the aggregated latent, not per token."""
+    B, H, d_h, r = 2, 3, 16, 8
+    lens = [130, 64]
+    pt = S.page_table(22, lens, 64, spare_blocks=1)
+    pools = random_pools(22, pt.num_blocks, H, d_h, r)
+    q = S.int_grid_bf16(22, "q", (B, H, d_h), -1, 1)
+    BK = S.int_grid_bf16(22, "BK", (H, d_h, r), -1, 1)
+    BV = S.gaussian_bf16(22, "BV", (H, d_h, r), 0.5)
+    qt_exact = np.einsum("bhd,hdr->bhr", f64(q), f64(BK))
+    assert np.all(np.abs(qt_exact) <= 256) and np.all(qt_exact == np.round(qt_exact))
+    qt = _lib_bf16(qt_exact)
+    fused = o.decode_fused(pools, pt.block_table, lens, q, qt)
+    o_s, o_z = fused[..., :d_h], fused[..., d_h:]
+    recomposed = o_s + np.einsum("hdr,bhr->bhd", f64(BV), o_z)
+    ref = o.decode_cache(pools, pt.block_table, lens, BK, BV, q)
+    np.testing.assert_allclose(recomposed, ref, rtol=1e-12, atol=1e-13)
+
+
 PINS = [pin_softmax_worked_value, pin_softmax_normalised, pin_attend_special_cases,
         pin_append_integer_exact, pin_append_gaussian_rounding, pin_r0_is_mqa, pin_mha_special_case,
         pin_factored_equals_expanded, pin_cache_path_matches_weight_path,
-        pin_head_permutation_equivariance, pin_page_permutation_invariance, pin_prefill_causal_edges]
+        pin_head_permutation_equivariance, pin_page_permutation_invariance, pin_prefill_causal_edges,
+        pin_fused_is_concatenated_attention, pin_fused_matches_factored_decode]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -288,7 +338,8 @@ def test_pin(pin, oracle_lib):
 # Each planted mistake, and what it models:
 #  1 residual term U_h B_h^T dropped      2 B^K used for values       3 scale 1/d_h
 #  4 causal diagonal excluded             5 shared term dropped       6 B_h read transposed
-MUTANTS = [1, 2, 3, 4, 5, 6]
+#  7 absorbed decode drops the residual values z^V
+MUTANTS = [1, 2, 3, 4, 5, 6, 7]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
