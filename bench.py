@@ -16,10 +16,12 @@ Other workloads (--workload): "dsv2" (H=128, d_h=128, r=16, d=16384, batch 8,
 2048 tokens), "small" (the single-layer parity case) -- decode steps as above;
 "prefill": causal chunked prefill plus cache append (d=4096, H=32, d_h=128,
 r=16, batch 2, 4096-token prompts in 512-token chunks), value in prompt
-tokens/s with the tensor roofline of the prefill kernel.
+tokens/s with the tensor roofline of the prefill kernel.  --fused runs a decode
+workload through lrkv_decode_fused (both absorptions in the caller's weights:
+q~ given, [o_s | o_z] returned), counting that form's own bytes.
 
 Prints one JSON line.
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lrkv|reference] [--workload NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lrkv|reference] [--workload NAME] [--fused]
 """
 from __future__ import annotations
 
@@ -169,11 +171,11 @@ class DecodeHarness:
     profile = "decode_split_longctx.md"
     sources = ("decode.cu", "lrkv_internal.cuh", "kernels.h")
 
-    def __init__(self, wl, rank):
+    def __init__(self, wl, rank, fused=False):
         import torch
 
         from compressed_kv_cache_lrkv_gb300 import binding as b
-        self.torch, self.b, self.wl = torch, b, wl
+        self.torch, self.b, self.wl, self.fused = torch, b, wl, fused
         B, H, d_h, r, d = wl.B, wl.H, wl.d_h, wl.r, wl.d
         self.seq_lens = workload_seq_lens(wl)
         self.pt = S.page_table(wl.seed, self.seq_lens, 64)
@@ -188,35 +190,43 @@ class DecodeHarness:
                 cache=b.PagedCache(rn(nb, 64, d_h), rn(nb, 64, d_h), rn(nb, 64, H, r), rn(nb, 64, H, r)),
                 q=rn(B, H, d_h), BK=rn(H, d_h, r, scale=r ** -0.5), BV=rn(H, d_h, r, scale=r ** -0.5),
                 wcat=rn(2 * (d_h + H * r), d, scale=d ** -0.5), x=rn(B, d),
-                out=torch.empty(B, H, d_h, dtype=torch.bfloat16, device="cuda")))
+                qt=rn(B, H, r) if fused else None,
+                out=torch.empty(B, H, d_h + (r if fused else 0), dtype=torch.bfloat16, device="cuda")))
         self.bt = i32(self.pt.block_table)
         self.sl = i32(self.pt.seq_lens)
         self.slots = i32([self.pt.slot(i, int(L) - 1) for i, L in enumerate(self.seq_lens)])
         self.ws = b.alloc_workspace(b.decode_workspace_bytes(self.dims, B))
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.cache_bytes = wl.layers * sum(t.numel() * t.element_size() for t in self.layers[0]["cache"].tensors())
-        dec = A.decode_algorithmic_bytes(H, d_h, r, self.seq_lens, layers=wl.layers)
+        acct = A.decode_fused_algorithmic_bytes if fused else A.decode_algorithmic_bytes
+        dec = acct(H, d_h, r, self.seq_lens, layers=wl.layers)
         app = wl.layers * A.append_algorithmic_bytes(B, d, H, d_h, r)
         self.kernel_units = dec          # algorithmic bytes of the timed kernel calls
         self.step_units = dec + app      # algorithmic bytes of a step
-        self.launches_per_step = wl.layers * 4
+        self.launches_per_step = wl.layers * (3 if fused else 4)
+
+    def _decode(self, L, stream):
+        if self.fused:
+            self.b.lrkv_decode_fused(self.dims, L["q"], L["qt"], L["cache"], self.bt, self.sl, L["out"], self.ws,
+                                     status=self.status, stream=stream)
+        else:
+            self.b.lrkv_decode(self.dims, L["q"], L["BK"], L["BV"], L["cache"], self.bt, self.sl, L["out"], self.ws,
+                               status=self.status, stream=stream)
 
     def step(self, stream):
         b = self.b
         for L in self.layers:
             b.lrkv_append(self.dims, L["x"], L["wcat"], self.slots, L["cache"], status=self.status, stream=stream)
-            b.lrkv_decode(self.dims, L["q"], L["BK"], L["BV"], L["cache"], self.bt, self.sl, L["out"], self.ws,
-                          status=self.status, stream=stream)
+            self._decode(L, stream)
 
     def kernel(self, stream):
         for L in self.layers:
-            self.b.lrkv_decode(self.dims, L["q"], L["BK"], L["BV"], L["cache"], self.bt, self.sl, L["out"], self.ws,
-                               status=self.status, stream=stream)
+            self._decode(L, stream)
 
     def e2e_setup(self):
         t = self.torch
         self.h_in = [(L["x"].cpu().pin_memory(), L["x"]) for L in self.layers] + \
-                    [(L["q"].cpu().pin_memory(), L["q"]) for L in self.layers] + \
+                    [(L[k].cpu().pin_memory(), L[k]) for L in self.layers for k in ("q", "qt") if L[k] is not None] + \
                     [(self.slots.cpu().pin_memory(), self.slots), (self.sl.cpu().pin_memory(), self.sl)]
         self.h_out = [(t.empty_like(L["out"], device="cpu").pin_memory(), L["out"]) for L in self.layers]
         return (sum(h.numel() * h.element_size() for h, _ in self.h_in),
@@ -244,12 +254,15 @@ class DecodeHarness:
                        "l2": (f"inputs larger than L2: cache {self.cache_bytes / 2**20:.0f} MiB vs L2 "
                               f"{L2_BYTES / 2**20:.0f} MiB") if self.cache_bytes > L2_BYTES else
                              "cache fits in L2 (parity-sized workload; not an HBM measurement)",
-                       "step": "per layer: lrkv_append (1 row per sequence) + lrkv_decode",
+                       "step": "per layer: lrkv_append (1 row per sequence) + " +
+                               ("lrkv_decode_fused (q~ given, [o_s | o_z] returned)" if self.fused else "lrkv_decode"),
                        "parallelism": f"replicas x{world} (independent batches)"},
-            "roofline": {"kernel": "lrkv_decode (absorb + split + combine kernels)", "bound": "hbm",
+            "roofline": {"kernel": "lrkv_decode_fused (split + combine kernels)" if self.fused else
+                                   "lrkv_decode (absorb + split + combine kernels)", "bound": "hbm",
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": recorded_traffic(self.profile, self.sources) if wl.key == "longctx" else None,
+                         "traffic": recorded_traffic(self.profile, self.sources)
+                                    if wl.key == "longctx" and not self.fused else None,
                          "algorithmic_bytes_per_launch": self.kernel_units // wl.layers,
                          "avg_launch_ms": kernel_s * 1e3 / wl.layers},
             "e2e_unit_value": lambda s: self.step_units * world / s / 1e9, "e2e_unit": "GB/s",
@@ -268,16 +281,22 @@ class DecodeHarness:
         BK = S.gaussian_bf16(wl.seed, "bl_BK", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
         BV = S.gaussian_bf16(wl.seed, "bl_BV", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
         q = S.gaussian_bf16(wl.seed, "bl_q", (1, wl.H, wl.d_h))
+        qt = S.gaussian_bf16(wl.seed, "bl_qt", (1, wl.H, wl.r))
         reps, t0 = 0, time.perf_counter()
         while True:
-            o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
+            if self.fused:
+                o.decode_fused(pools, pt.block_table, pt.seq_lens, q, qt)
+            else:
+                o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
             reps += 1
             dt = time.perf_counter() - t0
             if dt >= budget_s:
                 break
-        nbytes = A.decode_algorithmic_bytes(wl.H, wl.d_h, wl.r, [tokens]) * reps
+        acct = A.decode_fused_algorithmic_bytes if self.fused else A.decode_algorithmic_bytes
+        nbytes = acct(wl.H, wl.d_h, wl.r, [tokens]) * reps
+        what = "absorbed-weights decode" if self.fused else "E2 decode"
         return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
-                "sample": f"E2 decode of the workload's first sequence ({tokens} cached tokens, all {wl.H} heads, "
+                "sample": f"{what} of the workload's first sequence ({tokens} cached tokens, all {wl.H} heads, "
                           f"one layer), {reps} repetitions in {dt:.1f} s; fp64, OpenMP over heads"}
 
 
@@ -422,7 +441,9 @@ def run_gpu(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     wl = S.WORKLOADS[args.workload]
-    hz = HARNESS[args.workload](wl, rank)
+    if args.fused and HARNESS[args.workload] is not DecodeHarness:
+        raise SystemExit("--fused applies to the decode workloads")
+    hz = DecodeHarness(wl, rank, fused=True) if args.fused else HARNESS[args.workload](wl, rank)
     stream = torch.cuda.current_stream()
 
     # Each timed step is one replay of a CUDA graph of the public calls, so host
@@ -564,6 +585,8 @@ def main():
     ap.add_argument("--impl", default="lrkv", choices=["lrkv", "reference"])
     ap.add_argument("--workload", default="longctx", choices=sorted(HARNESS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="decode with absorbed weights (lrkv_decode_fused: q~ given, [o_s | o_z] returned)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

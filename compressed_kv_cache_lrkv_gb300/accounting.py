@@ -68,6 +68,15 @@ def decode_algorithmic_bytes(H: int, d_h: int, r: int, seq_lens: Iterable[int], 
     return per_layer * layers
 
 
+def decode_fused_algorithmic_bytes(H: int, d_h: int, r: int, seq_lens: Iterable[int], layers: int = 1) -> int:
+    """Bytes of one decode step with both absorptions in the caller's weights: every cached
+    token's compressed row, the query [q | q~] in and [o_s | o_z] out (all bf16)."""
+    seq_lens = list(int(x) for x in seq_lens)
+    B = len(seq_lens)
+    per_layer = sum(seq_lens) * lrkv_cache_elements(H, d_h, r) * BF16_BYTES + 2 * B * H * (d_h + r) * BF16_BYTES
+    return per_layer * layers
+
+
 def decode_flops(H: int, d_h: int, r: int, seq_lens: Iterable[int], layers: int = 1) -> int:
     """Multiply-adds x 2 of factored decode: per cached token 4H(d_h + r); per sequence
     4 H d_h r for q~ = q B^K and the B^V up-projection."""
