@@ -568,19 +568,22 @@ __global__ void __launch_bounds__(256, 1)
 
 // ------------------------------------------------------------------ kernel 2
 // Log-sum-exp merge of a sequence's partials, residual up-projection, bf16 store.
-// grid (H, B), 1024 threads = NSL partial slices x W columns.  Each slice merges
+// grid (H, B), blockDim = NSL partial slices x W columns, NSL <= 1024 / W chosen on the
+// host so that the grid is about one wave (many (head, sequence) pairs get small
+// blocks, several per SM; few pairs get many slices each).  Each slice merges
 // its own partials (all loads issued together), then the slices are merged in
 // shared memory; the B_h^V row of each output column is prefetched up front.
 template <int D_H, int R>
 __global__ void __launch_bounds__(1024) decode_combine_kernel(const DecodeArgs a, int G) {
     constexpr int W = D_H + R;
-    constexpr int NSL = 1024 / W;     // slices
-    constexpr int PPS = 8;            // partials a slice loads per round
+    constexpr int NSL_MAX = 1024 / W;  // slices at most
+    constexpr int PPS = 8;             // partials a slice loads per round
+    const int NSL = blockDim.x / W;    // slices of this launch
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int H = a.H;
     const int cap = a.max_pages * kBlockSize;
-    __shared__ float sm_m[NSL], sm_l[NSL];
-    __shared__ float sm_acc[NSL][W];
+    __shared__ float sm_m[NSL_MAX], sm_l[NSL_MAX];
+    __shared__ float sm_acc[NSL_MAX][W];
     __shared__ int slc[kSeqCache];
     const int sl = tid / W, c = tid - (tid / W) * W;
 
@@ -591,7 +594,7 @@ __global__ void __launch_bounds__(1024) decode_combine_kernel(const DecodeArgs a
 #pragma unroll
         for (int i = 0; i < R / 8; ++i) bvr[i] = __ldg(bv + i);
     }
-    stage_seq_lens(slc, a.seq_lens, a.B, tid, 1024);
+    stage_seq_lens(slc, a.seq_lens, a.B, tid, blockDim.x);
     __syncthreads();
     const SeqLens seql{a.seq_lens, slc};
     pdl_wait();
@@ -647,7 +650,7 @@ __global__ void __launch_bounds__(1024) decode_combine_kernel(const DecodeArgs a
     if (tid < W) {
         float M = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < NSL; ++i) M = fmaxf(M, sm_m[i]);
+        for (int i = 0; i < NSL; ++i) M = fmaxf(M, sm_m[i]);  // (NSL is known at run time only)
         float lsum = 0.f, v = 0.f;
 #pragma unroll
         for (int i = 0; i < NSL; ++i) {
@@ -764,7 +767,11 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
         e = launch_pdl(split, dim3(G), dim3(p.threads), p.smem_bytes, stream, tK, tV, a);
     }
     if (e != cudaSuccess) return e;
-    return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, a.B), dim3(1024), 0, stream, a, G);
+    // Slices per (head, sequence): enough threads for about one wave of the GPU in total.
+    constexpr int W = D_H + R;
+    const long long pairs = (long long)a.H * a.B;
+    const int nsl = (int)max(1LL, min((long long)(1024 / W), ((long long)G * 1024) / max(1LL, pairs * W)));
+    return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, a.B), dim3(nsl * W), 0, stream, a, G);
 }
 
 cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int G,
