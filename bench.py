@@ -396,6 +396,7 @@ class PrefillHarness:
                        "parallelism": f"replicas x{world} (independent batches)"},
             "roofline": {"kernel": "lrkv_prefill (8 chunk launches)", "bound": "tensor", "achieved": achieved,
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                         "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                          "traffic": recorded_traffic(self.profile, self.sources),
                          "algorithmic_flops_per_launch": self.kernel_units / len(self.chunks),
                          "avg_launch_ms": kernel_s * 1e3 / len(self.chunks)},
@@ -483,6 +484,15 @@ def run_gpu(args, world, rank, local):
         dist.barrier()
     torch.cuda.synchronize()
     step_s = e0.elapsed_time(e1) * 1e-3 / args.steps
+    # per-step spread, from a separate shorter loop so the timed region above has no extra events
+    nd = max(1, min(args.steps, 200))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nd + 1)]
+    evs[0].record(stream)
+    for i in range(nd):
+        g_step.replay()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per_step_ms = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(nd))
     k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     k0.record(stream)
     for _ in range(args.steps):
@@ -522,6 +532,8 @@ def run_gpu(args, world, rank, local):
     line["cpu_baseline"] = cpu
     line["e2e"] = {"value": e2e_fn(e2e_s), "unit": e2e_unit, "ms_per_step": e2e_s * 1e3,
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+    line["step_ms_spread"] = {"median": statistics.median(per_step_ms), "min": per_step_ms[0],
+                              "max": per_step_ms[-1], "reps": nd}
     line["gpu_launches"] = hz.launches_per_step * args.steps
     line["timing"] = "each step is one replay of a CUDA graph of the public calls; CUDA events on the stream"
     line["clocks"] = sampler.summary(t_wall0 - 0.3, t_wall1 + 0.3)
