@@ -57,6 +57,7 @@ _u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
 _i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
 _f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
 _u8p_or_null = ctypes.c_void_p
+_i32p_or_null = ctypes.c_void_p
 _c_int = ctypes.c_int
 _c_double = ctypes.c_double
 
@@ -95,9 +96,17 @@ class Oracle:
         L.oracle_decode_cache.argtypes = ([_c_int] * 6 + [_u16p] * 4 + [_i32p, _c_int, _i32p] +
                                           [_u16p] * 3 + [_c_double, _u8p_or_null, _f64p])
         L.oracle_decode_cache.restype = _c_int
-        L.oracle_decode_fused.argtypes = ([_c_int] * 6 + [_u16p] * 4 + [_i32p, _c_int, _i32p] +
-                                          [_u16p, _u16p, _c_double, _u8p_or_null, _f64p])
-        L.oracle_decode_fused.restype = _c_int
+        L.oracle_decode_fused_rope.argtypes = ([_c_int] * 7 + [_u16p] * 4 + [_i32p, _c_int, _i32p] +
+                                               [_u16p, _u16p, _c_double, _u8p_or_null, _f64p])
+        L.oracle_decode_fused_rope.restype = _c_int
+        L.oracle_decode_cache_rope.argtypes = ([_c_int] * 7 + [_u16p] * 4 + [_i32p, _c_int, _i32p] +
+                                               [_u16p] * 3 + [_c_double, _u8p_or_null, _f64p])
+        L.oracle_decode_cache_rope.restype = _c_int
+        L.oracle_prefill_cache_rope.argtypes = ([_c_int] * 8 + [_u16p] * 4 + [_i32p, _c_int, _i32p] +
+                                                [_u16p] * 3 + [_c_double, _u8p_or_null, _f64p])
+        L.oracle_prefill_cache_rope.restype = _c_int
+        L.oracle_append_rope.argtypes = ([_c_int] * 6 + [_c_double] + [_u16p] * 6 + [_i32p_or_null] +
+                                         [_u16p] * 4)
         L.oracle_prefill_expanded.argtypes = ([_c_int] * 7 + [_i32p] + [_u16p] * 8 +
                                               [_c_double, _u8p_or_null, _f64p])
         L.oracle_prefill_expanded.restype = _c_int
@@ -129,18 +138,24 @@ class Oracle:
         return out
 
     # -- Eqs. (4)-(5) ---------------------------------------------------------
-    def append(self, X, WsK, WsV, UK, UV):
-        """Dense cache rows for X [n, d]: (sK [n,d_h], sV, zK [n,H,r], zV) as bf16 bits."""
+    def append(self, X, WsK, WsV, UK, UV, WKR=None, positions=None, rope_base=10000.0):
+        """Dense cache rows for X [n, d]: (sK [n, d_h + d_rope], sV [n, d_h], zK [n,H,r], zV) as
+        bf16 bits.  With WKR [d, d_rope], sK carries the shared positional key rotated at
+        positions[t] after its d_h content entries."""
         X = _u16(X)
         n, d = X.shape
         d_h = WsK.shape[1]
         H, _, r = UK.shape
-        sK = np.empty((n, d_h), np.uint16)
+        d_rope = 0 if WKR is None else WKR.shape[1]
+        sK = np.empty((n, d_h + d_rope), np.uint16)
         sV = np.empty((n, d_h), np.uint16)
         zK = np.empty((n, H, r), np.uint16)
         zV = np.empty((n, H, r), np.uint16)
-        self.lib.oracle_append(n, d, d_h, H, r, X, _u16(WsK), _u16(WsV), _u16(UK), _u16(UV),
-                               sK, sV, zK, zV)
+        wkr = _u16(WKR) if d_rope else _u16(np.zeros((1, 1), np.uint16))
+        pos = _i32(positions) if d_rope else None
+        self.lib.oracle_append_rope(n, d, d_h, H, r, d_rope, float(rope_base), X, _u16(WsK), wkr, _u16(WsV),
+                                    _u16(UK), _u16(UV), None if pos is None else pos.ctypes.data_as(ctypes.c_void_p),
+                                    sK, sV, zK, zV)
         return sK, sV, zK, zV
 
     # -- decode -----------------------------------------------------------------
@@ -159,17 +174,19 @@ class Oracle:
         return out
 
     def decode_cache(self, cache, block_table, seq_lens, BK, BV, q, scale=0.0, want=None, bs=64):
-        """E2 decode from pools cache=(sK, sV, zK, zV), shaped [nb, bs, d_h] / [nb, bs, H, r]."""
+        """E2 decode from pools cache=(sK, sV, zK, zV), shaped [nb, bs, d_h + d_rope], [nb, bs, d_h],
+        [nb, bs, H, r]; q [B, H, d_h + d_rope] (d_rope > 0: shared positional key after s^K)."""
         sK, sV, zK, zV = (_u16(c) for c in cache)
         H, d_h, r = BK.shape
+        d_rope = sK.shape[-1] - d_h
         nb = sK.shape[0]
         bt = _i32(block_table)
         B, max_pages = bt.shape
         out = np.zeros((B, H, d_h), np.float64)
         w, wp = _want_ptr(want, B, H)
-        rc = self.lib.oracle_decode_cache(B, H, d_h, r, bs, nb, sK, sV, zK, zV, bt, max_pages,
-                                          _i32(seq_lens), _u16(BK), _u16(BV), _u16(q),
-                                          float(scale), wp, out)
+        rc = self.lib.oracle_decode_cache_rope(B, H, d_h, r, d_rope, bs, nb, sK, sV, zK, zV, bt, max_pages,
+                                               _i32(seq_lens), _u16(BK), _u16(BV), _u16(q),
+                                               float(scale), wp, out)
         if rc != 0:
             raise ValueError("oracle_decode_cache: bad block id or length")
         return out
@@ -177,15 +194,17 @@ class Oracle:
     def decode_fused(self, cache, block_table, seq_lens, q, q_tilde, scale=0.0, want=None, bs=64):
         """Decode with absorbed weights: q [B, H, d_h], q~ [B, H, r] -> [B, H, d_h + r] = [o_s | o_z]."""
         sK, sV, zK, zV = (_u16(c) for c in cache)
-        B, H, d_h = q.shape
+        B, H = q.shape[:2]
+        d_h = sV.shape[-1]
+        d_rope = sK.shape[-1] - d_h
         r = q_tilde.shape[2]
         nb = sK.shape[0]
         bt = _i32(block_table)
         max_pages = bt.shape[1]
         out = np.zeros((B, H, d_h + r), np.float64)
         w, wp = _want_ptr(want, B, H)
-        rc = self.lib.oracle_decode_fused(B, H, d_h, r, bs, nb, sK, sV, zK, zV, bt, max_pages, _i32(seq_lens),
-                                          _u16(q), _u16(q_tilde), float(scale), wp, out)
+        rc = self.lib.oracle_decode_fused_rope(B, H, d_h, r, d_rope, bs, nb, sK, sV, zK, zV, bt, max_pages,
+                                               _i32(seq_lens), _u16(q), _u16(q_tilde), float(scale), wp, out)
         if rc != 0:
             raise ValueError("oracle_decode_fused: bad block id or length")
         return out
@@ -209,16 +228,17 @@ class Oracle:
     def prefill_cache(self, cache, block_table, q_start, BK, BV, q, scale=0.0, want=None, bs=64):
         """E2 causal prefill from the paged pools; q [B, Tq, H, d_h]."""
         sK, sV, zK, zV = (_u16(c) for c in cache)
-        _, Tq, H, d_h = q.shape
-        r = BK.shape[2]
+        _, Tq, H = q.shape[:3]
+        d_h, r = BK.shape[1], BK.shape[2]
+        d_rope = sK.shape[-1] - d_h
         nb = sK.shape[0]
         bt = _i32(block_table)
         B, max_pages = bt.shape
         out = np.zeros((B, Tq, H, d_h), np.float64)
         w, wp = _want_ptr(want, B, H)
-        rc = self.lib.oracle_prefill_cache(B, Tq, H, d_h, r, bs, nb, sK, sV, zK, zV, bt, max_pages,
-                                           _i32(q_start), _u16(BK), _u16(BV), _u16(q), float(scale),
-                                           wp, out)
+        rc = self.lib.oracle_prefill_cache_rope(B, Tq, H, d_h, r, d_rope, bs, nb, sK, sV, zK, zV, bt, max_pages,
+                                                _i32(q_start), _u16(BK), _u16(BV), _u16(q), float(scale),
+                                                wp, out)
         if rc != 0:
             raise ValueError("oracle_prefill_cache: bad block id or length")
         return out

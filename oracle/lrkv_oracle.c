@@ -95,23 +95,43 @@ void oracle_softmax(int n, const double* logits, double* p) {
 }
 
 /* Single-head attention over explicit keys and values:
- *   out = softmax(q K^T * scale) V,  K, V: [L][d_h] row-major. */
-void oracle_attend(int L, int d_h, const double* q, const double* K, const double* V,
-                   double scale, double* out) {
-    for (int i = 0; i < d_h; ++i) out[i] = 0.0;
+ *   out = softmax(q K^T * scale) V,  K: [L][dk], V: [L][dv] row-major. */
+static void attend_kv(int L, int dk, int dv, const double* q, const double* K, const double* V, double scale,
+                      double* out) {
+    for (int i = 0; i < dv; ++i) out[i] = 0.0;
     if (L <= 0) return;
     double* logits = (double*)malloc(sizeof(double) * (size_t)L);
     double* p = (double*)malloc(sizeof(double) * (size_t)L);
     for (int t = 0; t < L; ++t) {
         double acc = 0.0;
-        for (int i = 0; i < d_h; ++i) acc += q[i] * K[(size_t)t * d_h + i];
+        for (int i = 0; i < dk; ++i) acc += q[i] * K[(size_t)t * dk + i];
         logits[t] = acc * scale;
     }
     oracle_softmax(L, logits, p);
     for (int t = 0; t < L; ++t)
-        for (int i = 0; i < d_h; ++i) out[i] += p[t] * V[(size_t)t * d_h + i];
+        for (int i = 0; i < dv; ++i) out[i] += p[t] * V[(size_t)t * dv + i];
     free(logits);
     free(p);
+}
+
+void oracle_attend(int L, int d_h, const double* q, const double* K, const double* V,
+                   double scale, double* out) {
+    attend_kv(L, d_h, d_h, q, K, V, scale, out);
+}
+
+/* Rotary position encoding of a d_rope-wide vector at position pos: each pair
+ * (2i, 2i+1) is rotated by the angle pos * base^(-2i / d_rope). */
+static void rope_rotate(double* v, int d_rope, int pos, double base) {
+    for (int i = 0; i < d_rope / 2; ++i) {
+#if LRKV_ORACLE_MUTANT == 8
+        const double a = -(double)pos * pow(base, -2.0 * i / d_rope); /* planted: rotation reversed */
+#else
+        const double a = (double)pos * pow(base, -2.0 * i / d_rope);
+#endif
+        const double c = cos(a), sn = sin(a), x0 = v[2 * i], x1 = v[2 * i + 1];
+        v[2 * i] = x0 * c - x1 * sn;
+        v[2 * i + 1] = x0 * sn + x1 * c;
+    }
 }
 
 static double default_scale(double scale, int d_h) {
@@ -135,13 +155,18 @@ static double b_elem(const uint16_t* Bm, int h, int d_h, int r, int i, int j) {
 /* ---------------------------------------------------------------- Eqs. (4)-(5) */
 
 /* Cache contents for n token rows of X [n][d]:
- *   sK = X W_shared^K, sV = X W_shared^V       -> [n][d_h]
- *   zK[:,h,:] = X U_h^K, zV[:,h,:] = X U_h^V    -> [n][H][r]
- * Weights: Ws* [d][d_h]; U* [H][d][r].  Each element is an fp64 sum over d,
- * rounded to fp32 and then to bf16 (the reference rounding of the cache). */
-void oracle_append(int n, int d, int d_h, int H, int r, const uint16_t* X,
-                   const uint16_t* WsK, const uint16_t* WsV, const uint16_t* UK, const uint16_t* UV,
-                   uint16_t* sK, uint16_t* sV, uint16_t* zK, uint16_t* zV) {
+ *   sK = [X W_shared^K | RoPE(X W^KR)], sV = X W_shared^V   -> [n][d_h + d_rope], [n][d_h]
+ *   zK[:,h,:] = X U_h^K, zV[:,h,:] = X U_h^V                 -> [n][H][r]
+ * The optional decoupled positional key (d_rope > 0; frame "Decoupled RoPE, derived" of
+ * the MLA lesson: one small key per token, shared by all heads, that alone carries the
+ * rotation) is rotated at the token's position before rounding.
+ * Weights: Ws* [d][d_h]; WKR [d][d_rope]; U* [H][d][r].  Each element is an fp64 sum over
+ * d, rounded to fp32 and then to bf16 (the reference rounding of the cache). */
+void oracle_append_rope(int n, int d, int d_h, int H, int r, int d_rope, double rope_base, const uint16_t* X,
+                        const uint16_t* WsK, const uint16_t* WKR, const uint16_t* WsV, const uint16_t* UK,
+                        const uint16_t* UV, const int32_t* positions, uint16_t* sK, uint16_t* sV, uint16_t* zK,
+                        uint16_t* zV) {
+    const int dk = d_h + d_rope;
     #pragma omp parallel for schedule(dynamic)
     for (int t = 0; t < n; ++t) {
         const uint16_t* x = X + (size_t)t * d;
@@ -151,8 +176,18 @@ void oracle_append(int n, int d, int d_h, int H, int r, const uint16_t* X,
                 ak += bf(x[k]) * bf(WsK[(size_t)k * d_h + i]);
                 av += bf(x[k]) * bf(WsV[(size_t)k * d_h + i]);
             }
-            sK[(size_t)t * d_h + i] = oracle_round_to_cache(ak);
+            sK[(size_t)t * dk + i] = oracle_round_to_cache(ak);
             sV[(size_t)t * d_h + i] = oracle_round_to_cache(av);
+        }
+        if (d_rope > 0) {
+            double kr[256];
+            for (int i = 0; i < d_rope && i < 256; ++i) {
+                double a = 0.0;
+                for (int k = 0; k < d; ++k) a += bf(x[k]) * bf(WKR[(size_t)k * d_rope + i]);
+                kr[i] = a;
+            }
+            rope_rotate(kr, d_rope, positions[t], rope_base);
+            for (int i = 0; i < d_rope && i < 256; ++i) sK[(size_t)t * dk + d_h + i] = oracle_round_to_cache(kr[i]);
         }
         for (int h = 0; h < H; ++h)
             for (int j = 0; j < r; ++j) {
@@ -165,6 +200,12 @@ void oracle_append(int n, int d, int d_h, int H, int r, const uint16_t* X,
                 zV[((size_t)t * H + h) * r + j] = oracle_round_to_cache(av);
             }
     }
+}
+
+void oracle_append(int n, int d, int d_h, int H, int r, const uint16_t* X,
+                   const uint16_t* WsK, const uint16_t* WsV, const uint16_t* UK, const uint16_t* UV,
+                   uint16_t* sK, uint16_t* sV, uint16_t* zK, uint16_t* zV) {
+    oracle_append_rope(n, d, d_h, H, r, 0, 0.0, X, WsK, NULL, WsV, UK, UV, NULL, sK, sV, zK, zV);
 }
 
 /* ---------------------------------------------------------------- Eqs. (2)-(3) */
@@ -199,10 +240,10 @@ static void project(int L, int d, int d_h, const uint16_t* Xb, const double* W, 
 
 /* Implied full features from the cache of one token slot:
  *   K_h[t] = s^K_t + B_h^K z^K_{h,t}   (row t of K_s + R_h^K (B_h^K)^T). */
-static void expand_from_cache(int d_h, int H, int r, int h, int64_t slot, const uint16_t* s_pool,
+static void expand_from_cache(int d_h, int s_stride, int H, int r, int h, int64_t slot, const uint16_t* s_pool,
                               const uint16_t* z_pool, const uint16_t* Bm, double* row) {
     for (int i = 0; i < d_h; ++i) {
-        double v = bf(s_pool[slot * d_h + i]);
+        double v = bf(s_pool[slot * s_stride + i]);
 #if LRKV_ORACLE_MUTANT == 5
         v = 0.0;
 #endif
@@ -259,16 +300,19 @@ int oracle_decode_expanded(int B, int H, int d_h, int r, int d, int Lmax, const 
     return bad ? -1 : 0;
 }
 
-/* E2 (expanded from the paged cache).  Pools: s*[num_blocks*bs][d_h],
- * z*[num_blocks*bs][H][r]; token t of sequence b lives in slot
+/* E2 (expanded from the paged cache).  Pools: sK[num_blocks*bs][d_h + d_rope],
+ * sV[num_blocks*bs][d_h], z*[num_blocks*bs][H][r]; token t of sequence b lives in slot
  * block_table[b][t / bs] * bs + t % bs.  For each (b, h): materialise
- * K_h, V_h for t < seq_lens[b] and run textbook attention.
+ *   K_h[t] = [s^K_t + B_h^K z^K_{h,t} | k^R_t]   (k^R: the shared positional key, if any)
+ *   V_h[t] = s^V_t + B_h^V z^V_{h,t}
+ * for t < seq_lens[b] and run textbook attention with q [B][H][d_h + d_rope] at scale
+ * 1/sqrt(d_h + d_rope) (the width of the dotted vectors) unless one is given.
  * Returns 0, or -1 when a block id or length is out of range. */
-int oracle_decode_cache(int B, int H, int d_h, int r, int bs, int num_blocks,
-                        const uint16_t* sK, const uint16_t* sV, const uint16_t* zK, const uint16_t* zV,
-                        const int32_t* block_table, int max_pages, const int32_t* seq_lens,
-                        const uint16_t* BK, const uint16_t* BV, const uint16_t* q, double scale,
-                        const uint8_t* want, double* out) {
+int oracle_decode_cache_rope(int B, int H, int d_h, int r, int d_rope, int bs, int num_blocks,
+                             const uint16_t* sK, const uint16_t* sV, const uint16_t* zK, const uint16_t* zV,
+                             const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                             const uint16_t* BK, const uint16_t* BV, const uint16_t* q, double scale,
+                             const uint8_t* want, double* out) {
     for (int b = 0; b < B; ++b) {
         if (seq_lens[b] < 0 || seq_lens[b] > max_pages * bs) return -1;
         for (int p = 0; p < (seq_lens[b] + bs - 1) / bs; ++p) {
@@ -276,50 +320,68 @@ int oracle_decode_cache(int B, int H, int d_h, int r, int bs, int num_blocks,
             if (blk < 0 || blk >= num_blocks) return -1;
         }
     }
-    scale = default_scale(scale, d_h);
+    const int dk = d_h + d_rope;
+#if LRKV_ORACLE_MUTANT == 9
+    scale = default_scale(scale, d_h); /* planted: scale of the content width only */
+#else
+    scale = default_scale(scale, dk);
+#endif
     int bad = 0;
     #pragma omp parallel for schedule(dynamic)
     for (int bh = 0; bh < B * H; ++bh) {
         int b = bh / H, h = bh % H;
         if (want && !want[bh]) continue;
         int L = seq_lens[b];
-        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * dk);
         double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
-        double qd[512];
-        if (!K || !V || d_h > 512) {
+        double qd[768];
+        if (!K || !V || dk > 768) {
             #pragma omp atomic write
             bad = 1;
         } else {
             for (int t = 0; t < L; ++t) {
                 int64_t slot = (int64_t)block_table[(size_t)b * max_pages + t / bs] * bs + t % bs;
 #if LRKV_ORACLE_MUTANT == 2
-                expand_from_cache(d_h, H, r, h, slot, sK, zK, BK, K + (size_t)t * d_h);
-                expand_from_cache(d_h, H, r, h, slot, sV, zV, BK, V + (size_t)t * d_h); /* planted */
+                expand_from_cache(d_h, dk, H, r, h, slot, sK, zK, BK, K + (size_t)t * dk);
+                expand_from_cache(d_h, d_h, H, r, h, slot, sV, zV, BK, V + (size_t)t * d_h); /* planted */
 #else
-                expand_from_cache(d_h, H, r, h, slot, sK, zK, BK, K + (size_t)t * d_h);
-                expand_from_cache(d_h, H, r, h, slot, sV, zV, BV, V + (size_t)t * d_h);
+                expand_from_cache(d_h, dk, H, r, h, slot, sK, zK, BK, K + (size_t)t * dk);
+                expand_from_cache(d_h, d_h, H, r, h, slot, sV, zV, BV, V + (size_t)t * d_h);
 #endif
+                for (int i = 0; i < d_rope; ++i) K[(size_t)t * dk + d_h + i] = bf(sK[slot * dk + d_h + i]);
             }
-            for (int i = 0; i < d_h; ++i) qd[i] = bf(q[((size_t)b * H + h) * d_h + i]);
-            oracle_attend(L, d_h, qd, K, V, scale, out + ((size_t)b * H + h) * d_h);
+            for (int i = 0; i < dk; ++i) qd[i] = bf(q[((size_t)b * H + h) * dk + i]);
+            attend_kv(L, dk, d_h, qd, K, V, scale, out + ((size_t)b * H + h) * d_h);
         }
         free(K); free(V);
     }
     return bad ? -1 : 0;
 }
 
+int oracle_decode_cache(int B, int H, int d_h, int r, int bs, int num_blocks,
+                        const uint16_t* sK, const uint16_t* sV, const uint16_t* zK, const uint16_t* zV,
+                        const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                        const uint16_t* BK, const uint16_t* BV, const uint16_t* q, double scale,
+                        const uint8_t* want, double* out) {
+    return oracle_decode_cache_rope(B, H, d_h, r, 0, bs, num_blocks, sK, sV, zK, zV, block_table, max_pages,
+                                    seq_lens, BK, BV, q, scale, want, out);
+}
+
 /* Decode with absorbed weights (both absorptions folded into the caller's projections,
  * frame "Compute logits without expanding historical keys" step 1 and Eq. (7)): the query
  * arrives as [q_h | q~_h] (q~_h = x W_h^Q B_h^K) and the result is returned before the
  * residual up-projection.  Written out plainly, that is single-head softmax attention over
- * concatenated features, with the scale of the d_h-wide dot product:
- *     keys [s^K_t | z^K_{h,t}],  values [s^V_t | z^V_{h,t}],  query [q_h | q~_h],
- *     out_h = softmax_t(([q_h | q~_h] . [s^K_t | z^K_{h,t}]) * scale) [s^V_t | z^V_{h,t}]
+ * concatenated features, with the scale of the (d_h + d_rope)-wide dot product:
+ *     keys [s^K_t | k^R_t | z^K_{h,t}],  values [s^V_t | z^V_{h,t}],  query [q_h | q~_h],
+ *     out_h = softmax_t(query . key * scale) value
+ * (k^R, the shared positional key, is present when d_rope > 0; q_h then carries the
+ * caller's rotated positional query in its last d_rope entries).
  * out: [B][H][d_h + r].  Returns 0, or -1 when a block id or length is out of range. */
-int oracle_decode_fused(int B, int H, int d_h, int r, int bs, int num_blocks,
-                        const uint16_t* sK, const uint16_t* sV, const uint16_t* zK, const uint16_t* zV,
-                        const int32_t* block_table, int max_pages, const int32_t* seq_lens,
-                        const uint16_t* q, const uint16_t* qt, double scale, const uint8_t* want, double* out) {
+int oracle_decode_fused_rope(int B, int H, int d_h, int r, int d_rope, int bs, int num_blocks,
+                             const uint16_t* sK, const uint16_t* sV, const uint16_t* zK, const uint16_t* zV,
+                             const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                             const uint16_t* q, const uint16_t* qt, double scale, const uint8_t* want,
+                             double* out) {
     for (int b = 0; b < B; ++b) {
         if (seq_lens[b] < 0 || seq_lens[b] > max_pages * bs) return -1;
         for (int p = 0; p < (seq_lens[b] + bs - 1) / bs; ++p) {
@@ -327,43 +389,50 @@ int oracle_decode_fused(int B, int H, int d_h, int r, int bs, int num_blocks,
             if (blk < 0 || blk >= num_blocks) return -1;
         }
     }
-    scale = default_scale(scale, d_h);
-    const int w = d_h + r;
+    const int ds = d_h + d_rope;      /* shared key width */
+    const int wk = ds + r, wv = d_h + r;
+    scale = default_scale(scale, ds);
     int bad = 0;
     #pragma omp parallel for schedule(dynamic)
     for (int bh = 0; bh < B * H; ++bh) {
         int b = bh / H, h = bh % H;
         if (want && !want[bh]) continue;
         int L = seq_lens[b];
-        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * w);
-        double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * w);
-        double* qc = (double*)malloc(sizeof(double) * (size_t)w);
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * wk);
+        double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * wv);
+        double* qc = (double*)malloc(sizeof(double) * (size_t)wk);
         if (!K || !V || !qc) {
             #pragma omp atomic write
             bad = 1;
         } else {
             for (int t = 0; t < L; ++t) {
                 int64_t slot = (int64_t)block_table[(size_t)b * max_pages + t / bs] * bs + t % bs;
-                for (int i = 0; i < d_h; ++i) {
-                    K[(size_t)t * w + i] = bf(sK[slot * d_h + i]);
-                    V[(size_t)t * w + i] = bf(sV[slot * d_h + i]);
-                }
+                for (int i = 0; i < ds; ++i) K[(size_t)t * wk + i] = bf(sK[slot * ds + i]);
+                for (int i = 0; i < d_h; ++i) V[(size_t)t * wv + i] = bf(sV[slot * d_h + i]);
                 for (int j = 0; j < r; ++j) {
-                    K[(size_t)t * w + d_h + j] = bf(zK[(slot * H + h) * r + j]);
+                    K[(size_t)t * wk + ds + j] = bf(zK[(slot * H + h) * r + j]);
 #if LRKV_ORACLE_MUTANT == 7
-                    V[(size_t)t * w + d_h + j] = 0.0; /* planted: residual values dropped */
+                    V[(size_t)t * wv + d_h + j] = 0.0; /* planted: residual values dropped */
 #else
-                    V[(size_t)t * w + d_h + j] = bf(zV[(slot * H + h) * r + j]);
+                    V[(size_t)t * wv + d_h + j] = bf(zV[(slot * H + h) * r + j]);
 #endif
                 }
             }
-            for (int i = 0; i < d_h; ++i) qc[i] = bf(q[((size_t)b * H + h) * d_h + i]);
-            for (int j = 0; j < r; ++j) qc[d_h + j] = bf(qt[((size_t)b * H + h) * r + j]);
-            oracle_attend(L, w, qc, K, V, scale, out + ((size_t)b * H + h) * w);
+            for (int i = 0; i < ds; ++i) qc[i] = bf(q[((size_t)b * H + h) * ds + i]);
+            for (int j = 0; j < r; ++j) qc[ds + j] = bf(qt[((size_t)b * H + h) * r + j]);
+            attend_kv(L, wk, wv, qc, K, V, scale, out + ((size_t)b * H + h) * wv);
         }
         free(K); free(V); free(qc);
     }
     return bad ? -1 : 0;
+}
+
+int oracle_decode_fused(int B, int H, int d_h, int r, int bs, int num_blocks,
+                        const uint16_t* sK, const uint16_t* sV, const uint16_t* zK, const uint16_t* zV,
+                        const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                        const uint16_t* q, const uint16_t* qt, double scale, const uint8_t* want, double* out) {
+    return oracle_decode_fused_rope(B, H, d_h, r, 0, bs, num_blocks, sK, sV, zK, zV, block_table, max_pages,
+                                    seq_lens, q, qt, scale, want, out);
 }
 
 /* ---------------------------------------------------------------- prefill */
@@ -420,12 +489,14 @@ int oracle_prefill_expanded(int B, int Tq, int H, int d_h, int r, int d, int Lma
     return bad ? -1 : 0;
 }
 
-/* E2 causal prefill from the paged cache (layout as oracle_decode_cache). */
-int oracle_prefill_cache(int B, int Tq, int H, int d_h, int r, int bs, int num_blocks,
-                         const uint16_t* sK, const uint16_t* sV, const uint16_t* zK,
-                         const uint16_t* zV, const int32_t* block_table, int max_pages,
-                         const int32_t* q_start, const uint16_t* BK, const uint16_t* BV,
-                         const uint16_t* q, double scale, const uint8_t* want, double* out) {
+/* E2 causal prefill from the paged cache (layout as oracle_decode_cache_rope): query i of
+ * sequence b, at absolute position q_start[b] + i, attends to keys j <= that position.
+ * q [B][Tq][H][d_h + d_rope] (the positional part already rotated by the caller). */
+int oracle_prefill_cache_rope(int B, int Tq, int H, int d_h, int r, int d_rope, int bs, int num_blocks,
+                              const uint16_t* sK, const uint16_t* sV, const uint16_t* zK,
+                              const uint16_t* zV, const int32_t* block_table, int max_pages,
+                              const int32_t* q_start, const uint16_t* BK, const uint16_t* BV,
+                              const uint16_t* q, double scale, const uint8_t* want, double* out) {
     for (int b = 0; b < B; ++b) {
         int L = q_start[b] + Tq;
         if (q_start[b] < 0 || L > max_pages * bs) return -1;
@@ -434,33 +505,44 @@ int oracle_prefill_cache(int B, int Tq, int H, int d_h, int r, int bs, int num_b
             if (blk < 0 || blk >= num_blocks) return -1;
         }
     }
-    scale = default_scale(scale, d_h);
+    const int dk = d_h + d_rope;
+    scale = default_scale(scale, dk);
     int bad = 0;
     #pragma omp parallel for schedule(dynamic)
     for (int bh = 0; bh < B * H; ++bh) {
         int b = bh / H, h = bh % H;
         if (want && !want[bh]) continue;
         int L = q_start[b] + Tq;
-        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * dk);
         double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_h);
-        double qd[512];
-        if (!K || !V || d_h > 512) {
+        double qd[768];
+        if (!K || !V || dk > 768) {
             #pragma omp atomic write
             bad = 1;
         } else {
             for (int t = 0; t < L; ++t) {
                 int64_t slot = (int64_t)block_table[(size_t)b * max_pages + t / bs] * bs + t % bs;
-                expand_from_cache(d_h, H, r, h, slot, sK, zK, BK, K + (size_t)t * d_h);
-                expand_from_cache(d_h, H, r, h, slot, sV, zV, BV, V + (size_t)t * d_h);
+                expand_from_cache(d_h, dk, H, r, h, slot, sK, zK, BK, K + (size_t)t * dk);
+                expand_from_cache(d_h, d_h, H, r, h, slot, sV, zV, BV, V + (size_t)t * d_h);
+                for (int c = 0; c < d_rope; ++c) K[(size_t)t * dk + d_h + c] = bf(sK[slot * dk + d_h + c]);
             }
             for (int i = 0; i < Tq; ++i) {
-                const uint16_t* qi = q + (((size_t)b * Tq + i) * H + h) * d_h;
-                for (int c = 0; c < d_h; ++c) qd[c] = bf(qi[c]);
-                oracle_attend(visible(q_start[b] + i), d_h, qd, K, V, scale,
-                              out + (((size_t)b * Tq + i) * H + h) * d_h);
+                const uint16_t* qi = q + (((size_t)b * Tq + i) * H + h) * dk;
+                for (int c = 0; c < dk; ++c) qd[c] = bf(qi[c]);
+                attend_kv(visible(q_start[b] + i), dk, d_h, qd, K, V, scale,
+                          out + (((size_t)b * Tq + i) * H + h) * d_h);
             }
         }
         free(K); free(V);
     }
     return bad ? -1 : 0;
+}
+
+int oracle_prefill_cache(int B, int Tq, int H, int d_h, int r, int bs, int num_blocks,
+                         const uint16_t* sK, const uint16_t* sV, const uint16_t* zK,
+                         const uint16_t* zV, const int32_t* block_table, int max_pages,
+                         const int32_t* q_start, const uint16_t* BK, const uint16_t* BV,
+                         const uint16_t* q, double scale, const uint8_t* want, double* out) {
+    return oracle_prefill_cache_rope(B, Tq, H, d_h, r, 0, bs, num_blocks, sK, sV, zK, zV, block_table, max_pages,
+                                     q_start, BK, BV, q, scale, want, out);
 }

@@ -323,11 +323,82 @@ def pin_fused_matches_factored_decode(o):
     np.testing.assert_allclose(recomposed, ref, rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------------------- decoupled positional key
+ROPE_BASE = 10000.0
+
+
+def _rope_np(v: np.ndarray, pos: np.ndarray, base: float = ROPE_BASE) -> np.ndarray:
+    """Rotary encoding written out in numpy: pair (2i, 2i+1) of row t turned by the angle
+    pos[t] * base^(-2i / d)."""
+    d = v.shape[-1]
+    ang = pos[:, None].astype(np.float64) * base ** (-2.0 * np.arange(d // 2) / d)[None, :]
+    c, s_ = np.cos(ang), np.sin(ang)
+    out = np.empty_like(v, dtype=np.float64)
+    out[:, 0::2] = v[:, 0::2] * c - v[:, 1::2] * s_
+    out[:, 1::2] = v[:, 0::2] * s_ + v[:, 1::2] * c
+    return out
+
+
+def pin_rope_append_is_rotation(o):
+    """With a positional key branch the append writes [x W_s^K | R(pos) x W^KR] into the
+    shared key row: on small-integer inputs x W^KR is exact, so the stored positional key
+    must equal the closed-form rotation at each row's position, rounded to bf16 by torch;
+    the content columns must be those of the plain append."""
+    n, d, d_h, H, r, d_rope = 9, 24, 16, 2, 8, 16
+    X = S.int_grid_bf16(31, "X", (n, d), -1, 1)
+    WsK, WsV, WKR = (S.int_grid_bf16(31, nm, (d, w), -1, 1) for nm, w in [("a", d_h), ("b", d_h), ("c", d_rope)])
+    UK, UV = (S.int_grid_bf16(31, nm, (H, d, r), -1, 1) for nm in ["e", "f"])
+    pos = np.array([0, 1, 2, 7, 63, 64, 1000, 4097, 32767], np.int32)
+    sK, sV, zK, zV = o.append(X, WsK, WsV, UK, UV, WKR=WKR, positions=pos)
+    plain = o.append(X, WsK, WsV, UK, UV)
+    np.testing.assert_array_equal(sK[:, :d_h], plain[0])
+    for a_, b_ in zip((sV, zK, zV), plain[1:]):
+        np.testing.assert_array_equal(a_, b_)
+    u = f64(X) @ f64(WKR)  # exact integers
+    want = _lib_bf16(_rope_np(u, pos).astype(np.float32))
+    np.testing.assert_array_equal(sK[:, d_h:], want)
+
+
+def pin_rope_attention_is_concatenated(o):
+    """Decode and causal prefill with the positional branch are textbook attention over the
+    concatenated key [K_h | k^R] and query [q | q^R] at the scale of the (d_h + d_rope)-wide
+    dot product (the MLA lesson, Ch. 3): torch SDPA on exactly those tensors."""
+    B, H, d_h, r, d_rope = 2, 3, 16, 8, 16
+    lens = [140, 70]
+    pt = S.page_table(32, lens, 64, spare_blocks=1)
+    sK, sV, zK, zV = random_pools(32, pt.num_blocks, H, d_h, r)
+    kR = S.gaussian_bf16(32, "kR", (pt.num_blocks, 64, d_rope))
+    pools = (np.ascontiguousarray(np.concatenate([sK, kR], axis=2)), sV, zK, zV)
+    w = weights(32, H * d_h, d_h, H, r)
+    q = S.gaussian_bf16(32, "q", (B, H, d_h + d_rope))
+    scale = 1.0 / np.sqrt(d_h + d_rope)
+    got = o.decode_cache(pools, pt.block_table, lens, w.BK, w.BV, q)
+    Tq = 30
+    qp = S.gaussian_bf16(32, "qp", (B, Tq, H, d_h + d_rope))
+    qs = [lens[0] - Tq, lens[1] - Tq]
+    gotp = o.prefill_cache(pools, pt.block_table, qs, w.BK, w.BV, qp)
+    for b in range(B):
+        rows = _gather_rows(pools, pt, b, lens[b])
+        for h in range(H):
+            Kc = rows[0][:, :d_h] + rows[2][:, h] @ f64(w.BK[h]).T
+            K = np.concatenate([Kc, rows[0][:, d_h:]], axis=1)
+            V = rows[1] + rows[3][:, h] @ f64(w.BV[h]).T
+            ref = _sdpa(f64(q[b, h])[None, None], K[None], V[None], scale)[0, 0]
+            np.testing.assert_allclose(got[b, h], ref, rtol=1e-12, atol=1e-14)
+            # causal: query i at position qs[b] + i sees keys 0 .. qs[b] + i
+            mask = np.arange(lens[b])[None, :] <= (qs[b] + np.arange(Tq))[:, None]
+            out = F.scaled_dot_product_attention(torch.from_numpy(f64(qp[b, :, h])[None]), torch.from_numpy(K[None]),
+                                                 torch.from_numpy(V[None]), attn_mask=torch.from_numpy(mask[None]),
+                                                 scale=scale).numpy()[0]
+            np.testing.assert_allclose(gotp[b, :, h], out, rtol=1e-12, atol=1e-14)
+
+
 PINS = [pin_softmax_worked_value, pin_softmax_normalised, pin_attend_special_cases,
         pin_append_integer_exact, pin_append_gaussian_rounding, pin_r0_is_mqa, pin_mha_special_case,
         pin_factored_equals_expanded, pin_cache_path_matches_weight_path,
         pin_head_permutation_equivariance, pin_page_permutation_invariance, pin_prefill_causal_edges,
-        pin_fused_is_concatenated_attention, pin_fused_matches_factored_decode]
+        pin_fused_is_concatenated_attention, pin_fused_matches_factored_decode,
+        pin_rope_append_is_rotation, pin_rope_attention_is_concatenated]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -339,7 +410,8 @@ def test_pin(pin, oracle_lib):
 #  1 residual term U_h B_h^T dropped      2 B^K used for values       3 scale 1/d_h
 #  4 causal diagonal excluded             5 shared term dropped       6 B_h read transposed
 #  7 absorbed decode drops the residual values z^V
-MUTANTS = [1, 2, 3, 4, 5, 6, 7]
+#  8 positional key rotated the wrong way    9 scale of the content width only with a positional key
+MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
