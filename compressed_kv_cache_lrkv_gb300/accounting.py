@@ -18,9 +18,10 @@ from typing import Iterable
 BF16_BYTES = 2
 
 
-def lrkv_cache_elements(H: int, d_h: int, r: int) -> int:
-    """Elements one token adds to one layer's LRKV cache: s^K, s^V (d_h each) + z^K_h, z^V_h (r each, per head)."""
-    return 2 * (d_h + H * r)
+def lrkv_cache_elements(H: int, d_h: int, r: int, d_rope: int = 0) -> int:
+    """Elements one token adds to one layer's LRKV cache: s^K, s^V (d_h each) + z^K_h, z^V_h (r each, per head),
+    plus the decoupled positional key k^R (d_rope, shared by all heads) when there is one."""
+    return 2 * (d_h + H * r) + d_rope
 
 
 def mha_cache_elements(H: int, d_h: int, layers: int = 1) -> int:
@@ -53,9 +54,9 @@ def kv_params_mha(d: int, d_h: int, H: int) -> int:
     return 2 * H * d * d_h
 
 
-def page_bytes(H: int, d_h: int, r: int, block_size: int = 64) -> int:
+def page_bytes(H: int, d_h: int, r: int, block_size: int = 64, d_rope: int = 0) -> int:
     """Bytes of one cache page (all four arrays, bf16)."""
-    return block_size * lrkv_cache_elements(H, d_h, r) * BF16_BYTES
+    return block_size * lrkv_cache_elements(H, d_h, r, d_rope) * BF16_BYTES
 
 
 def decode_algorithmic_bytes(H: int, d_h: int, r: int, seq_lens: Iterable[int], layers: int = 1) -> int:

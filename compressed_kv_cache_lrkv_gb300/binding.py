@@ -33,7 +33,8 @@ class LrkvError(RuntimeError):
 
 class Dims(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("d_h", ctypes.c_int32), ("r", ctypes.c_int32), ("d", ctypes.c_int32),
-                ("block_size", ctypes.c_int32), ("softmax_scale", ctypes.c_float)]
+                ("block_size", ctypes.c_int32), ("softmax_scale", ctypes.c_float), ("d_rope", ctypes.c_int32),
+                ("rope_base", ctypes.c_float)]
 
 
 class Cache(ctypes.Structure):
@@ -62,7 +63,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lrkv_cache_block_bytes.restype = sz
     lib.lrkv_cache_block_bytes.argtypes = [P(Dims)]
     lib.lrkv_append.restype = ctypes.c_int
-    lib.lrkv_append.argtypes = [P(Dims), vp, vp, i32, vp, P(Cache), vp, vp]
+    lib.lrkv_append.argtypes = [P(Dims), vp, vp, i32, vp, vp, P(Cache), vp, vp]
     lib.lrkv_decode_workspace_bytes.restype = sz
     lib.lrkv_decode_workspace_bytes.argtypes = [P(Dims), i32]
     lib.lrkv_decode.restype = ctypes.c_int
@@ -79,8 +80,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     return lib
 
 
-def make_dims(H: int, d_h: int, r: int, d: int, block_size: int = 64, softmax_scale: float = 0.0) -> Dims:
-    return Dims(H, d_h, r, d, block_size, softmax_scale)
+def make_dims(H: int, d_h: int, r: int, d: int, block_size: int = 64, softmax_scale: float = 0.0, d_rope: int = 0,
+              rope_base: float = 0.0) -> Dims:
+    return Dims(H, d_h, r, d, block_size, softmax_scale, d_rope, rope_base)
 
 
 def _ptr(t) -> int | None:
@@ -112,9 +114,9 @@ class PagedCache:
         self.num_blocks = int(sK.shape[0])
 
     @classmethod
-    def empty(cls, num_blocks: int, H: int, d_h: int, r: int, block_size: int = 64, device="cuda"):
+    def empty(cls, num_blocks: int, H: int, d_h: int, r: int, block_size: int = 64, device="cuda", d_rope: int = 0):
         mk = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=device)
-        return cls(mk(num_blocks, block_size, d_h), mk(num_blocks, block_size, d_h),
+        return cls(mk(num_blocks, block_size, d_h + d_rope), mk(num_blocks, block_size, d_h),
                    mk(num_blocks, block_size, H, r), mk(num_blocks, block_size, H, r))
 
     def struct(self) -> Cache:
@@ -140,12 +142,13 @@ def prefill_workspace_bytes(dims: Dims, batch: int, Tq: int) -> int:
     return int(load().lrkv_prefill_workspace_bytes(ctypes.byref(dims), batch, Tq))
 
 
-def lrkv_append(dims: Dims, X, W_catT, slot_mapping, cache: PagedCache, status=None, stream=None):
-    """Eqs. (4)-(5): write rows of X [n, d] into the cache at slot_mapping [n]."""
+def lrkv_append(dims: Dims, X, W_catT, slot_mapping, cache: PagedCache, status=None, stream=None, positions=None):
+    """Eqs. (4)-(5): write rows of X [n, d] into the cache at slot_mapping [n]; with a
+    positional key (dims.d_rope > 0) its columns are rotated at positions [n] (int32)."""
     n = int(X.shape[0])
     c = cache.struct()
-    rc = load().lrkv_append(ctypes.byref(dims), _ptr(X), _ptr(W_catT), n, _ptr(slot_mapping), ctypes.byref(c),
-                            _ptr(status), _stream(stream))
+    rc = load().lrkv_append(ctypes.byref(dims), _ptr(X), _ptr(W_catT), n, _ptr(slot_mapping), _ptr(positions),
+                            ctypes.byref(c), _ptr(status), _stream(stream))
     _check(rc, "lrkv_append")
 
 
@@ -201,8 +204,10 @@ def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
-def pack_wcat_t(WsK, WsV, UK, UV) -> torch.Tensor:
-    """W_cat^T [N, d] from W_shared^{K,V} [d, d_h] and U^{K,V} [H, d, r] (column order of lrkv_append)."""
+def pack_wcat_t(WsK, WsV, UK, UV, WKR=None) -> torch.Tensor:
+    """W_cat^T [N, d] from W_shared^{K,V} [d, d_h], U^{K,V} [H, d, r] and the optional positional-key
+    projection W^KR [d, d_rope] (column order of lrkv_append)."""
     H, d, r = UK.shape
-    return torch.cat([WsK.t(), WsV.t(), UK.permute(0, 2, 1).reshape(H * r, d),
-                      UV.permute(0, 2, 1).reshape(H * r, d)], dim=0).contiguous()
+    parts = [WsK.t()] + ([] if WKR is None else [WKR.t()])
+    return torch.cat(parts + [WsV.t(), UK.permute(0, 2, 1).reshape(H * r, d),
+                              UV.permute(0, 2, 1).reshape(H * r, d)], dim=0).contiguous()

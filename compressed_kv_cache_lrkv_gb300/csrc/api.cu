@@ -42,7 +42,16 @@ lrkv_status check_dims(const lrkv_dims* dm) {
     if (dm->d < 8 || dm->d % 8 != 0) return fail(LRKV_ERR_UNSUPPORTED, "d %d (must be a positive multiple of 8)", dm->d);
     if (!(dm->softmax_scale >= 0.f) || std::isinf(dm->softmax_scale))
         return fail(LRKV_ERR_INVALID_ARG, "softmax_scale %g", (double)dm->softmax_scale);
+    if (dm->d_rope != 0 && dm->d_rope != 64)
+        return fail(LRKV_ERR_UNSUPPORTED, "d_rope %d (supported: 0, 64)", dm->d_rope);
+    if (!(dm->rope_base >= 0.f) || std::isinf(dm->rope_base) || (dm->rope_base > 0.f && dm->rope_base <= 1.f))
+        return fail(LRKV_ERR_INVALID_ARG, "rope_base %g (0 for 10000, else > 1)", (double)dm->rope_base);
     return LRKV_OK;
+}
+
+// Logit scale: the caller's, else 1/sqrt of the full key width d_h + d_rope.
+float logit_scale(const lrkv_dims* dm) {
+    return dm->softmax_scale > 0.f ? dm->softmax_scale : 1.0f / std::sqrt((float)(dm->d_h + dm->d_rope));
 }
 
 lrkv_status check_cache(const lrkv_cache* c) {
@@ -138,11 +147,12 @@ const char* lrkv_last_error(void) { return g_last_error; }
 
 size_t lrkv_cache_block_bytes(const lrkv_dims* dims) {
     if (check_dims(dims) != LRKV_OK) return 0;
-    return (size_t)dims->block_size * 2 * 2 * (size_t)(dims->d_h + dims->H * dims->r);
+    return (size_t)dims->block_size * 2 * (2 * (size_t)(dims->d_h + dims->H * dims->r) + (size_t)dims->d_rope);
 }
 
 lrkv_status lrkv_append(const lrkv_dims* dims, const void* X, const void* W_catT, int32_t n_tok,
-                        const int32_t* slot_mapping, const lrkv_cache* cache, uint32_t* status_dev, void* stream) {
+                        const int32_t* slot_mapping, const int32_t* positions, const lrkv_cache* cache,
+                        uint32_t* status_dev, void* stream) {
     lrkv_status s = check_dims(dims);
     if (s != LRKV_OK) return s;
     if ((s = check_cache(cache)) != LRKV_OK) return s;
@@ -151,6 +161,8 @@ lrkv_status lrkv_append(const lrkv_dims* dims, const void* X, const void* W_catT
     LRKV_REQUIRE_PTR(X);
     LRKV_REQUIRE_PTR(W_catT);
     if (!slot_mapping) return fail(LRKV_ERR_INVALID_ARG, "slot_mapping is NULL");
+    if (dims->d_rope > 0 && !positions)
+        return fail(LRKV_ERR_INVALID_ARG, "positions is NULL but d_rope is %d", dims->d_rope);
     lrkv::AppendArgs a{};
     a.X = static_cast<const uint16_t*>(X);
     a.W = static_cast<const uint16_t*>(W_catT);
@@ -162,8 +174,11 @@ lrkv_status lrkv_append(const lrkv_dims* dims, const void* X, const void* W_catT
     a.status = status_dev;
     a.n = n_tok;
     a.d = dims->d;
-    a.N = 2 * (dims->d_h + dims->H * dims->r);
+    a.N = 2 * (dims->d_h + dims->H * dims->r) + dims->d_rope;
     a.d_h = dims->d_h;
+    a.d_rope = dims->d_rope;
+    a.rope_base = dims->rope_base > 0.f ? dims->rope_base : 10000.f;
+    a.positions = dims->d_rope > 0 ? positions : nullptr;
     a.HR = dims->H * dims->r;
     a.nslots = (long long)cache->num_blocks * dims->block_size;
     if (n_tok >= lrkv::kAppendTcMinRows) {
@@ -218,7 +233,8 @@ static lrkv_status decode_impl(const lrkv_dims* dims, const void* q, const void*
 
     CUtensorMap tK, tV;
     const uint64_t rows = (uint64_t)cache->num_blocks * dims->block_size;
-    if ((s = make_tmap(&tK, cache->sK, dims->d_h, rows, 64, 8, CU_TENSOR_MAP_SWIZZLE_128B, "sK")) != LRKV_OK) return s;
+    const uint64_t dk = (uint64_t)dims->d_h + dims->d_rope;  // key row [s^K | k^R]
+    if ((s = make_tmap(&tK, cache->sK, dk, rows, 64, 8, CU_TENSOR_MAP_SWIZZLE_128B, "sK")) != LRKV_OK) return s;
     if ((s = make_tmap(&tV, cache->sV, dims->d_h, rows, 64, 8, CU_TENSOR_MAP_SWIZZLE_128B, "sV")) != LRKV_OK) return s;
 
     lrkv::DecodeArgs a{};
@@ -237,10 +253,9 @@ static lrkv_status decode_impl(const lrkv_dims* dims, const void* q, const void*
     a.H = dims->H;
     a.max_pages = max_blocks_per_seq;
     a.num_blocks = cache->num_blocks;
-    const float scale = dims->softmax_scale > 0.f ? dims->softmax_scale : 1.0f / std::sqrt((float)dims->d_h);
-    a.scale_log2 = scale * 1.4426950408889634f;
+    a.scale_log2 = logit_scale(dims) * 1.4426950408889634f;
     lrkv::decode_carve_workspace(&a, workspace, dims->H, dims->d_h, dims->r, batch, di.sms, di.smem_optin);
-    return cuda_status(lrkv::launch_decode(tK, tV, a, dims->d_h, dims->r, di.sms, di.smem_optin,
+    return cuda_status(lrkv::launch_decode(tK, tV, a, dims->d_h, dims->r, dims->d_rope, di.sms, di.smem_optin,
                                            static_cast<cudaStream_t>(stream)),
                        fused ? "lrkv_decode_fused launch" : "lrkv_decode launch");
 }
@@ -304,9 +319,8 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, c
     a.H = dims->H;
     a.max_pages = max_blocks_per_seq;
     a.num_blocks = cache->num_blocks;
-    const float scale = dims->softmax_scale > 0.f ? dims->softmax_scale : 1.0f / std::sqrt((float)dims->d_h);
-    a.scale_log2 = scale * 1.4426950408889634f;
-    if (dims->d_h == 128 && dims->r == 16) {
+    a.scale_log2 = logit_scale(dims) * 1.4426950408889634f;
+    if (dims->d_h == 128 && dims->r == 16 && dims->d_rope == 0) {
         lrkv::PrefillMaps mp;
         const uint64_t rows = (uint64_t)cache->num_blocks * dims->block_size;
         const uint64_t HR = (uint64_t)dims->H * dims->r;
@@ -321,7 +335,7 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, c
             return s;
         return cuda_status(lrkv::launch_prefill_tc(mp, a, static_cast<cudaStream_t>(stream)), "lrkv_prefill launch");
     }
-    return cuda_status(lrkv::launch_prefill(a, dims->d_h, dims->r, static_cast<cudaStream_t>(stream)),
+    return cuda_status(lrkv::launch_prefill(a, dims->d_h, dims->r, dims->d_rope, static_cast<cudaStream_t>(stream)),
                        "lrkv_prefill launch");
 }
 

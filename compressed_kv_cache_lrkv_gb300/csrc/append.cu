@@ -19,14 +19,15 @@ namespace lrkv {
 __device__ __forceinline__ void store_cache_value(const AppendArgs& a, long long slot, int col, float v) {
     const __nv_bfloat16 b = __float2bfloat16_rn(v);
     const uint16_t bits = *reinterpret_cast<const uint16_t*>(&b);
-    if (col < a.d_h)
-        a.sK[slot * a.d_h + col] = bits;
-    else if (col < 2 * a.d_h)
-        a.sV[slot * a.d_h + col - a.d_h] = bits;
-    else if (col < 2 * a.d_h + a.HR)
-        a.zK[slot * a.HR + col - 2 * a.d_h] = bits;
+    const int dk = a.d_h + a.d_rope;  // shared key row: [s^K | k^R]
+    if (col < dk)
+        a.sK[slot * dk + col] = bits;
+    else if (col < dk + a.d_h)
+        a.sV[slot * a.d_h + col - dk] = bits;
+    else if (col < dk + a.d_h + a.HR)
+        a.zK[slot * a.HR + col - dk - a.d_h] = bits;
     else
-        a.zV[slot * a.HR + col - 2 * a.d_h - a.HR] = bits;
+        a.zV[slot * a.HR + col - dk - a.d_h - a.HR] = bits;
 }
 
 // Slot of row t, or -1 to skip it (negative entry: padding; too large: status bit).
@@ -57,49 +58,65 @@ __device__ __forceinline__ float dot8(const uint4& w, const uint4& x) {
 // contiguous along d), so the whole weight matrix is in flight in about one
 // memory round trip (N CTAs, one wave); the NT hidden rows are small and
 // stay in L1/L2.  Partial sums are reduced with warp shuffles and then across
-// the four warps in shared memory, always in the same order.
+// the four warps in shared memory, always in the same order.  In the range of the
+// shared positional key a CTA computes the two columns of one rotation pair and turns
+// them at each row's position before rounding.
 template <int NT>
 __global__ void __launch_bounds__(128) append_rowwise_kernel(const AppendArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = blockIdx.x;
+    const int u = blockIdx.x, half = a.d_rope / 2;
+    const bool pair = a.d_rope > 0 && u >= a.d_h && u < a.d_h + half;
+    const int c = (a.d_rope > 0 && u >= a.d_h) ? (pair ? a.d_h + 2 * (u - a.d_h) : u + half) : u;
     const int t0 = blockIdx.y * NT;
-    __shared__ float red[4][NT];
-    float acc[NT];
+    __shared__ float red[2][4][NT];
+    float acc[2][NT];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+    for (int t = 0; t < NT; ++t) acc[0][t] = acc[1][t] = 0.f;
     const uint16_t* wrow = a.W + (size_t)c * a.d;
+    const uint16_t* wrow1 = a.W + (size_t)(pair ? c + 1 : c) * a.d;
     const int nchunk = a.d >> 3;
 #pragma unroll 4
     for (int k8 = threadIdx.x; k8 < nchunk; k8 += 128) {
         const uint4 w = __ldg(reinterpret_cast<const uint4*>(wrow) + k8);
+        const uint4 w1 = pair ? __ldg(reinterpret_cast<const uint4*>(wrow1) + k8) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             if (t0 + t < a.n) {
                 const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + t) * a.d) + k8);
-                acc[t] += dot8(w, x);
+                acc[0][t] += dot8(w, x);
+                if (pair) acc[1][t] += dot8(w1, x);
             }
         }
     }
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        float v = acc[t];
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) red[warp][t] = v;
-    }
+        for (int t = 0; t < NT; ++t) {
+            float v = acc[j][t];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0) red[j][warp][t] = v;
+        }
     __syncthreads();
     if (threadIdx.x < NT && t0 + threadIdx.x < a.n) {
         const int t = threadIdx.x;
-        const float v = (red[0][t] + red[1][t]) + (red[2][t] + red[3][t]);
+        float v0 = (red[0][0][t] + red[0][1][t]) + (red[0][2][t] + red[0][3][t]);
         const long long slot = checked_slot(a, t0 + t);
-        if (slot >= 0) store_cache_value(a, slot, c, v);
+        if (slot >= 0) {
+            if (pair) {
+                float v1 = (red[1][0][t] + red[1][1][t]) + (red[1][2][t] + red[1][3][t]);
+                rope_pair(v0, v1, u - a.d_h, a.d_rope, a.positions[t0 + t], a.rope_base);
+                store_cache_value(a, slot, c + 1, v1);
+            }
+            store_cache_value(a, slot, c, v0);
+        }
     }
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
 #define LRKV_ROW(NTV)                                                                    \
     {                                                                                    \
-        dim3 grid(a.N, (a.n + NTV - 1) / NTV);                                           \
+        dim3 grid(a.N - a.d_rope / 2, (a.n + NTV - 1) / NTV); /* pairs: one CTA each */ \
         append_rowwise_kernel<NTV><<<grid, 128, 0, stream>>>(a);                         \
         return cudaGetLastError();                                                       \
     }

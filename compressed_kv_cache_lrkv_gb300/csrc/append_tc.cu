@@ -34,15 +34,16 @@ __device__ __forceinline__ long long tc_checked_slot(const AppendArgs& a, int t)
 // Eight consecutive output columns col..col+7 (never straddling a segment:
 // every segment boundary is a multiple of 8) of the row at `slot`.
 __device__ __forceinline__ void store8(const AppendArgs& a, long long slot, int col, uint4 v) {
+    const int dk = a.d_h + a.d_rope;  // shared key row: [s^K | k^R]
     uint16_t* dst;
-    if (col < a.d_h)
-        dst = a.sK + slot * a.d_h + col;
-    else if (col < 2 * a.d_h)
-        dst = a.sV + slot * a.d_h + (col - a.d_h);
-    else if (col < 2 * a.d_h + a.HR)
-        dst = a.zK + slot * a.HR + (col - 2 * a.d_h);
+    if (col < dk)
+        dst = a.sK + slot * dk + col;
+    else if (col < dk + a.d_h)
+        dst = a.sV + slot * a.d_h + (col - dk);
+    else if (col < dk + a.d_h + a.HR)
+        dst = a.zK + slot * a.HR + (col - dk - a.d_h);
     else
-        dst = a.zV + slot * a.HR + (col - 2 * a.d_h - a.HR);
+        dst = a.zV + slot * a.HR + (col - dk - a.d_h - a.HR);
     *reinterpret_cast<uint4*>(dst) = v;
 }
 
@@ -136,6 +137,18 @@ __global__ void __launch_bounds__(192, 1)
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+                // Columns of the shared positional key (a 32-aligned range [d_h, d_h + d_rope))
+                // are rotated at the row's position before rounding.
+                if (slot >= 0 && n0 + c0 >= a.d_h && n0 + c0 < a.d_h + a.d_rope) {
+                    const int pos = a.positions[row];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
+                        rope_pair(x0, x1, (n0 + c0 - a.d_h) / 2 + e, a.d_rope, pos, a.rope_base);
+                        v[2 * e] = __float_as_uint(x0);
+                        v[2 * e + 1] = __float_as_uint(x1);
+                    }
+                }
                 if (slot >= 0) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {

@@ -5,6 +5,9 @@
 //     score_t = (q_h . s^K_t + q~_h . z^K_{h,t}) * scale
 //     out_h   = sum_t p_t s^V_t + B_h^V (sum_t p_t z^V_{h,t})       (Eq. (7))
 // Per-head K_h / V_h are never formed.
+// With a decoupled positional key (D_R > 0) the shared key row is [s^K | k^R] and the
+// query [q | q^R]: the tensor-core logits simply run over D_K = D_H + D_R columns,
+// while q~ = q B^K uses the first D_H of them.
 //
 // Kernel 0 (absorb): q~ for every (sequence, head) into the workspace, fp32.
 // Kernel 1 (split): a persistent grid of one CTA per SM, launched with
@@ -120,7 +123,7 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // q~[b][h][j] = sum_d q[b][h][d] B^K[h][d][j]; one block per (head, sequence):
 // 256 / R slices of the d range are summed in parallel, then reduced in
 // shared memory, so all of B_h^K (d_h x r) is in flight at once.
-template <int D_H, int R>
+template <int D_H, int R, int D_R>
 __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) {
     pdl_trigger();
     constexpr int NS = 256 / R;           // d slices
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) 
     const int h = blockIdx.x, b = blockIdx.y;
     const int j = threadIdx.x % R, sl = threadIdx.x / R;
     __shared__ float part[NS][R];
-    const uint16_t* qrow = a.q + ((size_t)b * a.H + h) * D_H + sl * DS;
+    const uint16_t* qrow = a.q + ((size_t)b * a.H + h) * (D_H + D_R) + sl * DS;
     const uint16_t* bk = a.BK + ((size_t)h * D_H + sl * DS) * R + j;
     float acc = 0.f;
 #pragma unroll
@@ -146,9 +149,9 @@ __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) 
 }
 
 // Issue the loads of one 8-token granule (stage) of block `blk` into a ring slot:
-// s^K, s^V by TMA tensor copies (128-byte swizzle), z^K, z^V by bulk copies.
-// An out-of-range block id is reported and the stage is marked empty.
-template <int D_H, int R>
+// s^K (with k^R when D_R > 0), s^V by TMA tensor copies (128-byte swizzle), z^K, z^V by
+// bulk copies.  An out-of-range block id is reported and the stage is marked empty.
+template <int D_H, int R, int D_R>
 __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUtensorMap* tm_sV, const DecodeArgs& a,
                                             uint32_t st, uint32_t bar, int* meta_slot, int blk, int gi,
                                             uint64_t pol) {
@@ -159,16 +162,16 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUte
         return;
     }
     *meta_slot = 1;
-    mbar_arrive_expect_tx(bar, 32u * D_H + 32u * a.H * R);
+    constexpr int D_K = D_H + D_R;
+    mbar_arrive_expect_tx(bar, 16u * (D_K + D_H) + 32u * a.H * R);
     const int row = blk * kBlockSize + ((gi & 7) << 3);
 #pragma unroll
-    for (int i = 0; i < D_H / 64; ++i) {
-        tma_load_2d_hint(st + i * 1024, tm_sK, i * 64, row, bar, pol);
-        tma_load_2d_hint(st + 16 * D_H + i * 1024, tm_sV, i * 64, row, bar, pol);
-    }
+    for (int i = 0; i < D_K / 64; ++i) tma_load_2d_hint(st + i * 1024, tm_sK, i * 64, row, bar, pol);
+#pragma unroll
+    for (int i = 0; i < D_H / 64; ++i) tma_load_2d_hint(st + 16 * D_K + i * 1024, tm_sV, i * 64, row, bar, pol);
     const size_t zoff = (size_t)row * a.H * R;
-    bulk_load_hint(st + 32 * D_H, a.zK + zoff, 16u * a.H * R, bar, pol);
-    bulk_load_hint(st + 32 * D_H + 16 * a.H * R, a.zV + zoff, 16u * a.H * R, bar, pol);
+    bulk_load_hint(st + 16 * (D_K + D_H), a.zK + zoff, 16u * a.H * R, bar, pol);
+    bulk_load_hint(st + 16 * (D_K + D_H) + 16 * a.H * R, a.zV + zoff, 16u * a.H * R, bar, pol);
 }
 
 // ------------------------------------------------------------------ kernel 1
@@ -176,12 +179,14 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUte
 // hold up to 255 registers.  There is no dedicated producer warp: thread 0
 // fills the ring at the start of each split, and afterwards the last warp to
 // release a stage refills that slot with the stage nslot positions ahead.
-template <int D_H, int R>
+template <int D_H, int R, int D_R>
 __global__ void __launch_bounds__(256, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_sK, const __grid_constant__ CUtensorMap tm_sV,
                         const DecodeArgs a) {
     static_assert(D_H == 64 || D_H == 128, "d_h");
+    static_assert(D_R == 0 || D_R == 64, "d_rope");
     static_assert(R % 8 == 0 && R <= 32, "r");
+    constexpr int D_K = D_H + D_R;                              // shared key row [s^K | k^R]
     constexpr int NC = R / 8;                                   // 16-byte chunks per z row
     constexpr int RP128 = (2 * R >= 128) ? 1 : 128 / (2 * R);   // z rows per 128-byte bank line
     constexpr int W = D_H + R;                                  // accumulator width per head
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(256, 1)
                 const int slot = (kbase + k) % nslot;
                 const int pi = ((sp.g0 + k) >> 3) - pg0;
                 tag[slot] = kbase + k;
-                issue_stage<D_H, R>(&tm_sK, &tm_sV, a, smem_s + slot * stage_bytes, smem_u32(&full[slot]),
+                issue_stage<D_H, R, D_R>(&tm_sK, &tm_sV, a, smem_s + slot * stage_bytes, smem_u32(&full[slot]),
                                     &meta[slot], pi < kPageCache ? pages[pi] : bt_row[pg0 + pi], sp.g0 + k, pol);
                 ++nissued[slot];
             }
@@ -305,13 +310,13 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
 
-        // Query A fragments (heads on M): rows hA, hB; k = head dimension.
-        uint32_t qa[D_H / 16][4];
+        // Query A fragments (heads on M): rows hA, hB; k = key feature ([q | q^R]).
+        uint32_t qa[D_K / 16][4];
         {
-            const uint32_t* qA = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * H + hA) * D_H);
-            const uint32_t* qB = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * H + hB) * D_H);
+            const uint32_t* qA = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * H + hA) * D_K);
+            const uint32_t* qB = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * H + hB) * D_K);
 #pragma unroll
-            for (int kk = 0; kk < D_H / 16; ++kk) {
+            for (int kk = 0; kk < D_K / 16; ++kk) {
                 qa[kk][0] = hA < H ? qA[kk * 8 + tq] : 0u;
                 qa[kk][1] = hB < H ? qB[kk * 8 + tq] : 0u;
                 qa[kk][2] = hA < H ? qA[kk * 8 + 4 + tq] : 0u;
@@ -347,14 +352,14 @@ __global__ void __launch_bounds__(256, 1)
             const int t0 = (sp.g0 + j) * kGran;
             const int nvalid = meta[slot] ? min(kGran, L - t0) : 0;
             const uint32_t st = smem_s + slot * stage_bytes;
-            const uint32_t sK_s = st, sV_s = st + 16 * D_H;
-            const uint8_t* zK_p = smem + slot * stage_bytes + 32 * D_H;
+            const uint32_t sK_s = st, sV_s = st + 16 * D_K;
+            const uint8_t* zK_p = smem + slot * stage_bytes + 16 * (D_K + D_H);
             const uint8_t* zV_p = zK_p + 16 * H * R;
 
-            // --- shared logits q . s^K (tensor cores): 16 heads x 8 tokens
+            // --- shared logits [q | q^R] . [s^K | k^R] (tensor cores): 16 heads x 8 tokens
             float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int kk2 = 0; kk2 < D_H / 16; kk2 += 2) {
+            for (int kk2 = 0; kk2 < D_K / 16; kk2 += 2) {
                 const int chunk16 = kk2 * 2 + (lane >> 3);
                 uint32_t b0, b1, b2, b3;
                 ldmatrix_x4(sw128(sK_s + (chunk16 >> 3) * 1024, lane & 7, chunk16 & 7), b0, b1, b2, b3);
@@ -481,7 +486,7 @@ __global__ void __launch_bounds__(256, 1)
                     if (jn < nst && !*abort_flag) {
                         const int pi = ((sp.g0 + jn) >> 3) - pg0;
                         tag[slot] = kk + nslot;
-                        issue_stage<D_H, R>(&tm_sK, &tm_sV, a, st, smem_u32(&full[slot]), &meta[slot],
+                        issue_stage<D_H, R, D_R>(&tm_sK, &tm_sV, a, st, smem_u32(&full[slot]), &meta[slot],
                                             pi < kPageCache ? pages[pi] : bt_row[pg0 + pi], sp.g0 + jn, pol);
                         ++nissued[slot];
                     }
@@ -696,10 +701,10 @@ static int decode_fixed_smem(int ncw, int nslot) {
            1024;
 }
 
-DecodePlan decode_plan(int H, int D_H, int R, int smem_limit) {
+DecodePlan decode_plan(int H, int D_H, int R, int D_R, int smem_limit) {
     DecodePlan p{};
     const int HT = (H + 15) / 16;
-    p.stage_bytes = ((32 * D_H + 32 * H * R) + 1023) & ~1023;
+    p.stage_bytes = ((16 * (2 * D_H + D_R) + 32 * H * R) + 1023) & ~1023;
     int nslot = 16;
     while (nslot > 2 && nslot * p.stage_bytes + decode_fixed_smem(8, nslot) > smem_limit) --nslot;
     p.nslot = nslot;
@@ -748,10 +753,10 @@ static cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-template <int D_H, int R>
+template <int D_H, int R, int D_R>
 static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, const DecodePlan& p,
                                    int G, cudaStream_t stream) {
-    auto split = decode_split_kernel<D_H, R>;
+    auto split = decode_split_kernel<D_H, R, D_R>;
     cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
     if (a.qt_in) {
@@ -761,7 +766,7 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
         split<<<G, p.threads, p.smem_bytes, stream>>>(tK, tV, a);
         e = cudaGetLastError();
     } else {
-        decode_absorb_kernel<D_H, R><<<dim3(a.H, a.B), 256, 0, stream>>>(a);
+        decode_absorb_kernel<D_H, R, D_R><<<dim3(a.H, a.B), 256, 0, stream>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         e = launch_pdl(split, dim3(G), dim3(p.threads), p.smem_bytes, stream, tK, tV, a);
@@ -774,15 +779,17 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
     return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, a.B), dim3(nsl * W), 0, stream, a, G);
 }
 
-cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int G,
-                          int smem_limit, cudaStream_t stream) {
-    const DecodePlan p = decode_plan(a.H, D_H, R, smem_limit);
+cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int D_R,
+                          int G, int smem_limit, cudaStream_t stream) {
+    const DecodePlan p = decode_plan(a.H, D_H, R, D_R, smem_limit);
     a.ng = p.ng;
     a.nslot = p.nslot;
     a.stage_bytes = p.stage_bytes;
     a.pmax = max(G, a.B);
-#define LRKV_DEC(DH, RR) \
-    if (D_H == DH && R == RR) return launch_decode_t<DH, RR>(tK, tV, a, p, G, stream);
+#define LRKV_DEC(DH, RR)                                                                     \
+    if (D_H == DH && R == RR)                                                                \
+        return D_R == 0 ? launch_decode_t<DH, RR, 0>(tK, tV, a, p, G, stream)                \
+                        : launch_decode_t<DH, RR, 64>(tK, tV, a, p, G, stream);
     LRKV_DEC(64, 8) LRKV_DEC(64, 16) LRKV_DEC(64, 32) LRKV_DEC(128, 8) LRKV_DEC(128, 16) LRKV_DEC(128, 32)
 #undef LRKV_DEC
     return cudaErrorInvalidValue;

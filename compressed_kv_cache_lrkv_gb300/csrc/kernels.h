@@ -10,11 +10,14 @@ namespace lrkv {
 
 struct AppendArgs {
     const uint16_t* X;      // [n][d]
-    const uint16_t* W;      // [N][d]
+    const uint16_t* W;      // [N][d], rows [W_s^K | W^KR | W_s^V | U^K | U^V]
     const int32_t* slots;   // [n]
-    uint16_t *sK, *sV, *zK, *zV;
+    const int32_t* positions;  // [n] token positions (for the positional key), or null without one
+    uint16_t *sK, *sV, *zK, *zV;  // sK rows are d_h + d_rope wide: [s^K | k^R]
     uint32_t* status;
     int n, d, N, d_h, HR;
+    int d_rope;             // width of the shared positional key (0: none)
+    float rope_base;
     long long nslots;       // num_blocks * block_size
 };
 
@@ -60,10 +63,10 @@ cudaError_t launch_append_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, con
 
 size_t decode_workspace_bytes(int H, int D_H, int R, int B, int G, int smem_limit);
 void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int B, int G, int smem_limit);
-cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int G,
+cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int D_R, int G,
                           int smem_limit, cudaStream_t stream);
 
-cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, int D_R, cudaStream_t stream);
 
 // Tensor-core prefill (d_h = 128, r = 16).  Maps: q as [B*Tq][H*d_h] box {64,128}
 // and s^K, s^V pools [nb*64][d_h] box {64,64}, both 128-byte swizzle; z^K, z^V

@@ -299,6 +299,20 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Rotary encoding of one pair of the shared positional key (the columns d_h + 2i and
+// d_h + 2i + 1 of a cache row) for token position pos: the pair is turned by the angle
+// pos * base^(-2i / d_rope).  Angle, sine and cosine in double (positions reach 10^5, where
+// an fp32 angle would already be off by ~0.2%), then rounded to fp32 like every column.
+__device__ __forceinline__ void rope_pair(float& x0, float& x1, int i, int d_rope, int pos, float base) {
+    const double ang = (double)pos * pow((double)base, -2.0 * i / d_rope);
+    double sn, cs;
+    sincos(ang, &sn, &cs);
+    const double y0 = (double)x0 * cs - (double)x1 * sn;
+    const double y1 = (double)x0 * sn + (double)x1 * cs;
+    x0 = (float)y0;
+    x1 = (float)y1;
+}
+
 // One lane of a converged warp (the same lane every time for the same active set), for
 // issuing single-thread tcgen05 instructions while the whole warp keeps warp-uniform
 // operands (descriptors, TMEM addresses) in uniform registers.

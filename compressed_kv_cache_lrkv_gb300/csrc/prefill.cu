@@ -5,7 +5,9 @@
 // concatenated rows [q_i | q~_i] . [s^K_j | z^K_{h,j}] (width d_h + r), with
 // q~_i = q_i B_h^K; the value side accumulates P [s^V | z^V_h] into (o_s, o_z)
 // and the epilogue returns o_s + B_h^V o_z.  Query i sits at absolute position
-// q_start + i and sees keys j <= q_start + i.
+// q_start + i and sees keys j <= q_start + i.  With a decoupled positional key
+// (D_R > 0) the shared key row is [s^K | k^R] and the query [q | q^R]: the
+// shared logits run over D_K = D_H + D_R columns, q~ uses the first D_H.
 //
 // One CTA = 64 queries of one (sequence, head); four warps of 16 query rows
 // each run a flash-attention loop over 64-token key tiles (one cache page per
@@ -34,21 +36,24 @@ constexpr int padded_pitch(int row_bytes) { return ((row_bytes / 16) % 2 == 1) ?
 
 }  // namespace
 
-template <int D_H, int R>
+template <int D_H, int R, int D_R>
 struct PrefillTile {
     static constexpr int kTok = 64;
-    static constexpr int kPitchS = padded_pitch(D_H * 2);
+    static constexpr int kPitchK = padded_pitch((D_H + D_R) * 2);  // key rows [s^K | k^R]
+    static constexpr int kPitchS = padded_pitch(D_H * 2);          // value rows s^V
     static constexpr int kPitchZ = padded_pitch(R * 2);
+    static constexpr int kKBytes = kTok * kPitchK;
     static constexpr int kSBytes = kTok * kPitchS;
     static constexpr int kZBytes = kTok * kPitchZ;
-    static constexpr int kStage = 2 * kSBytes + 2 * kZBytes;
+    static constexpr int kStage = kKBytes + kSBytes + 2 * kZBytes;
     static constexpr int kScratch = 4 * 16 * R * 4;  // per-warp [16][R] fp32
     static constexpr int kSmem = 2 * kStage + kScratch;
 };
 
-template <int D_H, int R>
+template <int D_H, int R, int D_R>
 __global__ void __launch_bounds__(128) prefill_kernel(const PrefillArgs a) {
-    using T = PrefillTile<D_H, R>;
+    using T = PrefillTile<D_H, R, D_R>;
+    constexpr int D_K = D_H + D_R;
     extern __shared__ __align__(16) uint8_t smem[];
     const uint32_t smem_s = smem_u32(smem);
     const int qtile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -74,12 +79,12 @@ __global__ void __launch_bounds__(128) prefill_kernel(const PrefillArgs a) {
     const int n_tiles = (qs + last_row) / 64 + 1;
 
     // ---- q fragments and q~ = q B_h^K (fp32, rounded to bf16 for the MMA)
-    uint32_t qa[D_H / 16][4];
+    uint32_t qa[D_K / 16][4];
     {
-        const uint32_t* qA = reinterpret_cast<const uint32_t*>(a.q + (((size_t)b * Tq + rA) * H + h) * D_H);
-        const uint32_t* qB = reinterpret_cast<const uint32_t*>(a.q + (((size_t)b * Tq + rB) * H + h) * D_H);
+        const uint32_t* qA = reinterpret_cast<const uint32_t*>(a.q + (((size_t)b * Tq + rA) * H + h) * D_K);
+        const uint32_t* qB = reinterpret_cast<const uint32_t*>(a.q + (((size_t)b * Tq + rB) * H + h) * D_K);
 #pragma unroll
-        for (int kk = 0; kk < D_H / 16; ++kk) {
+        for (int kk = 0; kk < D_K / 16; ++kk) {
             qa[kk][0] = rA < Tq ? qA[kk * 8 + tq] : 0u;
             qa[kk][1] = rB < Tq ? qB[kk * 8 + tq] : 0u;
             qa[kk][2] = rA < Tq ? qA[kk * 8 + 4 + tq] : 0u;
@@ -90,7 +95,7 @@ __global__ void __launch_bounds__(128) prefill_kernel(const PrefillArgs a) {
     {
         const int row = lane & 15, jh = lane >> 4;
         const int i = i0 + row;
-        const uint16_t* qrow = a.q + (((size_t)b * Tq + min(i, Tq - 1)) * H + h) * D_H;
+        const uint16_t* qrow = a.q + (((size_t)b * Tq + min(i, Tq - 1)) * H + h) * D_K;
         for (int j = jh * (R / 2); j < (jh + 1) * (R / 2); ++j) {
             float acc = 0.f;
             const uint16_t* bk = a.BK + (size_t)h * D_H * R + j;
@@ -115,7 +120,7 @@ __global__ void __launch_bounds__(128) prefill_kernel(const PrefillArgs a) {
         }
     }
 
-    // ---- tile loader: 64 tokens of s^K, s^V (all d_h) and z^K_h, z^V_h (r) for head h
+    // ---- tile loader: 64 tokens of [s^K | k^R], s^V and z^K_h, z^V_h (r) for head h
     auto load_tile = [&](int kt, int buf) {
         const uint32_t st = smem_s + buf * T::kStage;
         int blk = a.block_table[(size_t)b * a.max_pages + kt];
@@ -125,20 +130,28 @@ __global__ void __launch_bounds__(128) prefill_kernel(const PrefillArgs a) {
             if (threadIdx.x == 0) set_status(a.status, LRKV_DEV_BAD_BLOCK);
             blk = 0;
         }
-        constexpr int CS = D_H / 8, CZ = R / 8;
+        constexpr int CK = D_K / 8, CS = D_H / 8, CZ = R / 8;
+        if (D_R > 0) {
+            for (int idx = threadIdx.x; idx < 64 * CK; idx += 128) {
+                const int tok = idx / CK, c = idx % CK;
+                const bool live = ok && (kt * 64 + tok < ctx);
+                cp_async16(st + tok * T::kPitchK + c * 16, a.sK + ((size_t)blk * 64 + tok) * D_K + c * 8, live ? 16 : 0);
+            }
+        }
         for (int idx = threadIdx.x; idx < 64 * CS; idx += 128) {
             const int tok = idx / CS, c = idx % CS;
             const bool live = ok && (kt * 64 + tok < ctx);
             const size_t go = ((size_t)blk * 64 + tok) * D_H + c * 8;
-            cp_async16(st + tok * T::kPitchS + c * 16, a.sK + go, live ? 16 : 0);
-            cp_async16(st + T::kSBytes + tok * T::kPitchS + c * 16, a.sV + go, live ? 16 : 0);
+            if (D_R == 0) cp_async16(st + tok * T::kPitchK + c * 16, a.sK + go, live ? 16 : 0);
+            cp_async16(st + T::kKBytes + tok * T::kPitchS + c * 16, a.sV + go, live ? 16 : 0);
         }
         for (int idx = threadIdx.x; idx < 64 * CZ; idx += 128) {
             const int tok = idx / CZ, c = idx % CZ;
             const bool live = ok && (kt * 64 + tok < ctx);
             const size_t go = (((size_t)blk * 64 + tok) * H + h) * R + c * 8;
-            cp_async16(st + 2 * T::kSBytes + tok * T::kPitchZ + c * 16, a.zK + go, live ? 16 : 0);
-            cp_async16(st + 2 * T::kSBytes + T::kZBytes + tok * T::kPitchZ + c * 16, a.zV + go, live ? 16 : 0);
+            cp_async16(st + T::kKBytes + T::kSBytes + tok * T::kPitchZ + c * 16, a.zK + go, live ? 16 : 0);
+            cp_async16(st + T::kKBytes + T::kSBytes + T::kZBytes + tok * T::kPitchZ + c * 16, a.zV + go,
+                       live ? 16 : 0);
         }
     };
 
@@ -161,8 +174,8 @@ __global__ void __launch_bounds__(128) prefill_kernel(const PrefillArgs a) {
         __syncthreads();
         const int buf = kt & 1;
         const uint32_t sK_s = smem_s + buf * T::kStage;
-        const uint32_t sV_s = sK_s + T::kSBytes;
-        const uint32_t zK_s = sK_s + 2 * T::kSBytes;
+        const uint32_t sV_s = sK_s + T::kKBytes;
+        const uint32_t zK_s = sV_s + T::kSBytes;
         const uint32_t zV_s = zK_s + T::kZBytes;
         const int key0 = kt * 64;
         if (i0 < Tq && key0 <= warp_last_pos) {
@@ -173,9 +186,9 @@ __global__ void __launch_bounds__(128) prefill_kernel(const PrefillArgs a) {
                 s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
                 const int tok = nt * 8 + (lane & 7);
 #pragma unroll
-                for (int kk = 0; kk < D_H / 16; kk += 2) {
+                for (int kk = 0; kk < D_K / 16; kk += 2) {
                     uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(sK_s + tok * T::kPitchS + (kk * 2 + (lane >> 3)) * 16, b0, b1, b2, b3);
+                    ldmatrix_x4(sK_s + tok * T::kPitchK + (kk * 2 + (lane >> 3)) * 16, b0, b1, b2, b3);
                     mma_16816(s[nt], qa[kk], b0, b1);
                     mma_16816(s[nt], qa[kk + 1], b2, b3);
                 }
@@ -300,10 +313,10 @@ __global__ void __launch_bounds__(128) prefill_kernel(const PrefillArgs a) {
     }
 }
 
-template <int D_H, int R>
+template <int D_H, int R, int D_R>
 static cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
-    using T = PrefillTile<D_H, R>;
-    auto kern = prefill_kernel<D_H, R>;
+    using T = PrefillTile<D_H, R, D_R>;
+    auto kern = prefill_kernel<D_H, R, D_R>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.Tq + 63) / 64, a.H, a.B);
@@ -311,9 +324,10 @@ static cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, cudaStream_t stream) {
-#define LRKV_PF(DH, RR) \
-    if (D_H == DH && R == RR) return launch_prefill_t<DH, RR>(a, stream);
+cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, int D_R, cudaStream_t stream) {
+#define LRKV_PF(DH, RR)                                                                                  \
+    if (D_H == DH && R == RR)                                                                            \
+        return D_R == 0 ? launch_prefill_t<DH, RR, 0>(a, stream) : launch_prefill_t<DH, RR, 64>(a, stream);
     LRKV_PF(64, 8) LRKV_PF(64, 16) LRKV_PF(64, 32) LRKV_PF(128, 8) LRKV_PF(128, 16) LRKV_PF(128, 32)
 #undef LRKV_PF
     return cudaErrorInvalidValue;

@@ -28,14 +28,25 @@
  *     synchronising the stream.
  *   - Cache pages: the pools are indexed by physical block id b in
  *     [0, num_blocks); token slot = b * block_size + offset.
- *        sK, sV : [num_blocks][block_size][d_h]
+ *        sK     : [num_blocks][block_size][d_h + d_rope]   rows [s^K | k^R]
+ *        sV     : [num_blocks][block_size][d_h]
  *        zK, zV : [num_blocks][block_size][H][r]
  *     (s = shared features K_s, V_s of Eq. (4); z_h = per-head latents R_h^K,
- *     R_h^V of Eq. (5).)  B_h^K, B_h^V are weights, not cache entries.
+ *     R_h^V of Eq. (5); k^R = the optional decoupled positional key, below.)
+ *     B_h^K, B_h^V are weights, not cache entries.
+ *   - Decoupled positional key (d_rope > 0; "Low-Rank Key Value Attention",
+ *     combination with MLA-style latent caches, whose decoupled rotary key is
+ *     one d_rope-vector per token shared by all heads): every key row carries
+ *     k^R = RoPE(x W^KR, pos) after s^K.  A query is then [q | q^R] (q^R already
+ *     rotated by the caller), logits are q . (s^K + B_h^K z^K_h) + q^R . k^R, and
+ *     the default scale is 1/sqrt(d_h + d_rope).  RoPE turns the pair (2i, 2i+1)
+ *     of a d_rope-vector by the angle pos * rope_base^(-2i / d_rope).  Values
+ *     carry no positional part.  d_rope == 0 is the plain method, bit for bit.
  *
  * Supported shapes (others return LRKV_ERR_UNSUPPORTED):
  *   block_size == 64, d_h in {64, 128}, r in {8, 16, 32, 64} with r <= d_h,
- *   1 <= H <= 128, d a positive multiple of 8 (of 64 for the tensor-core append).
+ *   1 <= H <= 128, d a positive multiple of 8 (of 64 for the tensor-core append),
+ *   d_rope in {0, 64}.
  */
 #ifndef LRKV_H
 #define LRKV_H
@@ -47,7 +58,7 @@
 extern "C" {
 #endif
 
-#define LRKV_ABI_VERSION 1
+#define LRKV_ABI_VERSION 2
 
 typedef enum lrkv_status {
     LRKV_OK = 0,
@@ -73,7 +84,9 @@ typedef struct lrkv_dims {
     int32_t r;           /* residual rank of U_h B_h^T */
     int32_t d;           /* hidden size of the rows appended to the cache */
     int32_t block_size;  /* tokens per cache page; must be 64 */
-    float softmax_scale; /* logit scale; 0 means 1/sqrt(d_h) (frame "Compute logits ...") */
+    float softmax_scale; /* logit scale; 0 means 1/sqrt(d_h + d_rope) (frame "Compute logits ...") */
+    int32_t d_rope;      /* width of the decoupled positional key shared by all heads; 0 = none */
+    float rope_base;     /* RoPE base; 0 means 10000 (ignored when d_rope == 0) */
 } lrkv_dims;
 
 /* One layer's paged cache (device pointers, caller-owned, layout above). */
@@ -94,28 +107,32 @@ const char* lrkv_status_string(lrkv_status s);
 /* Explanation of the last non-OK status returned on the calling thread ("" if none). */
 const char* lrkv_last_error(void);
 
-/* Bytes of one cache page across the four pools: block_size * 2 * 2(d_h + H r).
+/* Bytes of one cache page across the four pools: block_size * 2 * (2(d_h + H r) + d_rope).
  * Returns 0 for unsupported dims. */
 size_t lrkv_cache_block_bytes(const lrkv_dims* dims);
 
 /*
  * lrkv_append -- Eqs. (4)-(5): project n_tok hidden rows into the cache.
- *   Y = X W_cat, W_cat = [W_shared^K | W_shared^V | U_1^K .. U_H^K | U_1^V .. U_H^V]
- *   (d x N, N = 2(d_h + H r)), accumulated in fp32 and rounded to bf16
- *   (nearest, ties to even); row t is written to token slot slot_mapping[t]:
- *   columns [0,d_h) -> sK, [d_h,2d_h) -> sV, the next H r -> zK (head-major),
- *   the last H r -> zV.
+ *   Y = X W_cat, W_cat = [W_shared^K | W^KR | W_shared^V | U_1^K .. U_H^K | U_1^V .. U_H^V]
+ *   (d x N, N = 2(d_h + H r) + d_rope; W^KR absent when d_rope == 0), accumulated
+ *   in fp32; the d_rope columns of W^KR are then rotated at positions[t] (angle,
+ *   sine and cosine in double, result rounded to fp32); everything is rounded to bf16
+ *   (nearest, ties to even).  Row t is written to token slot slot_mapping[t]:
+ *   columns [0, d_h + d_rope) -> sK, the next d_h -> sV, the next H r -> zK
+ *   (head-major), the last H r -> zV.
  *   X            [n_tok][d]
  *   W_catT       [N][d]  (W_cat transposed: row c holds the weights of output column c)
  *   slot_mapping [n_tok] int32 (device); a negative entry skips the row,
  *                an entry >= num_blocks*block_size sets LRKV_DEV_BAD_SLOT and skips it.
+ *   positions    [n_tok] int32 (device) token positions, >= 0; required when
+ *                d_rope > 0, ignored (may be NULL) otherwise.
  *   n_tok == 0 is a no-op.  Small n_tok runs a bandwidth-bound kernel, large n_tok a
  *   tcgen05 tensor-core GEMM; both give bit-identical results whenever every fp32
  *   partial sum is exact.
  */
 lrkv_status lrkv_append(const lrkv_dims* dims, const void* X, const void* W_catT, int32_t n_tok,
-                        const int32_t* slot_mapping, const lrkv_cache* cache, uint32_t* status_dev,
-                        void* stream);
+                        const int32_t* slot_mapping, const int32_t* positions, const lrkv_cache* cache,
+                        uint32_t* status_dev, void* stream);
 
 /* Workspace bytes lrkv_decode needs for `batch` sequences on the CURRENT device. */
 size_t lrkv_decode_workspace_bytes(const lrkv_dims* dims, int32_t batch);
@@ -126,8 +143,9 @@ size_t lrkv_decode_workspace_bytes(const lrkv_dims* dims, int32_t batch);
  *   a_h = softmax_t(score);  out_h = a_h V_s + (a_h R_h^V) (B_h^V)^T.
  *   The query attends to all seq_lens[b] cached tokens (positions 0..L-1; it is
  *   the newest position and is already in the cache).  Split over the sequence
- *   across the GPU's SMs, merged by log-sum-exp in a second kernel.
- *   q           [batch][H][d_h]
+ *   across the GPU's SMs, merged by log-sum-exp in a second kernel.  With a
+ *   positional key the logit gains q^R . k^R_t (see the conventions above).
+ *   q           [batch][H][d_h + d_rope]  ([q_h | q^R_h]; q~ uses the first d_h)
  *   BK, BV      [H][d_h][r]  (B_h^K, B_h^V)
  *   block_table [batch][max_blocks_per_seq] int32 (device)
  *   seq_lens    [batch] int32 (device)
@@ -148,8 +166,9 @@ lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, co
  *   projection with B_h^V folded into W^O.  Per sequence b and head h:
  *     score_t = ([q_h | q~_h] . [s^K_t | z^K_{h,t}]) * scale;  a_h = softmax_t(score)
  *     out_h   = [ sum_t a_t s^V_t  |  sum_t a_t z^V_{h,t} ]        (width d_h + r)
- *   i.e. single-head softmax attention over the concatenated features.
- *   q           [batch][H][d_h]   bf16
+ *   i.e. single-head softmax attention over the concatenated features (with a
+ *   positional key, [q_h | q^R_h | q~_h] . [s^K_t | k^R_t | z^K_{h,t}]).
+ *   q           [batch][H][d_h + d_rope]   bf16
  *   q_tilde     [batch][H][r]     bf16, 16-byte aligned
  *   out         [batch][H][d_h + r] bf16 (nearest, ties to even from fp32)
  *   Everything else (cache, block_table, seq_lens, workspace, status, errors, the

@@ -34,24 +34,26 @@ def weights(seed: int, d: int, d_h: int, H: int, r: int, b_scale: float = 1.0, t
     )
 
 
-def pack_wcat_t(w: Weights) -> np.ndarray:
+def pack_wcat_t(w: Weights, WKR: np.ndarray | None = None) -> np.ndarray:
     """Concatenated projection in the library's layout: W_catT [N, d] (row c = weights of output column c),
-    columns ordered [W_shared^K | W_shared^V | U_1^K .. U_H^K | U_1^V .. U_H^V]."""
+    columns ordered [W_shared^K | W^KR | W_shared^V | U_1^K .. U_H^K | U_1^V .. U_H^V] (W^KR [d, d_rope],
+    the positional-key projection, only when given)."""
     H, d, r = w.UK.shape
-    cols = [w.WsK.T, w.WsV.T,
+    cols = [w.WsK.T] + ([] if WKR is None else [WKR.T]) + [w.WsV.T,
             np.transpose(w.UK, (0, 2, 1)).reshape(H * r, d),
             np.transpose(w.UV, (0, 2, 1)).reshape(H * r, d)]
     return np.ascontiguousarray(np.concatenate(cols, axis=0))
 
 
-def empty_pools(num_blocks: int, H: int, d_h: int, r: int, bs: int = 64, fill: int = 0):
-    return (np.full((num_blocks, bs, d_h), fill, np.uint16), np.full((num_blocks, bs, d_h), fill, np.uint16),
+def empty_pools(num_blocks: int, H: int, d_h: int, r: int, bs: int = 64, fill: int = 0, d_rope: int = 0):
+    return (np.full((num_blocks, bs, d_h + d_rope), fill, np.uint16), np.full((num_blocks, bs, d_h), fill, np.uint16),
             np.full((num_blocks, bs, H, r), fill, np.uint16), np.full((num_blocks, bs, H, r), fill, np.uint16))
 
 
-def random_pools(seed: int, num_blocks: int, H: int, d_h: int, r: int, bs: int = 64):
-    """Cache pools filled with bf16(N(0,1)) -- the distribution of x W with x ~ N(0,1), W ~ N(0, 1/d)."""
-    return (S.gaussian_bf16(seed, "pool_sK", (num_blocks, bs, d_h)),
+def random_pools(seed: int, num_blocks: int, H: int, d_h: int, r: int, bs: int = 64, d_rope: int = 0):
+    """Cache pools filled with bf16(N(0,1)) -- the distribution of x W with x ~ N(0,1), W ~ N(0, 1/d); a
+    rotation keeps that distribution, so the positional key columns (d_rope > 0) are drawn the same way."""
+    return (S.gaussian_bf16(seed, "pool_sK", (num_blocks, bs, d_h + d_rope)),
             S.gaussian_bf16(seed, "pool_sV", (num_blocks, bs, d_h)),
             S.gaussian_bf16(seed, "pool_zK", (num_blocks, bs, H, r)),
             S.gaussian_bf16(seed, "pool_zV", (num_blocks, bs, H, r)))

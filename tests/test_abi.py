@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol():
     for name in _declared():
         assert hasattr(lib, name), name
     assert set(_declared()) <= set(b.EXPORTED) | set(_declared())
-    assert b.abi_version() == 1
+    assert b.abi_version() == 2
 
 
 def test_status_strings():
@@ -43,6 +43,7 @@ def test_cache_block_bytes_matches_accounting():
     from compressed_kv_cache_lrkv_gb300 import accounting as A
     for H, d_h, r in [(8, 64, 8), (8, 64, 16), (128, 128, 16), (32, 128, 32), (32, 128, 16)]:
         assert b.cache_block_bytes(b.make_dims(H, d_h, r, H * d_h)) == A.page_bytes(H, d_h, r)
+        assert b.cache_block_bytes(b.make_dims(H, d_h, r, H * d_h, d_rope=64)) == A.page_bytes(H, d_h, r, d_rope=64)
 
 
 @pytest.mark.parametrize("H,d_h,r,d,bs,why", [
@@ -54,7 +55,7 @@ def test_unsupported_dims_rejected(H, d_h, r, d, bs, why):
     assert b.cache_block_bytes(dims) == 0, why
     lib = b.load()
     c = b.Cache(16, 16, 16, 16, 1)
-    rc = lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, ctypes.byref(c), None, None)
+    rc = lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, None, ctypes.byref(c), None, None)
     assert rc == 2, lib.lrkv_last_error()
 
 
@@ -62,17 +63,17 @@ def test_null_and_misaligned_pointers_rejected():
     lib = b.load()
     dims = b.make_dims(8, 64, 8, 512)
     c = b.Cache(16, 16, 16, 16, 1)
-    assert lib.lrkv_append(ctypes.byref(dims), None, 16, 1, 16, ctypes.byref(c), None, None) == 1
+    assert lib.lrkv_append(ctypes.byref(dims), None, 16, 1, 16, None, ctypes.byref(c), None, None) == 1
     assert b"X is NULL" in lib.lrkv_last_error()
-    assert lib.lrkv_append(ctypes.byref(dims), 24, 16, 1, 16, ctypes.byref(c), None, None) == 1
+    assert lib.lrkv_append(ctypes.byref(dims), 24, 16, 1, 16, None, ctypes.byref(c), None, None) == 1
     assert b"aligned" in lib.lrkv_last_error()
     bad = b.Cache(16, 0, 16, 16, 1)
-    assert lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, ctypes.byref(bad), None, None) == 1
+    assert lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, None, ctypes.byref(bad), None, None) == 1
     bad = b.Cache(16, 16, 16, 16, 0)
-    assert lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, ctypes.byref(bad), None, None) == 1
-    assert lib.lrkv_append(ctypes.byref(dims), 16, 16, -1, 16, ctypes.byref(c), None, None) == 1
+    assert lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, None, ctypes.byref(bad), None, None) == 1
+    assert lib.lrkv_append(ctypes.byref(dims), 16, 16, -1, 16, None, ctypes.byref(c), None, None) == 1
     # zero rows / zero batch are no-ops that succeed without touching the device
-    assert lib.lrkv_append(ctypes.byref(dims), None, None, 0, None, ctypes.byref(c), None, None) == 0
+    assert lib.lrkv_append(ctypes.byref(dims), None, None, 0, None, None, ctypes.byref(c), None, None) == 0
     assert lib.lrkv_decode(ctypes.byref(dims), 16, 16, 16, ctypes.byref(c), 16, 1, 16, 0, 16, 256, 0, None,
                            None) == 0
     assert lib.lrkv_decode(ctypes.byref(dims), 16, 16, 16, ctypes.byref(c), 16, 0, 16, 1, 16, 256, 0, None,
@@ -94,3 +95,25 @@ def test_nan_scale_rejected():
     lib = b.load()
     dims = b.make_dims(8, 64, 8, 512, softmax_scale=float("nan"))
     assert b.cache_block_bytes(dims) == 0
+
+
+@pytest.mark.parametrize("d_rope,base,code", [(32, 0.0, 2), (128, 0.0, 2), (-64, 0.0, 2), (64, float("nan"), 1),
+                                              (64, 1.0, 1), (64, -5.0, 1), (64, float("inf"), 1)])
+def test_positional_key_dims_rejected(d_rope, base, code):
+    """d_rope outside {0, 64} is an unsupported shape; a RoPE base that is NaN, infinite or <= 1 is invalid."""
+    lib = b.load()
+    dims = b.make_dims(8, 64, 8, 512, d_rope=d_rope, rope_base=base)
+    assert b.cache_block_bytes(dims) == 0
+    c = b.Cache(16, 16, 16, 16, 1)
+    assert lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, 16, ctypes.byref(c), None, None) == code
+
+
+def test_positional_key_needs_positions():
+    lib = b.load()
+    dims = b.make_dims(8, 64, 8, 512, d_rope=64)
+    c = b.Cache(16, 16, 16, 16, 1)
+    assert lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, None, ctypes.byref(c), None, None) == 1
+    assert b"positions" in lib.lrkv_last_error()
+    # without a positional key the positions pointer is ignored
+    plain = b.make_dims(8, 64, 8, 512)
+    assert lib.lrkv_append(ctypes.byref(plain), None, None, 0, None, None, ctypes.byref(c), None, None) == 0
