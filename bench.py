@@ -18,10 +18,11 @@ Other workloads (--workload): "dsv2" (H=128, d_h=128, r=16, d=16384, batch 8,
 r=16, batch 2, 4096-token prompts in 512-token chunks), value in prompt
 tokens/s with the tensor roofline of the prefill kernel.  --fused runs a decode
 workload through lrkv_decode_fused (both absorptions in the caller's weights:
-q~ given, [o_s | o_z] returned), counting that form's own bytes.
+q~ given, [o_s | o_z] returned), counting that form's own bytes.  --rope adds the
+64-wide decoupled positional key (key rows [s^K | k^R], rotated in the append).
 
 Prints one JSON line.
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lrkv|reference] [--workload NAME] [--fused]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lrkv|reference] [--workload NAME] [--fused] [--rope]
 """
 from __future__ import annotations
 
@@ -171,11 +172,12 @@ class DecodeHarness:
     profile = "decode_split_longctx.md"
     sources = ("decode.cu", "lrkv_internal.cuh", "kernels.h")
 
-    def __init__(self, wl, rank, fused=False):
+    def __init__(self, wl, rank, fused=False, d_rope=0):
         import torch
 
         from compressed_kv_cache_lrkv_gb300 import binding as b
-        self.torch, self.b, self.wl, self.fused = torch, b, wl, fused
+        self.torch, self.b, self.wl, self.fused, self.d_rope = torch, b, wl, fused, d_rope
+        dr = d_rope
         B, H, d_h, r, d = wl.B, wl.H, wl.d_h, wl.r, wl.d
         self.seq_lens = workload_seq_lens(wl)
         self.pt = S.page_table(wl.seed, self.seq_lens, 64)
@@ -183,24 +185,25 @@ class DecodeHarness:
         gen = torch.Generator(device="cuda").manual_seed(replica_seed(rank, 1234))
         rn = lambda *s, scale=1.0: (torch.randn(*s, generator=gen, device="cuda") * scale).to(torch.bfloat16)
         i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
-        self.dims = b.make_dims(H, d_h, r, d)
+        self.dims = b.make_dims(H, d_h, r, d, d_rope=dr)
         self.layers = []
         for _ in range(wl.layers):
             self.layers.append(dict(
-                cache=b.PagedCache(rn(nb, 64, d_h), rn(nb, 64, d_h), rn(nb, 64, H, r), rn(nb, 64, H, r)),
-                q=rn(B, H, d_h), BK=rn(H, d_h, r, scale=r ** -0.5), BV=rn(H, d_h, r, scale=r ** -0.5),
-                wcat=rn(2 * (d_h + H * r), d, scale=d ** -0.5), x=rn(B, d),
+                cache=b.PagedCache(rn(nb, 64, d_h + dr), rn(nb, 64, d_h), rn(nb, 64, H, r), rn(nb, 64, H, r)),
+                q=rn(B, H, d_h + dr), BK=rn(H, d_h, r, scale=r ** -0.5), BV=rn(H, d_h, r, scale=r ** -0.5),
+                wcat=rn(2 * (d_h + H * r) + dr, d, scale=d ** -0.5), x=rn(B, d),
                 qt=rn(B, H, r) if fused else None,
                 out=torch.empty(B, H, d_h + (r if fused else 0), dtype=torch.bfloat16, device="cuda")))
         self.bt = i32(self.pt.block_table)
         self.sl = i32(self.pt.seq_lens)
         self.slots = i32([self.pt.slot(i, int(L) - 1) for i, L in enumerate(self.seq_lens)])
+        self.positions = i32(self.seq_lens - 1) if dr else None  # the newest token's position
         self.ws = b.alloc_workspace(b.decode_workspace_bytes(self.dims, B))
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.cache_bytes = wl.layers * sum(t.numel() * t.element_size() for t in self.layers[0]["cache"].tensors())
         acct = A.decode_fused_algorithmic_bytes if fused else A.decode_algorithmic_bytes
-        dec = acct(H, d_h, r, self.seq_lens, layers=wl.layers)
-        app = wl.layers * A.append_algorithmic_bytes(B, d, H, d_h, r)
+        dec = acct(H, d_h, r, self.seq_lens, layers=wl.layers, d_rope=dr)
+        app = wl.layers * A.append_algorithmic_bytes(B, d, H, d_h, r, d_rope=dr)
         self.kernel_units = dec          # algorithmic bytes of the timed kernel calls
         self.step_units = dec + app      # algorithmic bytes of a step
         self.launches_per_step = wl.layers * (3 if fused else 4)
@@ -216,7 +219,8 @@ class DecodeHarness:
     def step(self, stream):
         b = self.b
         for L in self.layers:
-            b.lrkv_append(self.dims, L["x"], L["wcat"], self.slots, L["cache"], status=self.status, stream=stream)
+            b.lrkv_append(self.dims, L["x"], L["wcat"], self.slots, L["cache"], status=self.status, stream=stream,
+                          positions=self.positions)
             self._decode(L, stream)
 
     def kernel(self, stream):
@@ -227,7 +231,8 @@ class DecodeHarness:
         t = self.torch
         self.h_in = [(L["x"].cpu().pin_memory(), L["x"]) for L in self.layers] + \
                     [(L[k].cpu().pin_memory(), L[k]) for L in self.layers for k in ("q", "qt") if L[k] is not None] + \
-                    [(self.slots.cpu().pin_memory(), self.slots), (self.sl.cpu().pin_memory(), self.sl)]
+                    [(self.slots.cpu().pin_memory(), self.slots), (self.sl.cpu().pin_memory(), self.sl)] + \
+                    ([(self.positions.cpu().pin_memory(), self.positions)] if self.d_rope else [])
         self.h_out = [(t.empty_like(L["out"], device="cpu").pin_memory(), L["out"]) for L in self.layers]
         return (sum(h.numel() * h.element_size() for h, _ in self.h_in),
                 sum(h.numel() * h.element_size() for h, _ in self.h_out))
@@ -249,12 +254,14 @@ class DecodeHarness:
             "tokens_per_s": wl.B * world / step_s, "pct_of_hbm_peak": 100.0 * value / peaks["hbm_gbs"],
             "config": {"workload": f"{wl.key}: {wl.description}", "B": wl.B,
                        "seq_lens": [int(x) for x in self.seq_lens], "layers": wl.layers, "H": wl.H, "d_h": wl.d_h,
-                       "r": wl.r, "d": wl.d, "block_size": 64, "pages_per_layer": int(self.pt.num_blocks),
+                       "r": wl.r, "d": wl.d, "d_rope": self.d_rope, "block_size": 64,
+                       "pages_per_layer": int(self.pt.num_blocks),
                        "cache_bytes": int(self.cache_bytes),
                        "l2": (f"inputs larger than L2: cache {self.cache_bytes / 2**20:.0f} MiB vs L2 "
                               f"{L2_BYTES / 2**20:.0f} MiB") if self.cache_bytes > L2_BYTES else
                              "cache fits in L2 (parity-sized workload; not an HBM measurement)",
-                       "step": "per layer: lrkv_append (1 row per sequence) + " +
+                       "step": "per layer: lrkv_append (1 row per sequence" +
+                               (", positional key rotated at its position) + " if self.d_rope else ") + ") +
                                ("lrkv_decode_fused (q~ given, [o_s | o_z] returned)" if self.fused else "lrkv_decode"),
                        "parallelism": f"replicas x{world} (independent batches)"},
             "roofline": {"kernel": "lrkv_decode_fused (split + combine kernels)" if self.fused else
@@ -262,7 +269,7 @@ class DecodeHarness:
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
                          "traffic": recorded_traffic(self.profile, self.sources)
-                                    if wl.key == "longctx" and not self.fused else None,
+                                    if wl.key == "longctx" and not self.fused and not self.d_rope else None,
                          "algorithmic_bytes_per_launch": self.kernel_units // wl.layers,
                          "avg_launch_ms": kernel_s * 1e3 / wl.layers},
             "e2e_unit_value": lambda s: self.step_units * world / s / 1e9, "e2e_unit": "GB/s",
@@ -274,13 +281,14 @@ class DecodeHarness:
         wl = self.wl
         o = oracle.get()
         tokens = int(self.seq_lens[0])
+        dr = self.d_rope
         pt = S.page_table(wl.seed, [tokens], 64)
         pools = tuple(S.gaussian_bf16(wl.seed, n, shp) for n, shp in
-                      [("bl_sK", (pt.num_blocks, 64, wl.d_h)), ("bl_sV", (pt.num_blocks, 64, wl.d_h)),
+                      [("bl_sK", (pt.num_blocks, 64, wl.d_h + dr)), ("bl_sV", (pt.num_blocks, 64, wl.d_h)),
                        ("bl_zK", (pt.num_blocks, 64, wl.H, wl.r)), ("bl_zV", (pt.num_blocks, 64, wl.H, wl.r))])
         BK = S.gaussian_bf16(wl.seed, "bl_BK", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
         BV = S.gaussian_bf16(wl.seed, "bl_BV", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
-        q = S.gaussian_bf16(wl.seed, "bl_q", (1, wl.H, wl.d_h))
+        q = S.gaussian_bf16(wl.seed, "bl_q", (1, wl.H, wl.d_h + dr))
         qt = S.gaussian_bf16(wl.seed, "bl_qt", (1, wl.H, wl.r))
         reps, t0 = 0, time.perf_counter()
         while True:
@@ -293,7 +301,7 @@ class DecodeHarness:
             if dt >= budget_s:
                 break
         acct = A.decode_fused_algorithmic_bytes if self.fused else A.decode_algorithmic_bytes
-        nbytes = acct(wl.H, wl.d_h, wl.r, [tokens]) * reps
+        nbytes = acct(wl.H, wl.d_h, wl.r, [tokens], d_rope=dr) * reps
         what = "absorbed-weights decode" if self.fused else "E2 decode"
         return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
                 "sample": f"{what} of the workload's first sequence ({tokens} cached tokens, all {wl.H} heads, "
@@ -442,9 +450,12 @@ def run_gpu(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     wl = S.WORKLOADS[args.workload]
-    if args.fused and HARNESS[args.workload] is not DecodeHarness:
-        raise SystemExit("--fused applies to the decode workloads")
-    hz = DecodeHarness(wl, rank, fused=True) if args.fused else HARNESS[args.workload](wl, rank)
+    if (args.fused or args.rope) and HARNESS[args.workload] is not DecodeHarness:
+        raise SystemExit("--fused and --rope apply to the decode workloads")
+    if args.fused or args.rope:
+        hz = DecodeHarness(wl, rank, fused=args.fused, d_rope=64 if args.rope else 0)
+    else:
+        hz = HARNESS[args.workload](wl, rank)
     stream = torch.cuda.current_stream()
 
     # Each timed step is one replay of a CUDA graph of the public calls, so host
@@ -599,6 +610,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused", action="store_true",
                     help="decode with absorbed weights (lrkv_decode_fused: q~ given, [o_s | o_z] returned)")
+    ap.add_argument("--rope", action="store_true",
+                    help="decode with a 64-wide decoupled positional key shared by all heads (d_rope = 64)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

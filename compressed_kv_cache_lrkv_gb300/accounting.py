@@ -59,22 +59,25 @@ def page_bytes(H: int, d_h: int, r: int, block_size: int = 64, d_rope: int = 0) 
     return block_size * lrkv_cache_elements(H, d_h, r, d_rope) * BF16_BYTES
 
 
-def decode_algorithmic_bytes(H: int, d_h: int, r: int, seq_lens: Iterable[int], layers: int = 1) -> int:
+def decode_algorithmic_bytes(H: int, d_h: int, r: int, seq_lens: Iterable[int], layers: int = 1,
+                             d_rope: int = 0) -> int:
     """Bytes one decode step must move: every cached token's compressed row, the
-    two factor tensors B^K, B^V, the query in and the output out (all bf16)."""
+    two factor tensors B^K, B^V, the query [q | q^R] in and the output out (all bf16)."""
     seq_lens = list(int(x) for x in seq_lens)
     B = len(seq_lens)
-    per_layer = (sum(seq_lens) * lrkv_cache_elements(H, d_h, r) * BF16_BYTES
-                 + 2 * H * d_h * r * BF16_BYTES + 2 * B * H * d_h * BF16_BYTES)
+    per_layer = (sum(seq_lens) * lrkv_cache_elements(H, d_h, r, d_rope) * BF16_BYTES
+                 + 2 * H * d_h * r * BF16_BYTES + B * H * (2 * d_h + d_rope) * BF16_BYTES)
     return per_layer * layers
 
 
-def decode_fused_algorithmic_bytes(H: int, d_h: int, r: int, seq_lens: Iterable[int], layers: int = 1) -> int:
+def decode_fused_algorithmic_bytes(H: int, d_h: int, r: int, seq_lens: Iterable[int], layers: int = 1,
+                                   d_rope: int = 0) -> int:
     """Bytes of one decode step with both absorptions in the caller's weights: every cached
-    token's compressed row, the query [q | q~] in and [o_s | o_z] out (all bf16)."""
+    token's compressed row, the query [q | q^R | q~] in and [o_s | o_z] out (all bf16)."""
     seq_lens = list(int(x) for x in seq_lens)
     B = len(seq_lens)
-    per_layer = sum(seq_lens) * lrkv_cache_elements(H, d_h, r) * BF16_BYTES + 2 * B * H * (d_h + r) * BF16_BYTES
+    per_layer = (sum(seq_lens) * lrkv_cache_elements(H, d_h, r, d_rope) * BF16_BYTES
+                 + B * H * (2 * (d_h + r) + d_rope) * BF16_BYTES)
     return per_layer * layers
 
 
@@ -90,9 +93,9 @@ def append_flops(n_tok: int, d: int, H: int, d_h: int, r: int) -> int:
     return 2 * n_tok * d * lrkv_cache_elements(H, d_h, r)
 
 
-def append_algorithmic_bytes(n_tok: int, d: int, H: int, d_h: int, r: int) -> int:
+def append_algorithmic_bytes(n_tok: int, d: int, H: int, d_h: int, r: int, d_rope: int = 0) -> int:
     """X in, W_cat in, cache rows out (bf16)."""
-    N = lrkv_cache_elements(H, d_h, r)
+    N = lrkv_cache_elements(H, d_h, r, d_rope)
     return BF16_BYTES * (n_tok * d + d * N + n_tok * N)
 
 

@@ -53,6 +53,28 @@ __device__ __forceinline__ float dot8(const uint4& w, const uint4& x) {
     return acc;
 }
 
+// Partial dot products of this thread's chunks of NCOL weight rows (w0, and w1 when NCOL == 2)
+// with the block's NT hidden rows.
+template <int NT, int NCOL>
+__device__ __forceinline__ void rowwise_partials(const AppendArgs& a, const uint16_t* w0, const uint16_t* w1, int t0,
+                                                 float (&acc)[2][NT]) {
+    const int nchunk = a.d >> 3;
+#pragma unroll 4
+    for (int k8 = threadIdx.x; k8 < nchunk; k8 += 128) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(w0) + k8);
+        uint4 w1v = make_uint4(0, 0, 0, 0);
+        if (NCOL == 2) w1v = __ldg(reinterpret_cast<const uint4*>(w1) + k8);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t0 + t < a.n) {
+                const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + t) * a.d) + k8);
+                acc[0][t] += dot8(w, x);
+                if (NCOL == 2) acc[1][t] += dot8(w1v, x);
+            }
+        }
+    }
+}
+
 // One 128-thread CTA per output column c and block of NT token rows: lane i of
 // the CTA reads the 16-byte chunks i, i + 128, ... of weight row c (W_cat^T is
 // contiguous along d), so the whole weight matrix is in flight in about one
@@ -61,35 +83,24 @@ __device__ __forceinline__ float dot8(const uint4& w, const uint4& x) {
 // the four warps in shared memory, always in the same order.  In the range of the
 // shared positional key a CTA computes the two columns of one rotation pair and turns
 // them at each row's position before rounding.
-template <int NT>
+template <int NT, bool ROPE>
 __global__ void __launch_bounds__(128) append_rowwise_kernel(const AppendArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int u = blockIdx.x, half = a.d_rope / 2;
-    const bool pair = a.d_rope > 0 && u >= a.d_h && u < a.d_h + half;
-    const int c = (a.d_rope > 0 && u >= a.d_h) ? (pair ? a.d_h + 2 * (u - a.d_h) : u + half) : u;
+    const int u = blockIdx.x, half = ROPE ? a.d_rope / 2 : 0;
+    const bool pair = ROPE && u >= a.d_h && u < a.d_h + half;  // uniform over the CTA
+    const int c = (ROPE && u >= a.d_h) ? (pair ? a.d_h + 2 * (u - a.d_h) : u + half) : u;
     const int t0 = blockIdx.y * NT;
-    __shared__ float red[2][4][NT];
+    __shared__ float red[ROPE ? 2 : 1][4][NT];
     float acc[2][NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[0][t] = acc[1][t] = 0.f;
     const uint16_t* wrow = a.W + (size_t)c * a.d;
-    const uint16_t* wrow1 = a.W + (size_t)(pair ? c + 1 : c) * a.d;
-    const int nchunk = a.d >> 3;
-#pragma unroll 4
-    for (int k8 = threadIdx.x; k8 < nchunk; k8 += 128) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(wrow) + k8);
-        const uint4 w1 = pair ? __ldg(reinterpret_cast<const uint4*>(wrow1) + k8) : make_uint4(0, 0, 0, 0);
+    if (ROPE && pair)
+        rowwise_partials<NT, 2>(a, wrow, wrow + a.d, t0, acc);
+    else
+        rowwise_partials<NT, 1>(a, wrow, wrow, t0, acc);
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            if (t0 + t < a.n) {
-                const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + t) * a.d) + k8);
-                acc[0][t] += dot8(w, x);
-                if (pair) acc[1][t] += dot8(w1, x);
-            }
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
+    for (int j = 0; j < (ROPE ? 2 : 1); ++j)
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             float v = acc[j][t];
@@ -103,8 +114,9 @@ __global__ void __launch_bounds__(128) append_rowwise_kernel(const AppendArgs a)
         float v0 = (red[0][0][t] + red[0][1][t]) + (red[0][2][t] + red[0][3][t]);
         const long long slot = checked_slot(a, t0 + t);
         if (slot >= 0) {
-            if (pair) {
-                float v1 = (red[1][0][t] + red[1][1][t]) + (red[1][2][t] + red[1][3][t]);
+            if (ROPE && pair) {
+                float v1 = (red[ROPE ? 1 : 0][0][t] + red[ROPE ? 1 : 0][1][t]) +
+                           (red[ROPE ? 1 : 0][2][t] + red[ROPE ? 1 : 0][3][t]);
                 rope_pair(v0, v1, u - a.d_h, a.d_rope, a.positions[t0 + t], a.rope_base);
                 store_cache_value(a, slot, c + 1, v1);
             }
@@ -117,7 +129,10 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
 #define LRKV_ROW(NTV)                                                                    \
     {                                                                                    \
         dim3 grid(a.N - a.d_rope / 2, (a.n + NTV - 1) / NTV); /* pairs: one CTA each */ \
-        append_rowwise_kernel<NTV><<<grid, 128, 0, stream>>>(a);                         \
+        if (a.d_rope > 0)                                                                \
+            append_rowwise_kernel<NTV, true><<<grid, 128, 0, stream>>>(a);               \
+        else                                                                             \
+            append_rowwise_kernel<NTV, false><<<grid, 128, 0, stream>>>(a);              \
         return cudaGetLastError();                                                       \
     }
     if (a.n <= 1) LRKV_ROW(1)

@@ -49,7 +49,7 @@ __device__ __forceinline__ void store8(const AppendArgs& a, long long slot, int 
 
 }  // namespace
 
-template <int BN>
+template <int BN, bool ROPE>
 __global__ void __launch_bounds__(192, 1)
     append_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const AppendArgs a) {
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(192, 1)
                 tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
                 // Columns of the shared positional key (a 32-aligned range [d_h, d_h + d_rope))
                 // are rotated at the row's position before rounding.
-                if (slot >= 0 && n0 + c0 >= a.d_h && n0 + c0 < a.d_h + a.d_rope) {
+                if (ROPE && slot >= 0 && n0 + c0 >= a.d_h && n0 + c0 < a.d_h + a.d_rope) {
                     const int pos = a.positions[row];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -174,11 +174,11 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-template <int BN>
+template <int BN, bool ROPE>
 static cudaError_t launch_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const AppendArgs& a,
                              cudaStream_t stream) {
     constexpr int smem = kStages * (kBM * kBK * 2 + BN * kBK * 2) + 2 * kStages * 8 + 8 + 8 + 1024;
-    auto kern = append_tc_kernel<BN>;
+    auto kern = append_tc_kernel<BN, ROPE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.N + BN - 1) / BN, (a.n + kBM - 1) / kBM);
@@ -190,7 +190,12 @@ int append_tc_block_n(int N) { return (N % 256 == 0) ? 256 : 128; }
 
 cudaError_t launch_append_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const AppendArgs& a,
                              cudaStream_t stream) {
-    return append_tc_block_n(a.N) == 256 ? launch_tc<256>(tmX, tmW, a, stream) : launch_tc<128>(tmX, tmW, a, stream);
+    // the positional-key rotation is compiled only into the kernels that need it
+    if (a.d_rope > 0)
+        return append_tc_block_n(a.N) == 256 ? launch_tc<256, true>(tmX, tmW, a, stream)
+                                             : launch_tc<128, true>(tmX, tmW, a, stream);
+    return append_tc_block_n(a.N) == 256 ? launch_tc<256, false>(tmX, tmW, a, stream)
+                                         : launch_tc<128, false>(tmX, tmW, a, stream);
 }
 
 }  // namespace lrkv

@@ -29,15 +29,18 @@ from gpu_util import assert_close, host_bits, host_f64
 pytestmark = pytest.mark.gpu
 
 
-def _unpack_wcat(wcat_t, d_h, H, r):
-    """W_cat^T [N, d] (library layout) -> W_shared^K, W_shared^V [d, d_h] and U^K, U^V [H, d, r]."""
+def _unpack_wcat(wcat_t, d_h, H, r, d_rope=0):
+    """W_cat^T [N, d] (library layout) -> W_shared^K, W_shared^V [d, d_h], U^K, U^V [H, d, r] and the
+    positional-key projection W^KR [d, d_rope] (None without one)."""
     d = wcat_t.shape[1]
-    z0 = 2 * d_h
+    v0 = d_h + d_rope
+    z0 = v0 + d_h
     WsK = np.ascontiguousarray(wcat_t[:d_h].T)
-    WsV = np.ascontiguousarray(wcat_t[d_h:z0].T)
+    WKR = np.ascontiguousarray(wcat_t[d_h:v0].T) if d_rope else None
+    WsV = np.ascontiguousarray(wcat_t[v0:z0].T)
     UK = np.ascontiguousarray(wcat_t[z0:z0 + H * r].reshape(H, r, d).transpose(0, 2, 1))
     UV = np.ascontiguousarray(wcat_t[z0 + H * r:z0 + 2 * H * r].reshape(H, r, d).transpose(0, 2, 1))
-    return WsK, WsV, UK, UV
+    return WsK, WsV, UK, UV, WKR
 
 
 def _heads(H, n):
@@ -62,10 +65,11 @@ def _run_step(hz):
     assert int(hz.status.item()) == 0
 
 
-@pytest.mark.parametrize("key", ["small", "backbone12", "dsv2", "longctx"])
-def test_decode_workload_full_size(key, oracle_lib):
+@pytest.mark.parametrize("key,d_rope", [("small", 0), ("backbone12", 0), ("dsv2", 0), ("longctx", 0), ("dsv2", 64),
+                                        ("longctx", 64)])
+def test_decode_workload_full_size(key, d_rope, oracle_lib):
     wl = S.WORKLOADS[key]
-    hz = bench.DecodeHarness(wl, 0)
+    hz = bench.DecodeHarness(wl, 0, d_rope=d_rope)
     heads = _heads(wl.H, 8)
     layers = sorted({0, wl.layers // 2, wl.layers - 1})
     seqs = sorted({0, wl.B // 2, wl.B - 1})
@@ -80,12 +84,13 @@ def test_decode_workload_full_size(key, oracle_lib):
     got, ref = [], []
     for li in layers:
         L = hz.layers[li]
-        WsK, WsV, UK, UV = _unpack_wcat(host_bits(L["wcat"]), wl.d_h, wl.H, wl.r)
+        WsK, WsV, UK, UV, WKR = _unpack_wcat(host_bits(L["wcat"]), wl.d_h, wl.H, wl.r, d_rope)
         X, q = host_bits(L["x"]), host_bits(L["q"])
         BK, BV = host_bits(L["BK"])[heads], host_bits(L["BV"])[heads]
         out = host_f64(L["out"])
         # the step appended each sequence's newest token (position seq_len - 1) before decoding
-        newest = oracle_lib.append(X[seqs], WsK, WsV, UK[heads], UV[heads])
+        pos = (hz.seq_lens[seqs] - 1).astype(np.int32)
+        newest = oracle_lib.append(X[seqs], WsK, WsV, UK[heads], UV[heads], WKR=WKR, positions=pos)
         for k, b in enumerate(seqs):
             n = int(hz.seq_lens[b])
             pools = pages[li, b]
@@ -105,7 +110,7 @@ def test_prefill_workload_full_size(oracle_lib):
 
     heads = _heads(wl.H, 4)
     C, T = wl.chunk, wl.L
-    WsK, WsV, UK, UV = _unpack_wcat(host_bits(hz.wcat), wl.d_h, wl.H, wl.r)
+    WsK, WsV, UK, UV, _ = _unpack_wcat(host_bits(hz.wcat), wl.d_h, wl.H, wl.r)
     BK, BV = host_bits(hz.BK)[heads], host_bits(hz.BV)[heads]
     xs = [host_bits(ch["x"]) for ch in hz.chunks]
     got, ref = [], []
