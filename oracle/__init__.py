@@ -14,7 +14,9 @@ Pins: every function here is pinned in ``tests/test_oracle_pins.py`` against
 facts the pages or mathematics fix (softmax worked value, r=0 -> MQA,
 W_shared=0 & B_h=permutation -> MHA through a library attention routine,
 L=1 and equal-key special cases, head-permutation equivariance, integer-exact
-append, causal-mask special cases).  Planted-mistake builds
+append, causal-mask special cases, the positional key's rotation against the pages'
+worked 90-degree example, absorbed MLA against library multi-query attention and
+against its expanded form).  Planted-mistake builds
 (``LRKV_ORACLE_MUTANT``) check that those pins catch a dropped term, a wrong
 factor, a transposed factor, a wrong scale and an off-by-one causal mask.
 """
@@ -113,6 +115,11 @@ class Oracle:
         L.oracle_prefill_cache.argtypes = ([_c_int] * 7 + [_u16p] * 4 + [_i32p, _c_int, _i32p] +
                                            [_u16p] * 3 + [_c_double, _u8p_or_null, _f64p])
         L.oracle_prefill_cache.restype = _c_int
+        L.oracle_mla_decode.argtypes = ([_c_int] * 7 + [_u16p, _i32p, _c_int, _i32p, _u16p] +
+                                        [_c_double, _u8p_or_null, _f64p])
+        L.oracle_mla_decode.restype = _c_int
+        L.oracle_mla_decode_expanded.argtypes = ([_c_int] * 6 + [_i32p] + [_u16p] * 5 + [_c_double, _f64p])
+        L.oracle_mla_decode_expanded.restype = _c_int
 
     # -- small pieces ---------------------------------------------------------
     def num_threads(self) -> int:
@@ -207,6 +214,48 @@ class Oracle:
                                                _i32(seq_lens), _u16(q), _u16(q_tilde), float(scale), wp, out)
         if rc != 0:
             raise ValueError("oracle_decode_fused: bad block id or length")
+        return out
+
+    # -- MLA (absorbed and expanded) ----------------------------------------------
+    def mla_append(self, X, WDKV, WKR, positions, rope_base=10000.0):
+        """MLA cache rows [c | k^R] for X [n, d]: c = X W^DKV (d_c), k^R = RoPE(X W^KR, pos) (d_rope),
+        each an fp64 sum rounded to fp32 then bf16.  Returns [n, d_c + d_rope] bf16 bits."""
+        X = _u16(X)
+        n, d = X.shape
+        d_c, d_rope = WDKV.shape[1], WKR.shape[1]
+        z1 = np.zeros((1, d, 0), np.uint16)
+        sK, _, _, _ = self.append(X, WDKV, np.zeros((d, d_c), np.uint16), z1, z1, WKR=WKR, positions=positions,
+                                  rope_base=rope_base)
+        return sK
+
+    def mla_decode(self, kv, block_table, seq_lens, q, d_rope, d_head, scale=0.0, want=None, bs=64):
+        """Absorbed MLA decode: kv [nb, bs, d_c + d_rope] (rows [c | k^R]), q [B, H, d_c + d_rope]
+        ([q~ | q^R]) -> o [B, H, d_c] = sum_t p_t c_t; scale 1/sqrt(d_head + d_rope) by default."""
+        kv = _u16(kv)
+        B, H, dk = q.shape
+        d_c = dk - d_rope
+        bt = _i32(block_table)
+        out = np.zeros((B, H, d_c), np.float64)
+        w, wp = _want_ptr(want, B, H)
+        rc = self.lib.oracle_mla_decode(B, H, d_c, d_rope, d_head, bs, kv.shape[0], kv, bt, bt.shape[1],
+                                        _i32(seq_lens), _u16(q), float(scale), wp, out)
+        if rc != 0:
+            raise ValueError("oracle_mla_decode: bad block id or length")
+        return out
+
+    def mla_decode_expanded(self, rows, ctx_len, qC, qR, WUK, WUV, scale=0.0):
+        """MLA decode with per-head keys [c W^UK_h | k^R] and values c W^UV_h formed explicitly:
+        rows [B, Lmax, d_c + d_rope], qC [B, H, d_head], qR [B, H, d_rope], WUK, WUV [H, d_c, d_head]
+        -> [B, H, d_head]."""
+        rows = _u16(rows)
+        B, Lmax, dk = rows.shape
+        H, d_c, d_head = WUK.shape
+        d_rope = dk - d_c
+        out = np.zeros((B, H, d_head), np.float64)
+        rc = self.lib.oracle_mla_decode_expanded(B, H, d_c, d_rope, d_head, Lmax, _i32(ctx_len), rows, _u16(qC),
+                                                 _u16(qR), _u16(WUK), _u16(WUV), float(scale), out)
+        if rc != 0:
+            raise ValueError("oracle_mla_decode_expanded: bad argument")
         return out
 
     # -- prefill ----------------------------------------------------------------

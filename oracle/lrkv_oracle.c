@@ -37,6 +37,12 @@
  *   - cache values are produced by an fp64 sum, rounded to fp32 (nearest) and
  *     then to bf16 (nearest, ties to even).
  *
+ * Second workload: multi-head latent attention ("Embeddings II: MLA & Architectural
+ * Choices", weight absorption and decoupled RoPE), absorbed (attention over the cached
+ * rows [c_t | k^R_t], values c_t) and expanded (per-head keys and values reconstructed
+ * through W^UK, W^UV) -- the associativity of the LRKV slides' backup frame "MLA also
+ * admits associative computation".
+ *
  * Everything is fp64; bf16 inputs are widened exactly.  Parallelism is plain
  * OpenMP over independent (sequence, head) pairs or token rows; no blocking,
  * fusion or reordering of any sum.
@@ -545,4 +551,112 @@ int oracle_prefill_cache(int B, int Tq, int H, int d_h, int r, int bs, int num_b
                          const uint16_t* q, double scale, const uint8_t* want, double* out) {
     return oracle_prefill_cache_rope(B, Tq, H, d_h, r, 0, bs, num_blocks, sK, sV, zK, zV, block_table, max_pages,
                                      q_start, BK, BV, q, scale, want, out);
+}
+
+/* ---------------------------------------------------------------- MLA, absorbed and expanded */
+/*
+ * Multi-head latent attention as the MLA lesson ("Embeddings II: MLA & Architectural
+ * Choices") builds it, in the associative form of the LRKV slides' backup frame "MLA
+ * also admits associative computation": per token the cache holds the latent
+ * c_t = x_t W^DKV (width d_c) and the decoupled positional key k^R_t (width d_rope, shared
+ * by all heads, rotated at the token's position), stored as one row [c_t | k^R_t].
+ * Head i's key and value are k_{i,t} = [c_t W^UK_i | k^R_t] and v_{i,t} = c_t W^UV_i
+ * (W^UK_i, W^UV_i: d_c x d_head), its query [q^C_i | q^R_i], and the logit scale
+ * 1/sqrt(d_head + d_rope) -- the width of the vectors actually dotted (section
+ * "the softmax denominator changes too").
+ */
+
+/* Absorbed: W^UK_i folded into the query (q~_i = q^C_i (W^UK_i)^T, width d_c) and W^UV_i into
+ * the output projection, so head i attends with [q~_i | q^R_i] against the cache rows and
+ * returns o_i = sum_t p_t c_t (width d_c), before W^UV_i.
+ *   kv [num_blocks][bs][d_c + d_rope], q [B][H][d_c + d_rope], out [B][H][d_c]. */
+int oracle_mla_decode(int B, int H, int d_c, int d_rope, int d_head, int bs, int num_blocks, const uint16_t* kv,
+                      const int32_t* block_table, int max_pages, const int32_t* seq_lens, const uint16_t* q,
+                      double scale, const uint8_t* want, double* out) {
+    for (int b = 0; b < B; ++b) {
+        if (seq_lens[b] < 0 || seq_lens[b] > max_pages * bs) return -1;
+        for (int p = 0; p < (seq_lens[b] + bs - 1) / bs; ++p) {
+            int32_t blk = block_table[(size_t)b * max_pages + p];
+            if (blk < 0 || blk >= num_blocks) return -1;
+        }
+    }
+    const int dk = d_c + d_rope;
+#if LRKV_ORACLE_MUTANT == 10
+    scale = default_scale(scale, dk); /* planted: scale over the cached row's width */
+#else
+    scale = default_scale(scale, d_head + d_rope);
+#endif
+    int bad = 0;
+    #pragma omp parallel for schedule(dynamic)
+    for (int b = 0; b < B; ++b) {
+        int L = seq_lens[b];
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * dk);
+        double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_c);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)dk);
+        if (!K || !V || !qd) {
+            #pragma omp atomic write
+            bad = 1;
+        } else {
+            for (int t = 0; t < L; ++t) {
+                int64_t slot = (int64_t)block_table[(size_t)b * max_pages + t / bs] * bs + t % bs;
+                for (int i = 0; i < dk; ++i) K[(size_t)t * dk + i] = bf(kv[slot * dk + i]);
+#if LRKV_ORACLE_MUTANT == 11
+                for (int i = 0; i < d_c; ++i) V[(size_t)t * d_c + i] = bf(kv[slot * dk + d_rope + i]); /* planted */
+#else
+                for (int i = 0; i < d_c; ++i) V[(size_t)t * d_c + i] = bf(kv[slot * dk + i]);
+#endif
+            }
+            for (int h = 0; h < H; ++h) {
+                if (want && !want[(size_t)b * H + h]) continue;
+                for (int i = 0; i < dk; ++i) qd[i] = bf(q[((size_t)b * H + h) * dk + i]);
+                attend_kv(L, dk, d_c, qd, K, V, scale, out + ((size_t)b * H + h) * d_c);
+            }
+        }
+        free(K); free(V); free(qd);
+    }
+    return bad ? -1 : 0;
+}
+
+/* Expanded ("reconstruct, then attend"): per head the full keys and values are formed from
+ * the cached rows and the up-projections, then textbook attention.
+ *   rows [B][Lmax][d_c + d_rope], qC [B][H][d_head], qR [B][H][d_rope],
+ *   WUK, WUV [H][d_c][d_head], out [B][H][d_head]. */
+int oracle_mla_decode_expanded(int B, int H, int d_c, int d_rope, int d_head, int Lmax, const int32_t* ctx_len,
+                               const uint16_t* rows, const uint16_t* qC, const uint16_t* qR, const uint16_t* WUK,
+                               const uint16_t* WUV, double scale, double* out) {
+    for (int b = 0; b < B; ++b)
+        if (ctx_len[b] < 0 || ctx_len[b] > Lmax) return -1;
+    const int dk = d_c + d_rope, wk = d_head + d_rope;
+    scale = default_scale(scale, wk);
+    int bad = 0;
+    #pragma omp parallel for schedule(dynamic)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H, L = ctx_len[b];
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * wk);
+        double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_head);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)wk);
+        if (!K || !V || !qd) {
+            #pragma omp atomic write
+            bad = 1;
+        } else {
+            for (int t = 0; t < L; ++t) {
+                const uint16_t* row = rows + ((size_t)b * Lmax + t) * dk;
+                for (int e = 0; e < d_head; ++e) {
+                    double ak = 0.0, av = 0.0;
+                    for (int c = 0; c < d_c; ++c) {
+                        ak += bf(row[c]) * bf(WUK[((size_t)h * d_c + c) * d_head + e]);
+                        av += bf(row[c]) * bf(WUV[((size_t)h * d_c + c) * d_head + e]);
+                    }
+                    K[(size_t)t * wk + e] = ak;
+                    V[(size_t)t * d_head + e] = av;
+                }
+                for (int e = 0; e < d_rope; ++e) K[(size_t)t * wk + d_head + e] = bf(row[d_c + e]);
+            }
+            for (int e = 0; e < d_head; ++e) qd[e] = bf(qC[((size_t)b * H + h) * d_head + e]);
+            for (int e = 0; e < d_rope; ++e) qd[d_head + e] = bf(qR[((size_t)b * H + h) * d_rope + e]);
+            attend_kv(L, wk, d_head, qd, K, V, scale, out + ((size_t)b * H + h) * d_head);
+        }
+        free(K); free(V); free(qd);
+    }
+    return bad ? -1 : 0;
 }

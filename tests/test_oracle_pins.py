@@ -393,12 +393,86 @@ def pin_rope_attention_is_concatenated(o):
             np.testing.assert_allclose(gotp[b, :, h], out, rtol=1e-12, atol=1e-14)
 
 
+def pin_rotation_direction_worked_example(o):
+    """The rotation the positional key gets is the pages' R(theta) = [[cos, -sin], [sin, cos]]: the
+    MLA lesson's worked theta = 90 degree products A.R and R.A (golden file).  The oracle rotates pair i
+    of a d_rope-vector by pos * base^(-2i/d_rope); with d_rope = 4, pos = 1 and base = 4/pi^2, pair 1
+    turns by exactly pi/2, and the unit inputs e_2, e_3 give the two columns of R."""
+    g = {}
+    for line in open(os.path.join(GOLDEN, "rotation_90deg.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        name, vals = (t.strip() for t in line.split("|"))
+        g[name] = np.array([float(v) for v in vals.split()]).reshape(2, 2)
+    d = 4
+    X = _lib_bf16(np.eye(d, dtype=np.float32)[2:4])            # rows e_2, e_3
+    WKR = _lib_bf16(np.eye(d, dtype=np.float32))
+    rows = o.mla_append(X, np.zeros((d, 8), np.uint16), WKR, np.array([1, 1], np.int32),
+                        rope_base=4.0 / np.pi ** 2)
+    kr = f64(rows[:, 8:])                                       # [2 inputs, 4]
+    R = np.stack([kr[0, 2:4], kr[1, 2:4]], axis=1)              # columns R e_0, R e_1 of the pair
+    np.testing.assert_allclose(g["A"] @ R, g["A_R"], atol=1e-6)
+    np.testing.assert_allclose(R @ g["A"], g["R_A"], atol=1e-6)
+
+
+# ---------------------------------------------------------------------------- MLA
+def _mla_case(seed, B, H, d_c, d_rope, lens):
+    pt = S.page_table(seed, lens, 64, spare_blocks=1)
+    kv = S.gaussian_bf16(seed, "mla_kv", (pt.num_blocks, 64, d_c + d_rope))
+    return pt, kv
+
+
+def pin_mla_absorbed_is_mqa(o):
+    """Absorbed MLA decode is multi-query attention over the cached rows: keys [c | k^R], values c,
+    one query [q~_h | q^R_h] per head, scale 1/sqrt(d_head + d_rope) (the MLA lesson: weight
+    absorption; decoupled RoPE; the softmax denominator of the concatenated per-head width).
+    Checked against torch SDPA on exactly those tensors, page by page gathered here."""
+    B, H, d_c, d_rope, d_head = 2, 3, 64, 16, 32
+    lens = [150, 9]
+    pt, kv = _mla_case(41, B, H, d_c, d_rope, lens)
+    q = S.gaussian_bf16(41, "mla_q", (B, H, d_c + d_rope))
+    got = o.mla_decode(kv, pt.block_table, lens, q, d_rope, d_head)
+    flat = f64(kv.reshape(-1, d_c + d_rope))
+    for b in range(B):
+        rows = flat[[pt.slot(b, t) for t in range(lens[b])]]
+        ref = _sdpa(f64(q[b])[:, None], np.broadcast_to(rows, (H,) + rows.shape).copy(),
+                    np.broadcast_to(rows[:, :d_c], (H, lens[b], d_c)).copy(), 1.0 / np.sqrt(d_head + d_rope))
+        np.testing.assert_allclose(got[b], ref[:, 0], rtol=1e-12, atol=1e-14)
+
+
+def pin_mla_absorbed_equals_expanded(o):
+    """Associativity ("Low-Rank Key Value Attention", backup frame "MLA also admits associative
+    computation"; the MLA lesson's weight absorption): scoring against the latent with q~ = q^C (W^UK)^T
+    and mapping o = a C through W^UV equals reconstructing per-head keys c W^UK and values c W^UV and
+    attending to them.  Small-integer q^C and W^UK make q~ exact in bf16."""
+    B, H, d_c, d_rope, d_head = 2, 2, 32, 8, 8
+    lens = [90, 17]
+    pt, kv = _mla_case(42, B, H, d_c, d_rope, lens)
+    qC = S.int_grid_bf16(42, "qC", (B, H, d_head), -2, 2)
+    qR = S.gaussian_bf16(42, "qR", (B, H, d_rope))
+    WUK = S.int_grid_bf16(42, "WUK", (H, d_c, d_head), -2, 2)
+    WUV = S.gaussian_bf16(42, "WUV", (H, d_c, d_head), d_c ** -0.5)
+    qt = np.einsum("bhe,hce->bhc", f64(qC), f64(WUK))
+    assert np.all(np.abs(qt) <= 256)                          # integers, exact in bf16
+    q = np.concatenate([_lib_bf16(qt), qR], axis=2)
+    o_abs = o.mla_decode(kv, pt.block_table, lens, q, d_rope, d_head)
+    got = np.einsum("bhc,hce->bhe", o_abs, f64(WUV))
+    flat = kv.reshape(-1, d_c + d_rope)
+    Lmax = max(lens)
+    rows = np.zeros((B, Lmax, d_c + d_rope), np.uint16)
+    for b in range(B):
+        rows[b, :lens[b]] = flat[[pt.slot(b, t) for t in range(lens[b])]]
+    ref = o.mla_decode_expanded(rows, lens, qC, qR, WUK, WUV)
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
+
+
 PINS = [pin_softmax_worked_value, pin_softmax_normalised, pin_attend_special_cases,
         pin_append_integer_exact, pin_append_gaussian_rounding, pin_r0_is_mqa, pin_mha_special_case,
         pin_factored_equals_expanded, pin_cache_path_matches_weight_path,
         pin_head_permutation_equivariance, pin_page_permutation_invariance, pin_prefill_causal_edges,
         pin_fused_is_concatenated_attention, pin_fused_matches_factored_decode,
-        pin_rope_append_is_rotation, pin_rope_attention_is_concatenated]
+        pin_rope_append_is_rotation, pin_rope_attention_is_concatenated, pin_rotation_direction_worked_example,
+        pin_mla_absorbed_is_mqa, pin_mla_absorbed_equals_expanded]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -411,7 +485,8 @@ def test_pin(pin, oracle_lib):
 #  4 causal diagonal excluded             5 shared term dropped       6 B_h read transposed
 #  7 absorbed decode drops the residual values z^V
 #  8 positional key rotated the wrong way    9 scale of the content width only with a positional key
-MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9]
+# 10 MLA scale over the cached row's width  11 MLA values read from the wrong slice of the row
+MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
