@@ -21,7 +21,8 @@ DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 EXPORTED = ["lrkv_abi_version", "lrkv_status_string", "lrkv_last_error", "lrkv_cache_block_bytes", "lrkv_append",
             "lrkv_decode_workspace_bytes", "lrkv_decode", "lrkv_decode_fused", "lrkv_decode_static_ws",
-            "lrkv_prefill_workspace_bytes", "lrkv_prefill"]
+            "lrkv_prefill_workspace_bytes", "lrkv_prefill", "lrkv_mla_cache_block_bytes", "lrkv_mla_append",
+            "lrkv_mla_decode_workspace_bytes", "lrkv_mla_decode"]
 STATIC_WS_BYTES = 16 << 20  # LRKV_STATIC_WS_BYTES
 
 
@@ -34,6 +35,12 @@ class LrkvError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("d_h", ctypes.c_int32), ("r", ctypes.c_int32), ("d", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("softmax_scale", ctypes.c_float), ("d_rope", ctypes.c_int32),
+                ("rope_base", ctypes.c_float)]
+
+
+class MlaDims(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int32), ("d_c", ctypes.c_int32), ("d_rope", ctypes.c_int32), ("d_head", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("block_size", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
                 ("rope_base", ctypes.c_float)]
 
 
@@ -76,6 +83,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lrkv_prefill_workspace_bytes.argtypes = [P(Dims), i32, i32]
     lib.lrkv_prefill.restype = ctypes.c_int
     lib.lrkv_prefill.argtypes = [P(Dims), vp, vp, vp, P(Cache), vp, i32, vp, i32, i32, vp, vp, sz, vp, vp]
+    lib.lrkv_mla_cache_block_bytes.restype = sz
+    lib.lrkv_mla_cache_block_bytes.argtypes = [P(MlaDims)]
+    lib.lrkv_mla_append.restype = ctypes.c_int
+    lib.lrkv_mla_append.argtypes = [P(MlaDims), vp, vp, i32, vp, vp, vp, i32, vp, vp]
+    lib.lrkv_mla_decode_workspace_bytes.restype = sz
+    lib.lrkv_mla_decode_workspace_bytes.argtypes = [P(MlaDims), i32]
+    lib.lrkv_mla_decode.restype = ctypes.c_int
+    lib.lrkv_mla_decode.argtypes = [P(MlaDims), vp, vp, i32, vp, i32, vp, i32, vp, vp, sz, vp, vp]
     _lib = lib
     return lib
 
@@ -83,6 +98,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
 def make_dims(H: int, d_h: int, r: int, d: int, block_size: int = 64, softmax_scale: float = 0.0, d_rope: int = 0,
               rope_base: float = 0.0) -> Dims:
     return Dims(H, d_h, r, d, block_size, softmax_scale, d_rope, rope_base)
+
+
+def make_mla_dims(H: int, d: int, d_head: int = 128, d_c: int = 512, d_rope: int = 64, block_size: int = 64,
+                  softmax_scale: float = 0.0, rope_base: float = 0.0) -> MlaDims:
+    return MlaDims(H, d_c, d_rope, d_head, d, block_size, softmax_scale, rope_base)
 
 
 def _ptr(t) -> int | None:
@@ -197,6 +217,30 @@ def lrkv_prefill(dims: Dims, q, BK, BV, cache: PagedCache, block_table, q_start,
                              int(block_table.shape[1]), _ptr(q_start), B, Tq, _ptr(out), _ptr(workspace), ws_bytes,
                              _ptr(status), _stream(stream))
     _check(rc, "lrkv_prefill")
+
+
+def mla_cache_block_bytes(dims: MlaDims) -> int:
+    return int(load().lrkv_mla_cache_block_bytes(ctypes.byref(dims)))
+
+
+def mla_decode_workspace_bytes(dims: MlaDims, batch: int) -> int:
+    return int(load().lrkv_mla_decode_workspace_bytes(ctypes.byref(dims), batch))
+
+
+def lrkv_mla_append(dims: MlaDims, X, W_T, slot_mapping, positions, kv, status=None, stream=None):
+    """MLA cache rows [c | RoPE(k^R)] of X [n, d] into kv [num_blocks, 64, d_c + d_rope] at slot_mapping [n]."""
+    rc = load().lrkv_mla_append(ctypes.byref(dims), _ptr(X), _ptr(W_T), int(X.shape[0]), _ptr(slot_mapping),
+                                _ptr(positions), _ptr(kv), int(kv.shape[0]), _ptr(status), _stream(stream))
+    _check(rc, "lrkv_mla_append")
+
+
+def lrkv_mla_decode(dims: MlaDims, q, kv, block_table, seq_lens, out, workspace, status=None, stream=None):
+    """Absorbed MLA decode: q [B, H, d_c + d_rope] -> out [B, H, d_c]."""
+    rc = load().lrkv_mla_decode(ctypes.byref(dims), _ptr(q), _ptr(kv), int(kv.shape[0]), _ptr(block_table),
+                                int(block_table.shape[1]), _ptr(seq_lens), int(q.shape[0]), _ptr(out),
+                                _ptr(workspace), int(workspace.numel() * workspace.element_size()), _ptr(status),
+                                _stream(stream))
+    _check(rc, "lrkv_mla_decode")
 
 
 def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:

@@ -11,6 +11,7 @@
 #include "lrkv_internal.cuh"
 
 #include "kernels.h"
+#include "mla.h"
 
 namespace {
 
@@ -113,6 +114,40 @@ lrkv_status make_tmap(CUtensorMap* m, const void* base, uint64_t cols, uint64_t 
     if (r != CUDA_SUCCESS) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
     return LRKV_OK;
 }
+
+// 3-D bf16 tensor map over a row-major [d2][d1][d0] array with a [1][box1][box0] box
+// (box rows past d1 read as zeros).
+lrkv_status make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                         uint32_t box1, CUtensorMapSwizzle swz, const char* what) {
+    auto enc = encode_fn();
+    if (!enc) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+    return LRKV_OK;
+}
+
+lrkv_status check_mla_dims(const lrkv_mla_dims* dm) {
+    if (!dm) return fail(LRKV_ERR_INVALID_ARG, "dims is NULL");
+    if (dm->block_size != 64) return fail(LRKV_ERR_UNSUPPORTED, "block_size %d (only 64 is supported)", dm->block_size);
+    if (dm->d_c != 512) return fail(LRKV_ERR_UNSUPPORTED, "d_c %d (supported: 512)", dm->d_c);
+    if (dm->d_rope != 64) return fail(LRKV_ERR_UNSUPPORTED, "d_rope %d (supported: 64)", dm->d_rope);
+    if (dm->H < 1 || dm->H > 128) return fail(LRKV_ERR_UNSUPPORTED, "H %d (supported: 1..128)", dm->H);
+    if (dm->d_head < 1 || dm->d_head > 4096) return fail(LRKV_ERR_INVALID_ARG, "d_head %d", dm->d_head);
+    if (dm->d < 8 || dm->d % 8 != 0) return fail(LRKV_ERR_UNSUPPORTED, "d %d (must be a positive multiple of 8)", dm->d);
+    if (!(dm->softmax_scale >= 0.f) || std::isinf(dm->softmax_scale))
+        return fail(LRKV_ERR_INVALID_ARG, "softmax_scale %g", (double)dm->softmax_scale);
+    if (!(dm->rope_base >= 0.f) || std::isinf(dm->rope_base) || (dm->rope_base > 0.f && dm->rope_base <= 1.f))
+        return fail(LRKV_ERR_INVALID_ARG, "rope_base %g (0 for 10000, else > 1)", (double)dm->rope_base);
+    return LRKV_OK;
+}
+
+int mla_pairs(const DeviceInfo& di) { return di.sms / 2 > 0 ? di.sms / 2 : 1; }
 
 lrkv_status cuda_status(cudaError_t e, const char* what) {
     if (e != cudaSuccess) return fail(LRKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -337,6 +372,106 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, c
     }
     return cuda_status(lrkv::launch_prefill(a, dims->d_h, dims->r, dims->d_rope, static_cast<cudaStream_t>(stream)),
                        "lrkv_prefill launch");
+}
+
+size_t lrkv_mla_cache_block_bytes(const lrkv_mla_dims* dims) {
+    if (check_mla_dims(dims) != LRKV_OK) return 0;
+    return (size_t)dims->block_size * 2 * (size_t)(dims->d_c + dims->d_rope);
+}
+
+lrkv_status lrkv_mla_append(const lrkv_mla_dims* dims, const void* X, const void* W_T, int32_t n_tok,
+                            const int32_t* slot_mapping, const int32_t* positions, void* kv, int32_t num_blocks,
+                            uint32_t* status_dev, void* stream) {
+    lrkv_status s = check_mla_dims(dims);
+    if (s != LRKV_OK) return s;
+    if (n_tok < 0) return fail(LRKV_ERR_INVALID_ARG, "n_tok %d < 0", n_tok);
+    if (n_tok == 0) return ok();
+    LRKV_REQUIRE_PTR(X);
+    LRKV_REQUIRE_PTR(W_T);
+    LRKV_REQUIRE_PTR(kv);
+    if (num_blocks < 1 || num_blocks > (1 << 24)) return fail(LRKV_ERR_INVALID_ARG, "num_blocks %d", num_blocks);
+    if (!slot_mapping || !positions) return fail(LRKV_ERR_INVALID_ARG, "slot_mapping or positions is NULL");
+    // The cache row [c | k^R] is the shared key row of the append kernels with d_h = d_c and no
+    // value or per-head columns: columns [0, d_c) plain, [d_c, d_c + d_rope) rotated.
+    uint16_t* pool = static_cast<uint16_t*>(kv);
+    lrkv::AppendArgs a{};
+    a.X = static_cast<const uint16_t*>(X);
+    a.W = static_cast<const uint16_t*>(W_T);
+    a.slots = slot_mapping;
+    a.positions = positions;
+    a.sK = pool;
+    a.sV = a.zK = a.zV = pool;  // never addressed: every column maps into the key row
+    a.status = status_dev;
+    a.n = n_tok;
+    a.d = dims->d;
+    a.N = dims->d_c + dims->d_rope;
+    a.d_h = dims->d_c;
+    a.HR = 0;
+    a.d_rope = dims->d_rope;
+    a.rope_base = dims->rope_base > 0.f ? dims->rope_base : 10000.f;
+    a.nslots = (long long)num_blocks * dims->block_size;
+    if (n_tok >= lrkv::kAppendTcMinRows) {
+        CUtensorMap tX, tW;
+        const int bn = lrkv::append_tc_block_n(a.N);
+        if ((s = make_tmap(&tX, X, dims->d, n_tok, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "X")) != LRKV_OK) return s;
+        if ((s = make_tmap(&tW, W_T, dims->d, a.N, 64, bn, CU_TENSOR_MAP_SWIZZLE_128B, "W_T")) != LRKV_OK) return s;
+        return cuda_status(lrkv::launch_append_tc(tX, tW, a, static_cast<cudaStream_t>(stream)),
+                           "lrkv_mla_append launch");
+    }
+    return cuda_status(lrkv::launch_append(a, static_cast<cudaStream_t>(stream)), "lrkv_mla_append launch");
+}
+
+size_t lrkv_mla_decode_workspace_bytes(const lrkv_mla_dims* dims, int32_t batch) {
+    if (check_mla_dims(dims) != LRKV_OK || batch < 0) return 0;
+    DeviceInfo di;
+    if (device_info(&di) != LRKV_OK) return 0;
+    return lrkv::mla_workspace_bytes(dims->H, batch, mla_pairs(di));
+}
+
+lrkv_status lrkv_mla_decode(const lrkv_mla_dims* dims, const void* q, const void* kv, int32_t num_blocks,
+                            const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                            int32_t batch, void* out, void* workspace, size_t workspace_bytes,
+                            uint32_t* status_dev, void* stream) {
+    lrkv_status s = check_mla_dims(dims);
+    if (s != LRKV_OK) return s;
+    if (batch < 0) return fail(LRKV_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (batch == 0) return ok();
+    if (num_blocks < 1 || num_blocks > (1 << 24)) return fail(LRKV_ERR_INVALID_ARG, "num_blocks %d", num_blocks);
+    if (max_blocks_per_seq < 1 || (long long)max_blocks_per_seq * dims->block_size > (1LL << 30))
+        return fail(LRKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", max_blocks_per_seq);
+    LRKV_REQUIRE_PTR(q);
+    LRKV_REQUIRE_PTR(kv);
+    LRKV_REQUIRE_PTR(out);
+    if (!block_table || !seq_lens) return fail(LRKV_ERR_INVALID_ARG, "block_table or seq_lens is NULL");
+    DeviceInfo di;
+    if ((s = device_info(&di)) != LRKV_OK) return s;
+    lrkv::MlaArgs a{};
+    a.npairs = mla_pairs(di);
+    const size_t need = lrkv::mla_workspace_bytes(dims->H, batch, a.npairs);
+    if (!workspace || ((uintptr_t)workspace & 255u))
+        return fail(LRKV_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+    if (workspace_bytes < need) return fail(LRKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+    const uint64_t dk = (uint64_t)dims->d_c + dims->d_rope;
+    CUtensorMap tQ, tKV;
+    if ((s = make_tmap_3d(&tQ, q, dk, dims->H, batch, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "q")) != LRKV_OK) return s;
+    if ((s = make_tmap(&tKV, kv, dk, (uint64_t)num_blocks * dims->block_size, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                       "kv")) != LRKV_OK)
+        return s;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.status = status_dev;
+    a.out = static_cast<uint16_t*>(out);
+    a.B = batch;
+    a.H = dims->H;
+    a.max_pages = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.pmax = a.npairs > batch ? a.npairs : batch;
+    const float scale = dims->softmax_scale > 0.f ? dims->softmax_scale
+                                                  : 1.0f / std::sqrt((float)(dims->d_head + dims->d_rope));
+    a.scale_log2 = scale * 1.4426950408889634f;
+    lrkv::mla_carve_workspace(&a, workspace);
+    return cuda_status(lrkv::launch_mla_decode(tQ, tKV, a, static_cast<cudaStream_t>(stream)),
+                       "lrkv_mla_decode launch");
 }
 
 }  // extern "C"

@@ -215,8 +215,9 @@ size_t lrkv_prefill_workspace_bytes(const lrkv_dims* dims, int32_t batch, int32_
  *   position p = q_start[b] + i and attends to cached tokens j <= p.  The chunk's
  *   own rows must already be in the cache (lrkv_append first).
  *   Logits use the concatenated width d_h + r: [q | q~] . [s^K | z^K_h]; the
- *   scale stays 1/sqrt(d_h) (the dot product is the same one).
- *   q        [batch][Tq][H][d_h]
+ *   scale stays 1/sqrt(d_h) (the dot product is the same one), or 1/sqrt(d_h + d_rope)
+ *   with a positional key (whose term q^R . k^R joins the logit).
+ *   q        [batch][Tq][H][d_h + d_rope]
  *   q_start  [batch] int32 (device)
  *   out      [batch][Tq][H][d_h]
  */
@@ -224,6 +225,71 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, c
                          const lrkv_cache* cache, const int32_t* block_table, int32_t max_blocks_per_seq,
                          const int32_t* q_start, int32_t batch, int32_t Tq, void* out, void* workspace,
                          size_t workspace_bytes, uint32_t* status_dev, void* stream);
+
+/* ======================================================================
+ * Multi-head latent attention (second workload on the same skeleton).
+ *
+ * "Embeddings II: MLA & Architectural Choices" (weight absorption, decoupled RoPE,
+ * the softmax denominator of the concatenated width), in the associative form of
+ * "Low-Rank Key Value Attention", backup frame "MLA also admits associative
+ * computation": per token and layer the cache holds one row [c_t | k^R_t] -- the
+ * latent c_t = x_t W^DKV (d_c = 512) and the decoupled positional key
+ * k^R_t = RoPE(x_t W^KR, t) (d_rope = 64), both shared by all heads:
+ *        kv : [num_blocks][block_size][d_c + d_rope]   bf16
+ * With W^UK_i folded into the query and W^UV_i into the output projection, head i
+ * computes  logit_t = [q~_i | q^R_i] . [c_t | k^R_t] * scale  and returns
+ * o_i = sum_t softmax(logit)_t c_t (width d_c, before W^UV_i).
+ * Conventions (ownership, alignment, streams, errors, status bits) as above.
+ * ====================================================================== */
+typedef struct lrkv_mla_dims {
+    int32_t H;           /* query heads, 1..128 */
+    int32_t d_c;         /* latent width; must be 512 */
+    int32_t d_rope;      /* positional key width; must be 64 */
+    int32_t d_head;      /* per-head content width the absorbed dot product stands for (>= 1) */
+    int32_t d;           /* hidden size of appended rows; a positive multiple of 8 */
+    int32_t block_size;  /* tokens per cache page; must be 64 */
+    float softmax_scale; /* 0 means 1/sqrt(d_head + d_rope) */
+    float rope_base;     /* RoPE base; 0 means 10000 */
+} lrkv_mla_dims;
+
+/* Bytes of one cache page: block_size * 2 * (d_c + d_rope); 0 for unsupported dims. */
+size_t lrkv_mla_cache_block_bytes(const lrkv_mla_dims* dims);
+
+/*
+ * lrkv_mla_append -- write n_tok cache rows: Y = X [W^DKV | W^KR] accumulated in fp32;
+ *   the last d_rope columns are rotated at positions[t] (pair (2i, 2i+1) by the angle
+ *   pos * rope_base^(-2i / d_rope); angle, sine, cosine in double, result rounded to
+ *   fp32); then bf16 (nearest, ties to even) into slot slot_mapping[t] of kv.
+ *   X            [n_tok][d]
+ *   W_T          [d_c + d_rope][d]  (row c holds the weights of output column c)
+ *   slot_mapping [n_tok] int32 (device); negative skips the row, >= num_blocks*block_size
+ *                sets LRKV_DEV_BAD_SLOT and skips it
+ *   positions    [n_tok] int32 (device), >= 0
+ */
+lrkv_status lrkv_mla_append(const lrkv_mla_dims* dims, const void* X, const void* W_T, int32_t n_tok,
+                            const int32_t* slot_mapping, const int32_t* positions, void* kv, int32_t num_blocks,
+                            uint32_t* status_dev, void* stream);
+
+/* Workspace bytes lrkv_mla_decode needs for `batch` sequences on the CURRENT device. */
+size_t lrkv_mla_decode_workspace_bytes(const lrkv_mla_dims* dims, int32_t batch);
+
+/*
+ * lrkv_mla_decode -- one decode step per sequence over all seq_lens[b] cached tokens.
+ *   q           [batch][H][d_c + d_rope]  ([q~_i | q^R_i], q^R rotated by the caller)
+ *   kv          [num_blocks][block_size][d_c + d_rope]
+ *   block_table [batch][max_blocks_per_seq] int32 (device)
+ *   seq_lens    [batch] int32 (device)
+ *   out         [batch][H][d_c] bf16 (nearest, ties to even from fp32)
+ *   workspace   >= lrkv_mla_decode_workspace_bytes(dims, batch) bytes, 256-byte aligned
+ *   Split over the sequence across pairs of CTAs (each pair divides the row's columns),
+ *   merged by log-sum-exp in a second kernel.  A sequence with a length outside
+ *   [1, max_blocks_per_seq * block_size] sets LRKV_DEV_BAD_SEQLEN and gets zero rows.
+ *   The call does not overlap the caller's previous kernel on the stream.
+ */
+lrkv_status lrkv_mla_decode(const lrkv_mla_dims* dims, const void* q, const void* kv, int32_t num_blocks,
+                            const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                            int32_t batch, void* out, void* workspace, size_t workspace_bytes,
+                            uint32_t* status_dev, void* stream);
 
 #ifdef __cplusplus
 }

@@ -117,3 +117,31 @@ def test_positional_key_needs_positions():
     # without a positional key the positions pointer is ignored
     plain = b.make_dims(8, 64, 8, 512)
     assert lib.lrkv_append(ctypes.byref(plain), None, None, 0, None, None, ctypes.byref(c), None, None) == 0
+
+
+@pytest.mark.parametrize("kw,code", [(dict(d_c=256), 2), (dict(d_rope=32), 2), (dict(H=0), 2), (dict(H=129), 2),
+                                     (dict(block_size=32), 2), (dict(d=500), 2), (dict(d_head=0), 1),
+                                     (dict(softmax_scale=float("nan")), 1), (dict(rope_base=0.5), 1)])
+def test_mla_dims_rejected(kw, code):
+    """Multi-head latent attention: d_c = 512, d_rope = 64, block 64, 1 <= H <= 128 are the supported shape."""
+    lib = b.load()
+    base = dict(H=128, d=5120)
+    base.update(kw)
+    dims = b.make_mla_dims(**base)
+    assert b.mla_cache_block_bytes(dims) == 0
+    assert lib.lrkv_mla_append(ctypes.byref(dims), 16, 16, 1, 16, 16, 16, 1, None, None) == code
+    assert lib.lrkv_mla_decode(ctypes.byref(dims), 16, 16, 1, 16, 1, 16, 1, 16, 256, 1 << 30, None, None) == code
+
+
+def test_mla_arguments():
+    lib = b.load()
+    dims = b.make_mla_dims(128, 5120)
+    assert b.mla_cache_block_bytes(dims) == 64 * 2 * 576
+    # positions are required; zero rows / zero batch are no-ops
+    assert lib.lrkv_mla_append(ctypes.byref(dims), 16, 16, 1, 16, None, 16, 1, None, None) == 1
+    assert b"positions" in lib.lrkv_last_error()
+    assert lib.lrkv_mla_append(ctypes.byref(dims), None, None, 0, None, None, None, 1, None, None) == 0
+    assert lib.lrkv_mla_append(ctypes.byref(dims), 24, 16, 1, 16, 16, 16, 1, None, None) == 1
+    assert lib.lrkv_mla_decode(ctypes.byref(dims), 16, 16, 1, 16, 1, 16, 0, 16, 256, 0, None, None) == 0
+    assert lib.lrkv_mla_decode(ctypes.byref(dims), 16, 16, 0, 16, 1, 16, 1, 16, 256, 0, None, None) == 1
+    assert lib.lrkv_mla_decode(ctypes.byref(dims), 16, 16, 1, None, 1, 16, 1, 16, 256, 0, None, None) == 1
