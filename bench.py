@@ -16,7 +16,9 @@ Other workloads (--workload): "dsv2" (H=128, d_h=128, r=16, d=16384, batch 8,
 2048 tokens), "small" (the single-layer parity case) -- decode steps as above;
 "prefill": causal chunked prefill plus cache append (d=4096, H=32, d_h=128,
 r=16, batch 2, 4096-token prompts in 512-token chunks), value in prompt
-tokens/s with the tensor roofline of the prefill kernel.  --fused runs a decode
+tokens/s with the tensor roofline of the prefill kernel; "mla": multi-head latent
+attention decode with absorbed weights at DeepSeek-V2's attention shape (H=128,
+d_c=512, d_h^R=64, d=5120, batch 8, 16384 cached tokens), GB/s as for decode.  --fused runs a decode
 workload through lrkv_decode_fused (both absorptions in the caller's weights:
 q~ given, [o_s | o_z] returned), counting that form's own bytes.  --rope adds the
 64-wide decoupled positional key (key rows [s^K | k^R], rotated in the append).
@@ -46,6 +48,7 @@ import lrkv_synth as S  # noqa: E402
 from compressed_kv_cache_lrkv_gb300 import accounting as A  # noqa: E402
 
 METRIC_DECODE = "LRKV decode cache-read GB/s (% of GB300 HBM peak) and decode tokens/sec"
+METRIC_MLA = "MLA (absorbed) decode cache-read GB/s (% of GB300 HBM peak) and decode tokens/sec"
 METRIC_PREFILL = "LRKV chunked prefill + append prompt tokens/sec (bf16 tensor TFLOP/s of the prefill kernel)"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
@@ -436,8 +439,123 @@ class PrefillHarness:
                           f"{reps} repetitions in {dt:.1f} s; fp64, OpenMP over heads"}
 
 
+# ----------------------------------------------------------------------------- MLA decode
+class MlaHarness:
+    """Multi-head latent attention with absorbed weights, per layer: lrkv_mla_append of each
+    sequence's newest row [c | RoPE(k^R)], then lrkv_mla_decode."""
+
+    profile = "mla_decode.md"
+    sources = ("mla_decode.cu", "mla.h", "lrkv_internal.cuh", "kernels.h")
+
+    def __init__(self, wl, rank):
+        import torch
+
+        from compressed_kv_cache_lrkv_gb300 import binding as b
+        self.torch, self.b, self.wl = torch, b, wl
+        B, H, d, dc, dr = wl.B, wl.H, wl.d, wl.d_c, wl.d_rope
+        dk = dc + dr
+        self.seq_lens = workload_seq_lens(wl)
+        self.pt = S.page_table(wl.seed, self.seq_lens, 64)
+        nb = self.pt.num_blocks
+        gen = torch.Generator(device="cuda").manual_seed(replica_seed(rank, 5678))
+        rn = lambda *s, scale=1.0: (torch.randn(*s, generator=gen, device="cuda") * scale).to(torch.bfloat16)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+        self.dims = b.make_mla_dims(H, d, d_head=wl.d_h, d_c=dc, d_rope=dr)
+        self.kv = rn(nb, 64, dk)
+        self.q = rn(B, H, dk)
+        self.wt = rn(dk, d, scale=d ** -0.5)
+        self.x = rn(B, d)
+        self.out = torch.empty(B, H, dc, dtype=torch.bfloat16, device="cuda")
+        self.bt = i32(self.pt.block_table)
+        self.sl = i32(self.pt.seq_lens)
+        self.slots = i32([self.pt.slot(i, int(L) - 1) for i, L in enumerate(self.seq_lens)])
+        self.positions = i32(self.seq_lens - 1)
+        self.ws = b.alloc_workspace(b.mla_decode_workspace_bytes(self.dims, B))
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.cache_bytes = self.kv.numel() * self.kv.element_size()
+        self.kernel_units = A.mla_decode_algorithmic_bytes(H, dc, dr, self.seq_lens)
+        self.step_units = self.kernel_units + A.mla_append_algorithmic_bytes(B, d, dc, dr)
+        self.flops = A.mla_decode_flops(H, dc, dr, self.seq_lens)
+        self.launches_per_step = 3
+
+    def step(self, stream):
+        b = self.b
+        b.lrkv_mla_append(self.dims, self.x, self.wt, self.slots, self.positions, self.kv, status=self.status,
+                          stream=stream)
+        b.lrkv_mla_decode(self.dims, self.q, self.kv, self.bt, self.sl, self.out, self.ws, status=self.status,
+                          stream=stream)
+
+    def kernel(self, stream):
+        self.b.lrkv_mla_decode(self.dims, self.q, self.kv, self.bt, self.sl, self.out, self.ws, status=self.status,
+                               stream=stream)
+
+    def e2e_setup(self):
+        t = self.torch
+        self.h_in = [(x.cpu().pin_memory(), x) for x in (self.x, self.q, self.slots, self.positions, self.sl)]
+        self.h_out = [(t.empty_like(self.out, device="cpu").pin_memory(), self.out)]
+        return (sum(h.numel() * h.element_size() for h, _ in self.h_in),
+                sum(h.numel() * h.element_size() for h, _ in self.h_out))
+
+    def e2e_step(self, stream):
+        for h, d in self.h_in:
+            d.copy_(h, non_blocking=True)
+        self.step(stream)
+        for h, d in self.h_out:
+            h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    def report(self, step_s, kernel_s, e2e_s, world, peaks):
+        wl = self.wl
+        value = self.step_units * world / step_s / 1e9
+        achieved = self.kernel_units / kernel_s / 1e9
+        return {
+            "metric": METRIC_MLA, "value": value, "unit": "GB/s",
+            "tokens_per_s": wl.B * world / step_s, "pct_of_hbm_peak": 100.0 * value / peaks["hbm_gbs"],
+            "config": {"workload": f"{wl.key}: {wl.description}", "B": wl.B,
+                       "seq_lens": [int(x) for x in self.seq_lens], "H": wl.H, "d_c": wl.d_c, "d_rope": wl.d_rope,
+                       "d_head": wl.d_h, "d": wl.d, "block_size": 64, "pages": int(self.pt.num_blocks),
+                       "cache_bytes": int(self.cache_bytes),
+                       "l2": f"inputs larger than L2: cache {self.cache_bytes / 2**20:.0f} MiB vs L2 "
+                             f"{L2_BYTES / 2**20:.0f} MiB",
+                       "step": "lrkv_mla_append (1 row per sequence, positional key rotated) + lrkv_mla_decode",
+                       "parallelism": f"replicas x{world} (independent batches)"},
+            "roofline": {"kernel": "lrkv_mla_decode (cluster split + combine kernels)", "bound": "hbm",
+                         "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic(self.profile, self.sources),
+                         "tensor_tflops": self.flops / kernel_s / 1e12,
+                         "tensor_frac": self.flops / kernel_s / 1e12 / peaks["bf16_tflops"],
+                         "algorithmic_bytes_per_launch": self.kernel_units,
+                         "algorithmic_flops_per_launch": self.flops,
+                         "avg_launch_ms": kernel_s * 1e3},
+            "e2e_unit_value": lambda s: self.step_units * world / s / 1e9, "e2e_unit": "GB/s",
+        }
+
+    def cpu_baseline(self, budget_s):
+        """fp64 oracle (absorbed MLA decode, all heads) on a prefix of the first sequence."""
+        import oracle
+        wl = self.wl
+        o = oracle.get()
+        dk = wl.d_c + wl.d_rope
+        tokens = min(int(self.seq_lens[0]), 2048)
+        pt = S.page_table(wl.seed, [tokens], 64)
+        kv = S.gaussian_bf16(wl.seed, "bl_kv", (pt.num_blocks, 64, dk))
+        q = S.gaussian_bf16(wl.seed, "bl_q", (1, wl.H, dk))
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            o.mla_decode(kv, pt.block_table, pt.seq_lens, q, wl.d_rope, wl.d_h)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget_s:
+                break
+        nbytes = A.mla_decode_algorithmic_bytes(wl.H, wl.d_c, wl.d_rope, [tokens]) * reps
+        return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
+                "sample": f"absorbed MLA decode of the first {tokens} cached tokens of one sequence (all {wl.H} "
+                          f"heads), {reps} repetitions in {dt:.1f} s; fp64, OpenMP over heads"}
+
+
 HARNESS = {"longctx": DecodeHarness, "dsv2": DecodeHarness, "backbone12": DecodeHarness, "small": DecodeHarness,
-           "prefill": PrefillHarness}
+           "prefill": PrefillHarness, "mla": MlaHarness}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -565,6 +683,9 @@ def run_reference(args, world, rank):
     o = oracle.get()
     per_step_budget = max(0.01, 90.0 / max(args.steps + args.warmup, 1))
 
+    if wl.d_c:
+        return run_reference_mla(args, wl, seq_lens, o, per_step_budget)
+
     def inputs(tokens):
         pt = S.page_table(wl.seed, [tokens], 64)
         pools = tuple(S.gaussian_bf16(wl.seed, n, shp) for n, shp in
@@ -597,6 +718,42 @@ def run_reference(args, world, rank):
                    "d_h": wl.d_h, "r": wl.r},
         "cpu_baseline": {"value": val, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
                          "sample": f"E2 decode of the first {tokens} tokens of one sequence, all heads, per step"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+def run_reference_mla(args, wl, seq_lens, o, per_step_budget):
+    """--impl reference on the MLA workload: the oracle's absorbed MLA decode of a prefix of the
+    first sequence, all heads, each step."""
+    dk = wl.d_c + wl.d_rope
+
+    def inputs(tokens):
+        pt = S.page_table(wl.seed, [tokens], 64)
+        return (pt, S.gaussian_bf16(wl.seed, "rf_kv", (pt.num_blocks, 64, dk)),
+                S.gaussian_bf16(wl.seed, "rf_q", (1, wl.H, dk)))
+
+    probe = 256
+    pt, kv, q = inputs(probe)
+    t0 = time.perf_counter()
+    o.mla_decode(kv, pt.block_table, pt.seq_lens, q, wl.d_rope, wl.d_h)
+    rate = probe / max(time.perf_counter() - t0, 1e-6)
+    tokens = max(64, int(min(int(seq_lens[0]), rate * per_step_budget)) // 64 * 64)
+    pt, kv, q = inputs(tokens)
+    for _ in range(args.warmup):
+        o.mla_decode(kv, pt.block_table, pt.seq_lens, q, wl.d_rope, wl.d_h)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.mla_decode(kv, pt.block_table, pt.seq_lens, q, wl.d_rope, wl.d_h)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    val = A.mla_decode_algorithmic_bytes(wl.H, wl.d_c, wl.d_rope, [tokens]) / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC_MLA, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.key}: {wl.description}", "sample_tokens_per_step": tokens, "H": wl.H,
+                   "d_c": wl.d_c, "d_rope": wl.d_rope},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
+                         "sample": f"absorbed MLA decode of the first {tokens} tokens of one sequence, all heads, "
+                                   f"per step"},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
 

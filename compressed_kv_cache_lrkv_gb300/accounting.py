@@ -105,3 +105,24 @@ def prefill_flops(B: int, T: int, H: int, d_h: int, r: int, q_start: int = 0) ->
     q~ absorption and B^V up-projection, 4 B T H d_h r."""
     pairs = T * q_start + T * (T + 1) // 2
     return 4 * (d_h + r) * H * B * pairs + 4 * B * T * H * d_h * r
+
+
+def mla_decode_algorithmic_bytes(H: int, d_c: int, d_rope: int, seq_lens: Iterable[int], layers: int = 1) -> int:
+    """Bytes of one absorbed MLA decode step: every cached row [c | k^R], the query [q~ | q^R] in and
+    o (width d_c) out, all bf16."""
+    seq_lens = list(int(x) for x in seq_lens)
+    B = len(seq_lens)
+    per_layer = (sum(seq_lens) * (d_c + d_rope) + B * H * (2 * d_c + d_rope)) * BF16_BYTES
+    return per_layer * layers
+
+
+def mla_decode_flops(H: int, d_c: int, d_rope: int, seq_lens: Iterable[int], layers: int = 1) -> int:
+    """Multiply-adds x 2 of absorbed MLA decode: per cached token and head (d_c + d_rope) for the
+    logit and d_c for the value sum."""
+    return layers * 2 * H * (2 * d_c + d_rope) * sum(int(x) for x in seq_lens)
+
+
+def mla_append_algorithmic_bytes(n_tok: int, d: int, d_c: int, d_rope: int) -> int:
+    """X in, [W^DKV | W^KR] in, cache rows out (bf16)."""
+    N = d_c + d_rope
+    return BF16_BYTES * (n_tok * d + d * N + n_tok * N)

@@ -1,4 +1,4 @@
-"""The five synthetic workloads (shapes only; no arithmetic of the method).
+"""The synthetic workloads (shapes only; no arithmetic of the method).
 
 Shapes follow the pages' models: the 12-layer d=512, 8-head, d_h=64 backbone of
 the KVPath experiments page; DeepSeek-V2's 128 heads x 128 of the MLA lesson;
@@ -26,6 +26,8 @@ class Workload:
     chunk: int | None = None   # prefill query chunk
     seed: int = 0
     block_size: int = 64
+    d_c: int = 0               # multi-head latent attention: latent width (0: an LRKV workload)
+    d_rope: int = 0            # decoupled positional key width
 
     @property
     def ragged(self) -> bool:
@@ -46,6 +48,9 @@ WORKLOADS = {
                      B=8, L=8192, H=128, d_h=128, r=16, d=16384, seed=2),
     "longctx": Workload("longctx", "long-context decode d=4096, H=32, d_h=128, r=32, batch 4, ragged lengths uniform in [16384, 32768]",
                         B=4, L=32768, L_min=16384, H=32, d_h=128, r=32, d=4096, seed=3),
+    "mla": Workload("mla", "multi-head latent attention decode at DeepSeek-V2's attention shape (H=128, d_c=512, "
+                    "d_h^R=64, d_h=128, d=5120), absorbed weights, batch 8, 16384 cached tokens, 64-token pages",
+                    B=8, L=16384, H=128, d_h=128, r=0, d=5120, d_c=512, d_rope=64, seed=5),
     "prefill": Workload("prefill", "causal chunked prefill + append d=4096, H=32, d_h=128, r=16, batch 2, 4096-token prompts, 512-token chunks",
                         B=2, L=4096, H=32, d_h=128, r=16, d=4096, chunk=512, seed=4),
 }

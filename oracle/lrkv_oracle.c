@@ -581,20 +581,18 @@ int oracle_mla_decode(int B, int H, int d_c, int d_rope, int d_head, int bs, int
         }
     }
     const int dk = d_c + d_rope;
+    if (dk > 1024) return -1;
 #if LRKV_ORACLE_MUTANT == 10
     scale = default_scale(scale, dk); /* planted: scale over the cached row's width */
 #else
     scale = default_scale(scale, d_head + d_rope);
 #endif
     int bad = 0;
-    #pragma omp parallel for schedule(dynamic)
     for (int b = 0; b < B; ++b) {
         int L = seq_lens[b];
         double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * dk);
         double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * d_c);
-        double* qd = (double*)malloc(sizeof(double) * (size_t)dk);
-        if (!K || !V || !qd) {
-            #pragma omp atomic write
+        if (!K || !V) {
             bad = 1;
         } else {
             for (int t = 0; t < L; ++t) {
@@ -606,13 +604,16 @@ int oracle_mla_decode(int B, int H, int d_c, int d_rope, int d_head, int bs, int
                 for (int i = 0; i < d_c; ++i) V[(size_t)t * d_c + i] = bf(kv[slot * dk + i]);
 #endif
             }
+            /* heads are independent: one query row each against the same keys and values */
+            #pragma omp parallel for schedule(dynamic)
             for (int h = 0; h < H; ++h) {
                 if (want && !want[(size_t)b * H + h]) continue;
-                for (int i = 0; i < dk; ++i) qd[i] = bf(q[((size_t)b * H + h) * dk + i]);
+                double qd[1024];
+                for (int i = 0; i < dk && i < 1024; ++i) qd[i] = bf(q[((size_t)b * H + h) * dk + i]);
                 attend_kv(L, dk, d_c, qd, K, V, scale, out + ((size_t)b * H + h) * d_c);
             }
         }
-        free(K); free(V); free(qd);
+        free(K); free(V);
     }
     return bad ? -1 : 0;
 }
