@@ -452,10 +452,12 @@ lrkv_status lrkv_mla_decode(const lrkv_mla_dims* dims, const void* q, const void
         return fail(LRKV_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
     if (workspace_bytes < need) return fail(LRKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
     const uint64_t dk = (uint64_t)dims->d_c + dims->d_rope;
-    CUtensorMap tQ, tKV;
-    if ((s = make_tmap_3d(&tQ, q, dk, dims->H, batch, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "q")) != LRKV_OK) return s;
-    if ((s = make_tmap(&tKV, kv, dk, (uint64_t)num_blocks * dims->block_size, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B,
-                       "kv")) != LRKV_OK)
+    CUtensorMap tQ, tQr, tKV, tKVr;
+    const uint64_t rows = (uint64_t)num_blocks * dims->block_size;
+    if ((s = make_tmap_3d(&tQ, q, dk, dims->H, batch, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "q")) != LRKV_OK ||
+        (s = make_tmap_3d(&tQr, q, dk, dims->H, batch, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B, "q^R")) != LRKV_OK ||
+        (s = make_tmap(&tKV, kv, dk, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "kv")) != LRKV_OK ||
+        (s = make_tmap(&tKVr, kv, dk, rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B, "k^R")) != LRKV_OK)
         return s;
     a.block_table = block_table;
     a.seq_lens = seq_lens;
@@ -470,7 +472,7 @@ lrkv_status lrkv_mla_decode(const lrkv_mla_dims* dims, const void* q, const void
                                                   : 1.0f / std::sqrt((float)(dims->d_head + dims->d_rope));
     a.scale_log2 = scale * 1.4426950408889634f;
     lrkv::mla_carve_workspace(&a, workspace);
-    return cuda_status(lrkv::launch_mla_decode(tQ, tKV, a, static_cast<cudaStream_t>(stream)),
+    return cuda_status(lrkv::launch_mla_decode(tQ, tQr, tKV, tKVr, a, static_cast<cudaStream_t>(stream)),
                        "lrkv_mla_decode launch");
 }
 

@@ -16,6 +16,8 @@ struct MlaArgs {
     uint16_t* out;               // [B][H][512] bf16
     float* part_ml;              // [H][pmax][2]   running max (log2 units) and sum per split
     float* part_acc;             // [H][pmax][512] unnormalised sum_t p_t c_t per split
+    int* seq_first;              // [B] first split of each sequence (written by the split kernel)
+    int* seq_count;              // [B] its number of splits (0: length out of range)
     int B, H, max_pages, num_blocks;
     int npairs;                  // CTA pairs (clusters) of the split kernel
     int pmax;                    // max(npairs, B): split slots per head
@@ -24,7 +26,9 @@ struct MlaArgs {
 
 size_t mla_workspace_bytes(int H, int B, int npairs);
 void mla_carve_workspace(MlaArgs* a, void* ws);
-cudaError_t launch_mla_decode(const CUtensorMap& tmQ, const CUtensorMap& tmKV, const MlaArgs& a,
-                              cudaStream_t stream);
+// tmQ / tmKV: 64-column boxes (128-byte swizzle) of q and the cache; tmQr / tmKVr: 32-column
+// boxes (64-byte swizzle) of their positional-key columns.
+cudaError_t launch_mla_decode(const CUtensorMap& tmQ, const CUtensorMap& tmQr, const CUtensorMap& tmKV,
+                              const CUtensorMap& tmKVr, const MlaArgs& a, cudaStream_t stream);
 
 }  // namespace lrkv
