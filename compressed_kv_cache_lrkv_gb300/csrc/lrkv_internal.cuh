@@ -301,12 +301,14 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 
 // Rotary encoding of one pair of the shared positional key (the columns d_h + 2i and
 // d_h + 2i + 1 of a cache row) for token position pos: the pair is turned by the angle
-// pos * base^(-2i / d_rope).  Angle, sine and cosine in double (positions reach 10^5, where
-// an fp32 angle would already be off by ~0.2%), then rounded to fp32 like every column.
+// pos * base^(-2i / d_rope).  All in double: the angle is reduced to a fraction of a turn
+// (positions reach 10^5 radians) so that sine and cosine need no argument reduction
+// (sincospi), and the products are double too -- with large |x0|, |x1| cancelling to a small
+// result, fp32 would not hold one bf16 ulp.  The result is rounded to fp32 like every column.
 __device__ __forceinline__ void rope_pair(float& x0, float& x1, int i, int d_rope, int pos, float base) {
-    const double ang = (double)pos * pow((double)base, -2.0 * i / d_rope);
+    const double turns = (double)pos * pow((double)base, -2.0 * i / d_rope) * 0.15915494309189533577;
     double sn, cs;
-    sincos(ang, &sn, &cs);
+    sincospi(2.0 * (turns - floor(turns)), &sn, &cs);
     const double y0 = (double)x0 * cs - (double)x1 * sn;
     const double y1 = (double)x0 * sn + (double)x1 * cs;
     x0 = (float)y0;
