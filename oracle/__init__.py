@@ -120,6 +120,8 @@ class Oracle:
         L.oracle_mla_decode.restype = _c_int
         L.oracle_mla_decode_expanded.argtypes = ([_c_int] * 6 + [_i32p] + [_u16p] * 5 + [_c_double, _f64p])
         L.oracle_mla_decode_expanded.restype = _c_int
+        L.oracle_train_forward.argtypes = [_c_int] * 5 + [_u16p] * 4 + [_f64p]
+        L.oracle_train_backward.argtypes = [_c_int] * 5 + [_u16p] * 5 + [_f64p] * 4
 
     # -- small pieces ---------------------------------------------------------
     def num_threads(self) -> int:
@@ -257,6 +259,27 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_mla_decode_expanded: bad argument")
         return out
+
+    # -- training: expanded projections ----------------------------------------------
+    def train_forward(self, X, Ws, U, B):
+        """K_h = X (W_s + U_h B_h^T) for all heads: X [n, d], Ws [d, d_h], U [H, d, r], B [H, d_h, r]
+        -> [n, H, d_h] fp64."""
+        X = _u16(X)
+        n, d = X.shape
+        H, d_h, r = B.shape
+        K = np.zeros((n, H, d_h), np.float64)
+        self.lib.oracle_train_forward(n, d, d_h, H, r, X, _u16(Ws), _u16(U), _u16(B), K)
+        return K
+
+    def train_backward(self, X, Ws, U, B, dK):
+        """Gradients of sum(dK * K) w.r.t. X, W_s, U, B (the chain rule through K_h = X W_h):
+        returns dX [n, d], dWs [d, d_h], dU [H, d, r], dB [H, d_h, r], fp64."""
+        X = _u16(X)
+        n, d = X.shape
+        H, d_h, r = B.shape
+        dX = np.zeros((n, d)); dWs = np.zeros((d, d_h)); dU = np.zeros((H, d, r)); dB = np.zeros((H, d_h, r))
+        self.lib.oracle_train_backward(n, d, d_h, H, r, X, _u16(Ws), _u16(U), _u16(B), _u16(dK), dX, dWs, dU, dB)
+        return dX, dWs, dU, dB
 
     # -- prefill ----------------------------------------------------------------
     def prefill_expanded(self, X, q_start, WsK, WsV, UK, UV, BK, BV, q, scale=0.0, want=None):

@@ -37,6 +37,9 @@
  *   - cache values are produced by an fp64 sum, rounded to fp32 (nearest) and
  *     then to bf16 (nearest, ties to even).
  *
+ * Training: forward and backward of one expanded projection K_h = X (W_shared + U_h B_h^T)
+ * (frame "Training learns the base and residuals together"), by the chain rule.
+ *
  * Second workload: multi-head latent attention ("Embeddings II: MLA & Architectural
  * Choices", weight absorption and decoupled RoPE), absorbed (attention over the cached
  * rows [c_t | k^R_t], values c_t) and expanded (per-head keys and values reconstructed
@@ -660,4 +663,98 @@ int oracle_mla_decode_expanded(int B, int H, int d_c, int d_rope, int d_head, in
         free(K); free(V); free(qd);
     }
     return bad ? -1 : 0;
+}
+
+/* ---------------------------------------------------------------- training: expanded projections */
+/*
+ * "Low-Rank Key Value Attention", frame "Training learns the base and residuals together":
+ * during training the full per-head features are materialised, K_h = X W_h with
+ * W_h = W_shared + U_h B_h^T (Eqs. (2)-(3)), and the base and residual factors receive
+ * gradients through that product.  Forward and backward of one such projection (keys or
+ * values alike), by the plain definition and the chain rule:
+ *   K_h    = X W_h                          [n][H][d_h]
+ *   dX     = sum_h dK_h W_h^T               [n][d]
+ *   dW_s   = X^T sum_h dK_h                 [d][d_h]
+ *   dU_h   = X^T (dK_h B_h)                 [H][d][r]
+ *   dB_h   = dK_h^T (X U_h)                 [H][d_h][r]
+ * X [n][d], Ws [d][d_h], U [H][d][r], B [H][d_h][r], dK [n][H][d_h] (bf16); outputs fp64.
+ */
+void oracle_train_forward(int n, int d, int d_h, int H, int r, const uint16_t* X, const uint16_t* Ws,
+                          const uint16_t* U, const uint16_t* Bm, double* K) {
+    #pragma omp parallel for schedule(dynamic)
+    for (int h = 0; h < H; ++h) {
+        double* W = (double*)malloc(sizeof(double) * (size_t)d * d_h);
+        double* F = (double*)malloc(sizeof(double) * (size_t)n * d_h);
+        if (W && F) {
+            form_w_h(d, d_h, r, h, Ws, U, Bm, W);
+            project(n, d, d_h, X, W, F);
+            for (int t = 0; t < n; ++t)
+                for (int i = 0; i < d_h; ++i) K[((size_t)t * H + h) * d_h + i] = F[(size_t)t * d_h + i];
+        }
+        free(W); free(F);
+    }
+}
+
+void oracle_train_backward(int n, int d, int d_h, int H, int r, const uint16_t* X, const uint16_t* Ws,
+                           const uint16_t* U, const uint16_t* Bm, const uint16_t* dK, double* dX, double* dWs,
+                           double* dU, double* dB) {
+    /* dX = sum_h dK_h W_h^T, with W_h formed explicitly */
+    for (size_t i = 0; i < (size_t)n * d; ++i) dX[i] = 0.0;
+    double* W = (double*)malloc(sizeof(double) * (size_t)d * d_h);
+    for (int h = 0; h < H && W; ++h) {
+        form_w_h(d, d_h, r, h, Ws, U, Bm, W);
+        #pragma omp parallel for schedule(static)
+        for (int t = 0; t < n; ++t)
+            for (int k = 0; k < d; ++k) {
+                double acc = 0.0;
+                for (int i = 0; i < d_h; ++i) acc += bf(dK[((size_t)t * H + h) * d_h + i]) * W[(size_t)k * d_h + i];
+                dX[(size_t)t * d + k] += acc;
+            }
+    }
+    free(W);
+    /* dW_s = X^T sum_h dK_h */
+    #pragma omp parallel for schedule(static)
+    for (int k = 0; k < d; ++k)
+        for (int i = 0; i < d_h; ++i) {
+            double acc = 0.0;
+            for (int t = 0; t < n; ++t) {
+                double g = 0.0;
+                for (int h = 0; h < H; ++h) g += bf(dK[((size_t)t * H + h) * d_h + i]);
+                acc += bf(X[(size_t)t * d + k]) * g;
+            }
+            dWs[(size_t)k * d_h + i] = acc;
+        }
+    /* dU_h = X^T (dK_h B_h),  dB_h = dK_h^T (X U_h) */
+    #pragma omp parallel for schedule(dynamic)
+    for (int h = 0; h < H; ++h) {
+        double* dR = (double*)malloc(sizeof(double) * (size_t)n * r);
+        double* R = (double*)malloc(sizeof(double) * (size_t)n * r);
+        if (dR && R) {
+            for (int t = 0; t < n; ++t)
+                for (int j = 0; j < r; ++j) {
+                    double a = 0.0, c = 0.0;
+                    for (int i = 0; i < d_h; ++i) a += bf(dK[((size_t)t * H + h) * d_h + i]) * b_elem(Bm, h, d_h, r, i, j);
+                    for (int k = 0; k < d; ++k) c += bf(X[(size_t)t * d + k]) * bf(U[((size_t)h * d + k) * r + j]);
+                    dR[(size_t)t * r + j] = a;
+                    R[(size_t)t * r + j] = c;
+                }
+            for (int k = 0; k < d; ++k)
+                for (int j = 0; j < r; ++j) {
+                    double acc = 0.0;
+                    for (int t = 0; t < n; ++t) acc += bf(X[(size_t)t * d + k]) * dR[(size_t)t * r + j];
+                    dU[((size_t)h * d + k) * r + j] = acc;
+                }
+            for (int i = 0; i < d_h; ++i)
+                for (int j = 0; j < r; ++j) {
+                    double acc = 0.0;
+#if LRKV_ORACLE_MUTANT == 12
+                    for (int t = 0; t < n; ++t) acc += bf(dK[((size_t)t * H + h) * d_h + i]) * dR[(size_t)t * r + j]; /* planted */
+#else
+                    for (int t = 0; t < n; ++t) acc += bf(dK[((size_t)t * H + h) * d_h + i]) * R[(size_t)t * r + j];
+#endif
+                    dB[((size_t)h * d_h + i) * r + j] = acc;
+                }
+        }
+        free(dR); free(R);
+    }
 }

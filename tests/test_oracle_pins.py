@@ -466,13 +466,34 @@ def pin_mla_absorbed_equals_expanded(o):
     np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
 
 
+# ---------------------------------------------------------------------------- training
+def pin_train_is_autograd(o):
+    """The training projection K_h = X (W_s + U_h B_h^T) and its gradients: forward against a
+    direct fp64 evaluation, backward against torch autograd (fp64) of sum(dK * K) -- the
+    derivative of the definition, computed by a library, not by the oracle's formulas."""
+    n, d, d_h, H, r = 37, 24, 16, 3, 4
+    X = S.gaussian_bf16(51, "X", (n, d))
+    Ws = S.gaussian_bf16(51, "Ws", (d, d_h), d ** -0.5)
+    U = S.gaussian_bf16(51, "U", (H, d, r), d ** -0.5)
+    Bm = S.gaussian_bf16(51, "B", (H, d_h, r), r ** -0.5)
+    dK = S.gaussian_bf16(51, "dK", (n, H, d_h))
+    tX, tWs, tU, tB = (torch.from_numpy(f64(a)).requires_grad_(True) for a in (X, Ws, U, Bm))
+    W = tWs[None] + torch.einsum("hkj,hij->hki", tU, tB)        # [H, d, d_h]
+    K = torch.einsum("tk,hki->thi", tX, W)                       # [n, H, d_h]
+    np.testing.assert_allclose(o.train_forward(X, Ws, U, Bm), K.detach().numpy(), rtol=1e-12, atol=1e-12)
+    (K * torch.from_numpy(f64(dK))).sum().backward()
+    got = o.train_backward(X, Ws, U, Bm, dK)
+    for g_, ref in zip(got, (tX.grad, tWs.grad, tU.grad, tB.grad)):
+        np.testing.assert_allclose(g_, ref.numpy(), rtol=1e-11, atol=1e-11)
+
+
 PINS = [pin_softmax_worked_value, pin_softmax_normalised, pin_attend_special_cases,
         pin_append_integer_exact, pin_append_gaussian_rounding, pin_r0_is_mqa, pin_mha_special_case,
         pin_factored_equals_expanded, pin_cache_path_matches_weight_path,
         pin_head_permutation_equivariance, pin_page_permutation_invariance, pin_prefill_causal_edges,
         pin_fused_is_concatenated_attention, pin_fused_matches_factored_decode,
         pin_rope_append_is_rotation, pin_rope_attention_is_concatenated, pin_rotation_direction_worked_example,
-        pin_mla_absorbed_is_mqa, pin_mla_absorbed_equals_expanded]
+        pin_mla_absorbed_is_mqa, pin_mla_absorbed_equals_expanded, pin_train_is_autograd]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -486,7 +507,8 @@ def test_pin(pin, oracle_lib):
 #  7 absorbed decode drops the residual values z^V
 #  8 positional key rotated the wrong way    9 scale of the content width only with a positional key
 # 10 MLA scale over the cached row's width  11 MLA values read from the wrong slice of the row
-MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11]
+# 12 training: dB_h formed with dK_h B_h in place of X U_h
+MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
