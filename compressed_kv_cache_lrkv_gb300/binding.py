@@ -22,7 +22,8 @@ DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 EXPORTED = ["lrkv_abi_version", "lrkv_status_string", "lrkv_last_error", "lrkv_cache_block_bytes", "lrkv_append",
             "lrkv_decode_workspace_bytes", "lrkv_decode", "lrkv_decode_fused", "lrkv_decode_static_ws",
             "lrkv_prefill_workspace_bytes", "lrkv_prefill", "lrkv_mla_cache_block_bytes", "lrkv_mla_append",
-            "lrkv_mla_decode_workspace_bytes", "lrkv_mla_decode"]
+            "lrkv_mla_decode_workspace_bytes", "lrkv_mla_decode", "lrkv_train_forward", "lrkv_train_workspace_bytes",
+            "lrkv_train_backward"]
 STATIC_WS_BYTES = 16 << 20  # LRKV_STATIC_WS_BYTES
 
 
@@ -83,6 +84,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lrkv_prefill_workspace_bytes.argtypes = [P(Dims), i32, i32]
     lib.lrkv_prefill.restype = ctypes.c_int
     lib.lrkv_prefill.argtypes = [P(Dims), vp, vp, vp, P(Cache), vp, i32, vp, i32, i32, vp, vp, sz, vp, vp]
+    lib.lrkv_train_forward.restype = ctypes.c_int
+    lib.lrkv_train_forward.argtypes = [P(Dims), vp, vp, vp, i32, vp, vp, vp, vp]
+    lib.lrkv_train_workspace_bytes.restype = sz
+    lib.lrkv_train_workspace_bytes.argtypes = [P(Dims), i32]
+    lib.lrkv_train_backward.restype = ctypes.c_int
+    lib.lrkv_train_backward.argtypes = [P(Dims), vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp, vp]
     lib.lrkv_mla_cache_block_bytes.restype = sz
     lib.lrkv_mla_cache_block_bytes.argtypes = [P(MlaDims)]
     lib.lrkv_mla_append.restype = ctypes.c_int
@@ -217,6 +224,32 @@ def lrkv_prefill(dims: Dims, q, BK, BV, cache: PagedCache, block_table, q_start,
                              int(block_table.shape[1]), _ptr(q_start), B, Tq, _ptr(out), _ptr(workspace), ws_bytes,
                              _ptr(status), _stream(stream))
     _check(rc, "lrkv_prefill")
+
+
+def train_workspace_bytes(dims: Dims, n_tok: int) -> int:
+    return int(load().lrkv_train_workspace_bytes(ctypes.byref(dims), n_tok))
+
+
+def lrkv_train_forward(dims: Dims, X, W_T, B, Y, K, status=None, stream=None):
+    """Expanded projection: Y = X W_T^T = [S | R] ([n, d_h + H r]) and K = S + R_h B_h^T ([n, H, d_h])."""
+    rc = load().lrkv_train_forward(ctypes.byref(dims), _ptr(X), _ptr(W_T), _ptr(B), int(X.shape[0]), _ptr(Y),
+                                   _ptr(K), _ptr(status), _stream(stream))
+    _check(rc, "lrkv_train_forward")
+
+
+def lrkv_train_backward(dims: Dims, X, W_T, B, Y, dK, dX, dW_T, dB, workspace, status=None, stream=None):
+    """Gradients through K_h = X (W_shared + U_h B_h^T): dX [n, d], dW_T [d_h + H r, d], dB [H, d_h, r]."""
+    rc = load().lrkv_train_backward(ctypes.byref(dims), _ptr(X), _ptr(W_T), _ptr(B), _ptr(Y), _ptr(dK),
+                                    int(X.shape[0]), _ptr(dX), _ptr(dW_T), _ptr(dB), _ptr(workspace),
+                                    int(workspace.numel() * workspace.element_size()), _ptr(status),
+                                    _stream(stream))
+    _check(rc, "lrkv_train_backward")
+
+
+def pack_side_t(Ws, U) -> torch.Tensor:
+    """W_T [d_h + H r, d] of one projection from W_shared [d, d_h] and U [H, d, r]."""
+    H, d, r = U.shape
+    return torch.cat([Ws.t(), U.permute(0, 2, 1).reshape(H * r, d)], dim=0).contiguous()
 
 
 def mla_cache_block_bytes(dims: MlaDims) -> int:

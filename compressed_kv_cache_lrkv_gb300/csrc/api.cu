@@ -12,6 +12,7 @@
 
 #include "kernels.h"
 #include "mla.h"
+#include "train.h"
 
 namespace {
 
@@ -372,6 +373,129 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, c
     }
     return cuda_status(lrkv::launch_prefill(a, dims->d_h, dims->r, dims->d_rope, static_cast<cudaStream_t>(stream)),
                        "lrkv_prefill launch");
+}
+
+// ------------------------------------------------------------------ training-time projections
+static lrkv_status check_train(const lrkv_dims* dims, int32_t n_tok) {
+    lrkv_status s = check_dims(dims);
+    if (s != LRKV_OK) return s;
+    if (dims->d_rope != 0) return fail(LRKV_ERR_UNSUPPORTED, "training projections with d_rope %d", dims->d_rope);
+    if (n_tok < 0) return fail(LRKV_ERR_INVALID_ARG, "n_tok %d < 0", n_tok);
+    return LRKV_OK;
+}
+
+// Split-K factor of dB_h = dK_h^T R_h (a 128 x 128 tile per head over all tokens).
+static int train_dB_split(int H, int n_tok, int sms) {
+    int ks = (2 * sms + H - 1) / H;
+    const int maxk = (n_tok + 255) / 256;
+    ks = ks > maxk ? maxk : ks;
+    ks = ks > 8 ? 8 : ks;
+    return ks < 1 ? 1 : ks;
+}
+
+size_t lrkv_train_workspace_bytes(const lrkv_dims* dims, int32_t n_tok) {
+    if (check_train(dims, n_tok) != LRKV_OK) return 0;
+    DeviceInfo di;
+    if (device_info(&di) != LRKV_OK) return 0;
+    const size_t Ncat = (size_t)dims->d_h + (size_t)dims->H * dims->r;
+    const size_t gc = ((size_t)n_tok * Ncat * 2 + 255) & ~(size_t)255;
+    return gc + (size_t)dims->H * train_dB_split(dims->H, n_tok, di.sms) * 128 * 128 * 4;
+}
+
+lrkv_status lrkv_train_forward(const lrkv_dims* dims, const void* X, const void* W_T, const void* B, int32_t n_tok,
+                               void* Y, void* K, uint32_t* status_dev, void* stream) {
+    lrkv_status s = check_train(dims, n_tok);
+    if (s != LRKV_OK) return s;
+    if (n_tok == 0) return ok();
+    LRKV_REQUIRE_PTR(X);
+    LRKV_REQUIRE_PTR(W_T);
+    LRKV_REQUIRE_PTR(B);
+    LRKV_REQUIRE_PTR(Y);
+    LRKV_REQUIRE_PTR(K);
+    const int H = dims->H, d_h = dims->d_h, r = dims->r, d = dims->d, Ncat = d_h + H * r;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUtensorMap tX, tW, tY, tB;
+    if ((s = make_tmap(&tX, X, d, n_tok, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "X")) != LRKV_OK ||
+        (s = make_tmap(&tW, W_T, d, Ncat, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "W_T")) != LRKV_OK ||
+        (s = make_tmap(&tY, Y, Ncat, n_tok, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Y")) != LRKV_OK ||
+        (s = make_tmap(&tB, B, r, (uint64_t)H * d_h, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != LRKV_OK)
+        return s;
+    // Y = [S | R_1 .. R_H] = X W_T^T
+    lrkv::GemmArgs g{};
+    g.C = Y; g.ldc = Ncat; g.M = n_tok; g.N = Ncat; g.K = d; g.nbatch = 1; g.ksplit = 1; g.status = status_dev;
+    cudaError_t e = lrkv::launch_tgemm(tX, tW, g, false, false, false, st);
+    if (e != cudaSuccess) return cuda_status(e, "lrkv_train_forward launch");
+    // K_h = S + R_h B_h^T, one batch per head: A = R_h (Y columns d_h + h r ..), B = B_h as [d_h][r]
+    lrkv::GemmArgs x{};
+    x.C = K; x.ldc = H * d_h; x.c_zstride = d_h; x.M = n_tok; x.N = d_h; x.K = r;
+    x.a_x0 = d_h; x.a_zx = r; x.b_zy = d_h; x.nbatch = H; x.ksplit = 1;
+    x.add = static_cast<const uint16_t*>(Y); x.ld_add = Ncat; x.status = status_dev;
+    return cuda_status(lrkv::launch_tgemm(tY, tB, x, false, false, false, st), "lrkv_train_forward launch");
+}
+
+lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void* W_T, const void* B, const void* Y,
+                                const void* dK, int32_t n_tok, void* dX, void* dW_T, void* dB, void* workspace,
+                                size_t workspace_bytes, uint32_t* status_dev, void* stream) {
+    lrkv_status s = check_train(dims, n_tok);
+    if (s != LRKV_OK) return s;
+    if (n_tok == 0) return ok();
+    LRKV_REQUIRE_PTR(X);
+    LRKV_REQUIRE_PTR(W_T);
+    LRKV_REQUIRE_PTR(B);
+    LRKV_REQUIRE_PTR(Y);
+    LRKV_REQUIRE_PTR(dK);
+    LRKV_REQUIRE_PTR(dX);
+    LRKV_REQUIRE_PTR(dW_T);
+    LRKV_REQUIRE_PTR(dB);
+    DeviceInfo di;
+    if ((s = device_info(&di)) != LRKV_OK) return s;
+    const int H = dims->H, d_h = dims->d_h, r = dims->r, d = dims->d, Ncat = d_h + H * r;
+    const int ks = train_dB_split(H, n_tok, di.sms);
+    const size_t gc_bytes = ((size_t)n_tok * Ncat * 2 + 255) & ~(size_t)255;
+    const size_t need = gc_bytes + (size_t)H * ks * 128 * 128 * 4;
+    if (!workspace || ((uintptr_t)workspace & 255u))
+        return fail(LRKV_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+    if (workspace_bytes < need) return fail(LRKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+    uint16_t* Gc = static_cast<uint16_t*>(workspace);
+    float* P = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gc_bytes);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUtensorMap tdK_k, tdK_mn, tB_mn, tY_mn, tGc_mn, tGc_k, tX_mn, tW_mn;
+    const uint64_t HD = (uint64_t)H * d_h;
+    if ((s = make_tmap(&tdK_k, dK, HD, n_tok, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "dK")) != LRKV_OK ||
+        (s = make_tmap(&tdK_mn, dK, HD, n_tok, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "dK")) != LRKV_OK ||
+        (s = make_tmap(&tB_mn, B, r, HD, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != LRKV_OK ||
+        (s = make_tmap(&tY_mn, Y, Ncat, n_tok, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "Y")) != LRKV_OK ||
+        (s = make_tmap(&tGc_mn, Gc, Ncat, n_tok, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "Gc")) != LRKV_OK ||
+        (s = make_tmap(&tGc_k, Gc, Ncat, n_tok, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Gc")) != LRKV_OK ||
+        (s = make_tmap(&tX_mn, X, d, n_tok, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "X")) != LRKV_OK ||
+        (s = make_tmap(&tW_mn, W_T, d, Ncat, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "W_T")) != LRKV_OK)
+        return s;
+    cudaError_t e;
+    // Gc[:, 0:d_h] = G = sum_h dK_h
+    if ((e = lrkv::launch_head_sum(static_cast<const uint16_t*>(dK), Gc, n_tok, H, d_h, Ncat, st)) != cudaSuccess)
+        return cuda_status(e, "lrkv_train_backward launch");
+    // Gc[:, d_h + h r ..] = dR_h = dK_h B_h  (A = dK_h K-major, B = B_h read [d_h (K)][r (N)])
+    lrkv::GemmArgs g{};
+    g.C = Gc + d_h; g.ldc = Ncat; g.c_zstride = r; g.M = n_tok; g.N = r; g.K = d_h;
+    g.a_zx = d_h; g.b_zy = d_h; g.nbatch = H; g.ksplit = 1; g.status = status_dev;
+    if ((e = lrkv::launch_tgemm(tdK_k, tB_mn, g, false, true, false, st)) != cudaSuccess)
+        return cuda_status(e, "lrkv_train_backward launch");
+    // dB_h = dK_h^T R_h: split-K partials (A = dK read [n (K)][d_h (M)], B = R_h read [n (K)][r (N)])
+    g = lrkv::GemmArgs{};
+    g.C = P; g.M = d_h; g.N = r; g.K = n_tok; g.a_zx = d_h; g.b_x0 = d_h; g.b_zx = r; g.nbatch = H; g.ksplit = ks;
+    g.status = status_dev;
+    if ((e = lrkv::launch_tgemm(tdK_mn, tY_mn, g, true, true, true, st)) != cudaSuccess ||
+        (e = lrkv::launch_dB_reduce(P, static_cast<uint16_t*>(dB), H, ks, d_h, r, st)) != cudaSuccess)
+        return cuda_status(e, "lrkv_train_backward launch");
+    // dW_T = Gc^T X  ([d_h + H r][d]; A = Gc read [n (K)][Ncat (M)], B = X read [n (K)][d (N)])
+    g = lrkv::GemmArgs{};
+    g.C = dW_T; g.ldc = d; g.M = Ncat; g.N = d; g.K = n_tok; g.nbatch = 1; g.ksplit = 1; g.status = status_dev;
+    if ((e = lrkv::launch_tgemm(tGc_mn, tX_mn, g, true, true, false, st)) != cudaSuccess)
+        return cuda_status(e, "lrkv_train_backward launch");
+    // dX = Gc W_T  (A = Gc K-major, B = W_T read [Ncat (K)][d (N)])
+    g = lrkv::GemmArgs{};
+    g.C = dX; g.ldc = d; g.M = n_tok; g.N = d; g.K = Ncat; g.nbatch = 1; g.ksplit = 1; g.status = status_dev;
+    return cuda_status(lrkv::launch_tgemm(tGc_k, tW_mn, g, false, true, false, st), "lrkv_train_backward launch");
 }
 
 size_t lrkv_mla_cache_block_bytes(const lrkv_mla_dims* dims) {

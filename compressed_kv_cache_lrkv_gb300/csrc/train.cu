@@ -1,0 +1,255 @@
+// train.cu -- training-time forward and backward of one expanded LRKV projection
+// ("Low-Rank Key Value Attention", frame "Training learns the base and residuals together":
+// the full per-head features are materialised, K_h = X W_h with W_h = W_shared + U_h B_h^T,
+// Eqs. (2)-(3)).  Keys and values are the same operation with their own factors.
+//
+// Forward (W_T = [W_shared^T ; U_1^T ; ... ; U_H^T], [d_h + H r][d]):
+//   Y = X W_T^T = [S | R_1 .. R_H]            one GEMM, N = d_h + H r
+//   K_h = S + R_h B_h^T                          per head, K = r (B_h's box past r reads zeros)
+// Backward, for dK [n][H][d_h]:
+//   Gc = [G | dR_1 .. dR_H], G = sum_h dK_h, dR_h = dK_h B_h
+//   dB_h = dK_h^T R_h                            split-K over tokens, fp32 partials, ordered sum
+//   dW_T = Gc^T X                                (= [dW_shared^T ; dU_1^T ; ...]), K = n
+//   dX = Gc W_T                                  K = d_h + H r
+// All contractions run on tcgen05 (bf16 operands, fp32 accumulation in TMEM); S, R and Gc are
+// rounded to bf16 between the steps, as the inference cache rounds S and R.
+//
+// The GEMM kernel: one CTA per 128 x 128 output tile; warp 0 TMA producer (4-stage ring of
+// 64-wide K slices), warp 1 TMEM owner and single-thread MMA issue, warps 2-5 epilogue
+// (tcgen05.ld of their 32 TMEM lanes = tile rows).  All waits are bounded.
+#include "kernels.h"
+#include "lrkv_internal.cuh"
+#include "train.h"
+
+namespace lrkv {
+
+namespace {
+
+constexpr int kTM = 128, kTN = 128, kTK = 64, kTStages = 4;
+constexpr uint32_t T_A = kTM * kTK * 2, T_B = kTN * kTK * 2;  // 16 KiB each
+constexpr uint32_t kTSmem = kTStages * (T_A + T_B) + 256 + 1024;
+
+// K-major operand: rows x 64 K, 128-byte swizzle, 8-row groups 1 KiB apart.  MN-major operand:
+// two 64-wide blocks of [64 K rows][128 B], 8 KiB apart, 8-row K groups 1 KiB apart.
+__device__ __forceinline__ uint64_t kmaj(uint32_t a) { return sdesc(a, 16, 1024, 2); }
+__device__ __forceinline__ uint64_t mnmaj(uint32_t a) { return sdesc(a, 8192, 1024, 2); }
+
+}  // namespace
+
+template <bool AMN, bool BMN, bool OUTF32>
+__global__ void __launch_bounds__(192, 1)
+    tgemm_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB, const GemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sA = smem_u32(smem);
+    const uint32_t sB = sA + kTStages * T_A;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTStages * (T_A + T_B));
+    uint64_t* empty = full + kTStages;
+    uint64_t* accf = empty + kTStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    volatile int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kTN, m0 = blockIdx.y * kTM;
+    const int batch = blockIdx.z / g.ksplit, ks = blockIdx.z % g.ksplit;
+    const int KT_all = (g.K + kTK - 1) / kTK;
+    const int per = (KT_all + g.ksplit - 1) / g.ksplit;
+    const int kt0 = ks * per, kt1 = min(KT_all, kt0 + per);
+    const int KT = max(0, kt1 - kt0);
+    const int ax = g.a_x0 + batch * g.a_zx, ay = g.a_y0 + batch * g.a_zy;
+    const int bx = g.b_x0 + batch * g.b_zx, by = g.b_y0 + batch * g.b_zy;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(accf), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTN);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < KT; ++i) {
+                const int s = i % kTStages;
+                if (i >= kTStages && !mbar_wait(smem_u32(&empty[s]), ((i / kTStages) - 1) & 1, g.status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                const int k = (kt0 + i) * kTK;
+                const uint32_t bar = smem_u32(&full[s]);
+                mbar_arrive_expect_tx(bar, T_A + T_B);
+                if (AMN) {
+                    tma_load_2d(sA + s * T_A, &tA, ax + m0, ay + k, bar);
+                    tma_load_2d(sA + s * T_A + 8192, &tA, ax + m0 + 64, ay + k, bar);
+                } else {
+                    tma_load_2d(sA + s * T_A, &tA, ax + k, ay + m0, bar);
+                }
+                if (BMN) {
+                    tma_load_2d(sB + s * T_B, &tB, bx + n0, by + k, bar);
+                    tma_load_2d(sB + s * T_B + 8192, &tB, bx + n0 + 64, by + k, bar);
+                } else {
+                    tma_load_2d(sB + s * T_B, &tB, bx + k, by + n0, bar);
+                }
+                issued = i + 1;
+            }
+            if (*abort_flag)
+                for (int k = max(0, issued - kTStages); k < issued; ++k)
+                    mbar_wait(smem_u32(&full[k % kTStages]), (k / kTStages) & 1, g.status);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc =
+                idesc_bf16_f32(kTM, kTN) | ((AMN ? 1u : 0u) << 15) | ((BMN ? 1u : 0u) << 16);
+            for (int i = 0; i < KT; ++i) {
+                const int s = i % kTStages;
+                if (*abort_flag || !mbar_wait(smem_u32(&full[s]), (i / kTStages) & 1, g.status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTK / 16; ++kk) {
+                    // a K step of 16: 32 bytes along a K-major row, 16 rows (2 KiB) of an MN-major block
+                    const uint64_t ad = AMN ? mnmaj(sA + s * T_A + kk * 2048) : kmaj(sA + s * T_A + kk * 32);
+                    const uint64_t bd = BMN ? mnmaj(sB + s * T_B + kk * 2048) : kmaj(sB + s * T_B + kk * 32);
+                    tc_mma_bf16(tmem, ad, bd, idesc, (i | kk) != 0);
+                }
+                tc_commit(smem_u32(&empty[s]));
+            }
+            tc_commit(smem_u32(accf));  // fires once every issued MMA has completed
+        }
+    } else {
+        // epilogue: warps 2..5 -> TMEM lane quarters 2, 3, 0, 1
+        const int q = warp & 3;
+        bool ok = mbar_wait(smem_u32(accf), 0, g.status);
+        ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+        tc_fence_after();
+        if (ok) {
+            const int row = m0 + q * 32 + lane;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kTN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+                if (KT == 0)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                if (OUTF32) {
+                    // split-K partial of a single-tile product: [batch][ks][128][128] fp32
+                    float* dst = reinterpret_cast<float*>(g.C) +
+                                 (((size_t)blockIdx.z * kTM + (row - m0)) * kTN + c0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        reinterpret_cast<float4*>(dst)[i] =
+                            make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                        __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                } else if (row < g.M) {
+                    uint16_t* crow = reinterpret_cast<uint16_t*>(g.C) + batch * g.c_zstride + (size_t)row * g.ldc;
+#pragma unroll
+                    for (int gi = 0; gi < 4; ++gi) {
+                        const int col = n0 + c0 + gi * 8;
+                        if (col < g.N) {
+                            float f[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[gi * 8 + e]);
+                            if (g.add) {
+                                const uint4 s4 = *reinterpret_cast<const uint4*>(g.add + (size_t)row * g.ld_add + col);
+                                f[0] += bf16lo(s4.x); f[1] += bf16hi(s4.x); f[2] += bf16lo(s4.y); f[3] += bf16hi(s4.y);
+                                f[4] += bf16lo(s4.z); f[5] += bf16hi(s4.z); f[6] += bf16lo(s4.w); f[7] += bf16hi(s4.w);
+                            }
+                            uint4 pk;
+                            pk.x = pack_bf16x2(f[0], f[1]);
+                            pk.y = pack_bf16x2(f[2], f[3]);
+                            pk.z = pack_bf16x2(f[4], f[5]);
+                            pk.w = pack_bf16x2(f[6], f[7]);
+                            *reinterpret_cast<uint4*>(crow + col) = pk;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTN);
+    }
+}
+
+// G[t][e] = sum_h dK[t][h][e] (fp32, heads in order), eight columns per thread.
+__global__ void __launch_bounds__(256) head_sum_kernel(const uint16_t* dK, uint16_t* Gc, int n, int H, int d_h,
+                                                       int ldg) {
+    const int per_row = d_h / 8;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)n * per_row) return;
+    const int t = (int)(idx / per_row), c = (int)(idx % per_row) * 8;
+    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const uint16_t* src = dK + (size_t)t * H * d_h + c;
+    for (int h = 0; h < H; ++h) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(src + (size_t)h * d_h));
+        f[0] += bf16lo(x.x); f[1] += bf16hi(x.x); f[2] += bf16lo(x.y); f[3] += bf16hi(x.y);
+        f[4] += bf16lo(x.z); f[5] += bf16hi(x.z); f[6] += bf16lo(x.w); f[7] += bf16hi(x.w);
+    }
+    uint4 pk;
+    pk.x = pack_bf16x2(f[0], f[1]);
+    pk.y = pack_bf16x2(f[2], f[3]);
+    pk.z = pack_bf16x2(f[4], f[5]);
+    pk.w = pack_bf16x2(f[6], f[7]);
+    *reinterpret_cast<uint4*>(Gc + (size_t)t * ldg + c) = pk;
+}
+
+// dB[h][e][j] = sum_ks P[h][ks][e][j] in ks order, bf16.
+__global__ void __launch_bounds__(256) dB_reduce_kernel(const float* P, uint16_t* dB, int H, int ksplit, int d_h,
+                                                        int r) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)H * d_h * r) return;
+    const int h = (int)(idx / ((long long)d_h * r)), rem = (int)(idx % ((long long)d_h * r));
+    const int e = rem / r, j = rem % r;
+    float v = 0.f;
+    for (int ks = 0; ks < ksplit; ++ks) v += P[(((size_t)h * ksplit + ks) * kTM + e) * kTN + j];
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    dB[idx] = *reinterpret_cast<const uint16_t*>(&b);
+}
+
+cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& g, bool a_mn, bool b_mn,
+                         bool out_f32, cudaStream_t stream) {
+    const dim3 grid((g.N + kTN - 1) / kTN, (g.M + kTM - 1) / kTM, g.nbatch * g.ksplit);
+#define LRKV_TG(AM, BM, OF)                                                                                \
+    if (a_mn == AM && b_mn == BM && out_f32 == OF) {                                                       \
+        auto kern = tgemm_kernel<AM, BM, OF>;                                                              \
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);   \
+        if (e != cudaSuccess) return e;                                                                    \
+        kern<<<grid, 192, kTSmem, stream>>>(tA, tB, g);                                                     \
+        return cudaGetLastError();                                                                         \
+    }
+    LRKV_TG(false, false, false)
+    LRKV_TG(true, true, false)
+    LRKV_TG(false, true, false)
+    LRKV_TG(true, true, true)
+#undef LRKV_TG
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_head_sum(const uint16_t* dK, uint16_t* Gc, int n, int H, int d_h, int ldg, cudaStream_t stream) {
+    const long long total = (long long)n * (d_h / 8);
+    head_sum_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(dK, Gc, n, H, d_h, ldg);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dB_reduce(const float* P, uint16_t* dB, int H, int ksplit, int d_h, int r, cudaStream_t stream) {
+    const long long total = (long long)H * d_h * r;
+    dB_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(P, dB, H, ksplit, d_h, r);
+    return cudaGetLastError();
+}
+
+}  // namespace lrkv

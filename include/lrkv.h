@@ -227,6 +227,45 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, c
                          size_t workspace_bytes, uint32_t* status_dev, void* stream);
 
 /* ======================================================================
+ * Training-time expanded projections ("Low-Rank Key Value Attention", frame
+ * "Training learns the base and residuals together": the full per-head features
+ * are materialised during training).  One projection -- keys or values alike:
+ *   K_h = X W_h,  W_h = W_shared + U_h B_h^T                     (Eqs. (2)-(3))
+ * with its factors' gradients by the chain rule.  Dims as above (d_rope must be
+ * 0; block_size and softmax_scale are not used).  Layouts:
+ *   X    [n_tok][d]
+ *   W_T  [d_h + H r][d]   rows: W_shared^T (d_h rows), then U_1^T .. U_H^T (r rows each)
+ *   B    [H][d_h][r]
+ *   Y    [n_tok][d_h + H r]  = X W_T^T = [S | R_1 .. R_H], written by the forward
+ *        (bf16), read by the backward
+ *   K    [n_tok][H][d_h]   = S + R_h B_h^T
+ * All products on the tensor cores with fp32 accumulation; S, R and the backward's
+ * [G | dR] are rounded to bf16 between the steps; outputs bf16 (nearest even).
+ * n_tok == 0 is a no-op.  Every row count, d and d_h + H r are as in the ABI
+ * conventions (multiples of 8); r >= 8.
+ * ====================================================================== */
+
+/* Forward: Y and K. */
+lrkv_status lrkv_train_forward(const lrkv_dims* dims, const void* X, const void* W_T, const void* B, int32_t n_tok,
+                               void* Y, void* K, uint32_t* status_dev, void* stream);
+
+/* Workspace bytes lrkv_train_backward needs for n_tok rows on the CURRENT device. */
+size_t lrkv_train_workspace_bytes(const lrkv_dims* dims, int32_t n_tok);
+
+/*
+ * Backward for dK [n_tok][H][d_h]:
+ *   dX   [n_tok][d]       = sum_h dK_h W_h^T
+ *   dW_T [d_h + H r][d]   = [dW_shared^T ; dU_1^T ; ...] = [G | dR]^T X,
+ *                          G = sum_h dK_h, dR_h = dK_h B_h
+ *   dB   [H][d_h][r]      = dK_h^T R_h (split over tokens, partial sums added in a
+ *                          fixed order)
+ *   workspace >= lrkv_train_workspace_bytes(dims, n_tok) bytes, 256-byte aligned.
+ */
+lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void* W_T, const void* B, const void* Y,
+                                const void* dK, int32_t n_tok, void* dX, void* dW_T, void* dB, void* workspace,
+                                size_t workspace_bytes, uint32_t* status_dev, void* stream);
+
+/* ======================================================================
  * Multi-head latent attention (second workload on the same skeleton).
  *
  * "Embeddings II: MLA & Architectural Choices" (weight absorption, decoupled RoPE,
