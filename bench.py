@@ -49,6 +49,7 @@ from compressed_kv_cache_lrkv_gb300 import accounting as A  # noqa: E402
 
 METRIC_DECODE = "LRKV decode cache-read GB/s (% of GB300 HBM peak) and decode tokens/sec"
 METRIC_MLA = "MLA (absorbed) decode cache-read GB/s (% of GB300 HBM peak) and decode tokens/sec"
+METRIC_TRAIN = "LRKV expanded projection forward + backward TFLOP/s (bf16 tensor, fp32 accumulate)"
 METRIC_PREFILL = "LRKV chunked prefill + append prompt tokens/sec (bf16 tensor TFLOP/s of the prefill kernel)"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
@@ -554,8 +555,111 @@ class MlaHarness:
                           f"heads), {reps} repetitions in {dt:.1f} s; fp64, OpenMP over heads"}
 
 
+# ----------------------------------------------------------------------------- training projection
+class TrainHarness:
+    """One projection (keys or values) of a training step: lrkv_train_forward, then
+    lrkv_train_backward for a given dK."""
+
+    profile = "train_projection.md"
+    sources = ("train.cu", "train.h", "lrkv_internal.cuh", "kernels.h")
+
+    def __init__(self, wl, rank):
+        import torch
+
+        from compressed_kv_cache_lrkv_gb300 import binding as b
+        self.torch, self.b, self.wl = torch, b, wl
+        n, d, H, d_h, r = wl.B * wl.L, wl.d, wl.H, wl.d_h, wl.r
+        self.n = n
+        gen = torch.Generator(device="cuda").manual_seed(replica_seed(rank, 9012))
+        rn = lambda *s, scale=1.0: (torch.randn(*s, generator=gen, device="cuda") * scale).to(torch.bfloat16)
+        self.dims = b.make_dims(H, d_h, r, d)
+        N = d_h + H * r
+        self.X, self.Wt = rn(n, d), rn(N, d, scale=d ** -0.5)
+        self.B, self.dK = rn(H, d_h, r, scale=r ** -0.5), rn(n, H, d_h)
+        mk = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
+        self.Y, self.K = mk(n, N), mk(n, H, d_h)
+        self.dX, self.dWt, self.dB = mk(n, d), mk(N, d), mk(H, d_h, r)
+        self.ws = b.alloc_workspace(b.train_workspace_bytes(self.dims, n))
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fwd, bwd = A.train_flops(n, d, H, d_h, r)
+        self.kernel_units = bwd
+        self.step_units = fwd + bwd
+        self.fwd_units = fwd
+        self.launches_per_step = 2 + 5
+
+    def step(self, stream):
+        b = self.b
+        b.lrkv_train_forward(self.dims, self.X, self.Wt, self.B, self.Y, self.K, status=self.status, stream=stream)
+        b.lrkv_train_backward(self.dims, self.X, self.Wt, self.B, self.Y, self.dK, self.dX, self.dWt, self.dB,
+                              self.ws, status=self.status, stream=stream)
+
+    def kernel(self, stream):
+        self.b.lrkv_train_backward(self.dims, self.X, self.Wt, self.B, self.Y, self.dK, self.dX, self.dWt, self.dB,
+                                   self.ws, status=self.status, stream=stream)
+
+    def e2e_setup(self):
+        t = self.torch
+        self.h_in = [(x.cpu().pin_memory(), x) for x in (self.X, self.dK)]
+        self.h_out = [(t.empty_like(self.dB, device="cpu").pin_memory(), self.dB)]
+        return (sum(h.numel() * h.element_size() for h, _ in self.h_in),
+                sum(h.numel() * h.element_size() for h, _ in self.h_out))
+
+    def e2e_step(self, stream):
+        for h, d in self.h_in:
+            d.copy_(h, non_blocking=True)
+        self.step(stream)
+        for h, d in self.h_out:
+            h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    def report(self, step_s, kernel_s, e2e_s, world, peaks):
+        wl = self.wl
+        achieved = self.kernel_units / kernel_s / 1e12
+        return {
+            "metric": METRIC_TRAIN, "value": self.step_units * world / step_s / 1e12, "unit": "TFLOP/s",
+            "tokens_per_s": self.n * world / step_s,
+            "config": {"workload": f"{wl.key}: {wl.description}", "tokens": self.n, "H": wl.H, "d_h": wl.d_h,
+                       "r": wl.r, "d": wl.d, "flops_per_step": self.step_units, "forward_flops": self.fwd_units,
+                       "backward_flops": self.kernel_units,
+                       "l2": "activations (X, dK, Y, K, dX: 224 MiB) larger than L2",
+                       "step": "lrkv_train_forward (Y, K) + lrkv_train_backward (dX, dW_T, dB)",
+                       "parallelism": f"replicas x{world} (independent micro-batches)"},
+            "roofline": {"kernel": "lrkv_train_backward (head sum + 4 tcgen05 GEMM launches + dB reduce)",
+                         "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops"],
+                         "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                         "traffic": recorded_traffic(self.profile, self.sources),
+                         "algorithmic_flops_per_launch": self.kernel_units, "avg_launch_ms": kernel_s * 1e3},
+            "e2e_unit_value": lambda s: self.step_units * world / s / 1e12, "e2e_unit": "TFLOP/s",
+        }
+
+    def cpu_baseline(self, budget_s):
+        """fp64 oracle (forward + backward) on a 64-token sample of the workload's shape."""
+        import oracle
+        wl = self.wl
+        o = oracle.get()
+        n = 64
+        X = S.gaussian_bf16(wl.seed, "bl_X", (n, wl.d))
+        Ws = S.gaussian_bf16(wl.seed, "bl_Ws", (wl.d, wl.d_h), wl.d ** -0.5)
+        U = S.gaussian_bf16(wl.seed, "bl_U", (wl.H, wl.d, wl.r), wl.d ** -0.5)
+        Bm = S.gaussian_bf16(wl.seed, "bl_B", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
+        dK = S.gaussian_bf16(wl.seed, "bl_dK", (n, wl.H, wl.d_h))
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            o.train_forward(X, Ws, U, Bm)
+            o.train_backward(X, Ws, U, Bm, dK)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget_s:
+                break
+        f, bw = A.train_flops(n, wl.d, wl.H, wl.d_h, wl.r)
+        return {"value": (f + bw) * reps / dt / 1e12, "unit": "TFLOP/s", "cores": o.num_threads(), "kind": "oracle",
+                "sample": f"expanded projection forward + backward of {n} tokens at the workload's shape, "
+                          f"{reps} repetitions in {dt:.1f} s; fp64 (algorithmic flop count of the factored route)"}
+
+
 HARNESS = {"longctx": DecodeHarness, "dsv2": DecodeHarness, "backbone12": DecodeHarness, "small": DecodeHarness,
-           "prefill": PrefillHarness, "mla": MlaHarness}
+           "prefill": PrefillHarness, "mla": MlaHarness, "train": TrainHarness}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -678,7 +782,7 @@ def run_reference(args, world, rank):
         return
     import oracle
 
-    wl = S.WORKLOADS[args.workload if args.workload != "prefill" else "longctx"]
+    wl = S.WORKLOADS[args.workload if args.workload not in ("prefill", "train") else "longctx"]
     seq_lens = workload_seq_lens(wl)
     o = oracle.get()
     per_step_budget = max(0.01, 90.0 / max(args.steps + args.warmup, 1))

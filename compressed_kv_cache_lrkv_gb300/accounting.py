@@ -126,3 +126,15 @@ def mla_append_algorithmic_bytes(n_tok: int, d: int, d_c: int, d_rope: int) -> i
     """X in, [W^DKV | W^KR] in, cache rows out (bf16)."""
     N = d_c + d_rope
     return BF16_BYTES * (n_tok * d + d * N + n_tok * N)
+
+
+def train_flops(n_tok: int, d: int, H: int, d_h: int, r: int) -> tuple[int, int]:
+    """Multiply-adds x 2 of the expanded projection K_h = X (W_shared + U_h B_h^T) through the
+    factored route: forward X W_T^T (N = d_h + H r) and the per-head expansion R_h B_h^T; backward
+    dR_h = dK_h B_h, dB_h = dK_h^T R_h, dW_T = [G | dR]^T X and dX = [G | dR] W_T.
+    Returns (forward, backward)."""
+    N = d_h + H * r
+    head = 2 * n_tok * H * d_h * r
+    fwd = 2 * n_tok * d * N + head
+    bwd = 2 * head + 2 * (2 * n_tok * d * N)
+    return fwd, bwd

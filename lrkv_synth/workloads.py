@@ -51,6 +51,9 @@ WORKLOADS = {
     "mla": Workload("mla", "multi-head latent attention decode at DeepSeek-V2's attention shape (H=128, d_c=512, "
                     "d_h^R=64, d_h=128, d=5120), absorbed weights, batch 8, 16384 cached tokens, 64-token pages",
                     B=8, L=16384, H=128, d_h=128, r=0, d=5120, d_c=512, d_rope=64, seed=5),
+    "train": Workload("train", "training-time expanded projection forward + backward (one of K/V) at the 6.3B head "
+                      "shape d=4096, H=32, d_h=128, r=16, 8192 tokens (4 x 2048)",
+                      B=4, L=2048, H=32, d_h=128, r=16, d=4096, seed=6),
     "prefill": Workload("prefill", "causal chunked prefill + append d=4096, H=32, d_h=128, r=16, batch 2, 4096-token prompts, 512-token chunks",
                         B=2, L=4096, H=32, d_h=128, r=16, d=4096, chunk=512, seed=4),
 }
