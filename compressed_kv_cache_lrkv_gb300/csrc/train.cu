@@ -14,9 +14,11 @@
 // All contractions run on tcgen05 (bf16 operands, fp32 accumulation in TMEM); S, R and Gc are
 // rounded to bf16 between the steps, as the inference cache rounds S and R.
 //
-// The GEMM kernel: one CTA per 128 x 128 output tile; warp 0 TMA producer (4-stage ring of
-// 64-wide K slices), warp 1 TMEM owner and single-thread MMA issue, warps 2-5 epilogue
-// (tcgen05.ld of their 32 TMEM lanes = tile rows).  All waits are bounded.
+// The GEMM kernel is persistent (one CTA per SM looping over 128 x 128 output tiles): warp 0 TMA
+// producer (a 4-stage ring of 64-wide K slices, continuous across tiles), warp 1 TMEM owner and
+// single-thread MMA issue into one of two accumulator buffers, warps 2-5 epilogue (tcgen05.ld of
+// their 32 TMEM lanes = tile rows), so a tile's epilogue overlaps the next tile's MMAs.  All
+// waits are bounded.
 #include "kernels.h"
 #include "lrkv_internal.cuh"
 #include "train.h"
@@ -46,30 +48,45 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t sB = sA + kTStages * T_A;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTStages * (T_A + T_B));
     uint64_t* empty = full + kTStages;
-    uint64_t* accf = empty + kTStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    uint64_t* acc_full = empty + kTStages;  // [2] accumulator buffer holds a finished tile
+    uint64_t* acc_empty = acc_full + 2;     // [2] the epilogue has read it (128 arrivals)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kTN, m0 = blockIdx.y * kTM;
-    const int batch = blockIdx.z / g.ksplit, ks = blockIdx.z % g.ksplit;
+    const int tiles_n = (g.N + kTN - 1) / kTN, tiles_m = (g.M + kTM - 1) / kTM;
+    const int total = tiles_n * tiles_m * g.nbatch * g.ksplit;
     const int KT_all = (g.K + kTK - 1) / kTK;
     const int per = (KT_all + g.ksplit - 1) / g.ksplit;
-    const int kt0 = ks * per, kt1 = min(KT_all, kt0 + per);
-    const int KT = max(0, kt1 - kt0);
-    const int ax = g.a_x0 + batch * g.a_zx, ay = g.a_y0 + batch * g.a_zy;
-    const int bx = g.b_x0 + batch * g.b_zx, by = g.b_y0 + batch * g.b_zy;
+    // tile -> (n tile, m tile, batch, k split); n fastest, so consecutive CTAs share A rows in L2
+    struct Tile {
+        int n0, m0, z, batch, kt0, KT;
+    };
+    auto tile_of = [&](int t) {
+        Tile r;
+        r.n0 = (t % tiles_n) * kTN;
+        r.m0 = ((t / tiles_n) % tiles_m) * kTM;
+        r.z = t / (tiles_n * tiles_m);
+        r.batch = r.z / g.ksplit;
+        const int ks = r.z % g.ksplit;
+        r.kt0 = ks * per;
+        r.KT = max(0, min(KT_all, r.kt0 + per) - r.kt0);
+        return r;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
-        mbar_init(smem_u32(accf), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), 128);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTN);
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 2 * kTN);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -77,86 +94,113 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            int issued = 0;
-            for (int i = 0; i < KT; ++i) {
-                const int s = i % kTStages;
-                if (i >= kTStages && !mbar_wait(smem_u32(&empty[s]), ((i / kTStages) - 1) & 1, g.status)) {
-                    *abort_flag = 1;
-                    break;
+            int q = 0;  // K slices issued by this CTA (ring position and phase)
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile tl = tile_of(t);
+                const int ax = g.a_x0 + tl.batch * g.a_zx, ay = g.a_y0 + tl.batch * g.a_zy;
+                const int bx = g.b_x0 + tl.batch * g.b_zx, by = g.b_y0 + tl.batch * g.b_zy;
+                for (int i = 0; i < tl.KT; ++i, ++q) {
+                    const int s = q % kTStages;
+                    if ((q >= kTStages && !mbar_wait(smem_u32(&empty[s]), ((q / kTStages) - 1) & 1, g.status)) ||
+                        *abort_flag) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    const int k = (tl.kt0 + i) * kTK;
+                    const uint32_t bar = smem_u32(&full[s]);
+                    mbar_arrive_expect_tx(bar, T_A + T_B);
+                    if (AMN) {
+                        tma_load_2d(sA + s * T_A, &tA, ax + tl.m0, ay + k, bar);
+                        tma_load_2d(sA + s * T_A + 8192, &tA, ax + tl.m0 + 64, ay + k, bar);
+                    } else {
+                        tma_load_2d(sA + s * T_A, &tA, ax + k, ay + tl.m0, bar);
+                    }
+                    if (BMN) {
+                        tma_load_2d(sB + s * T_B, &tB, bx + tl.n0, by + k, bar);
+                        tma_load_2d(sB + s * T_B + 8192, &tB, bx + tl.n0 + 64, by + k, bar);
+                    } else {
+                        tma_load_2d(sB + s * T_B, &tB, bx + k, by + tl.n0, bar);
+                    }
                 }
-                if (*abort_flag) break;
-                const int k = (kt0 + i) * kTK;
-                const uint32_t bar = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(bar, T_A + T_B);
-                if (AMN) {
-                    tma_load_2d(sA + s * T_A, &tA, ax + m0, ay + k, bar);
-                    tma_load_2d(sA + s * T_A + 8192, &tA, ax + m0 + 64, ay + k, bar);
-                } else {
-                    tma_load_2d(sA + s * T_A, &tA, ax + k, ay + m0, bar);
-                }
-                if (BMN) {
-                    tma_load_2d(sB + s * T_B, &tB, bx + n0, by + k, bar);
-                    tma_load_2d(sB + s * T_B + 8192, &tB, bx + n0 + 64, by + k, bar);
-                } else {
-                    tma_load_2d(sB + s * T_B, &tB, bx + k, by + n0, bar);
-                }
-                issued = i + 1;
             }
-            if (*abort_flag)
-                for (int k = max(0, issued - kTStages); k < issued; ++k)
+            if (!ok)  // let the copies in flight land before the CTA exits
+                for (int k = max(0, q - kTStages); k < q; ++k)
                     mbar_wait(smem_u32(&full[k % kTStages]), (k / kTStages) & 1, g.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc =
                 idesc_bf16_f32(kTM, kTN) | ((AMN ? 1u : 0u) << 15) | ((BMN ? 1u : 0u) << 16);
-            for (int i = 0; i < KT; ++i) {
-                const int s = i % kTStages;
-                if (*abort_flag || !mbar_wait(smem_u32(&full[s]), (i / kTStages) & 1, g.status)) {
-                    *abort_flag = 1;
+            int q = 0, it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+                const Tile tl = tile_of(t);
+                const int buf = it & 1;
+                // the epilogue must have read this buffer's previous tile
+                if (it >= 2 && !mbar_wait(smem_u32(&acc_empty[buf]), ((it >> 1) - 1) & 1, g.status)) {
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t acc = tmem + buf * kTN;
+                for (int i = 0; i < tl.KT; ++i, ++q) {
+                    const int s = q % kTStages;
+                    if (*abort_flag || !mbar_wait(smem_u32(&full[s]), (q / kTStages) & 1, g.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kTK / 16; ++kk) {
-                    // a K step of 16: 32 bytes along a K-major row, 16 rows (2 KiB) of an MN-major block
-                    const uint64_t ad = AMN ? mnmaj(sA + s * T_A + kk * 2048) : kmaj(sA + s * T_A + kk * 32);
-                    const uint64_t bd = BMN ? mnmaj(sB + s * T_B + kk * 2048) : kmaj(sB + s * T_B + kk * 32);
-                    tc_mma_bf16(tmem, ad, bd, idesc, (i | kk) != 0);
+                    for (int kk = 0; kk < kTK / 16; ++kk) {
+                        // a K step of 16: 32 bytes along a K-major row, 16 rows (2 KiB) of an MN-major block
+                        const uint64_t ad = AMN ? mnmaj(sA + s * T_A + kk * 2048) : kmaj(sA + s * T_A + kk * 32);
+                        const uint64_t bd = BMN ? mnmaj(sB + s * T_B + kk * 2048) : kmaj(sB + s * T_B + kk * 32);
+                        tc_mma_bf16(acc, ad, bd, idesc, (i | kk) != 0);
+                    }
+                    tc_commit(smem_u32(&empty[s]));
                 }
-                tc_commit(smem_u32(&empty[s]));
+                if (!ok) break;
+                tc_commit(smem_u32(&acc_full[buf]));  // fires once this tile's MMAs have completed
             }
-            tc_commit(smem_u32(accf));  // fires once every issued MMA has completed
+            if (!ok) *abort_flag = 1;
         }
     } else {
         // epilogue: warps 2..5 -> TMEM lane quarters 2, 3, 0, 1
-        const int q = warp & 3;
-        bool ok = mbar_wait(smem_u32(accf), 0, g.status);
-        ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-        tc_fence_after();
-        if (ok) {
-            const int row = m0 + q * 32 + lane;
+        const int q4 = warp & 3;
+        int it = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const Tile tl = tile_of(t);
+            const int buf = it & 1;
+            bool ok = !*abort_flag && mbar_wait(smem_u32(&acc_full[buf]), (it >> 1) & 1, g.status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0) *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const int row = tl.m0 + q4 * 32 + lane;
 #pragma unroll 1
             for (int c0 = 0; c0 < kTN; c0 += 32) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
-                if (KT == 0)
+                tmem_ld_32x32b_x32(tmem + buf * kTN + ((uint32_t)(q4 * 32) << 16) + c0, v);
+                if (tl.KT == 0)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = 0u;
                 if (OUTF32) {
                     // split-K partial of a single-tile product: [batch][ks][128][128] fp32
-                    float* dst = reinterpret_cast<float*>(g.C) +
-                                 (((size_t)blockIdx.z * kTM + (row - m0)) * kTN + c0);
+                    float* dst = reinterpret_cast<float*>(g.C) + (((size_t)tl.z * kTM + (row - tl.m0)) * kTN + c0);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         reinterpret_cast<float4*>(dst)[i] =
                             make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                         __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
                 } else if (row < g.M) {
-                    uint16_t* crow = reinterpret_cast<uint16_t*>(g.C) + batch * g.c_zstride + (size_t)row * g.ldc;
+                    uint16_t* crow = reinterpret_cast<uint16_t*>(g.C) + tl.batch * g.c_zstride + (size_t)row * g.ldc;
 #pragma unroll
                     for (int gi = 0; gi < 4; ++gi) {
-                        const int col = n0 + c0 + gi * 8;
+                        const int col = tl.n0 + c0 + gi * 8;
                         if (col < g.N) {
                             float f[8];
 #pragma unroll
@@ -176,13 +220,15 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&acc_empty[buf]));
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTN);
+        tmem_dealloc(tmem, 2 * kTN);
     }
 }
 
@@ -223,7 +269,11 @@ __global__ void __launch_bounds__(256) dB_reduce_kernel(const float* P, uint16_t
 
 cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& g, bool a_mn, bool b_mn,
                          bool out_f32, cudaStream_t stream) {
-    const dim3 grid((g.N + kTN - 1) / kTN, (g.M + kTM - 1) / kTM, g.nbatch * g.ksplit);
+    // persistent: one CTA per SM (the ring takes 128 KiB of shared memory) looping over the tiles
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long tiles = (long long)((g.N + kTN - 1) / kTN) * ((g.M + kTM - 1) / kTM) * g.nbatch * g.ksplit;
+    const dim3 grid((unsigned)(tiles < sms ? tiles : sms));
 #define LRKV_TG(AM, BM, OF)                                                                                \
     if (a_mn == AM && b_mn == BM && out_f32 == OF) {                                                       \
         auto kern = tgemm_kernel<AM, BM, OF>;                                                              \
