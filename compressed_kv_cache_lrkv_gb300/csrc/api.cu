@@ -402,6 +402,45 @@ size_t lrkv_train_workspace_bytes(const lrkv_dims* dims, int32_t n_tok) {
     return gc + (size_t)dims->H * train_dB_split(dims->H, n_tok, di.sms) * 128 * 128 * 4;
 }
 
+// Output and added-matrix maps of a tcgen05 GEMM: set g->tma_out when the output (and `add`) can
+// go through TMA (16-byte aligned base and strides), else the epilogue stores directly.
+static void train_out_maps(lrkv::GemmArgs* g, CUtensorMap* tC, CUtensorMap* tAdd) {
+    g->tma_out = 0;
+    const uint64_t zs = g->nbatch > 1 ? (uint64_t)g->c_zstride * 2 : (uint64_t)g->ldc * 2;
+    if (((uintptr_t)g->C & 15u) || ((uint64_t)g->ldc * 2) % 16 || zs % 16 || zs == 0) return;
+    if (g->add && (((uintptr_t)g->add & 15u) || ((uint64_t)g->ld_add * 2) % 16)) return;
+    auto enc = encode_fn();
+    if (!enc) return;
+    cuuint64_t dims[3] = {(cuuint64_t)g->N, (cuuint64_t)g->nbatch, (cuuint64_t)g->M};
+    cuuint64_t strides[2] = {zs, (cuuint64_t)g->ldc * 2};
+    cuuint32_t box[3] = {32, 1, 32};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(tC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, g->C, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return;
+    if (g->add) {
+        cuuint64_t ad[2] = {(cuuint64_t)g->N, (cuuint64_t)g->M};
+        cuuint64_t as[1] = {(cuuint64_t)g->ld_add * 2};
+        cuuint32_t ab[2] = {32, 32};
+        if (enc(tAdd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(g->add), ad, as, ab, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return;
+    } else {
+        *tAdd = *tC;  // unused
+    }
+    g->tma_out = 1;
+}
+
+// C = A . B on the tensor cores (see train.h); bf16 outputs go through TMA when they can.
+static cudaError_t train_gemm(const CUtensorMap& tA, const CUtensorMap& tB, lrkv::GemmArgs g, int bn, bool a_mn,
+                              bool b_mn, bool out_f32, cudaStream_t st) {
+    CUtensorMap tC = tA, tAdd = tA;
+    if (!out_f32) train_out_maps(&g, &tC, &tAdd);
+    return lrkv::launch_tgemm(tA, tB, tC, tAdd, g, bn, a_mn, b_mn, out_f32, st);
+}
+
 lrkv_status lrkv_train_forward(const lrkv_dims* dims, const void* X, const void* W_T, const void* B, int32_t n_tok,
                                void* Y, void* K, uint32_t* status_dev, void* stream) {
     lrkv_status s = check_train(dims, n_tok);
@@ -416,21 +455,21 @@ lrkv_status lrkv_train_forward(const lrkv_dims* dims, const void* X, const void*
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     CUtensorMap tX, tW, tY, tB;
     if ((s = make_tmap(&tX, X, d, n_tok, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "X")) != LRKV_OK ||
-        (s = make_tmap(&tW, W_T, d, Ncat, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "W_T")) != LRKV_OK ||
+        (s = make_tmap(&tW, W_T, d, Ncat, 64, 160, CU_TENSOR_MAP_SWIZZLE_128B, "W_T")) != LRKV_OK ||
         (s = make_tmap(&tY, Y, Ncat, n_tok, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Y")) != LRKV_OK ||
         (s = make_tmap(&tB, B, r, (uint64_t)H * d_h, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != LRKV_OK)
         return s;
     // Y = [S | R_1 .. R_H] = X W_T^T
     lrkv::GemmArgs g{};
     g.C = Y; g.ldc = Ncat; g.M = n_tok; g.N = Ncat; g.K = d; g.nbatch = 1; g.ksplit = 1; g.status = status_dev;
-    cudaError_t e = lrkv::launch_tgemm(tX, tW, g, false, false, false, st);
+    cudaError_t e = train_gemm(tX, tW, g, 160, false, false, false, st);
     if (e != cudaSuccess) return cuda_status(e, "lrkv_train_forward launch");
     // K_h = S + R_h B_h^T, one batch per head: A = R_h (Y columns d_h + h r ..), B = B_h as [d_h][r]
     lrkv::GemmArgs x{};
     x.C = K; x.ldc = H * d_h; x.c_zstride = d_h; x.M = n_tok; x.N = d_h; x.K = r;
     x.a_x0 = d_h; x.a_zx = r; x.b_zy = d_h; x.nbatch = H; x.ksplit = 1;
     x.add = static_cast<const uint16_t*>(Y); x.ld_add = Ncat; x.status = status_dev;
-    return cuda_status(lrkv::launch_tgemm(tY, tB, x, false, false, false, st), "lrkv_train_forward launch");
+    return cuda_status(train_gemm(tY, tB, x, 128, false, false, false, st), "lrkv_train_forward launch");
 }
 
 lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void* W_T, const void* B, const void* Y,
@@ -478,24 +517,24 @@ lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void
     lrkv::GemmArgs g{};
     g.C = Gc + d_h; g.ldc = Ncat; g.c_zstride = r; g.M = n_tok; g.N = r; g.K = d_h;
     g.a_zx = d_h; g.b_zy = d_h; g.nbatch = H; g.ksplit = 1; g.status = status_dev;
-    if ((e = lrkv::launch_tgemm(tdK_k, tB_mn, g, false, true, false, st)) != cudaSuccess)
+    if ((e = train_gemm(tdK_k, tB_mn, g, 128, false, true, false, st)) != cudaSuccess)
         return cuda_status(e, "lrkv_train_backward launch");
     // dB_h = dK_h^T R_h: split-K partials (A = dK read [n (K)][d_h (M)], B = R_h read [n (K)][r (N)])
     g = lrkv::GemmArgs{};
     g.C = P; g.M = d_h; g.N = r; g.K = n_tok; g.a_zx = d_h; g.b_x0 = d_h; g.b_zx = r; g.nbatch = H; g.ksplit = ks;
     g.status = status_dev;
-    if ((e = lrkv::launch_tgemm(tdK_mn, tY_mn, g, true, true, true, st)) != cudaSuccess ||
+    if ((e = train_gemm(tdK_mn, tY_mn, g, 128, true, true, true, st)) != cudaSuccess ||
         (e = lrkv::launch_dB_reduce(P, static_cast<uint16_t*>(dB), H, ks, d_h, r, st)) != cudaSuccess)
         return cuda_status(e, "lrkv_train_backward launch");
     // dW_T = Gc^T X  ([d_h + H r][d]; A = Gc read [n (K)][Ncat (M)], B = X read [n (K)][d (N)])
     g = lrkv::GemmArgs{};
     g.C = dW_T; g.ldc = d; g.M = Ncat; g.N = d; g.K = n_tok; g.nbatch = 1; g.ksplit = 1; g.status = status_dev;
-    if ((e = lrkv::launch_tgemm(tGc_mn, tX_mn, g, true, true, false, st)) != cudaSuccess)
+    if ((e = train_gemm(tGc_mn, tX_mn, g, 256, true, true, false, st)) != cudaSuccess)
         return cuda_status(e, "lrkv_train_backward launch");
     // dX = Gc W_T  (A = Gc K-major, B = W_T read [Ncat (K)][d (N)])
     g = lrkv::GemmArgs{};
     g.C = dX; g.ldc = d; g.M = n_tok; g.N = d; g.K = Ncat; g.nbatch = 1; g.ksplit = 1; g.status = status_dev;
-    return cuda_status(lrkv::launch_tgemm(tGc_k, tW_mn, g, false, true, false, st), "lrkv_train_backward launch");
+    return cuda_status(train_gemm(tGc_k, tW_mn, g, 256, false, true, false, st), "lrkv_train_backward launch");
 }
 
 size_t lrkv_mla_cache_block_bytes(const lrkv_mla_dims* dims) {

@@ -15,10 +15,12 @@
 // rounded to bf16 between the steps, as the inference cache rounds S and R.
 //
 // The GEMM kernel is persistent (one CTA per SM looping over 128 x 128 output tiles): warp 0 TMA
-// producer (a 4-stage ring of 64-wide K slices, continuous across tiles), warp 1 TMEM owner and
+// producer (a 6-stage ring of 64-wide K slices, continuous across tiles), warp 1 TMEM owner and
 // single-thread MMA issue into one of two accumulator buffers, warps 2-5 epilogue (tcgen05.ld of
-// their 32 TMEM lanes = tile rows), so a tile's epilogue overlaps the next tile's MMAs.  All
-// waits are bounded.
+// their 32 TMEM lanes = tile rows), so a tile's epilogue overlaps the next tile's MMAs.  A bf16
+// tile leaves through shared memory: each epilogue warp writes its 32 rows into 32 x 32 boxes
+// (64-byte swizzle, conflict-free 16-byte stores) and one lane issues their TMA stores; an added
+// matrix comes in the same way.  All waits are bounded.
 #include "kernels.h"
 #include "lrkv_internal.cuh"
 #include "train.h"
@@ -27,34 +29,59 @@ namespace lrkv {
 
 namespace {
 
-constexpr int kTM = 128, kTN = 128, kTK = 64, kTStages = 4;
-constexpr uint32_t T_A = kTM * kTK * 2, T_B = kTN * kTK * 2;  // 16 KiB each
-constexpr uint32_t kTSmem = kTStages * (T_A + T_B) + 256 + 1024;
+constexpr int kTM = 128, kTK = 64;
+constexpr uint32_t T_A = kTM * kTK * 2;  // 16 KiB: 128 rows x 64 K
+constexpr uint32_t kTBox = 2048;         // staging box: 32 rows x 32 bf16 columns (64 bytes)
+constexpr uint32_t kTSmemMax = 232448;   // opt-in shared memory per block
+
+// Per output-tile width BN: bytes of one B slice, staging boxes per epilogue warp (two tiles'
+// worth when an added matrix is prefetched, BN = 128), ring depth, TMEM columns.
+template <int BN>
+struct TCfg {
+    static constexpr uint32_t B = (uint32_t)BN * kTK * 2;
+    static constexpr int NBOX = BN == 128 ? 8 : 4;
+    static constexpr uint32_t STG = 4u * NBOX * kTBox;
+    static constexpr int S0 = (int)((kTSmemMax - 1280 - STG) / (T_A + B));
+    static constexpr int STAGES = S0 > 8 ? 8 : S0;
+    static constexpr uint32_t SMEM = STAGES * (T_A + B) + STG + 256 + 1024;
+    static constexpr uint32_t TMEM = 2 * BN <= 256 ? 256 : 512;
+};
 
 // K-major operand: rows x 64 K, 128-byte swizzle, 8-row groups 1 KiB apart.  MN-major operand:
-// two 64-wide blocks of [64 K rows][128 B], 8 KiB apart, 8-row K groups 1 KiB apart.
+// 64-wide blocks of [64 K rows][128 B], 8 KiB apart, 8-row K groups 1 KiB apart.
 __device__ __forceinline__ uint64_t kmaj(uint32_t a) { return sdesc(a, 16, 1024, 2); }
 __device__ __forceinline__ uint64_t mnmaj(uint32_t a) { return sdesc(a, 8192, 1024, 2); }
 
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 }  // namespace
 
-template <bool AMN, bool BMN, bool OUTF32>
+template <bool AMN, bool BMN, bool OUTF32, int BN>
 __global__ void __launch_bounds__(192, 1)
-    tgemm_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB, const GemmArgs g) {
+    tgemm_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
+                 const __grid_constant__ CUtensorMap tC, const __grid_constant__ CUtensorMap tAdd, const GemmArgs g) {
+    using C = TCfg<BN>;
+    constexpr int kS = C::STAGES, NBOX = C::NBOX;
+    constexpr uint32_t T_B = C::B;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
     const uint32_t sA = smem_u32(smem);
-    const uint32_t sB = sA + kTStages * T_A;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTStages * (T_A + T_B));
-    uint64_t* empty = full + kTStages;
-    uint64_t* acc_full = empty + kTStages;  // [2] accumulator buffer holds a finished tile
-    uint64_t* acc_empty = acc_full + 2;     // [2] the epilogue has read it (128 arrivals)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    const uint32_t sB = sA + kS * T_A;
+    uint8_t* stg_base = smem + kS * (T_A + T_B);  // epilogue staging, 1 KiB aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(stg_base + C::STG);
+    uint64_t* empty = full + kS;
+    uint64_t* acc_full = empty + kS;      // [2] accumulator buffer holds a finished tile
+    uint64_t* acc_empty = acc_full + 2;   // [2] the epilogue has read it (128 arrivals)
+    uint64_t* add_full = acc_empty + 2;   // [4][2] an epilogue warp's added boxes (per tile parity)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(add_full + 8);
     volatile int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_n = (g.N + kTN - 1) / kTN, tiles_m = (g.M + kTM - 1) / kTM;
+    const int tiles_n = (g.N + BN - 1) / BN, tiles_m = (g.M + kTM - 1) / kTM;
     const int total = tiles_n * tiles_m * g.nbatch * g.ksplit;
     const int KT_all = (g.K + kTK - 1) / kTK;
     const int per = (KT_all + g.ksplit - 1) / g.ksplit;
@@ -64,7 +91,7 @@ __global__ void __launch_bounds__(192, 1)
     };
     auto tile_of = [&](int t) {
         Tile r;
-        r.n0 = (t % tiles_n) * kTN;
+        r.n0 = (t % tiles_n) * BN;
         r.m0 = ((t / tiles_n) % tiles_m) * kTM;
         r.z = t / (tiles_n * tiles_m);
         r.batch = r.z / g.ksplit;
@@ -75,7 +102,7 @@ __global__ void __launch_bounds__(192, 1)
     };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTStages; ++s) {
+        for (int s = 0; s < kS; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
@@ -83,10 +110,11 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(smem_u32(&acc_full[b]), 1);
             mbar_init(smem_u32(&acc_empty[b]), 128);
         }
+        for (int w = 0; w < 8; ++w) mbar_init(smem_u32(&add_full[w]), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 2 * kTN);
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -101,9 +129,8 @@ __global__ void __launch_bounds__(192, 1)
                 const int ax = g.a_x0 + tl.batch * g.a_zx, ay = g.a_y0 + tl.batch * g.a_zy;
                 const int bx = g.b_x0 + tl.batch * g.b_zx, by = g.b_y0 + tl.batch * g.b_zy;
                 for (int i = 0; i < tl.KT; ++i, ++q) {
-                    const int s = q % kTStages;
-                    if ((q >= kTStages && !mbar_wait(smem_u32(&empty[s]), ((q / kTStages) - 1) & 1, g.status)) ||
-                        *abort_flag) {
+                    const int s = q % kS;
+                    if ((q >= kS && !mbar_wait(smem_u32(&empty[s]), ((q / kS) - 1) & 1, g.status)) || *abort_flag) {
                         *abort_flag = 1;
                         ok = false;
                         break;
@@ -118,21 +145,20 @@ __global__ void __launch_bounds__(192, 1)
                         tma_load_2d(sA + s * T_A, &tA, ax + k, ay + tl.m0, bar);
                     }
                     if (BMN) {
-                        tma_load_2d(sB + s * T_B, &tB, bx + tl.n0, by + k, bar);
-                        tma_load_2d(sB + s * T_B + 8192, &tB, bx + tl.n0 + 64, by + k, bar);
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j) tma_load_2d(sB + s * T_B + j * 8192, &tB, bx + tl.n0 + 64 * j, by + k, bar);
                     } else {
-                        tma_load_2d(sB + s * T_B, &tB, bx + k, by + tl.n0, bar);
+                        tma_load_2d(sB + s * T_B, &tB, bx + k, by + tl.n0, bar);  // one [BN][64] box
                     }
                 }
             }
             if (!ok)  // let the copies in flight land before the CTA exits
-                for (int k = max(0, q - kTStages); k < q; ++k)
-                    mbar_wait(smem_u32(&full[k % kTStages]), (k / kTStages) & 1, g.status);
+                for (int k = max(0, q - kS); k < q; ++k) mbar_wait(smem_u32(&full[k % kS]), (k / kS) & 1, g.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc =
-                idesc_bf16_f32(kTM, kTN) | ((AMN ? 1u : 0u) << 15) | ((BMN ? 1u : 0u) << 16);
+                idesc_bf16_f32(kTM, BN) | ((AMN ? 1u : 0u) << 15) | ((BMN ? 1u : 0u) << 16);
             int q = 0, it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
@@ -144,10 +170,10 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t acc = tmem + buf * kTN;
+                const uint32_t acc = tmem + buf * BN;
                 for (int i = 0; i < tl.KT; ++i, ++q) {
-                    const int s = q % kTStages;
-                    if (*abort_flag || !mbar_wait(smem_u32(&full[s]), (q / kTStages) & 1, g.status)) {
+                    const int s = q % kS;
+                    if (*abort_flag || !mbar_wait(smem_u32(&full[s]), (q / kS) & 1, g.status)) {
                         ok = false;
                         break;
                     }
@@ -167,30 +193,86 @@ __global__ void __launch_bounds__(192, 1)
             if (!ok) *abort_flag = 1;
         }
     } else {
-        // epilogue: warps 2..5 -> TMEM lane quarters 2, 3, 0, 1
+        // epilogue: warps 2..5 -> TMEM lane quarters 2, 3, 0, 1.  Each warp stages its 32 rows of a
+        // 32-column chunk in a 2 KiB box (64-byte swizzle: 16-byte chunk j of row i sits at
+        // j ^ ((i >> 1) & 3), so the 16-byte stores are conflict-free) and one lane stores the box
+        // by TMA.  Boxes form a ring per warp; with an added matrix (BN = 128) the ring holds two
+        // tiles and the next tile's added boxes are fetched while this one is computed.
         const int q4 = warp & 3;
-        int it = 0;
+        const bool tma = !OUTF32 && g.tma_out;
+        const bool tadd = tma && g.add != nullptr && BN == 128;
+        uint8_t* stg = stg_base + q4 * (NBOX * kTBox);
+        const uint32_t stg_s = smem_u32(stg);
+        const int swz = (lane >> 1) & 3;
+        auto fetch_add = [&](int t, int set) {  // lane 0: the added boxes of tile t into box set `set`
+            const Tile tn = tile_of(t);
+            const uint32_t bar = smem_u32(&add_full[q4 * 2 + set]);
+            mbar_arrive_expect_tx(bar, 4 * kTBox);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch)
+                tma_load_2d(stg_s + (set * 4 + ch) * kTBox, &tAdd, tn.n0 + ch * 32, tn.m0 + q4 * 32, bar);
+        };
+        if (tadd && lane == 0 && (int)blockIdx.x < total) fetch_add(blockIdx.x, 0);
+        int it = 0, qc = 0;
+        bool add_pending = tadd && (int)blockIdx.x < total;  // an issued add fetch not yet waited for
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const Tile tl = tile_of(t);
             const int buf = it & 1;
-            bool ok = !*abort_flag && mbar_wait(smem_u32(&acc_full[buf]), (it >> 1) & 1, g.status);
+            const int ry = tl.m0 + q4 * 32;  // this warp's first output row
+            bool ok = !*abort_flag;
+            if (tadd) {
+                ok = mbar_wait(smem_u32(&add_full[q4 * 2 + (it & 1)]), (it >> 1) & 1, g.status) && ok;
+                add_pending = false;
+            }
+            ok = ok && mbar_wait(smem_u32(&acc_full[buf]), (it >> 1) & 1, g.status);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 if (lane == 0) *abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            const int row = tl.m0 + q4 * 32 + lane;
+            const int row = ry + lane;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kTN; c0 += 32) {
+            for (int c0 = 0; c0 < BN; c0 += 32, ++qc) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + buf * kTN + ((uint32_t)(q4 * 32) << 16) + c0, v);
+                tmem_ld_32x32b_x32(tmem + buf * BN + ((uint32_t)(q4 * 32) << 16) + c0, v);
                 if (tl.KT == 0)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = 0u;
-                if (OUTF32) {
-                    // split-K partial of a single-tile product: [batch][ks][128][128] fp32
-                    float* dst = reinterpret_cast<float*>(g.C) + (((size_t)tl.z * kTM + (row - tl.m0)) * kTN + c0);
+                if (tma) {
+                    const int box = tadd ? (it & 1) * 4 + c0 / 32 : qc % NBOX;
+                    if (!tadd) {  // the store that last used this box has read it
+                        if (lane == 0) bulk_wait_read<NBOX - 1>();
+                        __syncwarp();
+                    }
+                    uint8_t* rowp = stg + box * kTBox + lane * 64;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4* p16 = reinterpret_cast<uint4*>(rowp + ((j ^ swz) << 4));
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[j * 8 + e]);
+                        if (tadd) {
+                            const uint4 s4 = *p16;
+                            f[0] += bf16lo(s4.x); f[1] += bf16hi(s4.x); f[2] += bf16lo(s4.y); f[3] += bf16hi(s4.y);
+                            f[4] += bf16lo(s4.z); f[5] += bf16hi(s4.z); f[6] += bf16lo(s4.w); f[7] += bf16hi(s4.w);
+                        }
+                        uint4 pk;
+                        pk.x = pack_bf16x2(f[0], f[1]);
+                        pk.y = pack_bf16x2(f[2], f[3]);
+                        pk.z = pack_bf16x2(f[4], f[5]);
+                        pk.w = pack_bf16x2(f[6], f[7]);
+                        *p16 = pk;
+                    }
+                    fence_proxy_async_smem();  // the generic stores above, before the async-proxy read
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tC, stg_s + box * kTBox, tl.n0 + c0, tl.batch, ry);
+                        bulk_commit();
+                    }
+                } else if (OUTF32) {
+                    // split-K partial of a single-tile product: [batch][ks][128][BN] fp32
+                    float* dst = reinterpret_cast<float*>(g.C) + (((size_t)tl.z * kTM + (row - tl.m0)) * BN + c0);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         reinterpret_cast<float4*>(dst)[i] =
@@ -222,13 +304,25 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&acc_empty[buf]));
+            if (tadd && t + (int)gridDim.x < total) {
+                // the next tile's added boxes go into the other set once the previous tile's stores
+                // (that set's last users) have read it; this tile's four stores may still run
+                if (lane == 0) {
+                    bulk_wait_read<4>();
+                    fetch_add(t + gridDim.x, (it + 1) & 1);
+                }
+                add_pending = true;
+            }
         }
+        if (add_pending)  // a fetch issued before an abort: let it land before the CTA exits
+            mbar_wait(smem_u32(&add_full[q4 * 2 + (it & 1)]), (it >> 1) & 1, g.status);
+        if (tma && lane == 0) bulk_wait0();
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 2 * kTN);
+        tmem_dealloc(tmem, C::TMEM);
     }
 }
 
@@ -262,30 +356,33 @@ __global__ void __launch_bounds__(256) dB_reduce_kernel(const float* P, uint16_t
     const int h = (int)(idx / ((long long)d_h * r)), rem = (int)(idx % ((long long)d_h * r));
     const int e = rem / r, j = rem % r;
     float v = 0.f;
-    for (int ks = 0; ks < ksplit; ++ks) v += P[(((size_t)h * ksplit + ks) * kTM + e) * kTN + j];
+    for (int ks = 0; ks < ksplit; ++ks) v += P[(((size_t)h * ksplit + ks) * kTM + e) * 128 + j];
     const __nv_bfloat16 b = __float2bfloat16_rn(v);
     dB[idx] = *reinterpret_cast<const uint16_t*>(&b);
 }
 
-cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& g, bool a_mn, bool b_mn,
-                         bool out_f32, cudaStream_t stream) {
-    // persistent: one CTA per SM (the ring takes 128 KiB of shared memory) looping over the tiles
+cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tC, const CUtensorMap& tAdd,
+                         const GemmArgs& g, int bn, bool a_mn, bool b_mn, bool out_f32, cudaStream_t stream) {
+    // persistent: one CTA per SM (ring and staging fill its shared memory) looping over the tiles
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long tiles = (long long)((g.N + kTN - 1) / kTN) * ((g.M + kTM - 1) / kTM) * g.nbatch * g.ksplit;
+    if (g.add && g.tma_out && bn != 128) return cudaErrorInvalidValue;
+    const long long tiles = (long long)((g.N + bn - 1) / bn) * ((g.M + kTM - 1) / kTM) * g.nbatch * g.ksplit;
     const dim3 grid((unsigned)(tiles < sms ? tiles : sms));
-#define LRKV_TG(AM, BM, OF)                                                                                \
-    if (a_mn == AM && b_mn == BM && out_f32 == OF) {                                                       \
-        auto kern = tgemm_kernel<AM, BM, OF>;                                                              \
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);   \
-        if (e != cudaSuccess) return e;                                                                    \
-        kern<<<grid, 192, kTSmem, stream>>>(tA, tB, g);                                                     \
-        return cudaGetLastError();                                                                         \
+#define LRKV_TG(AM, BM, OF, NB)                                                                                \
+    if (a_mn == AM && b_mn == BM && out_f32 == OF && bn == NB) {                                               \
+        auto kern = tgemm_kernel<AM, BM, OF, NB>;                                                              \
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TCfg<NB>::SMEM); \
+        if (e != cudaSuccess) return e;                                                                        \
+        kern<<<grid, 192, TCfg<NB>::SMEM, stream>>>(tA, tB, tC, tAdd, g);                                      \
+        return cudaGetLastError();                                                                             \
     }
-    LRKV_TG(false, false, false)
-    LRKV_TG(true, true, false)
-    LRKV_TG(false, true, false)
-    LRKV_TG(true, true, true)
+    LRKV_TG(false, false, false, 128)  // expansion
+    LRKV_TG(false, false, false, 160)  // Y
+    LRKV_TG(true, true, false, 256)    // dW_T
+    LRKV_TG(false, true, false, 128)   // dR
+    LRKV_TG(false, true, false, 256)   // dX
+    LRKV_TG(true, true, true, 128)     // dB partials
 #undef LRKV_TG
     return cudaErrorInvalidValue;
 }

@@ -8,12 +8,15 @@
 
 namespace lrkv {
 
-// C = A . B on the tensor cores (bf16 operands, fp32 accumulation), 128 x 128 output tiles,
-// batched over grid.z = nbatch * ksplit.  Operand boxes are read through 2-D tensor maps
-// (128-byte swizzle): a K-major operand is a [rows][K] map read in 64 x 128 boxes, an MN-major
-// one a [K][rows] map read in two 64 x 64 boxes per stage.  Coordinates of batch z start at
+// C = A . B on the tensor cores (bf16 operands, fp32 accumulation), 128 x BN output tiles
+// (BN = 128, 160 or 256), batched over nbatch * ksplit.  Operand boxes are read through 2-D
+// tensor maps (128-byte swizzle): a K-major operand is a [rows][K] map read in 64-wide boxes of
+// 128 (A) or BN (B) rows, an MN-major one a [K][rows] map read in 64 x 64 boxes.  Coordinates of batch z start at
 // (x0 + z * zx, y0 + z * zy).  Output: bf16 (optionally plus a bf16 matrix `add`, rounded
 // once) or, for split-K partials, fp32 at C + ((batch * ksplit + ks) * M_pad) * ldc.
+// With tma_out the bf16 tile goes out through shared memory by TMA stores of a 3-D map
+// {N, nbatch, M} (strides c_zstride and ldc; 32 x 1 x 32 boxes, 64-byte swizzle) and `add` comes
+// in through a [M][N] map of 32 x 32 boxes.
 struct GemmArgs {
     void* C;
     int ldc;                  // elements
@@ -24,12 +27,15 @@ struct GemmArgs {
     int nbatch, ksplit;
     const uint16_t* add;      // bf16 matrix added in the epilogue (or null)
     int ld_add;
+    int tma_out;              // 1: store through tC (and read `add` through tAdd)
     uint32_t* status;
 };
 
-// Launch C = A . B.  AMN / BMN: operand is MN-major; OUTF32: fp32 split-K partials.
-cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& g, bool a_mn, bool b_mn,
-                         bool out_f32, cudaStream_t stream);
+// Launch C = A . B with 128 x bn tiles.  a_mn / b_mn: operand is MN-major; out_f32: fp32 split-K
+// partials (bn = 128).  Instantiated: expansion (K, K, bf16, 128), Y (K, K, bf16, 160), dW_T
+// (MN, MN, bf16, 256), dR (K, MN, bf16, 128), dX (K, MN, bf16, 256), dB (MN, MN, fp32, 128).
+cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tC, const CUtensorMap& tAdd,
+                         const GemmArgs& g, int bn, bool a_mn, bool b_mn, bool out_f32, cudaStream_t stream);
 
 // G[t] = sum_h dK[t][h][:] into columns [0, d_h) of Gc [n][ldg] (bf16, fp32 sums).
 cudaError_t launch_head_sum(const uint16_t* dK, uint16_t* Gc, int n, int H, int d_h, int ldg, cudaStream_t stream);

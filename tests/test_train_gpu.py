@@ -77,3 +77,30 @@ def test_train_zero_tokens_is_noop():
     dims = b.make_dims(8, 64, 8, 512)
     z = torch.empty(0, 512, dtype=torch.bfloat16, device="cuda")
     b.lrkv_train_forward(dims, z, z, z, z, z)
+
+
+def test_train_full_size_sampled():
+    """The timed training workload's launch configuration (8192 tokens, d=4096, H=32, d_h=128, r=16:
+    every GEMM loops over several tiles per CTA, so both accumulator buffers, the staging boxes and
+    the ring phases wrap), checked on outputs the oracle computes from a slice of the inputs:
+    K and dX rows from their own tokens, dW_T columns from their own feature columns of X (G and
+    dR do not depend on X), dB of two heads from those heads' factors and gradients."""
+    wl = S.WORKLOADS["train"]
+    n, d, d_h, H, r = wl.B * wl.L, wl.d, wl.d_h, wl.H, wl.r
+    (X, Ws, U, Bm, dK), (K, dX, dWt, dB, Y) = run_train(n, d, d_h, H, r, wl.seed)
+    o = oracle.get()
+    rows = np.unique(np.concatenate([np.arange(0, 8), np.arange(n - 8, n),
+                                     np.random.default_rng(wl.seed).choice(n, 48, replace=False)]))
+    _check(K[rows], o.train_forward(X[rows], Ws, U, Bm), "K rows")
+    rdX, _, _, _ = o.train_backward(X[rows], Ws, U, Bm, dK[rows])
+    _check(dX[rows], rdX, "dX rows")
+    cols = np.unique(np.concatenate([np.arange(0, 4), np.arange(d - 4, d),
+                                     np.random.default_rng(wl.seed + 1).choice(d, 8, replace=False)]))
+    _, rdWs, rdU, _ = o.train_backward(np.ascontiguousarray(X[:, cols]), np.ascontiguousarray(Ws[cols]),
+                                       np.ascontiguousarray(U[:, cols]), Bm, dK)
+    _check(dWt[:d_h][:, cols], rdWs.T, "dW_shared^T columns")
+    _check(dWt[d_h:].reshape(H, r, d)[:, :, cols], np.transpose(rdU, (0, 2, 1)), "dU^T columns")
+    hs = np.array([0, H - 1])
+    _, _, _, rdB = o.train_backward(X, Ws, np.ascontiguousarray(U[hs]), np.ascontiguousarray(Bm[hs]),
+                                    np.ascontiguousarray(dK[:, hs]))
+    _check(dB[hs], rdB, "dB heads")
