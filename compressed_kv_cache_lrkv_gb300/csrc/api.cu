@@ -116,6 +116,22 @@ lrkv_status make_tmap(CUtensorMap* m, const void* base, uint64_t cols, uint64_t 
     return LRKV_OK;
 }
 
+// 2-D bf16 tensor map over [rows][cols] with a row pitch of `pitch` bytes, 128-byte swizzle.
+lrkv_status make_tmap_strided(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch,
+                              uint32_t box_cols, uint32_t box_rows, const char* what) {
+    auto enc = encode_fn();
+    if (!enc) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {pitch};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+    return LRKV_OK;
+}
+
 // 3-D bf16 tensor map over a row-major [d2][d1][d0] array with a [1][box1][box0] box
 // (box rows past d1 read as zeros).
 lrkv_status make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
@@ -402,13 +418,12 @@ size_t lrkv_train_workspace_bytes(const lrkv_dims* dims, int32_t n_tok) {
     return gc + (size_t)dims->H * train_dB_split(dims->H, n_tok, di.sms) * 128 * 128 * 4;
 }
 
-// Output and added-matrix maps of a tcgen05 GEMM: set g->tma_out when the output (and `add`) can
-// go through TMA (16-byte aligned base and strides), else the epilogue stores directly.
-static void train_out_maps(lrkv::GemmArgs* g, CUtensorMap* tC, CUtensorMap* tAdd) {
+// Output map of a tcgen05 GEMM: set g->tma_out when the output can go through TMA (16-byte
+// aligned base and strides), else the epilogue stores directly.
+static void train_out_map(lrkv::GemmArgs* g, CUtensorMap* tC) {
     g->tma_out = 0;
     const uint64_t zs = g->nbatch > 1 ? (uint64_t)g->c_zstride * 2 : (uint64_t)g->ldc * 2;
     if (((uintptr_t)g->C & 15u) || ((uint64_t)g->ldc * 2) % 16 || zs % 16 || zs == 0) return;
-    if (g->add && (((uintptr_t)g->add & 15u) || ((uint64_t)g->ld_add * 2) % 16)) return;
     auto enc = encode_fn();
     if (!enc) return;
     cuuint64_t dims[3] = {(cuuint64_t)g->N, (cuuint64_t)g->nbatch, (cuuint64_t)g->M};
@@ -419,26 +434,15 @@ static void train_out_maps(lrkv::GemmArgs* g, CUtensorMap* tC, CUtensorMap* tAdd
             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return;
-    if (g->add) {
-        cuuint64_t ad[2] = {(cuuint64_t)g->N, (cuuint64_t)g->M};
-        cuuint64_t as[1] = {(cuuint64_t)g->ld_add * 2};
-        cuuint32_t ab[2] = {32, 32};
-        if (enc(tAdd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(g->add), ad, as, ab, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return;
-    } else {
-        *tAdd = *tC;  // unused
-    }
     g->tma_out = 1;
 }
 
 // C = A . B on the tensor cores (see train.h); bf16 outputs go through TMA when they can.
 static cudaError_t train_gemm(const CUtensorMap& tA, const CUtensorMap& tB, lrkv::GemmArgs g, int bn, bool a_mn,
-                              bool b_mn, bool out_f32, cudaStream_t st) {
-    CUtensorMap tC = tA, tAdd = tA;
-    if (!out_f32) train_out_maps(&g, &tC, &tAdd);
-    return lrkv::launch_tgemm(tA, tB, tC, tAdd, g, bn, a_mn, b_mn, out_f32, st);
+                              bool b_mn, bool out_f32, cudaStream_t st, const CUtensorMap* tB2 = nullptr) {
+    CUtensorMap tC = tA;
+    if (!out_f32) train_out_map(&g, &tC);
+    return lrkv::launch_tgemm(tA, tB, tB2 ? *tB2 : tB, tC, g, bn, a_mn, b_mn, out_f32, st);
 }
 
 lrkv_status lrkv_train_forward(const lrkv_dims* dims, const void* X, const void* W_T, const void* B, int32_t n_tok,
@@ -464,12 +468,16 @@ lrkv_status lrkv_train_forward(const lrkv_dims* dims, const void* X, const void*
     g.C = Y; g.ldc = Ncat; g.M = n_tok; g.N = Ncat; g.K = d; g.nbatch = 1; g.ksplit = 1; g.status = status_dev;
     cudaError_t e = train_gemm(tX, tW, g, 160, false, false, false, st);
     if (e != cudaSuccess) return cuda_status(e, "lrkv_train_forward launch");
-    // K_h = S + R_h B_h^T, one batch per head: A = R_h (Y columns d_h + h r ..), B = B_h as [d_h][r]
+    // K_h = [S | R_h] [I ; B_h^T], one batch per head: the first d_h K columns are S (Y columns
+    // [0, d_h)) against the identity, the rest R_h (Y columns d_h + h r ..) against B_h as [d_h][r]
+    const void* ident = lrkv::train_identity();
+    if (!ident) return fail(LRKV_ERR_CUDA, "identity table unavailable");
+    CUtensorMap tI;
+    if ((s = make_tmap_strided(&tI, ident, d_h, d_h, 256, 64, 128, "identity")) != LRKV_OK) return s;
     lrkv::GemmArgs x{};
-    x.C = K; x.ldc = H * d_h; x.c_zstride = d_h; x.M = n_tok; x.N = d_h; x.K = r;
-    x.a_x0 = d_h; x.a_zx = r; x.b_zy = d_h; x.nbatch = H; x.ksplit = 1;
-    x.add = static_cast<const uint16_t*>(Y); x.ld_add = Ncat; x.status = status_dev;
-    return cuda_status(train_gemm(tY, tB, x, 128, false, false, false, st), "lrkv_train_forward launch");
+    x.C = K; x.ldc = H * d_h; x.c_zstride = d_h; x.M = n_tok; x.N = d_h; x.K = d_h + r; x.kfix = d_h;
+    x.a_x0 = d_h; x.a_zx = r; x.b_zy = d_h; x.nbatch = H; x.ksplit = 1; x.status = status_dev;
+    return cuda_status(train_gemm(tY, tB, x, 128, false, false, false, st, &tI), "lrkv_train_forward launch");
 }
 
 lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void* W_T, const void* B, const void* Y,

@@ -5,7 +5,10 @@
 //
 // Forward (W_T = [W_shared^T ; U_1^T ; ... ; U_H^T], [d_h + H r][d]):
 //   Y = X W_T^T = [S | R_1 .. R_H]            one GEMM, N = d_h + H r
-//   K_h = S + R_h B_h^T                          per head, K = r (B_h's box past r reads zeros)
+//   K_h = S + R_h B_h^T = [S | R_h] [I ; B_h^T]  per head, K = d_h + r: the shared part enters the
+//                                                product through an identity block, so S and R_h B_h^T
+//                                                are summed in fp32 and rounded once (B_h's box past r
+//                                                reads zeros)
 // Backward, for dK [n][H][d_h]:
 //   Gc = [G | dR_1 .. dR_H], G = sum_h dK_h, dR_h = dK_h B_h
 //   dB_h = dK_h^T R_h                            split-K over tokens, fp32 partials, ordered sum
@@ -19,8 +22,8 @@
 // single-thread MMA issue into one of two accumulator buffers, warps 2-5 epilogue (tcgen05.ld of
 // their 32 TMEM lanes = tile rows), so a tile's epilogue overlaps the next tile's MMAs.  A bf16
 // tile leaves through shared memory: each epilogue warp writes its 32 rows into 32 x 32 boxes
-// (64-byte swizzle, conflict-free 16-byte stores) and one lane issues their TMA stores; an added
-// matrix comes in the same way.  All waits are bounded.
+// (64-byte swizzle, conflict-free 16-byte stores) and one lane issues their TMA stores.  All waits
+// are bounded.
 #include "kernels.h"
 #include "lrkv_internal.cuh"
 #include "train.h"
@@ -34,12 +37,12 @@ constexpr uint32_t T_A = kTM * kTK * 2;  // 16 KiB: 128 rows x 64 K
 constexpr uint32_t kTBox = 2048;         // staging box: 32 rows x 32 bf16 columns (64 bytes)
 constexpr uint32_t kTSmemMax = 232448;   // opt-in shared memory per block
 
-// Per output-tile width BN: bytes of one B slice, staging boxes per epilogue warp (two tiles'
-// worth when an added matrix is prefetched, BN = 128), ring depth, TMEM columns.
+// Per output-tile width BN: bytes of one B slice, staging boxes per epilogue warp, ring depth,
+// TMEM columns.
 template <int BN>
 struct TCfg {
     static constexpr uint32_t B = (uint32_t)BN * kTK * 2;
-    static constexpr int NBOX = BN == 128 ? 8 : 4;
+    static constexpr int NBOX = 4;
     static constexpr uint32_t STG = 4u * NBOX * kTBox;
     static constexpr int S0 = (int)((kTSmemMax - 1280 - STG) / (T_A + B));
     static constexpr int STAGES = S0 > 8 ? 8 : S0;
@@ -52,17 +55,45 @@ struct TCfg {
 __device__ __forceinline__ uint64_t kmaj(uint32_t a) { return sdesc(a, 16, 1024, 2); }
 __device__ __forceinline__ uint64_t mnmaj(uint32_t a) { return sdesc(a, 8192, 1024, 2); }
 
+// Tiled store shared -> global (bulk-group completion); the box is clipped at the tensor's extents.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's committed bulk stores still read shared memory.
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
+// Wait until this thread's committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// A 128 x 128 bf16 identity, the B block that adds the shared features S into the expansion.
+struct IdentityBf16 {
+    uint16_t v[128 * 128];
+    constexpr IdentityBf16() : v() {
+        for (int i = 0; i < 128; ++i) v[i * 129] = 0x3F80;  // 1.0
+    }
+};
+__device__ const IdentityBf16 g_identity{};
+
 }  // namespace
+
+const void* train_identity() {
+    void* p = nullptr;
+    return cudaGetSymbolAddress(&p, g_identity) == cudaSuccess ? p : nullptr;
+}
 
 template <bool AMN, bool BMN, bool OUTF32, int BN>
 __global__ void __launch_bounds__(192, 1)
     tgemm_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
-                 const __grid_constant__ CUtensorMap tC, const __grid_constant__ CUtensorMap tAdd, const GemmArgs g) {
+                 const __grid_constant__ CUtensorMap tB2, const __grid_constant__ CUtensorMap tC, const GemmArgs g) {
     using C = TCfg<BN>;
     constexpr int kS = C::STAGES, NBOX = C::NBOX;
     constexpr uint32_t T_B = C::B;
@@ -76,8 +107,7 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* empty = full + kS;
     uint64_t* acc_full = empty + kS;      // [2] accumulator buffer holds a finished tile
     uint64_t* acc_empty = acc_full + 2;   // [2] the epilogue has read it (128 arrivals)
-    uint64_t* add_full = acc_empty + 2;   // [4][2] an epilogue warp's added boxes (per tile parity)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(add_full + 8);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -110,7 +140,6 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(smem_u32(&acc_full[b]), 1);
             mbar_init(smem_u32(&acc_empty[b]), 128);
         }
-        for (int w = 0; w < 8; ++w) mbar_init(smem_u32(&add_full[w]), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -138,17 +167,24 @@ __global__ void __launch_bounds__(192, 1)
                     const int k = (tl.kt0 + i) * kTK;
                     const uint32_t bar = smem_u32(&full[s]);
                     mbar_arrive_expect_tx(bar, T_A + T_B);
+                    if (!AMN && !BMN && k < g.kfix) {
+                        // leading K columns shared by every batch: A at x = k, B from the second map
+                        tma_load_2d(sA + s * T_A, &tA, k, ay + tl.m0, bar);
+                        tma_load_2d(sB + s * T_B, &tB2, k, tl.n0, bar);
+                        continue;
+                    }
+                    const int kb = k - g.kfix;
                     if (AMN) {
                         tma_load_2d(sA + s * T_A, &tA, ax + tl.m0, ay + k, bar);
                         tma_load_2d(sA + s * T_A + 8192, &tA, ax + tl.m0 + 64, ay + k, bar);
                     } else {
-                        tma_load_2d(sA + s * T_A, &tA, ax + k, ay + tl.m0, bar);
+                        tma_load_2d(sA + s * T_A, &tA, ax + kb, ay + tl.m0, bar);
                     }
                     if (BMN) {
 #pragma unroll
                         for (int j = 0; j < BN / 64; ++j) tma_load_2d(sB + s * T_B + j * 8192, &tB, bx + tl.n0 + 64 * j, by + k, bar);
                     } else {
-                        tma_load_2d(sB + s * T_B, &tB, bx + k, by + tl.n0, bar);  // one [BN][64] box
+                        tma_load_2d(sB + s * T_B, &tB, bx + kb, by + tl.n0, bar);  // one [BN][64] box
                     }
                 }
             }
@@ -196,35 +232,18 @@ __global__ void __launch_bounds__(192, 1)
         // epilogue: warps 2..5 -> TMEM lane quarters 2, 3, 0, 1.  Each warp stages its 32 rows of a
         // 32-column chunk in a 2 KiB box (64-byte swizzle: 16-byte chunk j of row i sits at
         // j ^ ((i >> 1) & 3), so the 16-byte stores are conflict-free) and one lane stores the box
-        // by TMA.  Boxes form a ring per warp; with an added matrix (BN = 128) the ring holds two
-        // tiles and the next tile's added boxes are fetched while this one is computed.
+        // by TMA; the boxes form a ring per warp.
         const int q4 = warp & 3;
         const bool tma = !OUTF32 && g.tma_out;
-        const bool tadd = tma && g.add != nullptr && BN == 128;
         uint8_t* stg = stg_base + q4 * (NBOX * kTBox);
         const uint32_t stg_s = smem_u32(stg);
         const int swz = (lane >> 1) & 3;
-        auto fetch_add = [&](int t, int set) {  // lane 0: the added boxes of tile t into box set `set`
-            const Tile tn = tile_of(t);
-            const uint32_t bar = smem_u32(&add_full[q4 * 2 + set]);
-            mbar_arrive_expect_tx(bar, 4 * kTBox);
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
-                tma_load_2d(stg_s + (set * 4 + ch) * kTBox, &tAdd, tn.n0 + ch * 32, tn.m0 + q4 * 32, bar);
-        };
-        if (tadd && lane == 0 && (int)blockIdx.x < total) fetch_add(blockIdx.x, 0);
         int it = 0, qc = 0;
-        bool add_pending = tadd && (int)blockIdx.x < total;  // an issued add fetch not yet waited for
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const Tile tl = tile_of(t);
             const int buf = it & 1;
             const int ry = tl.m0 + q4 * 32;  // this warp's first output row
-            bool ok = !*abort_flag;
-            if (tadd) {
-                ok = mbar_wait(smem_u32(&add_full[q4 * 2 + (it & 1)]), (it >> 1) & 1, g.status) && ok;
-                add_pending = false;
-            }
-            ok = ok && mbar_wait(smem_u32(&acc_full[buf]), (it >> 1) & 1, g.status);
+            bool ok = !*abort_flag && mbar_wait(smem_u32(&acc_full[buf]), (it >> 1) & 1, g.status);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 if (lane == 0) *abort_flag = 1;
@@ -240,29 +259,18 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = 0u;
                 if (tma) {
-                    const int box = tadd ? (it & 1) * 4 + c0 / 32 : qc % NBOX;
-                    if (!tadd) {  // the store that last used this box has read it
-                        if (lane == 0) bulk_wait_read<NBOX - 1>();
-                        __syncwarp();
-                    }
+                    const int box = qc % NBOX;
+                    if (lane == 0) bulk_wait_read<NBOX - 1>();  // the store that last used this box has read it
+                    __syncwarp();
                     uint8_t* rowp = stg + box * kTBox + lane * 64;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        uint4* p16 = reinterpret_cast<uint4*>(rowp + ((j ^ swz) << 4));
-                        float f[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[j * 8 + e]);
-                        if (tadd) {
-                            const uint4 s4 = *p16;
-                            f[0] += bf16lo(s4.x); f[1] += bf16hi(s4.x); f[2] += bf16lo(s4.y); f[3] += bf16hi(s4.y);
-                            f[4] += bf16lo(s4.z); f[5] += bf16hi(s4.z); f[6] += bf16lo(s4.w); f[7] += bf16hi(s4.w);
-                        }
                         uint4 pk;
-                        pk.x = pack_bf16x2(f[0], f[1]);
-                        pk.y = pack_bf16x2(f[2], f[3]);
-                        pk.z = pack_bf16x2(f[4], f[5]);
-                        pk.w = pack_bf16x2(f[6], f[7]);
-                        *p16 = pk;
+                        pk.x = pack_bf16x2(__uint_as_float(v[j * 8 + 0]), __uint_as_float(v[j * 8 + 1]));
+                        pk.y = pack_bf16x2(__uint_as_float(v[j * 8 + 2]), __uint_as_float(v[j * 8 + 3]));
+                        pk.z = pack_bf16x2(__uint_as_float(v[j * 8 + 4]), __uint_as_float(v[j * 8 + 5]));
+                        pk.w = pack_bf16x2(__uint_as_float(v[j * 8 + 6]), __uint_as_float(v[j * 8 + 7]));
+                        *reinterpret_cast<uint4*>(rowp + ((j ^ swz) << 4)) = pk;
                     }
                     fence_proxy_async_smem();  // the generic stores above, before the async-proxy read
                     __syncwarp();
@@ -284,19 +292,11 @@ __global__ void __launch_bounds__(192, 1)
                     for (int gi = 0; gi < 4; ++gi) {
                         const int col = tl.n0 + c0 + gi * 8;
                         if (col < g.N) {
-                            float f[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[gi * 8 + e]);
-                            if (g.add) {
-                                const uint4 s4 = *reinterpret_cast<const uint4*>(g.add + (size_t)row * g.ld_add + col);
-                                f[0] += bf16lo(s4.x); f[1] += bf16hi(s4.x); f[2] += bf16lo(s4.y); f[3] += bf16hi(s4.y);
-                                f[4] += bf16lo(s4.z); f[5] += bf16hi(s4.z); f[6] += bf16lo(s4.w); f[7] += bf16hi(s4.w);
-                            }
                             uint4 pk;
-                            pk.x = pack_bf16x2(f[0], f[1]);
-                            pk.y = pack_bf16x2(f[2], f[3]);
-                            pk.z = pack_bf16x2(f[4], f[5]);
-                            pk.w = pack_bf16x2(f[6], f[7]);
+                            pk.x = pack_bf16x2(__uint_as_float(v[gi * 8 + 0]), __uint_as_float(v[gi * 8 + 1]));
+                            pk.y = pack_bf16x2(__uint_as_float(v[gi * 8 + 2]), __uint_as_float(v[gi * 8 + 3]));
+                            pk.z = pack_bf16x2(__uint_as_float(v[gi * 8 + 4]), __uint_as_float(v[gi * 8 + 5]));
+                            pk.w = pack_bf16x2(__uint_as_float(v[gi * 8 + 6]), __uint_as_float(v[gi * 8 + 7]));
                             *reinterpret_cast<uint4*>(crow + col) = pk;
                         }
                     }
@@ -304,18 +304,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&acc_empty[buf]));
-            if (tadd && t + (int)gridDim.x < total) {
-                // the next tile's added boxes go into the other set once the previous tile's stores
-                // (that set's last users) have read it; this tile's four stores may still run
-                if (lane == 0) {
-                    bulk_wait_read<4>();
-                    fetch_add(t + gridDim.x, (it + 1) & 1);
-                }
-                add_pending = true;
-            }
         }
-        if (add_pending)  // a fetch issued before an abort: let it land before the CTA exits
-            mbar_wait(smem_u32(&add_full[q4 * 2 + (it & 1)]), (it >> 1) & 1, g.status);
         if (tma && lane == 0) bulk_wait0();
     }
     tc_fence_before();
@@ -361,12 +350,12 @@ __global__ void __launch_bounds__(256) dB_reduce_kernel(const float* P, uint16_t
     dB[idx] = *reinterpret_cast<const uint16_t*>(&b);
 }
 
-cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tC, const CUtensorMap& tAdd,
+cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tB2, const CUtensorMap& tC,
                          const GemmArgs& g, int bn, bool a_mn, bool b_mn, bool out_f32, cudaStream_t stream) {
     // persistent: one CTA per SM (ring and staging fill its shared memory) looping over the tiles
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g.add && g.tma_out && bn != 128) return cudaErrorInvalidValue;
+    if (g.kfix % kTK != 0 || (g.kfix > 0 && (a_mn || b_mn))) return cudaErrorInvalidValue;
     const long long tiles = (long long)((g.N + bn - 1) / bn) * ((g.M + kTM - 1) / kTM) * g.nbatch * g.ksplit;
     const dim3 grid((unsigned)(tiles < sms ? tiles : sms));
 #define LRKV_TG(AM, BM, OF, NB)                                                                                \
@@ -374,7 +363,7 @@ cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUt
         auto kern = tgemm_kernel<AM, BM, OF, NB>;                                                              \
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TCfg<NB>::SMEM); \
         if (e != cudaSuccess) return e;                                                                        \
-        kern<<<grid, 192, TCfg<NB>::SMEM, stream>>>(tA, tB, tC, tAdd, g);                                      \
+        kern<<<grid, 192, TCfg<NB>::SMEM, stream>>>(tA, tB, tB2, tC, g);                                       \
         return cudaGetLastError();                                                                             \
     }
     LRKV_TG(false, false, false, 128)  // expansion

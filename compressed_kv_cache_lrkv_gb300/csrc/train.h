@@ -12,11 +12,12 @@ namespace lrkv {
 // (BN = 128, 160 or 256), batched over nbatch * ksplit.  Operand boxes are read through 2-D
 // tensor maps (128-byte swizzle): a K-major operand is a [rows][K] map read in 64-wide boxes of
 // 128 (A) or BN (B) rows, an MN-major one a [K][rows] map read in 64 x 64 boxes.  Coordinates of batch z start at
-// (x0 + z * zx, y0 + z * zy).  Output: bf16 (optionally plus a bf16 matrix `add`, rounded
-// once) or, for split-K partials, fp32 at C + ((batch * ksplit + ks) * M_pad) * ldc.
-// With tma_out the bf16 tile goes out through shared memory by TMA stores of a 3-D map
-// {N, nbatch, M} (strides c_zstride and ldc; 32 x 1 x 32 boxes, 64-byte swizzle) and `add` comes
-// in through a [M][N] map of 32 x 32 boxes.
+// (x0 + z * zx, y0 + z * zy).  With kfix > 0 (K-major operands only) the first kfix K columns
+// are shared by all batches: A's come from columns [0, kfix) of its map and B's from a second map
+// at (k, n0); K column k >= kfix is column k - kfix of the batch's own operand boxes.  Output:
+// bf16, or for split-K partials fp32 at C + ((batch * ksplit + ks) * 128 + row) * BN.  With
+// tma_out the bf16 tile goes out through shared memory by TMA stores of a 3-D map {N, nbatch, M}
+// (strides c_zstride and ldc; 32 x 1 x 32 boxes, 64-byte swizzle).
 struct GemmArgs {
     void* C;
     int ldc;                  // elements
@@ -25,17 +26,19 @@ struct GemmArgs {
     int a_x0, a_y0, a_zx, a_zy;
     int b_x0, b_y0, b_zx, b_zy;
     int nbatch, ksplit;
-    const uint16_t* add;      // bf16 matrix added in the epilogue (or null)
-    int ld_add;
-    int tma_out;              // 1: store through tC (and read `add` through tAdd)
+    int kfix;                 // leading K columns shared by all batches (multiple of 64)
+    int tma_out;              // 1: store through tC
     uint32_t* status;
 };
 
 // Launch C = A . B with 128 x bn tiles.  a_mn / b_mn: operand is MN-major; out_f32: fp32 split-K
 // partials (bn = 128).  Instantiated: expansion (K, K, bf16, 128), Y (K, K, bf16, 160), dW_T
 // (MN, MN, bf16, 256), dR (K, MN, bf16, 128), dX (K, MN, bf16, 256), dB (MN, MN, fp32, 128).
-cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tC, const CUtensorMap& tAdd,
+cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tB2, const CUtensorMap& tC,
                          const GemmArgs& g, int bn, bool a_mn, bool b_mn, bool out_f32, cudaStream_t stream);
+
+// Device address of a 128 x 128 bf16 identity matrix (row-major), or null.
+const void* train_identity();
 
 // G[t] = sum_h dK[t][h][:] into columns [0, d_h) of Gc [n][ldg] (bf16, fp32 sums).
 cudaError_t launch_head_sum(const uint16_t* dK, uint16_t* Gc, int n, int H, int d_h, int ldg, cudaStream_t stream);
