@@ -415,7 +415,8 @@ size_t lrkv_train_workspace_bytes(const lrkv_dims* dims, int32_t n_tok) {
     if (device_info(&di) != LRKV_OK) return 0;
     const size_t Ncat = (size_t)dims->d_h + (size_t)dims->H * dims->r;
     const size_t gc = ((size_t)n_tok * Ncat * 2 + 255) & ~(size_t)255;
-    return gc + (size_t)dims->H * train_dB_split(dims->H, n_tok, di.sms) * 128 * 128 * 4;
+    const size_t bt = ((size_t)dims->H * dims->r * dims->d_h * 2 + 255) & ~(size_t)255;
+    return gc + bt + (size_t)dims->H * train_dB_split(dims->H, n_tok, di.sms) * 128 * 128 * 4;
 }
 
 // Output map of a tcgen05 GEMM: set g->tma_out when the output can go through TMA (16-byte
@@ -499,12 +500,14 @@ lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void
     const int H = dims->H, d_h = dims->d_h, r = dims->r, d = dims->d, Ncat = d_h + H * r;
     const int ks = train_dB_split(H, n_tok, di.sms);
     const size_t gc_bytes = ((size_t)n_tok * Ncat * 2 + 255) & ~(size_t)255;
-    const size_t need = gc_bytes + (size_t)H * ks * 128 * 128 * 4;
+    const size_t bt_bytes = ((size_t)H * r * d_h * 2 + 255) & ~(size_t)255;
+    const size_t need = gc_bytes + bt_bytes + (size_t)H * ks * 128 * 128 * 4;
     if (!workspace || ((uintptr_t)workspace & 255u))
         return fail(LRKV_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
     if (workspace_bytes < need) return fail(LRKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
     uint16_t* Gc = static_cast<uint16_t*>(workspace);
-    float* P = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gc_bytes);
+    uint16_t* BT = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + gc_bytes);
+    float* P = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gc_bytes + bt_bytes);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     CUtensorMap tdK_k, tdK_mn, tB_mn, tY_mn, tGc_mn, tGc_k, tX_mn, tW_mn;
     const uint64_t HD = (uint64_t)H * d_h;
@@ -518,15 +521,26 @@ lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void
         (s = make_tmap(&tW_mn, W_T, d, Ncat, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "W_T")) != LRKV_OK)
         return s;
     cudaError_t e;
-    // Gc[:, 0:d_h] = G = sum_h dK_h
-    if ((e = lrkv::launch_head_sum(static_cast<const uint16_t*>(dK), Gc, n_tok, H, d_h, Ncat, st)) != cudaSuccess)
-        return cuda_status(e, "lrkv_train_backward launch");
-    // Gc[:, d_h + h r ..] = dR_h = dK_h B_h  (A = dK_h K-major, B = B_h read [d_h (K)][r (N)])
     lrkv::GemmArgs g{};
-    g.C = Gc + d_h; g.ldc = Ncat; g.c_zstride = r; g.M = n_tok; g.N = r; g.K = d_h;
-    g.a_zx = d_h; g.b_zy = d_h; g.nbatch = H; g.ksplit = 1; g.status = status_dev;
-    if ((e = train_gemm(tdK_k, tB_mn, g, 128, false, true, false, st)) != cudaSuccess)
-        return cuda_status(e, "lrkv_train_backward launch");
+    if (lrkv::dk_pass_supported(H, d_h, r)) {
+        // one pass over dK: Gc[:, 0:d_h] = G = sum_h dK_h and Gc[:, d_h + h r ..] = dR_h = dK_h B_h
+        CUtensorMap tBT;
+        if ((s = make_tmap(&tBT, BT, d_h, (uint64_t)H * r, 64, r, CU_TENSOR_MAP_SWIZZLE_128B, "B^T")) != LRKV_OK)
+            return s;
+        lrkv::DkArgs da{};
+        da.Gc = Gc; da.ldg = Ncat; da.n = n_tok; da.H = H; da.d_h = d_h; da.r = r; da.status = status_dev;
+        if ((e = lrkv::launch_dk_pass(tdK_k, tBT, static_cast<const uint16_t*>(B), BT, da, st)) != cudaSuccess)
+            return cuda_status(e, "lrkv_train_backward launch");
+    } else {
+        // Gc[:, 0:d_h] = G = sum_h dK_h
+        if ((e = lrkv::launch_head_sum(static_cast<const uint16_t*>(dK), Gc, n_tok, H, d_h, Ncat, st)) != cudaSuccess)
+            return cuda_status(e, "lrkv_train_backward launch");
+        // Gc[:, d_h + h r ..] = dR_h = dK_h B_h  (A = dK_h K-major, B = B_h read [d_h (K)][r (N)])
+        g.C = Gc + d_h; g.ldc = Ncat; g.c_zstride = r; g.M = n_tok; g.N = r; g.K = d_h;
+        g.a_zx = d_h; g.b_zy = d_h; g.nbatch = H; g.ksplit = 1; g.status = status_dev;
+        if ((e = train_gemm(tdK_k, tB_mn, g, 128, false, true, false, st)) != cudaSuccess)
+            return cuda_status(e, "lrkv_train_backward launch");
+    }
     // dB_h = dK_h^T R_h: split-K partials (A = dK read [n (K)][d_h (M)], B = R_h read [n (K)][r (N)])
     g = lrkv::GemmArgs{};
     g.C = P; g.M = d_h; g.N = r; g.K = n_tok; g.a_zx = d_h; g.b_x0 = d_h; g.b_zx = r; g.nbatch = H; g.ksplit = ks;

@@ -315,6 +315,289 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
+// ------------------------------------------------------------------ fused pass over dK
+// For one 128-token tile: G = sum_h dK_h (Gc columns [0, d_h)) and dR_h = dK_h B_h (Gc columns
+// d_h + h r ..), reading each dK_h tile once.  A cluster of two CTAs splits the heads:
+//   warp 0      TMA producer: B_h^T boxes of the CTA's heads, then its dK_h tiles into a ring
+//               (each tile starts its walk over the heads at a different head, so that the
+//               CTAs do not all read the same head's columns at once);
+//   warp 1      TMEM owner; one thread issues dR_h = dK_h B_h (M = 128 tokens, N = r, K = d_h)
+//               into r TMEM columns per head;
+//   warps 2..5  add every dK_h tile into fp32 registers (one token row per thread: G), then
+//               store dR.  Rank 1 stages its partial G in its own idle ring and copies it in one
+//               bulk transfer into rank 0's idle ring; rank 0 adds it and rounds the sum once.
+// A ring slot is free once the MMAs (commit) and the four summing warps have read it.
+namespace {
+
+__device__ __forceinline__ uint32_t cl_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cl_map(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+// Every thread of both CTAs: release its shared-memory writes, acquire the other CTA's.
+__device__ __forceinline__ void cl_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Bulk copy from this CTA's shared memory into another CTA's (dst and bar: cluster addresses).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+template <int D_H>
+struct DkCfg {
+    static constexpr int NBOX = D_H / 64;
+    static constexpr uint32_t TILE = NBOX * 16384u;  // one dK_h tile: 128 tokens x d_h
+    static constexpr int STAGES = D_H == 128 ? 4 : 6;
+    static constexpr int PITCH = D_H + 4;            // floats per row of a staged partial G
+    static constexpr uint32_t GBYTES = 128u * PITCH * 4u;
+};
+
+}  // namespace
+
+template <int D_H>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    dk_pass_kernel(const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmBT, const DkArgs a) {
+    using C = DkCfg<D_H>;
+    constexpr int NBOX = C::NBOX, NST = C::STAGES, PITCH = C::PITCH;
+    constexpr uint32_t TILE = C::TILE;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const int rank = (int)cl_rank();
+    const int m0 = blockIdx.y * kTM;
+    const int r = a.r;
+    const int hpr = (a.H + 1) / 2;
+    const int h0 = rank * hpr, nh = min(a.H - h0, hpr);
+    const int hoff = (int)(blockIdx.y % (unsigned)nh);  // first head of this tile's walk
+    const uint32_t BTB = (uint32_t)r * 128u;            // B^T box: r rows x 64 K
+    const uint32_t sRing = smem_u32(smem);
+    const uint32_t sBT = sRing + NST * TILE;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * TILE + (size_t)hpr * NBOX * BTB);
+    uint64_t* empty = full + NST;
+    uint64_t* cfull = empty + NST;  // B^T boxes landed
+    uint64_t* accf = cfull + 1;     // every MMA of this CTA has completed
+    uint64_t* recv = accf + 1;      // rank 0: rank 1's partial G has landed in the ring
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv + 1);
+    volatile int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 5);  // the MMA commit and the four summing warps
+        }
+        mbar_init(smem_u32(cfull), 1);
+        mbar_init(smem_u32(accf), 1);
+        mbar_init(smem_u32(recv), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    float g[D_H];  // this thread's token row of G (summing warps)
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint32_t cb = smem_u32(cfull);
+            mbar_arrive_expect_tx(cb, (uint32_t)nh * NBOX * BTB);
+            for (int hh = 0; hh < nh; ++hh)
+#pragma unroll
+                for (int j = 0; j < NBOX; ++j)
+                    tma_load_2d(sBT + (hh * NBOX + j) * BTB, &tmBT, 64 * j, (h0 + hh) * r, cb);
+            int issued = 0;
+            for (int i = 0; i < nh; ++i) {
+                const int s = i % NST, hh = (i + hoff) % nh;
+                if ((i >= NST && !mbar_wait(smem_u32(&empty[s]), ((i / NST) - 1) & 1, a.status)) || *abort_flag) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint32_t bar = smem_u32(&full[s]);
+                mbar_arrive_expect_tx(bar, TILE);
+#pragma unroll
+                for (int j = 0; j < NBOX; ++j)
+                    tma_load_2d(sRing + s * TILE + j * 16384, &tmdK, (h0 + hh) * D_H + 64 * j, m0, bar);
+                issued = i + 1;
+            }
+            mbar_wait(cb, 0, a.status);  // the B^T boxes have landed before the CTA can exit
+            if (*abort_flag)             // as have the tiles in flight
+                for (int k = max(0, issued - NST); k < issued; ++k)
+                    mbar_wait(smem_u32(&full[k % NST]), (k / NST) & 1, a.status);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idR = idesc_bf16_f32(kTM, r);
+            bool ok = mbar_wait(smem_u32(cfull), 0, a.status);
+            for (int i = 0; i < nh && ok; ++i) {
+                const int s = i % NST, hh = (i + hoff) % nh;
+                if (*abort_flag || !mbar_wait(smem_u32(&full[s]), (i / NST) & 1, a.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D_H / 16; ++kk) {
+                    const int j = kk >> 2;
+                    const uint32_t o = (kk & 3) * 32;
+                    tc_mma_bf16(tmem + hh * r, kmaj(sRing + s * TILE + j * 16384 + o),
+                                kmaj(sBT + (hh * NBOX + j) * BTB + o), idR, kk != 0);
+                }
+                tc_commit(smem_u32(&empty[s]));
+            }
+            if (ok) tc_commit(smem_u32(accf));
+            else *abort_flag = 1;
+        }
+    } else {
+        // G: add each dK_h tile's row into fp32 registers
+        const int rl = (warp & 3) * 32 + lane;  // tile row = TMEM lane of this warp's quarter
+#pragma unroll
+        for (int c = 0; c < D_H; ++c) g[c] = 0.f;
+        bool ok = true;
+        for (int i = 0; i < nh; ++i) {
+            const int s = i % NST;
+            ok = ok && !*abort_flag && mbar_wait(smem_u32(&full[s]), (i / NST) & 1, a.status);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            const uint8_t* tile = smem + s * TILE + rl * 128;
+#pragma unroll
+            for (int j = 0; j < NBOX; ++j)
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(tile + j * 16384 + ((c8 ^ (rl & 7)) << 4));
+                    float* gg = g + j * 64 + c8 * 8;
+                    gg[0] += bf16lo(v.x); gg[1] += bf16hi(v.x); gg[2] += bf16lo(v.y); gg[3] += bf16hi(v.y);
+                    gg[4] += bf16lo(v.z); gg[5] += bf16hi(v.z); gg[6] += bf16lo(v.w); gg[7] += bf16hi(v.w);
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        }
+        ok = ok && mbar_wait(smem_u32(accf), 0, a.status);
+        if (!__all_sync(0xffffffffu, ok) && lane == 0) *abort_flag = 1;
+        tc_fence_after();
+        if (rank == 1) {
+            // stage the partial G (fp32) in this CTA's idle ring for the copy to rank 0
+            float* dst = reinterpret_cast<float*>(smem) + (size_t)rl * PITCH;
+#pragma unroll
+            for (int c = 0; c < D_H; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(g[c], g[c + 1], g[c + 2], g[c + 3]);
+            fence_proxy_async_smem();  // generic writes, before the bulk copy reads them
+        } else if (threadIdx.x == 64) {
+            mbar_arrive_expect_tx(smem_u32(recv), C::GBYTES);
+        }
+    }
+    // Barrier 1: both rings are idle (every stage consumed, every MMA complete), rank 1's partial
+    // G is staged and rank 0 expects it.
+    __syncwarp();
+    cl_sync();
+    if (warp >= 2) {
+        const int rl = (warp & 3) * 32 + lane;
+        const int row = m0 + rl;
+        const bool ok = !*abort_flag;
+        if (rank == 1 && threadIdx.x == 64 && ok)
+            bulk_copy_to_peer(cl_map(sRing, 0), sRing, C::GBYTES, cl_map(smem_u32(recv), 0));
+        if (ok) {
+            // dR of this CTA's heads: Gc columns d_h + h0 r .. + nh r
+            uint16_t* grow = a.Gc + (size_t)row * a.ldg + D_H + h0 * r;
+            for (int c0 = 0; c0 < nh * r; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + c0, v);
+                if (row < a.n) {
+                    uint4 p0, p1;
+                    p0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+                    p0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+                    p0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+                    p0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+                    p1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
+                    p1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
+                    p1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
+                    p1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
+                    reinterpret_cast<uint4*>(grow + c0)[0] = p0;
+                    reinterpret_cast<uint4*>(grow + c0)[1] = p1;
+                }
+            }
+        }
+        if (rank == 0 && ok && mbar_wait(smem_u32(recv), 0, a.status) && row < a.n) {
+            const float* rv = reinterpret_cast<const float*>(smem) + (size_t)rl * PITCH;
+#pragma unroll
+            for (int c = 0; c < D_H; c += 8) {
+                const float4 x0 = *reinterpret_cast<const float4*>(rv + c);
+                const float4 x1 = *reinterpret_cast<const float4*>(rv + c + 4);
+                uint4 pk;
+                pk.x = pack_bf16x2(g[c] + x0.x, g[c + 1] + x0.y);
+                pk.y = pack_bf16x2(g[c + 2] + x0.z, g[c + 3] + x0.w);
+                pk.z = pack_bf16x2(g[c + 4] + x1.x, g[c + 5] + x1.y);
+                pk.w = pack_bf16x2(g[c + 6] + x1.z, g[c + 7] + x1.w);
+                *reinterpret_cast<uint4*>(a.Gc + (size_t)row * a.ldg + c) = pk;
+            }
+        }
+    }
+    // Barrier 2: rank 0 has received the copy, so rank 1's staging may go
+    __syncwarp();
+    cl_sync();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// BT[h][j][e] = B[h][e][j]: the residual factors as K-major [r][d_h] blocks.
+__global__ void __launch_bounds__(256) bt_kernel(const uint16_t* B, uint16_t* BT, int H, int d_h, int r) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= H * r * d_h) return;
+    const int h = idx / (r * d_h), rem = idx % (r * d_h);
+    const int j = rem / d_h, e = rem % d_h;
+    BT[idx] = B[((size_t)h * d_h + e) * r + j];
+}
+
+template <int D_H>
+static size_t dk_smem(int H, int r) {
+    return (size_t)DkCfg<D_H>::STAGES * DkCfg<D_H>::TILE + (size_t)((H + 1) / 2) * DkCfg<D_H>::NBOX * r * 128 + 256 +
+           1024;
+}
+
+bool dk_pass_supported(int H, int d_h, int r) {
+    if (H < 2 || !(d_h == 64 || d_h == 128) || !(r == 16 || r == 32) || ((H + 1) / 2) * r > 512) return false;
+    return (d_h == 64 ? dk_smem<64>(H, r) : dk_smem<128>(H, r)) <= kTSmemMax;
+}
+
+template <int D_H>
+static cudaError_t launch_dk_t(const CUtensorMap& tdK, const CUtensorMap& tBT, const DkArgs& a, cudaStream_t stream) {
+    // the staged partial G fits in the ring
+    static_assert((size_t)DkCfg<D_H>::STAGES * DkCfg<D_H>::TILE >= DkCfg<D_H>::GBYTES, "ring");
+    // at least 120 KiB, so that one CTA runs per SM: each allocates all 512 TMEM columns, and a
+    // second resident CTA would wait in its allocation for one that waits on its cluster peer
+    const size_t need = dk_smem<D_H>(a.H, a.r), smem = need > 122880 ? need : 122880;
+    auto kern = dk_pass_kernel<D_H>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(2, (a.n + kTM - 1) / kTM), 192, smem, stream>>>(tdK, tBT, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dk_pass(const CUtensorMap& tdK, const CUtensorMap& tBT, const uint16_t* B, uint16_t* BT,
+                           const DkArgs& a, cudaStream_t stream) {
+    if (!dk_pass_supported(a.H, a.d_h, a.r)) return cudaErrorInvalidValue;
+    const int tot = a.H * a.r * a.d_h;
+    bt_kernel<<<(tot + 255) / 256, 256, 0, stream>>>(B, BT, a.H, a.d_h, a.r);
+    return a.d_h == 64 ? launch_dk_t<64>(tdK, tBT, a, stream) : launch_dk_t<128>(tdK, tBT, a, stream);
+}
+
 // G[t][e] = sum_h dK[t][h][e] (fp32, heads in order), eight columns per thread.
 __global__ void __launch_bounds__(256) head_sum_kernel(const uint16_t* dK, uint16_t* Gc, int n, int H, int d_h,
                                                        int ldg) {

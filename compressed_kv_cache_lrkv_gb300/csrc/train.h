@@ -40,6 +40,20 @@ cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUt
 // Device address of a 128 x 128 bf16 identity matrix (row-major), or null.
 const void* train_identity();
 
+// Fused pass over dK for 128-token tiles: G = sum_h dK_h into Gc columns [0, d_h) and dR_h =
+// dK_h B_h into Gc columns d_h + h r .., each dK_h tile read once (a CTA pair splits the heads).
+struct DkArgs {
+    uint16_t* Gc;
+    int ldg;                  // Gc row pitch, elements
+    int n, H, d_h, r;
+    uint32_t* status;
+};
+bool dk_pass_supported(int H, int d_h, int r);
+// tdK: [n][H d_h] in 64 x 128 boxes; tBT: BT = [H r][d_h] in 64 x r boxes, written here from the
+// residual factors B [H][d_h][r] first.
+cudaError_t launch_dk_pass(const CUtensorMap& tdK, const CUtensorMap& tBT, const uint16_t* B, uint16_t* BT,
+                           const DkArgs& a, cudaStream_t stream);
+
 // G[t] = sum_h dK[t][h][:] into columns [0, d_h) of Gc [n][ldg] (bf16, fp32 sums).
 cudaError_t launch_head_sum(const uint16_t* dK, uint16_t* Gc, int n, int H, int d_h, int ldg, cudaStream_t stream);
 
