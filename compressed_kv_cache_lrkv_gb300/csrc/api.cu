@@ -416,7 +416,7 @@ size_t lrkv_train_workspace_bytes(const lrkv_dims* dims, int32_t n_tok) {
     const size_t Ncat = (size_t)dims->d_h + (size_t)dims->H * dims->r;
     const size_t gc = ((size_t)n_tok * Ncat * 2 + 255) & ~(size_t)255;
     const size_t bt = ((size_t)dims->H * dims->r * dims->d_h * 2 + 255) & ~(size_t)255;
-    return gc + bt + (size_t)dims->H * train_dB_split(dims->H, n_tok, di.sms) * 128 * 128 * 4;
+    return gc + bt + (size_t)dims->H * train_dB_split(dims->H, n_tok, di.sms) * 128 * 64 * 4;
 }
 
 // Output map of a tcgen05 GEMM: set g->tma_out when the output can go through TMA (16-byte
@@ -501,7 +501,7 @@ lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void
     const int ks = train_dB_split(H, n_tok, di.sms);
     const size_t gc_bytes = ((size_t)n_tok * Ncat * 2 + 255) & ~(size_t)255;
     const size_t bt_bytes = ((size_t)H * r * d_h * 2 + 255) & ~(size_t)255;
-    const size_t need = gc_bytes + bt_bytes + (size_t)H * ks * 128 * 128 * 4;
+    const size_t need = gc_bytes + bt_bytes + (size_t)H * ks * 128 * 64 * 4;
     if (!workspace || ((uintptr_t)workspace & 255u))
         return fail(LRKV_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
     if (workspace_bytes < need) return fail(LRKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
@@ -545,8 +545,8 @@ lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void
     g = lrkv::GemmArgs{};
     g.C = P; g.M = d_h; g.N = r; g.K = n_tok; g.a_zx = d_h; g.b_x0 = d_h; g.b_zx = r; g.nbatch = H; g.ksplit = ks;
     g.status = status_dev;
-    if ((e = train_gemm(tdK_mn, tY_mn, g, 128, true, true, true, st)) != cudaSuccess ||
-        (e = lrkv::launch_dB_reduce(P, static_cast<uint16_t*>(dB), H, ks, d_h, r, st)) != cudaSuccess)
+    if ((e = train_gemm(tdK_mn, tY_mn, g, 64, true, true, true, st)) != cudaSuccess ||
+        (e = lrkv::launch_dB_reduce(P, static_cast<uint16_t*>(dB), H, ks, d_h, r, 64, st)) != cudaSuccess)
         return cuda_status(e, "lrkv_train_backward launch");
     // dW_T = Gc^T X  ([d_h + H r][d]; A = Gc read [n (K)][Ncat (M)], B = X read [n (K)][d (N)])
     g = lrkv::GemmArgs{};

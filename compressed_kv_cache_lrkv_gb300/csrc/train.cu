@@ -324,8 +324,9 @@ __global__ void __launch_bounds__(192, 1)
 //   warp 1      TMEM owner; one thread issues dR_h = dK_h B_h (M = 128 tokens, N = r, K = d_h)
 //               into r TMEM columns per head;
 //   warps 2..5  add every dK_h tile into fp32 registers (one token row per thread: G), then
-//               store dR.  Rank 1 stages its partial G in its own idle ring and copies it in one
-//               bulk transfer into rank 0's idle ring; rank 0 adds it and rounds the sum once.
+//               store dR.  Each rank finishes half of G's columns: it stages the other half of
+//               its partial G in its idle ring and copies it in one bulk transfer into the
+//               peer's ring, then adds the peer's half to its own and rounds the sum once.
 // A ring slot is free once the MMAs (commit) and the four summing warps have read it.
 namespace {
 
@@ -359,8 +360,10 @@ struct DkCfg {
     static constexpr int NBOX = D_H / 64;
     static constexpr uint32_t TILE = NBOX * 16384u;  // one dK_h tile: 128 tokens x d_h
     static constexpr int STAGES = D_H == 128 ? 4 : 6;
-    static constexpr int PITCH = D_H + 4;            // floats per row of a staged partial G
+    static constexpr int HALF = D_H / 2;             // G columns finished by each rank
+    static constexpr int PITCH = HALF + 4;           // floats per row of a staged half of G
     static constexpr uint32_t GBYTES = 128u * PITCH * 4u;
+    static constexpr uint32_t GOFF = (GBYTES + 1023u) & ~1023u;  // where the peer's half lands
 };
 
 }  // namespace
@@ -369,7 +372,7 @@ template <int D_H>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     dk_pass_kernel(const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmBT, const DkArgs a) {
     using C = DkCfg<D_H>;
-    constexpr int NBOX = C::NBOX, NST = C::STAGES, PITCH = C::PITCH;
+    constexpr int NBOX = C::NBOX, NST = C::STAGES, PITCH = C::PITCH, HALF = C::HALF;
     constexpr uint32_t TILE = C::TILE;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -387,7 +390,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     uint64_t* empty = full + NST;
     uint64_t* cfull = empty + NST;  // B^T boxes landed
     uint64_t* accf = cfull + 1;     // every MMA of this CTA has completed
-    uint64_t* recv = accf + 1;      // rank 0: rank 1's partial G has landed in the ring
+    uint64_t* recv = accf + 1;      // the peer's half of G has landed in the ring
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv + 1);
     volatile int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -413,13 +416,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     if (warp == 0) {
         if (lane == 0) {
             const uint32_t cb = smem_u32(cfull);
-            mbar_arrive_expect_tx(cb, (uint32_t)nh * NBOX * BTB);
-            for (int hh = 0; hh < nh; ++hh)
+            bool bt_issued = false;
+            auto issue_bt = [&]() {
+                mbar_arrive_expect_tx(cb, (uint32_t)nh * NBOX * BTB);
+                for (int hh = 0; hh < nh; ++hh)
 #pragma unroll
-                for (int j = 0; j < NBOX; ++j)
-                    tma_load_2d(sBT + (hh * NBOX + j) * BTB, &tmBT, 64 * j, (h0 + hh) * r, cb);
+                    for (int j = 0; j < NBOX; ++j)
+                        tma_load_2d(sBT + (hh * NBOX + j) * BTB, &tmBT, 64 * j, (h0 + hh) * r, cb);
+                bt_issued = true;
+            };
             int issued = 0;
             for (int i = 0; i < nh; ++i) {
+                if (i == NST) issue_bt();  // the first tiles are on their way: now the B^T boxes
                 const int s = i % NST, hh = (i + hoff) % nh;
                 if ((i >= NST && !mbar_wait(smem_u32(&empty[s]), ((i / NST) - 1) & 1, a.status)) || *abort_flag) {
                     *abort_flag = 1;
@@ -432,6 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     tma_load_2d(sRing + s * TILE + j * 16384, &tmdK, (h0 + hh) * D_H + 64 * j, m0, bar);
                 issued = i + 1;
             }
+            if (!bt_issued) issue_bt();
             mbar_wait(cb, 0, a.status);  // the B^T boxes have landed before the CTA can exit
             if (*abort_flag)             // as have the tiles in flight
                 for (int k = max(0, issued - NST); k < issued; ++k)
@@ -489,26 +498,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         ok = ok && mbar_wait(smem_u32(accf), 0, a.status);
         if (!__all_sync(0xffffffffu, ok) && lane == 0) *abort_flag = 1;
         tc_fence_after();
-        if (rank == 1) {
-            // stage the partial G (fp32) in this CTA's idle ring for the copy to rank 0
-            float* dst = reinterpret_cast<float*>(smem) + (size_t)rl * PITCH;
+        // stage the half of the partial G that the peer finishes (rank 0 finishes columns
+        // [0, d_h / 2), rank 1 the rest) in this CTA's idle ring
+        float* dst = reinterpret_cast<float*>(smem) + (size_t)rl * PITCH;
+        if (rank == 0) {
 #pragma unroll
-            for (int c = 0; c < D_H; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(g[c], g[c + 1], g[c + 2], g[c + 3]);
-            fence_proxy_async_smem();  // generic writes, before the bulk copy reads them
-        } else if (threadIdx.x == 64) {
-            mbar_arrive_expect_tx(smem_u32(recv), C::GBYTES);
+            for (int c = 0; c < HALF; c += 4)
+                *reinterpret_cast<float4*>(dst + c) = make_float4(g[HALF + c], g[HALF + c + 1], g[HALF + c + 2], g[HALF + c + 3]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < HALF; c += 4)
+                *reinterpret_cast<float4*>(dst + c) = make_float4(g[c], g[c + 1], g[c + 2], g[c + 3]);
         }
+        fence_proxy_async_smem();  // generic writes, before the bulk copy reads them
+        if (threadIdx.x == 64) mbar_arrive_expect_tx(smem_u32(recv), C::GBYTES);
     }
-    // Barrier 1: both rings are idle (every stage consumed, every MMA complete), rank 1's partial
-    // G is staged and rank 0 expects it.
+    // Barrier 1: both rings are idle (every stage consumed, every MMA complete), each rank's half
+    // for the peer is staged and each rank expects the peer's.
     __syncwarp();
     cl_sync();
     if (warp >= 2) {
         const int rl = (warp & 3) * 32 + lane;
         const int row = m0 + rl;
         const bool ok = !*abort_flag;
-        if (rank == 1 && threadIdx.x == 64 && ok)
-            bulk_copy_to_peer(cl_map(sRing, 0), sRing, C::GBYTES, cl_map(smem_u32(recv), 0));
+        if (threadIdx.x == 64 && ok)
+            bulk_copy_to_peer(cl_map(sRing + C::GOFF, rank ^ 1), sRing, C::GBYTES, cl_map(smem_u32(recv), rank ^ 1));
         if (ok) {
             // dR of this CTA's heads: Gc columns d_h + h0 r .. + nh r
             uint16_t* grow = a.Gc + (size_t)row * a.ldg + D_H + h0 * r;
@@ -530,22 +544,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 }
             }
         }
-        if (rank == 0 && ok && mbar_wait(smem_u32(recv), 0, a.status) && row < a.n) {
-            const float* rv = reinterpret_cast<const float*>(smem) + (size_t)rl * PITCH;
+        if (ok && mbar_wait(smem_u32(recv), 0, a.status) && row < a.n) {
+            const float* rv = reinterpret_cast<const float*>(smem + C::GOFF) + (size_t)rl * PITCH;
+            uint16_t* grow = a.Gc + (size_t)row * a.ldg + rank * HALF;
+            auto finish = [&](const float* mine) {
 #pragma unroll
-            for (int c = 0; c < D_H; c += 8) {
-                const float4 x0 = *reinterpret_cast<const float4*>(rv + c);
-                const float4 x1 = *reinterpret_cast<const float4*>(rv + c + 4);
-                uint4 pk;
-                pk.x = pack_bf16x2(g[c] + x0.x, g[c + 1] + x0.y);
-                pk.y = pack_bf16x2(g[c + 2] + x0.z, g[c + 3] + x0.w);
-                pk.z = pack_bf16x2(g[c + 4] + x1.x, g[c + 5] + x1.y);
-                pk.w = pack_bf16x2(g[c + 6] + x1.z, g[c + 7] + x1.w);
-                *reinterpret_cast<uint4*>(a.Gc + (size_t)row * a.ldg + c) = pk;
-            }
+                for (int c = 0; c < HALF; c += 8) {
+                    const float4 x0 = *reinterpret_cast<const float4*>(rv + c);
+                    const float4 x1 = *reinterpret_cast<const float4*>(rv + c + 4);
+                    uint4 pk;
+                    pk.x = pack_bf16x2(mine[c] + x0.x, mine[c + 1] + x0.y);
+                    pk.y = pack_bf16x2(mine[c + 2] + x0.z, mine[c + 3] + x0.w);
+                    pk.z = pack_bf16x2(mine[c + 4] + x1.x, mine[c + 5] + x1.y);
+                    pk.w = pack_bf16x2(mine[c + 6] + x1.z, mine[c + 7] + x1.w);
+                    *reinterpret_cast<uint4*>(grow + c) = pk;
+                }
+            };
+            if (rank == 0) finish(g);
+            else finish(g + HALF);
         }
     }
-    // Barrier 2: rank 0 has received the copy, so rank 1's staging may go
+    // Barrier 2: both ranks have received the peer's copy, so the staging may go
     __syncwarp();
     cl_sync();
     tc_fence_before();
@@ -578,8 +597,8 @@ bool dk_pass_supported(int H, int d_h, int r) {
 
 template <int D_H>
 static cudaError_t launch_dk_t(const CUtensorMap& tdK, const CUtensorMap& tBT, const DkArgs& a, cudaStream_t stream) {
-    // the staged partial G fits in the ring
-    static_assert((size_t)DkCfg<D_H>::STAGES * DkCfg<D_H>::TILE >= DkCfg<D_H>::GBYTES, "ring");
+    // the staged half of G and the peer's half fit in the ring
+    static_assert((size_t)DkCfg<D_H>::STAGES * DkCfg<D_H>::TILE >= DkCfg<D_H>::GOFF + DkCfg<D_H>::GBYTES, "ring");
     // at least 120 KiB, so that one CTA runs per SM: each allocates all 512 TMEM columns, and a
     // second resident CTA would wait in its allocation for one that waits on its cluster peer
     const size_t need = dk_smem<D_H>(a.H, a.r), smem = need > 122880 ? need : 122880;
@@ -620,15 +639,15 @@ __global__ void __launch_bounds__(256) head_sum_kernel(const uint16_t* dK, uint1
     *reinterpret_cast<uint4*>(Gc + (size_t)t * ldg + c) = pk;
 }
 
-// dB[h][e][j] = sum_ks P[h][ks][e][j] in ks order, bf16.
+// dB[h][e][j] = sum_ks P[h][ks][e][j] in ks order, bf16 (partials [H][ks][128][pw]).
 __global__ void __launch_bounds__(256) dB_reduce_kernel(const float* P, uint16_t* dB, int H, int ksplit, int d_h,
-                                                        int r) {
+                                                        int r, int pw) {
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long long)H * d_h * r) return;
     const int h = (int)(idx / ((long long)d_h * r)), rem = (int)(idx % ((long long)d_h * r));
     const int e = rem / r, j = rem % r;
     float v = 0.f;
-    for (int ks = 0; ks < ksplit; ++ks) v += P[(((size_t)h * ksplit + ks) * kTM + e) * 128 + j];
+    for (int ks = 0; ks < ksplit; ++ks) v += P[(((size_t)h * ksplit + ks) * kTM + e) * pw + j];
     const __nv_bfloat16 b = __float2bfloat16_rn(v);
     dB[idx] = *reinterpret_cast<const uint16_t*>(&b);
 }
@@ -654,7 +673,7 @@ cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUt
     LRKV_TG(true, true, false, 256)    // dW_T
     LRKV_TG(false, true, false, 128)   // dR
     LRKV_TG(false, true, false, 256)   // dX
-    LRKV_TG(true, true, true, 128)     // dB partials
+    LRKV_TG(true, true, true, 64)      // dB partials
 #undef LRKV_TG
     return cudaErrorInvalidValue;
 }
@@ -665,9 +684,10 @@ cudaError_t launch_head_sum(const uint16_t* dK, uint16_t* Gc, int n, int H, int 
     return cudaGetLastError();
 }
 
-cudaError_t launch_dB_reduce(const float* P, uint16_t* dB, int H, int ksplit, int d_h, int r, cudaStream_t stream) {
+cudaError_t launch_dB_reduce(const float* P, uint16_t* dB, int H, int ksplit, int d_h, int r, int pw,
+                             cudaStream_t stream) {
     const long long total = (long long)H * d_h * r;
-    dB_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(P, dB, H, ksplit, d_h, r);
+    dB_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(P, dB, H, ksplit, d_h, r, pw);
     return cudaGetLastError();
 }
 

@@ -9,7 +9,7 @@
 namespace lrkv {
 
 // C = A . B on the tensor cores (bf16 operands, fp32 accumulation), 128 x BN output tiles
-// (BN = 128, 160 or 256), batched over nbatch * ksplit.  Operand boxes are read through 2-D
+// (BN = 64, 128, 160 or 256), batched over nbatch * ksplit.  Operand boxes are read through 2-D
 // tensor maps (128-byte swizzle): a K-major operand is a [rows][K] map read in 64-wide boxes of
 // 128 (A) or BN (B) rows, an MN-major one a [K][rows] map read in 64 x 64 boxes.  Coordinates of batch z start at
 // (x0 + z * zx, y0 + z * zy).  With kfix > 0 (K-major operands only) the first kfix K columns
@@ -32,8 +32,8 @@ struct GemmArgs {
 };
 
 // Launch C = A . B with 128 x bn tiles.  a_mn / b_mn: operand is MN-major; out_f32: fp32 split-K
-// partials (bn = 128).  Instantiated: expansion (K, K, bf16, 128), Y (K, K, bf16, 160), dW_T
-// (MN, MN, bf16, 256), dR (K, MN, bf16, 128), dX (K, MN, bf16, 256), dB (MN, MN, fp32, 128).
+// partials.  Instantiated: expansion (K, K, bf16, 128), Y (K, K, bf16, 160), dW_T (MN, MN, bf16,
+// 256), dR (K, MN, bf16, 128), dX (K, MN, bf16, 256), dB (MN, MN, fp32, 64).
 cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tB2, const CUtensorMap& tC,
                          const GemmArgs& g, int bn, bool a_mn, bool b_mn, bool out_f32, cudaStream_t stream);
 
@@ -57,7 +57,8 @@ cudaError_t launch_dk_pass(const CUtensorMap& tdK, const CUtensorMap& tBT, const
 // G[t] = sum_h dK[t][h][:] into columns [0, d_h) of Gc [n][ldg] (bf16, fp32 sums).
 cudaError_t launch_head_sum(const uint16_t* dK, uint16_t* Gc, int n, int H, int d_h, int ldg, cudaStream_t stream);
 
-// dB[h][e][j] = sum over split-K partials P[h][ks][e][0..127] (in ks order), j < r, bf16.
-cudaError_t launch_dB_reduce(const float* P, uint16_t* dB, int H, int ksplit, int d_h, int r, cudaStream_t stream);
+// dB[h][e][j] = sum over split-K partials P[h][ks][e][0..pw) (in ks order), j < r, bf16.
+cudaError_t launch_dB_reduce(const float* P, uint16_t* dB, int H, int ksplit, int d_h, int r, int pw,
+                             cudaStream_t stream);
 
 }  // namespace lrkv
