@@ -416,7 +416,7 @@ size_t lrkv_train_workspace_bytes(const lrkv_dims* dims, int32_t n_tok) {
     const size_t Ncat = (size_t)dims->d_h + (size_t)dims->H * dims->r;
     const size_t gc = ((size_t)n_tok * Ncat * 2 + 255) & ~(size_t)255;
     const size_t bt = ((size_t)dims->H * dims->r * dims->d_h * 2 + 255) & ~(size_t)255;
-    return gc + bt + (size_t)dims->H * train_dB_split(dims->H, n_tok, di.sms) * 128 * 64 * 4;
+    return gc + bt + 256 + (size_t)dims->H * train_dB_split(dims->H, n_tok, di.sms) * 128 * 64 * 4;
 }
 
 // Output map of a tcgen05 GEMM: set g->tma_out when the output can go through TMA (16-byte
@@ -442,8 +442,10 @@ static void train_out_map(lrkv::GemmArgs* g, CUtensorMap* tC) {
 static cudaError_t train_gemm(const CUtensorMap& tA, const CUtensorMap& tB, lrkv::GemmArgs g, int bn, bool a_mn,
                               bool b_mn, bool out_f32, cudaStream_t st, const CUtensorMap* tB2 = nullptr) {
     CUtensorMap tC = tA;
+    g.a_mn = a_mn;
+    g.b_mn = b_mn;
     if (!out_f32) train_out_map(&g, &tC);
-    return lrkv::launch_tgemm(tA, tB, tB2 ? *tB2 : tB, tC, g, bn, a_mn, b_mn, out_f32, st);
+    return lrkv::launch_tgemm(tA, tB, tB2 ? *tB2 : tB, tC, g, bn, out_f32, st);
 }
 
 lrkv_status lrkv_train_forward(const lrkv_dims* dims, const void* X, const void* W_T, const void* B, int32_t n_tok,
@@ -501,13 +503,14 @@ lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void
     const int ks = train_dB_split(H, n_tok, di.sms);
     const size_t gc_bytes = ((size_t)n_tok * Ncat * 2 + 255) & ~(size_t)255;
     const size_t bt_bytes = ((size_t)H * r * d_h * 2 + 255) & ~(size_t)255;
-    const size_t need = gc_bytes + bt_bytes + (size_t)H * ks * 128 * 64 * 4;
+    const size_t need = gc_bytes + bt_bytes + 256 + (size_t)H * ks * 128 * 64 * 4;
     if (!workspace || ((uintptr_t)workspace & 255u))
         return fail(LRKV_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
     if (workspace_bytes < need) return fail(LRKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
     uint16_t* Gc = static_cast<uint16_t*>(workspace);
     uint16_t* BT = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + gc_bytes);
-    float* P = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gc_bytes + bt_bytes);
+    int* ctr = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + gc_bytes + bt_bytes);
+    float* P = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gc_bytes + bt_bytes + 256);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     CUtensorMap tdK_k, tdK_mn, tB_mn, tY_mn, tGc_mn, tGc_k, tX_mn, tW_mn;
     const uint64_t HD = (uint64_t)H * d_h;
@@ -548,15 +551,23 @@ lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void
     if ((e = train_gemm(tdK_mn, tY_mn, g, 64, true, true, true, st)) != cudaSuccess ||
         (e = lrkv::launch_dB_reduce(P, static_cast<uint16_t*>(dB), H, ks, d_h, r, 64, st)) != cudaSuccess)
         return cuda_status(e, "lrkv_train_backward launch");
-    // dW_T = Gc^T X  ([d_h + H r][d]; A = Gc read [n (K)][Ncat (M)], B = X read [n (K)][d (N)])
-    g = lrkv::GemmArgs{};
-    g.C = dW_T; g.ldc = d; g.M = Ncat; g.N = d; g.K = n_tok; g.nbatch = 1; g.ksplit = 1; g.status = status_dev;
-    if ((e = train_gemm(tGc_mn, tX_mn, g, 256, true, true, false, st)) != cudaSuccess)
+    // One launch for both products of Gc, whose CTAs take tiles from a shared queue: the long
+    // tiles of dW_T first (fewer than the SMs), the short tiles of dX filling the other SMs.
+    //   dW_T = Gc^T X  ([d_h + H r][d]; A = Gc read [n (K)][Ncat (M)], B = X read [n (K)][d (N)])
+    //   dX = Gc W_T    (A = Gc K-major, B = W_T read [Ncat (K)][d (N)])
+    lrkv::GemmArgs gg[2] = {};
+    gg[0].C = dW_T; gg[0].ldc = d; gg[0].M = Ncat; gg[0].N = d; gg[0].K = n_tok; gg[0].a_mn = 1; gg[0].b_mn = 1;
+    gg[1].C = dX; gg[1].ldc = d; gg[1].M = n_tok; gg[1].N = d; gg[1].K = Ncat; gg[1].a_mn = 0; gg[1].b_mn = 1;
+    CUtensorMap tA2[2] = {tGc_mn, tGc_k}, tB2m[2] = {tX_mn, tW_mn}, tC2[2];
+    for (int i = 0; i < 2; ++i) {
+        gg[i].nbatch = 1; gg[i].ksplit = 1; gg[i].status = status_dev;
+        train_out_map(&gg[i], &tC2[i]);
+    }
+    if (gg[0].tma_out && gg[1].tma_out)
+        return cuda_status(lrkv::launch_tgemm2(tA2, tB2m, tC2, gg, 256, ctr, st), "lrkv_train_backward launch");
+    if ((e = train_gemm(tGc_mn, tX_mn, gg[0], 256, true, true, false, st)) != cudaSuccess)
         return cuda_status(e, "lrkv_train_backward launch");
-    // dX = Gc W_T  (A = Gc K-major, B = W_T read [Ncat (K)][d (N)])
-    g = lrkv::GemmArgs{};
-    g.C = dX; g.ldc = d; g.M = n_tok; g.N = d; g.K = Ncat; g.nbatch = 1; g.ksplit = 1; g.status = status_dev;
-    return cuda_status(train_gemm(tGc_k, tW_mn, g, 256, false, true, false, st), "lrkv_train_backward launch");
+    return cuda_status(train_gemm(tGc_k, tW_mn, gg[1], 256, false, true, false, st), "lrkv_train_backward launch");
 }
 
 size_t lrkv_mla_cache_block_bytes(const lrkv_mla_dims* dims) {

@@ -28,6 +28,8 @@
 #include "lrkv_internal.cuh"
 #include "train.h"
 
+#include <cstring>
+
 namespace lrkv {
 
 namespace {
@@ -90,10 +92,8 @@ const void* train_identity() {
     return cudaGetSymbolAddress(&p, g_identity) == cudaSuccess ? p : nullptr;
 }
 
-template <bool AMN, bool BMN, bool OUTF32, int BN>
-__global__ void __launch_bounds__(192, 1)
-    tgemm_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
-                 const __grid_constant__ CUtensorMap tB2, const __grid_constant__ CUtensorMap tC, const GemmArgs g) {
+template <bool OUTF32, int BN, bool GROUPED>
+__global__ void __launch_bounds__(192, 1) tgemm_kernel(const __grid_constant__ TGemmParams p) {
     using C = TCfg<BN>;
     constexpr int kS = C::STAGES, NBOX = C::NBOX;
     constexpr uint32_t T_B = C::B;
@@ -107,28 +107,44 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* empty = full + kS;
     uint64_t* acc_full = empty + kS;      // [2] accumulator buffer holds a finished tile
     uint64_t* acc_empty = acc_full + 2;   // [2] the epilogue has read it (128 arrivals)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    uint64_t* wq_full = acc_empty + 2;    // [4] work queue: the producer published an item
+    uint64_t* wq_empty = wq_full + 4;     // [4] the MMA thread and the 4 epilogue warps read it
+    int* wq = reinterpret_cast<int*>(wq_empty + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wq + 4);
     volatile int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+    uint32_t* status = p.g[0].status;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_n = (g.N + BN - 1) / BN, tiles_m = (g.M + kTM - 1) / kTM;
-    const int total = tiles_n * tiles_m * g.nbatch * g.ksplit;
-    const int KT_all = (g.K + kTK - 1) / kTK;
-    const int per = (KT_all + g.ksplit - 1) / g.ksplit;
-    // tile -> (n tile, m tile, batch, k split); n fastest, so consecutive CTAs share A rows in L2
+    const bool dyn = GROUPED && p.ctr != nullptr;
+    // work item -> (group, n tile, m tile, batch, k split); n fastest, so consecutive items share
+    // A rows in L2; group 0's items come first
     struct Tile {
-        int n0, m0, z, batch, kt0, KT;
+        int grp, n0, m0, z, batch, kt0, KT;
     };
-    auto tile_of = [&](int t) {
+    auto tile_of = [&](int w) {
         Tile r;
+        r.grp = GROUPED && w >= p.tiles0 ? 1 : 0;
+        const GemmArgs& g = p.g[r.grp];
+        const int t = w - (r.grp ? p.tiles0 : 0);
+        const int tiles_n = (g.N + BN - 1) / BN, tiles_m = (g.M + kTM - 1) / kTM;
+        const int KT_all = (g.K + kTK - 1) / kTK;
+        const int per = (KT_all + g.ksplit - 1) / g.ksplit;
         r.n0 = (t % tiles_n) * BN;
         r.m0 = ((t / tiles_n) % tiles_m) * kTM;
         r.z = t / (tiles_n * tiles_m);
         r.batch = r.z / g.ksplit;
-        const int ks = r.z % g.ksplit;
-        r.kt0 = ks * per;
+        r.kt0 = (r.z % g.ksplit) * per;
         r.KT = max(0, min(KT_all, r.kt0 + per) - r.kt0);
         return r;
+    };
+    // Work item of local iteration `it` for the MMA thread and the epilogue: the round-robin one,
+    // or the one the producer took from the queue (returns total at the end; arrives as reader)
+    auto next_item = [&](int it, bool lead, bool& ok) -> int {
+        if (!dyn) return blockIdx.x + it * gridDim.x < p.total ? (int)(blockIdx.x + it * gridDim.x) : p.total;
+        ok = ok && mbar_wait(smem_u32(&wq_full[it & 3]), (it >> 2) & 1, status);
+        const int w = ok ? wq[it & 3] : p.total;
+        if (lead) mbar_arrive(smem_u32(&wq_empty[it & 3]));
+        return w;
     };
 
     if (threadIdx.x == 0) {
@@ -139,6 +155,10 @@ __global__ void __launch_bounds__(192, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&acc_full[b]), 1);
             mbar_init(smem_u32(&acc_empty[b]), 128);
+        }
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(smem_u32(&wq_full[q]), 1);
+            mbar_init(smem_u32(&wq_empty[q]), 5);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -153,13 +173,33 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             int q = 0;  // K slices issued by this CTA (ring position and phase)
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = tile_of(t);
+            for (int it = 0; ok; ++it) {
+                int w;
+                if (dyn) {
+                    // take the next item and publish it (the first one is this CTA's own)
+                    w = it == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(p.ctr, 1);
+                    if (w > p.total) w = p.total;
+                    if (it >= 4 && !mbar_wait(smem_u32(&wq_empty[it & 3]), ((it >> 2) - 1) & 1, status)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    wq[it & 3] = w;
+                    mbar_arrive(smem_u32(&wq_full[it & 3]));
+                } else {
+                    w = blockIdx.x + it * gridDim.x;
+                }
+                if (w >= p.total) break;
+                const Tile tl = tile_of(w);
+                const GemmArgs& g = p.g[tl.grp];
+                const CUtensorMap* mA = GROUPED && tl.grp ? &p.A[1] : &p.A[0];
+                const CUtensorMap* mB = GROUPED && tl.grp ? &p.B[1] : &p.B[0];
                 const int ax = g.a_x0 + tl.batch * g.a_zx, ay = g.a_y0 + tl.batch * g.a_zy;
                 const int bx = g.b_x0 + tl.batch * g.b_zx, by = g.b_y0 + tl.batch * g.b_zy;
+                const bool amn = g.a_mn != 0, bmn = g.b_mn != 0;
+                const int kfix = (amn || bmn) ? 0 : g.kfix;
                 for (int i = 0; i < tl.KT; ++i, ++q) {
                     const int s = q % kS;
-                    if ((q >= kS && !mbar_wait(smem_u32(&empty[s]), ((q / kS) - 1) & 1, g.status)) || *abort_flag) {
+                    if ((q >= kS && !mbar_wait(smem_u32(&empty[s]), ((q / kS) - 1) & 1, status)) || *abort_flag) {
                         *abort_flag = 1;
                         ok = false;
                         break;
@@ -167,41 +207,48 @@ __global__ void __launch_bounds__(192, 1)
                     const int k = (tl.kt0 + i) * kTK;
                     const uint32_t bar = smem_u32(&full[s]);
                     mbar_arrive_expect_tx(bar, T_A + T_B);
-                    if (!AMN && !BMN && k < g.kfix) {
+                    if (k < kfix) {
                         // leading K columns shared by every batch: A at x = k, B from the second map
-                        tma_load_2d(sA + s * T_A, &tA, k, ay + tl.m0, bar);
-                        tma_load_2d(sB + s * T_B, &tB2, k, tl.n0, bar);
+                        tma_load_2d(sA + s * T_A, mA, k, ay + tl.m0, bar);
+                        tma_load_2d(sB + s * T_B, &p.B2, k, tl.n0, bar);
                         continue;
                     }
-                    const int kb = k - g.kfix;
-                    if (AMN) {
-                        tma_load_2d(sA + s * T_A, &tA, ax + tl.m0, ay + k, bar);
-                        tma_load_2d(sA + s * T_A + 8192, &tA, ax + tl.m0 + 64, ay + k, bar);
+                    const int kb = k - kfix;
+                    if (amn) {
+                        tma_load_2d(sA + s * T_A, mA, ax + tl.m0, ay + k, bar);
+                        tma_load_2d(sA + s * T_A + 8192, mA, ax + tl.m0 + 64, ay + k, bar);
                     } else {
-                        tma_load_2d(sA + s * T_A, &tA, ax + kb, ay + tl.m0, bar);
+                        tma_load_2d(sA + s * T_A, mA, ax + kb, ay + tl.m0, bar);
                     }
-                    if (BMN) {
+                    if (bmn) {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j) tma_load_2d(sB + s * T_B + j * 8192, &tB, bx + tl.n0 + 64 * j, by + k, bar);
+                        for (int j = 0; j < BN / 64; ++j) tma_load_2d(sB + s * T_B + j * 8192, mB, bx + tl.n0 + 64 * j, by + k, bar);
                     } else {
-                        tma_load_2d(sB + s * T_B, &tB, bx + kb, by + tl.n0, bar);  // one [BN][64] box
+                        tma_load_2d(sB + s * T_B, mB, bx + kb, by + tl.n0, bar);  // one [BN][64] box
                     }
                 }
             }
-            if (!ok)  // let the copies in flight land before the CTA exits
-                for (int k = max(0, q - kS); k < q; ++k) mbar_wait(smem_u32(&full[k % kS]), (k / kS) & 1, g.status);
+            if (*abort_flag)  // let the copies in flight land before the CTA exits
+                for (int k = max(0, q - kS); k < q; ++k) mbar_wait(smem_u32(&full[k % kS]), (k / kS) & 1, status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc =
-                idesc_bf16_f32(kTM, BN) | ((AMN ? 1u : 0u) << 15) | ((BMN ? 1u : 0u) << 16);
-            int q = 0, it = 0;
+            constexpr uint32_t idesc0 = idesc_bf16_f32(kTM, BN);
+            int q = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-                const Tile tl = tile_of(t);
+            for (int it = 0; ok; ++it) {
+                const int w = next_item(it, true, ok);
+                if (!ok || w >= p.total) break;
+                const Tile tl = tile_of(w);
+                const bool amn = p.g[tl.grp].a_mn != 0, bmn = p.g[tl.grp].b_mn != 0;
+                const uint32_t idesc = idesc0 | ((uint32_t)amn << 15) | ((uint32_t)bmn << 16);
+                // descriptor of K step 0 and the per-step advance (16 B in the encoded start address
+                // field per 16 elements: 2 for a K-major row step of 32 B, 128 for 2 KiB of an MN-major block)
+                const uint64_t a_base = amn ? mnmaj(sA) : kmaj(sA), b_base = bmn ? mnmaj(sB) : kmaj(sB);
+                const uint64_t a_kk = amn ? 128 : 2, b_kk = bmn ? 128 : 2;
                 const int buf = it & 1;
                 // the epilogue must have read this buffer's previous tile
-                if (it >= 2 && !mbar_wait(smem_u32(&acc_empty[buf]), ((it >> 1) - 1) & 1, g.status)) {
+                if (it >= 2 && !mbar_wait(smem_u32(&acc_empty[buf]), ((it >> 1) - 1) & 1, status)) {
                     ok = false;
                     break;
                 }
@@ -209,18 +256,15 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t acc = tmem + buf * BN;
                 for (int i = 0; i < tl.KT; ++i, ++q) {
                     const int s = q % kS;
-                    if (*abort_flag || !mbar_wait(smem_u32(&full[s]), (q / kS) & 1, g.status)) {
+                    if (*abort_flag || !mbar_wait(smem_u32(&full[s]), (q / kS) & 1, status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    const uint64_t a_s = a_base + (uint64_t)((s * T_A) >> 4), b_s = b_base + (uint64_t)((s * T_B) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kTK / 16; ++kk) {
-                        // a K step of 16: 32 bytes along a K-major row, 16 rows (2 KiB) of an MN-major block
-                        const uint64_t ad = AMN ? mnmaj(sA + s * T_A + kk * 2048) : kmaj(sA + s * T_A + kk * 32);
-                        const uint64_t bd = BMN ? mnmaj(sB + s * T_B + kk * 2048) : kmaj(sB + s * T_B + kk * 32);
-                        tc_mma_bf16(acc, ad, bd, idesc, (i | kk) != 0);
-                    }
+                    for (int kk = 0; kk < kTK / 16; ++kk)
+                        tc_mma_bf16(acc, a_s + kk * a_kk, b_s + kk * b_kk, idesc, (i | kk) != 0);
                     tc_commit(smem_u32(&empty[s]));
                 }
                 if (!ok) break;
@@ -234,16 +278,24 @@ __global__ void __launch_bounds__(192, 1)
         // j ^ ((i >> 1) & 3), so the 16-byte stores are conflict-free) and one lane stores the box
         // by TMA; the boxes form a ring per warp.
         const int q4 = warp & 3;
-        const bool tma = !OUTF32 && g.tma_out;
         uint8_t* stg = stg_base + q4 * (NBOX * kTBox);
         const uint32_t stg_s = smem_u32(stg);
         const int swz = (lane >> 1) & 3;
-        int it = 0, qc = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-            const Tile tl = tile_of(t);
+        int qc = 0;
+        bool used_tma = false;
+        bool okq = true;
+        for (int it = 0;; ++it) {
+            int w = next_item(it, false, okq);
+            __syncwarp();
+            if (dyn && lane == 0) mbar_arrive(smem_u32(&wq_empty[it & 3]));
+            if (!okq || w >= p.total) break;
+            const Tile tl = tile_of(w);
+            const GemmArgs& g = p.g[tl.grp];
+            const bool tma = !OUTF32 && g.tma_out;
+            const CUtensorMap* mC = GROUPED && tl.grp ? &p.C[1] : &p.C[0];
             const int buf = it & 1;
             const int ry = tl.m0 + q4 * 32;  // this warp's first output row
-            bool ok = !*abort_flag && mbar_wait(smem_u32(&acc_full[buf]), (it >> 1) & 1, g.status);
+            bool ok = !*abort_flag && mbar_wait(smem_u32(&acc_full[buf]), (it >> 1) & 1, status);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 if (lane == 0) *abort_flag = 1;
@@ -259,6 +311,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = 0u;
                 if (tma) {
+                    used_tma = true;
                     const int box = qc % NBOX;
                     if (lane == 0) bulk_wait_read<NBOX - 1>();  // the store that last used this box has read it
                     __syncwarp();
@@ -275,7 +328,7 @@ __global__ void __launch_bounds__(192, 1)
                     fence_proxy_async_smem();  // the generic stores above, before the async-proxy read
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(&tC, stg_s + box * kTBox, tl.n0 + c0, tl.batch, ry);
+                        tma_store_3d(mC, stg_s + box * kTBox, tl.n0 + c0, tl.batch, ry);
                         bulk_commit();
                     }
                 } else if (OUTF32) {
@@ -305,7 +358,7 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(&acc_empty[buf]));
         }
-        if (tma && lane == 0) bulk_wait0();
+        if (used_tma && lane == 0) bulk_wait0();
     }
     tc_fence_before();
     __syncthreads();
@@ -652,30 +705,70 @@ __global__ void __launch_bounds__(256) dB_reduce_kernel(const float* P, uint16_t
     dB[idx] = *reinterpret_cast<const uint16_t*>(&b);
 }
 
-cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tB2, const CUtensorMap& tC,
-                         const GemmArgs& g, int bn, bool a_mn, bool b_mn, bool out_f32, cudaStream_t stream) {
-    // persistent: one CTA per SM (ring and staging fill its shared memory) looping over the tiles
+static int tgemm_tiles(const GemmArgs& g, int bn) {
+    return ((g.N + bn - 1) / bn) * ((g.M + kTM - 1) / kTM) * g.nbatch * g.ksplit;
+}
+
+// One launch over p.ngroups products (their tiles in order: group 0 first); dynamic: items after
+// each CTA's first come from the queue at p.ctr, which must be zero at launch.
+static cudaError_t tgemm_launch(TGemmParams& p, int bn, bool out_f32, bool dynamic, cudaStream_t stream) {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g.kfix % kTK != 0 || (g.kfix > 0 && (a_mn || b_mn))) return cudaErrorInvalidValue;
-    const long long tiles = (long long)((g.N + bn - 1) / bn) * ((g.M + kTM - 1) / kTM) * g.nbatch * g.ksplit;
-    const dim3 grid((unsigned)(tiles < sms ? tiles : sms));
-#define LRKV_TG(AM, BM, OF, NB)                                                                                \
-    if (a_mn == AM && b_mn == BM && out_f32 == OF && bn == NB) {                                               \
-        auto kern = tgemm_kernel<AM, BM, OF, NB>;                                                              \
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TCfg<NB>::SMEM); \
-        if (e != cudaSuccess) return e;                                                                        \
-        kern<<<grid, 192, TCfg<NB>::SMEM, stream>>>(tA, tB, tB2, tC, g);                                       \
-        return cudaGetLastError();                                                                             \
+    for (int i = 0; i < p.ngroups; ++i) {
+        const GemmArgs& g = p.g[i];
+        if (g.kfix % kTK != 0 || (g.kfix > 0 && (g.a_mn || g.b_mn || i > 0))) return cudaErrorInvalidValue;
     }
-    LRKV_TG(false, false, false, 128)  // expansion
-    LRKV_TG(false, false, false, 160)  // Y
-    LRKV_TG(true, true, false, 256)    // dW_T
-    LRKV_TG(false, true, false, 128)   // dR
-    LRKV_TG(false, true, false, 256)   // dX
-    LRKV_TG(true, true, true, 64)      // dB partials
+    p.tiles0 = tgemm_tiles(p.g[0], bn);
+    p.total = p.tiles0 + (p.ngroups > 1 ? tgemm_tiles(p.g[1], bn) : 0);
+    if (p.total == 0) return cudaSuccess;
+    if (!dynamic) p.ctr = nullptr;
+    const dim3 grid((unsigned)(p.total < sms ? p.total : sms));
+#define LRKV_TG(OF, NB, GR)                                                                                     \
+    if (out_f32 == OF && bn == NB && (p.ngroups > 1) == GR) {                                                   \
+        auto kern = tgemm_kernel<OF, NB, GR>;                                                                   \
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TCfg<NB>::SMEM); \
+        if (e != cudaSuccess) return e;                                                                         \
+        kern<<<grid, 192, TCfg<NB>::SMEM, stream>>>(p);                                                         \
+        return cudaGetLastError();                                                                              \
+    }
+    LRKV_TG(false, 128, false)  // expansion, dR
+    LRKV_TG(false, 160, false)  // Y
+    LRKV_TG(false, 256, false)  // dW_T or dX alone
+    LRKV_TG(false, 256, true)   // dW_T and dX together
+    LRKV_TG(true, 64, false)    // dB partials
 #undef LRKV_TG
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tB2, const CUtensorMap& tC,
+                         const GemmArgs& g, int bn, bool out_f32, cudaStream_t stream) {
+    TGemmParams p;
+    memset(&p, 0, sizeof(p));
+    p.A[0] = p.A[1] = tA;
+    p.B[0] = p.B[1] = tB;
+    p.C[0] = p.C[1] = tC;
+    p.B2 = tB2;
+    p.g[0] = p.g[1] = g;
+    p.ngroups = 1;
+    return tgemm_launch(p, bn, out_f32, false, stream);
+}
+
+cudaError_t launch_tgemm2(const CUtensorMap* tA, const CUtensorMap* tB, const CUtensorMap* tC, const GemmArgs* g, int bn,
+                          int* ctr, cudaStream_t stream) {
+    TGemmParams p;
+    memset(&p, 0, sizeof(p));
+    for (int i = 0; i < 2; ++i) {
+        p.A[i] = tA[i];
+        p.B[i] = tB[i];
+        p.C[i] = tC[i];
+        p.g[i] = g[i];
+    }
+    p.B2 = tB[0];
+    p.ngroups = 2;
+    p.ctr = ctr;
+    cudaError_t e = cudaMemsetAsync(ctr, 0, sizeof(int), stream);
+    if (e != cudaSuccess) return e;
+    return tgemm_launch(p, bn, false, true, stream);
 }
 
 cudaError_t launch_head_sum(const uint16_t* dK, uint16_t* Gc, int n, int H, int d_h, int ldg, cudaStream_t stream) {

@@ -27,15 +27,30 @@ struct GemmArgs {
     int b_x0, b_y0, b_zx, b_zy;
     int nbatch, ksplit;
     int kfix;                 // leading K columns shared by all batches (multiple of 64)
-    int tma_out;              // 1: store through tC
+    int a_mn, b_mn;           // operand is MN-major ([K][rows] map) rather than K-major
+    int tma_out;              // 1: store through the output map
     uint32_t* status;
 };
 
-// Launch C = A . B with 128 x bn tiles.  a_mn / b_mn: operand is MN-major; out_f32: fp32 split-K
-// partials.  Instantiated: expansion (K, K, bf16, 128), Y (K, K, bf16, 160), dW_T (MN, MN, bf16,
-// 256), dR (K, MN, bf16, 128), dX (K, MN, bf16, 256), dB (MN, MN, fp32, 64).
+// Operand and output maps and arguments of up to two products run by one launch (their tiles
+// concatenated, group 0 first); B2 is the second B map of group 0 (kfix).
+struct TGemmParams {
+    CUtensorMap A[2], B[2], C[2], B2;
+    GemmArgs g[2];
+    int ngroups;
+    int tiles0, total;  // tiles of group 0, of all groups
+    int* ctr;           // work queue (zero at launch) or null: round-robin tiles
+};
+
+// Launch C = A . B with 128 x bn tiles (operand majors in g.a_mn / g.b_mn); out_f32: fp32 split-K
+// partials.  Tile widths: expansion and dR 128, Y 160, dW_T and dX 256, dB partials 64 (fp32).
 cudaError_t launch_tgemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tB2, const CUtensorMap& tC,
-                         const GemmArgs& g, int bn, bool a_mn, bool b_mn, bool out_f32, cudaStream_t stream);
+                         const GemmArgs& g, int bn, bool out_f32, cudaStream_t stream);
+
+// Two bf16-output products in one launch whose CTAs take tiles from a shared queue (`ctr`, one int
+// of device memory, zeroed here first): group 0's tiles are handed out first.
+cudaError_t launch_tgemm2(const CUtensorMap* tA, const CUtensorMap* tB, const CUtensorMap* tC, const GemmArgs* g, int bn,
+                          int* ctr, cudaStream_t stream);
 
 // Device address of a 128 x 128 bf16 identity matrix (row-major), or null.
 const void* train_identity();
