@@ -344,7 +344,8 @@ class PrefillHarness:
                 q=rn(B, C, H, d_h), qs=i32([c0] * B),
                 out=torch.empty(B, C, H, d_h, dtype=torch.bfloat16, device="cuda")))
         self.side = torch.cuda.Stream()
-        self.fork, self.join = torch.cuda.Event(), torch.cuda.Event()
+        self.p2 = torch.cuda.Stream()  # every other chunk's prefill
+        self.fork, self.join, self.join2 = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
         self.appended = [torch.cuda.Event() for _ in self.chunks]
         app = A.append_flops(B * T, d, H, d_h, r)
         pre = sum(A.prefill_flops(B, C, H, d_h, r, q_start=c0) for c0 in range(0, T, C))
@@ -355,26 +356,37 @@ class PrefillHarness:
 
     def step(self, stream):
         """Chunk c's prefill needs chunk c's rows in the cache; chunk c+1's append only writes
-        rows that prefill c never reads (its keys end with chunk c).  So the appends run in
-        order on a side stream, each prefill waits for its own chunk's append, and the side
-        stream's GEMMs fill the SMs the prefill's last wave of CTAs leaves idle."""
+        rows that prefill c never reads (its keys end with chunk c), and no prefill reads
+        another's output.  So the appends run in order on a side stream, each prefill waits
+        for its own chunk's append, and the prefills alternate between two streams: the side
+        stream's GEMMs and the next chunk's CTAs fill the SMs a prefill's last wave leaves idle."""
         b, side = self.b, self.side
         self.fork.record(stream)
         side.wait_event(self.fork)
+        self.p2.wait_event(self.fork)
         for ch, ev in zip(self.chunks, self.appended):
             b.lrkv_append(self.dims, ch["x"], self.wcat, ch["slots"], self.cache, status=self.status, stream=side)
             ev.record(side)
-        for ch, ev in zip(self.chunks, self.appended):
-            stream.wait_event(ev)
+        for i, (ch, ev) in enumerate(zip(self.chunks, self.appended)):
+            st = stream if i % 2 == 0 else self.p2
+            st.wait_event(ev)
             b.lrkv_prefill(self.dims, ch["q"], self.BK, self.BV, self.cache, self.bt, ch["qs"], ch["out"],
-                           status=self.status, stream=stream)
+                           status=self.status, stream=st)
         self.join.record(side)
+        self.join2.record(self.p2)
         stream.wait_event(self.join)
+        stream.wait_event(self.join2)
 
     def kernel(self, stream):
-        for ch in self.chunks:
+        """The eight chunk prefills alone (cache already filled), alternating between two
+        streams as in the step."""
+        self.fork.record(stream)
+        self.p2.wait_event(self.fork)
+        for i, ch in enumerate(self.chunks):
             self.b.lrkv_prefill(self.dims, ch["q"], self.BK, self.BV, self.cache, self.bt, ch["qs"], ch["out"],
-                                status=self.status, stream=stream)
+                                status=self.status, stream=stream if i % 2 == 0 else self.p2)
+        self.join2.record(self.p2)
+        stream.wait_event(self.join2)
 
     def e2e_setup(self):
         t = self.torch
@@ -402,11 +414,13 @@ class PrefillHarness:
                        "H": wl.H, "d_h": wl.d_h, "r": wl.r, "d": wl.d, "block_size": 64,
                        "l2": "prompt activations (X, q, out: 192 MiB) larger than L2",
                        "step": "per 512-token chunk: lrkv_append (1024 rows) + lrkv_prefill; the appends run on a "
-                               "side stream (chunk c+1's append overlaps chunk c's prefill)",
+                               "side stream (chunk c+1's append overlaps chunk c's prefill) and the prefills "
+                               "alternate between two streams (chunk c+1's CTAs fill chunk c's last wave)",
                        "flops_per_step": self.step_units, "append_flops": self.app_flops,
                        "prefill_flops": self.kernel_units,
                        "parallelism": f"replicas x{world} (independent batches)"},
-            "roofline": {"kernel": "lrkv_prefill (8 chunk launches)", "bound": "tensor", "achieved": achieved,
+            "roofline": {"kernel": "lrkv_prefill (8 chunk launches on two streams)", "bound": "tensor",
+                         "achieved": achieved,
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                          "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                          "traffic": recorded_traffic(self.profile, self.sources),
