@@ -416,7 +416,9 @@ size_t lrkv_train_workspace_bytes(const lrkv_dims* dims, int32_t n_tok) {
     const size_t Ncat = (size_t)dims->d_h + (size_t)dims->H * dims->r;
     const size_t gc = ((size_t)n_tok * Ncat * 2 + 255) & ~(size_t)255;
     const size_t bt = ((size_t)dims->H * dims->r * dims->d_h * 2 + 255) & ~(size_t)255;
-    return gc + bt + 256 + (size_t)dims->H * train_dB_split(dims->H, n_tok, di.sms) * 128 * 64 * 4;
+    const size_t split = (size_t)train_dB_split(dims->H, n_tok, di.sms) * 128 * 64;
+    const size_t tiles = (size_t)((n_tok + 127) / 128) * 128 * 16;  // partials of the folded dB
+    return gc + bt + 256 + (size_t)dims->H * (split > tiles ? split : tiles) * 4;
 }
 
 // Output map of a tcgen05 GEMM: set g->tma_out when the output can go through TMA (16-byte
@@ -503,7 +505,10 @@ lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void
     const int ks = train_dB_split(H, n_tok, di.sms);
     const size_t gc_bytes = ((size_t)n_tok * Ncat * 2 + 255) & ~(size_t)255;
     const size_t bt_bytes = ((size_t)H * r * d_h * 2 + 255) & ~(size_t)255;
-    const size_t need = gc_bytes + bt_bytes + 256 + (size_t)H * ks * 128 * 64 * 4;
+    const int ntiles = (n_tok + 127) / 128;
+    const bool fold_dB = lrkv::dk_pass_folds_dB(H, d_h, r);
+    const size_t pfl = fold_dB ? (size_t)ntiles * 128 * 16 : (size_t)ks * 128 * 64;  // floats per head
+    const size_t need = gc_bytes + bt_bytes + 256 + (size_t)H * pfl * 4;
     if (!workspace || ((uintptr_t)workspace & 255u))
         return fail(LRKV_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
     if (workspace_bytes < need) return fail(LRKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
@@ -527,12 +532,16 @@ lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void
     lrkv::GemmArgs g{};
     if (lrkv::dk_pass_supported(H, d_h, r)) {
         // one pass over dK: Gc[:, 0:d_h] = G = sum_h dK_h and Gc[:, d_h + h r ..] = dR_h = dK_h B_h
-        CUtensorMap tBT;
-        if ((s = make_tmap(&tBT, BT, d_h, (uint64_t)H * r, 64, r, CU_TENSOR_MAP_SWIZZLE_128B, "B^T")) != LRKV_OK)
+        CUtensorMap tBT, tR = tdK_k;
+        if ((s = make_tmap(&tBT, BT, d_h, (uint64_t)H * r, 64, r, CU_TENSOR_MAP_SWIZZLE_128B, "B^T")) != LRKV_OK ||
+            (fold_dB && (s = make_tmap(&tR, Y, Ncat, n_tok, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B, "R")) != LRKV_OK))
             return s;
         lrkv::DkArgs da{};
         da.Gc = Gc; da.ldg = Ncat; da.n = n_tok; da.H = H; da.d_h = d_h; da.r = r; da.status = status_dev;
-        if ((e = lrkv::launch_dk_pass(tdK_k, tBT, static_cast<const uint16_t*>(B), BT, da, st)) != cudaSuccess)
+        // dB_h's per-tile partials too (the same dK_h tiles against R_h), summed in tile order
+        da.dBp = fold_dB ? P : nullptr;
+        da.rx0 = d_h;
+        if ((e = lrkv::launch_dk_pass(tdK_k, tBT, tR, static_cast<const uint16_t*>(B), BT, da, st)) != cudaSuccess)
             return cuda_status(e, "lrkv_train_backward launch");
     } else {
         // Gc[:, 0:d_h] = G = sum_h dK_h
@@ -544,13 +553,18 @@ lrkv_status lrkv_train_backward(const lrkv_dims* dims, const void* X, const void
         if ((e = train_gemm(tdK_k, tB_mn, g, 128, false, true, false, st)) != cudaSuccess)
             return cuda_status(e, "lrkv_train_backward launch");
     }
-    // dB_h = dK_h^T R_h: split-K partials (A = dK read [n (K)][d_h (M)], B = R_h read [n (K)][r (N)])
-    g = lrkv::GemmArgs{};
-    g.C = P; g.M = d_h; g.N = r; g.K = n_tok; g.a_zx = d_h; g.b_x0 = d_h; g.b_zx = r; g.nbatch = H; g.ksplit = ks;
-    g.status = status_dev;
-    if ((e = train_gemm(tdK_mn, tY_mn, g, 64, true, true, true, st)) != cudaSuccess ||
-        (e = lrkv::launch_dB_reduce(P, static_cast<uint16_t*>(dB), H, ks, d_h, r, 64, st)) != cudaSuccess)
-        return cuda_status(e, "lrkv_train_backward launch");
+    if (fold_dB) {
+        if ((e = lrkv::launch_dB_reduce(P, static_cast<uint16_t*>(dB), H, ntiles, d_h, r, 16, st)) != cudaSuccess)
+            return cuda_status(e, "lrkv_train_backward launch");
+    } else {
+        // dB_h = dK_h^T R_h: split-K partials (A = dK read [n (K)][d_h (M)], B = R_h read [n (K)][r (N)])
+        g = lrkv::GemmArgs{};
+        g.C = P; g.M = d_h; g.N = r; g.K = n_tok; g.a_zx = d_h; g.b_x0 = d_h; g.b_zx = r; g.nbatch = H;
+        g.ksplit = ks; g.status = status_dev;
+        if ((e = train_gemm(tdK_mn, tY_mn, g, 64, true, true, true, st)) != cudaSuccess ||
+            (e = lrkv::launch_dB_reduce(P, static_cast<uint16_t*>(dB), H, ks, d_h, r, 64, st)) != cudaSuccess)
+            return cuda_status(e, "lrkv_train_backward launch");
+    }
     // One launch for both products of Gc, whose CTAs take tiles from a shared queue: the long
     // tiles of dW_T first (fewer than the SMs), the short tiles of dX filling the other SMs.
     //   dW_T = Gc^T X  ([d_h + H r][d]; A = Gc read [n (K)][Ncat (M)], B = X read [n (K)][d (N)])

@@ -375,9 +375,13 @@ __global__ void __launch_bounds__(192, 1) tgemm_kernel(const __grid_constant__ T
 //               (each tile starts its walk over the heads at a different head, so that the
 //               CTAs do not all read the same head's columns at once);
 //   warp 1      TMEM owner; one thread issues dR_h = dK_h B_h (M = 128 tokens, N = r, K = d_h)
-//               into r TMEM columns per head;
+//               into r TMEM columns per head and, when dB is folded in (d_h = 128, r = 16), this
+//               tile's part of dB_h = dK_h^T R_h (M = d_h, N = r, K = 128 tokens: the same dK_h
+//               tile read MN-major, R_h as a 16-column box of 32-byte swizzle next to it in the
+//               stage) into r more columns per head;
 //   warps 2..5  add every dK_h tile into fp32 registers (one token row per thread: G), then
-//               store dR.  Each rank finishes half of G's columns: it stages the other half of
+//               store dR and the fp32 dB partials ([H][tile][d_h][r], summed in tile order by
+//               the reduce kernel).  Each rank finishes half of G's columns: it stages the other half of
 //               its partial G in its idle ring and copies it in one bulk transfer into the
 //               peer's ring, then adds the peer's half to its own and rounds the sum once.
 // A ring slot is free once the MMAs (commit) and the four summing warps have read it.
@@ -423,7 +427,8 @@ struct DkCfg {
 
 template <int D_H>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
-    dk_pass_kernel(const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmBT, const DkArgs a) {
+    dk_pass_kernel(const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmBT,
+                   const __grid_constant__ CUtensorMap tmR, const DkArgs a) {
     using C = DkCfg<D_H>;
     constexpr int NBOX = C::NBOX, NST = C::STAGES, PITCH = C::PITCH, HALF = C::HALF;
     constexpr uint32_t TILE = C::TILE;
@@ -437,9 +442,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const int h0 = rank * hpr, nh = min(a.H - h0, hpr);
     const int hoff = (int)(blockIdx.y % (unsigned)nh);  // first head of this tile's walk
     const uint32_t BTB = (uint32_t)r * 128u;            // B^T box: r rows x 64 K
+    const bool fdb = D_H == 128 && a.dBp != nullptr;     // dB folded in (r = 16)
+    const uint32_t SST = TILE + (fdb ? 4096u : 0u);      // ring stage: dK_h tile [+ R_h box]
+    const int dboff = hpr * r;                           // TMEM columns of the dB partials
     const uint32_t sRing = smem_u32(smem);
-    const uint32_t sBT = sRing + NST * TILE;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * TILE + (size_t)hpr * NBOX * BTB);
+    const uint32_t sBT = sRing + NST * SST;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * SST + (size_t)hpr * NBOX * BTB);
     uint64_t* empty = full + NST;
     uint64_t* cfull = empty + NST;  // B^T boxes landed
     uint64_t* accf = cfull + 1;     // every MMA of this CTA has completed
@@ -487,10 +495,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     break;
                 }
                 const uint32_t bar = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(bar, TILE);
+                mbar_arrive_expect_tx(bar, SST);
 #pragma unroll
                 for (int j = 0; j < NBOX; ++j)
-                    tma_load_2d(sRing + s * TILE + j * 16384, &tmdK, (h0 + hh) * D_H + 64 * j, m0, bar);
+                    tma_load_2d(sRing + s * SST + j * 16384, &tmdK, (h0 + hh) * D_H + 64 * j, m0, bar);
+                if (fdb) tma_load_2d(sRing + s * SST + TILE, &tmR, a.rx0 + (h0 + hh) * r, m0, bar);
                 issued = i + 1;
             }
             if (!bt_issued) issue_bt();
@@ -502,6 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idR = idesc_bf16_f32(kTM, r);
+            const uint32_t idB = idesc_bf16_f32(kTM, r) | (1u << 15) | (1u << 16);  // both MN-major
             bool ok = mbar_wait(smem_u32(cfull), 0, a.status);
             for (int i = 0; i < nh && ok; ++i) {
                 const int s = i % NST, hh = (i + hoff) % nh;
@@ -514,9 +524,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 for (int kk = 0; kk < D_H / 16; ++kk) {
                     const int j = kk >> 2;
                     const uint32_t o = (kk & 3) * 32;
-                    tc_mma_bf16(tmem + hh * r, kmaj(sRing + s * TILE + j * 16384 + o),
+                    tc_mma_bf16(tmem + hh * r, kmaj(sRing + s * SST + j * 16384 + o),
                                 kmaj(sBT + (hh * NBOX + j) * BTB + o), idR, kk != 0);
                 }
+                if (fdb)  // A = dK_h^T: 64-row blocks 16 KiB apart, 16 tokens (2 KiB) per K step
+#pragma unroll
+                    for (int kk = 0; kk < kTM / 16; ++kk)
+                        tc_mma_bf16(tmem + dboff + hh * r, sdesc(sRing + s * SST + kk * 2048, 16384, 1024, 2),
+                                    sdesc(sRing + s * SST + TILE + kk * 512, 16, 256, 6), idB, kk != 0);
                 tc_commit(smem_u32(&empty[s]));
             }
             if (ok) tc_commit(smem_u32(accf));
@@ -535,7 +550,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 ok = false;
                 break;
             }
-            const uint8_t* tile = smem + s * TILE + rl * 128;
+            const uint8_t* tile = smem + s * SST + rl * 128;
 #pragma unroll
             for (int j = 0; j < NBOX; ++j)
 #pragma unroll
@@ -596,6 +611,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     reinterpret_cast<uint4*>(grow + c0)[1] = p1;
                 }
             }
+            if (fdb) {
+                // this tile's dB partials: TMEM lane = d_h row, r columns per head
+                const int ntile = gridDim.y;
+                for (int hh = 0; hh < nh; ++hh) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + dboff + hh * r, v);
+                    float4* dst = reinterpret_cast<float4*>(
+                        a.dBp + ((((size_t)(h0 + hh) * ntile + blockIdx.y) * kTM + rl) * r));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                             __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                }
+            }
         }
         if (ok && mbar_wait(smem_u32(recv), 0, a.status) && row < a.n) {
             const float* rv = reinterpret_cast<const float*>(smem + C::GOFF) + (size_t)rl * PITCH;
@@ -638,36 +667,43 @@ __global__ void __launch_bounds__(256) bt_kernel(const uint16_t* B, uint16_t* BT
 }
 
 template <int D_H>
-static size_t dk_smem(int H, int r) {
-    return (size_t)DkCfg<D_H>::STAGES * DkCfg<D_H>::TILE + (size_t)((H + 1) / 2) * DkCfg<D_H>::NBOX * r * 128 + 256 +
-           1024;
+static size_t dk_smem(int H, int r, bool fdb) {
+    return (size_t)DkCfg<D_H>::STAGES * (DkCfg<D_H>::TILE + (fdb ? 4096 : 0)) +
+           (size_t)((H + 1) / 2) * DkCfg<D_H>::NBOX * r * 128 + 256 + 1024;
 }
 
 bool dk_pass_supported(int H, int d_h, int r) {
     if (H < 2 || !(d_h == 64 || d_h == 128) || !(r == 16 || r == 32) || ((H + 1) / 2) * r > 512) return false;
-    return (d_h == 64 ? dk_smem<64>(H, r) : dk_smem<128>(H, r)) <= kTSmemMax;
+    return (d_h == 64 ? dk_smem<64>(H, r, false) : dk_smem<128>(H, r, false)) <= kTSmemMax;
+}
+
+bool dk_pass_folds_dB(int H, int d_h, int r) {
+    return dk_pass_supported(H, d_h, r) && d_h == 128 && r == 16 && 2 * ((H + 1) / 2) * r <= 512 &&
+           dk_smem<128>(H, r, true) <= kTSmemMax;
 }
 
 template <int D_H>
-static cudaError_t launch_dk_t(const CUtensorMap& tdK, const CUtensorMap& tBT, const DkArgs& a, cudaStream_t stream) {
+static cudaError_t launch_dk_t(const CUtensorMap& tdK, const CUtensorMap& tBT, const CUtensorMap& tR, const DkArgs& a,
+                               cudaStream_t stream) {
     // the staged half of G and the peer's half fit in the ring
     static_assert((size_t)DkCfg<D_H>::STAGES * DkCfg<D_H>::TILE >= DkCfg<D_H>::GOFF + DkCfg<D_H>::GBYTES, "ring");
     // at least 120 KiB, so that one CTA runs per SM: each allocates all 512 TMEM columns, and a
     // second resident CTA would wait in its allocation for one that waits on its cluster peer
-    const size_t need = dk_smem<D_H>(a.H, a.r), smem = need > 122880 ? need : 122880;
+    const size_t need = dk_smem<D_H>(a.H, a.r, a.dBp != nullptr), smem = need > 122880 ? need : 122880;
     auto kern = dk_pass_kernel<D_H>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(2, (a.n + kTM - 1) / kTM), 192, smem, stream>>>(tdK, tBT, a);
+    kern<<<dim3(2, (a.n + kTM - 1) / kTM), 192, smem, stream>>>(tdK, tBT, tR, a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dk_pass(const CUtensorMap& tdK, const CUtensorMap& tBT, const uint16_t* B, uint16_t* BT,
-                           const DkArgs& a, cudaStream_t stream) {
-    if (!dk_pass_supported(a.H, a.d_h, a.r)) return cudaErrorInvalidValue;
+cudaError_t launch_dk_pass(const CUtensorMap& tdK, const CUtensorMap& tBT, const CUtensorMap& tR, const uint16_t* B,
+                           uint16_t* BT, const DkArgs& a, cudaStream_t stream) {
+    if (!dk_pass_supported(a.H, a.d_h, a.r) || (a.dBp && !dk_pass_folds_dB(a.H, a.d_h, a.r)))
+        return cudaErrorInvalidValue;
     const int tot = a.H * a.r * a.d_h;
     bt_kernel<<<(tot + 255) / 256, 256, 0, stream>>>(B, BT, a.H, a.d_h, a.r);
-    return a.d_h == 64 ? launch_dk_t<64>(tdK, tBT, a, stream) : launch_dk_t<128>(tdK, tBT, a, stream);
+    return a.d_h == 64 ? launch_dk_t<64>(tdK, tBT, tR, a, stream) : launch_dk_t<128>(tdK, tBT, tR, a, stream);
 }
 
 // G[t][e] = sum_h dK[t][h][e] (fp32, heads in order), eight columns per thread.
@@ -692,17 +728,58 @@ __global__ void __launch_bounds__(256) head_sum_kernel(const uint16_t* dK, uint1
     *reinterpret_cast<uint4*>(Gc + (size_t)t * ldg + c) = pk;
 }
 
-// dB[h][e][j] = sum_ks P[h][ks][e][j] in ks order, bf16 (partials [H][ks][128][pw]).
+// dB[h][e][j] = sum over ks of P[h][ks][e][j], bf16 (partials [H][ks][128][pw]).  A block of 256
+// threads covers 64 outputs of four consecutive j each; its four thread groups sum interleaved
+// quarters of the partials (sixteen loads in flight per thread), then group 0 adds the four
+// sums in group order -- a fixed order, so the result does not depend on timing.
 __global__ void __launch_bounds__(256) dB_reduce_kernel(const float* P, uint16_t* dB, int H, int ksplit, int d_h,
                                                         int r, int pw) {
-    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= (long long)H * d_h * r) return;
-    const int h = (int)(idx / ((long long)d_h * r)), rem = (int)(idx % ((long long)d_h * r));
-    const int e = rem / r, j = rem % r;
-    float v = 0.f;
-    for (int ks = 0; ks < ksplit; ++ks) v += P[(((size_t)h * ksplit + ks) * kTM + e) * pw + j];
-    const __nv_bfloat16 b = __float2bfloat16_rn(v);
-    dB[idx] = *reinterpret_cast<const uint16_t*>(&b);
+    __shared__ float4 part[4][64];
+    const int r4 = r / 4;
+    const int grp = threadIdx.x >> 6, t = threadIdx.x & 63;
+    const long long idx = (long long)blockIdx.x * 64 + t;
+    const bool live = idx < (long long)H * d_h * r4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int h = 0, e = 0, j = 0;
+    if (live) {
+        h = (int)(idx / ((long long)d_h * r4));
+        const int rem = (int)(idx % ((long long)d_h * r4));
+        e = rem / r4;
+        j = (rem % r4) * 4;
+        const float4* src = reinterpret_cast<const float4*>(P + (((size_t)h * ksplit) * kTM + e) * pw + j);
+        const size_t stride = (size_t)kTM * pw / 4;  // float4s between consecutive partials
+        for (int k0 = grp; k0 < ksplit; k0 += 4 * 16) {
+            float4 v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int k = k0 + 4 * u;
+                v[u] = k < ksplit ? __ldg(src + (size_t)k * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                acc.x += v[u].x;
+                acc.y += v[u].y;
+                acc.z += v[u].z;
+                acc.w += v[u].w;
+            }
+        }
+    }
+    part[grp][t] = acc;
+    __syncthreads();
+    if (grp == 0 && live) {
+        float4 s4 = part[0][t];
+#pragma unroll
+        for (int g = 1; g < 4; ++g) {
+            s4.x += part[g][t].x;
+            s4.y += part[g][t].y;
+            s4.z += part[g][t].z;
+            s4.w += part[g][t].w;
+        }
+        uint2 o;
+        o.x = pack_bf16x2(s4.x, s4.y);
+        o.y = pack_bf16x2(s4.z, s4.w);
+        *reinterpret_cast<uint2*>(dB + ((size_t)h * d_h + e) * r + j) = o;
+    }
 }
 
 static int tgemm_tiles(const GemmArgs& g, int bn) {
@@ -779,8 +856,9 @@ cudaError_t launch_head_sum(const uint16_t* dK, uint16_t* Gc, int n, int H, int 
 
 cudaError_t launch_dB_reduce(const float* P, uint16_t* dB, int H, int ksplit, int d_h, int r, int pw,
                              cudaStream_t stream) {
-    const long long total = (long long)H * d_h * r;
-    dB_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(P, dB, H, ksplit, d_h, r, pw);
+    if (r % 4 != 0 || pw % 4 != 0) return cudaErrorInvalidValue;
+    const long long total = (long long)H * d_h * (r / 4);
+    dB_reduce_kernel<<<(unsigned)((total + 63) / 64), 256, 0, stream>>>(P, dB, H, ksplit, d_h, r, pw);
     return cudaGetLastError();
 }
 

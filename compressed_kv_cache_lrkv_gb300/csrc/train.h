@@ -61,13 +61,16 @@ struct DkArgs {
     uint16_t* Gc;
     int ldg;                  // Gc row pitch, elements
     int n, H, d_h, r;
+    float* dBp;               // fp32 dB partials [H][n / 128 tiles][d_h][r], or null (dB not folded in)
+    int rx0;                  // column of R_1 in the map tR (d_h)
     uint32_t* status;
 };
 bool dk_pass_supported(int H, int d_h, int r);
+bool dk_pass_folds_dB(int H, int d_h, int r);
 // tdK: [n][H d_h] in 64 x 128 boxes; tBT: BT = [H r][d_h] in 64 x r boxes, written here from the
-// residual factors B [H][d_h][r] first.
-cudaError_t launch_dk_pass(const CUtensorMap& tdK, const CUtensorMap& tBT, const uint16_t* B, uint16_t* BT,
-                           const DkArgs& a, cudaStream_t stream);
+// residual factors B [H][d_h][r] first; tR (with dBp): Y = [S | R] in 16 x 128 boxes (32-byte swizzle).
+cudaError_t launch_dk_pass(const CUtensorMap& tdK, const CUtensorMap& tBT, const CUtensorMap& tR, const uint16_t* B,
+                           uint16_t* BT, const DkArgs& a, cudaStream_t stream);
 
 // G[t] = sum_h dK[t][h][:] into columns [0, d_h) of Gc [n][ldg] (bf16, fp32 sums).
 cudaError_t launch_head_sum(const uint16_t* dK, uint16_t* Gc, int n, int H, int d_h, int ldg, cudaStream_t stream);
