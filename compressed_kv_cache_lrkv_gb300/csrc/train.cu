@@ -452,7 +452,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     uint64_t* cfull = empty + NST;  // B^T boxes landed
     uint64_t* accf = cfull + 1;     // every MMA of this CTA has completed
     uint64_t* recv = accf + 1;      // the peer's half of G has landed in the ring
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv + 1);
+    uint64_t* mmad = recv + 1;      // [NST] the MMAs of the head in this slot have completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mmad + NST);
     volatile int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -464,6 +465,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         mbar_init(smem_u32(cfull), 1);
         mbar_init(smem_u32(accf), 1);
         mbar_init(smem_u32(recv), 1);
+        for (int s = 0; s < NST; ++s) mbar_init(smem_u32(&mmad[s]), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -533,13 +535,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                         tc_mma_bf16(tmem + dboff + hh * r, sdesc(sRing + s * SST + kk * 2048, 16384, 1024, 2),
                                     sdesc(sRing + s * SST + TILE + kk * 512, 16, 256, 6), idB, kk != 0);
                 tc_commit(smem_u32(&empty[s]));
+                tc_commit(smem_u32(&mmad[s]));
             }
             if (ok) tc_commit(smem_u32(accf));
             else *abort_flag = 1;
         }
     } else {
-        // G: add each dK_h tile's row into fp32 registers
+        // G: add each dK_h tile's row into fp32 registers; after each tile, store the previous
+        // head's dR row (and dB partial row), whose MMAs have completed by then
         const int rl = (warp & 3) * 32 + lane;  // tile row = TMEM lane of this warp's quarter
+        const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+        const int row = m0 + rl;
+        auto drain = [&](int i) -> bool {
+            const int hh = (i + hoff) % nh;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&mmad[i % NST]), (i / NST) & 1, a.status))) return false;
+            tc_fence_after();
+            uint16_t* grow = a.Gc + (size_t)row * a.ldg + D_H + (h0 + hh) * r;
+            for (int c0 = 0; c0 < r; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem + lanes + hh * r + c0, v);
+                if (row < a.n) {
+                    uint4 p0, p1;
+                    p0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+                    p0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+                    p0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+                    p0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+                    p1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
+                    p1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
+                    p1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
+                    p1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
+                    reinterpret_cast<uint4*>(grow + c0)[0] = p0;
+                    reinterpret_cast<uint4*>(grow + c0)[1] = p1;
+                }
+            }
+            if (fdb) {
+                // this tile's dB_h partial: TMEM lane = d_h row, r = 16 columns
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem + lanes + dboff + hh * r, v);
+                float4* dst = reinterpret_cast<float4*>(
+                    a.dBp + ((((size_t)(h0 + hh) * gridDim.y + blockIdx.y) * kTM + rl) * r));
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                         __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            }
+            return true;
+        };
 #pragma unroll
         for (int c = 0; c < D_H; ++c) g[c] = 0.f;
         bool ok = true;
@@ -562,7 +603,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            if (i > 0 && !drain(i - 1)) {
+                ok = false;
+                break;
+            }
         }
+        if (ok && nh > 0) ok = drain(nh - 1);
         ok = ok && mbar_wait(smem_u32(accf), 0, a.status);
         if (!__all_sync(0xffffffffu, ok) && lane == 0) *abort_flag = 1;
         tc_fence_after();
@@ -591,41 +637,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const bool ok = !*abort_flag;
         if (threadIdx.x == 64 && ok)
             bulk_copy_to_peer(cl_map(sRing + C::GOFF, rank ^ 1), sRing, C::GBYTES, cl_map(smem_u32(recv), rank ^ 1));
-        if (ok) {
-            // dR of this CTA's heads: Gc columns d_h + h0 r .. + nh r
-            uint16_t* grow = a.Gc + (size_t)row * a.ldg + D_H + h0 * r;
-            for (int c0 = 0; c0 < nh * r; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + c0, v);
-                if (row < a.n) {
-                    uint4 p0, p1;
-                    p0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
-                    p0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
-                    p0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
-                    p0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
-                    p1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
-                    p1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
-                    p1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
-                    p1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
-                    reinterpret_cast<uint4*>(grow + c0)[0] = p0;
-                    reinterpret_cast<uint4*>(grow + c0)[1] = p1;
-                }
-            }
-            if (fdb) {
-                // this tile's dB partials: TMEM lane = d_h row, r columns per head
-                const int ntile = gridDim.y;
-                for (int hh = 0; hh < nh; ++hh) {
-                    uint32_t v[16];
-                    tmem_ld_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + dboff + hh * r, v);
-                    float4* dst = reinterpret_cast<float4*>(
-                        a.dBp + ((((size_t)(h0 + hh) * ntile + blockIdx.y) * kTM + rl) * r));
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                             __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-                }
-            }
-        }
         if (ok && mbar_wait(smem_u32(recv), 0, a.status) && row < a.n) {
             const float* rv = reinterpret_cast<const float*>(smem + C::GOFF) + (size_t)rl * PITCH;
             uint16_t* grow = a.Gc + (size_t)row * a.ldg + rank * HALF;
