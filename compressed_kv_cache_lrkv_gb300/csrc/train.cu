@@ -452,8 +452,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     uint64_t* cfull = empty + NST;  // B^T boxes landed
     uint64_t* accf = cfull + 1;     // every MMA of this CTA has completed
     uint64_t* recv = accf + 1;      // the peer's half of G has landed in the ring
-    uint64_t* mmad = recv + 1;      // [NST] the MMAs of the head in this slot have completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mmad + NST);
+    // [2 NST] the MMAs of head i have completed (barrier i % 2 NST).  Head i's barrier completes
+    // again only for head i + 2 NST, whose tile needs slot i % NST freed after head i + NST --
+    // which the summing warps release only after draining head i (they drain head i after
+    // summing head i + 1).  With NST barriers a slow drain could see head i + NST's completion
+    // too and wait for a phase that never comes.
+    uint64_t* mmad = recv + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mmad + 2 * NST);
     volatile int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -465,7 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         mbar_init(smem_u32(cfull), 1);
         mbar_init(smem_u32(accf), 1);
         mbar_init(smem_u32(recv), 1);
-        for (int s = 0; s < NST; ++s) mbar_init(smem_u32(&mmad[s]), 1);
+        for (int s = 0; s < 2 * NST; ++s) mbar_init(smem_u32(&mmad[s]), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -535,7 +540,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                         tc_mma_bf16(tmem + dboff + hh * r, sdesc(sRing + s * SST + kk * 2048, 16384, 1024, 2),
                                     sdesc(sRing + s * SST + TILE + kk * 512, 16, 256, 6), idB, kk != 0);
                 tc_commit(smem_u32(&empty[s]));
-                tc_commit(smem_u32(&mmad[s]));
+                tc_commit(smem_u32(&mmad[i % (2 * NST)]));
             }
             if (ok) tc_commit(smem_u32(accf));
             else *abort_flag = 1;
@@ -548,7 +553,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const int row = m0 + rl;
         auto drain = [&](int i) -> bool {
             const int hh = (i + hoff) % nh;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&mmad[i % NST]), (i / NST) & 1, a.status))) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&mmad[i % (2 * NST)]), (i / (2 * NST)) & 1, a.status)))
+                return false;
             tc_fence_after();
             uint16_t* grow = a.Gc + (size_t)row * a.ldg + D_H + (h0 + hh) * r;
             for (int c0 = 0; c0 < r; c0 += 16) {
