@@ -11,19 +11,21 @@
 //                                                reads zeros)
 // Backward, for dK [n][H][d_h]:
 //   Gc = [G | dR_1 .. dR_H], G = sum_h dK_h, dR_h = dK_h B_h
-//   dB_h = dK_h^T R_h                            split-K over tokens, fp32 partials, ordered sum
+//   dB_h = dK_h^T R_h                            per 128-token tile, fp32 partials, ordered sum
 //   dW_T = Gc^T X                                (= [dW_shared^T ; dU_1^T ; ...]), K = n
 //   dX = Gc W_T                                  K = d_h + H r
 // All contractions run on tcgen05 (bf16 operands, fp32 accumulation in TMEM); S, R and Gc are
 // rounded to bf16 between the steps, as the inference cache rounds S and R.
 //
-// The GEMM kernel is persistent (one CTA per SM looping over 128 x 128 output tiles): warp 0 TMA
-// producer (a 6-stage ring of 64-wide K slices, continuous across tiles), warp 1 TMEM owner and
-// single-thread MMA issue into one of two accumulator buffers, warps 2-5 epilogue (tcgen05.ld of
-// their 32 TMEM lanes = tile rows), so a tile's epilogue overlaps the next tile's MMAs.  A bf16
-// tile leaves through shared memory: each epilogue warp writes its 32 rows into 32 x 32 boxes
-// (64-byte swizzle, conflict-free 16-byte stores) and one lane issues their TMA stores.  All waits
-// are bounded.
+// tgemm_kernel: a persistent GEMM (one CTA per SM looping over 128 x BN output tiles of up to two
+// products, round robin or from a shared work queue): warp 0 TMA producer (a ring of 64-wide K
+// slices, continuous across tiles), warp 1 TMEM owner and single-thread MMA issue into one of two
+// accumulator buffers, warps 2-5 epilogue (tcgen05.ld of their 32 TMEM lanes = tile rows), so a
+// tile's epilogue overlaps the next tile's MMAs.  A bf16 tile leaves through shared memory: each
+// epilogue warp writes its 32 rows into 32 x 32 boxes (64-byte swizzle, conflict-free 16-byte
+// stores) and one lane issues their TMA stores.
+// dk_pass_kernel: the backward's one pass over dK on CTA pairs (G in registers, dR and the dB
+// partials on the tensor cores), described at the kernel.  All waits are bounded.
 #include "kernels.h"
 #include "lrkv_internal.cuh"
 #include "train.h"
