@@ -791,15 +791,20 @@ def run_gpu(args, world, rank, local):
 
 def run_reference(args, world, rank):
     """--impl reference: the fp64 oracle on the host cores; each step is a bounded sample
-    of the workload (E2 decode of a prefix of the first sequence, all heads)."""
+    of the workload (decode: E2 decode of a prefix of the first sequence, all heads; the
+    MLA, prefill and training workloads: see their functions below)."""
     if rank != 0:
         return
     import oracle
 
-    wl = S.WORKLOADS[args.workload if args.workload not in ("prefill", "train") else "longctx"]
-    seq_lens = workload_seq_lens(wl)
+    wl = S.WORKLOADS[args.workload]
     o = oracle.get()
     per_step_budget = max(0.01, 90.0 / max(args.steps + args.warmup, 1))
+    if args.workload == "prefill":
+        return run_reference_prefill(args, wl, o, per_step_budget)
+    if args.workload == "train":
+        return run_reference_train(args, wl, o, per_step_budget)
+    seq_lens = workload_seq_lens(wl)
 
     if wl.d_c:
         return run_reference_mla(args, wl, seq_lens, o, per_step_budget)
@@ -873,6 +878,105 @@ def run_reference_mla(args, wl, seq_lens, o, per_step_budget):
                          "sample": f"absorbed MLA decode of the first {tokens} tokens of one sequence, all heads, "
                                    f"per step"},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+def _timed_steps(args, fn):
+    for _ in range(args.warmup):
+        fn()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fn()
+    return (time.perf_counter() - t0) / max(args.steps, 1)
+
+
+def run_reference_prefill(args, wl, o, per_step_budget):
+    """--impl reference on the prefill workload: each step, the oracle appends one sequence's
+    first Tq prompt rows (the cache rows from X and the weights) and runs the E2 causal prefill of
+    those Tq queries over them, all heads; Tq (a multiple of 64, at most one chunk) sized from a
+    probe so that a step takes about its share of the run's budget."""
+    d, H, d_h, r = wl.d, wl.H, wl.d_h, wl.r
+
+    def inputs(tq):
+        X = S.gaussian_bf16(wl.seed, "rp_X", (tq, d))
+        W = [S.gaussian_bf16(wl.seed, "rp_WsK", (d, d_h), d ** -0.5),
+             S.gaussian_bf16(wl.seed, "rp_WsV", (d, d_h), d ** -0.5),
+             S.gaussian_bf16(wl.seed, "rp_UK", (H, d, r), d ** -0.5),
+             S.gaussian_bf16(wl.seed, "rp_UV", (H, d, r), d ** -0.5)]
+        BK = S.gaussian_bf16(wl.seed, "rp_BK", (H, d_h, r), r ** -0.5)
+        BV = S.gaussian_bf16(wl.seed, "rp_BV", (H, d_h, r), r ** -0.5)
+        q = S.gaussian_bf16(wl.seed, "rp_q", (1, tq, H, d_h))
+        pt = S.page_table(wl.seed, [tq], 64)
+        return X, W, BK, BV, q, pt
+
+    def step(tq, X, W, BK, BV, q, pt):
+        rows = o.append(X, *W)  # (sK, sV, zK, zV) rows, bf16 bits, token order
+        nb = pt.num_blocks
+        pools = [np.zeros((nb * 64,) + a.shape[1:], np.uint16) for a in rows]
+        slots = S.slots_for(pt, 0, 0, tq)
+        for pool, a in zip(pools, rows):
+            pool[slots] = a
+        pools = tuple(pool.reshape((nb, 64) + pool.shape[1:]) for pool in pools)
+        o.prefill_cache(pools, pt.block_table, [0], BK, BV, q)
+
+    probe = 64
+    args_p = inputs(probe)
+    t0 = time.perf_counter()
+    step(probe, *args_p)
+    dt0 = max(time.perf_counter() - t0, 1e-6)
+    tq = probe
+    while tq * 2 <= wl.chunk and dt0 * (tq * 2 / probe) ** 2 <= per_step_budget:
+        tq *= 2
+    a_in = inputs(tq)
+    dt = _timed_steps(args, lambda: step(tq, *a_in))
+    val = tq / dt
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC_PREFILL, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.key}: {wl.description}", "sample_prompt_tokens_per_step": tq, "H": H,
+                   "d_h": d_h, "r": r, "d": d},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": o.num_threads(), "kind": "oracle",
+                         "sample": f"append of one sequence's first {tq} prompt rows and the E2 causal prefill "
+                                   f"of those {tq} queries (all {H} heads), per step"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+def run_reference_train(args, wl, o, per_step_budget):
+    """--impl reference on the training workload: each step, the oracle's expanded projection
+    forward and backward on n tokens at the workload's shape (d, H, d_h, r), n (a multiple of 8)
+    sized from a probe to the step's share of the budget; TFLOP/s of the algorithmic flops."""
+    d, H, d_h, r = wl.d, wl.H, wl.d_h, wl.r
+
+    def inputs(n):
+        return (S.gaussian_bf16(wl.seed, "rt_X", (n, d)),
+                S.gaussian_bf16(wl.seed, "rt_Ws", (d, d_h), d ** -0.5),
+                S.gaussian_bf16(wl.seed, "rt_U", (H, d, r), d ** -0.5),
+                S.gaussian_bf16(wl.seed, "rt_B", (H, d_h, r), r ** -0.5),
+                S.gaussian_bf16(wl.seed, "rt_dK", (n, H, d_h)))
+
+    def step(X, Ws, U, Bm, dK):
+        o.train_forward(X, Ws, U, Bm)
+        o.train_backward(X, Ws, U, Bm, dK)
+
+    probe = 8
+    t0 = time.perf_counter()
+    step(*inputs(probe))
+    rate = probe / max(time.perf_counter() - t0, 1e-6)
+    n = max(8, min(wl.B * wl.L, int(rate * per_step_budget)) // 8 * 8)
+    a_in = inputs(n)
+    dt = _timed_steps(args, lambda: step(*a_in))
+    f, bw = A.train_flops(n, d, H, d_h, r)
+    val = (f + bw) / dt / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC_TRAIN, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.key}: {wl.description}", "sample_tokens_per_step": n, "H": H, "d_h": d_h,
+                   "r": r, "d": d, "flops_per_step": f + bw},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": o.num_threads(), "kind": "oracle",
+                         "sample": f"expanded projection forward + backward of {n} tokens at the workload's shape, "
+                                   f"per step (algorithmic flop count of the factored route)"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
 
 def main():
