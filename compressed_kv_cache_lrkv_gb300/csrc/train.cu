@@ -372,20 +372,22 @@ __global__ void __launch_bounds__(192, 1) tgemm_kernel(const __grid_constant__ T
 
 // ------------------------------------------------------------------ fused pass over dK
 // For one 128-token tile: G = sum_h dK_h (Gc columns [0, d_h)) and dR_h = dK_h B_h (Gc columns
-// d_h + h r ..), reading each dK_h tile once.  A cluster of two CTAs splits the heads:
-//   warp 0      TMA producer: B_h^T boxes of the CTA's heads, then its dK_h tiles into a ring
-//               (each tile starts its walk over the heads at a different head, so that the
-//               CTAs do not all read the same head's columns at once);
+// d_h + h r ..), and with dB folded in (d_h = 128, r = 16) this tile's part of every
+// dB_h = dK_h^T R_h, reading each dK_h tile once.  A cluster of two CTAs splits the heads:
+//   warp 0      TMA producer: the CTA's dK_h tiles (with their R_h boxes) into a ring, the B_h^T
+//               boxes once the first tiles are on their way; each tile starts its walk over the
+//               heads at a different head, so that the CTAs do not all read one head's columns
+//               at once;
 //   warp 1      TMEM owner; one thread issues dR_h = dK_h B_h (M = 128 tokens, N = r, K = d_h)
-//               into r TMEM columns per head and, when dB is folded in (d_h = 128, r = 16), this
-//               tile's part of dB_h = dK_h^T R_h (M = d_h, N = r, K = 128 tokens: the same dK_h
-//               tile read MN-major, R_h as a 16-column box of 32-byte swizzle next to it in the
-//               stage) into r more columns per head;
-//   warps 2..5  add every dK_h tile into fp32 registers (one token row per thread: G), then
-//               store dR and the fp32 dB partials ([H][tile][d_h][r], summed in tile order by
-//               the reduce kernel).  Each rank finishes half of G's columns: it stages the other half of
-//               its partial G in its idle ring and copies it in one bulk transfer into the
-//               peer's ring, then adds the peer's half to its own and rounds the sum once.
+//               into r TMEM columns per head and, with dB folded in, dB_h's partial (M = d_h,
+//               N = r, K = 128 tokens: the same dK_h tile read MN-major, R_h as a 16-column box
+//               of 32-byte swizzle next to it in the stage) into r more columns per head;
+//   warps 2..5  add every dK_h tile into fp32 registers (one token row per thread: G); after
+//               each tile they store the previous head's dR row and fp32 dB partial row
+//               ([H][tile][d_h][r], summed in tile order by the reduce kernel).  Each rank
+//               finishes half of G's columns: it stages the other half of its partial G in its
+//               idle ring and copies it in one bulk transfer into the peer's ring, then adds
+//               the peer's half to its own and rounds the sum once.
 // A ring slot is free once the MMAs (commit) and the four summing warps have read it.
 namespace {
 
