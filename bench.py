@@ -256,6 +256,8 @@ class DecodeHarness:
         return {
             "metric": METRIC_DECODE, "value": value, "unit": "GB/s",
             "tokens_per_s": wl.B * world / step_s, "pct_of_hbm_peak": 100.0 * value / peaks["hbm_gbs"],
+            # the decode call alone (cache + factor bytes over its own time), without the step's append
+            "decode_pct_of_hbm_peak": 100.0 * achieved / peaks["hbm_gbs"],
             "config": {"workload": f"{wl.key}: {wl.description}", "B": wl.B,
                        "seq_lens": [int(x) for x in self.seq_lens], "layers": wl.layers, "H": wl.H, "d_h": wl.d_h,
                        "r": wl.r, "d": wl.d, "d_rope": self.d_rope, "block_size": 64,
