@@ -174,6 +174,7 @@ class DecodeHarness:
     """Per layer: lrkv_append of each sequence's newest row, then lrkv_decode."""
 
     profile = "decode_split_longctx.md"
+    profiles = {"longctx": "decode_split_longctx.md", "dsv2": "decode_split_dsv2.md"}  # by workload
     sources = ("decode.cu", "lrkv_internal.cuh", "kernels.h")
 
     def __init__(self, wl, rank, fused=False, d_rope=0):
@@ -274,8 +275,8 @@ class DecodeHarness:
                                    "lrkv_decode (absorb + split + combine kernels)", "bound": "hbm",
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": recorded_traffic(self.profile, self.sources)
-                                    if wl.key == "longctx" and not self.fused and not self.d_rope else None,
+                         "traffic": recorded_traffic(self.profiles[wl.key], self.sources)
+                                    if wl.key in self.profiles and not self.fused and not self.d_rope else None,
                          "algorithmic_bytes_per_launch": self.kernel_units // wl.layers,
                          "avg_launch_ms": kernel_s * 1e3 / wl.layers},
             "e2e_unit_value": lambda s: self.step_units * world / s / 1e9, "e2e_unit": "GB/s",
