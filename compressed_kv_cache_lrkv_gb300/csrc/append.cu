@@ -4,12 +4,13 @@
 //   Y = X W_cat,  W_cat = [W_shared^K | W_shared^V | U_1^K..U_H^K | U_1^V..U_H^V]
 //   s^K_t = Y[t, 0:d_h], s^V_t = Y[t, d_h:2d_h], z^K_{h,t} = Y[t, 2d_h + h r : 2d_h + (h+1) r], z^V likewise.
 //
-// This file holds the bandwidth-bound variant used when few rows are appended
+// This file holds the bandwidth-bound variants used when few rows are appended
 // (a decode step appends one row per sequence): the weight rows (W_cat^T,
-// contiguous along d) are streamed exactly once with 16-byte loads, for up to
-// NT token rows at a time.  fp32 accumulation in a fixed order, round to
-// nearest even to bf16 (after rotating the positional-key pairs), scatter to
-// the row's slot.
+// contiguous along d) are streamed exactly once with 16-byte loads, for a block
+// of token rows at a time -- on the CUDA cores below 64 MB of weights, as a
+// split-K product on the warp-level tensor cores above.  fp32 accumulation in a
+// fixed order, round to nearest even to bf16 (after rotating the positional-key
+// pairs), scatter to the row's slot.
 #include "kernels.h"
 #include "lrkv_internal.cuh"
 
@@ -149,66 +150,135 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t local, uint32_t rank) {
     return v;
 }
 
-constexpr int kSplitCols = 64;   // output columns per CTA: 8 warps x 8 columns, 4 lanes per column
+// 16-byte load of streamed data that is read once: no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_16(const uint16_t* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
 
-// Few-row append (a decode step appends one row per sequence): a GEMV-like stream of W_cat^T.
-// A cluster of KS CTAs shares a group of 64 output columns and splits d into KS slices: each CTA
-// holds its slice of the NT hidden rows in shared memory and streams its slice of the 64 weight
-// rows once (16-byte loads, 4 lanes per row covering 64 contiguous bytes per step), so the hidden
-// rows are read KS * (N / 64) times in all instead of once per output column.  The fp32 partial
-// sums are reduced across the cluster through distributed shared memory by rank 0 in rank order
-// (deterministic), which then rounds (after rotating the positional-key pairs) and stores.
-template <int NT, bool ROPE>
-__global__ void __launch_bounds__(256) append_splitk_kernel(const AppendArgs a, int kslice) {
-    extern __shared__ __align__(16) uint8_t xs_raw[];
-    __shared__ float part[NT][kSplitCols];
-    const uint16_t* xs = reinterpret_cast<const uint16_t*>(xs_raw);  // [NT][kslice]
+constexpr int kMmaCols = 32;         // output columns per CTA: two 16-row tiles of W_cat^T
+constexpr int kMmaPitch = kMmaCols + 4;  // partial-sum row pitch in floats (conflict-free stores)
+
+// Few-row append on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulation):
+// C[col][t] = sum_k W_cat^T[col][k] X[t][k], with the weight columns on M and the 8 (NB = 1) or
+// 16 (NB = 2) token rows of the CTA on N.  The order in which k enters an MMA is free (a sum), so
+// every operand fragment is loaded straight from global memory as one 16-byte group per thread
+// and row: lane (g, q) of a warp reads elements [k + 8q, k + 8q + 8) of weight rows g and g + 8 of
+// each 16-row tile and of token row g, and its four 32-bit words feed two MMAs (words 0 and 1 the
+// first, 2 and 3 the second) as the pairs the fragment layout assigns to that lane; the A and B
+// operands see the same permutation of k.  No shared-memory staging: the weight stream (read once)
+// goes from HBM to registers, one 64-wide k step ahead of the MMAs.
+//
+// Work split: a cluster of KS CTAs owns 32 output columns and one block of token rows; each of
+// the 8 warps of each CTA sums a contiguous range of kwarp elements of k.  The warps' fp32 partial
+// sums are combined in shared memory in warp order, and the CTAs' through distributed shared
+// memory by rank 0 in rank order (deterministic), which then rounds (after rotating the
+// positional-key pairs) and stores.
+template <int NB, bool ROPE>
+__global__ void __launch_bounds__(256, 2) append_mma_kernel(const AppendArgs a, int kwarp) {
+    constexpr int NT = 8 * NB;
+    __shared__ float part[8][NT][kMmaPitch];
+    __shared__ float csum[NT][kMmaCols];
     const uint32_t r = cluster_ctarank(), KS = cluster_nctarank();
     const int group = blockIdx.x / KS;
     const int t0 = blockIdx.y * NT;
-    const int k0 = (int)r * kslice, k1 = min(a.d, k0 + kslice);
-    const int nk8 = kslice >> 3;  // 16-byte chunks per hidden-row slice
-    for (int idx = threadIdx.x; idx < NT * nk8; idx += blockDim.x) {
-        const int t = idx / nk8, c8 = idx - t * nk8;
-        const int k = k0 + c8 * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (t0 + t < a.n && k < k1) v = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + t) * a.d + k));
-        reinterpret_cast<uint4*>(xs_raw)[idx] = v;
-    }
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cl = warp * 8 + (lane >> 2), q = lane & 3;
-    const int col = group * kSplitCols + cl;
-    float acc[NT];
+    const int g = lane >> 2, q = lane & 3;
+    const int col0 = group * kMmaCols;
+
+    // operand rows (indices clamped into range: those lanes' results are never stored)
+    const uint16_t* wr[2][2];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-    if (col < a.N) {
-        const uint16_t* wrow = a.W + (size_t)col * a.d;
-#pragma unroll 4
-        for (int k = k0 + q * 8; k < k1; k += 32) {
-            const uint4 w = __ldg(reinterpret_cast<const uint4*>(wrow + k));
-            const int c8 = (k - k0) >> 3;
+    for (int i = 0; i < 2; ++i)
 #pragma unroll
-            for (int t = 0; t < NT; ++t)
-                acc[t] += dot8(w, reinterpret_cast<const uint4*>(xs)[t * nk8 + c8]);
+        for (int h = 0; h < 2; ++h) wr[i][h] = a.W + (size_t)min(col0 + 16 * i + 8 * h + g, a.N - 1) * a.d;
+    const uint16_t* xr[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) xr[j] = a.X + (size_t)min(t0 + 8 * j + g, a.n - 1) * a.d;
+
+    float acc[NB][2][4];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[j][i][e] = 0.f;
+
+    const int kbeg = ((int)r * 8 + warp) * kwarp;
+    const int kend = min(a.d, kbeg + kwarp);
+    // one 64-wide step: two 32-wide halves c, lane q holding elements [k + 32c + 8q, +8)
+    uint4 w[2][2][2], x[NB][2];  // w[tile][row half][c], x[row block][c]
+    auto load = [&](int k, uint4 (&wv)[2][2][2], uint4 (&xv)[NB][2]) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int kk = k + 32 * c + 8 * q;
+            const bool ok = kk < kend;  // d and kend are multiples of 8
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) wv[i][h][c] = ok ? ld_stream_16(wr[i][h] + kk) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+                xv[j][c] = ok ? __ldg(reinterpret_cast<const uint4*>(xr[j] + kk)) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    if (kbeg < kend) load(kbeg, w, x);
+    for (int k = kbeg; k < kend; k += 64) {
+        uint4 wn[2][2][2], xn[NB][2];
+        if (k + 64 < kend) load(k + 64, wn, xn);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int s = 0; s < 2; ++s)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&w[i][0][c]);
+                    const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&w[i][1][c]);
+                    const uint32_t af[4] = {w0[2 * s], w1[2 * s], w0[2 * s + 1], w1[2 * s + 1]};
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) {
+                        const uint32_t* xw = reinterpret_cast<const uint32_t*>(&x[j][c]);
+                        mma_16816(acc[j][i], af, xw[2 * s], xw[2 * s + 1]);
+                    }
+                }
+        if (k + 64 < kend) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) w[i][h][c] = wn[i][h][c];
+#pragma unroll
+                for (int j = 0; j < NB; ++j) x[j][c] = xn[j][c];
+            }
         }
     }
+    // accumulator (j, i, e): column 16 i + g + 8 (e >> 1), token row 8 j + 2 q + (e & 1)
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 1);
-        acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 2);
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) part[warp][8 * j + 2 * q + (e & 1)][16 * i + g + 8 * (e >> 1)] = acc[j][i][e];
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < NT * kMmaCols; idx += blockDim.x) {
+        const int t = idx / kMmaCols, cc = idx % kMmaCols;
+        float v = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < 8; ++ww) v += part[ww][t][cc];
+        csum[t][cc] = v;
     }
-    if (q == 0)
-#pragma unroll
-        for (int t = 0; t < NT; ++t) part[t][cl] = acc[t];
     cluster_sync_all();
     if (r == 0) {
-        // (row, column) pairs spread over all threads; each thread's KS partials are loaded
-        // together and summed in rank order.  Columns c and c ^ 1 sit in adjacent lanes.
-        for (int pidx = threadIdx.x; pidx < NT * kSplitCols; pidx += blockDim.x) {
-            const int t = pidx / kSplitCols, cc = pidx % kSplitCols;
-            const int c = group * kSplitCols + cc;
-            const uint32_t src = (uint32_t)__cvta_generic_to_shared(&part[t][cc]);
+        // (row, column) pairs spread over all threads (NT * 32 is a multiple of the block size, so
+        // every lane takes part in each shuffle); columns c and c ^ 1 sit in adjacent lanes.
+        for (int pidx = threadIdx.x; pidx < NT * kMmaCols; pidx += blockDim.x) {
+            const int t = pidx / kMmaCols, cc = pidx % kMmaCols;
+            const int c = col0 + cc;
+            const uint32_t src = (uint32_t)__cvta_generic_to_shared(&csum[t][cc]);
             float pv[8];
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr) pv[rr] = rr < (int)KS ? ld_cluster_f32(src, rr) : 0.f;
@@ -232,16 +302,12 @@ __global__ void __launch_bounds__(256) append_splitk_kernel(const AppendArgs a, 
     cluster_sync_all();  // rank 0 has read every CTA's partials before any of them exits
 }
 
-template <int NT, bool ROPE>
-static cudaError_t launch_splitk(const AppendArgs& a, int ks, int kslice, cudaStream_t stream) {
-    auto kern = append_splitk_kernel<NT, ROPE>;
-    const size_t smem = (size_t)NT * kslice * 2;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+template <int NB, bool ROPE>
+static cudaError_t launch_mma(const AppendArgs& a, int ks, int kwarp, cudaStream_t stream) {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(((a.N + kSplitCols - 1) / kSplitCols) * ks, (a.n + NT - 1) / NT);
+    cfg.gridDim = dim3(((a.N + kMmaCols - 1) / kMmaCols) * ks, (a.n + 8 * NB - 1) / (8 * NB));
     cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -250,7 +316,7 @@ static cudaError_t launch_splitk(const AppendArgs& a, int ks, int kslice, cudaSt
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, kslice);
+    return cudaLaunchKernelEx(&cfg, append_mma_kernel<NB, ROPE>, a, kwarp);
 }
 
 static cudaError_t launch_rowwise(const AppendArgs& a, cudaStream_t stream) {
@@ -274,31 +340,23 @@ static cudaError_t launch_rowwise(const AppendArgs& a, cudaStream_t stream) {
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     // Weight streams up to 64 MB: one CTA per output column (the hidden rows stay in L1/L2 at that
     // size and there is no cluster setup); larger ones re-read the hidden rows once per column
-    // from L2, so they go through the split-K cluster kernel below.
+    // from L2, so they go through the split-K tensor-core kernel above.
     if ((long long)a.N * a.d * 2 < (64LL << 20)) return launch_rowwise(a, stream);
-    // Split d so that the grid has about two CTAs per SM (at most 8 per cluster, slices of at
-    // least 32 elements), so the weight stream keeps every SM's loads in flight.
+    // Split d so that the grid fills two CTAs per SM in one wave (at most 8 CTAs per cluster,
+    // at least one 64-wide step per warp).
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int groups = (a.N + kSplitCols - 1) / kSplitCols;
-    int nt = a.n <= 1 ? 1 : a.n <= 2 ? 2 : a.n <= 4 ? 4 : a.n <= 8 ? 8 : 16;
-    const int rowblocks = (a.n + nt - 1) / nt;
-    int ks = (2 * sms + groups * rowblocks - 1) / (groups * rowblocks);
+    const int nb = a.n <= 8 ? 1 : 2;
+    const int groups = (a.N + kMmaCols - 1) / kMmaCols;
+    const int rowblocks = (a.n + 8 * nb - 1) / (8 * nb);
+    const int steps = (a.d + 63) / 64;  // 64-wide k steps
+    int ks = (2 * sms) / (groups * rowblocks);
     ks = ks < 1 ? 1 : ks > 8 ? 8 : ks;
-    // the hidden-row slice (nt rows x d / ks) must fit in shared memory: more slices, then fewer rows
-    const long long kMaxSlice = 192 * 1024;
-    while (ks < 8 && (long long)nt * ((a.d + ks - 1) / ks) * 2 > kMaxSlice) ++ks;
-    while (ks > 1 && (a.d + ks - 1) / ks < 32) --ks;
-    const int kslice = (((a.d + ks - 1) / ks) + 31) & ~31;
-    while (nt > 1 && (long long)nt * kslice * 2 > kMaxSlice) nt >>= 1;
-    if ((long long)nt * kslice * 2 > kMaxSlice) return cudaErrorInvalidValue;
-#define LRKV_SPLITK(NTV)                                                                        \
-    if (nt == NTV)                                                                              \
-        return a.d_rope > 0 ? launch_splitk<NTV, true>(a, ks, kslice, stream)                    \
-                            : launch_splitk<NTV, false>(a, ks, kslice, stream);
-    LRKV_SPLITK(1) LRKV_SPLITK(2) LRKV_SPLITK(4) LRKV_SPLITK(8) LRKV_SPLITK(16)
-#undef LRKV_SPLITK
-    return cudaErrorInvalidValue;
+    while (ks > 1 && ks * 8 > steps) --ks;
+    const int kwarp = ((steps + ks * 8 - 1) / (ks * 8)) * 64;
+    if (a.d_rope > 0)
+        return nb == 1 ? launch_mma<1, true>(a, ks, kwarp, stream) : launch_mma<2, true>(a, ks, kwarp, stream);
+    return nb == 1 ? launch_mma<1, false>(a, ks, kwarp, stream) : launch_mma<2, false>(a, ks, kwarp, stream);
 }
 
 }  // namespace lrkv
