@@ -13,6 +13,7 @@
 // pairs), scatter to the row's slot.
 #include "kernels.h"
 #include "lrkv_internal.cuh"
+#include "rotary.cuh"
 
 namespace lrkv {
 
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(128) append_rowwise_kernel(const AppendArgs a)
             if (ROPE && pair) {
                 float v1 = (red[ROPE ? 1 : 0][0][t] + red[ROPE ? 1 : 0][1][t]) +
                            (red[ROPE ? 1 : 0][2][t] + red[ROPE ? 1 : 0][3][t]);
-                rope_pair(v0, v1, u - a.d_h, a.d_rope, a.positions[t0 + t], a.rope_base);
+                rope_rotate(v0, v1, u - a.d_h, a.d_rope, a.positions[t0 + t], a.rope_base);
                 store_cache_value(a, slot, c + 1, v1);
             }
             store_cache_value(a, slot, c, v0);
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(256, 2) append_mma_kernel(const AppendArgs a, 
                 const float other = __shfl_xor_sync(0xffffffffu, v, 1);
                 if (c >= a.d_h && c < a.d_h + a.d_rope && slot >= 0) {
                     float x0 = (cc & 1) ? other : v, x1 = (cc & 1) ? v : other;
-                    rope_pair(x0, x1, (c - a.d_h) >> 1, a.d_rope, a.positions[t0 + t], a.rope_base);
+                    rope_rotate(x0, x1, (c - a.d_h) >> 1, a.d_rope, a.positions[t0 + t], a.rope_base);
                     v = (cc & 1) ? x1 : x0;
                 }
             }

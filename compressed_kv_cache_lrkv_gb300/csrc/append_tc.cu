@@ -14,6 +14,7 @@
 // All waits are bounded (LRKV_DEV_TIMEOUT); no spin is unbounded.
 #include "kernels.h"
 #include "lrkv_internal.cuh"
+#include "rotary.cuh"
 
 namespace lrkv {
 
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
-                        rope_pair(x0, x1, (n0 + c0 - a.d_h) / 2 + e, a.d_rope, pos, a.rope_base);
+                        rope_rotate(x0, x1, (n0 + c0 - a.d_h) / 2 + e, a.d_rope, pos, a.rope_base);
                         v[2 * e] = __float_as_uint(x0);
                         v[2 * e + 1] = __float_as_uint(x1);
                     }

@@ -2,11 +2,12 @@
 
 The key row grows to [s^K | k^R]: k^R = RoPE(x W^KR, pos) is one d_rope-vector per token shared
 by all heads (the decoupled rotary key of MLA-style latent caches, which "Low-Rank Key Value
-Attention" names as a combination with LRKV).  The kernels accumulate x W^KR in fp32, turn each
-pair at the row's position with angle, sine and cosine in double, round to fp32 and then to bf16;
-the oracle does the same from an fp64 sum.  On integer-grid inputs the fp32 sums are exact, so
-every content column must match bit for bit and a rotated column can differ only where the two
-sides' double-precision sine/cosine differ in the last bits and that moves a rounding boundary.
+Attention" names as a combination with LRKV).  The kernels accumulate x W^KR in fp32. They turn
+each pair at the row's position with the angle in double, and sine and cosine in fp32 corrected to
+first order in double (error ~1e-7 of the pair's magnitude), then round to fp32 and to bf16. The
+oracle rotates its fp64 sum in double.  On integer-grid inputs the fp32 sums are exact, so every
+content column must match bit for bit. A rotated column can differ by one ulp only where that
+small error moves a rounding boundary (a few in 10^5 values).
 """
 import numpy as np
 import pytest
