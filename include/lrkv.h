@@ -115,8 +115,10 @@ size_t lrkv_cache_block_bytes(const lrkv_dims* dims);
  * lrkv_append -- Eqs. (4)-(5): project n_tok hidden rows into the cache.
  *   Y = X W_cat, W_cat = [W_shared^K | W^KR | W_shared^V | U_1^K .. U_H^K | U_1^V .. U_H^V]
  *   (d x N, N = 2(d_h + H r) + d_rope; W^KR absent when d_rope == 0), accumulated
- *   in fp32; the d_rope columns of W^KR are then rotated at positions[t] (angle,
- *   sine and cosine in double, result rounded to fp32); everything is rounded to bf16
+ *   in fp32; the d_rope columns of W^KR are then rotated at positions[t] (angle in
+ *   double, sine and cosine in fp32 corrected to first order in double, products in
+ *   double, result rounded to fp32: within ~1e-7 of the pair's magnitude of the exact
+ *   rotation); everything is rounded to bf16
  *   (nearest, ties to even).  Row t is written to token slot slot_mapping[t]:
  *   columns [0, d_h + d_rope) -> sK, the next d_h -> sV, the next H r -> zK
  *   (head-major), the last H r -> zV.
@@ -297,7 +299,7 @@ size_t lrkv_mla_cache_block_bytes(const lrkv_mla_dims* dims);
 /*
  * lrkv_mla_append -- write n_tok cache rows: Y = X [W^DKV | W^KR] accumulated in fp32;
  *   the last d_rope columns are rotated at positions[t] (pair (2i, 2i+1) by the angle
- *   pos * rope_base^(-2i / d_rope); angle, sine, cosine in double, result rounded to
+ *   pos * rope_base^(-2i / d_rope), computed as for lrkv_append, result rounded to
  *   fp32); then bf16 (nearest, ties to even) into slot slot_mapping[t] of kv.
  *   X            [n_tok][d]
  *   W_T          [d_c + d_rope][d]  (row c holds the weights of output column c)
