@@ -169,21 +169,126 @@ def workload_seq_lens(wl):
     return np.full(wl.B, wl.L, np.int32)
 
 
-# ----------------------------------------------------------------------------- decode
-class DecodeHarness:
-    """Per layer: lrkv_append of each sequence's newest row, then lrkv_decode."""
+ROTATION_MAX_COPIES = 64
+ROTATION_MAX_BYTES = 32 << 30
 
+
+def _clone(v):
+    """Deep copy of per-step device data: tensors, paged caches, and lists / dicts of them."""
+    import torch
+
+    from compressed_kv_cache_lrkv_gb300 import binding as b
+    if isinstance(v, torch.Tensor):
+        return v.clone()
+    if isinstance(v, b.PagedCache):
+        return b.PagedCache(*(t.clone() for t in v.tensors()))
+    if isinstance(v, b.LayeredCache):
+        return b.LayeredCache(*(t.clone() for t in v.tensors()))
+    if isinstance(v, list):
+        return [_clone(x) for x in v]
+    if isinstance(v, dict):
+        return {k: _clone(x) for k, x in v.items()}
+    return v
+
+
+def _nbytes(v):
+    import torch
+
+    from compressed_kv_cache_lrkv_gb300 import binding as b
+    if isinstance(v, torch.Tensor):
+        return v.numel() * v.element_size()
+    if isinstance(v, (b.PagedCache, b.LayeredCache)):
+        return sum(_nbytes(t) for t in v.tensors())
+    if isinstance(v, (list, tuple)):
+        return sum(_nbytes(x) for x in v)
+    if isinstance(v, dict):
+        return sum(_nbytes(x) for x in v.values())
+    return 0
+
+
+class Rotating:
+    """Independent copies of a harness's per-step device data (caches, weights, activations).
+
+    Successive timed steps use successive copies, round-robin, so no step finds its inputs in
+    L2 from the step before: between two uses of a copy, every other copy's data streams
+    through.  The number of copies is chosen so that each large class of data (the cache
+    pools, the weights, ...) adds up to at least twice the L2 size over all copies; index
+    data (block tables, lengths, slots) and the workspace are shared."""
+
+    per_copy = ()  # attribute names that hold per-step device data
+
+    def rotation_classes(self):
+        """{label: bytes per copy} of the large data streams whose L2 residency must be broken."""
+        raise NotImplementedError
+
+    def copies_needed(self):
+        big = [v for v in self.rotation_classes().values() if v >= (1 << 20)]
+        need = max([3] + [-(-2 * L2_BYTES // v) for v in big])
+        per = max(1, sum(_nbytes(getattr(self, k)) for k in self.per_copy))
+        return int(max(1, min(need, ROTATION_MAX_COPIES, max(3, ROTATION_MAX_BYTES // per))))
+
+    def add_copies(self, n):
+        base = {k: getattr(self, k) for k in self.per_copy}
+        self.sets = [base] + [{k: _clone(v) for k, v in base.items()} for _ in range(n - 1)]
+        self.use(0)
+
+    def use(self, k):
+        for name, v in self.sets[k].items():
+            setattr(self, name, v)
+
+    def rotation_config(self):
+        n = len(self.sets)
+        per = sum(_nbytes(v) for v in self.sets[0].values())
+        return {"copies": n, "bytes_per_copy": int(per),
+                "classes_bytes_per_copy": {k: int(v) for k, v in self.rotation_classes().items()},
+                "rule": "consecutive steps use different copies round-robin; each large data class totals "
+                        ">= 2x L2 over the copies (at least 3 copies)"}
+
+    # end to end through the public API: upload each step's inputs from pinned host buffers into
+    # the copy the step uses, run the step's calls, download its result
+    def e2e_setup(self):
+        t = self.torch
+        self.use(0)
+        host_in = [x.cpu().pin_memory() for x in self.e2e_inputs()]
+        host_out = [t.empty_like(x, device="cpu").pin_memory() for x in self.e2e_outputs()]
+        self.e2e_pairs = []
+        for k in range(len(self.sets)):
+            self.use(k)
+            self.e2e_pairs.append((list(zip(host_in, self.e2e_inputs())), list(zip(host_out, self.e2e_outputs()))))
+        self.use(0)
+        return (sum(_nbytes(h) for h in host_in), sum(_nbytes(h) for h in host_out))
+
+    def e2e_step(self, stream, k=0):
+        self.use(k)
+        h_in, h_out = self.e2e_pairs[k]
+        for h, d in h_in:
+            d.copy_(h, non_blocking=True)
+        self.step(stream)
+        for h, d in h_out:
+            h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+
+# ----------------------------------------------------------------------------- decode
+class DecodeHarness(Rotating):
+    """Per layer: lrkv_append of each sequence's newest row, then lrkv_decode; several layers
+    go through the layer-batched calls (one launch of each kernel for all layers) unless
+    per_layer is set."""
+
+    per_copy = ("cache", "q", "BK", "BV", "wcat", "x", "qt", "out")
     profile = "decode_split_longctx.md"
     profiles = {"longctx": "decode_split_longctx.md", "dsv2": "decode_split_dsv2.md"}  # by workload
     sources = ("decode.cu", "lrkv_internal.cuh", "kernels.h")
 
-    def __init__(self, wl, rank, fused=False, d_rope=0):
+    def __init__(self, wl, rank, fused=False, d_rope=0, per_layer=False):
         import torch
 
         from compressed_kv_cache_lrkv_gb300 import binding as b
         self.torch, self.b, self.wl, self.fused, self.d_rope = torch, b, wl, fused, d_rope
         dr = d_rope
-        B, H, d_h, r, d = wl.B, wl.H, wl.d_h, wl.r, wl.d
+        B, H, d_h, r, d, Ly = wl.B, wl.H, wl.d_h, wl.r, wl.d, wl.layers
+        # the layer-batched calls have no absorbed-weights form: that one goes layer by layer
+        self.layered = Ly > 1 and not per_layer and not fused
         self.seq_lens = workload_seq_lens(wl)
         self.pt = S.page_table(wl.seed, self.seq_lens, 64)
         nb = self.pt.num_blocks
@@ -191,64 +296,69 @@ class DecodeHarness:
         rn = lambda *s, scale=1.0: (torch.randn(*s, generator=gen, device="cuda") * scale).to(torch.bfloat16)
         i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
         self.dims = b.make_dims(H, d_h, r, d, d_rope=dr)
-        self.layers = []
-        for _ in range(wl.layers):
-            self.layers.append(dict(
-                cache=b.PagedCache(rn(nb, 64, d_h + dr), rn(nb, 64, d_h), rn(nb, 64, H, r), rn(nb, 64, H, r)),
-                q=rn(B, H, d_h + dr), BK=rn(H, d_h, r, scale=r ** -0.5), BV=rn(H, d_h, r, scale=r ** -0.5),
-                wcat=rn(2 * (d_h + H * r) + dr, d, scale=d ** -0.5), x=rn(B, d),
-                qt=rn(B, H, r) if fused else None,
-                out=torch.empty(B, H, d_h + (r if fused else 0), dtype=torch.bfloat16, device="cuda")))
+        # every per-layer tensor carries a leading layer dimension
+        self.cache = b.LayeredCache(rn(Ly, nb, 64, d_h + dr), rn(Ly, nb, 64, d_h), rn(Ly, nb, 64, H, r),
+                                    rn(Ly, nb, 64, H, r))
+        self.q = rn(Ly, B, H, d_h + dr)
+        self.BK, self.BV = rn(Ly, H, d_h, r, scale=r ** -0.5), rn(Ly, H, d_h, r, scale=r ** -0.5)
+        self.wcat = rn(Ly, 2 * (d_h + H * r) + dr, d, scale=d ** -0.5)
+        self.x = rn(Ly, B, d)
+        self.qt = rn(Ly, B, H, r) if fused else None
+        self.out = torch.empty(Ly, B, H, d_h + (r if fused else 0), dtype=torch.bfloat16, device="cuda")
         self.bt = i32(self.pt.block_table)
         self.sl = i32(self.pt.seq_lens)
         self.slots = i32([self.pt.slot(i, int(L) - 1) for i, L in enumerate(self.seq_lens)])
         self.positions = i32(self.seq_lens - 1) if dr else None  # the newest token's position
-        self.ws = b.alloc_workspace(b.decode_workspace_bytes(self.dims, B))
+        self.ws = b.alloc_workspace(b.decode_workspace_bytes(self.dims, Ly * B))
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
-        self.cache_bytes = wl.layers * sum(t.numel() * t.element_size() for t in self.layers[0]["cache"].tensors())
+        self.cache_bytes = _nbytes(self.cache)
         acct = A.decode_fused_algorithmic_bytes if fused else A.decode_algorithmic_bytes
-        dec = acct(H, d_h, r, self.seq_lens, layers=wl.layers, d_rope=dr)
-        app = wl.layers * A.append_algorithmic_bytes(B, d, H, d_h, r, d_rope=dr)
+        dec = acct(H, d_h, r, self.seq_lens, layers=Ly, d_rope=dr)
+        app = Ly * A.append_algorithmic_bytes(B, d, H, d_h, r, d_rope=dr)
         self.kernel_units = dec          # algorithmic bytes of the timed kernel calls
         self.step_units = dec + app      # algorithmic bytes of a step
-        self.launches_per_step = wl.layers * (3 if fused else 4)
+        per = 3 if fused else 4
+        self.launches_per_step = per if self.layered else Ly * per
 
-    def _decode(self, L, stream):
+    def _decode(self, l, stream):
+        b = self.b
         if self.fused:
-            self.b.lrkv_decode_fused(self.dims, L["q"], L["qt"], L["cache"], self.bt, self.sl, L["out"], self.ws,
-                                     status=self.status, stream=stream)
+            b.lrkv_decode_fused(self.dims, self.q[l], self.qt[l], self.cache.layer(l), self.bt, self.sl, self.out[l],
+                                self.ws, status=self.status, stream=stream)
         else:
-            self.b.lrkv_decode(self.dims, L["q"], L["BK"], L["BV"], L["cache"], self.bt, self.sl, L["out"], self.ws,
-                               status=self.status, stream=stream)
+            b.lrkv_decode(self.dims, self.q[l], self.BK[l], self.BV[l], self.cache.layer(l), self.bt, self.sl,
+                          self.out[l], self.ws, status=self.status, stream=stream)
 
     def step(self, stream):
         b = self.b
-        for L in self.layers:
-            b.lrkv_append(self.dims, L["x"], L["wcat"], self.slots, L["cache"], status=self.status, stream=stream,
-                          positions=self.positions)
-            self._decode(L, stream)
+        if self.layered:
+            b.lrkv_append_layers(self.dims, self.x, self.wcat, self.slots, self.cache, status=self.status,
+                                 stream=stream, positions=self.positions)
+            b.lrkv_decode_layers(self.dims, self.q, self.BK, self.BV, self.cache, self.bt, self.sl, self.out,
+                                 self.ws, status=self.status, stream=stream)
+            return
+        for l in range(self.wl.layers):
+            b.lrkv_append(self.dims, self.x[l], self.wcat[l], self.slots, self.cache.layer(l), status=self.status,
+                          stream=stream, positions=self.positions)
+            self._decode(l, stream)
 
     def kernel(self, stream):
-        for L in self.layers:
-            self._decode(L, stream)
+        if self.layered:
+            self.b.lrkv_decode_layers(self.dims, self.q, self.BK, self.BV, self.cache, self.bt, self.sl, self.out,
+                                      self.ws, status=self.status, stream=stream)
+            return
+        for l in range(self.wl.layers):
+            self._decode(l, stream)
 
-    def e2e_setup(self):
-        t = self.torch
-        self.h_in = [(L["x"].cpu().pin_memory(), L["x"]) for L in self.layers] + \
-                    [(L[k].cpu().pin_memory(), L[k]) for L in self.layers for k in ("q", "qt") if L[k] is not None] + \
-                    [(self.slots.cpu().pin_memory(), self.slots), (self.sl.cpu().pin_memory(), self.sl)] + \
-                    ([(self.positions.cpu().pin_memory(), self.positions)] if self.d_rope else [])
-        self.h_out = [(t.empty_like(L["out"], device="cpu").pin_memory(), L["out"]) for L in self.layers]
-        return (sum(h.numel() * h.element_size() for h, _ in self.h_in),
-                sum(h.numel() * h.element_size() for h, _ in self.h_out))
+    def rotation_classes(self):
+        return {"cache": self.cache_bytes, "weights (W_cat, B^K, B^V)": _nbytes([self.wcat, self.BK, self.BV])}
 
-    def e2e_step(self, stream):
-        for h, d in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(stream)
-        for h, d in self.h_out:
-            h.copy_(d, non_blocking=True)
-        stream.synchronize()
+    def e2e_inputs(self):
+        return ([self.x, self.q] + ([self.qt] if self.qt is not None else []) + [self.slots, self.sl] +
+                ([self.positions] if self.d_rope else []))
+
+    def e2e_outputs(self):
+        return [self.out]
 
     def report(self, step_s, kernel_s, e2e_s, world, peaks):
         wl = self.wl
@@ -267,18 +377,23 @@ class DecodeHarness:
                        "l2": (f"inputs larger than L2: cache {self.cache_bytes / 2**20:.0f} MiB vs L2 "
                               f"{L2_BYTES / 2**20:.0f} MiB") if self.cache_bytes > L2_BYTES else
                              "cache fits in L2 (parity-sized workload; not an HBM measurement)",
-                       "step": "per layer: lrkv_append (1 row per sequence" +
-                               (", positional key rotated at its position) + " if self.d_rope else ") + ") +
-                               ("lrkv_decode_fused (q~ given, [o_s | o_z] returned)" if self.fused else "lrkv_decode"),
+                       "step": ("all layers at once: lrkv_append_layers (1 row per sequence and layer) + "
+                                "lrkv_decode_layers" if self.layered else
+                                "per layer: lrkv_append (1 row per sequence" +
+                                (", positional key rotated at its position) + " if self.d_rope else ") + ") +
+                                ("lrkv_decode_fused (q~ given, [o_s | o_z] returned)" if self.fused else
+                                 "lrkv_decode")),
                        "parallelism": f"replicas x{world} (independent batches)"},
             "roofline": {"kernel": "lrkv_decode_fused (split + combine kernels)" if self.fused else
-                                   "lrkv_decode (absorb + split + combine kernels)", "bound": "hbm",
+                                   ("lrkv_decode_layers (absorb + split + combine kernels, all layers)"
+                                    if self.layered else "lrkv_decode (absorb + split + combine kernels)"),
+                         "bound": "hbm",
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
                          "traffic": recorded_traffic(self.profiles[wl.key], self.sources)
                                     if wl.key in self.profiles and not self.fused and not self.d_rope else None,
-                         "algorithmic_bytes_per_launch": self.kernel_units // wl.layers,
-                         "avg_launch_ms": kernel_s * 1e3 / wl.layers},
+                         "algorithmic_bytes_per_launch": self.kernel_units // (1 if self.layered else wl.layers),
+                         "avg_launch_ms": kernel_s * 1e3 / (1 if self.layered else wl.layers)},
             "e2e_unit_value": lambda s: self.step_units * world / s / 1e9, "e2e_unit": "GB/s",
         }
 
@@ -316,8 +431,10 @@ class DecodeHarness:
 
 
 # ----------------------------------------------------------------------------- prefill
-class PrefillHarness:
+class PrefillHarness(Rotating):
     """Per 512-token chunk: lrkv_append of both sequences' rows, then lrkv_prefill."""
+
+    per_copy = ("cache", "BK", "BV", "wcat", "chunks")
 
     profile = "prefill_chunked.md"
     sources = ("prefill_tc.cu", "lrkv_internal.cuh", "kernels.h")
@@ -391,20 +508,15 @@ class PrefillHarness:
         self.join2.record(self.p2)
         stream.wait_event(self.join2)
 
-    def e2e_setup(self):
-        t = self.torch
-        self.h_in = [(ch[k].cpu().pin_memory(), ch[k]) for ch in self.chunks for k in ("x", "q")]
-        self.h_out = [(t.empty_like(ch["out"], device="cpu").pin_memory(), ch["out"]) for ch in self.chunks]
-        return (sum(h.numel() * h.element_size() for h, _ in self.h_in),
-                sum(h.numel() * h.element_size() for h, _ in self.h_out))
+    def rotation_classes(self):
+        return {"activations (X, q, out)": sum(_nbytes([ch["x"], ch["q"], ch["out"]]) for ch in self.chunks),
+                "cache": _nbytes(self.cache), "weights (W_cat, B^K, B^V)": _nbytes([self.wcat, self.BK, self.BV])}
 
-    def e2e_step(self, stream):
-        for h, d in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(stream)
-        for h, d in self.h_out:
-            h.copy_(d, non_blocking=True)
-        stream.synchronize()
+    def e2e_inputs(self):
+        return [ch[k] for ch in self.chunks for k in ("x", "q")]
+
+    def e2e_outputs(self):
+        return [ch["out"] for ch in self.chunks]
 
     def report(self, step_s, kernel_s, e2e_s, world, peaks):
         wl = self.wl
@@ -458,9 +570,11 @@ class PrefillHarness:
 
 
 # ----------------------------------------------------------------------------- MLA decode
-class MlaHarness:
+class MlaHarness(Rotating):
     """Multi-head latent attention with absorbed weights, per layer: lrkv_mla_append of each
     sequence's newest row [c | RoPE(k^R)], then lrkv_mla_decode."""
+
+    per_copy = ("kv", "q", "wt", "x", "out")
 
     profile = "mla_decode.md"
     sources = ("mla_decode.cu", "mla.h", "lrkv_internal.cuh", "kernels.h")
@@ -507,20 +621,14 @@ class MlaHarness:
         self.b.lrkv_mla_decode(self.dims, self.q, self.kv, self.bt, self.sl, self.out, self.ws, status=self.status,
                                stream=stream)
 
-    def e2e_setup(self):
-        t = self.torch
-        self.h_in = [(x.cpu().pin_memory(), x) for x in (self.x, self.q, self.slots, self.positions, self.sl)]
-        self.h_out = [(t.empty_like(self.out, device="cpu").pin_memory(), self.out)]
-        return (sum(h.numel() * h.element_size() for h, _ in self.h_in),
-                sum(h.numel() * h.element_size() for h, _ in self.h_out))
+    def rotation_classes(self):
+        return {"cache": self.cache_bytes, "weights ([W^DKV | W^KR])": _nbytes(self.wt)}
 
-    def e2e_step(self, stream):
-        for h, d in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(stream)
-        for h, d in self.h_out:
-            h.copy_(d, non_blocking=True)
-        stream.synchronize()
+    def e2e_inputs(self):
+        return [self.x, self.q, self.slots, self.positions, self.sl]
+
+    def e2e_outputs(self):
+        return [self.out]
 
     def report(self, step_s, kernel_s, e2e_s, world, peaks):
         wl = self.wl
@@ -573,9 +681,11 @@ class MlaHarness:
 
 
 # ----------------------------------------------------------------------------- training projection
-class TrainHarness:
+class TrainHarness(Rotating):
     """One projection (keys or values) of a training step: lrkv_train_forward, then
     lrkv_train_backward for a given dK."""
+
+    per_copy = ("X", "Wt", "B", "dK", "Y", "K", "dX", "dWt", "dB")
 
     profile = "train_projection.md"
     sources = ("train.cu", "train.h", "lrkv_internal.cuh", "kernels.h")
@@ -614,20 +724,15 @@ class TrainHarness:
         self.b.lrkv_train_backward(self.dims, self.X, self.Wt, self.B, self.Y, self.dK, self.dX, self.dWt, self.dB,
                                    self.ws, status=self.status, stream=stream)
 
-    def e2e_setup(self):
-        t = self.torch
-        self.h_in = [(x.cpu().pin_memory(), x) for x in (self.X, self.dK)]
-        self.h_out = [(t.empty_like(self.dB, device="cpu").pin_memory(), self.dB)]
-        return (sum(h.numel() * h.element_size() for h, _ in self.h_in),
-                sum(h.numel() * h.element_size() for h, _ in self.h_out))
+    def rotation_classes(self):
+        return {"activations (X, dK, Y, K, dX)": _nbytes([self.X, self.dK, self.Y, self.K, self.dX]),
+                "weights (W_T, B, dW_T, dB)": _nbytes([self.Wt, self.B, self.dWt, self.dB])}
 
-    def e2e_step(self, stream):
-        for h, d in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(stream)
-        for h, d in self.h_out:
-            h.copy_(d, non_blocking=True)
-        stream.synchronize()
+    def e2e_inputs(self):
+        return [self.X, self.dK]
+
+    def e2e_outputs(self):
+        return [self.dB]
 
     def report(self, step_s, kernel_s, e2e_s, world, peaks):
         wl = self.wl
@@ -691,65 +796,81 @@ def run_gpu(args, world, rank, local):
     wl = S.WORKLOADS[args.workload]
     if (args.fused or args.rope) and HARNESS[args.workload] is not DecodeHarness:
         raise SystemExit("--fused and --rope apply to the decode workloads")
-    if args.fused or args.rope:
-        hz = DecodeHarness(wl, rank, fused=args.fused, d_rope=64 if args.rope else 0)
+    if args.per_layer and HARNESS[args.workload] is not DecodeHarness:
+        raise SystemExit("--per-layer applies to the decode workloads")
+    if HARNESS[args.workload] is DecodeHarness:
+        hz = DecodeHarness(wl, rank, fused=args.fused, d_rope=64 if args.rope else 0, per_layer=args.per_layer)
     else:
         hz = HARNESS[args.workload](wl, rank)
     stream = torch.cuda.current_stream()
 
     # Each timed step is one replay of a CUDA graph of the public calls, so host
-    # launch overhead stays out of the device-timed region; a second graph holds
-    # only the dominant call (lrkv_decode / lrkv_prefill) for the roofline.
-    for _ in range(3):
+    # launch overhead stays out of the device-timed region; a second graph per copy holds
+    # only the dominant call (lrkv_decode / lrkv_prefill / ...) for the roofline.  The
+    # per-step data comes in independent copies replayed round-robin (Rotating), so no
+    # timed step or call reads inputs that the previous one left in L2.
+    n_copies = args.copies or hz.copies_needed()
+    hz.add_copies(n_copies)
+    for k in range(n_copies):
+        hz.use(k)
+        hz.step(stream)
+    for _ in range(2):
+        hz.use(0)
         hz.step(stream)
     torch.cuda.synchronize()
-    g_step, g_ker = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    g_step = [torch.cuda.CUDAGraph() for _ in range(n_copies)]
+    g_ker = [torch.cuda.CUDAGraph() for _ in range(n_copies)]
     cap = torch.cuda.Stream()
     cap.wait_stream(stream)
     with torch.cuda.stream(cap):
-        with torch.cuda.graph(g_step, stream=cap):
-            hz.step(cap)
-        with torch.cuda.graph(g_ker, stream=cap):
-            hz.kernel(cap)
+        for k in range(n_copies):
+            hz.use(k)
+            with torch.cuda.graph(g_step[k], stream=cap):
+                hz.step(cap)
+            with torch.cuda.graph(g_ker[k], stream=cap):
+                hz.kernel(cap)
+    hz.use(0)
     stream.wait_stream(cap)
     torch.cuda.synchronize()
 
+    def timed(graphs, reps):
+        """Seconds per replay over `reps` replays of `graphs` round-robin (CUDA events)."""
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(reps):
+            graphs[i % len(graphs)].replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) * 1e-3 / reps
+
     sampler = ClockSampler(local)
     sampler.start()
-    for _ in range(max(args.warmup, 3)):
-        g_step.replay()
+    for i in range(max(args.warmup, 3)):
+        g_step[i % n_copies].replay()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        g_step.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    step_s = timed(g_step, args.steps)
     t_wall1 = time.time()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    step_s = e0.elapsed_time(e1) * 1e-3 / args.steps
     # per-step spread, from a separate shorter loop so the timed region above has no extra events
     nd = max(1, min(args.steps, 200))
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(nd + 1)]
     evs[0].record(stream)
     for i in range(nd):
-        g_step.replay()
+        g_step[(args.steps + i) % n_copies].replay()
         evs[i + 1].record(stream)
     torch.cuda.synchronize()
     per_step_ms = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(nd))
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k0.record(stream)
-    for _ in range(args.steps):
-        g_ker.replay()
-    k1.record(stream)
-    torch.cuda.synchronize()
-    kernel_s = k0.elapsed_time(k1) * 1e-3 / args.steps
+    kernel_s = timed(g_ker, args.steps)
+    # the same graphs on one copy back to back: whatever of its inputs stays in L2 between
+    # replays is served from there (reported beside the rotated numbers, not as them)
+    kernel_warm_s = timed(g_ker[:1], args.steps)
+    step_warm_s = timed(g_step[:1], args.steps)
     if int(hz.status.item()) != 0:
         raise RuntimeError(f"device status {int(hz.status.item()):#x}")
 
@@ -758,13 +879,15 @@ def run_gpu(args, world, rank, local):
     e2e_steps = max(1, min(args.steps, 200))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        hz.e2e_step(stream)
+    for i in range(e2e_steps):
+        hz.e2e_step(stream, i % n_copies)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
+    hz.use(0)
     sampler.stop()
 
     if dist:
-        step_s, kernel_s, e2e_s = max_over_ranks([step_s, kernel_s, e2e_s], dist, device="cuda")
+        step_s, kernel_s, e2e_s, kernel_warm_s, step_warm_s = max_over_ranks(
+            [step_s, kernel_s, e2e_s, kernel_warm_s, step_warm_s], dist, device="cuda")
     if rank != 0:
         dist.destroy_process_group()
         return
@@ -785,7 +908,17 @@ def run_gpu(args, world, rank, local):
     line["step_ms_spread"] = {"median": statistics.median(per_step_ms), "min": per_step_ms[0],
                               "max": per_step_ms[-1], "reps": nd}
     line["gpu_launches"] = hz.launches_per_step * args.steps
-    line["timing"] = "each step is one replay of a CUDA graph of the public calls; CUDA events on the stream"
+    line["timing"] = ("each step is one replay of a CUDA graph of the public calls, the graphs of independent "
+                      "input copies replayed round-robin (see config.l2_rotation); CUDA events on the stream")
+    line["config"]["l2"] = "rotated input copies (no step reads inputs the previous step left in L2): " + \
+        line["config"].get("l2", "")
+    line["config"]["l2_rotation"] = hz.rotation_config()
+    rf = line["roofline"]
+    rf["avg_launch_ms_l2_warm"] = rf["avg_launch_ms"] * kernel_warm_s / kernel_s
+    rf["frac_l2_warm"] = rf["frac"] * kernel_s / kernel_warm_s
+    line["l2_warm"] = {"ms_per_step": step_warm_s * 1e3, "value": line["value"] * step_s / step_warm_s,
+                       "note": "one input copy replayed back to back (inputs may stay in L2 between steps); "
+                               "context only, not the reported value"}
     line["clocks"] = sampler.summary(t_wall0 - 0.3, t_wall1 + 0.3)
     print(json.dumps(line))
     if dist:
@@ -990,6 +1123,11 @@ def main():
     ap.add_argument("--impl", default="lrkv", choices=["lrkv", "reference"])
     ap.add_argument("--workload", default="longctx", choices=sorted(HARNESS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--per-layer", action="store_true",
+                    help="multi-layer decode workloads: one lrkv_append + lrkv_decode per layer instead of the "
+                         "layer-batched calls")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="independent input copies replayed round-robin (0: enough to break L2 residency)")
     ap.add_argument("--fused", action="store_true",
                     help="decode with absorbed weights (lrkv_decode_fused: q~ given, [o_s | o_z] returned)")
     ap.add_argument("--rope", action="store_true",

@@ -21,6 +21,7 @@ DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 EXPORTED = ["lrkv_abi_version", "lrkv_status_string", "lrkv_last_error", "lrkv_cache_block_bytes", "lrkv_append",
             "lrkv_decode_workspace_bytes", "lrkv_decode", "lrkv_decode_fused", "lrkv_decode_static_ws",
+            "lrkv_append_layers", "lrkv_decode_layers",
             "lrkv_prefill_workspace_bytes", "lrkv_prefill", "lrkv_mla_cache_block_bytes", "lrkv_mla_append",
             "lrkv_mla_decode_workspace_bytes", "lrkv_mla_decode", "lrkv_train_forward", "lrkv_train_workspace_bytes",
             "lrkv_train_backward"]
@@ -36,7 +37,12 @@ class LrkvError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("d_h", ctypes.c_int32), ("r", ctypes.c_int32), ("d", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("softmax_scale", ctypes.c_float), ("d_rope", ctypes.c_int32),
-                ("rope_base", ctypes.c_float)]
+                ("rope_base", ctypes.c_float), ("num_splits", ctypes.c_int32)]
+
+
+class LayerStrides(ctypes.Structure):
+    """Element strides between consecutive layers' tensors (lrkv_layer_strides)."""
+    _fields_ = [(n, ctypes.c_int64) for n in ("X", "W_catT", "q", "BK", "BV", "out", "sK", "sV", "zK", "zV")]
 
 
 class MlaDims(ctypes.Structure):
@@ -78,6 +84,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lrkv_decode.argtypes = [P(Dims), vp, vp, vp, P(Cache), vp, i32, vp, i32, vp, vp, sz, vp, vp]
     lib.lrkv_decode_fused.restype = ctypes.c_int
     lib.lrkv_decode_fused.argtypes = [P(Dims), vp, vp, P(Cache), vp, i32, vp, i32, vp, vp, sz, vp, vp]
+    lib.lrkv_append_layers.restype = ctypes.c_int
+    lib.lrkv_append_layers.argtypes = [P(Dims), i32, P(LayerStrides), vp, vp, i32, vp, vp, P(Cache), vp, vp]
+    lib.lrkv_decode_layers.restype = ctypes.c_int
+    lib.lrkv_decode_layers.argtypes = [P(Dims), i32, P(LayerStrides), vp, vp, vp, P(Cache), vp, i32, vp, i32, vp, vp,
+                                       sz, vp, vp]
     lib.lrkv_decode_static_ws.restype = ctypes.c_int
     lib.lrkv_decode_static_ws.argtypes = [P(Dims), vp, vp, vp, P(Cache), vp, i32, vp, i32, vp, vp, vp]
     lib.lrkv_prefill_workspace_bytes.restype = sz
@@ -103,8 +114,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
 
 
 def make_dims(H: int, d_h: int, r: int, d: int, block_size: int = 64, softmax_scale: float = 0.0, d_rope: int = 0,
-              rope_base: float = 0.0) -> Dims:
-    return Dims(H, d_h, r, d, block_size, softmax_scale, d_rope, rope_base)
+              rope_base: float = 0.0, num_splits: int = 0) -> Dims:
+    return Dims(H, d_h, r, d, block_size, softmax_scale, d_rope, rope_base, num_splits)
 
 
 def make_mla_dims(H: int, d: int, d_head: int = 128, d_c: int = 512, d_rope: int = 64, block_size: int = 64,
@@ -212,6 +223,65 @@ def lrkv_decode_static_ws(dims: Dims, q, BK, BV, cache: PagedCache, block_table,
                                       _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens), B, _ptr(out),
                                       _ptr(status), _stream(stream))
     _check(rc, "lrkv_decode_static_ws")
+
+
+class LayeredCache:
+    """Several layers' cache pools as tensors with a leading layer dimension
+    ([layers, num_blocks, block_size, ...]); layer l is at l * stride(0) elements."""
+
+    def __init__(self, sK, sV, zK, zV):
+        self.sK, self.sV, self.zK, self.zV = sK, sV, zK, zV
+        self.num_layers = int(sK.shape[0])
+        self.num_blocks = int(sK.shape[1])
+
+    @classmethod
+    def empty(cls, num_layers: int, num_blocks: int, H: int, d_h: int, r: int, block_size: int = 64, device="cuda",
+              d_rope: int = 0):
+        mk = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=device)
+        return cls(mk(num_layers, num_blocks, block_size, d_h + d_rope), mk(num_layers, num_blocks, block_size, d_h),
+                   mk(num_layers, num_blocks, block_size, H, r), mk(num_layers, num_blocks, block_size, H, r))
+
+    def struct(self) -> Cache:
+        return Cache(_ptr(self.sK), _ptr(self.sV), _ptr(self.zK), _ptr(self.zV), self.num_blocks)
+
+    def tensors(self):
+        return self.sK, self.sV, self.zK, self.zV
+
+    def layer(self, l: int) -> PagedCache:
+        return PagedCache(self.sK[l], self.sV[l], self.zK[l], self.zV[l])
+
+
+def _layer_stride(t) -> int:
+    return 0 if t is None else int(t.stride(0))
+
+
+def lrkv_append_layers(dims: Dims, X, W_catT, slot_mapping, cache: LayeredCache, status=None, stream=None,
+                       positions=None):
+    """lrkv_append of the same slots in every layer: X [L, n, d], W_catT [L, N, d] -> the L layers' pools."""
+    L, n = int(X.shape[0]), int(X.shape[1])
+    st = LayerStrides(X=_layer_stride(X), W_catT=_layer_stride(W_catT), sK=_layer_stride(cache.sK),
+                      sV=_layer_stride(cache.sV), zK=_layer_stride(cache.zK), zV=_layer_stride(cache.zV))
+    c = cache.struct()
+    rc = load().lrkv_append_layers(ctypes.byref(dims), L, ctypes.byref(st), _ptr(X), _ptr(W_catT), n,
+                                   _ptr(slot_mapping), _ptr(positions), ctypes.byref(c), _ptr(status),
+                                   _stream(stream))
+    _check(rc, "lrkv_append_layers")
+
+
+def lrkv_decode_layers(dims: Dims, q, BK, BV, cache: LayeredCache, block_table, seq_lens, out, workspace, status=None,
+                       stream=None):
+    """lrkv_decode of the same batch in every layer: q [L, B, H, d_h], B* [L, H, d_h, r] -> out [L, B, H, d_h];
+    workspace of decode_workspace_bytes(dims, L * B) bytes."""
+    L, B = int(q.shape[0]), int(q.shape[1])
+    st = LayerStrides(q=_layer_stride(q), BK=_layer_stride(BK), BV=_layer_stride(BV), out=_layer_stride(out),
+                      sK=_layer_stride(cache.sK), sV=_layer_stride(cache.sV), zK=_layer_stride(cache.zK),
+                      zV=_layer_stride(cache.zV))
+    c = cache.struct()
+    rc = load().lrkv_decode_layers(ctypes.byref(dims), L, ctypes.byref(st), _ptr(q), _ptr(BK), _ptr(BV),
+                                   ctypes.byref(c), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens), B,
+                                   _ptr(out), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                   _ptr(status), _stream(stream))
+    _check(rc, "lrkv_decode_layers")
 
 
 def lrkv_prefill(dims: Dims, q, BK, BV, cache: PagedCache, block_table, q_start, out, workspace=None, status=None,

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "lrkv_internal.cuh"
@@ -33,6 +34,8 @@ lrkv_status ok() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int kMaxSplits = 1 << 16;
+
 lrkv_status check_dims(const lrkv_dims* dm) {
     if (!dm) return fail(LRKV_ERR_INVALID_ARG, "dims is NULL");
     if (dm->block_size != 64) return fail(LRKV_ERR_UNSUPPORTED, "block_size %d (only 64 is supported)", dm->block_size);
@@ -48,8 +51,25 @@ lrkv_status check_dims(const lrkv_dims* dm) {
         return fail(LRKV_ERR_UNSUPPORTED, "d_rope %d (supported: 0, 64)", dm->d_rope);
     if (!(dm->rope_base >= 0.f) || std::isinf(dm->rope_base) || (dm->rope_base > 0.f && dm->rope_base <= 1.f))
         return fail(LRKV_ERR_INVALID_ARG, "rope_base %g (0 for 10000, else > 1)", (double)dm->rope_base);
+    if (dm->num_splits < 0 || dm->num_splits > kMaxSplits)
+        return fail(LRKV_ERR_INVALID_ARG, "num_splits %d (0 = automatic, else 1..%d)", dm->num_splits, kMaxSplits);
     return LRKV_OK;
 }
+
+// Limit of the decode split kernel's pipeline waits: about 2 s, unless the environment
+// variable LRKV_DEBUG_WAIT_LIMIT_NS sets another (a debugging aid: with a short limit a wait
+// that is merely slow gives up and the call reports LRKV_DEV_TIMEOUT, which lets a test see
+// the expiry path run to its end on a healthy GPU).
+unsigned long long decode_wait_limit_ns() {
+    const char* v = std::getenv("LRKV_DEBUG_WAIT_LIMIT_NS");
+    if (!v || !*v) return lrkv::kWaitLimitNs;
+    char* end = nullptr;
+    const unsigned long long x = std::strtoull(v, &end, 10);
+    return (end && *end == '\0' && x <= lrkv::kWaitLimitNs) ? x : lrkv::kWaitLimitNs;
+}
+
+// Ranges a decode cuts the batch's cached tokens into: the caller's count, else one per SM.
+int decode_ranges(const lrkv_dims* dm, int sms) { return dm->num_splits > 0 ? dm->num_splits : sms; }
 
 // Logit scale: the caller's, else 1/sqrt of the full key width d_h + d_rope.
 float logit_scale(const lrkv_dims* dm) {
@@ -149,6 +169,34 @@ lrkv_status make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t
     return LRKV_OK;
 }
 
+// 3-D bf16 tensor map over `layers` row-major [rows][cols] matrices, layer_pitch bytes apart
+// (any valid pitch when layers == 1), with a {box_cols, box_rows, 1} box and 128-byte swizzle.
+lrkv_status make_tmap_layers(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t layers,
+                             uint64_t layer_pitch, uint32_t box_cols, uint32_t box_rows, const char* what) {
+    auto enc = encode_fn();
+    if (!enc) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[3] = {cols, rows, layers};
+    cuuint64_t strides[2] = {cols * 2, layers > 1 ? layer_pitch : cols * 2 * rows};
+    cuuint32_t box[3] = {box_cols, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+    return LRKV_OK;
+}
+
+// A per-layer stride (elements) of a layer-batched call: at least the layer's own extent (layers
+// do not overlap) and a multiple of 8 elements (16 bytes).  Unused when num_layers == 1.
+lrkv_status check_stride(int64_t stride, uint64_t extent, int32_t num_layers, const char* what) {
+    if (num_layers <= 1) return LRKV_OK;
+    if (stride < 0 || (uint64_t)stride < extent || (stride & 7) != 0)
+        return fail(LRKV_ERR_INVALID_ARG,
+                    "layer stride of %s is %lld elements (must be a multiple of 8 and >= the layer's %llu)", what,
+                    (long long)stride, (unsigned long long)extent);
+    return LRKV_OK;
+}
+
 lrkv_status check_mla_dims(const lrkv_mla_dims* dm) {
     if (!dm) return fail(LRKV_ERR_INVALID_ARG, "dims is NULL");
     if (dm->block_size != 64) return fail(LRKV_ERR_UNSUPPORTED, "block_size %d (only 64 is supported)", dm->block_size);
@@ -202,13 +250,17 @@ size_t lrkv_cache_block_bytes(const lrkv_dims* dims) {
     return (size_t)dims->block_size * 2 * (2 * (size_t)(dims->d_h + dims->H * dims->r) + (size_t)dims->d_rope);
 }
 
-lrkv_status lrkv_append(const lrkv_dims* dims, const void* X, const void* W_catT, int32_t n_tok,
-                        const int32_t* slot_mapping, const int32_t* positions, const lrkv_cache* cache,
-                        uint32_t* status_dev, void* stream) {
+// Shared body of lrkv_append (one layer) and lrkv_append_layers.
+static lrkv_status append_impl(const lrkv_dims* dims, int32_t num_layers, const lrkv_layer_strides* ls,
+                               const void* X, const void* W_catT, int32_t n_tok, const int32_t* slot_mapping,
+                               const int32_t* positions, const lrkv_cache* cache, uint32_t* status_dev,
+                               void* stream) {
     lrkv_status s = check_dims(dims);
     if (s != LRKV_OK) return s;
     if ((s = check_cache(cache)) != LRKV_OK) return s;
     if (n_tok < 0) return fail(LRKV_ERR_INVALID_ARG, "n_tok %d < 0", n_tok);
+    if (num_layers < 1) return fail(LRKV_ERR_INVALID_ARG, "num_layers %d < 1", num_layers);
+    if (num_layers > 1 && !ls) return fail(LRKV_ERR_INVALID_ARG, "layer strides are NULL");
     if (n_tok == 0) return ok();
     LRKV_REQUIRE_PTR(X);
     LRKV_REQUIRE_PTR(W_catT);
@@ -233,36 +285,87 @@ lrkv_status lrkv_append(const lrkv_dims* dims, const void* X, const void* W_catT
     a.positions = dims->d_rope > 0 ? positions : nullptr;
     a.HR = dims->H * dims->r;
     a.nslots = (long long)cache->num_blocks * dims->block_size;
-    if (n_tok >= lrkv::kAppendTcMinRows) {
-        CUtensorMap tX, tW;
-        const int bn = lrkv::append_tc_block_n(a.N);
-        if ((s = make_tmap(&tX, X, dims->d, n_tok, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "X")) != LRKV_OK) return s;
-        if ((s = make_tmap(&tW, W_catT, dims->d, a.N, 64, bn, CU_TENSOR_MAP_SWIZZLE_128B, "W_catT")) != LRKV_OK)
+    a.layers = num_layers;
+    if (num_layers > 1) {
+        const uint64_t rows = (uint64_t)a.nslots;
+        if ((s = check_stride(ls->X, (uint64_t)n_tok * a.d, num_layers, "X")) != LRKV_OK ||
+            (s = check_stride(ls->W_catT, (uint64_t)a.N * a.d, num_layers, "W_catT")) != LRKV_OK ||
+            (s = check_stride(ls->sK, rows * (a.d_h + a.d_rope), num_layers, "sK")) != LRKV_OK ||
+            (s = check_stride(ls->sV, rows * a.d_h, num_layers, "sV")) != LRKV_OK ||
+            (s = check_stride(ls->zK, rows * a.HR, num_layers, "zK")) != LRKV_OK ||
+            (s = check_stride(ls->zV, rows * a.HR, num_layers, "zV")) != LRKV_OK)
             return s;
-        return cuda_status(lrkv::launch_append_tc(tX, tW, a, static_cast<cudaStream_t>(stream)),
-                           "lrkv_append launch");
+        a.ls_X = ls->X;
+        a.ls_W = ls->W_catT;
+        a.ls_sK = ls->sK;
+        a.ls_sV = ls->sV;
+        a.ls_zK = ls->zK;
+        a.ls_zV = ls->zV;
+    }
+    if (n_tok >= lrkv::kAppendTcMinRows) {
+        // the tensor-core GEMM: one launch per layer (its tensor maps are per layer)
+        lrkv::AppendArgs al = a;
+        al.layers = 1;
+        for (int l = 0; l < num_layers; ++l) {
+            al.X = a.X + l * a.ls_X;
+            al.W = a.W + l * a.ls_W;
+            al.sK = a.sK + l * a.ls_sK;
+            al.sV = a.sV + l * a.ls_sV;
+            al.zK = a.zK + l * a.ls_zK;
+            al.zV = a.zV + l * a.ls_zV;
+            CUtensorMap tX, tW;
+            const int bn = lrkv::append_tc_block_n(a.N);
+            if ((s = make_tmap(&tX, al.X, dims->d, n_tok, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "X")) != LRKV_OK)
+                return s;
+            if ((s = make_tmap(&tW, al.W, dims->d, a.N, 64, bn, CU_TENSOR_MAP_SWIZZLE_128B, "W_catT")) != LRKV_OK)
+                return s;
+            if ((s = cuda_status(lrkv::launch_append_tc(tX, tW, al, static_cast<cudaStream_t>(stream)),
+                                 "lrkv_append launch")) != LRKV_OK)
+                return s;
+        }
+        return ok();
     }
     return cuda_status(lrkv::launch_append(a, static_cast<cudaStream_t>(stream)), "lrkv_append launch");
+}
+
+lrkv_status lrkv_append(const lrkv_dims* dims, const void* X, const void* W_catT, int32_t n_tok,
+                        const int32_t* slot_mapping, const int32_t* positions, const lrkv_cache* cache,
+                        uint32_t* status_dev, void* stream) {
+    return append_impl(dims, 1, nullptr, X, W_catT, n_tok, slot_mapping, positions, cache, status_dev, stream);
+}
+
+lrkv_status lrkv_append_layers(const lrkv_dims* dims, int32_t num_layers, const lrkv_layer_strides* strides,
+                               const void* X, const void* W_catT, int32_t n_tok, const int32_t* slot_mapping,
+                               const int32_t* positions, const lrkv_cache* cache, uint32_t* status_dev,
+                               void* stream) {
+    return append_impl(dims, num_layers, strides, X, W_catT, n_tok, slot_mapping, positions, cache, status_dev,
+                       stream);
 }
 
 size_t lrkv_decode_workspace_bytes(const lrkv_dims* dims, int32_t batch) {
     if (check_dims(dims) != LRKV_OK || batch < 0) return 0;
     DeviceInfo di;
     if (device_info(&di) != LRKV_OK) return 0;
-    return lrkv::decode_workspace_bytes(dims->H, dims->d_h, dims->r, batch, di.sms, di.smem_optin);
+    return lrkv::decode_workspace_bytes(dims->H, dims->d_h, dims->r, batch, decode_ranges(dims, di.sms));
 }
 
-// Shared body of lrkv_decode (q~ = q B^K computed here, output B^V-projected) and
-// lrkv_decode_fused (q~ given by the caller, output [o_s | o_z] / l).
-static lrkv_status decode_impl(const lrkv_dims* dims, const void* q, const void* q_tilde, const void* BK,
-                               const void* BV, const lrkv_cache* cache, const int32_t* block_table,
-                               int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch, void* out,
-                               void* workspace, size_t workspace_bytes, uint32_t* status_dev, void* stream) {
+// Shared body of lrkv_decode (q~ = q B^K computed here, output B^V-projected), lrkv_decode_fused
+// (q~ given by the caller, output [o_s | o_z] / l) and lrkv_decode_layers (several layers).
+static lrkv_status decode_impl(const lrkv_dims* dims, int32_t num_layers, const lrkv_layer_strides* ls,
+                               const void* q, const void* q_tilde, const void* BK, const void* BV,
+                               const lrkv_cache* cache, const int32_t* block_table, int32_t max_blocks_per_seq,
+                               const int32_t* seq_lens, int32_t batch, void* out, void* workspace,
+                               size_t workspace_bytes, uint32_t* status_dev, void* stream) {
     const bool fused = q_tilde != nullptr;
     lrkv_status s = check_dims(dims);
     if (s != LRKV_OK) return s;
     if ((s = check_cache(cache)) != LRKV_OK) return s;
     if (batch < 0) return fail(LRKV_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (num_layers < 1) return fail(LRKV_ERR_INVALID_ARG, "num_layers %d < 1", num_layers);
+    if (num_layers > 1 && !ls) return fail(LRKV_ERR_INVALID_ARG, "layer strides are NULL");
+    if ((long long)num_layers * batch > 65535)  // one grid row per (layer, sequence)
+        return fail(LRKV_ERR_INVALID_ARG, "num_layers x batch = %lld (at most 65535)",
+                    (long long)num_layers * batch);
     if (batch == 0) return ok();
     if (max_blocks_per_seq < 1 || (long long)max_blocks_per_seq * dims->block_size > (1LL << 30))
         return fail(LRKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", max_blocks_per_seq);
@@ -275,21 +378,46 @@ static lrkv_status decode_impl(const lrkv_dims* dims, const void* q, const void*
     }
     LRKV_REQUIRE_PTR(out);
     if (!block_table || !seq_lens) return fail(LRKV_ERR_INVALID_ARG, "block_table or seq_lens is NULL");
+    const uint64_t rows = (uint64_t)cache->num_blocks * dims->block_size;
+    const uint64_t dk = (uint64_t)dims->d_h + dims->d_rope;  // key row [s^K | k^R]
+    const uint64_t HR = (uint64_t)dims->H * dims->r;
+    lrkv::DecodeArgs a{};
+    a.layers = num_layers;
+    if (num_layers > 1) {
+        if ((s = check_stride(ls->q, (uint64_t)batch * dims->H * dk, num_layers, "q")) != LRKV_OK ||
+            (s = check_stride(ls->out, (uint64_t)batch * dims->H * dims->d_h, num_layers, "out")) != LRKV_OK ||
+            (s = check_stride(ls->BK, HR * dims->d_h, num_layers, "BK")) != LRKV_OK ||
+            (s = check_stride(ls->BV, HR * dims->d_h, num_layers, "BV")) != LRKV_OK ||
+            (s = check_stride(ls->sK, rows * dk, num_layers, "sK")) != LRKV_OK ||
+            (s = check_stride(ls->sV, rows * dims->d_h, num_layers, "sV")) != LRKV_OK ||
+            (s = check_stride(ls->zK, rows * HR, num_layers, "zK")) != LRKV_OK ||
+            (s = check_stride(ls->zV, rows * HR, num_layers, "zV")) != LRKV_OK)
+            return s;
+        a.ls_q = ls->q;
+        a.ls_out = ls->out;
+        a.ls_BK = ls->BK;
+        a.ls_BV = ls->BV;
+        a.ls_zK = ls->zK;
+        a.ls_zV = ls->zV;
+    }
     DeviceInfo di;
     if ((s = device_info(&di)) != LRKV_OK) return s;
-    const size_t need = lrkv::decode_workspace_bytes(dims->H, dims->d_h, dims->r, batch, di.sms, di.smem_optin);
+    const int nvb = num_layers * batch;
+    const int nranges = decode_ranges(dims, di.sms);
+    const size_t need = lrkv::decode_workspace_bytes(dims->H, dims->d_h, dims->r, nvb, nranges);
     if (!workspace || ((uintptr_t)workspace & 255u))
         return fail(LRKV_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
     if (workspace_bytes < need)
         return fail(LRKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
 
     CUtensorMap tK, tV;
-    const uint64_t rows = (uint64_t)cache->num_blocks * dims->block_size;
-    const uint64_t dk = (uint64_t)dims->d_h + dims->d_rope;  // key row [s^K | k^R]
-    if ((s = make_tmap(&tK, cache->sK, dk, rows, 64, 8, CU_TENSOR_MAP_SWIZZLE_128B, "sK")) != LRKV_OK) return s;
-    if ((s = make_tmap(&tV, cache->sV, dims->d_h, rows, 64, 8, CU_TENSOR_MAP_SWIZZLE_128B, "sV")) != LRKV_OK) return s;
+    if ((s = make_tmap_layers(&tK, cache->sK, dk, rows, num_layers, num_layers > 1 ? (uint64_t)ls->sK * 2 : 0, 64, 8,
+                              "sK")) != LRKV_OK)
+        return s;
+    if ((s = make_tmap_layers(&tV, cache->sV, dims->d_h, rows, num_layers,
+                              num_layers > 1 ? (uint64_t)ls->sV * 2 : 0, 64, 8, "sV")) != LRKV_OK)
+        return s;
 
-    lrkv::DecodeArgs a{};
     a.q = static_cast<const uint16_t*>(q);
     a.BK = static_cast<const uint16_t*>(BK);
     a.BV = static_cast<const uint16_t*>(BV);
@@ -305,8 +433,10 @@ static lrkv_status decode_impl(const lrkv_dims* dims, const void* q, const void*
     a.H = dims->H;
     a.max_pages = max_blocks_per_seq;
     a.num_blocks = cache->num_blocks;
+    a.nranges = nranges;
+    a.wait_ns = decode_wait_limit_ns();
     a.scale_log2 = logit_scale(dims) * 1.4426950408889634f;
-    lrkv::decode_carve_workspace(&a, workspace, dims->H, dims->d_h, dims->r, batch, di.sms, di.smem_optin);
+    lrkv::decode_carve_workspace(&a, workspace, dims->H, dims->d_h, dims->r, nvb, nranges);
     return cuda_status(lrkv::launch_decode(tK, tV, a, dims->d_h, dims->r, dims->d_rope, di.sms, di.smem_optin,
                                            static_cast<cudaStream_t>(stream)),
                        fused ? "lrkv_decode_fused launch" : "lrkv_decode launch");
@@ -316,8 +446,17 @@ lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, co
                         const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                         int32_t batch, void* out, void* workspace, size_t workspace_bytes, uint32_t* status_dev,
                         void* stream) {
-    return decode_impl(dims, q, nullptr, BK, BV, cache, block_table, max_blocks_per_seq, seq_lens, batch, out,
-                       workspace, workspace_bytes, status_dev, stream);
+    return decode_impl(dims, 1, nullptr, q, nullptr, BK, BV, cache, block_table, max_blocks_per_seq, seq_lens, batch,
+                       out, workspace, workspace_bytes, status_dev, stream);
+}
+
+lrkv_status lrkv_decode_layers(const lrkv_dims* dims, int32_t num_layers, const lrkv_layer_strides* strides,
+                               const void* q, const void* BK, const void* BV, const lrkv_cache* cache,
+                               const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               int32_t batch, void* out, void* workspace, size_t workspace_bytes,
+                               uint32_t* status_dev, void* stream) {
+    return decode_impl(dims, num_layers, strides, q, nullptr, BK, BV, cache, block_table, max_blocks_per_seq,
+                       seq_lens, batch, out, workspace, workspace_bytes, status_dev, stream);
 }
 
 lrkv_status lrkv_decode_fused(const lrkv_dims* dims, const void* q, const void* q_tilde, const lrkv_cache* cache,
@@ -325,8 +464,8 @@ lrkv_status lrkv_decode_fused(const lrkv_dims* dims, const void* q, const void* 
                               int32_t batch, void* out, void* workspace, size_t workspace_bytes,
                               uint32_t* status_dev, void* stream) {
     if (!q_tilde) return fail(LRKV_ERR_INVALID_ARG, "q_tilde is NULL");
-    return decode_impl(dims, q, q_tilde, nullptr, nullptr, cache, block_table, max_blocks_per_seq, seq_lens, batch,
-                       out, workspace, workspace_bytes, status_dev, stream);
+    return decode_impl(dims, 1, nullptr, q, q_tilde, nullptr, nullptr, cache, block_table, max_blocks_per_seq,
+                       seq_lens, batch, out, workspace, workspace_bytes, status_dev, stream);
 }
 
 size_t lrkv_prefill_workspace_bytes(const lrkv_dims* dims, int32_t batch, int32_t Tq) {

@@ -8,7 +8,8 @@
 // (a decode step appends one row per sequence): the weight rows (W_cat^T,
 // contiguous along d) are streamed exactly once with 16-byte loads, for a block
 // of token rows at a time -- on the CUDA cores below 64 MB of weights, as a
-// split-K product on the warp-level tensor cores above.  fp32 accumulation in a
+// split-K product on the warp-level tensor cores above.  A layer-batched call runs
+// every layer in the same launch (grid z = layer, per-layer strides in the arguments).  fp32 accumulation in a
 // fixed order, round to nearest even to bf16 (after rotating the positional-key
 // pairs), scatter to the row's slot.
 #include "kernels.h"
@@ -17,6 +18,18 @@
 
 namespace lrkv {
 
+
+// The arguments of layer z of a layer-batched launch (z = 0 or a single layer: unchanged).
+__device__ __forceinline__ AppendArgs layer_args(const AppendArgs& a, int z) {
+    AppendArgs l = a;
+    l.X += z * a.ls_X;
+    l.W += z * a.ls_W;
+    l.sK += z * a.ls_sK;
+    l.sV += z * a.ls_sV;
+    l.zK += z * a.ls_zK;
+    l.zV += z * a.ls_zV;
+    return l;
+}
 
 // Store one finished fp32 value of output column `col` for token slot `slot`.
 __device__ __forceinline__ void store_cache_value(const AppendArgs& a, long long slot, int col, float v) {
@@ -87,7 +100,8 @@ __device__ __forceinline__ void rowwise_partials(const AppendArgs& a, const uint
 // shared positional key a CTA computes the two columns of one rotation pair and turns
 // them at each row's position before rounding.
 template <int NT, bool ROPE>
-__global__ void __launch_bounds__(128) append_rowwise_kernel(const AppendArgs a) {
+__global__ void __launch_bounds__(128) append_rowwise_kernel(const AppendArgs a0) {
+    const AppendArgs a = layer_args(a0, blockIdx.z);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int u = blockIdx.x, half = ROPE ? a.d_rope / 2 : 0;
     const bool pair = ROPE && u >= a.d_h && u < a.d_h + half;  // uniform over the CTA
@@ -179,7 +193,8 @@ constexpr int kMmaPitch = kMmaCols + 4;  // partial-sum row pitch in floats (con
 // memory by rank 0 in rank order (deterministic), which then rounds (after rotating the
 // positional-key pairs) and stores.
 template <int NB, bool ROPE>
-__global__ void __launch_bounds__(256, 2) append_mma_kernel(const AppendArgs a, int kwarp) {
+__global__ void __launch_bounds__(256, 2) append_mma_kernel(const AppendArgs a0, int kwarp) {
+    const AppendArgs a = layer_args(a0, blockIdx.z);
     constexpr int NT = 8 * NB;
     __shared__ float part[8][NT][kMmaPitch];
     __shared__ float csum[NT][kMmaCols];
@@ -306,7 +321,7 @@ __global__ void __launch_bounds__(256, 2) append_mma_kernel(const AppendArgs a, 
 template <int NB, bool ROPE>
 static cudaError_t launch_mma(const AppendArgs& a, int ks, int kwarp, cudaStream_t stream) {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(((a.N + kMmaCols - 1) / kMmaCols) * ks, (a.n + 8 * NB - 1) / (8 * NB));
+    cfg.gridDim = dim3(((a.N + kMmaCols - 1) / kMmaCols) * ks, (a.n + 8 * NB - 1) / (8 * NB), a.layers > 1 ? a.layers : 1);
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -323,7 +338,7 @@ static cudaError_t launch_mma(const AppendArgs& a, int ks, int kwarp, cudaStream
 static cudaError_t launch_rowwise(const AppendArgs& a, cudaStream_t stream) {
 #define LRKV_ROW(NTV)                                                                    \
     {                                                                                    \
-        dim3 grid(a.N - a.d_rope / 2, (a.n + NTV - 1) / NTV); /* pairs: one CTA each */ \
+        dim3 grid(a.N - a.d_rope / 2, (a.n + NTV - 1) / NTV, a.layers > 1 ? a.layers : 1);  \
         if (a.d_rope > 0)                                                                \
             append_rowwise_kernel<NTV, true><<<grid, 128, 0, stream>>>(a);               \
         else                                                                             \
@@ -342,6 +357,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     // Weight streams up to 64 MB: one CTA per output column (the hidden rows stay in L1/L2 at that
     // size and there is no cluster setup); larger ones re-read the hidden rows once per column
     // from L2, so they go through the split-K tensor-core kernel above.
+    // (pairs of the positional key: one CTA each; several layers: one grid slice each)
     if ((long long)a.N * a.d * 2 < (64LL << 20)) return launch_rowwise(a, stream);
     // Split d so that the grid fills two CTAs per SM in one wave (at most 8 CTAs per cluster,
     // at least one 64-wide step per warp).
@@ -351,7 +367,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     const int groups = (a.N + kMmaCols - 1) / kMmaCols;
     const int rowblocks = (a.n + 8 * nb - 1) / (8 * nb);
     const int steps = (a.d + 63) / 64;  // 64-wide k steps
-    int ks = (2 * sms) / (groups * rowblocks);
+    int ks = (2 * sms) / (groups * rowblocks * (a.layers > 1 ? a.layers : 1));
     ks = ks < 1 ? 1 : ks > 8 ? 8 : ks;
     while (ks > 1 && ks * 8 > steps) --ks;
     const int kwarp = ((steps + ks * 8 - 1) / (ks * 8)) * 64;

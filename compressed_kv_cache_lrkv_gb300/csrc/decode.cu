@@ -9,21 +9,27 @@
 // query [q | q^R]: the tensor-core logits simply run over D_K = D_H + D_R columns,
 // while q~ = q B^K uses the first D_H of them.
 //
-// Kernel 0 (absorb): q~ for every (sequence, head) into the workspace, fp32.
-// Kernel 1 (split): a persistent grid of one CTA per SM, launched with
+// One call may cover several layers (each with its own cache pools, q, B^K, B^V and
+// output, found at per-layer strides, all sharing the block table and lengths): every
+// (layer, sequence) pair is a "virtual sequence", and one launch of each kernel serves them all.
+//
+// Kernel 0 (absorb): q~ for every (virtual sequence, head) into the workspace, fp32.
+// Kernel 1 (split): a persistent grid of at most one CTA per SM, launched with
 //   programmatic dependent launch so it starts streaming while kernel 0 runs.
-//   The cached tokens of all sequences are cut into 8-token granules and divided
-//   evenly into at most one contiguous range ("split") per CTA.  Each granule's
-//   s^K, s^V (TMA tensor loads, 128-byte swizzle) and z^K, z^V (bulk copies) go
-//   into a ring of shared-memory stages, read from HBM once for all H heads.
-//   Consumer warps own 16 heads each; NG groups of ceil(H/16) warps take stages
-//   round-robin with their own online-softmax state, merged inside the CTA at
-//   the end of the split into one partial (m, l, acc_s[d_h], acc_z[r]) per head.
+//   The cached tokens of all virtual sequences are cut into 8-token granules; the
+//   granules, concatenated, are divided into equal contiguous ranges (one per SM
+//   unless the caller sets the count), each covering pieces ("segments") of one or
+//   more consecutive sequences.  Each granule's s^K, s^V (TMA tensor loads, 128-byte
+//   swizzle) and z^K, z^V (bulk copies) go into a ring of shared-memory stages, read
+//   from HBM once for all H heads.  Consumer warps own 16 heads each; NG groups of
+//   ceil(H/16) warps take stages round-robin with their own online-softmax state,
+//   merged inside the CTA at the end of each segment into one partial
+//   (m, l, acc_s[d_h], acc_z[r]) per head.
 //     - q . s^K and p . s^V run on the tensor cores (mma.sync m16n8k16 / m16n8k8,
 //       heads on M, tokens on N / K) -- s is shared by all heads of the CTA;
 //     - q~ . z^K and p . z^V run on CUDA cores in fp32 (each z element is used
 //       once; nothing for a tensor core to reuse).
-// Kernel 2 (combine): log-sum-exp merge of each (b, h)'s partials, the residual
+// Kernel 2 (combine): log-sum-exp merge of each (sequence, head)'s partials, the residual
 //   up-projection B_h^V acc_z, the bf16 store (also a dependent launch).
 #include "kernels.h"
 #include "lrkv_internal.cuh"
@@ -32,77 +38,250 @@ namespace lrkv {
 
 constexpr int kGran = 8;                              // tokens per pipeline stage (granule)
 constexpr int kScratchFloats = 16 * 8 + 16 * 8 + 16;  // per consumer warp: z-scores, p, alpha
-constexpr int kPageCache = 64;                        // page ids of a split kept in shared memory
+constexpr int kPageCache = 64;                        // page ids of a segment kept in shared memory
 
-struct Split {
-    int b, g0, g1;
+constexpr int kSeqCache = 128;                        // sequence lengths kept in shared memory
+
+// The work of a decode call: nvb = layers * B virtual sequences vb = layer * B + b (all
+// layers share the block table and lengths), each cut into 8-token granules, T granules in
+// all, scanned by `nranges` CTA-sized pieces of work.  Two ways to cut, chosen identically by
+// both kernels (plan()):
+//  - pieces: every sequence is cut into ceil(gr / chunk) near-equal pieces, with the smallest
+//    chunk for which all pieces number at most nranges; each piece is one segment with its
+//    own partial slot (the piece's global index).  No CTA crosses a sequence boundary, so no
+//    pipeline drains between sequences; used when the largest piece costs at most a pipeline
+//    drain-and-refill (`bubble` granules) more than an exact split would.
+//  - ranges: the granules of all virtual sequences, concatenated in vb order, are divided
+//    into nranges contiguous ranges of equal size (+-1): range c is [c T / nranges,
+//    (c + 1) T / nranges) (nranges first clamped to T, so that no range is empty).  A range
+//    covers one or more segments of consecutive sequences; the segment of sequence vb inside
+//    range c writes partial slot vb + c, so each sequence's partials sit in consecutive slots.
+//    Used when the sequences are too many or too uneven for pieces.
+// Either way the slots number at most nvb + nranges.
+struct Work {
+    const int32_t* g;  // lengths in global memory
+    const int* s;      // shared-memory copy of the first kSeqCache
+    int B, layers, cap, nranges;
+    long long Tb;      // granules of one layer (all B sequences)
+    int pieces;        // 1: pieces, 0: ranges
+    int chunk;         // pieces: largest piece, in granules
+    long long per_layer_pieces;
+
+    __device__ __forceinline__ int len(int b) const { return b < kSeqCache ? s[b] : g[b]; }
+    // Granules of sequence b, or 0 when its length is outside [1, cap].
+    __device__ __forceinline__ int gran_b(int b) const {
+        const int L = len(b);
+        return (L >= 1 && L <= cap) ? (L + kGran - 1) / kGran : 0;
+    }
+    __device__ __forceinline__ int gran(int vb) const { return gran_b(vb % B); }
+    __device__ __forceinline__ long long total() const { return Tb * layers; }
+    __device__ __forceinline__ long long range_start(int c) const { return (long long)c * total() / nranges; }
+    // Index of the range that holds granule gi (0 <= gi < total()).
+    __device__ __forceinline__ int range_of(long long gi) const {
+        const long long T = total();
+        return (int)(((gi + 1) * nranges + T - 1) / T - 1);
+    }
+    // First granule of virtual sequence vb in the concatenation.
+    __device__ __forceinline__ long long seq_start(int vb) const {
+        const int l = vb / B, b = vb - l * B;
+        long long p = Tb * l;
+        for (int bb = 0; bb < b; ++bb) p += gran_b(bb);
+        return p;
+    }
+    // The (non-empty) virtual sequence that holds granule gi, and its first granule.
+    __device__ __forceinline__ void locate(long long gi, int* vb, long long* start) const {
+        const int l = (int)(gi / Tb);
+        long long p = Tb * l;
+        int b = 0;
+        while (b < B - 1 && p + gran_b(b) <= gi) p += gran_b(b++);
+        *vb = l * B + b;
+        *start = p;
+    }
+    // Pieces of one layer's sequences with largest piece c.
+    __device__ __forceinline__ long long layer_pieces(int c) const {
+        long long n = 0;
+        for (int b = 0; b < B; ++b) n += (gran_b(b) + c - 1) / c;
+        return n;
+    }
+    // Pieces mode: first piece index of virtual sequence vb.
+    __device__ __forceinline__ long long first_piece(int vb) const {
+        const int l = vb / B, b = vb - l * B;
+        long long p = per_layer_pieces * l;
+        for (int bb = 0; bb < b; ++bb) p += (unsigned)(gran_b(bb) + chunk - 1) / (unsigned)chunk;
+        return p;
+    }
+    // Pieces mode: virtual sequence and granule range of piece pc.
+    __device__ __forceinline__ void piece(long long pc, int* vb, int* g0, int* g1) const {
+        const int l = (int)(pc / per_layer_pieces);
+        long long base = per_layer_pieces * l;
+        int b = 0;
+        for (;; ++b) {
+            const int n = (int)((unsigned)(gran_b(b) + chunk - 1) / (unsigned)chunk);
+            if (pc < base + n || b == B - 1) break;
+            base += n;
+        }
+        const int gr = gran_b(b);
+        const int np = (gr + chunk - 1) / chunk;
+        const int i = (int)(pc - base);
+        *vb = l * B + b;
+        *g0 = (int)((long long)i * gr / np);
+        *g1 = (int)((long long)(i + 1) * gr / np);
+    }
+
+    // Sum (max for gmax) over the NL lanes that share a plan (a no-op for one thread).
+    template <int NL>
+    __device__ __forceinline__ static long long lanes_sum(long long v) {
+        if (NL > 1) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        }
+        return v;
+    }
+    // Counts the granules and chooses the cut.  NL = 1: one thread alone walks every sequence
+    // (cheap for small batches, and needs no barrier when every thread does it); NL = 32: a full
+    // warp, lanes taking every 32nd sequence, sums exchanged by shuffles (every lane ends with
+    // the same plan; publish() then hands it to the rest of the block).
+    template <int NL>
+    __device__ __forceinline__ void plan(int bubble, int lane) {
+        // (per-sequence counts and piece sizes are 32-bit -- a 64-bit division is a long
+        // software sequence on the GPU; only the sums are 64-bit)
+        long long tb = 0, nonempty = 0;
+        int gmax = 0;
+        for (int b = lane; b < B; b += NL) {
+            const int gr = gran_b(b);
+            tb += gr;
+            nonempty += gr > 0;
+            gmax = max(gmax, gr);
+        }
+        tb = lanes_sum<NL>(tb);
+        nonempty = lanes_sum<NL>(nonempty);
+        if (NL > 1) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) gmax = max(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+        }
+        Tb = tb;
+        const long long T = total();
+        if (T < nranges) nranges = (int)T;  // no empty range
+        pieces = 0;
+        const long long occupied = nonempty * layers;
+        if (T == 0 || occupied > nranges) return;
+        // Smallest chunk c with layers * sum_b ceil(gr_b / c) <= nranges.  The count falls as c
+        // grows; c0 = ceil(T / (nranges - occupied)) already fits (sum ceil(gr / c0) <=
+        // T / c0 + occupied), so the search runs between the exact share and c0.
+        const long long share = (T + nranges - 1) / nranges;
+        const long long c0 = occupied < nranges ? (T + (nranges - occupied) - 1) / (nranges - occupied) : gmax;
+        const int hi0 = (int)min(c0, (long long)gmax);
+        int lo = (int)min(share, (long long)hi0), hi = hi0;
+        while (lo < hi) {
+            const int mid = lo + (hi - lo) / 2;
+            long long n = 0;
+            for (int b = lane; b < B; b += NL) n += (unsigned)(gran_b(b) + mid - 1) / (unsigned)mid;
+            n = lanes_sum<NL>(n);
+            if (n * layers <= nranges)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        if (lo <= share + bubble) {
+            long long n = 0;
+            for (int b = lane; b < B; b += NL) n += (unsigned)(gran_b(b) + lo - 1) / (unsigned)lo;
+            pieces = 1;
+            chunk = lo;
+            per_layer_pieces = lanes_sum<NL>(n);
+        }
+    }
+    // Number of pieces of work (CTA iterations) of the call.
+    __device__ __forceinline__ long long work_items() const {
+        return pieces ? per_layer_pieces * layers : nranges;
+    }
 };
 
-constexpr int kSeqCache = 256;                        // sequence lengths kept in shared memory
+// This CTA's walk over its segments: (virtual sequence, granule range in it, partial slot).
+struct SegWalk {
+    long long item;            // current piece or range
+    long long gcur, gend, vstart;
+    long long seg_start;       // ranges: first granule (in the concatenation) of the last segment returned
+    int vb;
 
-// Sequence lengths, read from a shared-memory copy for the first kSeqCache
-// sequences (the partition below walks them several times per CTA).
-struct SeqLens {
-    const int32_t* g;
-    const int* s;
-    __device__ __forceinline__ int operator[](int b) const { return b < kSeqCache ? s[b] : g[b]; }
+    __device__ __forceinline__ void start(int first_item) {
+        item = first_item;
+        gcur = gend = 0;
+        vb = 0;
+        vstart = 0;
+    }
+    __device__ __forceinline__ bool next(const Work& w, int* vb_out, int* g0, int* g1, int* slot) {
+        if (w.pieces) {
+            if (item >= w.work_items()) return false;
+            w.piece(item, vb_out, g0, g1);
+            *slot = (int)item;
+            item += gridDim.x;
+            return true;
+        }
+        const int nvb = w.layers * w.B;
+        if (gcur >= gend) {
+            if (gend > 0) item += gridDim.x;  // the current range is done
+            if (item >= w.nranges) return false;
+            gcur = w.range_start((int)item);
+            gend = w.range_start((int)item + 1);
+            w.locate(gcur, &vb, &vstart);
+        }
+        const int gr = w.gran(vb);
+        const long long se = min(gend, vstart + gr);
+        *vb_out = vb;
+        *g0 = (int)(gcur - vstart);
+        *g1 = (int)(se - vstart);
+        *slot = vb + (int)item;
+        seg_start = gcur;
+        gcur = se;
+        if (gcur == vstart + gr) {
+            vstart += gr;
+            do {
+                ++vb;
+            } while (vb < nvb && w.gran(vb) == 0);
+        }
+        return true;
+    }
 };
+
+// The split kernel's control block in shared memory: the plan and this CTA's walk over its
+// segments, advanced by thread 0 at each segment boundary and read by all threads after a
+// barrier (kept out of the registers that the stage loop needs).
+struct SplitCtl {
+    Work wk;
+    SegWalk walk;
+    int valid, vb, g0, g1, slot;  // the segment the CTA starts next
+
+    // (thread 0) Step the walk to the next segment; a sequence's first segment records where
+    // its partials are for the combine kernel.
+    __device__ __forceinline__ void advance(int2* seg_table) {
+        valid = walk.next(wk, &vb, &g0, &g1, &slot);
+        if (valid && g0 == 0) {
+            const int gr = wk.gran(vb);
+            int np;
+            if (wk.pieces)
+                np = (int)((unsigned)(gr + wk.chunk - 1) / (unsigned)wk.chunk);
+            else
+                np = wk.range_of(walk.seg_start + gr - 1) - (slot - vb) + 1;
+            seg_table[vb] = make_int2(slot, np);
+        }
+    }
+};
+constexpr int kCtlBytes = 256;
+static_assert(sizeof(SplitCtl) <= kCtlBytes, "control block");
+constexpr int kPlanAlone = 32;  // batches up to this size are planned by one thread
 
 // Cooperative copy of the first kSeqCache lengths (caller synchronises afterwards).
 __device__ __forceinline__ void stage_seq_lens(int* dst, const int32_t* src, int B, int tid, int nthreads) {
     for (int b = tid; b < B && b < kSeqCache; b += nthreads) dst[b] = src[b];
 }
 
-// Granules of sequence b, or 0 when its length is outside [1, cap].
-__device__ __forceinline__ int seq_granules(const SeqLens& sl, int b, int cap) {
-    const int L = sl[b];
-    return (L >= 1 && L <= cap) ? (L + kGran - 1) / kGran : 0;
-}
-
-// Even division of all granules into at most max(G, B) splits: chunk is chosen
-// so that sum_b ceil(gr_b / chunk) <= G whenever G > B; sequence b is then cut
-// into ns_b = ceil(gr_b / chunk) near-equal pieces.
-__device__ __forceinline__ int partition_chunk(const SeqLens& sl, int B, int cap, int G, int* nsplits) {
-    long long total = 0;
-    for (int b = 0; b < B; ++b) total += seq_granules(sl, b, cap);
-    const int denom = G > B ? G - B : 1;
-    const int chunk = (int)max(1LL, (total + denom - 1) / denom);
-    int ns = 0;
-    for (int b = 0; b < B; ++b) ns += (seq_granules(sl, b, cap) + chunk - 1) / chunk;
-    *nsplits = ns;
-    return chunk;
-}
-
-__device__ __forceinline__ Split split_info(const SeqLens& sl, int B, int cap, int chunk, int s) {
-    int base = 0;
-    for (int b = 0; b < B; ++b) {
-        const int gr = seq_granules(sl, b, cap);
-        const int ns = (gr + chunk - 1) / chunk;
-        if (s < base + ns) {
-            const int i = s - base;
-            return Split{b, (int)((long long)i * gr / ns), (int)((long long)(i + 1) * gr / ns)};
-        }
-        base += ns;
-    }
-    return Split{0, 0, 0};
-}
-
-// First split index and split count of sequence b.
-__device__ __forceinline__ void seq_splits(const SeqLens& sl, int B, int cap, int chunk, int b, int* first,
-                                           int* count) {
-    int base = 0;
-    for (int bb = 0; bb < b; ++bb) base += (seq_granules(sl, bb, cap) + chunk - 1) / chunk;
-    *first = base;
-    *count = (seq_granules(sl, b, cap) + chunk - 1) / chunk;
-}
-
 // Bounded wait until a slot's stage tag equals `want` (sets LRKV_DEV_TIMEOUT on expiry).
-__device__ __forceinline__ bool wait_tag(volatile int* tag, int want, uint32_t* status) {
+__device__ __forceinline__ bool wait_tag(volatile int* tag, int want, uint32_t* status, uint64_t limit_ns) {
     if (*tag == want) return true;
     const uint64_t t0 = globaltimer_ns();
     while (*tag != want) {
         __nanosleep(32);
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             set_status(status, LRKV_DEV_TIMEOUT);
             return false;
         }
@@ -120,7 +299,7 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------------ kernel 0
-// q~[b][h][j] = sum_d q[b][h][d] B^K[h][d][j]; one block per (head, sequence):
+// q~[vb][h][j] = sum_d q[vb][h][d] B^K[h][d][j]; one block per (head, virtual sequence):
 // 256 / R slices of the d range are summed in parallel, then reduced in
 // shared memory, so all of B_h^K (d_h x r) is in flight at once.
 template <int D_H, int R, int D_R>
@@ -129,11 +308,12 @@ __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) 
     constexpr int NS = 256 / R;           // d slices
     constexpr int DS = D_H / NS;          // d values per slice (>= 2)
     static_assert(DS >= 1 && D_H % NS == 0, "slices");
-    const int h = blockIdx.x, b = blockIdx.y;
+    const int h = blockIdx.x, vb = blockIdx.y;
+    const int l = vb / a.B, b = vb - l * a.B;
     const int j = threadIdx.x % R, sl = threadIdx.x / R;
     __shared__ float part[NS][R];
-    const uint16_t* qrow = a.q + ((size_t)b * a.H + h) * (D_H + D_R) + sl * DS;
-    const uint16_t* bk = a.BK + ((size_t)h * D_H + sl * DS) * R + j;
+    const uint16_t* qrow = a.q + l * a.ls_q + ((size_t)b * a.H + h) * (D_H + D_R) + sl * DS;
+    const uint16_t* bk = a.BK + l * a.ls_BK + ((size_t)h * D_H + sl * DS) * R + j;
     float acc = 0.f;
 #pragma unroll
     for (int dd = 0; dd < DS; ++dd)
@@ -144,16 +324,16 @@ __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) 
         float v = 0.f;
 #pragma unroll
         for (int i = 0; i < NS; ++i) v += part[i][threadIdx.x];
-        a.qt[((size_t)b * a.H + h) * R + threadIdx.x] = v;
+        a.qt[((size_t)vb * a.H + h) * R + threadIdx.x] = v;
     }
 }
 
-// Issue the loads of one 8-token granule (stage) of block `blk` into a ring slot:
+// Issue the loads of one 8-token granule (stage) of block `blk` of layer `l` into a ring slot:
 // s^K (with k^R when D_R > 0), s^V by TMA tensor copies (128-byte swizzle), z^K, z^V by
 // bulk copies.  An out-of-range block id is reported and the stage is marked empty.
 template <int D_H, int R, int D_R>
 __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUtensorMap* tm_sV, const DecodeArgs& a,
-                                            uint32_t st, uint32_t bar, int* meta_slot, int blk, int gi,
+                                            uint32_t st, uint32_t bar, int* meta_slot, int l, int blk, int gi,
                                             uint64_t pol) {
     if (blk < 0 || blk >= a.num_blocks) {
         set_status(a.status, LRKV_DEV_BAD_BLOCK);
@@ -166,18 +346,18 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUte
     mbar_arrive_expect_tx(bar, 16u * (D_K + D_H) + 32u * a.H * R);
     const int row = blk * kBlockSize + ((gi & 7) << 3);
 #pragma unroll
-    for (int i = 0; i < D_K / 64; ++i) tma_load_2d_hint(st + i * 1024, tm_sK, i * 64, row, bar, pol);
+    for (int i = 0; i < D_K / 64; ++i) tma_load_3d_hint(st + i * 1024, tm_sK, i * 64, row, l, bar, pol);
 #pragma unroll
-    for (int i = 0; i < D_H / 64; ++i) tma_load_2d_hint(st + 16 * D_K + i * 1024, tm_sV, i * 64, row, bar, pol);
+    for (int i = 0; i < D_H / 64; ++i) tma_load_3d_hint(st + 16 * D_K + i * 1024, tm_sV, i * 64, row, l, bar, pol);
     const size_t zoff = (size_t)row * a.H * R;
-    bulk_load_hint(st + 16 * (D_K + D_H), a.zK + zoff, 16u * a.H * R, bar, pol);
-    bulk_load_hint(st + 16 * (D_K + D_H) + 16 * a.H * R, a.zV + zoff, 16u * a.H * R, bar, pol);
+    bulk_load_hint(st + 16 * (D_K + D_H), a.zK + l * a.ls_zK + zoff, 16u * a.H * R, bar, pol);
+    bulk_load_hint(st + 16 * (D_K + D_H) + 16 * a.H * R, a.zV + l * a.ls_zV + zoff, 16u * a.H * R, bar, pol);
 }
 
 // ------------------------------------------------------------------ kernel 1
 // At most 8 warps per CTA (one per head tile and group), so each thread may
 // hold up to 255 registers.  There is no dedicated producer warp: thread 0
-// fills the ring at the start of each split, and afterwards the last warp to
+// fills the ring at the start of each segment, and afterwards the last warp to
 // release a stage refills that slot with the stage nslot positions ahead.
 template <int D_H, int R, int D_R>
 __global__ void __launch_bounds__(256, 1)
@@ -212,6 +392,7 @@ __global__ void __launch_bounds__(256, 1)
     int* slc = pages + kPageCache;                               // first kSeqCache sequence lengths
     float* scratch = reinterpret_cast<float*>(slc + kSeqCache);
     volatile int* abort_flag = reinterpret_cast<int*>(scratch + NCW * kScratchFloats);
+    SplitCtl* ctl = reinterpret_cast<SplitCtl*>((reinterpret_cast<uintptr_t>(abort_flag) + 16) & ~(uintptr_t)15);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nslot; ++s) {
@@ -226,10 +407,18 @@ __global__ void __launch_bounds__(256, 1)
     stage_seq_lens(slc, a.seq_lens, a.B, threadIdx.x, blockDim.x);
     __syncthreads();
 
-    const SeqLens seql{a.seq_lens, slc};
-    const int cap = a.max_pages * kBlockSize;
-    int nsplits;
-    const int chunk = partition_chunk(seql, a.B, cap, gridDim.x, &nsplits);
+    if (warp == 0) {
+        Work w{a.seq_lens, slc, a.B, a.layers, a.max_pages * kBlockSize, a.nranges, 0, 0, 1, 0};
+        if (a.B > kPlanAlone)
+            w.plan<32>(a.bubble, lane);
+        else if (lane == 0)
+            w.plan<1>(a.bubble, 0);
+        if (lane == 0) {
+            ctl->wk = w;
+            ctl->walk.start(blockIdx.x);
+            ctl->advance(a.seg_table);
+        }
+    }
     const uint64_t pol = policy_evict_first();
 
     const int grp = warp / HT, ht = warp % HT;
@@ -246,30 +435,39 @@ __global__ void __launch_bounds__(256, 1)
     const int hA = h0 + g, hB = h0 + g + 8;
     bool qt_ready = false;
 
-    int kbase = 0;  // stages consumed by this CTA before the current split (ring position and phase)
-    for (int s = blockIdx.x; s < nsplits; s += gridDim.x) {
-        const Split sp = split_info(seql, a.B, cap, chunk, s);
-        const int b = sp.b;
-        const int L = seql[b];
-        const int nst = sp.g1 - sp.g0;
-        const int pg0 = sp.g0 >> 3;
-        const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
-
-        // Once every warp is here the previous split is fully consumed and merged:
+    int kbase = 0;  // stages consumed by this CTA before the current segment (ring position and phase)
+    for (;;) {
+        // Once every warp is here the previous segment is fully consumed and merged:
         // no copy is in flight and the ring memory is free.
+        // (the descriptor of this segment was stepped to by thread 0 during the previous one)
         named_bar(1, nct);
+        if (!ctl->valid) break;
+        const int vb = ctl->vb, sg0 = ctl->g0, sg1 = ctl->g1, pslot = ctl->slot;
+        const int l = vb / a.B, bb = vb - (vb / a.B) * a.B;
+        const int L = bb < kSeqCache ? slc[bb] : a.seq_lens[bb];
+        const int nst = sg1 - sg0;
+        const int pg0 = sg0 >> 3;
+        const int32_t* bt_row = a.block_table + (size_t)bb * a.max_pages;
+
         for (int i = threadIdx.x; i < kPageCache && pg0 + i < a.max_pages; i += nct) pages[i] = bt_row[pg0 + i];
         fence_proxy_async_smem();  // generic accesses of the ring (merge) before async-proxy refills
         named_bar(1, nct);
-        if (threadIdx.x == 0 && !*abort_flag) {
-            for (int k = 0; k < min(nslot, nst); ++k) {
-                const int slot = (kbase + k) % nslot;
-                const int pi = ((sp.g0 + k) >> 3) - pg0;
-                tag[slot] = kbase + k;
-                issue_stage<D_H, R, D_R>(&tm_sK, &tm_sV, a, smem_s + slot * stage_bytes, smem_u32(&full[slot]),
-                                    &meta[slot], pi < kPageCache ? pages[pi] : bt_row[pg0 + pi], sp.g0 + k, pol);
-                ++nissued[slot];
+        if (threadIdx.x == 0) {
+            if (!*abort_flag) {
+                for (int k = 0; k < min(nslot, nst); ++k) {
+                    const int slot = (kbase + k) % nslot;
+                    const int pi = ((sg0 + k) >> 3) - pg0;
+                    tag[slot] = kbase + k;
+                    issue_stage<D_H, R, D_R>(&tm_sK, &tm_sV, a, smem_s + slot * stage_bytes, smem_u32(&full[slot]),
+                                             &meta[slot], l, pi < kPageCache ? pages[pi] : bt_row[pg0 + pi],
+                                             sg0 + k, pol);
+                    ++nissued[slot];
+                }
             }
+            // every thread has read this segment's descriptor (before the barrier above):
+            // step to the next one while this one streams (after an expired wait too, so
+            // that the walk ends)
+            ctl->advance(a.seg_table);
         }
         if (!qt_ready) {
             pdl_wait();  // q~ written by the absorb kernel
@@ -280,7 +478,8 @@ __global__ void __launch_bounds__(256, 1)
         // absorb kernel's fp32 output, or as bf16 straight from the caller (absorbed weights).
         float qt[R];
         if (a.qt_in) {
-            const uint4* qrow = reinterpret_cast<const uint4*>(a.qt_in + ((size_t)b * H + (hz_ok ? hzh : 0)) * R);
+            const uint4* qrow = reinterpret_cast<const uint4*>(a.qt_in + l * a.ls_qt +
+                                                                 ((size_t)bb * H + (hz_ok ? hzh : 0)) * R);
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) {
                 const uint4 x = qrow[(cc + rot) % NC];
@@ -294,7 +493,7 @@ __global__ void __launch_bounds__(256, 1)
                 qt[cc * 8 + 7] = hz_ok ? bf16hi(x.w) : 0.f;
             }
         } else {
-            const float* qrow = a.qt + ((size_t)b * H + (hz_ok ? hzh : 0)) * R;
+            const float* qrow = a.qt + ((size_t)vb * H + (hz_ok ? hzh : 0)) * R;
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) {
                 const float4* src = reinterpret_cast<const float4*>(qrow + ((cc + rot) % NC) * 8);
@@ -313,8 +512,9 @@ __global__ void __launch_bounds__(256, 1)
         // Query A fragments (heads on M): rows hA, hB; k = key feature ([q | q^R]).
         uint32_t qa[D_K / 16][4];
         {
-            const uint32_t* qA = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * H + hA) * D_K);
-            const uint32_t* qB = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * H + hB) * D_K);
+            const uint16_t* qbase = a.q + l * a.ls_q;
+            const uint32_t* qA = reinterpret_cast<const uint32_t*>(qbase + ((size_t)bb * H + hA) * D_K);
+            const uint32_t* qB = reinterpret_cast<const uint32_t*>(qbase + ((size_t)bb * H + hB) * D_K);
 #pragma unroll
             for (int kk = 0; kk < D_K / 16; ++kk) {
                 qa[kk][0] = hA < H ? qA[kk * 8 + tq] : 0u;
@@ -343,13 +543,13 @@ __global__ void __launch_bounds__(256, 1)
             // Groups run at different speeds, so the slot may still hold a stage one or
             // more ring rounds older than kk; its barrier parity alone cannot tell them
             // apart.  Wait until stage kk has been issued into the slot, then for its data.
-            const bool ready = wait_tag(tag + slot, kk, a.status) &&
-                               mbar_wait(smem_u32(&full[slot]), (kk / nslot) & 1, a.status);
+            const bool ready = wait_tag(tag + slot, kk, a.status, a.wait_ns) &&
+                               mbar_wait_for(smem_u32(&full[slot]), (kk / nslot) & 1, a.status, a.wait_ns);
             if (!__all_sync(0xffffffffu, ready)) {
                 *abort_flag = 1;
                 continue;
             }
-            const int t0 = (sp.g0 + j) * kGran;
+            const int t0 = (sg0 + j) * kGran;
             const int nvalid = meta[slot] ? min(kGran, L - t0) : 0;
             const uint32_t st = smem_s + slot * stage_bytes;
             const uint32_t sK_s = st, sV_s = st + 16 * D_K;
@@ -477,17 +677,17 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             if (lane == 0) {
                 // Release; the last of the HT warps reading this stage refills the slot
-                // with the stage nslot positions ahead in this split.
+                // with the stage nslot positions ahead in this segment.
                 __threadfence_block();
                 if (atomicAdd(&rel[slot], 1) == HT - 1) {
                     rel[slot] = 0;
                     __threadfence_block();
                     const int jn = j + nslot;
                     if (jn < nst && !*abort_flag) {
-                        const int pi = ((sp.g0 + jn) >> 3) - pg0;
+                        const int pi = ((sg0 + jn) >> 3) - pg0;
                         tag[slot] = kk + nslot;
-                        issue_stage<D_H, R, D_R>(&tm_sK, &tm_sV, a, st, smem_u32(&full[slot]), &meta[slot],
-                                            pi < kPageCache ? pages[pi] : bt_row[pg0 + pi], sp.g0 + jn, pol);
+                        issue_stage<D_H, R, D_R>(&tm_sK, &tm_sV, a, st, smem_u32(&full[slot]), &meta[slot], l,
+                                                 pi < kPageCache ? pages[pi] : bt_row[pg0 + pi], sg0 + jn, pol);
                         ++nissued[slot];
                     }
                 }
@@ -505,14 +705,14 @@ __global__ void __launch_bounds__(256, 1)
 
         // Groups write their state into the idle ring (or straight to the workspace
         // when there is one group), then all consumers merge it per head.
-        named_bar(1, nct);  // every stage of this split consumed: the ring is idle
+        named_bar(1, nct);  // every stage of this segment consumed: the ring is idle
         const bool direct = (a.ng == 1);
-        // Workspace partials are laid out [head][split][...] so that the combine reads
+        // Workspace partials are laid out [head][slot][...] so that the combine reads
         // one head's partials contiguously; the shared-memory staging is [group][head].
         const size_t hs_ml = direct ? (size_t)a.pmax * 2 : 2;     // stride between heads
         const size_t hs_acc = direct ? (size_t)a.pmax * W : W;
-        float* gml = direct ? a.part_ml + (size_t)s * 2 : reinterpret_cast<float*>(smem) + (size_t)grp * H * 2;
-        float* gacc = direct ? a.part_acc + (size_t)s * W
+        float* gml = direct ? a.part_ml + (size_t)pslot * 2 : reinterpret_cast<float*>(smem) + (size_t)grp * H * 2;
+        float* gacc = direct ? a.part_acc + (size_t)pslot * W
                              : reinterpret_cast<float*>(smem) + (size_t)a.ng * H * 2 + (size_t)grp * H * W;
         if (tq == 0) {
             if (hA < H) *reinterpret_cast<float2*>(gml + hA * hs_ml) = make_float2(m0, l0);
@@ -537,8 +737,8 @@ __global__ void __launch_bounds__(256, 1)
             named_bar(1, nct);
             const float* sml = reinterpret_cast<const float*>(smem);
             const float* sacc = sml + (size_t)a.ng * H * 2;
-            float* pml = a.part_ml + (size_t)s * 2;
-            float* pacc = a.part_acc + (size_t)s * W;
+            float* pml = a.part_ml + (size_t)pslot * 2;
+            float* pacc = a.part_acc + (size_t)pslot * W;
             for (int h = threadIdx.x; h < H; h += nct) {
                 float M = -INFINITY, Ls = 0.f;
                 for (int gg = 0; gg < a.ng; ++gg) M = fmaxf(M, sml[(gg * H + h) * 2]);
@@ -564,7 +764,8 @@ __global__ void __launch_bounds__(256, 1)
     // The combine kernel may now be scheduled; it waits for this grid to finish.
     pdl_trigger();
     // After an expired wait, make sure no copy is still landing in shared memory
-    // before the CTA exits: wait (bounded) for the last phase issued into each slot.
+    // before the CTA exits: wait (bounded, always with the full limit) for the last
+    // phase issued into each slot.
     named_bar(1, nct);
     if (threadIdx.x == 0 && *abort_flag)
         for (int sl = 0; sl < nslot; ++sl)
@@ -573,48 +774,43 @@ __global__ void __launch_bounds__(256, 1)
 
 // ------------------------------------------------------------------ kernel 2
 // Log-sum-exp merge of a sequence's partials, residual up-projection, bf16 store.
-// grid (H, B), blockDim = NSL partial slices x W columns, NSL <= 1024 / W chosen on the
-// host so that the grid is about one wave (many (head, sequence) pairs get small
+// grid (H, layers * B), blockDim = NSL partial slices x W columns, NSL <= 1024 / W chosen
+// on the host so that the grid is about one wave (many (head, sequence) pairs get small
 // blocks, several per SM; few pairs get many slices each).  Each slice merges
 // its own partials (all loads issued together), then the slices are merged in
 // shared memory; the B_h^V row of each output column is prefetched up front.
 template <int D_H, int R>
-__global__ void __launch_bounds__(1024) decode_combine_kernel(const DecodeArgs a, int G) {
+__global__ void __launch_bounds__(1024) decode_combine_kernel(const DecodeArgs a) {
     constexpr int W = D_H + R;
     constexpr int NSL_MAX = 1024 / W;  // slices at most
     constexpr int PPS = 8;             // partials a slice loads per round
     const int NSL = blockDim.x / W;    // slices of this launch
-    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    const int h = blockIdx.x, vb = blockIdx.y, tid = threadIdx.x;
+    const int ly = vb / a.B, bb = vb - (vb / a.B) * a.B;
     const int H = a.H;
-    const int cap = a.max_pages * kBlockSize;
     __shared__ float sm_m[NSL_MAX], sm_l[NSL_MAX];
     __shared__ float sm_acc[NSL_MAX][W];
-    __shared__ int slc[kSeqCache];
     const int sl = tid / W, c = tid - (tid / W) * W;
 
     // B_h^V row of output column c (prefetched while the partials are loaded)
     uint4 bvr[R / 8];
     if (tid < D_H && !a.fused_out) {  // (no B^V in the fused form)
-        const uint4* bv = reinterpret_cast<const uint4*>(a.BV + ((size_t)h * D_H + tid) * R);
+        const uint4* bv = reinterpret_cast<const uint4*>(a.BV + ly * a.ls_BV + ((size_t)h * D_H + tid) * R);
 #pragma unroll
         for (int i = 0; i < R / 8; ++i) bvr[i] = __ldg(bv + i);
     }
-    stage_seq_lens(slc, a.seq_lens, a.B, tid, blockDim.x);
-    __syncthreads();
-    const SeqLens seql{a.seq_lens, slc};
+    const int L = a.seq_lens[bb];
     pdl_wait();
     const int OW = a.fused_out ? W : D_H;  // output row width
-    uint16_t* dst = a.out + ((size_t)b * H + h) * OW;
-    const int L = seql[b];
-    if (L < 1 || L > cap) {
+    uint16_t* dst = a.out + ly * a.ls_out + ((size_t)bb * H + h) * OW;
+    if (L < 1 || L > a.max_pages * kBlockSize) {
         if (tid == 0 && h == 0) set_status(a.status, LRKV_DEV_BAD_SEQLEN);
         if (tid < OW) dst[tid] = 0;
         return;
     }
-    int nsplits;
-    const int chunk = partition_chunk(seql, a.B, cap, G, &nsplits);
-    int first, np;
-    seq_splits(seql, a.B, cap, chunk, b, &first, &np);
+    // partial slots first .. first + np - 1, recorded by the split kernel
+    const int2 fe = a.seg_table[vb];
+    const int first = fe.x, np = fe.y;
     const float* pml = a.part_ml + ((size_t)h * a.pmax + first) * 2;
     const float* pacc = a.part_acc + ((size_t)h * a.pmax + first) * W;
 
@@ -698,7 +894,7 @@ struct DecodePlan {
 
 static int decode_fixed_smem(int ncw, int nslot) {
     return nslot * 8 + ((4 * nslot + 3) & ~3) * 4 + (kPageCache + kSeqCache) * 4 + ncw * kScratchFloats * 4 + 16 +
-           1024;
+           kCtlBytes + 1024;  // (the abort flag; the control block; alignment of the ring)
 }
 
 DecodePlan decode_plan(int H, int D_H, int R, int D_R, int smem_limit) {
@@ -719,22 +915,23 @@ DecodePlan decode_plan(int H, int D_H, int R, int D_R, int smem_limit) {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-size_t decode_workspace_bytes(int H, int D_H, int R, int B, int G, int smem_limit) {
-    (void)smem_limit;
-    const size_t pmax = (size_t)max(G, B);
+size_t decode_workspace_bytes(int H, int D_H, int R, int nvb, int nranges) {
+    const size_t pmax = (size_t)nvb + (size_t)nranges;
     return align256(pmax * H * 2 * sizeof(float)) + align256(pmax * H * (D_H + R) * sizeof(float)) +
-           align256((size_t)B * H * R * sizeof(float));
+           align256((size_t)nvb * H * R * sizeof(float)) + align256((size_t)nvb * sizeof(int2));
 }
 
-void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int B, int G, int smem_limit) {
-    (void)smem_limit;
-    const size_t pmax = (size_t)max(G, B);
+void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int nvb, int nranges) {
+    const size_t pmax = (size_t)nvb + (size_t)nranges;
     uint8_t* base = static_cast<uint8_t*>(ws);
     a->part_ml = reinterpret_cast<float*>(base);
     base += align256(pmax * H * 2 * sizeof(float));
     a->part_acc = reinterpret_cast<float*>(base);
     base += align256(pmax * H * (D_H + R) * sizeof(float));
     a->qt = reinterpret_cast<float*>(base);
+    base += align256((size_t)nvb * H * R * sizeof(float));
+    a->seg_table = reinterpret_cast<int2*>(base);
+    a->pmax = (int)pmax;
 }
 
 template <typename... Args>
@@ -755,41 +952,45 @@ static cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size
 
 template <int D_H, int R, int D_R>
 static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, const DecodePlan& p,
-                                   int G, cudaStream_t stream) {
+                                   int sms, cudaStream_t stream) {
     auto split = decode_split_kernel<D_H, R, D_R>;
     cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
+    const int nvb = a.layers * a.B;
+    const int grid = a.nranges < sms ? a.nranges : sms;
     if (a.qt_in) {
         // q~ comes from the caller: no absorb kernel, and the split is an ordinary launch --
         // a dependent launch could start streaming the cache before the caller's previous
         // kernel on this stream (an append of the newest rows) has finished.
-        split<<<G, p.threads, p.smem_bytes, stream>>>(tK, tV, a);
+        split<<<grid, p.threads, p.smem_bytes, stream>>>(tK, tV, a);
         e = cudaGetLastError();
     } else {
-        decode_absorb_kernel<D_H, R, D_R><<<dim3(a.H, a.B), 256, 0, stream>>>(a);
+        decode_absorb_kernel<D_H, R, D_R><<<dim3(a.H, nvb), 256, 0, stream>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        e = launch_pdl(split, dim3(G), dim3(p.threads), p.smem_bytes, stream, tK, tV, a);
+        e = launch_pdl(split, dim3(grid), dim3(p.threads), p.smem_bytes, stream, tK, tV, a);
     }
     if (e != cudaSuccess) return e;
     // Slices per (head, sequence): enough threads for about one wave of the GPU in total.
     constexpr int W = D_H + R;
-    const long long pairs = (long long)a.H * a.B;
-    const int nsl = (int)max(1LL, min((long long)(1024 / W), ((long long)G * 1024) / max(1LL, pairs * W)));
-    return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, a.B), dim3(nsl * W), 0, stream, a, G);
+    const long long pairs = (long long)a.H * nvb;
+    const int nsl = (int)max(1LL, min((long long)(1024 / W), ((long long)sms * 1024) / max(1LL, pairs * W)));
+    return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, nvb), dim3(nsl * W), 0, stream, a);
 }
 
 cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int D_R,
-                          int G, int smem_limit, cudaStream_t stream) {
+                          int sms, int smem_limit, cudaStream_t stream) {
     const DecodePlan p = decode_plan(a.H, D_H, R, D_R, smem_limit);
     a.ng = p.ng;
     a.nslot = p.nslot;
     a.stage_bytes = p.stage_bytes;
-    a.pmax = max(G, a.B);
+    // a pipeline drain and refill at a sequence boundary costs about as long as streaming
+    // 128 KB through one SM (~3 us)
+    a.bubble = ((128 << 10) + p.stage_bytes - 1) / p.stage_bytes;
 #define LRKV_DEC(DH, RR)                                                                     \
     if (D_H == DH && R == RR)                                                                \
-        return D_R == 0 ? launch_decode_t<DH, RR, 0>(tK, tV, a, p, G, stream)                \
-                        : launch_decode_t<DH, RR, 64>(tK, tV, a, p, G, stream);
+        return D_R == 0 ? launch_decode_t<DH, RR, 0>(tK, tV, a, p, sms, stream)              \
+                        : launch_decode_t<DH, RR, 64>(tK, tV, a, p, sms, stream);
     LRKV_DEC(64, 8) LRKV_DEC(64, 16) LRKV_DEC(64, 32) LRKV_DEC(128, 8) LRKV_DEC(128, 16) LRKV_DEC(128, 32)
 #undef LRKV_DEC
     return cudaErrorInvalidValue;

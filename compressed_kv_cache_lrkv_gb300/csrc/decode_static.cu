@@ -11,7 +11,11 @@
 //
 // The array's name seen from host code is only a host-side stand-in, never a
 // device address, so its device address is looked up with cudaGetSymbolAddress
-// once per device (with that device current) and cached.
+// (with the device current) and cached per device together with the id of the
+// context it was found in: a context that is destroyed and created again (e.g.
+// after cudaDeviceReset) loads the module afresh, and the address is looked up again.
+#include <cudaTypedefs.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -28,6 +32,28 @@ static __device__ __align__(256) unsigned char g_decode_scratch[LRKV_STATIC_WS_B
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
+
+// Id of the calling thread's current context (0 if the driver cannot tell).
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_cur && get_id && get_cur(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS) return id;
+    return 0;
+}
 
 }  // namespace
 
@@ -49,8 +75,11 @@ extern "C" lrkv_status lrkv_decode_static_ws(const lrkv_dims* dims, const void* 
         return lrkv::report_error(LRKV_ERR_CUDA, "lrkv_decode_static_ws: no usable current device");
     void* ws = nullptr;
     {
+        // (0 before the runtime has made a context current: the lookup below does that, and
+        // the id is read again after it)
+        unsigned long long ctx = current_context_id();
         std::lock_guard<std::mutex> lock(g_scratch_mu);
-        if (!g_scratch_addr[dev]) {
+        if (!g_scratch_addr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
             void* p = nullptr;
             const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
             if (e != cudaSuccess || !p) {
@@ -60,6 +89,7 @@ extern "C" lrkv_status lrkv_decode_static_ws(const lrkv_dims* dims, const void* 
                 return lrkv::report_error(LRKV_ERR_CUDA, msg);
             }
             g_scratch_addr[dev] = p;
+            g_scratch_ctx[dev] = current_context_id();
         }
         ws = g_scratch_addr[dev];
     }

@@ -19,27 +19,41 @@ struct AppendArgs {
     int d_rope;             // width of the shared positional key (0: none)
     float rope_base;
     long long nslots;       // num_blocks * block_size
+    // Several layers in one launch (blockIdx.z = layer): element strides between consecutive
+    // layers' X, W and cache pools (slots and positions are shared by the layers).
+    int layers;
+    long long ls_X, ls_W, ls_sK, ls_sV, ls_zK, ls_zV;
 };
 
+// Decode over `layers` layers of B sequences at once: virtual sequence vb = layer * B + b
+// (every layer shares the block table and the lengths); per-layer tensors are found at
+// the element strides ls_* from layer 0's (sK, sV through the layer coordinate of their
+// 3-D tensor maps).
 struct DecodeArgs {
-    const uint16_t* q;     // [B][H][D_H]
-    const uint16_t* BK;    // [H][D_H][R]
-    const uint16_t* BV;    // [H][D_H][R]
-    const uint16_t* zK;    // [nb*64][H][R]
+    const uint16_t* q;     // [B][H][D_H + D_R] per layer
+    const uint16_t* BK;    // [H][D_H][R] per layer
+    const uint16_t* BV;    // [H][D_H][R] per layer
+    const uint16_t* zK;    // [nb*64][H][R] per layer
     const uint16_t* zV;
     const int32_t* block_table;  // [B][max_pages]
     const int32_t* seq_lens;     // [B]
-    float* part_ml;   // [H][Pmax][2]  running max (log2 domain) and sum
-    float* part_acc;  // [H][Pmax][D_H + R]
-    float* qt;        // [B][H][R]  q~ = q B^K, fp32
+    float* part_ml;   // [H][pmax][2]  running max (log2 domain) and sum
+    float* part_acc;  // [H][pmax][D_H + R]
+    float* qt;        // [layers * B][H][R]  q~ = q B^K, fp32
+    int2* seg_table;  // [layers * B] first partial slot and slot count of each virtual sequence
     const uint16_t* qt_in;  // [B][H][R] bf16 q~ supplied by the caller (absorbed query weights), or null
     uint32_t* status;
-    uint16_t* out;    // [B][H][D_H], or [B][H][D_H + R] = [o_s | o_z] / l when fused_out
+    uint16_t* out;    // [B][H][D_H], or [B][H][D_H + R] = [o_s | o_z] / l when fused_out, per layer
     int fused_out;    // 1: no B^V up-projection (absorbed into the output projection)
     int B, H, max_pages, num_blocks;
+    int layers;
+    long long ls_q, ls_qt, ls_BK, ls_BV, ls_zK, ls_zV, ls_out;
+    int nranges;       // pieces of work the batch's cached tokens are cut into (CTA iterations)
+    int bubble;        // granules a pipeline drain-and-refill costs (chooses how the work is cut)
     int ng, nslot, stage_bytes;
-    int pmax;          // partial slots per head in the workspace (max(G, B))
+    int pmax;          // partial slots per head in the workspace (layers * B + nranges)
     float scale_log2;  // softmax scale * log2(e)
+    unsigned long long wait_ns;  // limit of the split kernel's pipeline waits (a debugging aid may shorten it)
 };
 
 struct PrefillArgs {
@@ -61,10 +75,13 @@ int append_tc_block_n(int N);
 cudaError_t launch_append_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const AppendArgs& a,
                              cudaStream_t stream);
 
-size_t decode_workspace_bytes(int H, int D_H, int R, int B, int G, int smem_limit);
-void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int B, int G, int smem_limit);
-cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int D_R, int G,
-                          int smem_limit, cudaStream_t stream);
+// Workspace of a decode over nvb = layers * B virtual sequences cut into `nranges` ranges.
+size_t decode_workspace_bytes(int H, int D_H, int R, int nvb, int nranges);
+void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int nvb, int nranges);
+// tK, tV: 3-D maps {d_h (+ d_rope), nb * 64, layers}, box {64, 8, 1}, 128-byte swizzle.
+// The split kernel runs on min(nranges, sms) CTAs.
+cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int D_R,
+                          int sms, int smem_limit, cudaStream_t stream);
 
 cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, int D_R, cudaStream_t stream);
 

@@ -87,6 +87,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     }
 }
 
+// mbar_wait with a caller-chosen limit.  The timer is read every 256 tries at the full limit;
+// below it, after every failed try, so that a limit of 0 gives up at the first wait that
+// does not succeed within the timer's tick.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint32_t* status, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    const uint32_t every = limit_ns < kWaitLimitNs ? 0u : 255u;
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & every) == 0 && globaltimer_ns() - t0 > limit_ns) {
+            set_status(status, LRKV_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
     asm volatile(
@@ -103,6 +119,29 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         "{%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// 3-D tile {x, y, z} (z: the outermost coordinate, e.g. a layer) with an L2 cache hint.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                                 uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Prefetch of a 3-D tile into L2 (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+// Prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Untiled bulk copy global -> shared; dst, src 16-byte aligned, bytes a multiple of 16.
@@ -298,22 +337,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Rotary encoding of one pair of the shared positional key (the columns d_h + 2i and
-// d_h + 2i + 1 of a cache row) for token position pos: the pair is turned by the angle
-// pos * base^(-2i / d_rope).  All in double: the angle is reduced to a fraction of a turn
-// (positions reach 10^5 radians) so that sine and cosine need no argument reduction
-// (sincospi), and the products are double too -- with large |x0|, |x1| cancelling to a small
-// result, fp32 would not hold one bf16 ulp.  The result is rounded to fp32 like every column.
-__device__ __forceinline__ void rope_pair(float& x0, float& x1, int i, int d_rope, int pos, float base) {
-    const double turns = (double)pos * pow((double)base, -2.0 * i / d_rope) * 0.15915494309189533577;
-    double sn, cs;
-    sincospi(2.0 * (turns - floor(turns)), &sn, &cs);
-    const double y0 = (double)x0 * cs - (double)x1 * sn;
-    const double y1 = (double)x0 * sn + (double)x1 * cs;
-    x0 = (float)y0;
-    x1 = (float)y1;
-}
 
 // One lane of a converged warp (the same lane every time for the same active set), for
 // issuing single-thread tcgen05 instructions while the whole warp keeps warp-uniform

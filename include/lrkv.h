@@ -44,7 +44,7 @@
  *     carry no positional part.  d_rope == 0 is the plain method, bit for bit.
  *
  * Supported shapes (others return LRKV_ERR_UNSUPPORTED):
- *   block_size == 64, d_h in {64, 128}, r in {8, 16, 32, 64} with r <= d_h,
+ *   block_size == 64, d_h in {64, 128}, r in {8, 16, 32} with r <= d_h,
  *   1 <= H <= 128, d a positive multiple of 8 (of 64 for the tensor-core append),
  *   d_rope in {0, 64}.
  */
@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define LRKV_ABI_VERSION 2
+#define LRKV_ABI_VERSION 3
 
 typedef enum lrkv_status {
     LRKV_OK = 0,
@@ -87,6 +87,11 @@ typedef struct lrkv_dims {
     float softmax_scale; /* logit scale; 0 means 1/sqrt(d_h + d_rope) (frame "Compute logits ...") */
     int32_t d_rope;      /* width of the decoupled positional key shared by all heads; 0 = none */
     float rope_base;     /* RoPE base; 0 means 10000 (ignored when d_rope == 0) */
+    int32_t num_splits;  /* decode only: how many equal contiguous pieces the batch's cached tokens
+                            are cut into for the split-K scan (each piece is scanned by one CTA and
+                            leaves one partial softmax state per sequence it touches); 0 = one per
+                            SM (the default), else 1..65536.  Results agree across values up to
+                            floating-point rounding. */
 } lrkv_dims;
 
 /* One layer's paged cache (device pointers, caller-owned, layout above). */
@@ -136,7 +141,8 @@ lrkv_status lrkv_append(const lrkv_dims* dims, const void* X, const void* W_catT
                         const int32_t* slot_mapping, const int32_t* positions, const lrkv_cache* cache,
                         uint32_t* status_dev, void* stream);
 
-/* Workspace bytes lrkv_decode needs for `batch` sequences on the CURRENT device. */
+/* Workspace bytes lrkv_decode needs for `batch` sequences on the CURRENT device (for
+ * lrkv_decode_layers pass num_layers * batch). */
 size_t lrkv_decode_workspace_bytes(const lrkv_dims* dims, int32_t batch);
 
 /*
@@ -194,7 +200,10 @@ lrkv_status lrkv_decode_fused(const lrkv_dims* dims, const void* q, const void* 
  *   Arguments, layouts and results are those of lrkv_decode.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept per device together with
+ *     the id of the context it was found in; after a device reset (a new context,
+ *     which loads the library's device image afresh) the next call looks it up
+ *     again, so make that call outside a stream capture too.
  *   - Returns LRKV_ERR_WORKSPACE (explained by lrkv_last_error()) when
  *     lrkv_decode_workspace_bytes(dims, batch) exceeds LRKV_STATIC_WS_BYTES.
  *   - All calls on a device share the one array, which keeps the last call's
@@ -207,6 +216,50 @@ lrkv_status lrkv_decode_static_ws(const lrkv_dims* dims, const void* q, const vo
                                   const lrkv_cache* cache, const int32_t* block_table, int32_t max_blocks_per_seq,
                                   const int32_t* seq_lens, int32_t batch, void* out, uint32_t* status_dev,
                                   void* stream);
+
+/* ======================================================================
+ * Layer-batched calls: one launch of each kernel for several layers.
+ *
+ * A decode step of an L-layer model appends one row per sequence and attends over every
+ * layer's cache.  Each layer has its own weights, cache pools, queries and outputs; the block
+ * table and the lengths are the same for all layers.  When the queries of several layers are
+ * known together (independent layers, or layers whose inputs are already computed), these
+ * calls do the work of num_layers calls of lrkv_append / lrkv_decode in one launch per kernel,
+ * with the whole batch's cached tokens of all layers divided evenly over the SMs -- many small
+ * layers otherwise pay each kernel's fixed start-up and drain cost once per layer.
+ *
+ * Layer l's tensor is found at (layer 0's pointer) + l * stride, strides in bf16 elements
+ * (multiples of 8, so every layer's tensors stay 16-byte aligned, and at least the size of
+ * one layer's tensor: layers do not overlap).  The `cache` argument holds layer 0's pools
+ * and num_blocks, the number of blocks of each layer's pools.
+ * ====================================================================== */
+typedef struct lrkv_layer_strides {
+    int64_t X, W_catT;      /* lrkv_append_layers: hidden rows [n_tok][d], W_cat^T [N][d] */
+    int64_t q, BK, BV, out; /* lrkv_decode_layers: [batch][H][d_h + d_rope], [H][d_h][r] (x2), [batch][H][d_h] */
+    int64_t sK, sV, zK, zV; /* cache pools of both calls */
+} lrkv_layer_strides;
+
+/*
+ * lrkv_append_layers -- lrkv_append of the same n_tok token slots (slot_mapping, positions)
+ *   in num_layers layers: layer l's rows X_l W_cat,l go to layer l's pools.  Everything else
+ *   as for lrkv_append; num_layers == 1 is lrkv_append (strides ignored, may be NULL).
+ */
+lrkv_status lrkv_append_layers(const lrkv_dims* dims, int32_t num_layers, const lrkv_layer_strides* strides,
+                               const void* X, const void* W_catT, int32_t n_tok, const int32_t* slot_mapping,
+                               const int32_t* positions, const lrkv_cache* cache, uint32_t* status_dev,
+                               void* stream);
+
+/*
+ * lrkv_decode_layers -- lrkv_decode of the same batch (block_table, seq_lens) in num_layers
+ *   layers: out_l = decode(q_l, B^K_l, B^V_l, cache_l), Eqs. (6)-(7) per layer.  The workspace
+ *   is lrkv_decode_workspace_bytes(dims, num_layers * batch) bytes.  Everything else as for
+ *   lrkv_decode; num_layers == 1 is lrkv_decode (strides ignored, may be NULL).
+ */
+lrkv_status lrkv_decode_layers(const lrkv_dims* dims, int32_t num_layers, const lrkv_layer_strides* strides,
+                               const void* q, const void* BK, const void* BV, const lrkv_cache* cache,
+                               const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               int32_t batch, void* out, void* workspace, size_t workspace_bytes,
+                               uint32_t* status_dev, void* stream);
 
 /* Workspace bytes lrkv_prefill needs (0 today; kept so callers size it). */
 size_t lrkv_prefill_workspace_bytes(const lrkv_dims* dims, int32_t batch, int32_t Tq);

@@ -20,7 +20,7 @@ def _declared():
 def test_header_declares_expected_calls():
     names = _declared()
     for n in ("lrkv_append", "lrkv_decode", "lrkv_decode_fused", "lrkv_prefill", "lrkv_decode_workspace_bytes",
-              "lrkv_status_string"):
+              "lrkv_status_string", "lrkv_append_layers", "lrkv_decode_layers"):
         assert n in names
 
 
@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol():
     for name in _declared():
         assert hasattr(lib, name), name
     assert set(_declared()) <= set(b.EXPORTED) | set(_declared())
-    assert b.abi_version() == 2
+    assert b.abi_version() == 3
 
 
 def test_status_strings():
@@ -145,3 +145,71 @@ def test_mla_arguments():
     assert lib.lrkv_mla_decode(ctypes.byref(dims), 16, 16, 1, 16, 1, 16, 0, 16, 256, 0, None, None) == 0
     assert lib.lrkv_mla_decode(ctypes.byref(dims), 16, 16, 0, 16, 1, 16, 1, 16, 256, 0, None, None) == 1
     assert lib.lrkv_mla_decode(ctypes.byref(dims), 16, 16, 1, None, 1, 16, 1, 16, 256, 0, None, None) == 1
+
+
+def test_header_supported_ranks_match_the_library():
+    """The header's supported set of r is the one the library accepts."""
+    txt = open(HEADER).read()
+    m = re.search(r"r in \{([0-9, ]+)\}", txt)
+    assert m, "supported ranks not stated"
+    stated = sorted(int(x) for x in m.group(1).split(","))
+    accepted = [r for r in range(1, 129) if b.cache_block_bytes(b.make_dims(8, 128, r, 1024)) > 0]
+    assert stated == accepted == [8, 16, 32]
+
+
+@pytest.mark.parametrize("ns,ok", [(0, True), (1, True), (7, True), (65536, True), (-1, False), (65537, False)])
+def test_num_splits_range(ns, ok):
+    dims = b.make_dims(8, 64, 16, 512, num_splits=ns)
+    assert (b.cache_block_bytes(dims) > 0) == ok
+    if not ok:
+        lib = b.load()
+        c = b.Cache(16, 16, 16, 16, 1)
+        assert lib.lrkv_append(ctypes.byref(dims), 16, 16, 1, 16, None, ctypes.byref(c), None, None) == 1
+        assert b"num_splits" in lib.lrkv_last_error()
+
+
+def _strides(**kw):
+    st = b.LayerStrides()
+    for k, v in kw.items():
+        setattr(st, k, v)
+    return st
+
+
+def test_layer_batched_calls_validate_strides():
+    """Per-layer strides must be multiples of 8 elements and cover one layer's tensor; one layer
+    ignores them; checked before anything touches the device."""
+    lib = b.load()
+    H, d_h, r, d, nb, n = 8, 64, 16, 512, 4, 3
+    dims = b.make_dims(H, d_h, r, d)
+    c = b.Cache(16, 16, 16, 16, nb)
+    rows = nb * 64
+    N = 2 * (d_h + H * r)
+    good = dict(X=n * d, W_catT=N * d, sK=rows * d_h, sV=rows * d_h, zK=rows * H * r, zV=rows * H * r)
+    app = lambda L, st: lib.lrkv_append_layers(ctypes.byref(dims), L, st, 16, 16, n, 16, None, ctypes.byref(c), None,
+                                               None)
+    assert app(0, ctypes.byref(_strides(**good))) == 1
+    assert app(2, None) == 1
+    for k in good:
+        bad = dict(good)
+        bad[k] = good[k] - 8          # layers would overlap
+        assert app(2, ctypes.byref(_strides(**bad))) == 1, k
+        assert k in lib.lrkv_last_error().decode()
+        bad[k] = good[k] + 4          # not 16-byte aligned
+        assert app(2, ctypes.byref(_strides(**bad))) == 1, k
+    # zero rows: a no-op once the arguments are valid
+    assert lib.lrkv_append_layers(ctypes.byref(dims), 3, ctypes.byref(_strides(**good)), None, None, 0, None, None,
+                                  ctypes.byref(c), None, None) == 0
+    B = 2
+    dgood = dict(q=B * H * d_h, BK=H * d_h * r, BV=H * d_h * r, out=B * H * d_h, sK=rows * d_h, sV=rows * d_h,
+                 zK=rows * H * r, zV=rows * H * r)
+    dec = lambda L, st: lib.lrkv_decode_layers(ctypes.byref(dims), L, st, 16, 16, 16, ctypes.byref(c), 16, 1, 16, B,
+                                               16, 256, 1 << 30, None, None)
+    for k in dgood:
+        bad = dict(dgood)
+        bad[k] = dgood[k] - 8
+        assert dec(2, ctypes.byref(_strides(**bad))) == 1, k
+        assert k in lib.lrkv_last_error().decode()
+    assert dec(0, ctypes.byref(_strides(**dgood))) == 1
+    assert dec(2, None) == 1
+    assert lib.lrkv_decode_layers(ctypes.byref(dims), 2, ctypes.byref(_strides(**dgood)), 16, 16, 16,
+                                  ctypes.byref(c), 16, 1, 16, 0, 16, 256, 0, None, None) == 0

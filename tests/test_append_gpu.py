@@ -82,7 +82,11 @@ def test_append_gaussian_within_accumulation_bound(n, H, d_h, r, d):
         rv = f64(r_.reshape(-1, *r_.shape[2:])[:n])
         bound = _bf16_ulp(rv) + 2 * d * 2.0 ** -24 * mag
         assert np.all(np.abs(gv - rv) <= bound), nm
-        assert (gv != rv).mean() < 2e-2, nm
+        # Measured on GB300: 0 to 2.7e-3 of the elements per segment (1e-3 to 2e-3 for K = 4096,
+        # where the fp32 sums carry the most rounding); bound at about twice the largest.
+        frac = float((gv != rv).mean())
+        print(f"append ulp mismatch n={n} H={H} d_h={d_h} r={r} d={d} {nm}: {frac:.2e} of {gv.size}")
+        assert frac < 5e-3, nm
 
 
 @pytest.mark.parametrize("n", [6, 100])

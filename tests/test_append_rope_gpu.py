@@ -76,7 +76,9 @@ def test_append_rope_exact_inputs(n, H, d_h, r, d, base):
     # rotated columns: within one bf16 ulp, and almost all identical
     gr, rr = f64(g[0][:, d_h:]), f64(ref[0][:, d_h:])
     assert np.all(np.abs(gr - rr) <= _bf16_ulp(rr)), "k^R beyond one ulp"
-    assert (gr != rr).mean() <= 2e-3
+    # The rotation's last-bit differences from the plain-double rotation hit ~2e-5 of the rounded
+    # values (a CPU model of the arithmetic); allow 1e-4 of them, and at least one.
+    assert int((gr != rr).sum()) <= max(1, int(np.ceil(1e-4 * gr.size)))
     # position 0 is the identity rotation: k^R is the plain projection
     np.testing.assert_array_equal(g[0][0, d_h:], oracle_rows(X[:1], w, WKR, np.zeros(1, np.int32), base)[0][0, d_h:])
     # every other slot keeps its previous contents
@@ -110,7 +112,9 @@ def test_append_rope_gaussian_within_bound(n, H, d_h, r, d):
     for gi, ri, mag, nm in zip(g, ref, mags, ("sK", "sV", "zK", "zV")):
         gv, rv = f64(gi), f64(ri)
         assert np.all(np.abs(gv - rv) <= _bf16_ulp(rv) + 2 * d * 2.0 ** -24 * mag), nm
-        assert (gv != rv).mean() < 2e-2, nm
+        frac = float((gv != rv).mean())
+        print(f"rope append ulp mismatch n={n} H={H} d_h={d_h} r={r} d={d} {nm}: {frac:.2e} of {gv.size}")
+        assert frac < 2e-2, nm
 
 
 def test_append_without_positional_key_ignores_positions():

@@ -7,15 +7,15 @@ import torch
 import lrkv_synth as S
 import oracle
 from cases import random_pools, weights
-from gpu_util import assert_close, dev_bf16, dev_i32, host_f64
+from gpu_util import assert_close, dev_bf16, dev_i32, errors, host_f64
 
 pytestmark = pytest.mark.gpu
 
 from compressed_kv_cache_lrkv_gb300 import binding as b  # noqa: E402
 
 
-def run_decode(H, d_h, r, pools, pt, q, BK, BV, status=None, scale=0.0):
-    dims = b.make_dims(H, d_h, r, H * d_h, softmax_scale=scale)
+def run_decode(H, d_h, r, pools, pt, q, BK, BV, status=None, scale=0.0, num_splits=0):
+    dims = b.make_dims(H, d_h, r, H * d_h, softmax_scale=scale, num_splits=num_splits)
     cache = b.PagedCache(*(dev_bf16(p) for p in pools))
     Bn = q.shape[0]
     out = torch.empty((Bn, H, d_h), dtype=torch.bfloat16, device="cuda")
@@ -107,6 +107,55 @@ def test_decode_is_deterministic_and_page_permutation_invariant():
     assert torch.equal(a.view(torch.int16), c.view(torch.int16))
 
 
+def _bf16_ulp(x):
+    x = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+SPLITS = [1, 2, 7, 0]
+
+
+def test_split_count_invariance():
+    """The number of pieces the batch's tokens are cut into (num_splits; 0 = one per SM) changes
+    only the order of the fp32 sums and which running maximum each probability is taken against.
+    Every split count meets the oracle bar.  With flat logits (q = 0, so p = 1 exactly for every
+    token) every count sums the same exact products, so the fp32 results agree to ~1e-7 relative
+    and the bf16 outputs are equal except where the fp32 value lies within that distance of a
+    rounding boundary: at most one ulp apart, in well under 1% of the elements.  With Gaussian
+    queries the probabilities are rounded to bf16 (for the tensor-core p . s^V product) against
+    different running maxima, so counts differ at that rounding level: rel-L2 <= 2e-3."""
+    H, d_h, r = 32, 128, 32
+    pt, pools, w, q = decode_case(23, H, d_h, r, [3000, 129, 64, 1, 700])
+    ref = oracle.get().decode_cache(pools, pt.block_table, pt.seq_lens, w.BK, w.BV, q)
+    outs = {}
+    for ns in SPLITS:
+        out, st = run_decode(H, d_h, r, pools, pt, q, w.BK, w.BV, num_splits=ns)
+        assert st == 0
+        outs[ns] = host_f64(out)
+        rel, mx = assert_close(outs[ns], ref, f"num_splits={ns}")
+        print(f"num_splits={ns}: oracle rel_l2={rel:.2e} max_abs={mx:.2e}")
+    for ns in SPLITS[:-1]:
+        rel, _ = errors(outs[ns], outs[0])
+        print(f"num_splits={ns} vs automatic: rel_l2={rel:.2e}")
+        assert rel <= 2e-3, (ns, rel)
+
+    q0 = np.zeros_like(q)
+    flat = {}
+    for ns in SPLITS:
+        out, st = run_decode(H, d_h, r, pools, pt, q0, w.BK, w.BV, num_splits=ns)
+        assert st == 0
+        flat[ns] = host_f64(out)
+    ref0 = oracle.get().decode_cache(pools, pt.block_table, pt.seq_lens, w.BK, w.BV, q0)
+    assert_close(flat[0], ref0, "flat logits")
+    for ns in SPLITS[:-1]:
+        d = np.abs(flat[ns] - flat[0])
+        frac = float((d > 0).mean())
+        print(f"flat logits, num_splits={ns} vs automatic: {frac:.2e} of elements one ulp apart")
+        assert np.all(d <= _bf16_ulp(flat[0])), ns
+        assert frac <= 1e-2, (ns, frac)
+
+
 def test_decode_batch_composition_changes_only_rounding():
     """A sequence decoded alone or inside a batch gets the same result up to fp32
     summation order (the split boundaries depend on the whole batch)."""
@@ -150,3 +199,30 @@ def test_decode_nan_in_unused_slots_does_not_leak():
     out, st = run_decode(H, d_h, r, pools, pt, q, w.BK, w.BV)
     ref = oracle.get().decode_cache(pools, pt.block_table, pt.seq_lens, w.BK, w.BV, q)
     assert_close(host_f64(out), ref, "NaN in unused slots")
+
+
+def test_expired_wait_reports_timeout_and_gpu_stays_usable(monkeypatch):
+    """Failure detection without a fault: with the debugging limit LRKV_DEBUG_WAIT_LIMIT_NS=0 the
+    split kernel's pipeline waits give up as soon as a stage is not already there.  The kernel
+    then stops consuming, waits (with its full limit) for the copies it has in flight, and exits;
+    the call reports LRKV_DEV_TIMEOUT through the status word, and the next decode on the same
+    context is correct."""
+    H, d_h, r = 32, 128, 32
+    pt, pools, w, q = decode_case(29, H, d_h, r, [20000, 9000])
+    monkeypatch.setenv("LRKV_DEBUG_WAIT_LIMIT_NS", "0")
+    seen = 0
+    for _ in range(3):  # a wait is only sure to expire if some stage is not ready at once
+        _, st = run_decode(H, d_h, r, pools, pt, q, w.BK, w.BV)
+        seen |= st
+        if st & b.DEV_TIMEOUT:
+            break
+    assert seen & b.DEV_TIMEOUT
+    assert seen & ~b.DEV_TIMEOUT == 0
+    monkeypatch.delenv("LRKV_DEBUG_WAIT_LIMIT_NS")
+    out, st = run_decode(H, d_h, r, pools, pt, q, w.BK, w.BV)
+    assert st == 0
+    want = np.zeros((2, H), np.uint8)
+    want[:, ::4] = 1
+    ref = oracle.get().decode_cache(pools, pt.block_table, pt.seq_lens, w.BK, w.BV, q, want=want)
+    sel = want.astype(bool)
+    assert_close(host_f64(out)[sel], ref[sel], "decode after an expired wait")

@@ -116,7 +116,8 @@ def test_mla_append_exact_inputs(n):
     np.testing.assert_array_equal(got[slots, :DC], ref[:, :DC])
     gr, rr = f64(got[slots, DC:]), f64(ref[:, DC:])
     assert np.all(np.abs(gr - rr) <= _bf16_ulp(rr))
-    assert (gr != rr).mean() <= 2e-3
+    # last-bit differences of the rotation: ~2e-5 of the values; allow 1e-4 of them, and at least one
+    assert int((gr != rr).sum()) <= max(1, int(np.ceil(1e-4 * gr.size)))
     untouched = np.setdiff1d(np.arange(nb * 64), slots)
     assert np.all(got[untouched] == CANARY)
 

@@ -65,11 +65,14 @@ def _run_step(hz):
     assert int(hz.status.item()) == 0
 
 
-@pytest.mark.parametrize("key,d_rope", [("small", 0), ("backbone12", 0), ("dsv2", 0), ("longctx", 0), ("dsv2", 64),
-                                        ("longctx", 64)])
-def test_decode_workload_full_size(key, d_rope, oracle_lib):
+@pytest.mark.parametrize("key,d_rope,per_layer", [("small", 0, False), ("backbone12", 0, False),
+                                                  ("backbone12", 0, True), ("dsv2", 0, False), ("longctx", 0, False),
+                                                  ("dsv2", 64, False), ("longctx", 64, False)])
+def test_decode_workload_full_size(key, d_rope, per_layer, oracle_lib):
+    """(The 12-layer backbone runs through the layer-batched calls, as the benchmark times it,
+    and once more layer by layer.)"""
     wl = S.WORKLOADS[key]
-    hz = bench.DecodeHarness(wl, 0, d_rope=d_rope)
+    hz = bench.DecodeHarness(wl, 0, d_rope=d_rope, per_layer=per_layer)
     heads = _heads(wl.H, 8)
     layers = sorted({0, wl.layers // 2, wl.layers - 1})
     seqs = sorted({0, wl.B // 2, wl.B - 1})
@@ -78,16 +81,15 @@ def test_decode_workload_full_size(key, d_rope, oracle_lib):
     for li in layers:
         for b in seqs:
             n = int(hz.seq_lens[b])
-            pages[li, b] = _seq_pools(hz.layers[li]["cache"], hz.pt.block_table[b, :(n + 63) // 64], heads)
+            pages[li, b] = _seq_pools(hz.cache.layer(li), hz.pt.block_table[b, :(n + 63) // 64], heads)
     _run_step(hz)
 
     got, ref = [], []
     for li in layers:
-        L = hz.layers[li]
-        WsK, WsV, UK, UV, WKR = _unpack_wcat(host_bits(L["wcat"]), wl.d_h, wl.H, wl.r, d_rope)
-        X, q = host_bits(L["x"]), host_bits(L["q"])
-        BK, BV = host_bits(L["BK"])[heads], host_bits(L["BV"])[heads]
-        out = host_f64(L["out"])
+        WsK, WsV, UK, UV, WKR = _unpack_wcat(host_bits(hz.wcat[li]), wl.d_h, wl.H, wl.r, d_rope)
+        X, q = host_bits(hz.x[li]), host_bits(hz.q[li])
+        BK, BV = host_bits(hz.BK[li])[heads], host_bits(hz.BV[li])[heads]
+        out = host_f64(hz.out[li])
         # the step appended each sequence's newest token (position seq_len - 1) before decoding
         pos = (hz.seq_lens[seqs] - 1).astype(np.int32)
         newest = oracle_lib.append(X[seqs], WsK, WsV, UK[heads], UV[heads], WKR=WKR, positions=pos)

@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import lrkv_synth as S
+import oracle
 from cases import random_pools, weights
 from gpu_util import assert_close, dev_bf16, dev_i32, host_f64
 
@@ -23,11 +24,16 @@ pytestmark = pytest.mark.gpu
 from compressed_kv_cache_lrkv_gb300 import binding as b  # noqa: E402
 
 
-def _case(seed, H, d_h, r, lens):
+def _host_case(seed, H, d_h, r, lens):
     pt = S.page_table(seed, lens, 64, spare_blocks=1)
     pools = random_pools(seed, pt.num_blocks, H, d_h, r)
     w = weights(seed, H * d_h, d_h, H, r)
     q = S.gaussian_bf16(seed, "q", (len(lens), H, d_h))
+    return pt, pools, w, q
+
+
+def _case(seed, H, d_h, r, lens):
+    pt, pools, w, q = _host_case(seed, H, d_h, r, lens)
     dims = b.make_dims(H, d_h, r, H * d_h)
     cache = b.PagedCache(*(dev_bf16(p) for p in pools))
     return dims, cache, dev_bf16(q), dev_bf16(w.BK), dev_bf16(w.BV), dev_i32(pt.block_table), dev_i32(pt.seq_lens)
@@ -63,6 +69,13 @@ def test_static_scratch_decode_matches_workspace_decode_twice():
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         assert_close(host_f64(got), host_f64(ref), "static-scratch decode vs workspace decode")
+    # and directly against the fp64 oracle on the first problem, after the second has used the array
+    pt, pools, w, q = _host_case(41, 32, 128, 32, [9000, 300, 4100])
+    got, status = _static(*first)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.get().decode_cache(pools, pt.block_table, pt.seq_lens, w.BK, w.BV, q)
+    assert_close(host_f64(got), ref, "static-scratch decode vs oracle")
 
 
 def test_static_scratch_rejects_batches_that_do_not_fit():
