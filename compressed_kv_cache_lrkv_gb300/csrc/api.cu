@@ -169,17 +169,20 @@ lrkv_status make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t
     return LRKV_OK;
 }
 
-// 3-D bf16 tensor map over `layers` row-major [rows][cols] matrices, layer_pitch bytes apart
-// (any valid pitch when layers == 1), with a {box_cols, box_rows, 1} box and 128-byte swizzle.
-lrkv_status make_tmap_layers(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t layers,
-                             uint64_t layer_pitch, uint32_t box_cols, uint32_t box_rows, const char* what) {
+// 4-D bf16 tensor map over `layers` row-major [rows][cols] matrices (cols a multiple of 64),
+// layer_pitch bytes apart (any valid pitch when layers == 1), that views each row as cols / 64
+// parts of 64 columns, 128 bytes apart: dims {64, rows, parts, layers}.  A {64, box_rows, parts,
+// 1} box then brings box_rows whole rows in one copy, laid out [part][row][64] with 128-byte
+// swizzle, as cols / 64 boxes of {64, box_rows} would.
+lrkv_status make_tmap_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t layers,
+                           uint64_t layer_pitch, uint32_t box_rows, const char* what) {
     auto enc = encode_fn();
     if (!enc) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-    cuuint64_t dims[3] = {cols, rows, layers};
-    cuuint64_t strides[2] = {cols * 2, layers > 1 ? layer_pitch : cols * 2 * rows};
-    cuuint32_t box[3] = {box_cols, box_rows, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+    cuuint64_t dims[4] = {64, rows, cols / 64, layers};
+    cuuint64_t strides[3] = {cols * 2, 128, layers > 1 ? layer_pitch : cols * 2 * rows};
+    cuuint32_t box[4] = {64, box_rows, (cuuint32_t)(cols / 64), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
@@ -411,11 +414,11 @@ static lrkv_status decode_impl(const lrkv_dims* dims, int32_t num_layers, const 
         return fail(LRKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
 
     CUtensorMap tK, tV;
-    if ((s = make_tmap_layers(&tK, cache->sK, dk, rows, num_layers, num_layers > 1 ? (uint64_t)ls->sK * 2 : 0, 64, 8,
-                              "sK")) != LRKV_OK)
+    if ((s = make_tmap_rows(&tK, cache->sK, dk, rows, num_layers, num_layers > 1 ? (uint64_t)ls->sK * 2 : 0, 8,
+                            "sK")) != LRKV_OK)
         return s;
-    if ((s = make_tmap_layers(&tV, cache->sV, dims->d_h, rows, num_layers,
-                              num_layers > 1 ? (uint64_t)ls->sV * 2 : 0, 64, 8, "sV")) != LRKV_OK)
+    if ((s = make_tmap_rows(&tV, cache->sV, dims->d_h, rows, num_layers, num_layers > 1 ? (uint64_t)ls->sV * 2 : 0,
+                            8, "sV")) != LRKV_OK)
         return s;
 
     a.q = static_cast<const uint16_t*>(q);

@@ -165,29 +165,26 @@ struct Work {
         pieces = 0;
         const long long occupied = nonempty * layers;
         if (T == 0 || occupied > nranges) return;
-        // Smallest chunk c with layers * sum_b ceil(gr_b / c) <= nranges.  The count falls as c
-        // grows; c0 = ceil(T / (nranges - occupied)) already fits (sum ceil(gr / c0) <=
-        // T / c0 + occupied), so the search runs between the exact share and c0.
+        // Two candidate piece sizes: the exact share ceil(T / nranges), when its pieces fit in
+        // nranges, else c0 = ceil(T / (nranges - occupied)), which always fits (sum ceil(gr / c0)
+        // <= T / c0 + occupied).  (A search between them gained nothing measurable and, code
+        // being what it is, its loop made the stage loop slower.)
         const long long share = (T + nranges - 1) / nranges;
         const long long c0 = occupied < nranges ? (T + (nranges - occupied) - 1) / (nranges - occupied) : gmax;
-        const int hi0 = (int)min(c0, (long long)gmax);
-        int lo = (int)min(share, (long long)hi0), hi = hi0;
-        while (lo < hi) {
-            const int mid = lo + (hi - lo) / 2;
-            long long n = 0;
-            for (int b = lane; b < B; b += NL) n += (unsigned)(gran_b(b) + mid - 1) / (unsigned)mid;
+        int c = (int)min(share, (long long)gmax);
+        long long n = 0;
+        for (int b = lane; b < B; b += NL) n += (unsigned)(gran_b(b) + c - 1) / (unsigned)c;
+        n = lanes_sum<NL>(n);
+        if (n * layers > nranges) {
+            c = (int)min(c0, (long long)gmax);
+            n = 0;
+            for (int b = lane; b < B; b += NL) n += (unsigned)(gran_b(b) + c - 1) / (unsigned)c;
             n = lanes_sum<NL>(n);
-            if (n * layers <= nranges)
-                hi = mid;
-            else
-                lo = mid + 1;
         }
-        if (lo <= share + bubble) {
-            long long n = 0;
-            for (int b = lane; b < B; b += NL) n += (unsigned)(gran_b(b) + lo - 1) / (unsigned)lo;
+        if (c <= share + bubble) {
             pieces = 1;
-            chunk = lo;
-            per_layer_pieces = lanes_sum<NL>(n);
+            chunk = c;
+            per_layer_pieces = n;
         }
     }
     // Number of pieces of work (CTA iterations) of the call.
@@ -275,6 +272,12 @@ __device__ __forceinline__ void stage_seq_lens(int* dst, const int32_t* src, int
     for (int b = tid; b < B && b < kSeqCache; b += nthreads) dst[b] = src[b];
 }
 
+// Index of (head row h, token t) in a warp's 16 x 8 scratch of z-scores or probabilities.  The
+// token index is XOR-ed with bits 2-3 of h, so that both the stores and loads by (head, four
+// tokens) lanes and those by the (row group, token pair) lanes of the MMA fragments hit 32
+// different banks.
+__device__ __forceinline__ int sidx(int h, int t) { return h * 8 + (t ^ ((h >> 2) & 3)); }
+
 // Bounded wait until a slot's stage tag equals `want` (sets LRKV_DEV_TIMEOUT on expiry).
 __device__ __forceinline__ bool wait_tag(volatile int* tag, int want, uint32_t* status, uint64_t limit_ns) {
     if (*tag == want) return true;
@@ -329,8 +332,9 @@ __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) 
 }
 
 // Issue the loads of one 8-token granule (stage) of block `blk` of layer `l` into a ring slot:
-// s^K (with k^R when D_R > 0), s^V by TMA tensor copies (128-byte swizzle), z^K, z^V by
-// bulk copies.  An out-of-range block id is reported and the stage is marked empty.
+// s^K (with k^R when D_R > 0) and s^V by one TMA tensor copy each (128-byte swizzle; the map
+// views a row as 64-column parts 128 bytes apart, so one box brings all parts of the 8 rows),
+// z^K, z^V by bulk copies.  An out-of-range block id is reported and the stage is marked empty.
 template <int D_H, int R, int D_R>
 __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUtensorMap* tm_sV, const DecodeArgs& a,
                                             uint32_t st, uint32_t bar, int* meta_slot, int l, int blk, int gi,
@@ -345,10 +349,9 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUte
     constexpr int D_K = D_H + D_R;
     mbar_arrive_expect_tx(bar, 16u * (D_K + D_H) + 32u * a.H * R);
     const int row = blk * kBlockSize + ((gi & 7) << 3);
-#pragma unroll
-    for (int i = 0; i < D_K / 64; ++i) tma_load_3d_hint(st + i * 1024, tm_sK, i * 64, row, l, bar, pol);
-#pragma unroll
-    for (int i = 0; i < D_H / 64; ++i) tma_load_3d_hint(st + 16 * D_K + i * 1024, tm_sV, i * 64, row, l, bar, pol);
+    // one copy per shared part: the 8 rows' 64-column parts land as [part][row][64], 1 KB per part
+    tma_load_4d_hint(st, tm_sK, 0, row, 0, l, bar, pol);
+    tma_load_4d_hint(st + 16 * D_K, tm_sV, 0, row, 0, l, bar, pol);
     const size_t zoff = (size_t)row * a.H * R;
     bulk_load_hint(st + 16 * (D_K + D_H), a.zK + l * a.ls_zK + zoff, 16u * a.H * R, bar, pol);
     bulk_load_hint(st + 16 * (D_K + D_H) + 16 * a.H * R, a.zV + l * a.ls_zV + zoff, 16u * a.H * R, bar, pol);
@@ -587,16 +590,16 @@ __global__ void __launch_bounds__(256, 1)
                         acc = fmaf(qt[cc * 8 + 7], bf16hi(v.w), acc);
                     }
                 }
-                SZ[hz * 8 + t] = acc;
+                SZ[sidx(hz, t)] = acc;
             }
             __syncwarp();
 
             // --- scores, mask, online softmax (rows hA: c0,c1; hB: c2,c3; tokens 2tq, 2tq+1)
             const int ta = 2 * tq, tb = 2 * tq + 1;
-            float s0 = (ta < nvalid) ? (c[0] + SZ[g * 8 + ta]) * a.scale_log2 : -INFINITY;
-            float s1 = (tb < nvalid) ? (c[1] + SZ[g * 8 + tb]) * a.scale_log2 : -INFINITY;
-            float s2 = (ta < nvalid) ? (c[2] + SZ[(g + 8) * 8 + ta]) * a.scale_log2 : -INFINITY;
-            float s3 = (tb < nvalid) ? (c[3] + SZ[(g + 8) * 8 + tb]) * a.scale_log2 : -INFINITY;
+            float s0 = (ta < nvalid) ? (c[0] + SZ[sidx(g, ta)]) * a.scale_log2 : -INFINITY;
+            float s1 = (tb < nvalid) ? (c[1] + SZ[sidx(g, tb)]) * a.scale_log2 : -INFINITY;
+            float s2 = (ta < nvalid) ? (c[2] + SZ[sidx(g + 8, ta)]) * a.scale_log2 : -INFINITY;
+            float s3 = (tb < nvalid) ? (c[3] + SZ[sidx(g + 8, tb)]) * a.scale_log2 : -INFINITY;
             float mx0 = fmaxf(s0, s1), mx1 = fmaxf(s2, s3);
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
@@ -620,10 +623,10 @@ __global__ void __launch_bounds__(256, 1)
                 o[n][2] *= al1;
                 o[n][3] *= al1;
             }
-            SP[g * 8 + ta] = p0;
-            SP[g * 8 + tb] = p1;
-            SP[(g + 8) * 8 + ta] = p2;
-            SP[(g + 8) * 8 + tb] = p3;
+            SP[sidx(g, ta)] = p0;
+            SP[sidx(g, tb)] = p1;
+            SP[sidx(g + 8, ta)] = p2;
+            SP[sidx(g + 8, tb)] = p3;
             if (tq == 0) {
                 SA[g] = al0;
                 SA[g + 8] = al1;
@@ -639,7 +642,7 @@ __global__ void __launch_bounds__(256, 1)
                 for (int i = 0; i < 4; ++i) {
                     const int t = half * 4 + i;
                     if (hz_ok && t < nvalid) {
-                        const float p = SP[hz * 8 + t];
+                        const float p = SP[sidx(hz, t)];
                         const uint4* row = reinterpret_cast<const uint4*>(zV_p + ((size_t)t * H + hzh) * R * 2);
 #pragma unroll
                         for (int cc = 0; cc < NC; ++cc) {

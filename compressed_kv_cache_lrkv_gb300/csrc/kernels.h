@@ -78,7 +78,8 @@ cudaError_t launch_append_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, con
 // Workspace of a decode over nvb = layers * B virtual sequences cut into `nranges` ranges.
 size_t decode_workspace_bytes(int H, int D_H, int R, int nvb, int nranges);
 void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int nvb, int nranges);
-// tK, tV: 3-D maps {d_h (+ d_rope), nb * 64, layers}, box {64, 8, 1}, 128-byte swizzle.
+// tK, tV: 4-D maps {64, nb * 64, (d_h (+ d_rope)) / 64, layers}, box {64, 8, parts, 1}, 128-byte swizzle
+// (the parts dimension steps 128 bytes along a row).
 // The split kernel runs on min(nranges, sms) CTAs.
 cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int D_R,
                           int sms, int smem_limit, cudaStream_t stream);
