@@ -7,11 +7,12 @@
 // This file holds the bandwidth-bound variants used when few rows are appended
 // (a decode step appends one row per sequence): the weight rows (W_cat^T,
 // contiguous along d) are streamed exactly once with 16-byte loads, for a block
-// of token rows at a time -- on the CUDA cores below 64 MB of weights, as a
-// split-K product on the warp-level tensor cores above.  A layer-batched call runs
-// every layer in the same launch (grid z = layer, per-layer strides in the arguments).  fp32 accumulation in a
-// fixed order, round to nearest even to bf16 (after rotating the positional-key
-// pairs), scatter to the row's slot.
+// of token rows at a time -- on the CUDA cores a warp per column for d <= 1024
+// and a CTA per column below 64 MB of weights, as a split-K product on the
+// warp-level tensor cores above.  A layer-batched call runs every layer in the
+// same launch (grid z = layer, per-layer strides in the arguments).  fp32
+// accumulation in a fixed order, round to nearest even to bf16 (after rotating
+// the positional-key pairs), scatter to the row's slot.
 #include "kernels.h"
 #include "lrkv_internal.cuh"
 #include "rotary.cuh"
@@ -75,18 +76,23 @@ template <int NT, int NCOL>
 __device__ __forceinline__ void rowwise_partials(const AppendArgs& a, const uint16_t* w0, const uint16_t* w1, int t0,
                                                  float (&acc)[2][NT]) {
     const int nchunk = a.d >> 3;
-#pragma unroll 4
+    // Rows past n read the last row instead (their sums are never stored), so that every load
+    // of a chunk is issued before the first is used.
+    const uint4* xr[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) xr[t] = reinterpret_cast<const uint4*>(a.X + (size_t)min(t0 + t, a.n - 1) * a.d);
+#pragma unroll 2
     for (int k8 = threadIdx.x; k8 < nchunk; k8 += 128) {
         const uint4 w = __ldg(reinterpret_cast<const uint4*>(w0) + k8);
         uint4 w1v = make_uint4(0, 0, 0, 0);
         if (NCOL == 2) w1v = __ldg(reinterpret_cast<const uint4*>(w1) + k8);
+        uint4 x[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) x[t] = __ldg(xr[t] + k8);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-            if (t0 + t < a.n) {
-                const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + t) * a.d) + k8);
-                acc[0][t] += dot8(w, x);
-                if (NCOL == 2) acc[1][t] += dot8(w1v, x);
-            }
+            acc[0][t] += dot8(w, x[t]);
+            if (NCOL == 2) acc[1][t] += dot8(w1v, x[t]);
         }
     }
 }
@@ -138,6 +144,90 @@ __global__ void __launch_bounds__(128) append_rowwise_kernel(const AppendArgs a0
                 store_cache_value(a, slot, c + 1, v1);
             }
             store_cache_value(a, slot, c, v0);
+        }
+    }
+}
+
+// Few rows and a small hidden size (d <= 1024): one warp per output column, or per rotation pair
+// of the positional key (8 warps per CTA).  Lane l sums the 16-byte chunks l, l + 32, ... of the
+// column's weight row with the block's NT hidden rows (small, shared by every warp: L1 / L2
+// hits).  The V = NCOL x NT partial sums are then reduced across the warp by recursive halving:
+// at the step with lane mask m, a lane keeps one half of its values, adds the partner's copy of
+// that half and hands over the other half, so after log2(V) steps lane l holds value
+// (l >> (5 - log2 V)) summed over 2^log2(V) lanes, and the remaining masks finish the sum
+// (log2 V + ... shuffles instead of 5 V).  The order of the additions is fixed.
+template <int NT, bool ROPE>
+__global__ void __launch_bounds__(256) append_warp_kernel(const AppendArgs a0) {
+    const AppendArgs a = layer_args(a0, blockIdx.z);
+    constexpr int NCOL = ROPE ? 2 : 1;
+    constexpr int V = NCOL * NT;                                // values per lane: [column][row]
+    constexpr int LOGV = V >= 32 ? 5 : V >= 16 ? 4 : V >= 8 ? 3 : V >= 4 ? 2 : V >= 2 ? 1 : 0;
+    static_assert((1 << LOGV) == V, "V is a power of two <= 32");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = ROPE ? a.d_rope / 2 : 0;
+    const int u = blockIdx.x * 8 + warp;
+    if (u >= a.N - half) return;  // (warp-uniform; the kernel has no block-wide barrier)
+    const bool pair = ROPE && u >= a.d_h && u < a.d_h + half;
+    const int c = (ROPE && u >= a.d_h) ? (pair ? a.d_h + 2 * (u - a.d_h) : u + half) : u;
+    const int t0 = blockIdx.y * NT;
+    float v[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) v[i] = 0.f;
+    const uint4* w0 = reinterpret_cast<const uint4*>(a.W + (size_t)c * a.d);
+    const uint4* w1 = reinterpret_cast<const uint4*>(a.W + (size_t)(c + 1) * a.d);
+    const int nchunk = a.d >> 3;
+    // Rows past n read the last row instead (their sums are never stored), so that every load
+    // of a chunk is issued before the first is used.
+    const uint4* xr[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) xr[t] = reinterpret_cast<const uint4*>(a.X + (size_t)min(t0 + t, a.n - 1) * a.d);
+    for (int k8 = lane; k8 < nchunk; k8 += 32) {
+        const uint4 w = __ldg(w0 + k8);
+        uint4 wb = make_uint4(0, 0, 0, 0);
+        if (ROPE && pair) wb = __ldg(w1 + k8);
+        uint4 x[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) x[t] = __ldg(xr[t] + k8);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            v[t] += dot8(w, x[t]);
+            if (ROPE) v[NT + t] += dot8(wb, x[t]);
+        }
+    }
+    // recursive halving over masks 16, 8, ..., then plain butterflies
+#pragma unroll
+    for (int step = 0, n = V; step < 5; ++step) {
+        const int m = 16 >> step;
+        if (n > 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                if (i < n / 2) {
+                    const float keep = upper ? v[i + n / 2] : v[i];
+                    const float give = upper ? v[i] : v[i + n / 2];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, give, m);
+                }
+            }
+            n >>= 1;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+        }
+    }
+    const int vi = LOGV == 0 ? 0 : (lane >> (5 - LOGV)) & (V - 1);
+    const int col = vi / NT, t = vi - (vi / NT) * NT;
+    float other = 0.f;
+    if (ROPE) other = __shfl_xor_sync(0xffffffffu, v[0], 16);  // the pair's other column, same row
+    const bool writer = (lane & ((32 >> LOGV) - 1)) == 0 && col == 0 && t0 + t < a.n;
+    if (writer) {
+        const long long slot = checked_slot(a, t0 + t);
+        if (slot >= 0) {
+            float x0 = v[0];
+            if (ROPE && pair) {
+                float x1 = other;
+                rope_rotate(x0, x1, u - a.d_h, a.d_rope, a.positions[t0 + t], a.rope_base);
+                store_cache_value(a, slot, c + 1, x1);
+            }
+            store_cache_value(a, slot, c, x0);
         }
     }
 }
@@ -353,7 +443,28 @@ static cudaError_t launch_rowwise(const AppendArgs& a, cudaStream_t stream) {
 #undef LRKV_ROW
 }
 
+static cudaError_t launch_warp(const AppendArgs& a, cudaStream_t stream) {
+#define LRKV_WARP(NTV)                                                                                     \
+    {                                                                                                      \
+        dim3 grid((a.N - a.d_rope / 2 + 7) / 8, (a.n + NTV - 1) / NTV, a.layers > 1 ? a.layers : 1);       \
+        if (a.d_rope > 0)                                                                                  \
+            append_warp_kernel<NTV, true><<<grid, 256, 0, stream>>>(a);                                    \
+        else                                                                                               \
+            append_warp_kernel<NTV, false><<<grid, 256, 0, stream>>>(a);                                   \
+        return cudaGetLastError();                                                                         \
+    }
+    if (a.n <= 1) LRKV_WARP(1)
+    if (a.n <= 2) LRKV_WARP(2)
+    if (a.n <= 4) LRKV_WARP(4)
+    if (a.n <= 8) LRKV_WARP(8)
+    LRKV_WARP(16)
+#undef LRKV_WARP
+}
+
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
+    // Small hidden sizes: a warp per column (a CTA per column would leave most of its threads
+    // without a chunk of the row and run many small CTAs).
+    if (a.d <= 1024) return launch_warp(a, stream);
     // Weight streams up to 64 MB: one CTA per output column (the hidden rows stay in L1/L2 at that
     // size and there is no cluster setup); larger ones re-read the hidden rows once per column
     // from L2, so they go through the split-K tensor-core kernel above.
