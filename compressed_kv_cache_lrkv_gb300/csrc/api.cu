@@ -372,6 +372,10 @@ static lrkv_status decode_impl(const lrkv_dims* dims, int32_t num_layers, const 
     if (batch == 0) return ok();
     if (max_blocks_per_seq < 1 || (long long)max_blocks_per_seq * dims->block_size > (1LL << 30))
         return fail(LRKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", max_blocks_per_seq);
+    // the split kernel counts the call's 8-token granules in 32 bits
+    if ((long long)num_layers * batch * max_blocks_per_seq * dims->block_size >= (1LL << 34))
+        return fail(LRKV_ERR_INVALID_ARG, "num_layers x batch x max_blocks_per_seq x block_size = %lld (below 2^34)",
+                    (long long)num_layers * batch * max_blocks_per_seq * dims->block_size);
     LRKV_REQUIRE_PTR(q);
     if (fused) {
         LRKV_REQUIRE_PTR(q_tilde);

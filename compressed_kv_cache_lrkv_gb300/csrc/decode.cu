@@ -41,31 +41,42 @@ constexpr int kScratchFloats = 16 * 8 + 16 * 8 + 16;  // per consumer warp: z-sc
 constexpr int kPageCache = 64;                        // page ids of a segment kept in shared memory
 
 constexpr int kSeqCache = 128;                        // sequence lengths kept in shared memory
+constexpr int kMaxGroups = 8;                         // consumer groups at most (8 warps, one per group)
+
+// Row stride (floats) of a head's accumulator in the shared-memory staging of the group merge:
+// W itself when W = 8 or 24 (mod 32), else W + 8, so that the rows of one MMA fragment (8
+// heads) start 8 or 24 banks apart.
+__host__ __device__ constexpr int decode_stage_stride(int W) { return (W % 16 == 0) ? W + 8 : W; }
 
 // The work of a decode call: nvb = layers * B virtual sequences vb = layer * B + b (all
 // layers share the block table and lengths), each cut into 8-token granules, T granules in
 // all, scanned by `nranges` CTA-sized pieces of work.  Two ways to cut, chosen identically by
-// both kernels (plan()):
+// every CTA (plan()):
 //  - pieces: every sequence is cut into ceil(gr / chunk) near-equal pieces, with the smallest
 //    chunk for which all pieces number at most nranges; each piece is one segment with its
 //    own partial slot (the piece's global index).  No CTA crosses a sequence boundary, so no
 //    pipeline drains between sequences; used when the largest piece costs at most a pipeline
 //    drain-and-refill (`bubble` granules) more than an exact split would.
 //  - ranges: the granules of all virtual sequences, concatenated in vb order, are divided
-//    into nranges contiguous ranges of equal size (+-1): range c is [c T / nranges,
-//    (c + 1) T / nranges) (nranges first clamped to T, so that no range is empty).  A range
-//    covers one or more segments of consecutive sequences; the segment of sequence vb inside
-//    range c writes partial slot vb + c, so each sequence's partials sit in consecutive slots.
-//    Used when the sequences are too many or too uneven for pieces.
+//    into nranges contiguous ranges of equal size (+-1): range c is [floor(c T / nranges),
+//    floor((c + 1) T / nranges)) (nranges first clamped to T, so that no range is empty).  A
+//    range covers one or more segments of consecutive sequences; the segment of sequence vb
+//    inside range c writes partial slot vb + c, so each sequence's partials sit in
+//    consecutive slots.  Used when the sequences are too many or too uneven for pieces.
 // Either way the slots number at most nvb + nranges.
+// All counts are 32-bit (the host bounds T below 2^31 and nranges by 2^16): one thread
+// computes the plan before the first load of the CTA is issued, and a 64-bit division is a
+// long dependent software sequence on the GPU.  floor(c T / n) is formed as c (T / n) +
+// floor(c (T mod n) / n), whose product c (T mod n) < n^2 fits in 32 unsigned bits.
 struct Work {
     const int32_t* g;  // lengths in global memory
     const int* s;      // shared-memory copy of the first kSeqCache
     int B, layers, cap, nranges;
-    long long Tb;      // granules of one layer (all B sequences)
+    int Tb;            // granules of one layer (all B sequences)
     int pieces;        // 1: pieces, 0: ranges
     int chunk;         // pieces: largest piece, in granules
-    long long per_layer_pieces;
+    int per_layer_pieces;
+    int rq, rr;        // ranges: T / nranges and T mod nranges
 
     __device__ __forceinline__ int len(int b) const { return b < kSeqCache ? s[b] : g[b]; }
     // Granules of sequence b, or 0 when its length is outside [1, cap].
@@ -74,63 +85,55 @@ struct Work {
         return (L >= 1 && L <= cap) ? (L + kGran - 1) / kGran : 0;
     }
     __device__ __forceinline__ int gran(int vb) const { return gran_b(vb % B); }
-    __device__ __forceinline__ long long total() const { return Tb * layers; }
-    __device__ __forceinline__ long long range_start(int c) const { return (long long)c * total() / nranges; }
-    // Index of the range that holds granule gi (0 <= gi < total()).
-    __device__ __forceinline__ int range_of(long long gi) const {
-        const long long T = total();
-        return (int)(((gi + 1) * nranges + T - 1) / T - 1);
+    __device__ __forceinline__ int total() const { return Tb * layers; }
+    __device__ __forceinline__ int range_start(int c) const {
+        return c * rq + (int)(((unsigned)c * (unsigned)rr) / (unsigned)nranges);
     }
-    // First granule of virtual sequence vb in the concatenation.
-    __device__ __forceinline__ long long seq_start(int vb) const {
-        const int l = vb / B, b = vb - l * B;
-        long long p = Tb * l;
-        for (int bb = 0; bb < b; ++bb) p += gran_b(bb);
-        return p;
+    // Index of the range that holds granule gi (0 <= gi < total()): a float estimate of
+    // floor(gi nranges / T), off by at most one, stepped to the range whose bounds hold gi.
+    __device__ __forceinline__ int range_of(int gi) const {
+        int c = (int)((float)gi * (float)nranges / (float)total());
+        c = min(max(c, 0), nranges - 1);
+        while (c + 1 < nranges && range_start(c + 1) <= gi) ++c;
+        while (c > 0 && range_start(c) > gi) --c;
+        return c;
     }
     // The (non-empty) virtual sequence that holds granule gi, and its first granule.
-    __device__ __forceinline__ void locate(long long gi, int* vb, long long* start) const {
-        const int l = (int)(gi / Tb);
-        long long p = Tb * l;
+    __device__ __forceinline__ void locate(int gi, int* vb, int* start) const {
+        const int l = (int)((unsigned)gi / (unsigned)Tb);
+        int p = Tb * l;
         int b = 0;
         while (b < B - 1 && p + gran_b(b) <= gi) p += gran_b(b++);
         *vb = l * B + b;
         *start = p;
     }
-    // Pieces of one layer's sequences with largest piece c.
-    __device__ __forceinline__ long long layer_pieces(int c) const {
-        long long n = 0;
-        for (int b = 0; b < B; ++b) n += (gran_b(b) + c - 1) / c;
-        return n;
-    }
-    // Pieces mode: first piece index of virtual sequence vb.
-    __device__ __forceinline__ long long first_piece(int vb) const {
-        const int l = vb / B, b = vb - l * B;
-        long long p = per_layer_pieces * l;
-        for (int bb = 0; bb < b; ++bb) p += (unsigned)(gran_b(bb) + chunk - 1) / (unsigned)chunk;
-        return p;
+    // Pieces of sequence b with largest piece c.
+    __device__ __forceinline__ int npieces(int b, int c) const {
+        return (int)((unsigned)(gran_b(b) + c - 1) / (unsigned)c);
     }
     // Pieces mode: virtual sequence and granule range of piece pc.
-    __device__ __forceinline__ void piece(long long pc, int* vb, int* g0, int* g1) const {
-        const int l = (int)(pc / per_layer_pieces);
-        long long base = per_layer_pieces * l;
+    __device__ __forceinline__ void piece(int pc, int* vb, int* g0, int* g1) const {
+        const int l = (int)((unsigned)pc / (unsigned)per_layer_pieces);
+        int base = per_layer_pieces * l;
         int b = 0;
         for (;; ++b) {
-            const int n = (int)((unsigned)(gran_b(b) + chunk - 1) / (unsigned)chunk);
+            const int n = npieces(b, chunk);
             if (pc < base + n || b == B - 1) break;
             base += n;
         }
-        const int gr = gran_b(b);
-        const int np = (gr + chunk - 1) / chunk;
-        const int i = (int)(pc - base);
+        const unsigned gr = (unsigned)gran_b(b);
+        const unsigned np = (gr + chunk - 1) / (unsigned)chunk;
+        const unsigned i = (unsigned)(pc - base);
+        // floor(i gr / np) with i < np <= 2^16
+        const unsigned q = gr / np, r = gr - q * np;
         *vb = l * B + b;
-        *g0 = (int)((long long)i * gr / np);
-        *g1 = (int)((long long)(i + 1) * gr / np);
+        *g0 = (int)(i * q + (i * r) / np);
+        *g1 = (int)((i + 1) * q + ((i + 1) * r) / np);
     }
 
     // Sum (max for gmax) over the NL lanes that share a plan (a no-op for one thread).
     template <int NL>
-    __device__ __forceinline__ static long long lanes_sum(long long v) {
+    __device__ __forceinline__ static int lanes_sum(int v) {
         if (NL > 1) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -143,10 +146,7 @@ struct Work {
     // the same plan; publish() then hands it to the rest of the block).
     template <int NL>
     __device__ __forceinline__ void plan(int bubble, int lane) {
-        // (per-sequence counts and piece sizes are 32-bit -- a 64-bit division is a long
-        // software sequence on the GPU; only the sums are 64-bit)
-        long long tb = 0, nonempty = 0;
-        int gmax = 0;
+        int tb = 0, nonempty = 0, gmax = 0;
         for (int b = lane; b < B; b += NL) {
             const int gr = gran_b(b);
             tb += gr;
@@ -160,25 +160,29 @@ struct Work {
             for (int o = 16; o > 0; o >>= 1) gmax = max(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
         }
         Tb = tb;
-        const long long T = total();
-        if (T < nranges) nranges = (int)T;  // no empty range
+        const unsigned T = (unsigned)total();
+        if ((int)T < nranges) nranges = (int)T;  // no empty range
         pieces = 0;
-        const long long occupied = nonempty * layers;
+        rq = nranges > 0 ? (int)(T / (unsigned)nranges) : 0;
+        rr = nranges > 0 ? (int)(T - (unsigned)rq * (unsigned)nranges) : 0;
+        const int occupied = nonempty * layers;
         if (T == 0 || occupied > nranges) return;
         // Two candidate piece sizes: the exact share ceil(T / nranges), when its pieces fit in
         // nranges, else c0 = ceil(T / (nranges - occupied)), which always fits (sum ceil(gr / c0)
         // <= T / c0 + occupied).  (A search between them gained nothing measurable and, code
         // being what it is, its loop made the stage loop slower.)
-        const long long share = (T + nranges - 1) / nranges;
-        const long long c0 = occupied < nranges ? (T + (nranges - occupied) - 1) / (nranges - occupied) : gmax;
-        int c = (int)min(share, (long long)gmax);
-        long long n = 0;
-        for (int b = lane; b < B; b += NL) n += (unsigned)(gran_b(b) + c - 1) / (unsigned)c;
+        const int share = rq + (rr != 0);
+        const int c0 = occupied < nranges
+                           ? (int)((T + (unsigned)(nranges - occupied) - 1) / (unsigned)(nranges - occupied))
+                           : gmax;
+        int c = min(share, gmax);
+        int n = 0;
+        for (int b = lane; b < B; b += NL) n += npieces(b, c);
         n = lanes_sum<NL>(n);
         if (n * layers > nranges) {
-            c = (int)min(c0, (long long)gmax);
+            c = min(c0, gmax);
             n = 0;
-            for (int b = lane; b < B; b += NL) n += (unsigned)(gran_b(b) + c - 1) / (unsigned)c;
+            for (int b = lane; b < B; b += NL) n += npieces(b, c);
             n = lanes_sum<NL>(n);
         }
         if (c <= share + bubble) {
@@ -188,16 +192,14 @@ struct Work {
         }
     }
     // Number of pieces of work (CTA iterations) of the call.
-    __device__ __forceinline__ long long work_items() const {
-        return pieces ? per_layer_pieces * layers : nranges;
-    }
+    __device__ __forceinline__ int work_items() const { return pieces ? per_layer_pieces * layers : nranges; }
 };
 
 // This CTA's walk over its segments: (virtual sequence, granule range in it, partial slot).
 struct SegWalk {
-    long long item;            // current piece or range
-    long long gcur, gend, vstart;
-    long long seg_start;       // ranges: first granule (in the concatenation) of the last segment returned
+    int item;            // current piece or range
+    int gcur, gend, vstart;
+    int seg_start;       // ranges: first granule (in the concatenation) of the last segment returned
     int vb;
 
     __device__ __forceinline__ void start(int first_item) {
@@ -210,7 +212,7 @@ struct SegWalk {
         if (w.pieces) {
             if (item >= w.work_items()) return false;
             w.piece(item, vb_out, g0, g1);
-            *slot = (int)item;
+            *slot = item;
             item += gridDim.x;
             return true;
         }
@@ -218,16 +220,16 @@ struct SegWalk {
         if (gcur >= gend) {
             if (gend > 0) item += gridDim.x;  // the current range is done
             if (item >= w.nranges) return false;
-            gcur = w.range_start((int)item);
-            gend = w.range_start((int)item + 1);
+            gcur = w.range_start(item);
+            gend = w.range_start(item + 1);
             w.locate(gcur, &vb, &vstart);
         }
         const int gr = w.gran(vb);
-        const long long se = min(gend, vstart + gr);
+        const int se = min(gend, vstart + gr);
         *vb_out = vb;
-        *g0 = (int)(gcur - vstart);
-        *g1 = (int)(se - vstart);
-        *slot = vb + (int)item;
+        *g0 = gcur - vstart;
+        *g1 = se - vstart;
+        *slot = vb + item;
         seg_start = gcur;
         gcur = se;
         if (gcur == vstart + gr) {
@@ -256,7 +258,7 @@ struct SplitCtl {
             const int gr = wk.gran(vb);
             int np;
             if (wk.pieces)
-                np = (int)((unsigned)(gr + wk.chunk - 1) / (unsigned)wk.chunk);
+                np = wk.npieces(vb % wk.B, wk.chunk);
             else
                 np = wk.range_of(walk.seg_start + gr - 1) - (slot - vb) + 1;
             seg_table[vb] = make_int2(slot, np);
@@ -373,6 +375,7 @@ __global__ void __launch_bounds__(256, 1)
     constexpr int NC = R / 8;                                   // 16-byte chunks per z row
     constexpr int RP128 = (2 * R >= 128) ? 1 : 128 / (2 * R);   // z rows per 128-byte bank line
     constexpr int W = D_H + R;                                  // accumulator width per head
+    constexpr int WS = decode_stage_stride(W);                  // its row stride in the group staging
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -398,6 +401,8 @@ __global__ void __launch_bounds__(256, 1)
     SplitCtl* ctl = reinterpret_cast<SplitCtl*>((reinterpret_cast<uintptr_t>(abort_flag) + 16) & ~(uintptr_t)15);
 
     if (threadIdx.x == 0) {
+        prefetch_tmap(&tm_sK);
+        prefetch_tmap(&tm_sV);
         for (int s = 0; s < nslot; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             rel[s] = 0;
@@ -711,12 +716,15 @@ __global__ void __launch_bounds__(256, 1)
         named_bar(1, nct);  // every stage of this segment consumed: the ring is idle
         const bool direct = (a.ng == 1);
         // Workspace partials are laid out [head][slot][...] so that the combine reads
-        // one head's partials contiguously; the shared-memory staging is [group][head].
+        // one head's partials contiguously.  The shared-memory staging is [group][head][WS]
+        // behind the [group][head] (m, l) pairs (offset rounded to 16 bytes): rows WS floats
+        // apart, 8 or 24 banks, so the fragment stores below are free of bank conflicts.
         const size_t hs_ml = direct ? (size_t)a.pmax * 2 : 2;     // stride between heads
-        const size_t hs_acc = direct ? (size_t)a.pmax * W : W;
-        float* gml = direct ? a.part_ml + (size_t)pslot * 2 : reinterpret_cast<float*>(smem) + (size_t)grp * H * 2;
-        float* gacc = direct ? a.part_acc + (size_t)pslot * W
-                             : reinterpret_cast<float*>(smem) + (size_t)a.ng * H * 2 + (size_t)grp * H * W;
+        const size_t hs_acc = direct ? (size_t)a.pmax * W : WS;
+        float* const sml_base = reinterpret_cast<float*>(smem);
+        float* const sacc_base = sml_base + ((a.ng * H * 2 + 3) & ~3);
+        float* gml = direct ? a.part_ml + (size_t)pslot * 2 : sml_base + (size_t)grp * H * 2;
+        float* gacc = direct ? a.part_acc + (size_t)pslot * W : sacc_base + (size_t)grp * H * WS;
         if (tq == 0) {
             if (hA < H) *reinterpret_cast<float2*>(gml + hA * hs_ml) = make_float2(m0, l0);
             if (hB < H) *reinterpret_cast<float2*>(gml + hB * hs_ml) = make_float2(m1, l1);
@@ -737,30 +745,52 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
         if (!direct) {
+            // Merge the groups' states per head: first each head's merged (M, L) and every
+            // group's weight 2^(m_g - M) (0 for a group that saw no token), then the
+            // accumulators, four columns per thread, with all groups' loads issued together.
             named_bar(1, nct);
-            const float* sml = reinterpret_cast<const float*>(smem);
-            const float* sacc = sml + (size_t)a.ng * H * 2;
+            const int ng = a.ng;
+            const float* sml = sml_base;
+            const float* sacc = sacc_base;
+            float* swt = sacc_base + (size_t)ng * H * WS;  // [group][head] weights
             float* pml = a.part_ml + (size_t)pslot * 2;
             float* pacc = a.part_acc + (size_t)pslot * W;
             for (int h = threadIdx.x; h < H; h += nct) {
-                float M = -INFINITY, Ls = 0.f;
-                for (int gg = 0; gg < a.ng; ++gg) M = fmaxf(M, sml[(gg * H + h) * 2]);
-                for (int gg = 0; gg < a.ng; ++gg) {
-                    const float mg = sml[(gg * H + h) * 2];
-                    Ls += (mg == -INFINITY) ? 0.f : exp2f(mg - M) * sml[(gg * H + h) * 2 + 1];
+                float mg[kMaxGroups];
+                float M = -INFINITY;
+#pragma unroll
+                for (int gg = 0; gg < kMaxGroups; ++gg) {
+                    mg[gg] = gg < ng ? sml[(gg * H + h) * 2] : -INFINITY;
+                    M = fmaxf(M, mg[gg]);
+                }
+                float Ls = 0.f;
+#pragma unroll
+                for (int gg = 0; gg < kMaxGroups; ++gg) {
+                    if (gg < ng) {
+                        const float wg = (mg[gg] == -INFINITY) ? 0.f : exp2f(mg[gg] - M);
+                        swt[gg * H + h] = wg;
+                        Ls = fmaf(wg, sml[(gg * H + h) * 2 + 1], Ls);
+                    }
                 }
                 *reinterpret_cast<float2*>(pml + (size_t)h * a.pmax * 2) = make_float2(M, Ls);
             }
-            for (int idx = threadIdx.x; idx < H * W; idx += nct) {
-                const int h = idx / W, c = idx - (idx / W) * W;
-                float M = -INFINITY;
-                for (int gg = 0; gg < a.ng; ++gg) M = fmaxf(M, sml[(gg * H + h) * 2]);
-                float v = 0.f;
-                for (int gg = 0; gg < a.ng; ++gg) {
-                    const float mg = sml[(gg * H + h) * 2];
-                    if (mg != -INFINITY) v = fmaf(exp2f(mg - M), sacc[(size_t)gg * H * W + idx], v);
+            named_bar(1, nct);
+            constexpr int W4 = W / 4;
+            for (int i4 = threadIdx.x; i4 < H * W4; i4 += nct) {
+                const int h = i4 / W4, c4 = i4 - h * W4;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int gg = 0; gg < kMaxGroups; ++gg) {
+                    if (gg < ng) {
+                        const float4 x = *reinterpret_cast<const float4*>(sacc + ((size_t)gg * H + h) * WS + c4 * 4);
+                        const float wg = swt[gg * H + h];
+                        v.x = fmaf(wg, x.x, v.x);
+                        v.y = fmaf(wg, x.y, v.y);
+                        v.z = fmaf(wg, x.z, v.z);
+                        v.w = fmaf(wg, x.w, v.w);
+                    }
                 }
-                pacc[(size_t)h * a.pmax * W + c] = v;
+                *reinterpret_cast<float4*>(pacc + (size_t)h * a.pmax * W + c4 * 4) = v;
             }
         }
     }
@@ -777,16 +807,16 @@ __global__ void __launch_bounds__(256, 1)
 
 // ------------------------------------------------------------------ kernel 2
 // Log-sum-exp merge of a sequence's partials, residual up-projection, bf16 store.
-// grid (H, layers * B), blockDim = NSL partial slices x W columns, NSL <= 1024 / W chosen
+// grid (H, layers * B), blockDim = NSL partial slices x W columns, NSL <= 512 / W chosen
 // on the host so that the grid is about one wave (many (head, sequence) pairs get small
 // blocks, several per SM; few pairs get many slices each).  Each slice merges
 // its own partials (all loads issued together), then the slices are merged in
 // shared memory; the B_h^V row of each output column is prefetched up front.
 template <int D_H, int R>
-__global__ void __launch_bounds__(1024) decode_combine_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(512) decode_combine_kernel(const DecodeArgs a) {
     constexpr int W = D_H + R;
-    constexpr int NSL_MAX = 1024 / W;  // slices at most
-    constexpr int PPS = 8;             // partials a slice loads per round
+    constexpr int NSL_MAX = 512 / W;   // slices at most
+    constexpr int PPS = 24;            // partials a slice loads per round (one round for most sequences)
     const int NSL = blockDim.x / W;    // slices of this launch
     const int h = blockIdx.x, vb = blockIdx.y, tid = threadIdx.x;
     const int ly = vb / a.B, bb = vb - (vb / a.B) * a.B;
@@ -908,8 +938,9 @@ DecodePlan decode_plan(int H, int D_H, int R, int D_R, int smem_limit) {
     while (nslot > 2 && nslot * p.stage_bytes + decode_fixed_smem(8, nslot) > smem_limit) --nslot;
     p.nslot = nslot;
     int ng = max(1, min(8 / HT, nslot - 2));
-    // the group merge reuses the ring: ng * H * (D_H + R + 2) floats must fit in it
-    while (ng > 1 && (size_t)ng * H * (D_H + R + 2) * 4 > (size_t)nslot * p.stage_bytes) --ng;
+    // the group merge reuses the ring: ng * H * (WS + 3) floats (+ 3 of alignment) must fit in it
+    const int WS = decode_stage_stride(D_H + R);
+    while (ng > 1 && ((size_t)ng * H * (WS + 3) + 3) * 4 > (size_t)nslot * p.stage_bytes) --ng;
     p.ng = ng;
     p.threads = 32 * HT * ng;
     p.smem_bytes = nslot * p.stage_bytes + decode_fixed_smem(HT * ng, nslot);
@@ -977,7 +1008,7 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
     // Slices per (head, sequence): enough threads for about one wave of the GPU in total.
     constexpr int W = D_H + R;
     const long long pairs = (long long)a.H * nvb;
-    const int nsl = (int)max(1LL, min((long long)(1024 / W), ((long long)sms * 1024) / max(1LL, pairs * W)));
+    const int nsl = (int)max(1LL, min((long long)(512 / W), ((long long)sms * 1024) / max(1LL, pairs * W)));
     return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, nvb), dim3(nsl * W), 0, stream, a);
 }
 

@@ -150,6 +150,11 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, i
 }
 
 // Prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+// Fetch a tensor map (a kernel parameter) into the descriptor cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }

@@ -159,6 +159,8 @@ size_t lrkv_decode_workspace_bytes(const lrkv_dims* dims, int32_t batch);
  *   seq_lens    [batch] int32 (device)
  *   out         [batch][H][d_h]
  *   workspace   device scratch of >= lrkv_decode_workspace_bytes(dims, batch) bytes, 256-byte aligned.
+ *   Capacity of one call: batch x max_blocks_per_seq x block_size below 2^34 tokens (times
+ *   num_layers for lrkv_decode_layers); larger calls return LRKV_ERR_INVALID_ARG.
  */
 lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, const void* BV,
                         const lrkv_cache* cache, const int32_t* block_table, int32_t max_blocks_per_seq,
