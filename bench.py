@@ -804,11 +804,14 @@ def run_gpu(args, world, rank, local):
         hz = HARNESS[args.workload](wl, rank)
     stream = torch.cuda.current_stream()
 
-    # Each timed step is one replay of a CUDA graph of the public calls, so host
-    # launch overhead stays out of the device-timed region; a second graph per copy holds
-    # only the dominant call (lrkv_decode / lrkv_prefill / ...) for the roofline.  The
-    # per-step data comes in independent copies replayed round-robin (Rotating), so no
-    # timed step or call reads inputs that the previous one left in L2.
+    # The timed steps are CUDA graphs of the public calls, so host launch overhead stays out
+    # of the device-timed region; a second set of graphs holds only the dominant call
+    # (lrkv_decode / lrkv_prefill / ...) for the roofline.  The per-step data comes in
+    # independent copies used round-robin (Rotating), so no timed step or call reads inputs
+    # that the previous one left in L2.  One graph per copy holds one step; one "cycle" graph
+    # holds one step on every copy in turn, so that K steps are K / copies cycle replays (plus
+    # single-step replays for the remainder) and the gap between two graph launches is paid
+    # once per cycle, not once per step.
     n_copies = args.copies or hz.copies_needed()
     hz.add_copies(n_copies)
     for k in range(n_copies):
@@ -820,6 +823,7 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     g_step = [torch.cuda.CUDAGraph() for _ in range(n_copies)]
     g_ker = [torch.cuda.CUDAGraph() for _ in range(n_copies)]
+    g_step_cycle, g_ker_cycle = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
     cap.wait_stream(stream)
     with torch.cuda.stream(cap):
@@ -829,30 +833,52 @@ def run_gpu(args, world, rank, local):
                 hz.step(cap)
             with torch.cuda.graph(g_ker[k], stream=cap):
                 hz.kernel(cap)
+        with torch.cuda.graph(g_step_cycle, stream=cap):
+            for k in range(n_copies):
+                hz.use(k)
+                hz.step(cap)
+        with torch.cuda.graph(g_ker_cycle, stream=cap):
+            for k in range(n_copies):
+                hz.use(k)
+                hz.kernel(cap)
+        # the same number of steps on copy 0 alone, back to back (for the L2-warm figures)
+        hz.use(0)
+        g_step_warm, g_ker_warm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step_warm, stream=cap):
+            for k in range(n_copies):
+                hz.step(cap)
+        with torch.cuda.graph(g_ker_warm, stream=cap):
+            for k in range(n_copies):
+                hz.kernel(cap)
     hz.use(0)
     stream.wait_stream(cap)
     torch.cuda.synchronize()
 
-    def timed(graphs, reps):
-        """Seconds per replay over `reps` replays of `graphs` round-robin (CUDA events)."""
+    def timed_steps(cycle, singles, steps):
+        """Seconds per step over exactly `steps` steps on the copies in turn: steps // copies
+        replays of the cycle graph, then single-step graphs for the remainder (CUDA events)."""
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
-        for i in range(reps):
-            graphs[i % len(graphs)].replay()
+        for _ in range(steps // n_copies):
+            cycle.replay()
+        for k in range(steps % n_copies):
+            singles[k].replay()
         ev1.record(stream)
         torch.cuda.synchronize()
-        return ev0.elapsed_time(ev1) * 1e-3 / reps
+        return ev0.elapsed_time(ev1) * 1e-3 / steps
 
     sampler = ClockSampler(local)
     sampler.start()
     for i in range(max(args.warmup, 3)):
         g_step[i % n_copies].replay()
+    for g in (g_step_cycle, g_ker_cycle, g_step_warm, g_ker_warm):
+        g.replay()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    step_s = timed(g_step, args.steps)
+    step_s = timed_steps(g_step_cycle, g_step, args.steps)
     t_wall1 = time.time()
     if dist:
         dist.barrier()
@@ -866,11 +892,11 @@ def run_gpu(args, world, rank, local):
         evs[i + 1].record(stream)
     torch.cuda.synchronize()
     per_step_ms = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(nd))
-    kernel_s = timed(g_ker, args.steps)
+    kernel_s = timed_steps(g_ker_cycle, g_ker, args.steps)
     # the same graphs on one copy back to back: whatever of its inputs stays in L2 between
     # replays is served from there (reported beside the rotated numbers, not as them)
-    kernel_warm_s = timed(g_ker[:1], args.steps)
-    step_warm_s = timed(g_step[:1], args.steps)
+    kernel_warm_s = timed_steps(g_ker_warm, [g_ker[0]] * n_copies, args.steps)
+    step_warm_s = timed_steps(g_step_warm, [g_step[0]] * n_copies, args.steps)
     if int(hz.status.item()) != 0:
         raise RuntimeError(f"device status {int(hz.status.item()):#x}")
 
@@ -908,8 +934,10 @@ def run_gpu(args, world, rank, local):
     line["step_ms_spread"] = {"median": statistics.median(per_step_ms), "min": per_step_ms[0],
                               "max": per_step_ms[-1], "reps": nd}
     line["gpu_launches"] = hz.launches_per_step * args.steps
-    line["timing"] = ("each step is one replay of a CUDA graph of the public calls, the graphs of independent "
-                      "input copies replayed round-robin (see config.l2_rotation); CUDA events on the stream")
+    line["timing"] = ("each step is one pass of the public calls on its own copy of the inputs, the copies used "
+                      "round-robin (see config.l2_rotation); one CUDA graph holds one step on every copy in turn and "
+                      "is replayed steps // copies times, single-step graphs take the remainder; CUDA events on the "
+                      "stream")
     line["config"]["l2"] = "rotated input copies (no step reads inputs the previous step left in L2): " + \
         line["config"].get("l2", "")
     line["config"]["l2_rotation"] = hz.rotation_config()

@@ -267,7 +267,8 @@ struct SplitCtl {
 };
 constexpr int kCtlBytes = 256;
 static_assert(sizeof(SplitCtl) <= kCtlBytes, "control block");
-constexpr int kPlanAlone = 32;  // batches up to this size are planned by one thread
+constexpr int kBtPrefetchEntries = 1 << 14;  // block tables up to this many entries are prefetched into L2
+constexpr int kFillAlone = 8;                 // ring fills of up to this many stages are issued by one thread
 
 // Cooperative copy of the first kSeqCache lengths (caller synchronises afterwards).
 __device__ __forceinline__ void stage_seq_lens(int* dst, const int32_t* src, int B, int tid, int nthreads) {
@@ -337,6 +338,8 @@ __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) 
 // s^K (with k^R when D_R > 0) and s^V by one TMA tensor copy each (128-byte swizzle; the map
 // views a row as 64-column parts 128 bytes apart, so one box brings all parts of the 8 rows),
 // z^K, z^V by bulk copies.  An out-of-range block id is reported and the stage is marked empty.
+// (One thread issues all four: spreading them over four lanes of the refilling warp made each
+// refill cheaper but the H = 128 decode slower as a whole.)
 template <int D_H, int R, int D_R>
 __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUtensorMap* tm_sV, const DecodeArgs& a,
                                             uint32_t st, uint32_t bar, int* meta_slot, int l, int blk, int gi,
@@ -413,21 +416,23 @@ __global__ void __launch_bounds__(256, 1)
         fence_mbar_init();
     }
     stage_seq_lens(slc, a.seq_lens, a.B, threadIdx.x, blockDim.x);
+    // The block table is read right after the plan: start bringing it into L2.
+    if ((size_t)a.B * a.max_pages <= kBtPrefetchEntries)
+        for (int off = threadIdx.x * 32; off < a.B * a.max_pages; off += blockDim.x * 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.block_table + off));
     __syncthreads();
 
+    const uint64_t pol = policy_evict_first();
+    // Warp 0 plans the work (lanes over the sequences) and steps to this CTA's first segment.
     if (warp == 0) {
         Work w{a.seq_lens, slc, a.B, a.layers, a.max_pages * kBlockSize, a.nranges, 0, 0, 1, 0};
-        if (a.B > kPlanAlone)
-            w.plan<32>(a.bubble, lane);
-        else if (lane == 0)
-            w.plan<1>(a.bubble, 0);
+        w.plan<32>(a.bubble, lane);
         if (lane == 0) {
             ctl->wk = w;
             ctl->walk.start(blockIdx.x);
             ctl->advance(a.seg_table);
         }
     }
-    const uint64_t pol = policy_evict_first();
 
     const int grp = warp / HT, ht = warp % HT;
     const int h0 = ht * 16;
@@ -460,18 +465,23 @@ __global__ void __launch_bounds__(256, 1)
         for (int i = threadIdx.x; i < kPageCache && pg0 + i < a.max_pages; i += nct) pages[i] = bt_row[pg0 + i];
         fence_proxy_async_smem();  // generic accesses of the ring (merge) before async-proxy refills
         named_bar(1, nct);
-        if (threadIdx.x == 0) {
-            if (!*abort_flag) {
-                for (int k = 0; k < min(nslot, nst); ++k) {
-                    const int slot = (kbase + k) % nslot;
-                    const int pi = ((sg0 + k) >> 3) - pg0;
-                    tag[slot] = kbase + k;
-                    issue_stage<D_H, R, D_R>(&tm_sK, &tm_sV, a, smem_s + slot * stage_bytes, smem_u32(&full[slot]),
-                                             &meta[slot], l, pi < kPageCache ? pages[pi] : bt_row[pg0 + pi],
-                                             sg0 + k, pol);
-                    ++nissued[slot];
-                }
+        // Fill the ring.  A copy instruction costs its thread ~60-80 ns (~0.4 us a stage), so a
+        // long fill (many small stages) is spread over the warps, stage k by warp k mod NCW;
+        // a short one stays with thread 0, which measured faster there.
+        const int nfill = min(nslot, nst);
+        const int fstep = nfill > kFillAlone ? NCW : 1;
+        if (lane == 0 && (fstep > 1 || warp == 0) && !*abort_flag) {
+            for (int k = warp; k < nfill; k += fstep) {
+                const int slot = (kbase + k) % nslot;
+                const int pi = ((sg0 + k) >> 3) - pg0;
+                tag[slot] = kbase + k;
+                issue_stage<D_H, R, D_R>(&tm_sK, &tm_sV, a, smem_s + slot * stage_bytes, smem_u32(&full[slot]),
+                                         &meta[slot], l, pi < kPageCache ? pages[pi] : bt_row[pg0 + pi],
+                                         sg0 + k, pol);
+                ++nissued[slot];
             }
+        }
+        if (threadIdx.x == 0) {
             // every thread has read this segment's descriptor (before the barrier above):
             // step to the next one while this one streams (after an expired wait too, so
             // that the walk ends)
@@ -565,15 +575,19 @@ __global__ void __launch_bounds__(256, 1)
             const uint8_t* zV_p = zK_p + 16 * H * R;
 
             // --- shared logits [q | q^R] . [s^K | k^R] (tensor cores): 16 heads x 8 tokens
+            // (two accumulators, even and odd 16-wide k chunks, halve the dependent MMA chain)
             float c[4] = {0.f, 0.f, 0.f, 0.f};
+            float c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk2 = 0; kk2 < D_K / 16; kk2 += 2) {
                 const int chunk16 = kk2 * 2 + (lane >> 3);
                 uint32_t b0, b1, b2, b3;
                 ldmatrix_x4(sw128(sK_s + (chunk16 >> 3) * 1024, lane & 7, chunk16 & 7), b0, b1, b2, b3);
                 mma_16816(c, qa[kk2], b0, b1);
-                mma_16816(c, qa[kk2 + 1], b2, b3);
+                mma_16816(c2, qa[kk2 + 1], b2, b3);
             }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[i] += c2[i];
 
             // --- residual logits q~ . z^K (CUDA cores): lane = (head hz, tokens half*4 .. +3)
 #pragma unroll
@@ -807,30 +821,33 @@ __global__ void __launch_bounds__(256, 1)
 
 // ------------------------------------------------------------------ kernel 2
 // Log-sum-exp merge of a sequence's partials, residual up-projection, bf16 store.
-// grid (H, layers * B), blockDim = NSL partial slices x W columns, NSL <= 512 / W chosen
-// on the host so that the grid is about one wave (many (head, sequence) pairs get small
-// blocks, several per SM; few pairs get many slices each).  Each slice merges
-// its own partials (all loads issued together), then the slices are merged in
-// shared memory; the B_h^V row of each output column is prefetched up front.
+// grid (H, layers * B); block = NSL partial slices x W/4 column quads, one float4 of the
+// accumulator row per thread.  NSL (at least ceil(D_H / (W/4)), so that every output column
+// has a thread) is chosen on the host so that the grid is about one wave and most slices hold
+// at most PPS partials: each slice merges its partials with all loads of a round issued
+// together, then the slices are merged in shared memory; B_h^V rows are prefetched up front.
 template <int D_H, int R>
-__global__ void __launch_bounds__(512) decode_combine_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(512, 2) decode_combine_kernel(const DecodeArgs a) {
     constexpr int W = D_H + R;
-    constexpr int NSL_MAX = 512 / W;   // slices at most
-    constexpr int PPS = 24;            // partials a slice loads per round (one round for most sequences)
-    const int NSL = blockDim.x / W;    // slices of this launch
+    constexpr int W4 = W / 4;
+    constexpr int NSL_MAX = 512 / W4;  // slices at most
+    constexpr int PPS = 6;             // partials a slice loads per round
+    const int NSL = blockDim.x / W4;   // slices of this launch
     const int h = blockIdx.x, vb = blockIdx.y, tid = threadIdx.x;
     const int ly = vb / a.B, bb = vb - (vb / a.B) * a.B;
     const int H = a.H;
     __shared__ float sm_m[NSL_MAX], sm_l[NSL_MAX];
-    __shared__ float sm_acc[NSL_MAX][W];
-    const int sl = tid / W, c = tid - (tid / W) * W;
+    __shared__ __align__(16) float sm_acc[NSL_MAX][W];
+    __shared__ __align__(16) uint16_t sm_bv[D_H * R];  // B_h^V
+    const int sl = tid / W4, c4 = tid - (tid / W4) * W4;
 
-    // B_h^V row of output column c (prefetched while the partials are loaded)
-    uint4 bvr[R / 8];
-    if (tid < D_H && !a.fused_out) {  // (no B^V in the fused form)
-        const uint4* bv = reinterpret_cast<const uint4*>(a.BV + ly * a.ls_BV + ((size_t)h * D_H + tid) * R);
-#pragma unroll
-        for (int i = 0; i < R / 8; ++i) bvr[i] = __ldg(bv + i);
+    // B_h^V, copied into shared memory asynchronously while the partials are loaded
+    if (!a.fused_out) {  // (no B^V in the fused form)
+        const uint16_t* bv = a.BV + ly * a.ls_BV + (size_t)h * D_H * R;
+        for (int i = tid; i < D_H * R / 8; i += blockDim.x)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sm_bv + i * 8)), "l"(bv + i * 8)
+                         : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
     const int L = a.seq_lens[bb];
     pdl_wait();
@@ -838,25 +855,27 @@ __global__ void __launch_bounds__(512) decode_combine_kernel(const DecodeArgs a)
     uint16_t* dst = a.out + ly * a.ls_out + ((size_t)bb * H + h) * OW;
     if (L < 1 || L > a.max_pages * kBlockSize) {
         if (tid == 0 && h == 0) set_status(a.status, LRKV_DEV_BAD_SEQLEN);
-        if (tid < OW) dst[tid] = 0;
+        for (int i = tid; i < OW; i += blockDim.x) dst[i] = 0;
+        asm volatile("cp.async.wait_all;" ::: "memory");
         return;
     }
     // partial slots first .. first + np - 1, recorded by the split kernel
     const int2 fe = a.seg_table[vb];
     const int first = fe.x, np = fe.y;
     const float* pml = a.part_ml + ((size_t)h * a.pmax + first) * 2;
-    const float* pacc = a.part_acc + ((size_t)h * a.pmax + first) * W;
+    const float4* pacc = reinterpret_cast<const float4*>(a.part_acc + ((size_t)h * a.pmax + first) * W);
 
-    if (sl < NSL) {
-        float m = -INFINITY, l = 0.f, v = 0.f;
+    {
+        float m = -INFINITY, l = 0.f;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int p0 = sl; p0 < np; p0 += NSL * PPS) {
             float2 ml[PPS];
-            float x[PPS];
+            float4 x[PPS];
 #pragma unroll
             for (int u = 0; u < PPS; ++u) {
                 const int p = p0 + u * NSL;
                 ml[u] = p < np ? *reinterpret_cast<const float2*>(pml + 2 * p) : make_float2(-INFINITY, 0.f);
-                x[u] = p < np ? pacc[(size_t)p * W + c] : 0.f;
+                x[u] = p < np ? pacc[(size_t)p * W4 + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             float mn = m;
 #pragma unroll
@@ -864,45 +883,63 @@ __global__ void __launch_bounds__(512) decode_combine_kernel(const DecodeArgs a)
             if (mn != -INFINITY) {
                 const float sc = (m == -INFINITY) ? 0.f : exp2f(m - mn);
                 l *= sc;
-                v *= sc;
+                v.x *= sc;
+                v.y *= sc;
+                v.z *= sc;
+                v.w *= sc;
 #pragma unroll
                 for (int u = 0; u < PPS; ++u) {
                     const float w = (ml[u].x == -INFINITY) ? 0.f : exp2f(ml[u].x - mn);
                     l = fmaf(w, ml[u].y, l);
-                    v = fmaf(w, x[u], v);
+                    v.x = fmaf(w, x[u].x, v.x);
+                    v.y = fmaf(w, x[u].y, v.y);
+                    v.z = fmaf(w, x[u].z, v.z);
+                    v.w = fmaf(w, x[u].w, v.w);
                 }
                 m = mn;
             }
         }
-        sm_acc[sl][c] = v;
-        if (c == 0) {
+        *reinterpret_cast<float4*>(&sm_acc[sl][c4 * 4]) = v;
+        if (c4 == 0) {
             sm_m[sl] = m;
             sm_l[sl] = l;
         }
     }
     __syncthreads();
-    if (tid < W) {
+    if (tid < W4) {
         float M = -INFINITY;
-#pragma unroll
         for (int i = 0; i < NSL; ++i) M = fmaxf(M, sm_m[i]);  // (NSL is known at run time only)
-        float lsum = 0.f, v = 0.f;
-#pragma unroll
+        float lsum = 0.f;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int i = 0; i < NSL; ++i) {
             const float w = (sm_m[i] == -INFINITY) ? 0.f : exp2f(sm_m[i] - M);
+            const float4 x = *reinterpret_cast<const float4*>(&sm_acc[i][tid * 4]);
             lsum = fmaf(w, sm_l[i], lsum);
-            v = fmaf(w, sm_acc[i][tid], v);
+            v.x = fmaf(w, x.x, v.x);
+            v.y = fmaf(w, x.y, v.y);
+            v.z = fmaf(w, x.z, v.z);
+            v.w = fmaf(w, x.w, v.w);
         }
-        // each thread reads only its own column, so slice 0's slot can take the result
-        sm_acc[0][tid] = lsum > 0.f ? v / lsum : 0.f;
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const float4 r = lsum > 0.f ? make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        // each thread reads only its own quad, so slice 0's slot can take the result
+        *reinterpret_cast<float4*>(&sm_acc[0][tid * 4]) = r;
         if (a.fused_out) {  // [o_s | o_z] / l: the B^V up-projection belongs to the caller's W^O
-            const __nv_bfloat16 ob = __float2bfloat16_rn(sm_acc[0][tid]);
-            dst[tid] = *reinterpret_cast<const uint16_t*>(&ob);
+            const float rr[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const __nv_bfloat16 ob = __float2bfloat16_rn(rr[k]);
+                dst[tid * 4 + k] = *reinterpret_cast<const uint16_t*>(&ob);
+            }
         }
     }
     if (a.fused_out) return;
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     if (tid < D_H) {
         float v = sm_acc[0][tid];
+        const uint4* bvr = reinterpret_cast<const uint4*>(sm_bv + tid * R);
 #pragma unroll
         for (int i = 0; i < R / 8; ++i) {
             const uint4 q = bvr[i];
@@ -1005,11 +1042,14 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
         e = launch_pdl(split, dim3(grid), dim3(p.threads), p.smem_bytes, stream, tK, tV, a);
     }
     if (e != cudaSuccess) return e;
-    // Slices per (head, sequence): enough threads for about one wave of the GPU in total.
-    constexpr int W = D_H + R;
+    // Slices per (head, sequence): enough threads for about one wave of the GPU in total, and at
+    // least one thread per output column.
+    constexpr int W4 = (D_H + R) / 4;
     const long long pairs = (long long)a.H * nvb;
-    const int nsl = (int)max(1LL, min((long long)(512 / W), ((long long)sms * 1024) / max(1LL, pairs * W)));
-    return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, nvb), dim3(nsl * W), 0, stream, a);
+    const int nsl_min = (D_H + W4 - 1) / W4;
+    const int nsl = (int)max((long long)nsl_min,
+                             min((long long)(512 / W4), ((long long)sms * 1024) / max(1LL, pairs * W4)));
+    return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, nvb), dim3(nsl * W4), 0, stream, a);
 }
 
 cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int D_R,
