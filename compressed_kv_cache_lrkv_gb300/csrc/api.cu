@@ -189,6 +189,29 @@ lrkv_status make_tmap_rows(CUtensorMap* m, const void* base, uint64_t cols, uint
     return LRKV_OK;
 }
 
+// 4-D map of a latent pool [layers][rows][H][r] viewed as {128, H r / 128, rows, layers} (a token's
+// latents for all heads cut into 256-byte pieces) with box {128, hl r / 128, 8, 1}: one copy brings
+// the latents of hl consecutive heads (a whole number of pieces) for 8 tokens, landing as
+// [token][head][r].  (Boxes one head's r values wide made 32-byte rows, which the copy engine
+// moved far more slowly.)
+lrkv_status make_tmap_z(CUtensorMap* m, const void* base, uint64_t H, uint64_t r, uint64_t rows, uint64_t layers,
+                        uint64_t layer_pitch, uint32_t hl, const char* what) {
+    auto enc = encode_fn();
+    if (!enc) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    if ((H * r) % 128 != 0 || ((uint64_t)hl * r) % 128 != 0)
+        return fail(LRKV_ERR_UNSUPPORTED, "%s: head group of %u x r %llu is not a whole number of 128-element pieces",
+                    what, hl, (unsigned long long)r);
+    cuuint64_t dims[4] = {128, H * r / 128, rows, layers};
+    cuuint64_t strides[3] = {256, H * r * 2, layers > 1 ? layer_pitch : H * r * 2 * rows};
+    cuuint32_t box[4] = {128, (cuuint32_t)(hl * r / 128), 8, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult res = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS) return fail(LRKV_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)res);
+    return LRKV_OK;
+}
+
 // A per-layer stride (elements) of a layer-batched call: at least the layer's own extent (layers
 // do not overlap) and a multiple of 8 elements (16 bytes).  Unused when num_layers == 1.
 lrkv_status check_stride(int64_t stride, uint64_t extent, int32_t num_layers, const char* what) {
@@ -424,6 +447,20 @@ static lrkv_status decode_impl(const lrkv_dims* dims, int32_t num_layers, const 
     if ((s = make_tmap_rows(&tV, cache->sV, dims->d_h, rows, num_layers, num_layers > 1 ? (uint64_t)ls->sV * 2 : 0,
                             8, "sV")) != LRKV_OK)
         return s;
+    if (!lrkv::decode_fits(dims->H, dims->d_h, dims->r, dims->d_rope, di.smem_optin))
+        return fail(LRKV_ERR_UNSUPPORTED, "H %d x r %d: the decode's shared-memory stages do not fit on this device",
+                    dims->H, dims->r);
+    // Several head groups: each CTA copies its group's latent slice with a tensor map.
+    const int nhg = lrkv::decode_head_groups(dims->H, dims->r);
+    CUtensorMap tZK{}, tZV{};
+    if (nhg > 1) {
+        const uint32_t hl = (uint32_t)(dims->H / nhg);
+        if ((s = make_tmap_z(&tZK, cache->zK, dims->H, dims->r, rows, num_layers,
+                             num_layers > 1 ? (uint64_t)ls->zK * 2 : 0, hl, "zK")) != LRKV_OK ||
+            (s = make_tmap_z(&tZV, cache->zV, dims->H, dims->r, rows, num_layers,
+                             num_layers > 1 ? (uint64_t)ls->zV * 2 : 0, hl, "zV")) != LRKV_OK)
+            return s;
+    }
 
     a.q = static_cast<const uint16_t*>(q);
     a.BK = static_cast<const uint16_t*>(BK);
@@ -444,7 +481,9 @@ static lrkv_status decode_impl(const lrkv_dims* dims, int32_t num_layers, const 
     a.wait_ns = decode_wait_limit_ns();
     a.scale_log2 = logit_scale(dims) * 1.4426950408889634f;
     lrkv::decode_carve_workspace(&a, workspace, dims->H, dims->d_h, dims->r, nvb, nranges);
-    return cuda_status(lrkv::launch_decode(tK, tV, a, dims->d_h, dims->r, dims->d_rope, di.sms, di.smem_optin,
+    a.nhg = nhg;
+    return cuda_status(lrkv::launch_decode(tK, tV, tZK, tZV, a, dims->d_h, dims->r, dims->d_rope, di.sms,
+                                           di.smem_optin,
                                            static_cast<cudaStream_t>(stream)),
                        fused ? "lrkv_decode_fused launch" : "lrkv_decode launch");
 }

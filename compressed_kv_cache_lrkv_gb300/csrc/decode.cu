@@ -50,7 +50,9 @@ __host__ __device__ constexpr int decode_stage_stride(int W) { return (W % 16 ==
 
 // The work of a decode call: nvb = layers * B virtual sequences vb = layer * B + b (all
 // layers share the block table and lengths), each cut into 8-token granules, T granules in
-// all, scanned by `nranges` CTA-sized pieces of work.  Two ways to cut, chosen identically by
+// all, scanned by `nranges` CTA-sized pieces of work.  With head groups every (layer,
+// sequence) pair appears as `groups` consecutive virtual sequences, one per group of heads
+// (Work::B then counts groups x sequences per layer).  Two ways to cut, chosen identically by
 // every CTA (plan()):
 //  - pieces: every sequence is cut into ceil(gr / chunk) near-equal pieces, with the smallest
 //    chunk for which all pieces number at most nranges; each piece is one segment with its
@@ -77,8 +79,12 @@ struct Work {
     int chunk;         // pieces: largest piece, in granules
     int per_layer_pieces;
     int rq, rr;        // ranges: T / nranges and T mod nranges
+    int lgh;           // log2 of the head groups: entry b of a layer is sequence b >> lgh
 
-    __device__ __forceinline__ int len(int b) const { return b < kSeqCache ? s[b] : g[b]; }
+    __device__ __forceinline__ int len(int b) const {
+        const int q = b >> lgh;
+        return q < kSeqCache ? s[q] : g[q];
+    }
     // Granules of sequence b, or 0 when its length is outside [1, cap].
     __device__ __forceinline__ int gran_b(int b) const {
         const int L = len(b);
@@ -269,6 +275,10 @@ constexpr int kCtlBytes = 256;
 static_assert(sizeof(SplitCtl) <= kCtlBytes, "control block");
 constexpr int kBtPrefetchEntries = 1 << 14;  // block tables up to this many entries are prefetched into L2
 constexpr int kFillAlone = 8;                 // ring fills of up to this many stages are issued by one thread
+// A stage carries the latents of every head the CTA scans (two tensors, 8 tokens); up to this
+// many elements per token (64 KB a stage) all heads are scanned together, beyond it the heads
+// are split into groups scanned by different CTAs (else fewer than three stages would fit).
+constexpr int kGroupLatents = 2048;
 
 // Cooperative copy of the first kSeqCache lengths (caller synchronises afterwards).
 __device__ __forceinline__ void stage_seq_lens(int* dst, const int32_t* src, int B, int tid, int nthreads) {
@@ -340,10 +350,13 @@ __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) 
 // z^K, z^V by bulk copies.  An out-of-range block id is reported and the stage is marked empty.
 // (One thread issues all four: spreading them over four lanes of the refilling warp made each
 // refill cheaper but the H = 128 decode slower as a whole.)
-template <int D_H, int R, int D_R>
-__device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUtensorMap* tm_sV, const DecodeArgs& a,
+// With head groups, z^K and z^V of the group's HL heads come by one tensor copy each (the 8
+// tokens' slices of HL r elements, in 256-byte pieces, landing as [token][head][r]).
+template <int D_H, int R, int D_R, bool HG>
+__device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUtensorMap* tm_sV,
+                                            const CUtensorMap* tm_zK, const CUtensorMap* tm_zV, const DecodeArgs& a,
                                             uint32_t st, uint32_t bar, int* meta_slot, int l, int blk, int gi,
-                                            uint64_t pol) {
+                                            int hbase, int HL, uint64_t pol, uint64_t pol_s) {
     if (blk < 0 || blk >= a.num_blocks) {
         set_status(a.status, LRKV_DEV_BAD_BLOCK);
         *meta_slot = 0;
@@ -352,14 +365,21 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUte
     }
     *meta_slot = 1;
     constexpr int D_K = D_H + D_R;
-    mbar_arrive_expect_tx(bar, 16u * (D_K + D_H) + 32u * a.H * R);
+    mbar_arrive_expect_tx(bar, 16u * (D_K + D_H) + 32u * HL * R);
     const int row = blk * kBlockSize + ((gi & 7) << 3);
     // one copy per shared part: the 8 rows' 64-column parts land as [part][row][64], 1 KB per part
-    tma_load_4d_hint(st, tm_sK, 0, row, 0, l, bar, pol);
-    tma_load_4d_hint(st + 16 * D_K, tm_sV, 0, row, 0, l, bar, pol);
-    const size_t zoff = (size_t)row * a.H * R;
-    bulk_load_hint(st + 16 * (D_K + D_H), a.zK + l * a.ls_zK + zoff, 16u * a.H * R, bar, pol);
-    bulk_load_hint(st + 16 * (D_K + D_H) + 16 * a.H * R, a.zV + l * a.ls_zV + zoff, 16u * a.H * R, bar, pol);
+    tma_load_4d_hint(st, tm_sK, 0, row, 0, l, bar, pol_s);
+    tma_load_4d_hint(st + 16 * D_K, tm_sV, 0, row, 0, l, bar, pol_s);
+    const uint32_t zst = st + 16 * (D_K + D_H);
+    if (HG && a.nhg > 1) {
+        const int piece = hbase * R / 128;  // the group's first 128-element piece of a token's latents
+        tma_load_4d_hint(zst, tm_zK, 0, piece, row, l, bar, pol);
+        tma_load_4d_hint(zst + 16 * HL * R, tm_zV, 0, piece, row, l, bar, pol);
+    } else {
+        const size_t zoff = (size_t)row * a.H * R;
+        bulk_load_hint(zst, a.zK + l * a.ls_zK + zoff, 16u * a.H * R, bar, pol);
+        bulk_load_hint(zst + 16 * a.H * R, a.zV + l * a.ls_zV + zoff, 16u * a.H * R, bar, pol);
+    }
 }
 
 // ------------------------------------------------------------------ kernel 1
@@ -367,9 +387,10 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUte
 // hold up to 255 registers.  There is no dedicated producer warp: thread 0
 // fills the ring at the start of each segment, and afterwards the last warp to
 // release a stage refills that slot with the stage nslot positions ahead.
-template <int D_H, int R, int D_R>
+template <int D_H, int R, int D_R, bool HG>
 __global__ void __launch_bounds__(256, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_sK, const __grid_constant__ CUtensorMap tm_sV,
+                        const __grid_constant__ CUtensorMap tm_zK, const __grid_constant__ CUtensorMap tm_zV,
                         const DecodeArgs a) {
     static_assert(D_H == 64 || D_H == 128, "d_h");
     static_assert(D_R == 0 || D_R == 64, "d_rope");
@@ -385,8 +406,12 @@ __global__ void __launch_bounds__(256, 1)
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
     const uint32_t smem_s = smem_u32(smem);
 
-    const int H = a.H;
-    const int HT = (H + 15) >> 4;
+    const int H = a.H;                                           // all heads (global layouts)
+    // head groups (HG: compiled only where they can occur; without them the group terms fold away)
+    const int nhg = HG ? a.nhg : 1;
+    const int lgh = nhg == 8 ? 3 : nhg == 4 ? 2 : nhg == 2 ? 1 : 0;
+    const int HL = H >> lgh;                                     // heads of one group: this CTA's share
+    const int HT = (HL + 15) >> 4;
     const int NCW = HT * a.ng;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nslot = a.nslot;
@@ -406,6 +431,10 @@ __global__ void __launch_bounds__(256, 1)
     if (threadIdx.x == 0) {
         prefetch_tmap(&tm_sK);
         prefetch_tmap(&tm_sV);
+        if (nhg > 1) {
+            prefetch_tmap(&tm_zK);
+            prefetch_tmap(&tm_zV);
+        }
         for (int s = 0; s < nslot; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             rel[s] = 0;
@@ -423,9 +452,12 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
 
     const uint64_t pol = policy_evict_first();
+    // the shared rows are read by every head group's CTA: not evict-first then
+    const uint64_t pol_s = nhg > 1 ? policy_evict_normal() : pol;
     // Warp 0 plans the work (lanes over the sequences) and steps to this CTA's first segment.
     if (warp == 0) {
-        Work w{a.seq_lens, slc, a.B, a.layers, a.max_pages * kBlockSize, a.nranges, 0, 0, 1, 0};
+        Work w{a.seq_lens, slc, a.B << lgh, a.layers, a.max_pages * kBlockSize, a.nranges, 0, 0, 1, 0};
+        w.lgh = lgh;
         w.plan<32>(a.bubble, lane);
         if (lane == 0) {
             ctl->wk = w;
@@ -439,7 +471,7 @@ __global__ void __launch_bounds__(256, 1)
     const int g = lane >> 2, tq = lane & 3;
     const int hz = lane & 15, half = lane >> 4;
     const int hzh = h0 + hz;
-    const bool hz_ok = hzh < H;
+    const bool hz_ok = hzh < HL;
     const int rot = (hz / RP128) % NC;
     float* SZ = scratch + warp * kScratchFloats;
     float* SP = SZ + 128;
@@ -456,7 +488,9 @@ __global__ void __launch_bounds__(256, 1)
         named_bar(1, nct);
         if (!ctl->valid) break;
         const int vb = ctl->vb, sg0 = ctl->g0, sg1 = ctl->g1, pslot = ctl->slot;
-        const int l = vb / a.B, bb = vb - (vb / a.B) * a.B;
+        const int vbr = vb >> lgh;                       // the (layer, sequence) pair
+        const int hbase = (vb & (nhg - 1)) * HL;         // first head of this segment's group
+        const int l = vbr / a.B, bb = vbr - (vbr / a.B) * a.B;
         const int L = bb < kSeqCache ? slc[bb] : a.seq_lens[bb];
         const int nst = sg1 - sg0;
         const int pg0 = sg0 >> 3;
@@ -475,9 +509,10 @@ __global__ void __launch_bounds__(256, 1)
                 const int slot = (kbase + k) % nslot;
                 const int pi = ((sg0 + k) >> 3) - pg0;
                 tag[slot] = kbase + k;
-                issue_stage<D_H, R, D_R>(&tm_sK, &tm_sV, a, smem_s + slot * stage_bytes, smem_u32(&full[slot]),
-                                         &meta[slot], l, pi < kPageCache ? pages[pi] : bt_row[pg0 + pi],
-                                         sg0 + k, pol);
+                issue_stage<D_H, R, D_R, HG>(&tm_sK, &tm_sV, &tm_zK, &tm_zV, a, smem_s + slot * stage_bytes,
+                                         smem_u32(&full[slot]), &meta[slot], l,
+                                         pi < kPageCache ? pages[pi] : bt_row[pg0 + pi], sg0 + k, hbase, HL, pol,
+                                         pol_s);
                 ++nissued[slot];
             }
         }
@@ -497,7 +532,7 @@ __global__ void __launch_bounds__(256, 1)
         float qt[R];
         if (a.qt_in) {
             const uint4* qrow = reinterpret_cast<const uint4*>(a.qt_in + l * a.ls_qt +
-                                                                 ((size_t)bb * H + (hz_ok ? hzh : 0)) * R);
+                                                                 ((size_t)bb * H + hbase + (hz_ok ? hzh : 0)) * R);
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) {
                 const uint4 x = qrow[(cc + rot) % NC];
@@ -511,7 +546,7 @@ __global__ void __launch_bounds__(256, 1)
                 qt[cc * 8 + 7] = hz_ok ? bf16hi(x.w) : 0.f;
             }
         } else {
-            const float* qrow = a.qt + ((size_t)vb * H + (hz_ok ? hzh : 0)) * R;
+            const float* qrow = a.qt + ((size_t)vbr * H + hbase + (hz_ok ? hzh : 0)) * R;
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) {
                 const float4* src = reinterpret_cast<const float4*>(qrow + ((cc + rot) % NC) * 8);
@@ -531,14 +566,14 @@ __global__ void __launch_bounds__(256, 1)
         uint32_t qa[D_K / 16][4];
         {
             const uint16_t* qbase = a.q + l * a.ls_q;
-            const uint32_t* qA = reinterpret_cast<const uint32_t*>(qbase + ((size_t)bb * H + hA) * D_K);
-            const uint32_t* qB = reinterpret_cast<const uint32_t*>(qbase + ((size_t)bb * H + hB) * D_K);
+            const uint32_t* qA = reinterpret_cast<const uint32_t*>(qbase + ((size_t)bb * H + hbase + hA) * D_K);
+            const uint32_t* qB = reinterpret_cast<const uint32_t*>(qbase + ((size_t)bb * H + hbase + hB) * D_K);
 #pragma unroll
             for (int kk = 0; kk < D_K / 16; ++kk) {
-                qa[kk][0] = hA < H ? qA[kk * 8 + tq] : 0u;
-                qa[kk][1] = hB < H ? qB[kk * 8 + tq] : 0u;
-                qa[kk][2] = hA < H ? qA[kk * 8 + 4 + tq] : 0u;
-                qa[kk][3] = hB < H ? qB[kk * 8 + 4 + tq] : 0u;
+                qa[kk][0] = hA < HL ? qA[kk * 8 + tq] : 0u;
+                qa[kk][1] = hB < HL ? qB[kk * 8 + tq] : 0u;
+                qa[kk][2] = hA < HL ? qA[kk * 8 + 4 + tq] : 0u;
+                qa[kk][3] = hB < HL ? qB[kk * 8 + 4 + tq] : 0u;
             }
         }
 
@@ -572,7 +607,7 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t st = smem_s + slot * stage_bytes;
             const uint32_t sK_s = st, sV_s = st + 16 * D_K;
             const uint8_t* zK_p = smem + slot * stage_bytes + 16 * (D_K + D_H);
-            const uint8_t* zV_p = zK_p + 16 * H * R;
+            const uint8_t* zV_p = zK_p + 16 * HL * R;
 
             // --- shared logits [q | q^R] . [s^K | k^R] (tensor cores): 16 heads x 8 tokens
             // (two accumulators, even and odd 16-wide k chunks, halve the dependent MMA chain)
@@ -595,7 +630,7 @@ __global__ void __launch_bounds__(256, 1)
                 const int t = half * 4 + i;
                 float acc = 0.f;
                 if (hz_ok && t < nvalid) {
-                    const uint4* row = reinterpret_cast<const uint4*>(zK_p + ((size_t)t * H + hzh) * R * 2);
+                    const uint4* row = reinterpret_cast<const uint4*>(zK_p + ((size_t)t * HL + hzh) * R * 2);
 #pragma unroll
                     for (int cc = 0; cc < NC; ++cc) {
                         const uint4 v = row[(cc + rot) % NC];
@@ -662,7 +697,7 @@ __global__ void __launch_bounds__(256, 1)
                     const int t = half * 4 + i;
                     if (hz_ok && t < nvalid) {
                         const float p = SP[sidx(hz, t)];
-                        const uint4* row = reinterpret_cast<const uint4*>(zV_p + ((size_t)t * H + hzh) * R * 2);
+                        const uint4* row = reinterpret_cast<const uint4*>(zV_p + ((size_t)t * HL + hzh) * R * 2);
 #pragma unroll
                         for (int cc = 0; cc < NC; ++cc) {
                             const uint4 v = row[(cc + rot) % NC];
@@ -708,8 +743,9 @@ __global__ void __launch_bounds__(256, 1)
                     if (jn < nst && !*abort_flag) {
                         const int pi = ((sg0 + jn) >> 3) - pg0;
                         tag[slot] = kk + nslot;
-                        issue_stage<D_H, R, D_R>(&tm_sK, &tm_sV, a, st, smem_u32(&full[slot]), &meta[slot], l,
-                                                 pi < kPageCache ? pages[pi] : bt_row[pg0 + pi], sg0 + jn, pol);
+                        issue_stage<D_H, R, D_R, HG>(&tm_sK, &tm_sV, &tm_zK, &tm_zV, a, st, smem_u32(&full[slot]),
+                                                 &meta[slot], l, pi < kPageCache ? pages[pi] : bt_row[pg0 + pi],
+                                                 sg0 + jn, hbase, HL, pol, pol_s);
                         ++nissued[slot];
                     }
                 }
@@ -736,18 +772,20 @@ __global__ void __launch_bounds__(256, 1)
         const size_t hs_ml = direct ? (size_t)a.pmax * 2 : 2;     // stride between heads
         const size_t hs_acc = direct ? (size_t)a.pmax * W : WS;
         float* const sml_base = reinterpret_cast<float*>(smem);
-        float* const sacc_base = sml_base + ((a.ng * H * 2 + 3) & ~3);
-        float* gml = direct ? a.part_ml + (size_t)pslot * 2 : sml_base + (size_t)grp * H * 2;
-        float* gacc = direct ? a.part_acc + (size_t)pslot * W : sacc_base + (size_t)grp * H * WS;
+        float* const sacc_base = sml_base + ((a.ng * HL * 2 + 3) & ~3);
+        // (workspace rows are indexed by the global head, the staging by the group's own)
+        float* gml = direct ? a.part_ml + (size_t)pslot * 2 + (size_t)hbase * hs_ml : sml_base + (size_t)grp * HL * 2;
+        float* gacc = direct ? a.part_acc + (size_t)pslot * W + (size_t)hbase * hs_acc
+                             : sacc_base + (size_t)grp * HL * WS;
         if (tq == 0) {
-            if (hA < H) *reinterpret_cast<float2*>(gml + hA * hs_ml) = make_float2(m0, l0);
-            if (hB < H) *reinterpret_cast<float2*>(gml + hB * hs_ml) = make_float2(m1, l1);
+            if (hA < HL) *reinterpret_cast<float2*>(gml + hA * hs_ml) = make_float2(m0, l0);
+            if (hB < HL) *reinterpret_cast<float2*>(gml + hB * hs_ml) = make_float2(m1, l1);
         }
 #pragma unroll
         for (int n = 0; n < D_H / 8; ++n) {
             const int dcol = n * 8 + 2 * tq;
-            if (hA < H) *reinterpret_cast<float2*>(gacc + (size_t)hA * hs_acc + dcol) = make_float2(o[n][0], o[n][1]);
-            if (hB < H) *reinterpret_cast<float2*>(gacc + (size_t)hB * hs_acc + dcol) = make_float2(o[n][2], o[n][3]);
+            if (hA < HL) *reinterpret_cast<float2*>(gacc + (size_t)hA * hs_acc + dcol) = make_float2(o[n][0], o[n][1]);
+            if (hB < HL) *reinterpret_cast<float2*>(gacc + (size_t)hB * hs_acc + dcol) = make_float2(o[n][2], o[n][3]);
         }
         if (half == 0 && hz_ok) {
             float* dst = gacc + (size_t)hzh * hs_acc + D_H;
@@ -766,15 +804,15 @@ __global__ void __launch_bounds__(256, 1)
             const int ng = a.ng;
             const float* sml = sml_base;
             const float* sacc = sacc_base;
-            float* swt = sacc_base + (size_t)ng * H * WS;  // [group][head] weights
-            float* pml = a.part_ml + (size_t)pslot * 2;
-            float* pacc = a.part_acc + (size_t)pslot * W;
-            for (int h = threadIdx.x; h < H; h += nct) {
+            float* swt = sacc_base + (size_t)ng * HL * WS;  // [group][head] weights
+            float* pml = a.part_ml + (size_t)pslot * 2 + (size_t)hbase * a.pmax * 2;
+            float* pacc = a.part_acc + (size_t)pslot * W + (size_t)hbase * a.pmax * W;
+            for (int h = threadIdx.x; h < HL; h += nct) {
                 float mg[kMaxGroups];
                 float M = -INFINITY;
 #pragma unroll
                 for (int gg = 0; gg < kMaxGroups; ++gg) {
-                    mg[gg] = gg < ng ? sml[(gg * H + h) * 2] : -INFINITY;
+                    mg[gg] = gg < ng ? sml[(gg * HL + h) * 2] : -INFINITY;
                     M = fmaxf(M, mg[gg]);
                 }
                 float Ls = 0.f;
@@ -782,22 +820,22 @@ __global__ void __launch_bounds__(256, 1)
                 for (int gg = 0; gg < kMaxGroups; ++gg) {
                     if (gg < ng) {
                         const float wg = (mg[gg] == -INFINITY) ? 0.f : exp2f(mg[gg] - M);
-                        swt[gg * H + h] = wg;
-                        Ls = fmaf(wg, sml[(gg * H + h) * 2 + 1], Ls);
+                        swt[gg * HL + h] = wg;
+                        Ls = fmaf(wg, sml[(gg * HL + h) * 2 + 1], Ls);
                     }
                 }
                 *reinterpret_cast<float2*>(pml + (size_t)h * a.pmax * 2) = make_float2(M, Ls);
             }
             named_bar(1, nct);
             constexpr int W4 = W / 4;
-            for (int i4 = threadIdx.x; i4 < H * W4; i4 += nct) {
+            for (int i4 = threadIdx.x; i4 < HL * W4; i4 += nct) {
                 const int h = i4 / W4, c4 = i4 - h * W4;
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int gg = 0; gg < kMaxGroups; ++gg) {
                     if (gg < ng) {
-                        const float4 x = *reinterpret_cast<const float4*>(sacc + ((size_t)gg * H + h) * WS + c4 * 4);
-                        const float wg = swt[gg * H + h];
+                        const float4 x = *reinterpret_cast<const float4*>(sacc + ((size_t)gg * HL + h) * WS + c4 * 4);
+                        const float wg = swt[gg * HL + h];
                         v.x = fmaf(wg, x.x, v.x);
                         v.y = fmaf(wg, x.y, v.y);
                         v.z = fmaf(wg, x.z, v.z);
@@ -860,7 +898,7 @@ __global__ void __launch_bounds__(512, 2) decode_combine_kernel(const DecodeArgs
         return;
     }
     // partial slots first .. first + np - 1, recorded by the split kernel
-    const int2 fe = a.seg_table[vb];
+    const int2 fe = a.seg_table[vb * a.nhg + h / (H / a.nhg)];
     const int first = fe.x, np = fe.y;
     const float* pml = a.part_ml + ((size_t)h * a.pmax + first) * 2;
     const float4* pacc = reinterpret_cast<const float4*>(a.part_acc + ((size_t)h * a.pmax + first) * W);
@@ -967,8 +1005,16 @@ static int decode_fixed_smem(int ncw, int nslot) {
            kCtlBytes + 1024;  // (the abort flag; the control block; alignment of the ring)
 }
 
-DecodePlan decode_plan(int H, int D_H, int R, int D_R, int smem_limit) {
+int decode_head_groups(int H, int R) {
+    if (H * R <= kGroupLatents) return 1;
+    for (int g = 2; g <= 8; g *= 2)
+        if (H % g == 0 && (H / g) * R <= kGroupLatents && ((H / g) * R) % 128 == 0) return g;
+    return 1;
+}
+
+DecodePlan decode_plan(int H_all, int D_H, int R, int D_R, int smem_limit) {
     DecodePlan p{};
+    const int H = H_all / decode_head_groups(H_all, R);  // heads of one CTA's group
     const int HT = (H + 15) / 16;
     p.stage_bytes = ((16 * (2 * D_H + D_R) + 32 * H * R) + 1023) & ~1023;
     int nslot = 16;
@@ -986,14 +1032,20 @@ DecodePlan decode_plan(int H, int D_H, int R, int D_R, int smem_limit) {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+bool decode_fits(int H, int D_H, int R, int D_R, int smem_limit) {
+    const DecodePlan p = decode_plan(H, D_H, R, D_R, smem_limit);
+    return p.smem_bytes <= smem_limit;
+}
+
 size_t decode_workspace_bytes(int H, int D_H, int R, int nvb, int nranges) {
-    const size_t pmax = (size_t)nvb + (size_t)nranges;
+    const size_t nseg = (size_t)nvb * decode_head_groups(H, R);  // virtual sequences of the scan
+    const size_t pmax = nseg + (size_t)nranges;
     return align256(pmax * H * 2 * sizeof(float)) + align256(pmax * H * (D_H + R) * sizeof(float)) +
-           align256((size_t)nvb * H * R * sizeof(float)) + align256((size_t)nvb * sizeof(int2));
+           align256((size_t)nvb * H * R * sizeof(float)) + align256(nseg * sizeof(int2));
 }
 
 void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int nvb, int nranges) {
-    const size_t pmax = (size_t)nvb + (size_t)nranges;
+    const size_t pmax = (size_t)nvb * decode_head_groups(H, R) + (size_t)nranges;
     uint8_t* base = static_cast<uint8_t*>(ws);
     a->part_ml = reinterpret_cast<float*>(base);
     base += align256(pmax * H * 2 * sizeof(float));
@@ -1022,9 +1074,15 @@ static cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size
 }
 
 template <int D_H, int R, int D_R>
-static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, const DecodePlan& p,
-                                   int sms, cudaStream_t stream) {
-    auto split = decode_split_kernel<D_H, R, D_R>;
+static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV, const CUtensorMap& tZK,
+                                   const CUtensorMap& tZV, DecodeArgs a, const DecodePlan& p, int sms,
+                                   cudaStream_t stream) {
+    // Head groups occur only where a token's latents for all heads exceed kGroupLatents elements,
+    // which with H <= 128 needs r = 32.
+    auto split = decode_split_kernel<D_H, R, D_R, false>;
+    if constexpr (R * 128 > kGroupLatents) {
+        if (a.nhg > 1) split = decode_split_kernel<D_H, R, D_R, true>;
+    }
     cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
     const int nvb = a.layers * a.B;
@@ -1033,13 +1091,13 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
         // q~ comes from the caller: no absorb kernel, and the split is an ordinary launch --
         // a dependent launch could start streaming the cache before the caller's previous
         // kernel on this stream (an append of the newest rows) has finished.
-        split<<<grid, p.threads, p.smem_bytes, stream>>>(tK, tV, a);
+        split<<<grid, p.threads, p.smem_bytes, stream>>>(tK, tV, tZK, tZV, a);
         e = cudaGetLastError();
     } else {
         decode_absorb_kernel<D_H, R, D_R><<<dim3(a.H, nvb), 256, 0, stream>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        e = launch_pdl(split, dim3(grid), dim3(p.threads), p.smem_bytes, stream, tK, tV, a);
+        e = launch_pdl(split, dim3(grid), dim3(p.threads), p.smem_bytes, stream, tK, tV, tZK, tZV, a);
     }
     if (e != cudaSuccess) return e;
     // Slices per (head, sequence): enough threads for about one wave of the GPU in total, and at
@@ -1052,8 +1110,9 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
     return launch_pdl(decode_combine_kernel<D_H, R>, dim3(a.H, nvb), dim3(nsl * W4), 0, stream, a);
 }
 
-cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int D_R,
-                          int sms, int smem_limit, cudaStream_t stream) {
+cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, const CUtensorMap& tZK,
+                          const CUtensorMap& tZV, DecodeArgs a, int D_H, int R, int D_R, int sms, int smem_limit,
+                          cudaStream_t stream) {
     const DecodePlan p = decode_plan(a.H, D_H, R, D_R, smem_limit);
     a.ng = p.ng;
     a.nslot = p.nslot;
@@ -1063,8 +1122,8 @@ cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeAr
     a.bubble = ((128 << 10) + p.stage_bytes - 1) / p.stage_bytes;
 #define LRKV_DEC(DH, RR)                                                                     \
     if (D_H == DH && R == RR)                                                                \
-        return D_R == 0 ? launch_decode_t<DH, RR, 0>(tK, tV, a, p, sms, stream)              \
-                        : launch_decode_t<DH, RR, 64>(tK, tV, a, p, sms, stream);
+        return D_R == 0 ? launch_decode_t<DH, RR, 0>(tK, tV, tZK, tZV, a, p, sms, stream)    \
+                        : launch_decode_t<DH, RR, 64>(tK, tV, tZK, tZV, a, p, sms, stream);
     LRKV_DEC(64, 8) LRKV_DEC(64, 16) LRKV_DEC(64, 32) LRKV_DEC(128, 8) LRKV_DEC(128, 16) LRKV_DEC(128, 32)
 #undef LRKV_DEC
     return cudaErrorInvalidValue;

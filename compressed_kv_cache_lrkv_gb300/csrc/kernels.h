@@ -51,7 +51,8 @@ struct DecodeArgs {
     int nranges;       // pieces of work the batch's cached tokens are cut into (CTA iterations)
     int bubble;        // granules a pipeline drain-and-refill costs (chooses how the work is cut)
     int ng, nslot, stage_bytes;
-    int pmax;          // partial slots per head in the workspace (layers * B + nranges)
+    int nhg;           // head groups: each (layer, sequence) is scanned as nhg virtual sequences of H / nhg heads
+    int pmax;          // partial slots per head in the workspace (layers * B * nhg + nranges)
     float scale_log2;  // softmax scale * log2(e)
     unsigned long long wait_ns;  // limit of the split kernel's pipeline waits (a debugging aid may shorten it)
 };
@@ -75,14 +76,23 @@ int append_tc_block_n(int N);
 cudaError_t launch_append_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const AppendArgs& a,
                              cudaStream_t stream);
 
-// Workspace of a decode over nvb = layers * B virtual sequences cut into `nranges` ranges.
+// Head groups of the decode scan: 1 while a stage's latents for all heads (8 tokens x H r
+// elements, two tensors) fit in 64 KB; else the fewest groups (2, 4 or 8, dividing H into
+// whole 128-element pieces of a token's latents) that bring a group's share within that.
+int decode_head_groups(int H, int R);
+// Whether the split kernel's shared-memory ring (at least two stages) fits in smem_limit bytes.
+bool decode_fits(int H, int D_H, int R, int D_R, int smem_limit);
+// Workspace of a decode over nvb = layers * B (layer, sequence) pairs cut into `nranges` ranges.
 size_t decode_workspace_bytes(int H, int D_H, int R, int nvb, int nranges);
 void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int nvb, int nranges);
 // tK, tV: 4-D maps {64, nb * 64, (d_h (+ d_rope)) / 64, layers}, box {64, 8, parts, 1}, 128-byte swizzle
-// (the parts dimension steps 128 bytes along a row).
+// (the parts dimension steps 128 bytes along a row).  tZK, tZV (used with several head groups):
+// 4-D maps {128, H r / 128, nb * 64, layers} of z^K, z^V, box {128, (H / groups) r / 128, 8, 1},
+// no swizzle.
 // The split kernel runs on min(nranges, sms) CTAs.
-cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, DecodeArgs a, int D_H, int R, int D_R,
-                          int sms, int smem_limit, cudaStream_t stream);
+cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, const CUtensorMap& tZK,
+                          const CUtensorMap& tZV, DecodeArgs a, int D_H, int R, int D_R, int sms, int smem_limit,
+                          cudaStream_t stream);
 
 cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, int D_R, cudaStream_t stream);
 

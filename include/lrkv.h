@@ -46,7 +46,8 @@
  * Supported shapes (others return LRKV_ERR_UNSUPPORTED):
  *   block_size == 64, d_h in {64, 128}, r in {8, 16, 32} with r <= d_h,
  *   1 <= H <= 128, d a positive multiple of 8 (of 64 for the tensor-core append),
- *   d_rope in {0, 64}.
+ *   d_rope in {0, 64}.  The decode calls with r = 32 and H >= 105 need H a multiple
+ *   of 8: a stage of the scan then holds the latents of a group of heads, not of all.
  */
 #ifndef LRKV_H
 #define LRKV_H

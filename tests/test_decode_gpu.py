@@ -44,6 +44,11 @@ SHAPES = [
     (20, 128, 16, [333, 1024]),             # H not a multiple of 16 (padded head rows)
     (3, 64, 32, [95]),                      # few heads
     (32, 128, 8, [513]),
+    # many heads (up to eight 16-head warp tiles per stage), ragged
+    (128, 128, 16, [1500, 9, 300]),
+    (128, 64, 32, [900, 130]),
+    (96, 128, 32, [600]),
+    (64, 128, 32, [1500, 70]),
 ]
 
 
@@ -62,6 +67,7 @@ LONG = [
     (32, 128, 32, [32768]),
     (32, 128, 32, [20000, 17000, 31000, 16384]),
     (128, 128, 16, [8192]),
+    (128, 128, 32, [9000, 2000]),
     (8, 64, 16, [40000]),
     (8, 64, 8, [25000, 3]),
 ]
@@ -226,3 +232,18 @@ def test_expired_wait_reports_timeout_and_gpu_stays_usable(monkeypatch):
     ref = oracle.get().decode_cache(pools, pt.block_table, pt.seq_lens, w.BK, w.BV, q, want=want)
     sel = want.astype(bool)
     assert_close(host_f64(out)[sel], ref[sel], "decode after an expired wait")
+
+
+def test_decode_rejects_head_counts_without_a_group_split():
+    """With r = 32 and H >= 105 a stage of all heads' latents does not fit twice in shared memory;
+    H a multiple of 8 is scanned in head groups, any other H is refused before any launch."""
+    for H, ok in [(109, False), (112, True)]:
+        pt, pools, w, q = decode_case(31 + H, H, 64, 32, [70])
+        if ok:
+            out, st = run_decode(H, 64, 32, pools, pt, q, w.BK, w.BV)
+            assert st == 0
+            ref = oracle.get().decode_cache(pools, pt.block_table, pt.seq_lens, w.BK, w.BV, q)
+            assert_close(host_f64(out), ref, f"decode H={H} r=32")
+        else:
+            with pytest.raises(b.LrkvError, match="do not fit"):
+                run_decode(H, 64, 32, pools, pt, q, w.BK, w.BV)
