@@ -441,11 +441,12 @@ static lrkv_status decode_impl(const lrkv_dims* dims, int32_t num_layers, const 
         return fail(LRKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
 
     CUtensorMap tK, tV;
-    if ((s = make_tmap_rows(&tK, cache->sK, dk, rows, num_layers, num_layers > 1 ? (uint64_t)ls->sK * 2 : 0, 8,
-                            "sK")) != LRKV_OK)
+    const uint32_t box_rows = 8u * lrkv::decode_stage_granules(dims->H, dims->d_h, dims->r, dims->d_rope);
+    if ((s = make_tmap_rows(&tK, cache->sK, dk, rows, num_layers, num_layers > 1 ? (uint64_t)ls->sK * 2 : 0,
+                            box_rows, "sK")) != LRKV_OK)
         return s;
     if ((s = make_tmap_rows(&tV, cache->sV, dims->d_h, rows, num_layers, num_layers > 1 ? (uint64_t)ls->sV * 2 : 0,
-                            8, "sV")) != LRKV_OK)
+                            box_rows, "sV")) != LRKV_OK)
         return s;
     if (!lrkv::decode_fits(dims->H, dims->d_h, dims->r, dims->d_rope, di.smem_optin))
         return fail(LRKV_ERR_UNSUPPORTED, "H %d x r %d: the decode's shared-memory stages do not fit on this device",

@@ -279,6 +279,10 @@ constexpr int kFillAlone = 8;                 // ring fills of up to this many s
 // many elements per token (64 KB a stage) all heads are scanned together, beyond it the heads
 // are split into groups scanned by different CTAs (else fewer than three stages would fit).
 constexpr int kGroupLatents = 2048;
+// Stages of one granule smaller than a quarter of this are made four granules (32 tokens) long:
+// a copy instruction costs its thread ~60-80 ns whatever its size, so small stages were bound by
+// the issue of their four copies.
+constexpr int kSmallStageBytes = 32 << 10;
 
 // Cooperative copy of the first kSeqCache lengths (caller synchronises afterwards).
 __device__ __forceinline__ void stage_seq_lens(int* dst, const int32_t* src, int B, int tid, int nthreads) {
@@ -344,7 +348,8 @@ __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) 
     }
 }
 
-// Issue the loads of one 8-token granule (stage) of block `blk` of layer `l` into a ring slot:
+// Issue the loads of one stage -- GS 8-token granules from granule gi (GS-aligned, inside one
+// page) -- of block `blk` of layer `l` into a ring slot:
 // s^K (with k^R when D_R > 0) and s^V by one TMA tensor copy each (128-byte swizzle; the map
 // views a row as 64-column parts 128 bytes apart, so one box brings all parts of the 8 rows),
 // z^K, z^V by bulk copies.  An out-of-range block id is reported and the stage is marked empty.
@@ -352,7 +357,7 @@ __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) 
 // refill cheaper but the H = 128 decode slower as a whole.)
 // With head groups, z^K and z^V of the group's HL heads come by one tensor copy each (the 8
 // tokens' slices of HL r elements, in 256-byte pieces, landing as [token][head][r]).
-template <int D_H, int R, int D_R, bool HG>
+template <int D_H, int R, int D_R, bool HG, int GS>
 __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUtensorMap* tm_sV,
                                             const CUtensorMap* tm_zK, const CUtensorMap* tm_zV, const DecodeArgs& a,
                                             uint32_t st, uint32_t bar, int* meta_slot, int l, int blk, int gi,
@@ -365,20 +370,20 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUte
     }
     *meta_slot = 1;
     constexpr int D_K = D_H + D_R;
-    mbar_arrive_expect_tx(bar, 16u * (D_K + D_H) + 32u * HL * R);
+    mbar_arrive_expect_tx(bar, GS * (16u * (D_K + D_H) + 32u * HL * R));
     const int row = blk * kBlockSize + ((gi & 7) << 3);
-    // one copy per shared part: the 8 rows' 64-column parts land as [part][row][64], 1 KB per part
+    // one copy per shared part: the 8 GS rows' 64-column parts land as [part][row][64], GS KB per part
     tma_load_4d_hint(st, tm_sK, 0, row, 0, l, bar, pol_s);
-    tma_load_4d_hint(st + 16 * D_K, tm_sV, 0, row, 0, l, bar, pol_s);
-    const uint32_t zst = st + 16 * (D_K + D_H);
-    if (HG && a.nhg > 1) {
+    tma_load_4d_hint(st + 16 * D_K * GS, tm_sV, 0, row, 0, l, bar, pol_s);
+    const uint32_t zst = st + 16 * GS * (D_K + D_H);
+    if (HG && a.nhg > 1) {  // (head groups come with one-granule stages)
         const int piece = hbase * R / 128;  // the group's first 128-element piece of a token's latents
         tma_load_4d_hint(zst, tm_zK, 0, piece, row, l, bar, pol);
         tma_load_4d_hint(zst + 16 * HL * R, tm_zV, 0, piece, row, l, bar, pol);
     } else {
         const size_t zoff = (size_t)row * a.H * R;
-        bulk_load_hint(zst, a.zK + l * a.ls_zK + zoff, 16u * a.H * R, bar, pol);
-        bulk_load_hint(zst + 16 * a.H * R, a.zV + l * a.ls_zV + zoff, 16u * a.H * R, bar, pol);
+        bulk_load_hint(zst, a.zK + l * a.ls_zK + zoff, 16u * GS * a.H * R, bar, pol);
+        bulk_load_hint(zst + 16 * GS * a.H * R, a.zV + l * a.ls_zV + zoff, 16u * GS * a.H * R, bar, pol);
     }
 }
 
@@ -387,7 +392,7 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tm_sK, const CUte
 // hold up to 255 registers.  There is no dedicated producer warp: thread 0
 // fills the ring at the start of each segment, and afterwards the last warp to
 // release a stage refills that slot with the stage nslot positions ahead.
-template <int D_H, int R, int D_R, bool HG>
+template <int D_H, int R, int D_R, bool HG, int GS>
 __global__ void __launch_bounds__(256, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_sK, const __grid_constant__ CUtensorMap tm_sV,
                         const __grid_constant__ CUtensorMap tm_zK, const __grid_constant__ CUtensorMap tm_zV,
@@ -492,7 +497,9 @@ __global__ void __launch_bounds__(256, 1)
         const int hbase = (vb & (nhg - 1)) * HL;         // first head of this segment's group
         const int l = vbr / a.B, bb = vbr - (vbr / a.B) * a.B;
         const int L = bb < kSeqCache ? slc[bb] : a.seq_lens[bb];
-        const int nst = sg1 - sg0;
+        // stages: GS-granule blocks, aligned in the sequence, that meet [sg0, sg1)
+        const int base0 = sg0 & ~(GS - 1);
+        const int nst = GS == 1 ? sg1 - sg0 : (sg1 - 1) / GS - sg0 / GS + 1;
         const int pg0 = sg0 >> 3;
         const int32_t* bt_row = a.block_table + (size_t)bb * a.max_pages;
 
@@ -507,12 +514,13 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0 && (fstep > 1 || warp == 0) && !*abort_flag) {
             for (int k = warp; k < nfill; k += fstep) {
                 const int slot = (kbase + k) % nslot;
-                const int pi = ((sg0 + k) >> 3) - pg0;
+                const int gk = base0 + k * GS;
+                const int pi = (gk >> 3) - pg0;
                 tag[slot] = kbase + k;
-                issue_stage<D_H, R, D_R, HG>(&tm_sK, &tm_sV, &tm_zK, &tm_zV, a, smem_s + slot * stage_bytes,
-                                         smem_u32(&full[slot]), &meta[slot], l,
-                                         pi < kPageCache ? pages[pi] : bt_row[pg0 + pi], sg0 + k, hbase, HL, pol,
-                                         pol_s);
+                issue_stage<D_H, R, D_R, HG, GS>(&tm_sK, &tm_sV, &tm_zK, &tm_zV, a, smem_s + slot * stage_bytes,
+                                                 smem_u32(&full[slot]), &meta[slot], l,
+                                                 pi < kPageCache ? pages[pi] : bt_row[pg0 + pi], gk, hbase, HL, pol,
+                                                 pol_s);
                 ++nissued[slot];
             }
         }
@@ -602,133 +610,141 @@ __global__ void __launch_bounds__(256, 1)
                 *abort_flag = 1;
                 continue;
             }
-            const int t0 = (sg0 + j) * kGran;
-            const int nvalid = meta[slot] ? min(kGran, L - t0) : 0;
             const uint32_t st = smem_s + slot * stage_bytes;
-            const uint32_t sK_s = st, sV_s = st + 16 * D_K;
-            const uint8_t* zK_p = smem + slot * stage_bytes + 16 * (D_K + D_H);
-            const uint8_t* zV_p = zK_p + 16 * HL * R;
+            const int gfirst = base0 + j * GS;  // the stage's first granule (GS-aligned)
+#pragma unroll 1
+            for (int sub = 0; sub < GS; ++sub) {
+                const int gi = gfirst + sub;
+                if (GS > 1 && (gi < sg0 || gi >= sg1)) continue;  // a granule of a neighbouring segment
+                const int t0 = gi * kGran;
+                const int nvalid = meta[slot] ? min(kGran, L - t0) : 0;
+                // granule `sub` of the stage: rows 8 sub .. 8 sub + 7 of every 64-column part (parts
+                // GS KB apart), tokens 8 sub .. 8 sub + 7 of the latents
+                const uint32_t sK_s = st + sub * 1024, sV_s = st + 16 * D_K * GS + sub * 1024;
+                const uint8_t* zK_p = smem + slot * stage_bytes + 16 * GS * (D_K + D_H) + sub * 16 * HL * R;
+                const uint8_t* zV_p = zK_p + 16 * GS * HL * R;
 
-            // --- shared logits [q | q^R] . [s^K | k^R] (tensor cores): 16 heads x 8 tokens
-            // (two accumulators, even and odd 16-wide k chunks, halve the dependent MMA chain)
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            float c2[4] = {0.f, 0.f, 0.f, 0.f};
+                // --- shared logits [q | q^R] . [s^K | k^R] (tensor cores): 16 heads x 8 tokens
+                // (two accumulators, even and odd 16-wide k chunks, halve the dependent MMA chain)
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                float c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int kk2 = 0; kk2 < D_K / 16; kk2 += 2) {
-                const int chunk16 = kk2 * 2 + (lane >> 3);
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(sw128(sK_s + (chunk16 >> 3) * 1024, lane & 7, chunk16 & 7), b0, b1, b2, b3);
-                mma_16816(c, qa[kk2], b0, b1);
-                mma_16816(c2, qa[kk2 + 1], b2, b3);
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) c[i] += c2[i];
-
-            // --- residual logits q~ . z^K (CUDA cores): lane = (head hz, tokens half*4 .. +3)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = half * 4 + i;
-                float acc = 0.f;
-                if (hz_ok && t < nvalid) {
-                    const uint4* row = reinterpret_cast<const uint4*>(zK_p + ((size_t)t * HL + hzh) * R * 2);
-#pragma unroll
-                    for (int cc = 0; cc < NC; ++cc) {
-                        const uint4 v = row[(cc + rot) % NC];
-                        acc = fmaf(qt[cc * 8 + 0], bf16lo(v.x), acc);
-                        acc = fmaf(qt[cc * 8 + 1], bf16hi(v.x), acc);
-                        acc = fmaf(qt[cc * 8 + 2], bf16lo(v.y), acc);
-                        acc = fmaf(qt[cc * 8 + 3], bf16hi(v.y), acc);
-                        acc = fmaf(qt[cc * 8 + 4], bf16lo(v.z), acc);
-                        acc = fmaf(qt[cc * 8 + 5], bf16hi(v.z), acc);
-                        acc = fmaf(qt[cc * 8 + 6], bf16lo(v.w), acc);
-                        acc = fmaf(qt[cc * 8 + 7], bf16hi(v.w), acc);
-                    }
+                for (int kk2 = 0; kk2 < D_K / 16; kk2 += 2) {
+                    const int chunk16 = kk2 * 2 + (lane >> 3);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(sw128(sK_s + (chunk16 >> 3) * (GS * 1024), lane & 7, chunk16 & 7), b0, b1, b2, b3);
+                    mma_16816(c, qa[kk2], b0, b1);
+                    mma_16816(c2, qa[kk2 + 1], b2, b3);
                 }
-                SZ[sidx(hz, t)] = acc;
-            }
-            __syncwarp();
-
-            // --- scores, mask, online softmax (rows hA: c0,c1; hB: c2,c3; tokens 2tq, 2tq+1)
-            const int ta = 2 * tq, tb = 2 * tq + 1;
-            float s0 = (ta < nvalid) ? (c[0] + SZ[sidx(g, ta)]) * a.scale_log2 : -INFINITY;
-            float s1 = (tb < nvalid) ? (c[1] + SZ[sidx(g, tb)]) * a.scale_log2 : -INFINITY;
-            float s2 = (ta < nvalid) ? (c[2] + SZ[sidx(g + 8, ta)]) * a.scale_log2 : -INFINITY;
-            float s3 = (tb < nvalid) ? (c[3] + SZ[sidx(g + 8, tb)]) * a.scale_log2 : -INFINITY;
-            float mx0 = fmaxf(s0, s1), mx1 = fmaxf(s2, s3);
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
-            const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
-            const float p0 = (mn0 == -INFINITY) ? 0.f : exp2f(s0 - mn0);
-            const float p1 = (mn0 == -INFINITY) ? 0.f : exp2f(s1 - mn0);
-            const float p2 = (mn1 == -INFINITY) ? 0.f : exp2f(s2 - mn1);
-            const float p3 = (mn1 == -INFINITY) ? 0.f : exp2f(s3 - mn1);
-            m0 = mn0;
-            m1 = mn1;
-            l0 = l0 * al0 + p0 + p1;
-            l1 = l1 * al1 + p2 + p3;
 #pragma unroll
-            for (int n = 0; n < D_H / 8; ++n) {
-                o[n][0] *= al0;
-                o[n][1] *= al0;
-                o[n][2] *= al1;
-                o[n][3] *= al1;
-            }
-            SP[sidx(g, ta)] = p0;
-            SP[sidx(g, tb)] = p1;
-            SP[sidx(g + 8, ta)] = p2;
-            SP[sidx(g + 8, tb)] = p3;
-            if (tq == 0) {
-                SA[g] = al0;
-                SA[g + 8] = al1;
-            }
-            __syncwarp();
+                for (int i = 0; i < 4; ++i) c[i] += c2[i];
 
-            // --- residual values p . z^V (CUDA cores)
-            {
-                const float al = SA[hz];
-#pragma unroll
-                for (int i = 0; i < R; ++i) accz[i] *= al;
+                // --- residual logits q~ . z^K (CUDA cores): lane = (head hz, tokens half*4 .. +3)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int t = half * 4 + i;
+                    float acc = 0.f;
                     if (hz_ok && t < nvalid) {
-                        const float p = SP[sidx(hz, t)];
-                        const uint4* row = reinterpret_cast<const uint4*>(zV_p + ((size_t)t * HL + hzh) * R * 2);
+                        const uint4* row = reinterpret_cast<const uint4*>(zK_p + ((size_t)t * HL + hzh) * R * 2);
 #pragma unroll
                         for (int cc = 0; cc < NC; ++cc) {
                             const uint4 v = row[(cc + rot) % NC];
-                            accz[cc * 8 + 0] = fmaf(p, bf16lo(v.x), accz[cc * 8 + 0]);
-                            accz[cc * 8 + 1] = fmaf(p, bf16hi(v.x), accz[cc * 8 + 1]);
-                            accz[cc * 8 + 2] = fmaf(p, bf16lo(v.y), accz[cc * 8 + 2]);
-                            accz[cc * 8 + 3] = fmaf(p, bf16hi(v.y), accz[cc * 8 + 3]);
-                            accz[cc * 8 + 4] = fmaf(p, bf16lo(v.z), accz[cc * 8 + 4]);
-                            accz[cc * 8 + 5] = fmaf(p, bf16hi(v.z), accz[cc * 8 + 5]);
-                            accz[cc * 8 + 6] = fmaf(p, bf16lo(v.w), accz[cc * 8 + 6]);
-                            accz[cc * 8 + 7] = fmaf(p, bf16hi(v.w), accz[cc * 8 + 7]);
+                            acc = fmaf(qt[cc * 8 + 0], bf16lo(v.x), acc);
+                            acc = fmaf(qt[cc * 8 + 1], bf16hi(v.x), acc);
+                            acc = fmaf(qt[cc * 8 + 2], bf16lo(v.y), acc);
+                            acc = fmaf(qt[cc * 8 + 3], bf16hi(v.y), acc);
+                            acc = fmaf(qt[cc * 8 + 4], bf16lo(v.z), acc);
+                            acc = fmaf(qt[cc * 8 + 5], bf16hi(v.z), acc);
+                            acc = fmaf(qt[cc * 8 + 6], bf16lo(v.w), acc);
+                            acc = fmaf(qt[cc * 8 + 7], bf16hi(v.w), acc);
+                        }
+                    }
+                    SZ[sidx(hz, t)] = acc;
+                }
+                __syncwarp();
+
+                // --- scores, mask, online softmax (rows hA: c0,c1; hB: c2,c3; tokens 2tq, 2tq+1)
+                const int ta = 2 * tq, tb = 2 * tq + 1;
+                float s0 = (ta < nvalid) ? (c[0] + SZ[sidx(g, ta)]) * a.scale_log2 : -INFINITY;
+                float s1 = (tb < nvalid) ? (c[1] + SZ[sidx(g, tb)]) * a.scale_log2 : -INFINITY;
+                float s2 = (ta < nvalid) ? (c[2] + SZ[sidx(g + 8, ta)]) * a.scale_log2 : -INFINITY;
+                float s3 = (tb < nvalid) ? (c[3] + SZ[sidx(g + 8, tb)]) * a.scale_log2 : -INFINITY;
+                float mx0 = fmaxf(s0, s1), mx1 = fmaxf(s2, s3);
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
+                const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
+                const float p0 = (mn0 == -INFINITY) ? 0.f : exp2f(s0 - mn0);
+                const float p1 = (mn0 == -INFINITY) ? 0.f : exp2f(s1 - mn0);
+                const float p2 = (mn1 == -INFINITY) ? 0.f : exp2f(s2 - mn1);
+                const float p3 = (mn1 == -INFINITY) ? 0.f : exp2f(s3 - mn1);
+                m0 = mn0;
+                m1 = mn1;
+                l0 = l0 * al0 + p0 + p1;
+                l1 = l1 * al1 + p2 + p3;
+#pragma unroll
+                for (int n = 0; n < D_H / 8; ++n) {
+                    o[n][0] *= al0;
+                    o[n][1] *= al0;
+                    o[n][2] *= al1;
+                    o[n][3] *= al1;
+                }
+                SP[sidx(g, ta)] = p0;
+                SP[sidx(g, tb)] = p1;
+                SP[sidx(g + 8, ta)] = p2;
+                SP[sidx(g + 8, tb)] = p3;
+                if (tq == 0) {
+                    SA[g] = al0;
+                    SA[g + 8] = al1;
+                }
+                __syncwarp();
+
+                // --- residual values p . z^V (CUDA cores)
+                {
+                    const float al = SA[hz];
+#pragma unroll
+                    for (int i = 0; i < R; ++i) accz[i] *= al;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int t = half * 4 + i;
+                        if (hz_ok && t < nvalid) {
+                            const float p = SP[sidx(hz, t)];
+                            const uint4* row = reinterpret_cast<const uint4*>(zV_p + ((size_t)t * HL + hzh) * R * 2);
+#pragma unroll
+                            for (int cc = 0; cc < NC; ++cc) {
+                                const uint4 v = row[(cc + rot) % NC];
+                                accz[cc * 8 + 0] = fmaf(p, bf16lo(v.x), accz[cc * 8 + 0]);
+                                accz[cc * 8 + 1] = fmaf(p, bf16hi(v.x), accz[cc * 8 + 1]);
+                                accz[cc * 8 + 2] = fmaf(p, bf16lo(v.y), accz[cc * 8 + 2]);
+                                accz[cc * 8 + 3] = fmaf(p, bf16hi(v.y), accz[cc * 8 + 3]);
+                                accz[cc * 8 + 4] = fmaf(p, bf16lo(v.z), accz[cc * 8 + 4]);
+                                accz[cc * 8 + 5] = fmaf(p, bf16hi(v.z), accz[cc * 8 + 5]);
+                                accz[cc * 8 + 6] = fmaf(p, bf16lo(v.w), accz[cc * 8 + 6]);
+                                accz[cc * 8 + 7] = fmaf(p, bf16hi(v.w), accz[cc * 8 + 7]);
+                            }
                         }
                     }
                 }
-            }
 
-            // --- shared values p . s^V (tensor cores): P (16 heads x 8 tokens) . s^V (8 tokens x D_H)
-            {
-                const uint32_t pa0 = pack_bf16x2(p0, p1), pa1 = pack_bf16x2(p2, p3);
-                const uint32_t mlo = (ta < nvalid) ? 0x0000ffffu : 0u;
-                const uint32_t mhi = (tb < nvalid) ? 0xffff0000u : 0u;
-                const uint32_t msk = mlo | mhi;  // zero s^V of masked tokens (0 * NaN guard)
+                // --- shared values p . s^V (tensor cores): P (16 heads x 8 tokens) . s^V (8 tokens x D_H)
+                {
+                    const uint32_t pa0 = pack_bf16x2(p0, p1), pa1 = pack_bf16x2(p2, p3);
+                    const uint32_t mlo = (ta < nvalid) ? 0x0000ffffu : 0u;
+                    const uint32_t mhi = (tb < nvalid) ? 0xffff0000u : 0u;
+                    const uint32_t msk = mlo | mhi;  // zero s^V of masked tokens (0 * NaN guard)
 #pragma unroll
-                for (int q4 = 0; q4 < D_H / 32; ++q4) {
-                    const int chunk16 = q4 * 4 + (lane >> 3);
-                    uint32_t v0, v1, v2, v3;
-                    ldmatrix_x4_trans(sw128(sV_s + (chunk16 >> 3) * 1024, lane & 7, chunk16 & 7), v0, v1, v2, v3);
-                    mma_1688(o[q4 * 4 + 0], pa0, pa1, v0 & msk);
-                    mma_1688(o[q4 * 4 + 1], pa0, pa1, v1 & msk);
-                    mma_1688(o[q4 * 4 + 2], pa0, pa1, v2 & msk);
-                    mma_1688(o[q4 * 4 + 3], pa0, pa1, v3 & msk);
+                    for (int q4 = 0; q4 < D_H / 32; ++q4) {
+                        const int chunk16 = q4 * 4 + (lane >> 3);
+                        uint32_t v0, v1, v2, v3;
+                        ldmatrix_x4_trans(sw128(sV_s + (chunk16 >> 3) * (GS * 1024), lane & 7, chunk16 & 7), v0, v1, v2, v3);
+                        mma_1688(o[q4 * 4 + 0], pa0, pa1, v0 & msk);
+                        mma_1688(o[q4 * 4 + 1], pa0, pa1, v1 & msk);
+                        mma_1688(o[q4 * 4 + 2], pa0, pa1, v2 & msk);
+                        mma_1688(o[q4 * 4 + 3], pa0, pa1, v3 & msk);
+                    }
                 }
             }
             __syncwarp();
@@ -741,11 +757,12 @@ __global__ void __launch_bounds__(256, 1)
                     __threadfence_block();
                     const int jn = j + nslot;
                     if (jn < nst && !*abort_flag) {
-                        const int pi = ((sg0 + jn) >> 3) - pg0;
+                        const int gn = base0 + jn * GS;
+                        const int pi = (gn >> 3) - pg0;
                         tag[slot] = kk + nslot;
-                        issue_stage<D_H, R, D_R, HG>(&tm_sK, &tm_sV, &tm_zK, &tm_zV, a, st, smem_u32(&full[slot]),
-                                                 &meta[slot], l, pi < kPageCache ? pages[pi] : bt_row[pg0 + pi],
-                                                 sg0 + jn, hbase, HL, pol, pol_s);
+                        issue_stage<D_H, R, D_R, HG, GS>(&tm_sK, &tm_sV, &tm_zK, &tm_zV, a, st, smem_u32(&full[slot]),
+                                                         &meta[slot], l, pi < kPageCache ? pages[pi] : bt_row[pg0 + pi],
+                                                         gn, hbase, HL, pol, pol_s);
                         ++nissued[slot];
                     }
                 }
@@ -997,7 +1014,7 @@ __global__ void __launch_bounds__(512, 2) decode_combine_kernel(const DecodeArgs
 
 // ------------------------------------------------------------------ host side
 struct DecodePlan {
-    int ng, nslot, stage_bytes, smem_bytes, threads;
+    int ng, nslot, stage_bytes, smem_bytes, threads, gpst;
 };
 
 static int decode_fixed_smem(int ncw, int nslot) {
@@ -1012,11 +1029,18 @@ int decode_head_groups(int H, int R) {
     return 1;
 }
 
+int decode_stage_granules(int H, int D_H, int R, int D_R) {
+    if (decode_head_groups(H, R) > 1) return 1;
+    const int gran_bytes = 16 * (2 * D_H + D_R) + 32 * H * R;
+    return 4 * gran_bytes <= kSmallStageBytes ? 4 : 1;
+}
+
 DecodePlan decode_plan(int H_all, int D_H, int R, int D_R, int smem_limit) {
     DecodePlan p{};
     const int H = H_all / decode_head_groups(H_all, R);  // heads of one CTA's group
     const int HT = (H + 15) / 16;
-    p.stage_bytes = ((16 * (2 * D_H + D_R) + 32 * H * R) + 1023) & ~1023;
+    p.gpst = decode_stage_granules(H_all, D_H, R, D_R);
+    p.stage_bytes = ((p.gpst * (16 * (2 * D_H + D_R) + 32 * H * R)) + 1023) & ~1023;
     int nslot = 16;
     while (nslot > 2 && nslot * p.stage_bytes + decode_fixed_smem(8, nslot) > smem_limit) --nslot;
     p.nslot = nslot;
@@ -1079,9 +1103,9 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
                                    cudaStream_t stream) {
     // Head groups occur only where a token's latents for all heads exceed kGroupLatents elements,
     // which with H <= 128 needs r = 32.
-    auto split = decode_split_kernel<D_H, R, D_R, false>;
+    auto split = a.gpst == 4 ? decode_split_kernel<D_H, R, D_R, false, 4> : decode_split_kernel<D_H, R, D_R, false, 1>;
     if constexpr (R * 128 > kGroupLatents) {
-        if (a.nhg > 1) split = decode_split_kernel<D_H, R, D_R, true>;
+        if (a.nhg > 1) split = decode_split_kernel<D_H, R, D_R, true, 1>;
     }
     cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
@@ -1117,9 +1141,10 @@ cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, const CU
     a.ng = p.ng;
     a.nslot = p.nslot;
     a.stage_bytes = p.stage_bytes;
+    a.gpst = p.gpst;
     // a pipeline drain and refill at a sequence boundary costs about as long as streaming
     // 128 KB through one SM (~3 us)
-    a.bubble = ((128 << 10) + p.stage_bytes - 1) / p.stage_bytes;
+    a.bubble = ((128 << 10) * p.gpst + p.stage_bytes - 1) / p.stage_bytes;  // (in granules)
 #define LRKV_DEC(DH, RR)                                                                     \
     if (D_H == DH && R == RR)                                                                \
         return D_R == 0 ? launch_decode_t<DH, RR, 0>(tK, tV, tZK, tZV, a, p, sms, stream)    \

@@ -52,6 +52,7 @@ struct DecodeArgs {
     int bubble;        // granules a pipeline drain-and-refill costs (chooses how the work is cut)
     int ng, nslot, stage_bytes;
     int nhg;           // head groups: each (layer, sequence) is scanned as nhg virtual sequences of H / nhg heads
+    int gpst;          // 8-token granules per pipeline stage (1 or 4)
     int pmax;          // partial slots per head in the workspace (layers * B * nhg + nranges)
     float scale_log2;  // softmax scale * log2(e)
     unsigned long long wait_ns;  // limit of the split kernel's pipeline waits (a debugging aid may shorten it)
@@ -80,12 +81,16 @@ cudaError_t launch_append_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, con
 // elements, two tensors) fit in 64 KB; else the fewest groups (2, 4 or 8, dividing H into
 // whole 128-element pieces of a token's latents) that bring a group's share within that.
 int decode_head_groups(int H, int R);
+// 8-token granules per stage of the decode scan (1, or 4 for small stages); the s^K, s^V maps'
+// box is 8 x this many rows.
+int decode_stage_granules(int H, int D_H, int R, int D_R);
 // Whether the split kernel's shared-memory ring (at least two stages) fits in smem_limit bytes.
 bool decode_fits(int H, int D_H, int R, int D_R, int smem_limit);
 // Workspace of a decode over nvb = layers * B (layer, sequence) pairs cut into `nranges` ranges.
 size_t decode_workspace_bytes(int H, int D_H, int R, int nvb, int nranges);
 void decode_carve_workspace(DecodeArgs* a, void* ws, int H, int D_H, int R, int nvb, int nranges);
-// tK, tV: 4-D maps {64, nb * 64, (d_h (+ d_rope)) / 64, layers}, box {64, 8, parts, 1}, 128-byte swizzle
+// tK, tV: 4-D maps {64, nb * 64, (d_h (+ d_rope)) / 64, layers}, box {64, 8 g, parts, 1} (g the stage's
+// granules), 128-byte swizzle
 // (the parts dimension steps 128 bytes along a row).  tZK, tZV (used with several head groups):
 // 4-D maps {128, H r / 128, nb * 64, layers} of z^K, z^V, box {128, (H / groups) r / 128, 8, 1},
 // no swizzle.

@@ -247,3 +247,16 @@ def test_decode_rejects_head_counts_without_a_group_split():
         else:
             with pytest.raises(b.LrkvError, match="do not fit"):
                 run_decode(H, 64, 32, pools, pt, q, w.BK, w.BV)
+
+
+@pytest.mark.parametrize("ns", [1, 3, 7, 13, 50, 0])
+def test_small_stages_with_segment_edges_inside_a_stage(ns):
+    """Small-head shapes stream four granules (32 tokens) per stage; with these split counts and
+    ragged lengths the pieces and ranges begin and end inside a stage, whose granules outside the
+    segment must be skipped."""
+    H, d_h, r = 8, 64, 16
+    pt, pools, w, q = decode_case(61, H, d_h, r, [2048, 1, 7, 65, 500, 333, 1000])
+    out, st = run_decode(H, d_h, r, pools, pt, q, w.BK, w.BV, num_splits=ns)
+    assert st == 0
+    ref = oracle.get().decode_cache(pools, pt.block_table, pt.seq_lens, w.BK, w.BV, q)
+    assert_close(host_f64(out), ref, f"decode H={H} num_splits={ns}")
