@@ -277,7 +277,8 @@ class DecodeHarness(Rotating):
 
     per_copy = ("cache", "q", "BK", "BV", "wcat", "x", "qt", "out")
     profile = "decode_split_longctx.md"
-    profiles = {"longctx": "decode_split_longctx.md", "dsv2": "decode_split_dsv2.md"}  # by workload
+    profiles = {"longctx": "decode_split_longctx.md", "dsv2": "decode_split_dsv2.md",
+                "backbone12": "decode_layers_backbone12.md"}  # by workload
     sources = ("decode.cu", "lrkv_internal.cuh", "kernels.h")
 
     def __init__(self, wl, rank, fused=False, d_rope=0, per_layer=False):
@@ -391,7 +392,8 @@ class DecodeHarness(Rotating):
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
                          "traffic": recorded_traffic(self.profiles[wl.key], self.sources)
-                                    if wl.key in self.profiles and not self.fused and not self.d_rope else None,
+                                    if wl.key in self.profiles and not self.fused and not self.d_rope
+                                    and (self.layered or wl.layers == 1) else None,
                          "algorithmic_bytes_per_launch": self.kernel_units // (1 if self.layered else wl.layers),
                          "avg_launch_ms": kernel_s * 1e3 / (1 if self.layered else wl.layers)},
             "e2e_unit_value": lambda s: self.step_units * world / s / 1e9, "e2e_unit": "GB/s",
