@@ -99,6 +99,13 @@ cudaError_t launch_decode(const CUtensorMap& tK, const CUtensorMap& tV, const CU
                           const CUtensorMap& tZV, DecodeArgs a, int D_H, int R, int D_R, int sms, int smem_limit,
                           cudaStream_t stream);
 
+// The split-K scan on the tensor cores (H = 128, d_h = 128, no positional key, one head group):
+// launched in place of the CUDA-core scan by launch_decode; smem_bytes from decode_tc_smem_bytes.
+int decode_tc_smem_bytes(int nslot, int stage_bytes);
+template <int R>
+cudaError_t launch_decode_tc_split(const CUtensorMap& tK, const CUtensorMap& tV, const DecodeArgs& a, int grid,
+                                   int smem_bytes, bool pdl, cudaStream_t stream);
+
 cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, int D_R, cudaStream_t stream);
 
 // Tensor-core prefill (d_h = 128, r = 16).  Maps: q as [B*Tq][H*d_h] box {64,128}
