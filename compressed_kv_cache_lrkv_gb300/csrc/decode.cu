@@ -75,8 +75,13 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // q~[vb][h][j] = sum_d q[vb][h][d] B^K[h][d][j]; one block per (head, virtual sequence):
 // 256 / R slices of the d range are summed in parallel, then reduced in
 // shared memory, so all of B_h^K (d_h x r) is in flight at once.
+// Launched as a dependent of the caller's previous kernel on the stream, so its blocks are in
+// place when that kernel ends; it waits for that kernel's completion before touching memory and
+// only then lets the scan start (the scan reads the cache, which the previous kernel -- an
+// append of the newest rows -- may have written).
 template <int D_H, int R, int D_R>
 __global__ void __launch_bounds__(256) decode_absorb_kernel(const DecodeArgs a) {
+    pdl_wait();
     pdl_trigger();
     constexpr int NS = 256 / R;           // d slices
     constexpr int DS = D_H / NS;          // d values per slice (>= 2)
@@ -636,6 +641,9 @@ __global__ void __launch_bounds__(256, 1)
 // together, then the slices are merged in shared memory; B_h^V rows are prefetched up front.
 template <int D_H, int R>
 __global__ void __launch_bounds__(512, 2) decode_combine_kernel(const DecodeArgs a) {
+    // The next call's absorb kernel may be scheduled now: it waits for this grid to end before
+    // it reads anything (an ordinary launch after this one keeps the full stream order).
+    pdl_trigger();
     constexpr int W = D_H + R;
     constexpr int W4 = W / 4;
     constexpr int NSL_MAX = 512 / W4;  // slices at most
@@ -785,7 +793,7 @@ int decode_head_groups(int H, int R) {
 int decode_stage_granules(int H, int D_H, int R, int D_R) {
     if (decode_head_groups(H, R) > 1) return 1;
     const int gran_bytes = 16 * (2 * D_H + D_R) + 32 * H * R;
-    return 4 * gran_bytes <= kSmallStageBytes ? 4 : 1;
+    return 2 * gran_bytes <= kSmallStageBytes ? 2 : 1;
 }
 
 DecodePlan decode_plan(int H_all, int D_H, int R, int D_R, int smem_limit) {
@@ -868,7 +876,7 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
                                    cudaStream_t stream) {
     // Head groups occur only where a token's latents for all heads exceed kGroupLatents elements,
     // which with H <= 128 needs r = 32.
-    auto split = a.gpst == 4 ? decode_split_kernel<D_H, R, D_R, false, 4> : decode_split_kernel<D_H, R, D_R, false, 1>;
+    auto split = a.gpst == 2 ? decode_split_kernel<D_H, R, D_R, false, 2> : decode_split_kernel<D_H, R, D_R, false, 1>;
     if constexpr (R * 128 > kGroupLatents) {
         if (a.nhg > 1) split = decode_split_kernel<D_H, R, D_R, true, 1>;
     }
@@ -880,8 +888,7 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
     if constexpr (D_H == 128 && D_R == 0 && (R == 8 || R == 16)) {
         if (a.H == 128 && a.nhg == 1 && a.gpst == 1) {
             if (!a.qt_in) {
-                decode_absorb_kernel<D_H, R, D_R><<<dim3(a.H, nvb), 256, 0, stream>>>(a);
-                e = cudaGetLastError();
+                e = launch_pdl(decode_absorb_kernel<D_H, R, D_R>, dim3(a.H, nvb), dim3(256), 0, stream, a);
                 if (e != cudaSuccess) return e;
             }
             e = launch_decode_tc_split<R>(tK, tV, a, grid, decode_tc_smem_bytes(p.nslot, p.stage_bytes), !a.qt_in,
@@ -897,8 +904,7 @@ static cudaError_t launch_decode_t(const CUtensorMap& tK, const CUtensorMap& tV,
         split<<<grid, p.threads, p.smem_bytes, stream>>>(tK, tV, tZK, tZV, a);
         e = cudaGetLastError();
     } else {
-        decode_absorb_kernel<D_H, R, D_R><<<dim3(a.H, nvb), 256, 0, stream>>>(a);
-        e = cudaGetLastError();
+        e = launch_pdl(decode_absorb_kernel<D_H, R, D_R>, dim3(a.H, nvb), dim3(256), 0, stream, a);
         if (e != cudaSuccess) return e;
         e = launch_pdl(split, dim3(grid), dim3(p.threads), p.smem_bytes, stream, tK, tV, tZK, tZV, a);
     }

@@ -251,9 +251,10 @@ constexpr int kFillAlone = 8;                 // ring fills of up to this many s
 // many elements per token (64 KB a stage) all heads are scanned together, beyond it the heads
 // are split into groups scanned by different CTAs (else fewer than three stages would fit).
 constexpr int kGroupLatents = 2048;
-// Stages of one granule smaller than a quarter of this are made four granules (32 tokens) long:
-// a copy instruction costs its thread ~60-80 ns whatever its size, so small stages were bound by
-// the issue of their four copies.
-constexpr int kSmallStageBytes = 32 << 10;
+// Stages of one granule at most half of this are made two granules (16 tokens) long: a copy
+// instruction costs its thread ~60-80 ns whatever its size, so small stages were bound by the
+// issue of their four copies.  (Four granules per stage measured slower on the 12-layer
+// backbone, 90.2 vs 85.7 us: fewer ring slots and consumer groups; eight, 197 us.)
+constexpr int kSmallStageBytes = 16 << 10;
 
 }  // namespace lrkv

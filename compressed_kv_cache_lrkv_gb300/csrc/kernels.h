@@ -81,7 +81,7 @@ cudaError_t launch_append_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, con
 // elements, two tensors) fit in 64 KB; else the fewest groups (2, 4 or 8, dividing H into
 // whole 128-element pieces of a token's latents) that bring a group's share within that.
 int decode_head_groups(int H, int R);
-// 8-token granules per stage of the decode scan (1, or 4 for small stages); the s^K, s^V maps'
+// 8-token granules per stage of the decode scan (1, or 2 for small stages); the s^K, s^V maps'
 // box is 8 x this many rows.
 int decode_stage_granules(int H, int D_H, int R, int D_R);
 // Whether the split kernel's shared-memory ring (at least two stages) fits in smem_limit bytes.

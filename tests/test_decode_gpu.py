@@ -251,7 +251,7 @@ def test_decode_rejects_head_counts_without_a_group_split():
 
 @pytest.mark.parametrize("ns", [1, 3, 7, 13, 50, 0])
 def test_small_stages_with_segment_edges_inside_a_stage(ns):
-    """Small-head shapes stream four granules (32 tokens) per stage; with these split counts and
+    """Small-head shapes stream two granules (16 tokens) per stage; with these split counts and
     ragged lengths the pieces and ranges begin and end inside a stage, whose granules outside the
     segment must be skipped."""
     H, d_h, r = 8, 64, 16
