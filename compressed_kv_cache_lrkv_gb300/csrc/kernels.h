@@ -114,6 +114,6 @@ cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, int D_R, cudaSt
 struct PrefillMaps {
     CUtensorMap q, sK, sV, zK, zV, BK;
 };
-cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int d_h, cudaStream_t stream);
 
 }  // namespace lrkv

@@ -1,6 +1,6 @@
 // prefill_tc.cu -- causal chunked prefill on the 5th-generation tensor cores
 // ("Low-Rank Key Value Attention", Eqs. (6)-(7) with the causal mask of the
-// softmax frame), for d_h = 128, r = 16.
+// softmax frame), for d_h = 64 or 128 and r = 16.
 //
 // One CTA = 128 queries of one (sequence, head); key tiles of 128 tokens (two
 // cache pages).  Per tile j:
@@ -30,21 +30,30 @@ namespace lrkv {
 namespace {
 
 constexpr int kBM = 128, kBN = 128;
-constexpr uint32_t OFF_Q = 0;           // [128 q][128 d] K-major, 128B swizzle, two 64-column blocks
-constexpr uint32_t OFF_QT = 32768;      // [128 q][16] K-major, 32B swizzle
-constexpr uint32_t OFF_BK = 36864;      // [128 d][16] MN-major (B operand of Q~), 32B swizzle
-// After the prologue the B^K area and the 4 KiB after it hold B_h^V as fp32 for the final tf32 MMA:
-// [128 d][16 j], K-major without swizzle -- 8 x 4-element core matrices, element (d, j)
-// at (d / 8) * 512 + (j / 4) * 128 + (d % 8) * 16 + (j % 4) * 4.
-constexpr uint32_t OFF_BVF = OFF_BK;
-// Key ring (3 stages: s^K [128 keys][128] K-major 128B swizzle, then z^K_h [128][16] 32B
-// swizzle) and value ring (2 stages: s^V, z^V_h, same layouts, read MN-major).
 constexpr int kKStages = 3, kVStages = 2;
-constexpr uint32_t STAGE_BYTES = 36864, STAGE_Z = 32768;
-constexpr uint32_t OFF_K = 45056;
-constexpr uint32_t OFF_V = OFF_K + kKStages * STAGE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_V + kVStages * STAGE_BYTES;
-constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;
+// Shared-memory layout for d_h = D_H (64 or 128; the tiles are D_H / 64 blocks of 64 columns):
+//   Q    [128 q][D_H] K-major, 128B swizzle
+//   Q~   [128 q][16] K-major, 32B swizzle
+//   B^K  [D_H d][16] MN-major (B operand of Q~), 32B swizzle; after the prologue this area (and
+//        the same again after it) holds B_h^V as fp32 for the final tf32 MMA: [D_H d][16 j],
+//        K-major without swizzle -- 8 x 4-element core matrices, element (d, j) at
+//        (d / 8) * 512 + (j / 4) * 128 + (d % 8) * 16 + (j % 4) * 4
+//   key ring (3 stages: s^K [128 keys][D_H] K-major 128B swizzle, then z^K_h [128][16] 32B
+//   swizzle) and value ring (2 stages: s^V, z^V_h, same layouts, read MN-major).
+template <int D_H>
+struct PfLayout {
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_QT = 128 * D_H * 2;
+    static constexpr uint32_t OFF_BK = OFF_QT + 4096;
+    static constexpr uint32_t OFF_BVF = OFF_BK;
+    static constexpr uint32_t STAGE_Z = 128 * D_H * 2;
+    static constexpr uint32_t STAGE_BYTES = STAGE_Z + 4096;
+    static constexpr uint32_t OFF_K = OFF_BK + D_H * 64;
+    static constexpr uint32_t OFF_V = OFF_K + kKStages * STAGE_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + kVStages * STAGE_BYTES;
+    static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+    static_assert(OFF_K % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzled TMA tiles start 1024-aligned");
+};
 constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_OS = 256, TM_OZ = 384, TM_QT = 448, TM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -69,8 +78,14 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, uint32_t
 
 constexpr int kThreads = 256;
 
+template <int D_H>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillMaps m, const PrefillArgs a) {
-    constexpr int D_H = 128, R = 16;
+    constexpr int R = 16;
+    constexpr int NB = D_H / 64;  // 64-column blocks of a row
+    using Lay = PfLayout<D_H>;
+    constexpr uint32_t OFF_Q = Lay::OFF_Q, OFF_QT = Lay::OFF_QT, OFF_BK = Lay::OFF_BK, OFF_BVF = Lay::OFF_BVF;
+    constexpr uint32_t STAGE_Z = Lay::STAGE_Z, STAGE_BYTES = Lay::STAGE_BYTES;
+    constexpr uint32_t OFF_K = Lay::OFF_K, OFF_V = Lay::OFF_V, OFF_BAR = Lay::OFF_BAR;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -170,9 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             return row;
         };
         if (keys && lane == 0) {
-            mbar_arrive_expect_tx(B(q_full), 32768 + 4096);
-            tma_load_2d(S0 + OFF_Q, &m.q, h * D_H, b * Tq + q0, B(q_full));
-            tma_load_2d(S0 + OFF_Q + 16384, &m.q, h * D_H + 64, b * Tq + q0, B(q_full));
+            mbar_arrive_expect_tx(B(q_full), 128 * D_H * 2 + D_H * 32);
+#pragma unroll
+            for (int bk = 0; bk < NB; ++bk) tma_load_2d(S0 + OFF_Q + bk * 16384, &m.q, h * D_H + 64 * bk, b * Tq + q0, B(q_full));
             tma_load_2d(S0 + OFF_BK, &m.BK, 0, h * D_H, B(q_full));
         }
         const int depth = keys ? kKStages : kVStages;
@@ -205,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 mbar_arrive_expect_tx(bar, STAGE_BYTES);
                 for (int p = 0; p < 2; ++p) {
                     const int row = p ? row1 : row0;
-                    tma_load_2d(base + p * 8192, ms, 0, row, bar);
-                    tma_load_2d(base + 16384 + p * 8192, ms, 64, row, bar);
+#pragma unroll
+                    for (int bk = 0; bk < NB; ++bk) tma_load_2d(base + bk * 16384 + p * 8192, ms, 64 * bk, row, bar);
                     tma_load_2d(base + STAGE_Z + p * 2048, mz, h * R, row, bar);
                 }
             }
@@ -231,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         // to tile cost a register-to-uniform move per MMA and halve the issue rate.
         constexpr uint32_t id_S = idesc_bf16_f32(128, 128);
         constexpr uint32_t id_QT = idesc_bf16_f32(128, 16) | (1u << 16);
-        constexpr uint32_t id_PVs = idesc_bf16_f32(128, 128) | (1u << 16);
+        constexpr uint32_t id_PVs = idesc_bf16_f32(128, D_H) | (1u << 16);
         constexpr uint32_t id_PVz = idesc_bf16_f32(128, 16) | (1u << 16);
         constexpr uint64_t kStage = STAGE_BYTES >> 4;
         bool ok = true;
@@ -322,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             // accumulation must have completed first.
             ok = ok && wait_all(B(o_done + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, a.status);
             if (ok) {
-                constexpr uint32_t id_fin = idesc_tf32_f32(128, 128);
+                constexpr uint32_t id_fin = idesc_tf32_f32(128, D_H);
                 const uint64_t dBV = sdesc(S0 + OFF_BVF, 128, 512, 0);
                 tc_fence_after();
                 if (elect_one_sync()) {
@@ -348,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tc_fence_after();
         // B^K has been consumed (qt_mma): B_h^V, widened to fp32, takes its place for the
         // final tf32 MMA -- thread d writes row d (16 values, 4 core-matrix chunks).
-        {
+        if (st_tid < D_H) {
             const uint4* src = reinterpret_cast<const uint4*>(a.BV + ((size_t)h * D_H + st_tid) * R);
             const uint4 w0 = src[0], w1 = src[1];
             const uint32_t wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -428,13 +443,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 if (!ok) break;
                 if (k0 + row >= ctx) {
                     const uint4 z = make_uint4(0, 0, 0, 0);
-                    uint4* r0 = reinterpret_cast<uint4*>(smem + kvb + row * 128);
-                    uint4* r1 = reinterpret_cast<uint4*>(smem + kvb + 16384 + row * 128);
                     uint4* rz = reinterpret_cast<uint4*>(smem + kvb + STAGE_Z + row * 32);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        r0[i] = z;
-                        r1[i] = z;
+                    for (int bk = 0; bk < NB; ++bk) {
+                        uint4* r0 = reinterpret_cast<uint4*>(smem + kvb + bk * 16384 + row * 128);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) r0[i] = z;
                     }
                     rz[0] = z;
                     rz[1] = z;
@@ -470,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 tc_fence_after();
                 uint32_t v[32];
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < D_H / 32; ++c) {
                     tmem_ld_32x32b_x32(tmem + tl + TM_OS + c * 32, v);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
@@ -493,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int qrow = q0 + row;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < D_H / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem + tl + TM_OS + c * 32, v);
                 if (qrow < Tq) {
@@ -517,12 +531,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
 }
 
-cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+template <int D_H>
+static cudaError_t launch_prefill_tc_t(const PrefillMaps& maps, const PrefillArgs& a, cudaStream_t stream) {
+    constexpr uint32_t smem = PfLayout<D_H>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D_H>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.Tq + kBM - 1) / kBM, a.H, a.B);
-    prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(maps, a);
+    prefill_tc_kernel<D_H><<<grid, kThreads, smem, stream>>>(maps, a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int d_h, cudaStream_t stream) {
+    return d_h == 64 ? launch_prefill_tc_t<64>(maps, a, stream) : launch_prefill_tc_t<128>(maps, a, stream);
 }
 
 }  // namespace lrkv

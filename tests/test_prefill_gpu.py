@@ -35,12 +35,16 @@ CASES = [
     (4, 128, 32, 1, [0, 1000]),
     (32, 128, 16, 96, [256, 0]),
     (2, 128, 8, 70, [63, 1]),
-    # d_h = 128, r = 16 runs the tcgen05 kernel: ragged query tiles, contexts not
-    # aligned to pages or key tiles, the last chunk of a 4096-token prompt
+    # d_h = 128 or 64 with r = 16 runs the tcgen05 kernel: ragged query tiles, contexts
+    # not aligned to pages or key tiles, the last chunk of a 4096-token prompt
     (1, 128, 16, 300, [37, 0]),
     (3, 128, 16, 512, [3584, 1000]),
     (2, 128, 16, 129, [127, 64]),
     (8, 128, 16, 1, [4095, 0]),
+    (1, 64, 16, 300, [37, 0]),
+    (3, 64, 16, 512, [3584, 1000]),
+    (12, 64, 16, 129, [127, 64]),
+    (2, 64, 16, 1, [4095, 0]),
 ]
 
 
