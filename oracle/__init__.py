@@ -115,6 +115,9 @@ class Oracle:
         L.oracle_prefill_cache.argtypes = ([_c_int] * 7 + [_u16p] * 4 + [_i32p, _c_int, _i32p] +
                                            [_u16p] * 3 + [_c_double, _u8p_or_null, _f64p])
         L.oracle_prefill_cache.restype = _c_int
+        L.oracle_prefill_fused_rope.argtypes = ([_c_int] * 8 + [_u16p] * 4 + [_i32p, _c_int, _i32p] +
+                                                [_u16p, _u16p, _c_double, _u8p_or_null, _f64p])
+        L.oracle_prefill_fused_rope.restype = _c_int
         L.oracle_mla_decode.argtypes = ([_c_int] * 7 + [_u16p, _i32p, _c_int, _i32p, _u16p] +
                                         [_c_double, _u8p_or_null, _f64p])
         L.oracle_mla_decode.restype = _c_int
@@ -313,6 +316,25 @@ class Oracle:
                                                 wp, out)
         if rc != 0:
             raise ValueError("oracle_prefill_cache: bad block id or length")
+        return out
+
+    def prefill_fused(self, cache, block_table, q_start, q, q_tilde, scale=0.0, want=None, bs=64):
+        """E2 causal prefill with absorbed weights: q [B, Tq, H, d_h + d_rope], q~ [B, Tq, H, r]
+        -> [B, Tq, H, d_h + r] = [o_s | o_z]."""
+        sK, sV, zK, zV = (_u16(c) for c in cache)
+        _, Tq, H = q.shape[:3]
+        d_h = sV.shape[-1]
+        d_rope = sK.shape[-1] - d_h
+        r = q_tilde.shape[3]
+        nb = sK.shape[0]
+        bt = _i32(block_table)
+        B, max_pages = bt.shape
+        out = np.zeros((B, Tq, H, d_h + r), np.float64)
+        w, wp = _want_ptr(want, B, H)
+        rc = self.lib.oracle_prefill_fused_rope(B, Tq, H, d_h, r, d_rope, bs, nb, sK, sV, zK, zV, bt, max_pages,
+                                                _i32(q_start), _u16(q), _u16(q_tilde), float(scale), wp, out)
+        if rc != 0:
+            raise ValueError("oracle_prefill_fused: bad block id or length")
         return out
 
 

@@ -556,6 +556,70 @@ int oracle_prefill_cache(int B, int Tq, int H, int d_h, int r, int bs, int num_b
                                      q_start, BK, BV, q, scale, want, out);
 }
 
+/* E2 causal prefill with absorbed weights (the associativity of the LRKV slides' frame
+ * "Compute logits without expanding historical keys" and of Eq. (7), applied to a chunk of
+ * queries): query i of sequence b, at absolute position q_start[b] + i, brings q~_i = q_i B_h^K
+ * already projected, and head h returns the aggregate before the residual up-projection,
+ *     out = sum_{j <= q_start[b] + i} p_j [s^V_j | z^V_{h,j}],
+ *     p = softmax_j([q_i | q~_i] . [s^K_j | z^K_{h,j}] * scale)
+ * i.e. causal single-head attention over the concatenated features (with a positional key,
+ * [q | q^R | q~] . [s^K | k^R | z^K_h]).  q [B][Tq][H][d_h + d_rope], qt [B][Tq][H][r],
+ * out [B][Tq][H][d_h + r].  Returns 0, or -1 when a block id or length is out of range. */
+int oracle_prefill_fused_rope(int B, int Tq, int H, int d_h, int r, int d_rope, int bs, int num_blocks,
+                              const uint16_t* sK, const uint16_t* sV, const uint16_t* zK,
+                              const uint16_t* zV, const int32_t* block_table, int max_pages,
+                              const int32_t* q_start, const uint16_t* q, const uint16_t* qt, double scale,
+                              const uint8_t* want, double* out) {
+    for (int b = 0; b < B; ++b) {
+        int L = q_start[b] + Tq;
+        if (q_start[b] < 0 || L > max_pages * bs) return -1;
+        for (int p = 0; p < (L + bs - 1) / bs; ++p) {
+            int32_t blk = block_table[(size_t)b * max_pages + p];
+            if (blk < 0 || blk >= num_blocks) return -1;
+        }
+    }
+    const int ds = d_h + d_rope;      /* shared key width */
+    const int wk = ds + r, wv = d_h + r;
+    scale = default_scale(scale, ds);
+    int bad = 0;
+    #pragma omp parallel for schedule(dynamic)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        if (want && !want[bh]) continue;
+        int L = q_start[b] + Tq;
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * wk);
+        double* V = (double*)malloc(sizeof(double) * (size_t)(L ? L : 1) * wv);
+        double* qc = (double*)malloc(sizeof(double) * (size_t)wk);
+        if (!K || !V || !qc) {
+            #pragma omp atomic write
+            bad = 1;
+        } else {
+            for (int t = 0; t < L; ++t) {
+                int64_t slot = (int64_t)block_table[(size_t)b * max_pages + t / bs] * bs + t % bs;
+                for (int i = 0; i < ds; ++i) K[(size_t)t * wk + i] = bf(sK[slot * ds + i]);
+                for (int i = 0; i < d_h; ++i) V[(size_t)t * wv + i] = bf(sV[slot * d_h + i]);
+                for (int j = 0; j < r; ++j) {
+                    K[(size_t)t * wk + ds + j] = bf(zK[(slot * H + h) * r + j]);
+                    V[(size_t)t * wv + d_h + j] = bf(zV[(slot * H + h) * r + j]);
+                }
+            }
+            for (int i = 0; i < Tq; ++i) {
+                const size_t row = ((size_t)b * Tq + i) * H + h;
+                for (int c = 0; c < ds; ++c) qc[c] = bf(q[row * ds + c]);
+#if LRKV_ORACLE_MUTANT == 13
+                /* planted: q~ of the next head */
+                for (int j = 0; j < r; ++j) qc[ds + j] = bf(qt[(row - h + (h + 1) % H) * r + j]);
+#else
+                for (int j = 0; j < r; ++j) qc[ds + j] = bf(qt[row * r + j]);
+#endif
+                attend_kv(visible(q_start[b] + i), wk, wv, qc, K, V, scale, out + row * wv);
+            }
+        }
+        free(K); free(V); free(qc);
+    }
+    return bad ? -1 : 0;
+}
+
 /* ---------------------------------------------------------------- MLA, absorbed and expanded */
 /*
  * Multi-head latent attention as the MLA lesson ("Embeddings II: MLA & Architectural

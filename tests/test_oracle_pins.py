@@ -22,10 +22,11 @@ from cases import Weights, empty_pools, f64, random_pools, weights
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def _sdpa(q, K, V, scale, causal=False):
-    """Library attention: q [Hq, Tq, d_h], K/V [Hq, L, d_h] (fp64)."""
+def _sdpa(q, K, V, scale, causal=False, mask=None):
+    """Library attention: q [Hq, Tq, d_h], K/V [Hq, L, d_h] (fp64); mask [Tq, L] bool (True = attend)."""
+    m = None if mask is None else torch.from_numpy(mask)
     out = F.scaled_dot_product_attention(torch.from_numpy(q), torch.from_numpy(K), torch.from_numpy(V),
-                                         scale=scale, is_causal=causal)
+                                         attn_mask=m, scale=scale, is_causal=causal)
     return out.numpy()
 
 
@@ -323,6 +324,54 @@ def pin_fused_matches_factored_decode(o):
     np.testing.assert_allclose(recomposed, ref, rtol=1e-12, atol=1e-13)
 
 
+
+def pin_prefill_fused_is_concatenated_causal_attention(o):
+    """The absorbed-weights prefill is causal single-head attention over the concatenated
+    features: query i of a chunk starting at q_start attends, with [q_i | q~_i], to the keys
+    [s^K_j | z^K_{h,j}] of positions j <= q_start + i and aggregates [s^V_j | z^V_{h,j}]:
+    torch SDPA with that mask on exactly those tensors.  With a positional key the shared key
+    row is [s^K | k^R], the query [q | q^R | q~], the scale 1/sqrt(d_h + d_rope)."""
+    B, H, d_h, r, Tq = 2, 3, 16, 8, 40
+    qs = [100, 0]
+    for d_rope in (0, 16):
+        lens = [qs[b] + Tq for b in range(B)]
+        pt = S.page_table(23 + d_rope, lens, 64, spare_blocks=2)
+        pools = random_pools(23 + d_rope, pt.num_blocks, H, d_h, r, d_rope=d_rope)
+        q = S.gaussian_bf16(23, "q", (B, Tq, H, d_h + d_rope))
+        qt = S.gaussian_bf16(23, "qt", (B, Tq, H, r))
+        got = o.prefill_fused(pools, pt.block_table, qs, q, qt)
+        for b in range(B):
+            sK, sV, zK, zV = _gather_rows(pools, pt, b, lens[b])
+            mask = np.arange(lens[b])[None, :] <= (qs[b] + np.arange(Tq))[:, None]
+            for h in range(H):
+                Kc = np.concatenate([sK, zK[:, h]], axis=1)[None]
+                Vc = np.concatenate([sV, zV[:, h]], axis=1)[None]
+                qc = np.concatenate([f64(q[b, :, h]), f64(qt[b, :, h])], axis=1)[None]
+                ref = _sdpa(qc, Kc, Vc, 1.0 / np.sqrt(d_h + d_rope), mask=mask)[0]
+                np.testing.assert_allclose(got[b, :, h], ref, rtol=1e-12, atol=1e-14)
+
+
+def pin_prefill_fused_matches_factored_prefill(o):
+    """On integer q and B^K, q~ = q B^K is exact in bf16, so every query row of the
+    absorbed-weights prefill, recomposed as o_s + B^V o_z, must equal the factored causal
+    prefill (which computes q~ and applies B^V itself)."""
+    B, H, d_h, r, Tq = 2, 3, 16, 8, 70
+    qs = [60, 5]
+    lens = [qs[b] + Tq for b in range(B)]
+    pt = S.page_table(24, lens, 64, spare_blocks=1)
+    pools = random_pools(24, pt.num_blocks, H, d_h, r)
+    q = S.int_grid_bf16(24, "q", (B, Tq, H, d_h), -1, 1)
+    BK = S.int_grid_bf16(24, "BK", (H, d_h, r), -1, 1)
+    BV = S.gaussian_bf16(24, "BV", (H, d_h, r), 0.5)
+    qt_exact = np.einsum("bthd,hdr->bthr", f64(q), f64(BK))
+    assert np.all(np.abs(qt_exact) <= 256) and np.all(qt_exact == np.round(qt_exact))
+    qt = _lib_bf16(qt_exact)
+    fused = o.prefill_fused(pools, pt.block_table, qs, q, qt)
+    o_s, o_z = fused[..., :d_h], fused[..., d_h:]
+    recomposed = o_s + np.einsum("hdr,bthr->bthd", f64(BV), o_z)
+    ref = o.prefill_cache(pools, pt.block_table, qs, BK, BV, q)
+    np.testing.assert_allclose(recomposed, ref, rtol=1e-12, atol=1e-13)
+
 # ---------------------------------------------------------------------------- decoupled positional key
 ROPE_BASE = 10000.0
 
@@ -492,6 +541,7 @@ PINS = [pin_softmax_worked_value, pin_softmax_normalised, pin_attend_special_cas
         pin_factored_equals_expanded, pin_cache_path_matches_weight_path,
         pin_head_permutation_equivariance, pin_page_permutation_invariance, pin_prefill_causal_edges,
         pin_fused_is_concatenated_attention, pin_fused_matches_factored_decode,
+        pin_prefill_fused_is_concatenated_causal_attention, pin_prefill_fused_matches_factored_prefill,
         pin_rope_append_is_rotation, pin_rope_attention_is_concatenated, pin_rotation_direction_worked_example,
         pin_mla_absorbed_is_mqa, pin_mla_absorbed_equals_expanded, pin_train_is_autograd]
 
@@ -508,7 +558,8 @@ def test_pin(pin, oracle_lib):
 #  8 positional key rotated the wrong way    9 scale of the content width only with a positional key
 # 10 MLA scale over the cached row's width  11 MLA values read from the wrong slice of the row
 # 12 training: dB_h formed with dK_h B_h in place of X U_h
-MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12]
+# 13 absorbed prefill reads q~ of the next head
+MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
