@@ -22,7 +22,7 @@ DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 EXPORTED = ["lrkv_abi_version", "lrkv_status_string", "lrkv_last_error", "lrkv_cache_block_bytes", "lrkv_append",
             "lrkv_decode_workspace_bytes", "lrkv_decode", "lrkv_decode_fused", "lrkv_decode_static_ws",
             "lrkv_append_layers", "lrkv_decode_layers",
-            "lrkv_prefill_workspace_bytes", "lrkv_prefill", "lrkv_mla_cache_block_bytes", "lrkv_mla_append",
+            "lrkv_prefill_workspace_bytes", "lrkv_prefill", "lrkv_prefill_fused", "lrkv_mla_cache_block_bytes", "lrkv_mla_append",
             "lrkv_mla_decode_workspace_bytes", "lrkv_mla_decode", "lrkv_train_forward", "lrkv_train_workspace_bytes",
             "lrkv_train_backward"]
 STATIC_WS_BYTES = 16 << 20  # LRKV_STATIC_WS_BYTES
@@ -95,6 +95,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lrkv_prefill_workspace_bytes.argtypes = [P(Dims), i32, i32]
     lib.lrkv_prefill.restype = ctypes.c_int
     lib.lrkv_prefill.argtypes = [P(Dims), vp, vp, vp, P(Cache), vp, i32, vp, i32, i32, vp, vp, sz, vp, vp]
+    lib.lrkv_prefill_fused.restype = ctypes.c_int
+    lib.lrkv_prefill_fused.argtypes = [P(Dims), vp, vp, P(Cache), vp, i32, vp, i32, i32, vp, vp, vp]
     lib.lrkv_train_forward.restype = ctypes.c_int
     lib.lrkv_train_forward.argtypes = [P(Dims), vp, vp, vp, i32, vp, vp, vp, vp]
     lib.lrkv_train_workspace_bytes.restype = sz
@@ -294,6 +296,16 @@ def lrkv_prefill(dims: Dims, q, BK, BV, cache: PagedCache, block_table, q_start,
                              int(block_table.shape[1]), _ptr(q_start), B, Tq, _ptr(out), _ptr(workspace), ws_bytes,
                              _ptr(status), _stream(stream))
     _check(rc, "lrkv_prefill")
+
+
+def lrkv_prefill_fused(dims: Dims, q, q_tilde, cache: PagedCache, block_table, q_start, out, status=None, stream=None):
+    """Causal prefill with absorbed weights: q [B, Tq, H, d_h], q~ [B, Tq, H, r] -> out [B, Tq, H, d_h + r]."""
+    B, Tq = int(q.shape[0]), int(q.shape[1])
+    c = cache.struct()
+    rc = load().lrkv_prefill_fused(ctypes.byref(dims), _ptr(q), _ptr(q_tilde), ctypes.byref(c), _ptr(block_table),
+                                   int(block_table.shape[1]), _ptr(q_start), B, Tq, _ptr(out), _ptr(status),
+                                   _stream(stream))
+    _check(rc, "lrkv_prefill_fused")
 
 
 def train_workspace_bytes(dims: Dims, n_tok: int) -> int:

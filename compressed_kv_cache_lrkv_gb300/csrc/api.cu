@@ -522,12 +522,13 @@ size_t lrkv_prefill_workspace_bytes(const lrkv_dims* dims, int32_t batch, int32_
     return 0;
 }
 
-lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, const void* BV, const lrkv_cache* cache,
-                         const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* q_start, int32_t batch,
-                         int32_t Tq, void* out, void* workspace, size_t workspace_bytes, uint32_t* status_dev,
-                         void* stream) {
-    (void)workspace;
-    (void)workspace_bytes;
+// Shared body of lrkv_prefill (q~ = q B^K computed here, output B^V-projected) and
+// lrkv_prefill_fused (q~ given by the caller, output [o_s | o_z] / l).
+static lrkv_status prefill_impl(bool fused, const lrkv_dims* dims, const void* q, const void* q_tilde,
+                                const void* BK, const void* BV, const lrkv_cache* cache, const int32_t* block_table,
+                                int32_t max_blocks_per_seq, const int32_t* q_start, int32_t batch, int32_t Tq,
+                                void* out, uint32_t* status_dev, void* stream) {
+    const char* what = fused ? "lrkv_prefill_fused launch" : "lrkv_prefill launch";
     lrkv_status s = check_dims(dims);
     if (s != LRKV_OK) return s;
     if ((s = check_cache(cache)) != LRKV_OK) return s;
@@ -536,12 +537,17 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, c
     if (max_blocks_per_seq < 1 || (long long)max_blocks_per_seq * dims->block_size > (1LL << 30))
         return fail(LRKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", max_blocks_per_seq);
     LRKV_REQUIRE_PTR(q);
-    LRKV_REQUIRE_PTR(BK);
-    LRKV_REQUIRE_PTR(BV);
+    if (fused) {
+        LRKV_REQUIRE_PTR(q_tilde);
+    } else {
+        LRKV_REQUIRE_PTR(BK);
+        LRKV_REQUIRE_PTR(BV);
+    }
     LRKV_REQUIRE_PTR(out);
     if (!block_table || !q_start) return fail(LRKV_ERR_INVALID_ARG, "block_table or q_start is NULL");
     lrkv::PrefillArgs a{};
     a.q = static_cast<const uint16_t*>(q);
+    a.qt = static_cast<const uint16_t*>(q_tilde);
     a.BK = static_cast<const uint16_t*>(BK);
     a.BV = static_cast<const uint16_t*>(BV);
     a.sK = static_cast<const uint16_t*>(cache->sK);
@@ -568,15 +574,37 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, c
             (s = make_tmap(&mp.sK, cache->sK, dh, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "sK")) != LRKV_OK ||
             (s = make_tmap(&mp.sV, cache->sV, dh, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "sV")) != LRKV_OK ||
             (s = make_tmap(&mp.zK, cache->zK, HR, rows, 16, 64, CU_TENSOR_MAP_SWIZZLE_32B, "zK")) != LRKV_OK ||
-            (s = make_tmap(&mp.zV, cache->zV, HR, rows, 16, 64, CU_TENSOR_MAP_SWIZZLE_32B, "zV")) != LRKV_OK ||
-            (s = make_tmap(&mp.BK, BK, 16, (uint64_t)dims->H * dh, 16, (uint32_t)dh, CU_TENSOR_MAP_SWIZZLE_32B,
-                           "BK")) != LRKV_OK)
+            (s = make_tmap(&mp.zV, cache->zV, HR, rows, 16, 64, CU_TENSOR_MAP_SWIZZLE_32B, "zV")) != LRKV_OK)
             return s;
-        return cuda_status(lrkv::launch_prefill_tc(mp, a, dims->d_h, static_cast<cudaStream_t>(stream)),
-                           "lrkv_prefill launch");
+        if (fused) {
+            s = make_tmap(&mp.qt, q_tilde, HR, (uint64_t)batch * Tq, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B, "q_tilde");
+            mp.BK = mp.qt;
+        } else {
+            s = make_tmap(&mp.BK, BK, 16, (uint64_t)dims->H * dh, 16, (uint32_t)dh, CU_TENSOR_MAP_SWIZZLE_32B, "BK");
+            mp.qt = mp.BK;
+        }
+        if (s != LRKV_OK) return s;
+        return cuda_status(lrkv::launch_prefill_tc(mp, a, dims->d_h, static_cast<cudaStream_t>(stream)), what);
     }
     return cuda_status(lrkv::launch_prefill(a, dims->d_h, dims->r, dims->d_rope, static_cast<cudaStream_t>(stream)),
-                       "lrkv_prefill launch");
+                       what);
+}
+
+lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, const void* BV, const lrkv_cache* cache,
+                         const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* q_start, int32_t batch,
+                         int32_t Tq, void* out, void* workspace, size_t workspace_bytes, uint32_t* status_dev,
+                         void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    return prefill_impl(false, dims, q, nullptr, BK, BV, cache, block_table, max_blocks_per_seq, q_start, batch, Tq, out,
+                        status_dev, stream);
+}
+
+lrkv_status lrkv_prefill_fused(const lrkv_dims* dims, const void* q, const void* q_tilde, const lrkv_cache* cache,
+                               const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* q_start,
+                               int32_t batch, int32_t Tq, void* out, uint32_t* status_dev, void* stream) {
+    return prefill_impl(true, dims, q, q_tilde, nullptr, nullptr, cache, block_table, max_blocks_per_seq, q_start, batch,
+                        Tq, out, status_dev, stream);
 }
 
 // ------------------------------------------------------------------ training-time projections

@@ -60,11 +60,14 @@ struct DecodeArgs {
 
 struct PrefillArgs {
     const uint16_t *q, *BK, *BV;        // q [B][Tq][H][D_H]; B* [H][D_H][R]
+    // Absorbed weights when non-null: q~ [B][Tq][H][R] given (B^K, B^V unused) and
+    // out [B][Tq][H][D_H + R] = [o_s | o_z] / l.
+    const uint16_t* qt;
     const uint16_t *sK, *sV, *zK, *zV;  // cache pools
     const int32_t* block_table;         // [B][max_pages]
     const int32_t* q_start;             // [B]
     uint32_t* status;
-    uint16_t* out;                      // [B][Tq][H][D_H]
+    uint16_t* out;                      // [B][Tq][H][D_H] (absorbed: [B][Tq][H][D_H + R])
     int B, Tq, H, max_pages, num_blocks;
     float scale_log2;
 };
@@ -108,11 +111,12 @@ cudaError_t launch_decode_tc_split(const CUtensorMap& tK, const CUtensorMap& tV,
 
 cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, int D_R, cudaStream_t stream);
 
-// Tensor-core prefill (d_h = 128, r = 16).  Maps: q as [B*Tq][H*d_h] box {64,128}
+// Tensor-core prefill (d_h = 64 or 128, r = 16).  Maps: q as [B*Tq][H*d_h] box {64,128}
 // and s^K, s^V pools [nb*64][d_h] box {64,64}, both 128-byte swizzle; z^K, z^V
-// pools [nb*64][H*r] box {16,64} and B^K as [H*d_h][r] box {16,128}, 32-byte swizzle.
+// pools [nb*64][H*r] box {16,64} and B^K as [H*d_h][r] box {16,d_h}, 32-byte swizzle;
+// with absorbed weights, q~ as [B*Tq][H*r] box {16,128}, 32-byte swizzle, in place of B^K.
 struct PrefillMaps {
-    CUtensorMap q, sK, sV, zK, zV, BK;
+    CUtensorMap q, sK, sV, zK, zV, BK, qt;
 };
 cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int d_h, cudaStream_t stream);
 

@@ -4,7 +4,8 @@
 // For head h the logits of query i against key j are the dot product of the
 // concatenated rows [q_i | q~_i] . [s^K_j | z^K_{h,j}] (width d_h + r), with
 // q~_i = q_i B_h^K; the value side accumulates P [s^V | z^V_h] into (o_s, o_z)
-// and the epilogue returns o_s + B_h^V o_z.  Query i sits at absolute position
+// and the epilogue returns o_s + B_h^V o_z.  With absorbed weights (a.qt set) q~
+// comes from the caller and the epilogue returns [o_s | o_z] instead.  Query i sits at absolute position
 // q_start + i and sees keys j <= q_start + i.  With a decoupled positional key
 // (D_R > 0) the shared key row is [s^K | k^R] and the query [q | q^R]: the
 // shared logits run over D_K = D_H + D_R columns, q~ uses the first D_H.
@@ -66,19 +67,21 @@ __global__ void __launch_bounds__(128) prefill_kernel(const PrefillArgs a) {
     const int i0 = qtile * 64 + warp * 16;  // this warp's first query row
     const int rA = i0 + g, rB = i0 + g + 8;
 
-    auto out_row = [&](int i) { return a.out + (((size_t)b * Tq + i) * H + h) * D_H; };
+    const bool fused = a.qt != nullptr;
+    const int ow = fused ? D_H + R : D_H;  // output row width
+    auto out_row = [&](int i) { return a.out + (((size_t)b * Tq + i) * H + h) * ow; };
     if (qs < 0 || ctx > cap) {
         if (threadIdx.x == 0 && qtile == 0 && h == 0) set_status(a.status, LRKV_DEV_BAD_SEQLEN);
-        for (int idx = threadIdx.x; idx < 64 * D_H; idx += 128) {
-            const int i = qtile * 64 + idx / D_H;
-            if (i < Tq) out_row(i)[idx % D_H] = 0;
+        for (int idx = threadIdx.x; idx < 64 * ow; idx += 128) {
+            const int i = qtile * 64 + idx / ow;
+            if (i < Tq) out_row(i)[idx % ow] = 0;
         }
         return;
     }
     const int last_row = min(qtile * 64 + 63, Tq - 1);
     const int n_tiles = (qs + last_row) / 64 + 1;
 
-    // ---- q fragments and q~ = q B_h^K (fp32, rounded to bf16 for the MMA)
+    // ---- q fragments and q~ = q B_h^K (fp32, rounded to bf16 for the MMA), or the caller's q~
     uint32_t qa[D_K / 16][4];
     {
         const uint32_t* qA = reinterpret_cast<const uint32_t*>(a.q + (((size_t)b * Tq + rA) * H + h) * D_K);
@@ -95,12 +98,18 @@ __global__ void __launch_bounds__(128) prefill_kernel(const PrefillArgs a) {
     {
         const int row = lane & 15, jh = lane >> 4;
         const int i = i0 + row;
-        const uint16_t* qrow = a.q + (((size_t)b * Tq + min(i, Tq - 1)) * H + h) * D_K;
+        const size_t qi = ((size_t)b * Tq + min(i, Tq - 1)) * H + h;
+        const uint16_t* qrow = a.q + qi * D_K;
         for (int j = jh * (R / 2); j < (jh + 1) * (R / 2); ++j) {
             float acc = 0.f;
-            const uint16_t* bk = a.BK + (size_t)h * D_H * R + j;
-            for (int dd = 0; dd < D_H; ++dd)
-                acc = fmaf(__uint_as_float((uint32_t)qrow[dd] << 16), __uint_as_float((uint32_t)bk[dd * R] << 16), acc);
+            if (fused) {
+                acc = __uint_as_float((uint32_t)a.qt[qi * R + j] << 16);
+            } else {
+                const uint16_t* bk = a.BK + (size_t)h * D_H * R + j;
+                for (int dd = 0; dd < D_H; ++dd)
+                    acc = fmaf(__uint_as_float((uint32_t)qrow[dd] << 16), __uint_as_float((uint32_t)bk[dd * R] << 16),
+                               acc);
+            }
             wscr[row * R + j] = i < Tq ? acc : 0.f;
         }
     }
@@ -285,6 +294,21 @@ __global__ void __launch_bounds__(128) prefill_kernel(const PrefillArgs a) {
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+    if (fused) {  // [o_s | o_z] / l
+#pragma unroll
+        for (int n = 0; n < D_H / 8; ++n) {
+            const int dcol = n * 8 + 2 * tq;
+            if (rA < Tq) *reinterpret_cast<uint32_t*>(out_row(rA) + dcol) = pack_bf16x2(os[n][0] * inv0, os[n][1] * inv0);
+            if (rB < Tq) *reinterpret_cast<uint32_t*>(out_row(rB) + dcol) = pack_bf16x2(os[n][2] * inv1, os[n][3] * inv1);
+        }
+#pragma unroll
+        for (int n = 0; n < R / 8; ++n) {
+            const int zcol = D_H + n * 8 + 2 * tq;
+            if (rA < Tq) *reinterpret_cast<uint32_t*>(out_row(rA) + zcol) = pack_bf16x2(oz[n][0] * inv0, oz[n][1] * inv0);
+            if (rB < Tq) *reinterpret_cast<uint32_t*>(out_row(rB) + zcol) = pack_bf16x2(oz[n][2] * inv1, oz[n][3] * inv1);
+        }
+        return;
+    }
     __syncwarp();
 #pragma unroll
     for (int n = 0; n < R / 8; ++n) {

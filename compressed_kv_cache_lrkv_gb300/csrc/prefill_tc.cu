@@ -78,9 +78,12 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, uint32_t
 
 constexpr int kThreads = 256;
 
-template <int D_H>
+// FUSED: absorbed weights -- Q~ arrives from the caller (TMA into the Q~ tile, no absorption
+// MMA) and the epilogue returns [O_s | O_z] / l (no B^V MMA).
+template <int D_H, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillMaps m, const PrefillArgs a) {
     constexpr int R = 16;
+    constexpr int OW = FUSED ? D_H + R : D_H;  // output row width
     constexpr int NB = D_H / 64;  // 64-column blocks of a row
     using Lay = PfLayout<D_H>;
     constexpr uint32_t OFF_Q = Lay::OFF_Q, OFF_QT = Lay::OFF_QT, OFF_BK = Lay::OFF_BK, OFF_BVF = Lay::OFF_BVF;
@@ -97,12 +100,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int qs = a.q_start[b];
     const int ctx = qs + Tq;
     const int q0 = qt * kBM;
-    auto out_row = [&](int i) { return a.out + (((size_t)b * Tq + i) * H + h) * D_H; };
+    auto out_row = [&](int i) { return a.out + (((size_t)b * Tq + i) * H + h) * OW; };
     if (qs < 0 || ctx > a.max_pages * kBlockSize) {
         if (threadIdx.x == 0 && qt == 0 && h == 0) set_status(a.status, LRKV_DEV_BAD_SEQLEN);
-        for (int idx = threadIdx.x; idx < kBM * D_H; idx += blockDim.x) {
-            const int i = q0 + idx / D_H;
-            if (i < Tq) out_row(i)[idx % D_H] = 0;
+        for (int idx = threadIdx.x; idx < kBM * OW; idx += blockDim.x) {
+            const int i = q0 + idx / OW;
+            if (i < Tq) out_row(i)[idx % OW] = 0;
         }
         return;
     }
@@ -185,10 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             return row;
         };
         if (keys && lane == 0) {
-            mbar_arrive_expect_tx(B(q_full), 128 * D_H * 2 + D_H * 32);
+            mbar_arrive_expect_tx(B(q_full), 128 * D_H * 2 + (FUSED ? 128 * R * 2 : D_H * R * 2));
 #pragma unroll
             for (int bk = 0; bk < NB; ++bk) tma_load_2d(S0 + OFF_Q + bk * 16384, &m.q, h * D_H + 64 * bk, b * Tq + q0, B(q_full));
-            tma_load_2d(S0 + OFF_BK, &m.BK, 0, h * D_H, B(q_full));
+            if (FUSED)
+                tma_load_2d(S0 + OFF_QT, &m.qt, h * R, b * Tq + q0, B(q_full));
+            else
+                tma_load_2d(S0 + OFF_BK, &m.BK, 0, h * D_H, B(q_full));
         }
         const int depth = keys ? kKStages : kVStages;
         uint64_t* full = keys ? k_full : v_full;
@@ -256,15 +262,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             // K-step kk of a K-major 128-byte-swizzled [rows][128] tile: 64-column block kk/4, 32 bytes in.
             auto kstep = [](int kk) -> uint64_t { return (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
             ok = wait_all(B(q_full), 0, a.status);
-            if (ok) {
-                tc_fence_after();
+            if (!FUSED) {
+                if (ok) {
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D_H / 16; ++kk)
-                    if (elect_one_sync()) tc_mma_bf16(tmem + TM_QT, dQ + kstep(kk), dBK + (kk * 512 >> 4), id_QT, kk > 0);
+                    for (int kk = 0; kk < D_H / 16; ++kk)
+                        if (elect_one_sync())
+                            tc_mma_bf16(tmem + TM_QT, dQ + kstep(kk), dBK + (kk * 512 >> 4), id_QT, kk > 0);
+                }
+                if (elect_one_sync()) tc_commit(B(qt_mma));
+                __syncwarp();
+                ok = ok && wait_all(B(qt_ready), 0, a.status);
             }
-            if (elect_one_sync()) tc_commit(B(qt_mma));
-            __syncwarp();
-            ok = ok && wait_all(B(qt_ready), 0, a.status);
             auto s_tile = [&](int jj, auto U) -> bool {
                 constexpr int st = decltype(U)::value % kKStages, sb = decltype(U)::value & 1;
                 // S buffer sb still holds P_{jj-2} until P_{jj-2} . V_{jj-2} has completed
@@ -336,7 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             // O_s += O_z . (B_h^V)^T.  O_z is read as an MMA operand, so its last
             // accumulation must have completed first.
             ok = ok && wait_all(B(o_done + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, a.status);
-            if (ok) {
+            if (ok && FUSED) {  // [O_s | O_z] leave as they are: fin_done only marks them complete
+                if (elect_one_sync()) tc_commit(B(fin_done));
+                __syncwarp();
+            } else if (ok) {
                 constexpr uint32_t id_fin = idesc_tf32_f32(128, D_H);
                 const uint64_t dBV = sdesc(S0 + OFF_BVF, 128, 512, 0);
                 tc_fence_after();
@@ -358,40 +370,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int row = qq * 32 + lane;              // query row within the tile = TMEM lane
         const uint32_t tl = (uint32_t)(qq * 32) << 16;
         const int st_tid = threadIdx.x - 64;         // 0..127
-        // Q~ row from TMEM -> bf16 -> shared memory (K-major, 32-byte swizzle).
-        bool ok = wait_all(B(qt_mma), 0, a.status);
-        tc_fence_after();
-        // B^K has been consumed (qt_mma): B_h^V, widened to fp32, takes its place for the
-        // final tf32 MMA -- thread d writes row d (16 values, 4 core-matrix chunks).
-        if (st_tid < D_H) {
-            const uint4* src = reinterpret_cast<const uint4*>(a.BV + ((size_t)h * D_H + st_tid) * R);
-            const uint4 w0 = src[0], w1 = src[1];
-            const uint32_t wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            uint8_t* rowp = smem + OFF_BVF + (st_tid >> 3) * 512 + (st_tid & 7) * 16;
+        bool ok = true;
+        if (!FUSED) {
+            // Q~ row from TMEM -> bf16 -> shared memory (K-major, 32-byte swizzle).
+            ok = wait_all(B(qt_mma), 0, a.status);
+            tc_fence_after();
+            // B^K has been consumed (qt_mma): B_h^V, widened to fp32, takes its place for the
+            // final tf32 MMA -- thread d writes row d (16 values, 4 core-matrix chunks).
+            if (st_tid < D_H) {
+                const uint4* src = reinterpret_cast<const uint4*>(a.BV + ((size_t)h * D_H + st_tid) * R);
+                const uint4 w0 = src[0], w1 = src[1];
+                const uint32_t wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                uint8_t* rowp = smem + OFF_BVF + (st_tid >> 3) * 512 + (st_tid & 7) * 16;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<float4*>(rowp + q4 * 128) =
-                    make_float4(bf16lo(wb[2 * q4]), bf16hi(wb[2 * q4]), bf16lo(wb[2 * q4 + 1]), bf16hi(wb[2 * q4 + 1]));
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<float4*>(rowp + q4 * 128) =
+                        make_float4(bf16lo(wb[2 * q4]), bf16hi(wb[2 * q4]), bf16lo(wb[2 * q4 + 1]), bf16hi(wb[2 * q4 + 1]));
+            }
+            {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem + tl + TM_QT, v);
+                uint4 c0, c1;
+                c0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+                c0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+                c0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+                c0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+                c1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
+                c1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
+                c1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
+                c1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
+                const int sw = (row >> 2) & 1;
+                *reinterpret_cast<uint4*>(smem + OFF_QT + row * 32 + ((0 ^ sw) << 4)) = c0;
+                *reinterpret_cast<uint4*>(smem + OFF_QT + row * 32 + ((1 ^ sw) << 4)) = c1;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(B(qt_ready));
         }
-        {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(tmem + tl + TM_QT, v);
-            uint4 c0, c1;
-            c0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
-            c0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
-            c0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
-            c0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
-            c1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
-            c1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
-            c1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
-            c1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
-            const int sw = (row >> 2) & 1;
-            *reinterpret_cast<uint4*>(smem + OFF_QT + row * 32 + ((0 ^ sw) << 4)) = c0;
-            *reinterpret_cast<uint4*>(smem + OFF_QT + row * 32 + ((1 ^ sw) << 4)) = c1;
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(B(qt_ready));
 
         const int qpos = qs + min(q0 + row, Tq - 1);
         float mref = -INFINITY, l = 0.f;
@@ -500,7 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             tc_fence_before();
             mbar_arrive(B(p_full));
         }
-        // ---- epilogue: out = O_s / l (O_s already holds the B_h^V O_z term)
+        // ---- epilogue: out = O_s / l (O_s already holds the B_h^V O_z term); absorbed weights:
+        // out = [O_s | O_z] / l
         if (ok) ok = wait_all(B(fin_done), 0, a.status);
         if (ok) {
             tc_fence_after();
@@ -520,6 +536,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
             }
+            if (FUSED) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem + tl + TM_OZ, v);
+                if (qrow < Tq) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2)
+                        pk[e / 2] = pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+                    uint4* dst = reinterpret_cast<uint4*>(out_row(qrow) + D_H);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+            }
         }
         if (!ok) *abort_flag = 1;
     }
@@ -531,18 +560,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
 }
 
-template <int D_H>
+template <int D_H, bool FUSED>
 static cudaError_t launch_prefill_tc_t(const PrefillMaps& maps, const PrefillArgs& a, cudaStream_t stream) {
     constexpr uint32_t smem = PfLayout<D_H>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D_H>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kern = prefill_tc_kernel<D_H, FUSED>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.Tq + kBM - 1) / kBM, a.H, a.B);
-    prefill_tc_kernel<D_H><<<grid, kThreads, smem, stream>>>(maps, a);
+    kern<<<grid, kThreads, smem, stream>>>(maps, a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int d_h, cudaStream_t stream) {
-    return d_h == 64 ? launch_prefill_tc_t<64>(maps, a, stream) : launch_prefill_tc_t<128>(maps, a, stream);
+    if (a.qt) return d_h == 64 ? launch_prefill_tc_t<64, true>(maps, a, stream) : launch_prefill_tc_t<128, true>(maps, a, stream);
+    return d_h == 64 ? launch_prefill_tc_t<64, false>(maps, a, stream) : launch_prefill_tc_t<128, false>(maps, a, stream);
 }
 
 }  // namespace lrkv

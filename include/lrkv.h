@@ -284,6 +284,25 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, const void* q, const void* BK, c
                          const int32_t* q_start, int32_t batch, int32_t Tq, void* out, void* workspace,
                          size_t workspace_bytes, uint32_t* status_dev, void* stream);
 
+/*
+ * lrkv_prefill_fused -- lrkv_prefill with both absorptions moved into the caller's
+ *   weights, as lrkv_decode_fused does for one query (associativity of frame "Compute
+ *   logits without expanding historical keys", step 1, and of Eq. (7)): query i of
+ *   sequence b, at absolute position p = q_start[b] + i, arrives with q~_i = q_i B_h^K
+ *   already projected, and head h returns
+ *     out = [ sum_{j<=p} a_j s^V_j  |  sum_{j<=p} a_j z^V_{h,j} ]   (width d_h + r),
+ *     a = softmax_{j<=p}(([q_i | q~_i] . [s^K_j | z^K_{h,j}]) * scale)
+ *   (with a positional key, [q | q^R | q~] . [s^K | k^R | z^K_h]).
+ *   q        [batch][Tq][H][d_h + d_rope]  bf16
+ *   q_tilde  [batch][Tq][H][r]             bf16, 16-byte aligned
+ *   out      [batch][Tq][H][d_h + r]       bf16 (nearest, ties to even from fp32)
+ *   Everything else (cache, block_table, q_start, status, errors, the stream) is as
+ *   for lrkv_prefill; no B^K or B^V is read and no workspace is needed.
+ */
+lrkv_status lrkv_prefill_fused(const lrkv_dims* dims, const void* q, const void* q_tilde, const lrkv_cache* cache,
+                               const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* q_start,
+                               int32_t batch, int32_t Tq, void* out, uint32_t* status_dev, void* stream);
+
 /* ======================================================================
  * Training-time expanded projections ("Low-Rank Key Value Attention", frame
  * "Training learns the base and residuals together": the full per-head features

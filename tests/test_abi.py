@@ -19,7 +19,8 @@ def _declared():
 
 def test_header_declares_expected_calls():
     names = _declared()
-    for n in ("lrkv_append", "lrkv_decode", "lrkv_decode_fused", "lrkv_prefill", "lrkv_decode_workspace_bytes",
+    for n in ("lrkv_append", "lrkv_decode", "lrkv_decode_fused", "lrkv_prefill", "lrkv_prefill_fused",
+              "lrkv_decode_workspace_bytes",
               "lrkv_status_string", "lrkv_append_layers", "lrkv_decode_layers"):
         assert n in names
 
@@ -89,6 +90,19 @@ def test_null_and_misaligned_pointers_rejected():
     assert b"aligned" in lib.lrkv_last_error()
     assert lib.lrkv_decode_fused(ctypes.byref(dims), 16, 16, ctypes.byref(c), 16, 1, 16, 0, 16, 256, 0, None,
                                  None) == 0
+    # absorbed-weights prefill: the same rules for q~; batch 0 or Tq 0 is a no-op
+    assert lib.lrkv_prefill_fused(ctypes.byref(dims), 16, None, ctypes.byref(c), 16, 1, 16, 1, 4, 16, None,
+                                  None) == 1
+    assert b"q_tilde" in lib.lrkv_last_error()
+    assert lib.lrkv_prefill_fused(ctypes.byref(dims), 16, 24, ctypes.byref(c), 16, 1, 16, 1, 4, 16, None,
+                                  None) == 1
+    assert b"aligned" in lib.lrkv_last_error()
+    assert lib.lrkv_prefill_fused(ctypes.byref(dims), 16, 16, ctypes.byref(c), 16, 1, 16, 1, -1, 16, None,
+                                  None) == 1
+    assert lib.lrkv_prefill_fused(ctypes.byref(dims), 16, 16, ctypes.byref(c), 16, 1, 16, 0, 4, 16, None,
+                                  None) == 0
+    assert lib.lrkv_prefill_fused(ctypes.byref(dims), 16, 16, ctypes.byref(c), 16, 1, 16, 3, 0, 16, None,
+                                  None) == 0
 
 
 def test_nan_scale_rejected():

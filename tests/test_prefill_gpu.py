@@ -151,3 +151,60 @@ def test_prefill_bad_context_reports_status():
     out, st = run_prefill(H, d_h, r, pools, pt, np.array([40], np.int32), q, w.BK, w.BV)  # 40 + 32 > 64
     assert st & b.DEV_BAD_SEQLEN
     assert np.all(host_f64(out) == 0)
+
+
+FUSED_CASES = [
+    # H, d_h, r, d_rope, Tq, q_starts -- d_h = 128 or 64 with r = 16 and no positional key
+    # runs the tcgen05 kernel, the rest the warp-level one
+    (2, 128, 16, 0, 300, [37, 1000]),
+    (3, 128, 16, 0, 512, [3584, 0]),
+    (12, 64, 16, 0, 129, [127, 64]),
+    (2, 64, 16, 0, 1, [4095, 0]),
+    (4, 64, 8, 0, 130, [0, 100]),
+    (3, 64, 32, 0, 17, [511, 5]),
+    (2, 128, 16, 64, 96, [256, 0]),
+    (4, 128, 32, 64, 1, [0, 1000]),
+]
+
+
+@pytest.mark.parametrize("H,d_h,r,d_rope,Tq,qs", FUSED_CASES,
+                         ids=[f"H{c[0]}_dh{c[1]}_r{c[2]}_rope{c[3]}_T{c[4]}" for c in FUSED_CASES])
+def test_prefill_fused_matches_oracle(H, d_h, r, d_rope, Tq, qs):
+    """lrkv_prefill_fused (q~ given, [o_s | o_z] returned) against the oracle's causal prefill
+    with absorbed weights."""
+    seed = 610 + H + r + Tq + d_rope
+    pt = S.page_table(seed, [s + Tq for s in qs], 64, spare_blocks=1)
+    pools = random_pools(seed, pt.num_blocks, H, d_h, r, d_rope=d_rope)
+    q = S.gaussian_bf16(seed, "q", (len(qs), Tq, H, d_h + d_rope))
+    qt = S.gaussian_bf16(seed, "qt", (len(qs), Tq, H, r))
+    q_start = np.array(qs, np.int32)
+    dims = b.make_dims(H, d_h, r, H * d_h, d_rope=d_rope)
+    cache = b.PagedCache(*(dev_bf16(p) for p in pools))
+    out = torch.empty((len(qs), Tq, H, d_h + r), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    b.lrkv_prefill_fused(dims, dev_bf16(q), dev_bf16(qt), cache, dev_i32(pt.block_table), dev_i32(q_start), out,
+                         status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle.get().prefill_fused(pools, pt.block_table, q_start, q, qt)
+    assert_close(host_f64(out), ref, f"absorbed prefill H={H} d_h={d_h} r={r} d_rope={d_rope} Tq={Tq}")
+
+
+@pytest.mark.parametrize("d_h,r", [(128, 16), (64, 8)])
+def test_prefill_fused_bad_context_zeroes_rows(d_h, r):
+    """A context past the block table: status LRKV_DEV_BAD_SEQLEN and all d_h + r columns zeroed
+    (tcgen05 kernel for r = 16, warp-level kernel for r = 8)."""
+    H, Tq = 2, 32
+    pt = S.page_table(7, [64], 64)
+    pools = random_pools(7, pt.num_blocks, H, d_h, r)
+    q = S.gaussian_bf16(7, "q", (1, Tq, H, d_h))
+    qt = S.gaussian_bf16(7, "qt", (1, Tq, H, r))
+    dims = b.make_dims(H, d_h, r, H * d_h)
+    cache = b.PagedCache(*(dev_bf16(p) for p in pools))
+    out = torch.full((1, Tq, H, d_h + r), 1.0, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    b.lrkv_prefill_fused(dims, dev_bf16(q), dev_bf16(qt), cache, dev_i32(pt.block_table),
+                         dev_i32(np.array([40], np.int32)), out, status=st)  # 40 + 32 > 64
+    torch.cuda.synchronize()
+    assert int(st.item()) & b.DEV_BAD_SEQLEN
+    assert float(out.abs().max()) == 0.0
