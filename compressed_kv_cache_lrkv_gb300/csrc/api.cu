@@ -564,14 +564,16 @@ static lrkv_status prefill_impl(bool fused, const lrkv_dims* dims, const void* q
     a.max_pages = max_blocks_per_seq;
     a.num_blocks = cache->num_blocks;
     a.scale_log2 = logit_scale(dims) * 1.4426950408889634f;
-    if ((dims->d_h == 64 || dims->d_h == 128) && dims->r == 16 && dims->d_rope == 0) {
+    const bool tc = (dims->d_h == 64 || dims->d_h == 128) && dims->r == 16 &&
+                    (dims->d_rope == 0 || (dims->d_rope == 64 && dims->d_h == 128 && !fused));
+    if (tc) {
         lrkv::PrefillMaps mp;
-        const uint64_t dh = (uint64_t)dims->d_h;
+        const uint64_t dh = (uint64_t)dims->d_h, dk = dh + (uint64_t)dims->d_rope;
         const uint64_t rows = (uint64_t)cache->num_blocks * dims->block_size;
         const uint64_t HR = (uint64_t)dims->H * dims->r;
-        if ((s = make_tmap(&mp.q, q, (uint64_t)dims->H * dh, (uint64_t)batch * Tq, 64, 128,
+        if ((s = make_tmap(&mp.q, q, (uint64_t)dims->H * dk, (uint64_t)batch * Tq, 64, 128,
                            CU_TENSOR_MAP_SWIZZLE_128B, "q")) != LRKV_OK ||
-            (s = make_tmap(&mp.sK, cache->sK, dh, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "sK")) != LRKV_OK ||
+            (s = make_tmap(&mp.sK, cache->sK, dk, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "sK")) != LRKV_OK ||
             (s = make_tmap(&mp.sV, cache->sV, dh, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "sV")) != LRKV_OK ||
             (s = make_tmap(&mp.zK, cache->zK, HR, rows, 16, 64, CU_TENSOR_MAP_SWIZZLE_32B, "zK")) != LRKV_OK ||
             (s = make_tmap(&mp.zV, cache->zV, HR, rows, 16, 64, CU_TENSOR_MAP_SWIZZLE_32B, "zV")) != LRKV_OK)
@@ -584,7 +586,8 @@ static lrkv_status prefill_impl(bool fused, const lrkv_dims* dims, const void* q
             mp.qt = mp.BK;
         }
         if (s != LRKV_OK) return s;
-        return cuda_status(lrkv::launch_prefill_tc(mp, a, dims->d_h, static_cast<cudaStream_t>(stream)), what);
+        return cuda_status(lrkv::launch_prefill_tc(mp, a, dims->d_h, dims->d_rope, static_cast<cudaStream_t>(stream)),
+                           what);
     }
     return cuda_status(lrkv::launch_prefill(a, dims->d_h, dims->r, dims->d_rope, static_cast<cudaStream_t>(stream)),
                        what);

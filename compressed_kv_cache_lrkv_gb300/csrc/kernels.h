@@ -111,13 +111,14 @@ cudaError_t launch_decode_tc_split(const CUtensorMap& tK, const CUtensorMap& tV,
 
 cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, int D_R, cudaStream_t stream);
 
-// Tensor-core prefill (d_h = 64 or 128, r = 16).  Maps: q as [B*Tq][H*d_h] box {64,128}
-// and s^K, s^V pools [nb*64][d_h] box {64,64}, both 128-byte swizzle; z^K, z^V
+// Tensor-core prefill (d_h = 64 or 128 with r = 16; d_rope = 64 with d_h = 128 and no absorbed
+// weights).  Maps: q as [B*Tq][H*(d_h + d_rope)] box {64,128} and s^K ([s^K | k^R]), s^V pools
+// [nb*64][d_h + d_rope], [nb*64][d_h] box {64,64}, all 128-byte swizzle; z^K, z^V
 // pools [nb*64][H*r] box {16,64} and B^K as [H*d_h][r] box {16,d_h}, 32-byte swizzle;
 // with absorbed weights, q~ as [B*Tq][H*r] box {16,128}, 32-byte swizzle, in place of B^K.
 struct PrefillMaps {
     CUtensorMap q, sK, sV, zK, zV, BK, qt;
 };
-cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int d_h, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int d_h, int d_rope, cudaStream_t stream);
 
 }  // namespace lrkv

@@ -1,6 +1,7 @@
 // prefill_tc.cu -- causal chunked prefill on the 5th-generation tensor cores
 // ("Low-Rank Key Value Attention", Eqs. (6)-(7) with the causal mask of the
-// softmax frame), for d_h = 64 or 128 and r = 16.
+// softmax frame), for d_h = 64 or 128 and r = 16, and for d_h = 128 with the decoupled
+// positional key (d_rope = 64: key rows [s^K | k^R], queries [q | q^R]).
 //
 // One CTA = 128 queries of one (sequence, head); key tiles of 128 tokens (two
 // cache pages).  Per tile j:
@@ -20,6 +21,11 @@
 // by more than 2^8, so most tiles need no O round trip.  Key rows past the
 // context are zero-filled (TMA out-of-bounds fill, or cleared in shared memory)
 // so masked tokens cannot inject NaN through 0 * garbage.
+// With a positional key the shared logits run over D_K = d_h + 64 columns and the key ring
+// has two stages (its stages grow by 16 KB); Q~ then lives in TMEM as the A operand of its
+// MMA instead of in shared memory, B^K is staged in the second value stage (the value
+// producer fills that stage only after the Q~ MMA has read it) and B^V, at the end, in the
+// first key stage.
 #include <type_traits>
 
 #include "kernels.h"
@@ -30,31 +36,43 @@ namespace lrkv {
 namespace {
 
 constexpr int kBM = 128, kBN = 128;
-constexpr int kKStages = 3, kVStages = 2;
-// Shared-memory layout for d_h = D_H (64 or 128; the tiles are D_H / 64 blocks of 64 columns):
-//   Q    [128 q][D_H] K-major, 128B swizzle
-//   Q~   [128 q][16] K-major, 32B swizzle
-//   B^K  [D_H d][16] MN-major (B operand of Q~), 32B swizzle; after the prologue this area (and
-//        the same again after it) holds B_h^V as fp32 for the final tf32 MMA: [D_H d][16 j],
-//        K-major without swizzle -- 8 x 4-element core matrices, element (d, j) at
-//        (d / 8) * 512 + (j / 4) * 128 + (d % 8) * 16 + (j % 4) * 4
-//   key ring (3 stages: s^K [128 keys][D_H] K-major 128B swizzle, then z^K_h [128][16] 32B
-//   swizzle) and value ring (2 stages: s^V, z^V_h, same layouts, read MN-major).
-template <int D_H>
+constexpr int kVStages = 2;
+// Shared-memory layout for d_h = D_H and a positional key of D_R columns (the tiles are blocks
+// of 64 columns; D_K = D_H + D_R):
+//   Q    [128 q][D_K] K-major, 128B swizzle
+//   Q~   [128 q][16] K-major, 32B swizzle (no positional key; with one, Q~ sits in TMEM)
+//   B^K  [D_H d][16] MN-major (B operand of Q~), 32B swizzle
+//   B^V  as fp32 for the final tf32 MMA: [D_H d][16 j], K-major without swizzle -- 8 x
+//        4-element core matrices, element (d, j) at (d / 8) * 512 + (j / 4) * 128 + (d % 8) * 16
+//        + (j % 4) * 4.  Without a positional key it takes the place of B^K (and the 4 KB
+//        after it) once Q~ is computed; with one it goes into key stage 0 after the last S MMA.
+//   key ring (3 stages, 2 with a positional key: [s^K | k^R] [128 keys][D_K] K-major 128B
+//   swizzle, then z^K_h [128][16] 32B swizzle) and value ring (2 stages: s^V [128][D_H],
+//   z^V_h, same layouts, read MN-major); with a positional key B^K sits in value stage 1.
+template <int D_H, int D_R>
 struct PfLayout {
+    static constexpr bool ROPE = D_R > 0;
+    static constexpr int D_K = D_H + D_R;
+    static constexpr int KST = ROPE ? 2 : 3;  // key ring stages
     static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_QT = 128 * D_H * 2;
-    static constexpr uint32_t OFF_BK = OFF_QT + 4096;
-    static constexpr uint32_t OFF_BVF = OFF_BK;
-    static constexpr uint32_t STAGE_Z = 128 * D_H * 2;
-    static constexpr uint32_t STAGE_BYTES = STAGE_Z + 4096;
-    static constexpr uint32_t OFF_K = OFF_BK + D_H * 64;
-    static constexpr uint32_t OFF_V = OFF_K + kKStages * STAGE_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_V + kVStages * STAGE_BYTES;
+    static constexpr uint32_t Q_BYTES = 128 * D_K * 2;
+    static constexpr uint32_t K_Z = 128 * D_K * 2, K_BYTES = K_Z + 4096;  // key stage: [s^K | k^R], z^K_h
+    static constexpr uint32_t V_Z = 128 * D_H * 2, V_BYTES = V_Z + 4096;  // value stage: s^V, z^V_h
+    static constexpr uint32_t OFF_QT = Q_BYTES;
+    static constexpr uint32_t OFF_K = ROPE ? Q_BYTES : OFF_QT + 4096 + D_H * 64;
+    static constexpr uint32_t OFF_V = OFF_K + KST * K_BYTES;
+    static constexpr uint32_t OFF_BK = ROPE ? OFF_V + V_BYTES : OFF_QT + 4096;
+    static constexpr uint32_t OFF_BVF = ROPE ? OFF_K : OFF_BK;
+    static constexpr uint32_t OFF_BAR = OFF_V + kVStages * V_BYTES;
     static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
-    static_assert(OFF_K % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzled TMA tiles start 1024-aligned");
+    static_assert(OFF_K % 1024 == 0 && K_BYTES % 1024 == 0 && V_BYTES % 1024 == 0 && OFF_BK % 1024 == 0,
+                  "swizzled TMA tiles start 1024-aligned");
+    static_assert(D_H * 64 <= (ROPE ? K_BYTES : 8192), "B^V (fp32) fits its area");
+    static_assert(SMEM <= 232448, "fits one CTA's opt-in shared memory");
 };
-constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_OS = 256, TM_OZ = 384, TM_QT = 448, TM_COLS = 512;
+// TMEM columns: S buffers, O_s, O_z, Q~ (fp32 from its MMA) and, with a positional key, Q~ as
+// bf16 pairs (the A operand of its MMA).
+constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_OS = 256, TM_OZ = 384, TM_QTB = 400, TM_QT = 448, TM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 __device__ __forceinline__ uint64_t kdesc128(uint32_t a) { return sdesc(a, 16, 1024, 2); }
@@ -69,6 +87,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
+// 32 lanes x 8 consecutive 32-bit columns, register -> TMEM.
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t* v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, uint32_t* status) {
     const bool ok = mbar_wait(bar, parity, status);
     return __all_sync(0xffffffffu, ok);
@@ -80,14 +105,17 @@ constexpr int kThreads = 256;
 
 // FUSED: absorbed weights -- Q~ arrives from the caller (TMA into the Q~ tile, no absorption
 // MMA) and the epilogue returns [O_s | O_z] / l (no B^V MMA).
-template <int D_H, bool FUSED>
+template <int D_H, int D_R, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillMaps m, const PrefillArgs a) {
     constexpr int R = 16;
     constexpr int OW = FUSED ? D_H + R : D_H;  // output row width
-    constexpr int NB = D_H / 64;  // 64-column blocks of a row
-    using Lay = PfLayout<D_H>;
+    using Lay = PfLayout<D_H, D_R>;
+    constexpr bool ROPE = Lay::ROPE;
+    static_assert(!(ROPE && FUSED), "absorbed weights with a positional key run on the warp-level kernel");
+    constexpr int D_K = Lay::D_K, KST = Lay::KST;
+    constexpr int NBK = D_K / 64, NBV = D_H / 64;  // 64-column blocks of a key / value row
     constexpr uint32_t OFF_Q = Lay::OFF_Q, OFF_QT = Lay::OFF_QT, OFF_BK = Lay::OFF_BK, OFF_BVF = Lay::OFF_BVF;
-    constexpr uint32_t STAGE_Z = Lay::STAGE_Z, STAGE_BYTES = Lay::STAGE_BYTES;
+    constexpr uint32_t K_Z = Lay::K_Z, K_BYTES = Lay::K_BYTES, V_Z = Lay::V_Z, V_BYTES = Lay::V_BYTES;
     constexpr uint32_t OFF_K = Lay::OFF_K, OFF_V = Lay::OFF_V, OFF_BAR = Lay::OFF_BAR;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -132,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     volatile int* abort_flag = reinterpret_cast<int*>(bars + 19);
     uint64_t* s_free = bars + 20;    // [2] P_j . V_j done: S buffer j % 2 may take S_{j+2}
     uint64_t* pv_drain = bars + 22;  // all P.V MMAs complete
+    uint64_t* bvf_ready = bars + 26;  // positional key: B^V (fp32) written into key stage 0
     auto B = [&](uint64_t* p) { return smem_u32(p); };
     // The abort flag is read warp-uniformly: a warp whose lanes saw different values would
     // reach its later warp-wide votes and shuffles with only some of its lanes.
@@ -141,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         mbar_init(B(q_full), 1);
         mbar_init(B(qt_mma), 1);
         mbar_init(B(qt_ready), 128);
-        for (int i = 0; i < kKStages; ++i) {
+        for (int i = 0; i < KST; ++i) {
             mbar_init(B(k_full + i), 1);
             mbar_init(B(k_empty + i), 1);
         }
@@ -153,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         mbar_init(B(p_full), 128);
         for (int i = 0; i < 2; ++i) mbar_init(B(o_done + i), 1);
         mbar_init(B(fin_done), 1);
+        mbar_init(B(bvf_ready), 128);
         mbar_init(B(mma_drain), 1);
         mbar_init(B(pv_drain), 1);
         for (int i = 0; i < 2; ++i) mbar_init(B(s_free + i), 1);
@@ -188,15 +218,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             return row;
         };
         if (keys && lane == 0) {
-            mbar_arrive_expect_tx(B(q_full), 128 * D_H * 2 + (FUSED ? 128 * R * 2 : D_H * R * 2));
+            mbar_arrive_expect_tx(B(q_full), 128 * D_K * 2 + (FUSED ? 128 * R * 2 : D_H * R * 2));
 #pragma unroll
-            for (int bk = 0; bk < NB; ++bk) tma_load_2d(S0 + OFF_Q + bk * 16384, &m.q, h * D_H + 64 * bk, b * Tq + q0, B(q_full));
+            for (int bk = 0; bk < NBK; ++bk) tma_load_2d(S0 + OFF_Q + bk * 16384, &m.q, h * D_K + 64 * bk, b * Tq + q0, B(q_full));
             if (FUSED)
                 tma_load_2d(S0 + OFF_QT, &m.qt, h * R, b * Tq + q0, B(q_full));
             else
                 tma_load_2d(S0 + OFF_BK, &m.BK, 0, h * D_H, B(q_full));
         }
-        const int depth = keys ? kKStages : kVStages;
+        const int depth = keys ? KST : kVStages;
+        const uint32_t stage_bytes = keys ? K_BYTES : V_BYTES, zoff = keys ? K_Z : V_Z;
+        const int nblk = keys ? NBK : NBV;
         uint64_t* full = keys ? k_full : v_full;
         uint64_t* empty = keys ? k_empty : v_empty;
         const CUtensorMap* ms = keys ? &m.sK : &m.sV;
@@ -217,18 +249,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 ok = false;
                 break;
             }
+            // with a positional key, value stage 1 holds B^K until the Q~ MMA has read it
+            if (ROPE && !keys && j == 1 && !wait_all(B(qt_mma), 0, a.status)) {
+                ok = false;
+                break;
+            }
             if (aborted()) {
                 ok = false;
                 break;
             }
             if (lane == 0) {
-                const uint32_t base = ring + st * STAGE_BYTES, bar = B(full + st);
-                mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                const uint32_t base = ring + st * stage_bytes, bar = B(full + st);
+                mbar_arrive_expect_tx(bar, stage_bytes);
                 for (int p = 0; p < 2; ++p) {
                     const int row = p ? row1 : row0;
-#pragma unroll
-                    for (int bk = 0; bk < NB; ++bk) tma_load_2d(base + bk * 16384 + p * 8192, ms, 64 * bk, row, bar);
-                    tma_load_2d(base + STAGE_Z + p * 2048, mz, h * R, row, bar);
+                    for (int bk = 0; bk < nblk; ++bk) tma_load_2d(base + bk * 16384 + p * 8192, ms, 64 * bk, row, bar);
+                    tma_load_2d(base + zoff + p * 2048, mz, h * R, row, bar);
                 }
             }
             __syncwarp();
@@ -254,11 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         constexpr uint32_t id_QT = idesc_bf16_f32(128, 16) | (1u << 16);
         constexpr uint32_t id_PVs = idesc_bf16_f32(128, D_H) | (1u << 16);
         constexpr uint32_t id_PVz = idesc_bf16_f32(128, 16) | (1u << 16);
-        constexpr uint64_t kStage = STAGE_BYTES >> 4;
+        constexpr uint64_t kKStage = K_BYTES >> 4, kVStage = V_BYTES >> 4;
         bool ok = true;
         if (warp == 1) {
             const uint64_t dQ = kdesc128(S0 + OFF_Q), dQT = kdesc32(S0 + OFF_QT), dBK = mndesc32(S0 + OFF_BK);
-            const uint64_t dSK = kdesc128(S0 + OFF_K), dZK = kdesc32(S0 + OFF_K + STAGE_Z);
+            const uint64_t dSK = kdesc128(S0 + OFF_K), dZK = kdesc32(S0 + OFF_K + K_Z);
             // K-step kk of a K-major 128-byte-swizzled [rows][128] tile: 64-column block kk/4, 32 bytes in.
             auto kstep = [](int kk) -> uint64_t { return (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
             ok = wait_all(B(q_full), 0, a.status);
@@ -275,19 +311,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 ok = ok && wait_all(B(qt_ready), 0, a.status);
             }
             auto s_tile = [&](int jj, auto U) -> bool {
-                constexpr int st = decltype(U)::value % kKStages, sb = decltype(U)::value & 1;
+                constexpr int st = decltype(U)::value % KST, sb = decltype(U)::value & 1;
                 // S buffer sb still holds P_{jj-2} until P_{jj-2} . V_{jj-2} has completed
-                if (aborted() || !wait_all(B(k_full + st), (jj / kKStages) & 1, a.status) ||
+                if (aborted() || !wait_all(B(k_full + st), (jj / KST) & 1, a.status) ||
                     (jj >= 2 && !wait_all(B(s_free + sb), ((jj >> 1) - 1) & 1, a.status)))
                     return false;
                 tc_fence_after();
-                constexpr uint64_t so = st * kStage;
+                constexpr uint64_t so = st * kKStage;
                 const uint32_t d = tmem + (sb ? TM_S1 : TM_S0);
 #pragma unroll
-                for (int kk = 0; kk < D_H / 16; ++kk)
+                for (int kk = 0; kk < D_K / 16; ++kk)
                     if (elect_one_sync()) tc_mma_bf16(d, dQ + kstep(kk), dSK + so + kstep(kk), id_S, kk > 0);
                 if (elect_one_sync()) {
-                    tc_mma_bf16(d, dQT, dZK + so, id_S, 1);
+                    if (ROPE)
+                        tc_mma_bf16_ts(d, tmem + TM_QTB, dZK + so, id_S, 1);
+                    else
+                        tc_mma_bf16(d, dQT, dZK + so, id_S, 1);
                     tc_commit(B(s_full + sb));
                     tc_commit(B(k_empty + st));
                 }
@@ -314,14 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             __syncwarp();
             wait_all(B(mma_drain), 0, a.status);
         } else {
-            const uint64_t dSV = mndesc128(S0 + OFF_V), dZV = mndesc32(S0 + OFF_V + STAGE_Z);
+            const uint64_t dSV = mndesc128(S0 + OFF_V), dZV = mndesc32(S0 + OFF_V + V_Z);
             auto pv_tile = [&](int j, auto PAR) -> bool {
                 constexpr int vs = decltype(PAR)::value;  // value stage = S buffer = j % 2
                 if (aborted() || !wait_all(B(p_full), j & 1, a.status) ||
                     !wait_all(B(v_full + vs), (j >> 1) & 1, a.status))
                     return false;
                 tc_fence_after();
-                constexpr uint64_t so = vs * kStage;
+                constexpr uint64_t so = vs * kVStage;
                 const uint32_t pt = tmem + (vs ? TM_S1 : TM_S0);  // P_j over S_j's columns
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -345,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             // O_s += O_z . (B_h^V)^T.  O_z is read as an MMA operand, so its last
             // accumulation must have completed first.
             ok = ok && wait_all(B(o_done + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, a.status);
+            if (ROPE) ok = ok && wait_all(B(bvf_ready), 0, a.status);  // B^V in key stage 0
             if (ok && FUSED) {  // [O_s | O_z] leave as they are: fin_done only marks them complete
                 if (elect_one_sync()) tc_commit(B(fin_done));
                 __syncwarp();
@@ -370,13 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int row = qq * 32 + lane;              // query row within the tile = TMEM lane
         const uint32_t tl = (uint32_t)(qq * 32) << 16;
         const int st_tid = threadIdx.x - 64;         // 0..127
-        bool ok = true;
-        if (!FUSED) {
-            // Q~ row from TMEM -> bf16 -> shared memory (K-major, 32-byte swizzle).
-            ok = wait_all(B(qt_mma), 0, a.status);
-            tc_fence_after();
-            // B^K has been consumed (qt_mma): B_h^V, widened to fp32, takes its place for the
-            // final tf32 MMA -- thread d writes row d (16 values, 4 core-matrix chunks).
+        // B_h^V widened to fp32 for the final tf32 MMA: thread d writes row d (16 values, 4
+        // core-matrix chunks).
+        auto stage_bv = [&]() {
             if (st_tid < D_H) {
                 const uint4* src = reinterpret_cast<const uint4*>(a.BV + ((size_t)h * D_H + st_tid) * R);
                 const uint4 w0 = src[0], w1 = src[1];
@@ -384,24 +420,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 uint8_t* rowp = smem + OFF_BVF + (st_tid >> 3) * 512 + (st_tid & 7) * 16;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<float4*>(rowp + q4 * 128) =
-                        make_float4(bf16lo(wb[2 * q4]), bf16hi(wb[2 * q4]), bf16lo(wb[2 * q4 + 1]), bf16hi(wb[2 * q4 + 1]));
+                    *reinterpret_cast<float4*>(rowp + q4 * 128) = make_float4(
+                        bf16lo(wb[2 * q4]), bf16hi(wb[2 * q4]), bf16lo(wb[2 * q4 + 1]), bf16hi(wb[2 * q4 + 1]));
             }
-            {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(tmem + tl + TM_QT, v);
-                uint4 c0, c1;
-                c0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
-                c0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
-                c0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
-                c0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
-                c1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
-                c1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
-                c1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
-                c1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
+        };
+        bool ok = true;
+        if (!FUSED) {
+            // Q~ row from TMEM -> bf16 -> shared memory (K-major, 32-byte swizzle), or with a
+            // positional key back into TMEM as bf16 pairs (the A operand of its MMA).
+            ok = wait_all(B(qt_mma), 0, a.status);
+            tc_fence_after();
+            // B^K has been consumed (qt_mma): without a positional key B_h^V takes its place.
+            if (!ROPE) stage_bv();
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(tmem + tl + TM_QT, v);
+            uint32_t c[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) c[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+            if (ROPE) {
+                tmem_st_32x32b_x8(tmem + tl + TM_QTB, c);
+                tmem_wait_st();
+            } else {
                 const int sw = (row >> 2) & 1;
-                *reinterpret_cast<uint4*>(smem + OFF_QT + row * 32 + ((0 ^ sw) << 4)) = c0;
-                *reinterpret_cast<uint4*>(smem + OFF_QT + row * 32 + ((1 ^ sw) << 4)) = c1;
+                *reinterpret_cast<uint4*>(smem + OFF_QT + row * 32 + ((0 ^ sw) << 4)) = make_uint4(c[0], c[1], c[2], c[3]);
+                *reinterpret_cast<uint4*>(smem + OFF_QT + row * 32 + ((1 ^ sw) << 4)) = make_uint4(c[4], c[5], c[6], c[7]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -452,15 +494,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const float muse = raise ? mnew : mref;
             const float alpha = raise ? ((mref == -INFINITY) ? 0.f : ex2_approx(mref - mnew)) : 1.f;
             // Key rows past the context may hold any bits: clear them before P . V reads them.
-            const uint32_t kvb = OFF_V + (j % kVStages) * STAGE_BYTES;
+            const uint32_t kvb = OFF_V + (j % kVStages) * V_BYTES;
             if (k0 + kBN > ctx) {
                 ok = wait_all(B(v_full + (j & 1)), (j >> 1) & 1, a.status);
                 if (!ok) break;
                 if (k0 + row >= ctx) {
                     const uint4 z = make_uint4(0, 0, 0, 0);
-                    uint4* rz = reinterpret_cast<uint4*>(smem + kvb + STAGE_Z + row * 32);
+                    uint4* rz = reinterpret_cast<uint4*>(smem + kvb + V_Z + row * 32);
 #pragma unroll
-                    for (int bk = 0; bk < NB; ++bk) {
+                    for (int bk = 0; bk < NBV; ++bk) {
                         uint4* r0 = reinterpret_cast<uint4*>(smem + kvb + bk * 16384 + row * 128);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) r0[i] = z;
@@ -515,6 +557,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             tc_fence_before();
             mbar_arrive(B(p_full));
         }
+        if (ROPE) {
+            // Every S MMA has completed (S_{nt-1} was read above), so key stage 0 is free:
+            // B_h^V goes there for the final MMA.  Arrive even on failure, so that MMA's wait ends.
+            if (ok) stage_bv();
+            fence_proxy_async_smem();
+            mbar_arrive(B(bvf_ready));
+        }
         // ---- epilogue: out = O_s / l (O_s already holds the B_h^V O_z term); absorbed weights:
         // out = [O_s | O_z] / l
         if (ok) ok = wait_all(B(fin_done), 0, a.status);
@@ -560,10 +609,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
 }
 
-template <int D_H, bool FUSED>
+template <int D_H, int D_R, bool FUSED>
 static cudaError_t launch_prefill_tc_t(const PrefillMaps& maps, const PrefillArgs& a, cudaStream_t stream) {
-    constexpr uint32_t smem = PfLayout<D_H>::SMEM;
-    auto kern = prefill_tc_kernel<D_H, FUSED>;
+    constexpr uint32_t smem = PfLayout<D_H, D_R>::SMEM;
+    auto kern = prefill_tc_kernel<D_H, D_R, FUSED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.Tq + kBM - 1) / kBM, a.H, a.B);
@@ -571,9 +620,10 @@ static cudaError_t launch_prefill_tc_t(const PrefillMaps& maps, const PrefillArg
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int d_h, cudaStream_t stream) {
-    if (a.qt) return d_h == 64 ? launch_prefill_tc_t<64, true>(maps, a, stream) : launch_prefill_tc_t<128, true>(maps, a, stream);
-    return d_h == 64 ? launch_prefill_tc_t<64, false>(maps, a, stream) : launch_prefill_tc_t<128, false>(maps, a, stream);
+cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int d_h, int d_rope, cudaStream_t stream) {
+    if (d_rope == 64) return d_h == 128 && !a.qt ? launch_prefill_tc_t<128, 64, false>(maps, a, stream) : cudaErrorInvalidValue;
+    if (a.qt) return d_h == 64 ? launch_prefill_tc_t<64, 0, true>(maps, a, stream) : launch_prefill_tc_t<128, 0, true>(maps, a, stream);
+    return d_h == 64 ? launch_prefill_tc_t<64, 0, false>(maps, a, stream) : launch_prefill_tc_t<128, 0, false>(maps, a, stream);
 }
 
 }  // namespace lrkv

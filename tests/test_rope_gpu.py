@@ -135,6 +135,14 @@ PREFILL_CASES = [
     (4, 128, 32, 1, [0, 1000]),
     (8, 128, 16, 96, [256, 0]),
     (2, 128, 8, 70, [63, 1]),
+    # d_h = 128, r = 16 runs the tcgen05 kernel (two-stage key ring of [s^K | k^R] rows):
+    # ragged query tiles, contexts not aligned to pages or key tiles, a 4096-token prompt's
+    # last chunk, one key tile only
+    (1, 128, 16, 300, [37, 0]),
+    (3, 128, 16, 512, [3584, 1000]),
+    (2, 128, 16, 129, [127, 64]),
+    (8, 128, 16, 1, [4095, 0]),
+    (2, 128, 16, 40, [0, 60]),
 ]
 
 
