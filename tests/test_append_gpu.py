@@ -52,6 +52,27 @@ def test_append_bit_exact_on_exact_inputs(n, H, d_h, r, d):
     assert st == 0
     for g_, r_, nm in zip(got, ref, ("sK", "sV", "zK", "zV")):
         np.testing.assert_array_equal(g_, r_, err_msg=nm)
+    # The kernels' fp32 accumulators hold these exact sums, so the match above is the
+    # epilogue's rounding checked bit for bit; show that it covers rounding at all and the
+    # ties-to-even rule: count the exact sums that bf16 cannot hold, and those exactly
+    # halfway between two bf16 neighbours.
+    Xf = f64(X)
+    sums = (Xf @ f64(w.WsK), Xf @ f64(w.WsV), np.einsum("nd,hdr->nhr", Xf, f64(w.UK)),
+            np.einsum("nd,hdr->nhr", Xf, f64(w.UV)))
+    for v, nm in zip(sums, ("sK", "sV", "zK", "zV")):
+        inexact, ties = _bf16_rounding_cases(v)
+        print(f"append exact-input rounding n={n} H={H} {nm}: {inexact} rounded, {ties} ties of {v.size}")
+        assert inexact > 0 and ties > 0, nm
+
+
+def _bf16_rounding_cases(v):
+    """(sums that bf16 must round, sums exactly halfway between two bf16 values) among integer sums."""
+    a = np.abs(np.asarray(v, np.float64).ravel())
+    assert np.all(a == np.round(a)) and np.all(a < 2.0 ** 52)
+    a = a[a >= 256].astype(np.int64)  # below 2^8 every integer is a bf16 value
+    step = 2 ** (np.floor(np.log2(a)).astype(np.int64) - 7)  # bf16 spacing in [2^k, 2^(k+1))
+    rem = a % step
+    return int(np.sum(rem != 0)), int(np.sum(rem == step // 2))
 
 
 def _bf16_ulp(x):
