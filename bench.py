@@ -19,9 +19,9 @@ r=16, batch 2, 4096-token prompts in 512-token chunks), value in prompt
 tokens/s with the tensor roofline of the prefill kernel; "mla": multi-head latent
 attention decode with absorbed weights at DeepSeek-V2's attention shape (H=128,
 d_c=512, d_h^R=64, d=5120, batch 8, 16384 cached tokens), GB/s as for decode.  --fused runs a decode
-workload through lrkv_decode_fused (both absorptions in the caller's weights:
-q~ given, [o_s | o_z] returned), counting that form's own bytes.  --rope adds the
-64-wide decoupled positional key (key rows [s^K | k^R], rotated in the append).
+or prefill workload through lrkv_decode_fused / lrkv_prefill_fused (both absorptions in the
+caller's weights: q~ given, [o_s | o_z] returned), counting that form's own bytes or flops.
+--rope adds the 64-wide decoupled positional key (key rows [s^K | k^R], rotated in the append).
 
 Prints one JSON line.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lrkv|reference] [--workload NAME] [--fused] [--rope]
@@ -434,47 +434,59 @@ class DecodeHarness(Rotating):
 
 # ----------------------------------------------------------------------------- prefill
 class PrefillHarness(Rotating):
-    """Per 512-token chunk: lrkv_append of both sequences' rows, then lrkv_prefill."""
+    """Per 512-token chunk: lrkv_append of both sequences' rows, then lrkv_prefill (or, with
+    absorbed weights, lrkv_prefill_fused)."""
 
     per_copy = ("cache", "BK", "BV", "wcat", "chunks")
 
     profile = "prefill_chunked.md"
     sources = ("prefill_tc.cu", "lrkv_internal.cuh", "kernels.h")
 
-    def __init__(self, wl, rank):
+    def __init__(self, wl, rank, fused=False, d_rope=0):
         import torch
 
         from compressed_kv_cache_lrkv_gb300 import binding as b
-        self.torch, self.b, self.wl = torch, b, wl
-        B, H, d_h, r, d, T, C = wl.B, wl.H, wl.d_h, wl.r, wl.d, wl.L, wl.chunk
+        self.torch, self.b, self.wl, self.fused, self.d_rope = torch, b, wl, fused, d_rope
+        B, H, d_h, r, d, T, C, dr = wl.B, wl.H, wl.d_h, wl.r, wl.d, wl.L, wl.chunk, d_rope
         self.pt = S.page_table(wl.seed, [T] * B, 64)
         nb = self.pt.num_blocks
         gen = torch.Generator(device="cuda").manual_seed(replica_seed(rank, 4321))
         rn = lambda *s, scale=1.0: (torch.randn(*s, generator=gen, device="cuda") * scale).to(torch.bfloat16)
         i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
-        self.dims = b.make_dims(H, d_h, r, d)
-        self.cache = b.PagedCache.empty(nb, H, d_h, r)
+        self.dims = b.make_dims(H, d_h, r, d, d_rope=dr)
+        self.cache = b.PagedCache.empty(nb, H, d_h, r, d_rope=dr)
         self.BK, self.BV = rn(H, d_h, r, scale=r ** -0.5), rn(H, d_h, r, scale=r ** -0.5)
-        self.wcat = rn(2 * (d_h + H * r), d, scale=d ** -0.5)
+        self.wcat = rn(2 * (d_h + H * r) + dr, d, scale=d ** -0.5)
         self.bt = i32(self.pt.block_table)
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.chunks = []
+        ow = d_h + (r if fused else 0)
         for c0 in range(0, T, C):
             self.chunks.append(dict(
                 x=rn(B * C, d),  # both sequences' rows of this chunk
                 slots=i32(np.concatenate([S.slots_for(self.pt, bb, c0, c0 + C) for bb in range(B)])),
-                q=rn(B, C, H, d_h), qs=i32([c0] * B),
-                out=torch.empty(B, C, H, d_h, dtype=torch.bfloat16, device="cuda")))
+                pos=i32(np.tile(np.arange(c0, c0 + C), B)) if dr else None,
+                q=rn(B, C, H, d_h + dr), qs=i32([c0] * B),
+                qt=rn(B, C, H, r) if fused else None,
+                out=torch.empty(B, C, H, ow, dtype=torch.bfloat16, device="cuda")))
         self.side = torch.cuda.Stream()
         self.p2 = torch.cuda.Stream()  # every other chunk's prefill
         self.fork, self.join, self.join2 = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
         self.appended = [torch.cuda.Event() for _ in self.chunks]
-        app = A.append_flops(B * T, d, H, d_h, r)
-        pre = sum(A.prefill_flops(B, C, H, d_h, r, q_start=c0) for c0 in range(0, T, C))
+        app = A.append_flops(B * T, d, H, d_h, r) + 2 * B * T * d * dr
+        pre = sum(A.prefill_flops(B, C, H, d_h, r, q_start=c0, d_rope=dr, absorbed=fused) for c0 in range(0, T, C))
         self.kernel_units = pre
         self.step_units = app + pre
         self.app_flops = app
         self.launches_per_step = 2 * len(self.chunks)
+
+    def _prefill(self, ch, stream):
+        if self.fused:
+            self.b.lrkv_prefill_fused(self.dims, ch["q"], ch["qt"], self.cache, self.bt, ch["qs"], ch["out"],
+                                      status=self.status, stream=stream)
+        else:
+            self.b.lrkv_prefill(self.dims, ch["q"], self.BK, self.BV, self.cache, self.bt, ch["qs"], ch["out"],
+                                status=self.status, stream=stream)
 
     def step(self, stream):
         """Chunk c's prefill needs chunk c's rows in the cache; chunk c+1's append only writes
@@ -487,13 +499,13 @@ class PrefillHarness(Rotating):
         side.wait_event(self.fork)
         self.p2.wait_event(self.fork)
         for ch, ev in zip(self.chunks, self.appended):
-            b.lrkv_append(self.dims, ch["x"], self.wcat, ch["slots"], self.cache, status=self.status, stream=side)
+            b.lrkv_append(self.dims, ch["x"], self.wcat, ch["slots"], self.cache, status=self.status, stream=side,
+                          positions=ch["pos"])
             ev.record(side)
         for i, (ch, ev) in enumerate(zip(self.chunks, self.appended)):
             st = stream if i % 2 == 0 else self.p2
             st.wait_event(ev)
-            b.lrkv_prefill(self.dims, ch["q"], self.BK, self.BV, self.cache, self.bt, ch["qs"], ch["out"],
-                           status=self.status, stream=st)
+            self._prefill(ch, st)
         self.join.record(side)
         self.join2.record(self.p2)
         stream.wait_event(self.join)
@@ -505,8 +517,7 @@ class PrefillHarness(Rotating):
         self.fork.record(stream)
         self.p2.wait_event(self.fork)
         for i, ch in enumerate(self.chunks):
-            self.b.lrkv_prefill(self.dims, ch["q"], self.BK, self.BV, self.cache, self.bt, ch["qs"], ch["out"],
-                                status=self.status, stream=stream if i % 2 == 0 else self.p2)
+            self._prefill(ch, stream if i % 2 == 0 else self.p2)
         self.join2.record(self.p2)
         stream.wait_event(self.join2)
 
@@ -515,7 +526,8 @@ class PrefillHarness(Rotating):
                 "cache": _nbytes(self.cache), "weights (W_cat, B^K, B^V)": _nbytes([self.wcat, self.BK, self.BV])}
 
     def e2e_inputs(self):
-        return [ch[k] for ch in self.chunks for k in ("x", "q")]
+        keys = ("x", "q") + (("qt",) if self.fused else ()) + (("pos",) if self.d_rope else ())
+        return [ch[k] for ch in self.chunks for k in keys]
 
     def e2e_outputs(self):
         return [ch["out"] for ch in self.chunks]
@@ -528,46 +540,59 @@ class PrefillHarness(Rotating):
             "metric": METRIC_PREFILL, "value": tokens / step_s, "unit": "tokens/s",
             "step_tflops": self.step_units * world / step_s / 1e12,
             "config": {"workload": f"{wl.key}: {wl.description}", "B": wl.B, "prompt": wl.L, "chunk": wl.chunk,
-                       "H": wl.H, "d_h": wl.d_h, "r": wl.r, "d": wl.d, "block_size": 64,
-                       "l2": "prompt activations (X, q, out: 192 MiB) larger than L2",
-                       "step": "per 512-token chunk: lrkv_append (1024 rows) + lrkv_prefill; the appends run on a "
-                               "side stream (chunk c+1's append overlaps chunk c's prefill) and the prefills "
-                               "alternate between two streams (chunk c+1's CTAs fill chunk c's last wave)",
+                       "H": wl.H, "d_h": wl.d_h, "r": wl.r, "d": wl.d, "d_rope": self.d_rope,
+                       "absorbed_weights": self.fused, "block_size": 64,
+                       "l2": "prompt activations (X, q, out) larger than L2",
+                       "step": "per 512-token chunk: lrkv_append (1024 rows" +
+                               (", positional key rotated at each row's position) + " if self.d_rope else ") + ") +
+                               ("lrkv_prefill_fused (q~ given, [o_s | o_z] returned)" if self.fused else
+                                "lrkv_prefill") +
+                               "; the appends run on a side stream (chunk c+1's append overlaps chunk c's prefill) "
+                               "and the prefills alternate between two streams (chunk c+1's CTAs fill chunk c's "
+                               "last wave)",
                        "flops_per_step": self.step_units, "append_flops": self.app_flops,
                        "prefill_flops": self.kernel_units,
                        "parallelism": f"replicas x{world} (independent batches)"},
-            "roofline": {"kernel": "lrkv_prefill (8 chunk launches on two streams)", "bound": "tensor",
+            "roofline": {"kernel": ("lrkv_prefill_fused" if self.fused else "lrkv_prefill") +
+                                   " (8 chunk launches on two streams)", "bound": "tensor",
                          "achieved": achieved,
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                          "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                         "traffic": recorded_traffic(self.profile, self.sources),
+                         "traffic": (recorded_traffic(self.profile, self.sources)
+                                     if not self.fused and not self.d_rope else None),
                          "algorithmic_flops_per_launch": self.kernel_units / len(self.chunks),
                          "avg_launch_ms": kernel_s * 1e3 / len(self.chunks)},
             "e2e_unit_value": lambda s: tokens / s, "e2e_unit": "tokens/s",
         }
 
     def cpu_baseline(self, budget_s):
-        """fp64 oracle (E2 causal prefill, all heads) on the first chunk of one sequence."""
+        """fp64 oracle (E2 causal prefill, all heads; absorbed-weights form with --fused) on the
+        first chunk of one sequence."""
         import oracle
         wl = self.wl
         o = oracle.get()
-        C = wl.chunk
+        C, dr = wl.chunk, self.d_rope
         pt = S.page_table(wl.seed, [C], 64)
         pools = tuple(S.gaussian_bf16(wl.seed, n, shp) for n, shp in
-                      [("bl_sK", (pt.num_blocks, 64, wl.d_h)), ("bl_sV", (pt.num_blocks, 64, wl.d_h)),
+                      [("bl_sK", (pt.num_blocks, 64, wl.d_h + dr)), ("bl_sV", (pt.num_blocks, 64, wl.d_h)),
                        ("bl_zK", (pt.num_blocks, 64, wl.H, wl.r)), ("bl_zV", (pt.num_blocks, 64, wl.H, wl.r))])
         BK = S.gaussian_bf16(wl.seed, "bl_BK", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
         BV = S.gaussian_bf16(wl.seed, "bl_BV", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
-        q = S.gaussian_bf16(wl.seed, "bl_q", (1, C, wl.H, wl.d_h))
+        q = S.gaussian_bf16(wl.seed, "bl_q", (1, C, wl.H, wl.d_h + dr))
+        qt = S.gaussian_bf16(wl.seed, "bl_qt", (1, C, wl.H, wl.r))
         reps, t0 = 0, time.perf_counter()
         while True:
-            o.prefill_cache(pools, pt.block_table, [0], BK, BV, q)
+            if self.fused:
+                o.prefill_fused(pools, pt.block_table, [0], q, qt)
+            else:
+                o.prefill_cache(pools, pt.block_table, [0], BK, BV, q)
             reps += 1
             dt = time.perf_counter() - t0
             if dt >= budget_s:
                 break
+        what = "absorbed-weights causal prefill" if self.fused else "E2 causal prefill"
         return {"value": C * reps / dt, "unit": "tokens/s", "cores": o.num_threads(), "kind": "oracle",
-                "sample": f"E2 causal prefill of one sequence's first {C}-token chunk (all {wl.H} heads), "
+                "sample": f"{what} of one sequence's first {C}-token chunk (all {wl.H} heads), "
                           f"{reps} repetitions in {dt:.1f} s; fp64, OpenMP over heads"}
 
 
@@ -796,12 +821,14 @@ def run_gpu(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     wl = S.WORKLOADS[args.workload]
-    if (args.fused or args.rope) and HARNESS[args.workload] is not DecodeHarness:
-        raise SystemExit("--fused and --rope apply to the decode workloads")
+    if (args.fused or args.rope) and HARNESS[args.workload] not in (DecodeHarness, PrefillHarness):
+        raise SystemExit("--fused and --rope apply to the decode and prefill workloads")
     if args.per_layer and HARNESS[args.workload] is not DecodeHarness:
         raise SystemExit("--per-layer applies to the decode workloads")
     if HARNESS[args.workload] is DecodeHarness:
         hz = DecodeHarness(wl, rank, fused=args.fused, d_rope=64 if args.rope else 0, per_layer=args.per_layer)
+    elif HARNESS[args.workload] is PrefillHarness:
+        hz = PrefillHarness(wl, rank, fused=args.fused, d_rope=64 if args.rope else 0)
     else:
         hz = HARNESS[args.workload](wl, rank)
     stream = torch.cuda.current_stream()
@@ -1159,9 +1186,11 @@ def main():
     ap.add_argument("--copies", type=int, default=0,
                     help="independent input copies replayed round-robin (0: enough to break L2 residency)")
     ap.add_argument("--fused", action="store_true",
-                    help="decode with absorbed weights (lrkv_decode_fused: q~ given, [o_s | o_z] returned)")
+                    help="decode or prefill with absorbed weights (lrkv_decode_fused / lrkv_prefill_fused: "
+                         "q~ given, [o_s | o_z] returned)")
     ap.add_argument("--rope", action="store_true",
-                    help="decode with a 64-wide decoupled positional key shared by all heads (d_rope = 64)")
+                    help="decode or prefill with a 64-wide decoupled positional key shared by all heads "
+                         "(d_rope = 64)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

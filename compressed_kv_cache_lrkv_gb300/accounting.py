@@ -99,12 +99,15 @@ def append_algorithmic_bytes(n_tok: int, d: int, H: int, d_h: int, r: int, d_rop
     return BF16_BYTES * (n_tok * d + d * N + n_tok * N)
 
 
-def prefill_flops(B: int, T: int, H: int, d_h: int, r: int, q_start: int = 0) -> int:
-    """Causal attention flops over head width d_h + r (logits and values) for queries at
-    positions [q_start, q_start + T): 4 (d_h + r) H B * sum_i (q_start + i + 1), plus the
-    q~ absorption and B^V up-projection, 4 B T H d_h r."""
+def prefill_flops(B: int, T: int, H: int, d_h: int, r: int, q_start: int = 0, d_rope: int = 0,
+                  absorbed: bool = False) -> int:
+    """Causal attention flops for queries at positions [q_start, q_start + T): per visible
+    (query, key) pair 2 (d_h + d_rope + r) for the logit and 2 (d_h + r) for the value side,
+    i.e. 4 (d_h + r) + 2 d_rope, times H B sum_i (q_start + i + 1); plus the q~ absorption and
+    the B^V up-projection, 4 B T H d_h r, unless the weights are absorbed by the caller."""
     pairs = T * q_start + T * (T + 1) // 2
-    return 4 * (d_h + r) * H * B * pairs + 4 * B * T * H * d_h * r
+    proj = 0 if absorbed else 4 * B * T * H * d_h * r
+    return (4 * (d_h + r) + 2 * d_rope) * H * B * pairs + proj
 
 
 def mla_decode_algorithmic_bytes(H: int, d_c: int, d_rope: int, seq_lens: Iterable[int], layers: int = 1) -> int:

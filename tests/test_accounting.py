@@ -67,3 +67,9 @@ def test_workload_byte_counts():
     assert A.decode_algorithmic_bytes(128, 128, 16, [8192] * 8) == 571998208
     assert A.append_flops(8192, 4096, 32, 128, 16) == 85899345920
     assert A.prefill_flops(2, 4096, 32, 128, 16) - 4 * 2 * 4096 * 32 * 128 * 16 == 4 * 144 * 32 * 2 * 4096 * 4097 // 2
+    # the positional key adds its 64 columns to the logit side only; absorbed weights drop the
+    # two projections
+    assert (A.prefill_flops(2, 4096, 32, 128, 16, d_rope=64) - A.prefill_flops(2, 4096, 32, 128, 16)
+            == 2 * 64 * 32 * 2 * 4096 * 4097 // 2)
+    assert (A.prefill_flops(2, 4096, 32, 128, 16) - A.prefill_flops(2, 4096, 32, 128, 16, absorbed=True)
+            == 4 * 2 * 4096 * 32 * 128 * 16)

@@ -105,27 +105,36 @@ def test_decode_workload_full_size(key, d_rope, per_layer, oracle_lib):
                                                f"heads {heads})")
 
 
-def test_prefill_workload_full_size(oracle_lib):
+@pytest.mark.parametrize("fused,d_rope", [(False, 0), (False, 64), (True, 0)])
+def test_prefill_workload_full_size(fused, d_rope, oracle_lib):
+    """Also with the positional key (rotated in the append at each row's position) and with
+    absorbed weights (lrkv_prefill_fused), as `bench.py --workload prefill --rope / --fused` runs."""
     wl = S.WORKLOADS["prefill"]
-    hz = bench.PrefillHarness(wl, 0)
+    hz = bench.PrefillHarness(wl, 0, fused=fused, d_rope=d_rope)
     _run_step(hz)
 
     heads = _heads(wl.H, 4)
     C, T = wl.chunk, wl.L
-    WsK, WsV, UK, UV, _ = _unpack_wcat(host_bits(hz.wcat), wl.d_h, wl.H, wl.r)
+    WsK, WsV, UK, UV, WKR = _unpack_wcat(host_bits(hz.wcat), wl.d_h, wl.H, wl.r, d_rope)
     BK, BV = host_bits(hz.BK)[heads], host_bits(hz.BV)[heads]
     xs = [host_bits(ch["x"]) for ch in hz.chunks]
     got, ref = [], []
     for b in range(wl.B):
         # sequence b's prompt rows in token order (chunk c holds both sequences' rows, b-major)
         X = np.concatenate([x[b * C:(b + 1) * C] for x in xs])
-        rows = oracle_lib.append(X, WsK, WsV, UK[heads], UV[heads])
+        rows = oracle_lib.append(X, WsK, WsV, UK[heads], UV[heads], WKR=WKR,
+                                 positions=np.arange(T, dtype=np.int32) if d_rope else None)
         npg = T // 64
         pools = [np.zeros((npg, 64) + rr.shape[1:], np.uint16) for rr in rows]
         oracle.scatter_rows(pools, np.arange(T), rows)
         bt = np.arange(npg, dtype=np.int32)[None]
         for ci, ch in enumerate(hz.chunks):
             q = np.ascontiguousarray(host_bits(ch["q"])[b:b + 1][:, :, heads])
-            ref.append(oracle_lib.prefill_cache(pools, bt, [ci * C], BK, BV, q)[0])
+            if fused:
+                qt = np.ascontiguousarray(host_bits(ch["qt"])[b:b + 1][:, :, heads])
+                ref.append(oracle_lib.prefill_fused(pools, bt, [ci * C], q, qt)[0])
+            else:
+                ref.append(oracle_lib.prefill_cache(pools, bt, [ci * C], BK, BV, q)[0])
             got.append(host_f64(ch["out"])[b][:, heads])
-    assert_close(np.stack(got), np.stack(ref), f"prefill at full size (both sequences, all chunks, heads {heads})")
+    assert_close(np.stack(got), np.stack(ref), f"prefill (absorbed {fused}, d_rope {d_rope}) at full size "
+                                               f"(both sequences, all chunks, heads {heads})")
