@@ -128,6 +128,14 @@ __global__ void __launch_bounds__(192, 1)
     } else {
         // epilogue: warps 2..5 -> TMEM lane quarters 2, 3, 0, 1
         const int q = warp & 3;
+        // The positional key's inverse frequencies depend on the pair alone: computed once per
+        // CTA (in double, a few dozen operations each on the narrow FP64 pipe) for all rows.
+        __shared__ double inv_freq[32];
+        if (ROPE && n0 < a.d_h + a.d_rope && n0 + BN > a.d_h) {
+            const int t = threadIdx.x - 64;
+            if (t < a.d_rope / 2 && t < 32) inv_freq[t] = rope_inv_freq(t, a.d_rope, a.rope_base);
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+        }
         bool ok = mbar_wait(smem_u32(accf), 0, a.status);
         ok = __all_sync(0xffffffffu, ok && !*abort_flag);  // warp-uniform: tcgen05.ld below is warp-collective
         tc_fence_after();
@@ -145,7 +153,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
-                        rope_rotate(x0, x1, (n0 + c0 - a.d_h) / 2 + e, a.d_rope, pos, a.rope_base);
+                        rope_rotate_f(x0, x1, inv_freq[(n0 + c0 - a.d_h) / 2 + e], pos);
                         v[2 * e] = __float_as_uint(x0);
                         v[2 * e + 1] = __float_as_uint(x1);
                     }

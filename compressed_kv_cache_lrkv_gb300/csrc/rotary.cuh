@@ -48,9 +48,9 @@ __device__ __forceinline__ double rope_inv_freq(int i, int d_rope, float base) {
     return y;
 }
 
-// Rotate the fp32 pair (x0, x1) = columns (2i, 2i+1) of k^R at position pos.
-__device__ __forceinline__ void rope_rotate(float& x0, float& x1, int i, int d_rope, int pos, float base) {
-    const double turns = (double)pos * rope_inv_freq(i, d_rope, base) * 0.15915494309189533577;  // / 2 pi
+// Rotate the fp32 pair (x0, x1) by pos * inv_freq, inv_freq = rope_inv_freq(i, ...) of its pair.
+__device__ __forceinline__ void rope_rotate_f(float& x0, float& x1, double inv_freq, int pos) {
+    const double turns = (double)pos * inv_freq * 0.15915494309189533577;  // / 2 pi
     const double fr = turns - floor(turns);
     const float f = (float)fr;
     float sf, cf;
@@ -62,6 +62,11 @@ __device__ __forceinline__ void rope_rotate(float& x0, float& x1, int i, int d_r
     const double y1 = (double)x0 * sn + (double)x1 * cs;
     x0 = (float)y0;
     x1 = (float)y1;
+}
+
+// Rotate the fp32 pair (x0, x1) = columns (2i, 2i+1) of k^R at position pos.
+__device__ __forceinline__ void rope_rotate(float& x0, float& x1, int i, int d_rope, int pos, float base) {
+    rope_rotate_f(x0, x1, rope_inv_freq(i, d_rope, base), pos);
 }
 
 }  // namespace lrkv
