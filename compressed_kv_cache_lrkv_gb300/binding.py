@@ -21,6 +21,7 @@ DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 EXPORTED = ["lrkv_abi_version", "lrkv_status_string", "lrkv_last_error", "lrkv_cache_block_bytes", "lrkv_append",
             "lrkv_decode_workspace_bytes", "lrkv_decode", "lrkv_decode_fused", "lrkv_decode_static_ws",
+            "lrkv_decode_partials", "lrkv_decode_merge",
             "lrkv_append_layers", "lrkv_decode_layers",
             "lrkv_prefill_workspace_bytes", "lrkv_prefill", "lrkv_prefill_fused", "lrkv_mla_cache_block_bytes", "lrkv_mla_append",
             "lrkv_mla_decode_workspace_bytes", "lrkv_mla_decode", "lrkv_train_forward", "lrkv_train_workspace_bytes",
@@ -89,6 +90,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lrkv_decode_layers.restype = ctypes.c_int
     lib.lrkv_decode_layers.argtypes = [P(Dims), i32, P(LayerStrides), vp, vp, vp, P(Cache), vp, i32, vp, i32, vp, vp,
                                        sz, vp, vp]
+    lib.lrkv_decode_partials.restype = ctypes.c_int
+    lib.lrkv_decode_partials.argtypes = [P(Dims), vp, vp, P(Cache), vp, i32, vp, i32, vp, vp, sz, vp, vp]
+    lib.lrkv_decode_merge.restype = ctypes.c_int
+    lib.lrkv_decode_merge.argtypes = [P(Dims), i32, vp, vp, i32, vp, vp, vp]
     lib.lrkv_decode_static_ws.restype = ctypes.c_int
     lib.lrkv_decode_static_ws.argtypes = [P(Dims), vp, vp, vp, P(Cache), vp, i32, vp, i32, vp, vp, vp]
     lib.lrkv_prefill_workspace_bytes.restype = sz
@@ -213,6 +218,26 @@ def lrkv_decode_fused(dims: Dims, q, q_tilde, cache: PagedCache, block_table, se
                                   int(block_table.shape[1]), _ptr(seq_lens), B, _ptr(out), _ptr(workspace),
                                   int(workspace.numel() * workspace.element_size()), _ptr(status), _stream(stream))
     _check(rc, "lrkv_decode_fused")
+
+
+def lrkv_decode_partials(dims: Dims, q, BK, cache: PagedCache, block_table, seq_lens, partials, workspace,
+                         status=None, stream=None):
+    """Decode partials over this cache's tokens: q [B, H, d_h] -> partials [B, H, d_h + r + 2] fp32
+    (acc_s, acc_z, m, l)."""
+    B = int(q.shape[0])
+    c = cache.struct()
+    rc = load().lrkv_decode_partials(ctypes.byref(dims), _ptr(q), _ptr(BK), ctypes.byref(c), _ptr(block_table),
+                                     int(block_table.shape[1]), _ptr(seq_lens), B, _ptr(partials), _ptr(workspace),
+                                     int(workspace.numel() * workspace.element_size()), _ptr(status), _stream(stream))
+    _check(rc, "lrkv_decode_partials")
+
+
+def lrkv_decode_merge(dims: Dims, partials, BV, out, status=None, stream=None):
+    """Merge partials [P, B, H, d_h + r + 2] of P parts of the sequences' tokens -> out [B, H, d_h]."""
+    P, B = int(partials.shape[0]), int(partials.shape[1])
+    rc = load().lrkv_decode_merge(ctypes.byref(dims), P, _ptr(partials), _ptr(BV), B, _ptr(out), _ptr(status),
+                                  _stream(stream))
+    _check(rc, "lrkv_decode_merge")
 
 
 def lrkv_decode_static_ws(dims: Dims, q, BK, BV, cache: PagedCache, block_table, seq_lens, out, status=None,

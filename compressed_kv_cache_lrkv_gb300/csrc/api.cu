@@ -376,13 +376,17 @@ size_t lrkv_decode_workspace_bytes(const lrkv_dims* dims, int32_t batch) {
 }
 
 // Shared body of lrkv_decode (q~ = q B^K computed here, output B^V-projected), lrkv_decode_fused
-// (q~ given by the caller, output [o_s | o_z] / l) and lrkv_decode_layers (several layers).
+// (q~ given by the caller, output [o_s | o_z] / l), lrkv_decode_layers (several layers) and
+// lrkv_decode_partials (partials instead of an output: q~ computed, no B^V).
 static lrkv_status decode_impl(const lrkv_dims* dims, int32_t num_layers, const lrkv_layer_strides* ls,
                                const void* q, const void* q_tilde, const void* BK, const void* BV,
                                const lrkv_cache* cache, const int32_t* block_table, int32_t max_blocks_per_seq,
                                const int32_t* seq_lens, int32_t batch, void* out, void* workspace,
-                               size_t workspace_bytes, uint32_t* status_dev, void* stream) {
+                               size_t workspace_bytes, uint32_t* status_dev, void* stream,
+                               float* partials = nullptr) {
     const bool fused = q_tilde != nullptr;
+    const char* what = partials ? "lrkv_decode_partials launch"
+                                : fused ? "lrkv_decode_fused launch" : "lrkv_decode launch";
     lrkv_status s = check_dims(dims);
     if (s != LRKV_OK) return s;
     if ((s = check_cache(cache)) != LRKV_OK) return s;
@@ -402,11 +406,14 @@ static lrkv_status decode_impl(const lrkv_dims* dims, int32_t num_layers, const 
     LRKV_REQUIRE_PTR(q);
     if (fused) {
         LRKV_REQUIRE_PTR(q_tilde);
+    } else if (partials) {
+        LRKV_REQUIRE_PTR(BK);
+        LRKV_REQUIRE_PTR(partials);
     } else {
         LRKV_REQUIRE_PTR(BK);
         LRKV_REQUIRE_PTR(BV);
     }
-    LRKV_REQUIRE_PTR(out);
+    if (!partials) LRKV_REQUIRE_PTR(out);
     if (!block_table || !seq_lens) return fail(LRKV_ERR_INVALID_ARG, "block_table or seq_lens is NULL");
     const uint64_t rows = (uint64_t)cache->num_blocks * dims->block_size;
     const uint64_t dk = (uint64_t)dims->d_h + dims->d_rope;  // key row [s^K | k^R]
@@ -468,6 +475,7 @@ static lrkv_status decode_impl(const lrkv_dims* dims, int32_t num_layers, const 
     a.BV = static_cast<const uint16_t*>(BV);
     a.qt_in = static_cast<const uint16_t*>(q_tilde);
     a.fused_out = fused ? 1 : 0;
+    a.part_out = partials;
     a.zK = static_cast<const uint16_t*>(cache->zK);
     a.zV = static_cast<const uint16_t*>(cache->zV);
     a.block_table = block_table;
@@ -486,7 +494,7 @@ static lrkv_status decode_impl(const lrkv_dims* dims, int32_t num_layers, const 
     return cuda_status(lrkv::launch_decode(tK, tV, tZK, tZV, a, dims->d_h, dims->r, dims->d_rope, di.sms,
                                            di.smem_optin,
                                            static_cast<cudaStream_t>(stream)),
-                       fused ? "lrkv_decode_fused launch" : "lrkv_decode launch");
+                       what);
 }
 
 lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* BK, const void* BV, const lrkv_cache* cache,
@@ -513,6 +521,32 @@ lrkv_status lrkv_decode_fused(const lrkv_dims* dims, const void* q, const void* 
     if (!q_tilde) return fail(LRKV_ERR_INVALID_ARG, "q_tilde is NULL");
     return decode_impl(dims, 1, nullptr, q, q_tilde, nullptr, nullptr, cache, block_table, max_blocks_per_seq,
                        seq_lens, batch, out, workspace, workspace_bytes, status_dev, stream);
+}
+
+lrkv_status lrkv_decode_partials(const lrkv_dims* dims, const void* q, const void* BK, const lrkv_cache* cache,
+                                 const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t batch, float* partials, void* workspace, size_t workspace_bytes,
+                                 uint32_t* status_dev, void* stream) {
+    if (!partials) return fail(LRKV_ERR_INVALID_ARG, "partials is NULL");
+    return decode_impl(dims, 1, nullptr, q, nullptr, BK, nullptr, cache, block_table, max_blocks_per_seq, seq_lens,
+                       batch, nullptr, workspace, workspace_bytes, status_dev, stream, partials);
+}
+
+lrkv_status lrkv_decode_merge(const lrkv_dims* dims, int32_t num_parts, const float* partials, const void* BV,
+                              int32_t batch, void* out, uint32_t* status_dev, void* stream) {
+    lrkv_status s = check_dims(dims);
+    if (s != LRKV_OK) return s;
+    if (num_parts < 1) return fail(LRKV_ERR_INVALID_ARG, "num_parts %d < 1", num_parts);
+    if (batch < 0) return fail(LRKV_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (batch == 0) return ok();
+    if (batch > 65535) return fail(LRKV_ERR_INVALID_ARG, "batch %d (at most 65535)", batch);
+    LRKV_REQUIRE_PTR(partials);
+    LRKV_REQUIRE_PTR(BV);
+    LRKV_REQUIRE_PTR(out);
+    return cuda_status(lrkv::launch_decode_merge(partials, num_parts, static_cast<const uint16_t*>(BV), batch, dims->H,
+                                                 dims->d_h, dims->r, static_cast<uint16_t*>(out), status_dev,
+                                                 static_cast<cudaStream_t>(stream)),
+                       "lrkv_decode_merge launch");
 }
 
 size_t lrkv_prefill_workspace_bytes(const lrkv_dims* dims, int32_t batch, int32_t Tq) {

@@ -658,7 +658,7 @@ __global__ void __launch_bounds__(512, 2) decode_combine_kernel(const DecodeArgs
     const int sl = tid / W4, c4 = tid - (tid / W4) * W4;
 
     // B_h^V, copied into shared memory asynchronously while the partials are loaded
-    if (!a.fused_out) {  // (no B^V in the fused form)
+    if (!a.fused_out && !a.part_out) {  // (no B^V in the fused form, nor for partials out)
         const uint16_t* bv = a.BV + ly * a.ls_BV + (size_t)h * D_H * R;
         for (int i = tid; i < D_H * R / 8; i += blockDim.x)
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sm_bv + i * 8)), "l"(bv + i * 8)
@@ -669,9 +669,15 @@ __global__ void __launch_bounds__(512, 2) decode_combine_kernel(const DecodeArgs
     pdl_wait();
     const int OW = a.fused_out ? W : D_H;  // output row width
     uint16_t* dst = a.out + ly * a.ls_out + ((size_t)bb * H + h) * OW;
+    float* pdst = a.part_out ? a.part_out + ((size_t)bb * H + h) * (W + 2) : nullptr;
     if (L < 1 || L > a.max_pages * kBlockSize) {
-        if (tid == 0 && h == 0) set_status(a.status, LRKV_DEV_BAD_SEQLEN);
-        for (int i = tid; i < OW; i += blockDim.x) dst[i] = 0;
+        // partials out: a sequence with no tokens in this range is an empty partial, not an error
+        if (tid == 0 && h == 0 && !(pdst && L == 0)) set_status(a.status, LRKV_DEV_BAD_SEQLEN);
+        if (pdst) {
+            for (int i = tid; i < W + 2; i += blockDim.x) pdst[i] = i == W ? -INFINITY : 0.f;
+        } else {
+            for (int i = tid; i < OW; i += blockDim.x) dst[i] = 0;
+        }
         asm volatile("cp.async.wait_all;" ::: "memory");
         return;
     }
@@ -736,6 +742,16 @@ __global__ void __launch_bounds__(512, 2) decode_combine_kernel(const DecodeArgs
             v.z = fmaf(w, x.z, v.z);
             v.w = fmaf(w, x.w, v.w);
         }
+        if (pdst) {  // unnormalised: the merge over token ranges normalises
+            pdst[tid * 4] = v.x;
+            pdst[tid * 4 + 1] = v.y;
+            pdst[tid * 4 + 2] = v.z;
+            pdst[tid * 4 + 3] = v.w;
+            if (tid == 0) {
+                pdst[W] = M;
+                pdst[W + 1] = lsum;
+            }
+        }
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
         const float4 r = lsum > 0.f ? make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv)
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -750,7 +766,7 @@ __global__ void __launch_bounds__(512, 2) decode_combine_kernel(const DecodeArgs
             }
         }
     }
-    if (a.fused_out) return;
+    if (a.fused_out || pdst) return;
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     if (tid < D_H) {
@@ -771,6 +787,61 @@ __global__ void __launch_bounds__(512, 2) decode_combine_kernel(const DecodeArgs
         const __nv_bfloat16 ob = __float2bfloat16_rn(v);
         dst[tid] = *reinterpret_cast<const uint16_t*>(&ob);
     }
+}
+
+// Merge of decode partials over parts of the sequences' token ranges (each part, e.g. the
+// cache shard of one device, decoded with partials out): log-sum-exp over the parts,
+//   M = max_p m_p,  w_p = 2^(m_p - M),  acc = sum_p w_p acc_p,  l = sum_p w_p l_p,
+//   out = (acc_s + B_h^V acc_z) / l,
+// i.e. the combine's merge with the parts in place of the splits.  grid (H, B), one thread per
+// accumulator column.
+template <int D_H, int R>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const float* parts, int nparts, const uint16_t* BV,
+                                                           int B, int H, uint16_t* out, uint32_t* status) {
+    constexpr int W = D_H + R, PW = W + 2;
+    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    __shared__ float sacc[W];
+    __shared__ float sl;
+    const size_t pstride = (size_t)B * H * PW;  // between parts
+    const float* p0 = parts + ((size_t)b * H + h) * PW;
+    float M = -INFINITY;
+    for (int p = 0; p < nparts; ++p) M = fmaxf(M, p0[p * pstride + W]);
+    float l = 0.f, acc = 0.f;
+    for (int p = 0; p < nparts; ++p) {
+        const float* row = p0 + p * pstride;
+        const float m = row[W];
+        const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+        l = fmaf(w, row[W + 1], l);
+        if (tid < W) acc = fmaf(w, row[tid], acc);
+    }
+    if (tid < W) sacc[tid] = acc;
+    if (tid == 0) {
+        sl = l;
+        if (!(l > 0.f)) set_status(status, LRKV_DEV_BAD_SEQLEN);  // no part held a token of it
+    }
+    __syncthreads();
+    if (tid < D_H) {
+        float v = sacc[tid];
+        const uint16_t* bv = BV + ((size_t)h * D_H + tid) * R;
+#pragma unroll
+        for (int j = 0; j < R; ++j) v = fmaf(__uint_as_float((uint32_t)bv[j] << 16), sacc[D_H + j], v);
+        const float inv = sl > 0.f ? 1.f / sl : 0.f;
+        const __nv_bfloat16 ob = __float2bfloat16_rn(v * inv);
+        out[((size_t)b * H + h) * D_H + tid] = *reinterpret_cast<const uint16_t*>(&ob);
+    }
+}
+
+cudaError_t launch_decode_merge(const float* parts, int nparts, const uint16_t* BV, int B, int H, int d_h, int r,
+                                uint16_t* out, uint32_t* status, cudaStream_t stream) {
+#define LRKV_MERGE(DH, RR)                                                                                    \
+    if (d_h == DH && r == RR) {                                                                               \
+        decode_merge_kernel<DH, RR><<<dim3(H, B), 256, 0, stream>>>(parts, nparts, BV, B, H, out, status);   \
+        return cudaGetLastError();                                                                            \
+    }
+    LRKV_MERGE(64, 8) LRKV_MERGE(64, 16) LRKV_MERGE(64, 32) LRKV_MERGE(128, 8) LRKV_MERGE(128, 16)
+    LRKV_MERGE(128, 32)
+#undef LRKV_MERGE
+    return cudaErrorInvalidValue;
 }
 
 // ------------------------------------------------------------------ host side

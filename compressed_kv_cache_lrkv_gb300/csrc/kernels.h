@@ -56,6 +56,10 @@ struct DecodeArgs {
     int pmax;          // partial slots per head in the workspace (layers * B * nhg + nranges)
     float scale_log2;  // softmax scale * log2(e)
     unsigned long long wait_ns;  // limit of the split kernel's pipeline waits (a debugging aid may shorten it)
+    // Partials out (a token-range split of the sequences): when set, the combine writes each
+    // (sequence, head)'s merged, unnormalised [acc_s | acc_z | m | l] ([B][H][D_H + R + 2],
+    // m in the log2 domain) here instead of out, and no B^V is read.
+    float* part_out;
 };
 
 struct PrefillArgs {
@@ -108,6 +112,11 @@ int decode_tc_smem_bytes(int nslot, int stage_bytes);
 template <int R>
 cudaError_t launch_decode_tc_split(const CUtensorMap& tK, const CUtensorMap& tV, const DecodeArgs& a, int grid,
                                    int smem_bytes, bool pdl, cudaStream_t stream);
+
+// Log-sum-exp merge of nparts decode partials ([nparts][B][H][d_h + r + 2], as the combine
+// writes them with part_out) and the B^V up-projection: out [B][H][d_h] bf16.
+cudaError_t launch_decode_merge(const float* parts, int nparts, const uint16_t* BV, int B, int H, int d_h, int r,
+                                uint16_t* out, uint32_t* status, cudaStream_t stream);
 
 cudaError_t launch_prefill(const PrefillArgs& a, int D_H, int R, int D_R, cudaStream_t stream);
 

@@ -192,6 +192,35 @@ lrkv_status lrkv_decode_fused(const lrkv_dims* dims, const void* q, const void* 
                               uint32_t* status_dev, void* stream);
 
 /*
+ * lrkv_decode_partials / lrkv_decode_merge -- lrkv_decode cut at the log-sum-exp merge, for a
+ *   sequence whose cached tokens are spread over several caches (e.g. one token range per
+ *   device).  The online softmax of frame "Compute logits without expanding historical keys"
+ *   is associative over any split of the tokens, and B_h^V is applied after the merge (Eq. (7):
+ *   the latents are aggregated first), so each part only has to return, per (sequence, head),
+ *   over its own tokens t:
+ *     m   = max_t s_t,  s_t = ([q | q~] . [s^K_t | z^K_{h,t}]) * scale * log2(e)
+ *     l   = sum_t 2^(s_t - m)
+ *     acc = sum_t 2^(s_t - m) [s^V_t | z^V_{h,t}]                    (width d_h + r)
+ *   and the merge of P parts is M = max_p m_p, w_p = 2^(m_p - M),
+ *     out_h = (sum_p w_p acc_s,p + B_h^V sum_p w_p acc_z,p) / sum_p w_p l_p.
+ *   lrkv_decode_partials: arguments as lrkv_decode (no B^V, no out); seq_lens[b] counts the
+ *     tokens of sequence b held in THIS cache and may be 0 (an empty part: m = -inf, l = 0,
+ *     acc = 0; no status bit).
+ *     partials  [batch][H][d_h + r + 2] fp32: acc_s (d_h), acc_z (r), m, l
+ *   lrkv_decode_merge: partials [num_parts][batch][H][d_h + r + 2] (the parts' outputs stacked,
+ *     e.g. by an all-gather), BV as for lrkv_decode, out [batch][H][d_h] bf16 (nearest, ties to
+ *     even).  A (sequence, head) that no part holds a token of gets zeros and
+ *     LRKV_DEV_BAD_SEQLEN.  num_parts >= 1; 1 <= batch <= 65535 (0 is a no-op).
+ *   Pointers 16-byte aligned, device memory, the caller's stream; errors as for lrkv_decode.
+ */
+lrkv_status lrkv_decode_partials(const lrkv_dims* dims, const void* q, const void* BK, const lrkv_cache* cache,
+                                 const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t batch, float* partials, void* workspace, size_t workspace_bytes,
+                                 uint32_t* status_dev, void* stream);
+lrkv_status lrkv_decode_merge(const lrkv_dims* dims, int32_t num_parts, const float* partials, const void* BV,
+                              int32_t batch, void* out, uint32_t* status_dev, void* stream);
+
+/*
  * lrkv_decode_static_ws -- lrkv_decode without a caller workspace.  (The paper has
  *   no counterpart; this is a deployment convenience.)
  *   For callers that cannot allocate device memory: cudaMalloc/cudaFree can

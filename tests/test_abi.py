@@ -90,6 +90,17 @@ def test_null_and_misaligned_pointers_rejected():
     assert b"aligned" in lib.lrkv_last_error()
     assert lib.lrkv_decode_fused(ctypes.byref(dims), 16, 16, ctypes.byref(c), 16, 1, 16, 0, 16, 256, 0, None,
                                  None) == 0
+    # token-split decode: partials and the merge need their buffers; a merge of no parts is refused
+    assert lib.lrkv_decode_partials(ctypes.byref(dims), 16, 16, ctypes.byref(c), 16, 1, 16, 1, None, 256, 0, None,
+                                    None) == 1
+    assert b"partials" in lib.lrkv_last_error()
+    assert lib.lrkv_decode_partials(ctypes.byref(dims), 16, 16, ctypes.byref(c), 16, 1, 16, 0, 16, 256, 0, None,
+                                    None) == 0
+    assert lib.lrkv_decode_merge(ctypes.byref(dims), 0, 16, 16, 1, 16, None, None) == 1
+    assert lib.lrkv_decode_merge(ctypes.byref(dims), 2, None, 16, 1, 16, None, None) == 1
+    assert lib.lrkv_decode_merge(ctypes.byref(dims), 2, 16, 24, 1, 16, None, None) == 1
+    assert b"aligned" in lib.lrkv_last_error()
+    assert lib.lrkv_decode_merge(ctypes.byref(dims), 2, 16, 16, 0, 16, None, None) == 0
     # absorbed-weights prefill: the same rules for q~; batch 0 or Tq 0 is a no-op
     assert lib.lrkv_prefill_fused(ctypes.byref(dims), 16, None, ctypes.byref(c), 16, 1, 16, 1, 4, 16, None,
                                   None) == 1
