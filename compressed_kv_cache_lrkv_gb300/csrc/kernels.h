@@ -52,7 +52,7 @@ struct DecodeArgs {
     int bubble;        // granules a pipeline drain-and-refill costs (chooses how the work is cut)
     int ng, nslot, stage_bytes;
     int nhg;           // head groups: each (layer, sequence) is scanned as nhg virtual sequences of H / nhg heads
-    int gpst;          // 8-token granules per pipeline stage (1 or 4)
+    int gpst;          // 8-token granules per pipeline stage (1 or 2)
     int pmax;          // partial slots per head in the workspace (layers * B * nhg + nranges)
     float scale_log2;  // softmax scale * log2(e)
     unsigned long long wait_ns;  // limit of the split kernel's pipeline waits (a debugging aid may shorten it)
