@@ -279,7 +279,7 @@ class DecodeHarness(Rotating):
     profile = "decode_split_longctx.md"
     profiles = {"longctx": "decode_split_longctx.md", "dsv2": "decode_split_dsv2.md",
                 "backbone12": "decode_layers_backbone12.md"}  # by workload
-    sources = ("decode.cu", "lrkv_internal.cuh", "kernels.h")
+    sources = ("decode.cu", "decode_tc.cu", "decode_work.cuh", "lrkv_internal.cuh", "kernels.h")
 
     def __init__(self, wl, rank, fused=False, d_rope=0, per_layer=False):
         import torch
