@@ -10,7 +10,11 @@
 //               to release each stage and, at the end, the accumulator;
 //   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
 //               round to bf16 (nearest even), 16-byte stores into the row's
-//               cache slot (s^K | s^V | z^K | z^V segments).
+//               cache slot (s^K | s^V | z^K | z^V segments).  In the CTAs that
+//               hold the positional key's columns they first compute, while the
+//               MMAs run, the cosine and sine of every rotated pair of their rows
+//               (double precision, on the narrow FP64 pipe), so that after the
+//               accumulator lands only the rotation's products remain.
 // All waits are bounded (LRKV_DEV_TIMEOUT); no spin is unbounded.
 #include "kernels.h"
 #include "lrkv_internal.cuh"
@@ -21,6 +25,20 @@ namespace lrkv {
 namespace {
 
 constexpr int kBM = 128, kBK = 64, kStages = 4;
+
+// Shared memory: the operand ring, the barriers, and (positional key, 128-column tiles) a table
+// [pair][2][128 rows] of the rotation's cosines and sines in double -- 64 KB, which fits beside
+// the 128 KB ring of 128-column tiles but not the 192 KB one of 256-column tiles; those compute
+// the angles in the epilogue instead.
+template <int BN, bool ROPE>
+struct TcLayout {
+    static constexpr uint32_t A_BYTES = kBM * kBK * 2, B_BYTES = BN * kBK * 2;
+    static constexpr uint32_t RING = kStages * (A_BYTES + B_BYTES);
+    static constexpr bool PRE = ROPE && BN == 128;
+    static constexpr uint32_t TAB = RING + 128;
+    static constexpr uint32_t SMEM = TAB + (PRE ? 32 * 2 * kBM * 8 : 0) + 1024;
+    static_assert(SMEM <= 232448, "fits one CTA's opt-in shared memory");
+};
 
 __device__ __forceinline__ long long tc_checked_slot(const AppendArgs& a, int t) {
     const long long s = a.slots[t];
@@ -128,13 +146,31 @@ __global__ void __launch_bounds__(192, 1)
     } else {
         // epilogue: warps 2..5 -> TMEM lane quarters 2, 3, 0, 1
         const int q = warp & 3;
+        constexpr bool PRE = TcLayout<BN, ROPE>::PRE;
+        double* tab = reinterpret_cast<double*>(smem + TcLayout<BN, ROPE>::TAB);
         // The positional key's inverse frequencies depend on the pair alone: computed once per
         // CTA (in double, a few dozen operations each on the narrow FP64 pipe) for all rows.
         __shared__ double inv_freq[32];
-        if (ROPE && n0 < a.d_h + a.d_rope && n0 + BN > a.d_h) {
+        const bool rope_cta = ROPE && n0 < a.d_h + a.d_rope && n0 + BN > a.d_h;
+        const int i0 = rope_cta ? (max(n0, a.d_h) - a.d_h) / 2 : 0;  // first pair of this CTA
+        if (rope_cta) {
             const int t = threadIdx.x - 64;
             if (t < a.d_rope / 2 && t < 32) inv_freq[t] = rope_inv_freq(t, a.d_rope, a.rope_base);
             asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+            if (PRE) {
+                // cosine and sine of each rotated pair of this thread's row, while the MMAs run
+                const int row = m0 + q * 32 + lane;
+                const int i1 = (min(n0 + BN, a.d_h + a.d_rope) - a.d_h) / 2;
+                if (row < a.n) {
+                    const int pos = a.positions[row];
+                    for (int i = i0; i < i1; ++i) {
+                        double cs, sn;
+                        rope_cos_sin(inv_freq[i], pos, cs, sn);
+                        tab[(2 * (i - i0)) * kBM + q * 32 + lane] = cs;
+                        tab[(2 * (i - i0) + 1) * kBM + q * 32 + lane] = sn;
+                    }
+                }
+            }
         }
         bool ok = mbar_wait(smem_u32(accf), 0, a.status);
         ok = __all_sync(0xffffffffu, ok && !*abort_flag);  // warp-uniform: tcgen05.ld below is warp-collective
@@ -153,7 +189,12 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
-                        rope_rotate_f(x0, x1, inv_freq[(n0 + c0 - a.d_h) / 2 + e], pos);
+                        const int i = (n0 + c0 - a.d_h) / 2 + e;
+                        if (PRE)
+                            rope_apply(x0, x1, tab[(2 * (i - i0)) * kBM + q * 32 + lane],
+                                       tab[(2 * (i - i0) + 1) * kBM + q * 32 + lane]);
+                        else
+                            rope_rotate_f(x0, x1, inv_freq[i], pos);
                         v[2 * e] = __float_as_uint(x0);
                         v[2 * e + 1] = __float_as_uint(x1);
                     }
@@ -186,7 +227,7 @@ __global__ void __launch_bounds__(192, 1)
 template <int BN, bool ROPE>
 static cudaError_t launch_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const AppendArgs& a,
                              cudaStream_t stream) {
-    constexpr int smem = kStages * (kBM * kBK * 2 + BN * kBK * 2) + 2 * kStages * 8 + 8 + 8 + 1024;
+    constexpr int smem = TcLayout<BN, ROPE>::SMEM;
     auto kern = append_tc_kernel<BN, ROPE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

@@ -48,20 +48,31 @@ __device__ __forceinline__ double rope_inv_freq(int i, int d_rope, float base) {
     return y;
 }
 
-// Rotate the fp32 pair (x0, x1) by pos * inv_freq, inv_freq = rope_inv_freq(i, ...) of its pair.
-__device__ __forceinline__ void rope_rotate_f(float& x0, float& x1, double inv_freq, int pos) {
+// Cosine and sine of the angle pos * inv_freq, inv_freq = rope_inv_freq(i, ...) of the pair.
+__device__ __forceinline__ void rope_cos_sin(double inv_freq, int pos, double& cs, double& sn) {
     const double turns = (double)pos * inv_freq * 0.15915494309189533577;  // / 2 pi
     const double fr = turns - floor(turns);
     const float f = (float)fr;
     float sf, cf;
     sincospif(2.0f * f, &sf, &cf);
     const double dl = (fr - (double)f) * 6.283185307179586477;  // residual angle, rad
-    const double sn = fma(dl, (double)cf, (double)sf);
-    const double cs = fma(-dl, (double)sf, (double)cf);
+    sn = fma(dl, (double)cf, (double)sf);
+    cs = fma(-dl, (double)sf, (double)cf);
+}
+
+// The fp32 pair (x0, x1) turned by the angle whose cosine and sine are cs, sn.
+__device__ __forceinline__ void rope_apply(float& x0, float& x1, double cs, double sn) {
     const double y0 = (double)x0 * cs - (double)x1 * sn;
     const double y1 = (double)x0 * sn + (double)x1 * cs;
     x0 = (float)y0;
     x1 = (float)y1;
+}
+
+// Rotate the fp32 pair (x0, x1) by pos * inv_freq.
+__device__ __forceinline__ void rope_rotate_f(float& x0, float& x1, double inv_freq, int pos) {
+    double cs, sn;
+    rope_cos_sin(inv_freq, pos, cs, sn);
+    rope_apply(x0, x1, cs, sn);
 }
 
 // Rotate the fp32 pair (x0, x1) = columns (2i, 2i+1) of k^R at position pos.
