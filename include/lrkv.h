@@ -59,7 +59,9 @@
 extern "C" {
 #endif
 
-#define LRKV_ABI_VERSION 3
+/* 3: lrkv_dims.num_splits and the layer-batched calls; 4: lrkv_prefill_fused,
+ * lrkv_decode_partials and lrkv_decode_merge (no struct changed). */
+#define LRKV_ABI_VERSION 4
 
 typedef enum lrkv_status {
     LRKV_OK = 0,

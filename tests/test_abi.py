@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
     for name in _declared():
         assert hasattr(lib, name), name
     assert set(_declared()) <= set(b.EXPORTED) | set(_declared())
-    assert b.abi_version() == 3
+    assert b.abi_version() == 4
 
 
 def test_status_strings():
