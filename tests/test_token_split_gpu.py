@@ -42,9 +42,9 @@ def local_cache(pools, pt, starts, lens):
     return out, bt
 
 
-def run_parts(H, d_h, r, pools, pt, lens, q, BK, parts_ranges, status):
+def run_parts(H, d_h, r, pools, pt, lens, q, BK, parts_ranges, status, d_rope=0):
     """Partials of every part, stacked [P, B, H, d_h + r + 2]."""
-    dims = b.make_dims(H, d_h, r, H * d_h)
+    dims = b.make_dims(H, d_h, r, H * d_h, d_rope=d_rope)
     qd, bkd = dev_bf16(q), dev_bf16(BK)
     out = []
     for starts, plens in parts_ranges:
@@ -59,8 +59,8 @@ def run_parts(H, d_h, r, pools, pt, lens, q, BK, parts_ranges, status):
     return torch.stack(out)
 
 
-def merge(H, d_h, r, parts, BV, status):
-    dims = b.make_dims(H, d_h, r, H * d_h)
+def merge(H, d_h, r, parts, BV, status, d_rope=0):
+    dims = b.make_dims(H, d_h, r, H * d_h, d_rope=d_rope)
     out = torch.empty((parts.shape[1], H, d_h), dtype=torch.bfloat16, device="cuda")
     b.lrkv_decode_merge(dims, parts, dev_bf16(BV), out, status=status)
     torch.cuda.synchronize()
@@ -73,30 +73,32 @@ def split(lens, world):
 
 
 CASES = [
-    # H, d_h, r, sequence lengths, parts -- 128 heads of d_h = 128 take the tcgen05 scan; the
-    # short sequences leave some parts empty
-    (8, 64, 16, [700, 150, 64, 1], 3),
-    (32, 128, 32, [3000, 1290], 4),
-    (128, 128, 16, [2048, 777, 130], 2),
-    (4, 64, 8, [1000, 70, 200, 5, 64], 5),
+    # H, d_h, r, d_rope, sequence lengths, parts -- 128 heads of d_h = 128 take the tcgen05
+    # scan; the short sequences leave some parts empty; one case with the positional key
+    (8, 64, 16, 0, [700, 150, 64, 1], 3),
+    (32, 128, 32, 0, [3000, 1290], 4),
+    (128, 128, 16, 0, [2048, 777, 130], 2),
+    (4, 64, 8, 0, [1000, 70, 200, 5, 64], 5),
+    (16, 128, 16, 64, [1500, 300, 1], 3),
 ]
 
 
-@pytest.mark.parametrize("H,d_h,r,lens,P", CASES, ids=[f"H{c[0]}_dh{c[1]}_r{c[2]}_P{c[4]}" for c in CASES])
-def test_token_split_matches_oracle(H, d_h, r, lens, P):
+@pytest.mark.parametrize("H,d_h,r,d_rope,lens,P", CASES,
+                         ids=[f"H{c[0]}_dh{c[1]}_r{c[2]}_rope{c[3]}_P{c[5]}" for c in CASES])
+def test_token_split_matches_oracle(H, d_h, r, d_rope, lens, P):
     seed = 900 + H + r + P
     pt = S.page_table(seed, lens, BS, spare_blocks=1)
-    pools = random_pools(seed, pt.num_blocks, H, d_h, r)
+    pools = random_pools(seed, pt.num_blocks, H, d_h, r, d_rope=d_rope)
     w = weights(seed, H * d_h, d_h, H, r)
-    q = S.gaussian_bf16(seed, "q", (len(lens), H, d_h))
+    q = S.gaussian_bf16(seed, "q", (len(lens), H, d_h + d_rope))
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    parts = run_parts(H, d_h, r, pools, pt, lens, q, w.BK, split(lens, P), st)
+    parts = run_parts(H, d_h, r, pools, pt, lens, q, w.BK, split(lens, P), st, d_rope)
     assert int(st.item()) == 0  # empty parts are not errors
     assert torch.isfinite(parts[..., :-2]).all() and not torch.isnan(parts).any()
-    out = merge(H, d_h, r, parts, w.BV, st)
+    out = merge(H, d_h, r, parts, w.BV, st, d_rope)
     assert int(st.item()) == 0
     ref = oracle.get().decode_cache(pools, pt.block_table, lens, w.BK, w.BV, q)
-    assert_close(host_f64(out), ref, f"token-split decode H={H} d_h={d_h} r={r} over {P} parts")
+    assert_close(host_f64(out), ref, f"token-split decode H={H} d_h={d_h} r={r} d_rope={d_rope} over {P} parts")
 
 
 def test_one_part_equals_decode_and_empty_parts_are_neutral():
