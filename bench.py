@@ -991,6 +991,8 @@ def run_reference(args, world, rank):
     import oracle
 
     wl = S.WORKLOADS[args.workload]
+    if (args.fused or args.rope) and HARNESS[args.workload] not in (DecodeHarness, PrefillHarness):
+        raise SystemExit("--fused and --rope apply to the decode and prefill workloads")
     o = oracle.get()
     per_step_budget = max(0.01, 90.0 / max(args.steps + args.warmup, 1))
     if args.workload == "prefill":
@@ -1002,38 +1004,49 @@ def run_reference(args, world, rank):
     if wl.d_c:
         return run_reference_mla(args, wl, seq_lens, o, per_step_budget)
 
+    dr = 64 if args.rope else 0
+
     def inputs(tokens):
         pt = S.page_table(wl.seed, [tokens], 64)
         pools = tuple(S.gaussian_bf16(wl.seed, n, shp) for n, shp in
-                      [("rf_sK", (pt.num_blocks, 64, wl.d_h)), ("rf_sV", (pt.num_blocks, 64, wl.d_h)),
+                      [("rf_sK", (pt.num_blocks, 64, wl.d_h + dr)), ("rf_sV", (pt.num_blocks, 64, wl.d_h)),
                        ("rf_zK", (pt.num_blocks, 64, wl.H, wl.r)), ("rf_zV", (pt.num_blocks, 64, wl.H, wl.r))])
         BK = S.gaussian_bf16(wl.seed, "rf_BK", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
         BV = S.gaussian_bf16(wl.seed, "rf_BV", (wl.H, wl.d_h, wl.r), wl.r ** -0.5)
-        q = S.gaussian_bf16(wl.seed, "rf_q", (1, wl.H, wl.d_h))
-        return pt, pools, BK, BV, q
+        q = S.gaussian_bf16(wl.seed, "rf_q", (1, wl.H, wl.d_h + dr))
+        qt = S.gaussian_bf16(wl.seed, "rf_qt", (1, wl.H, wl.r))
+        return pt, pools, BK, BV, q, qt
+
+    def step(pt, pools, BK, BV, q, qt):
+        if args.fused:
+            o.decode_fused(pools, pt.block_table, pt.seq_lens, q, qt)
+        else:
+            o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
 
     probe = 256
-    pt, pools, BK, BV, q = inputs(probe)
+    a_in = inputs(probe)
     t0 = time.perf_counter()
-    o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
+    step(*a_in)
     rate = probe / max(time.perf_counter() - t0, 1e-6)
     tokens = max(64, int(min(int(seq_lens[0]), rate * per_step_budget)) // 64 * 64)
-    pt, pools, BK, BV, q = inputs(tokens)
+    a_in = inputs(tokens)
     for _ in range(args.warmup):
-        o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
+        step(*a_in)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        o.decode_cache(pools, pt.block_table, pt.seq_lens, BK, BV, q)
+        step(*a_in)
     dt = (time.perf_counter() - t0) / max(args.steps, 1)
-    val = A.decode_algorithmic_bytes(wl.H, wl.d_h, wl.r, [tokens]) / dt / 1e9
+    acct = A.decode_fused_algorithmic_bytes if args.fused else A.decode_algorithmic_bytes
+    val = acct(wl.H, wl.d_h, wl.r, [tokens], d_rope=dr) / dt / 1e9
+    what = "absorbed-weights decode" if args.fused else "E2 decode"
     print(json.dumps({
         "impl": "reference", "metric": METRIC_DECODE, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{wl.key}: {wl.description}", "sample_tokens_per_step": tokens, "H": wl.H,
-                   "d_h": wl.d_h, "r": wl.r},
+                   "d_h": wl.d_h, "r": wl.r, "d_rope": dr, "absorbed_weights": bool(args.fused)},
         "cpu_baseline": {"value": val, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
-                         "sample": f"E2 decode of the first {tokens} tokens of one sequence, all heads, per step"},
+                         "sample": f"{what} of the first {tokens} tokens of one sequence, all heads, per step"},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
 
@@ -1086,8 +1099,11 @@ def run_reference_prefill(args, wl, o, per_step_budget):
     """--impl reference on the prefill workload: each step, the oracle appends one sequence's
     first Tq prompt rows (the cache rows from X and the weights) and runs the E2 causal prefill of
     those Tq queries over them, all heads; Tq (a multiple of 64, at most one chunk) sized from a
-    probe so that a step takes about its share of the run's budget."""
+    probe so that a step takes about its share of the run's budget.  With --rope the append
+    also rotates the positional key at each row's position; with --fused the prefill takes q~
+    and returns [o_s | o_z] (the oracle's absorbed-weights prefill)."""
     d, H, d_h, r = wl.d, wl.H, wl.d_h, wl.r
+    dr = 64 if args.rope else 0
 
     def inputs(tq):
         X = S.gaussian_bf16(wl.seed, "rp_X", (tq, d))
@@ -1095,21 +1111,27 @@ def run_reference_prefill(args, wl, o, per_step_budget):
              S.gaussian_bf16(wl.seed, "rp_WsV", (d, d_h), d ** -0.5),
              S.gaussian_bf16(wl.seed, "rp_UK", (H, d, r), d ** -0.5),
              S.gaussian_bf16(wl.seed, "rp_UV", (H, d, r), d ** -0.5)]
+        WKR = S.gaussian_bf16(wl.seed, "rp_WKR", (d, dr), d ** -0.5) if dr else None
         BK = S.gaussian_bf16(wl.seed, "rp_BK", (H, d_h, r), r ** -0.5)
         BV = S.gaussian_bf16(wl.seed, "rp_BV", (H, d_h, r), r ** -0.5)
-        q = S.gaussian_bf16(wl.seed, "rp_q", (1, tq, H, d_h))
+        q = S.gaussian_bf16(wl.seed, "rp_q", (1, tq, H, d_h + dr))
+        qt = S.gaussian_bf16(wl.seed, "rp_qt", (1, tq, H, r))
         pt = S.page_table(wl.seed, [tq], 64)
-        return X, W, BK, BV, q, pt
+        return X, W, WKR, BK, BV, q, qt, pt
 
-    def step(tq, X, W, BK, BV, q, pt):
-        rows = o.append(X, *W)  # (sK, sV, zK, zV) rows, bf16 bits, token order
+    def step(tq, X, W, WKR, BK, BV, q, qt, pt):
+        # (sK, sV, zK, zV) rows, bf16 bits, token order
+        rows = o.append(X, *W, WKR=WKR, positions=np.arange(tq, dtype=np.int32) if dr else None)
         nb = pt.num_blocks
         pools = [np.zeros((nb * 64,) + a.shape[1:], np.uint16) for a in rows]
         slots = S.slots_for(pt, 0, 0, tq)
         for pool, a in zip(pools, rows):
             pool[slots] = a
         pools = tuple(pool.reshape((nb, 64) + pool.shape[1:]) for pool in pools)
-        o.prefill_cache(pools, pt.block_table, [0], BK, BV, q)
+        if args.fused:
+            o.prefill_fused(pools, pt.block_table, [0], q, qt)
+        else:
+            o.prefill_cache(pools, pt.block_table, [0], BK, BV, q)
 
     probe = 64
     args_p = inputs(probe)
@@ -1127,9 +1149,10 @@ def run_reference_prefill(args, wl, o, per_step_budget):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{wl.key}: {wl.description}", "sample_prompt_tokens_per_step": tq, "H": H,
-                   "d_h": d_h, "r": r, "d": d},
+                   "d_h": d_h, "r": r, "d": d, "d_rope": dr, "absorbed_weights": bool(args.fused)},
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": o.num_threads(), "kind": "oracle",
-                         "sample": f"append of one sequence's first {tq} prompt rows and the E2 causal prefill "
+                         "sample": f"append of one sequence's first {tq} prompt rows and the "
+                                   f"{'absorbed-weights' if args.fused else 'E2'} causal prefill "
                                    f"of those {tq} queries (all {H} heads), per step"},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
